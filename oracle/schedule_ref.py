@@ -1,0 +1,457 @@
+"""ORACLE -- test infrastructure only.  An independent restatement of the offline tile
+scheduler, a schedule validator and a host simulator of the per-SM queue interpreter.
+
+The "Inference MegaKernel" page (section "Hand-written whole-model MegaKernel", paragraphs on
+principle/scheduling and the object table) describes the scheduler only in outline: cut every
+operator of a fixed Llama configuration into tiles, build the tile dependency DAG, assign
+"waves" and a memory/compute pool, and tensorise each SM's plan into an instruction queue of
+shape [S, Q, 32] int32 held in HBM for the life of the kernel; the runtime waits on counters
+before an instruction and adds to counters after it.  The exact rules below are this library's
+reading of that outline (the page fixes none of them):
+
+Tiles (per layer l, in this order; ids are assigned in enumeration order):
+  QKV     rows [r, r+R_qkv) of Wqkv (q heads, k heads, v heads); R_qkv divides head_dim, so a
+          tile lies in one KV group's q, k or v range.  RMSNorm of the layer input is its prologue.
+  ATTN    (b, g, c): sequence b, KV group g, KV positions [c*C, (c+1)*C) -- split-K decode
+          attention; c runs over ceil(max_seq / C) chunks (chunks past pos do no work).
+  COMB    (b, g): fixed-order log-sum-exp combine of the chunk partials of group g.
+  OPROJ   rows of Wo, residual add.
+  UPGATE  row pairs [r, r+R_up) of gate and of up, SiLU(gate)*up epilogue.
+  DOWN    rows of Wdown, residual add.
+then LMHEAD (rows of the LM head, final RMSNorm prologue, per-tile max/argmax partial) and
+ARGMAX (b).
+Waves: the DAG's longest-path level; per layer QKV=6l, ATTN=6l+1, COMB=6l+2, OPROJ=6l+3,
+UPGATE=6l+4, DOWN=6l+5; LMHEAD=6L, ARGMAX=6L+1.
+Pools: memory pool = tiles that stream weights or KV (QKV, ATTN, OPROJ, UPGATE, DOWN,
+LMHEAD); compute pool = COMB, ARGMAX.  Within a wave memory tiles are placed before compute tiles.
+Assignment, wave by wave: memory tiles sorted by (cost desc, tile id asc), then compute tiles
+likewise; each tile goes to the SM with the smallest accumulated cost (ties: lowest SM id);
+the accumulated cost carries across waves.  cost = streamed bytes + TILE_OVERHEAD.
+With a non-zero shuffle seed the wave's tiles are instead put in a splitmix64 Fisher-Yates
+order (pools still kept apart) -- the "shuffled assignment" used to test determinism.
+Queue of an SM: its tiles in assignment order, padded with END (all-zero words).
+"""
+from __future__ import annotations
+
+import heapq
+import random
+from dataclasses import dataclass
+from typing import Dict, List, Optional, Tuple
+
+import numpy as np
+
+# opcodes
+END, QKV, ATTN, COMB, OPROJ, UPGATE, DOWN, LMHEAD, ARGMAX = range(9)
+OPNAMES = ["END", "QKV", "ATTN", "COMB", "OPROJ", "UPGATE", "DOWN", "LMHEAD", "ARGMAX"]
+WORDS = 32
+MAX_WAIT = 4
+MAX_PUB = 2
+TILE_OVERHEAD = 1024
+MEMORY_OPS = (QKV, ATTN, OPROJ, UPGATE, DOWN, LMHEAD)
+U32 = 1 << 32
+M64 = (1 << 64) - 1
+
+
+@dataclass
+class SchedOpts:
+    page_bytes: int = 16384
+    tile_bytes: int = 32768
+    attn_chunk: int = 64
+    shuffle_seed: int = 0
+    rows_qkv: int = 0   # 0: derived from tile_bytes
+    rows_o: int = 0
+    pairs_up: int = 0
+    rows_down: int = 0
+    rows_lm: int = 0
+
+
+def tile_rows(cfg, o: SchedOpts) -> Dict[str, int]:
+    H, F, d, qd = cfg.hidden, cfg.ffn, cfg.head_dim, cfg.n_q_heads * cfg.head_dim
+
+    def fit(limit, nbytes_per_row):
+        return max(1, min(limit, o.tile_bytes // nbytes_per_row))
+
+    r_qkv = o.rows_qkv or fit(8, 2 * H)
+    while d % r_qkv:
+        r_qkv -= 1
+    return dict(qkv=r_qkv, o=o.rows_o or fit(8, 2 * qd), up=o.pairs_up or fit(4, 4 * H),
+                down=o.rows_down or fit(8, 2 * F), lm=o.rows_lm or fit(8, 2 * H))
+
+
+def ceil_div(a, b):
+    return -(-a // b)
+
+
+class Counters:
+    def __init__(self, cfg):
+        L, nkv, B = cfg.n_layers, cfg.n_kv_heads, cfg.batch
+        self.L, self.nkv, self.B = L, nkv, B
+        self.base2 = L * nkv * (1 + B)
+        self.n = self.base2 + 4 * L + 2
+
+    def qkv(self, l, g): return l * self.nkv + g
+    def attn(self, l, b, g): return self.L * self.nkv + (l * self.B + b) * self.nkv + g
+    def comb(self, l): return self.base2 + l
+    def o(self, l): return self.base2 + self.L + l
+    def up(self, l): return self.base2 + 2 * self.L + l
+    def down(self, l): return self.base2 + 3 * self.L + l
+    def lm(self): return self.base2 + 4 * self.L
+    def final(self): return self.base2 + 4 * self.L + 1
+
+
+@dataclass
+class Tile:
+    op: int
+    layer: int
+    b: int
+    a0: int
+    a1: int
+    a2: int
+    wave: int
+    waits: List[Tuple[int, int]]
+    pubs: List[Tuple[int, int]]
+    stream_bytes: int
+    tid: int = -1
+
+    @property
+    def memory(self) -> bool:
+        return self.op in MEMORY_OPS
+
+    @property
+    def cost(self) -> int:
+        return self.stream_bytes + TILE_OVERHEAD
+
+
+def enumerate_tiles(cfg, o: SchedOpts) -> Tuple[List[Tile], Counters, Dict[str, int]]:
+    L, H, F, V, B = cfg.n_layers, cfg.hidden, cfg.ffn, cfg.vocab, cfg.batch
+    nq, nkv, d = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    qd, kvd = nq * d, nkv * d
+    hpg = nq // nkv
+    R = tile_rows(cfg, o)
+    C = o.attn_chunk
+    nchunk = ceil_div(cfg.max_seq, C)
+    cnt = Counters(cfg)
+    n_qkv_rows = qd + 2 * kvd
+    n_qkv = ceil_div(n_qkv_rows, R["qkv"])
+    n_o = ceil_div(H, R["o"])
+    n_up = ceil_div(F, R["up"])
+    n_dn = ceil_div(H, R["down"])
+    n_lm = ceil_div(V, R["lm"])
+    per_group_qkv = (hpg * d + 2 * d) // R["qkv"]
+    tiles: List[Tile] = []
+
+    def group_of_row(r):
+        if r < qd:
+            return (r // d) // hpg
+        if r < qd + kvd:
+            return (r - qd) // d
+        return (r - qd - kvd) // d
+
+    for l in range(L):
+        wq = [] if l == 0 else [(cnt.down(l - 1), n_dn)]
+        for t in range(n_qkv):
+            r0 = t * R["qkv"]
+            n = min(R["qkv"], n_qkv_rows - r0)
+            tiles.append(Tile(QKV, l, 0, r0, n, 0, 6 * l, list(wq),
+                              [(cnt.qkv(l, group_of_row(r0)), 1)], n * H * 2))
+        for b in range(B):
+            for g in range(nkv):
+                for c in range(nchunk):
+                    tiles.append(Tile(ATTN, l, b, g, c, C, 6 * l + 1,
+                                      [(cnt.qkv(l, g), per_group_qkv)],
+                                      [(cnt.attn(l, b, g), 1)], 2 * C * d * 2))
+        for b in range(B):
+            for g in range(nkv):
+                tiles.append(Tile(COMB, l, b, g, nchunk, C, 6 * l + 2,
+                                  [(cnt.attn(l, b, g), nchunk)], [(cnt.comb(l), 1)], 0))
+        for t in range(n_o):
+            r0 = t * R["o"]
+            n = min(R["o"], H - r0)
+            tiles.append(Tile(OPROJ, l, 0, r0, n, 0, 6 * l + 3, [(cnt.comb(l), B * nkv)],
+                              [(cnt.o(l), 1)], n * qd * 2))
+        for t in range(n_up):
+            r0 = t * R["up"]
+            n = min(R["up"], F - r0)
+            tiles.append(Tile(UPGATE, l, 0, r0, n, 0, 6 * l + 4, [(cnt.o(l), n_o)],
+                              [(cnt.up(l), 1)], 2 * n * H * 2))
+        for t in range(n_dn):
+            r0 = t * R["down"]
+            n = min(R["down"], H - r0)
+            tiles.append(Tile(DOWN, l, 0, r0, n, 0, 6 * l + 5, [(cnt.up(l), n_up)],
+                              [(cnt.down(l), 1)], n * F * 2))
+    for t in range(n_lm):
+        r0 = t * R["lm"]
+        n = min(R["lm"], V - r0)
+        tiles.append(Tile(LMHEAD, L, 0, r0, n, t, 6 * L, [(cnt.down(L - 1), n_dn)],
+                          [(cnt.lm(), 1)], n * H * 2))
+    for b in range(B):
+        tiles.append(Tile(ARGMAX, L, b, 0, n_lm, 0, 6 * L + 1, [(cnt.lm(), n_lm)],
+                          [(cnt.final(), 1)], 0))
+    for i, t in enumerate(tiles):
+        t.tid = i
+    return tiles, cnt, R
+
+
+class SplitMix64:
+    def __init__(self, seed: int):
+        self.s = seed & M64
+
+    def next(self) -> int:
+        self.s = (self.s + 0x9E3779B97F4A7C15) & M64
+        z = self.s
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M64
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M64
+        return z ^ (z >> 31)
+
+
+def _shuffle(xs: List[Tile], rng: SplitMix64) -> List[Tile]:
+    xs = list(xs)
+    for i in range(len(xs) - 1, 0, -1):
+        j = rng.next() % (i + 1)
+        xs[i], xs[j] = xs[j], xs[i]
+    return xs
+
+
+def encode(t: Tile, n_pages: int) -> List[int]:
+    w = [0] * WORDS
+    w[0], w[1], w[2], w[3], w[4], w[5] = t.op, t.layer, t.b, t.a0, t.a1, t.a2
+    w[6] = len(t.waits)
+    for i, (c, need) in enumerate(t.waits):
+        w[7 + 2 * i], w[8 + 2 * i] = c, need
+    w[15] = len(t.pubs)
+    for i, (c, delta) in enumerate(t.pubs):
+        w[16 + 2 * i], w[17 + 2 * i] = c, delta
+    w[20] = n_pages
+    w[21] = t.tid
+    w[22] = t.wave
+    return w
+
+
+def build_schedule(cfg, S: int, opts: Optional[SchedOpts] = None):
+    """Returns (queues int32 [S, Q, 32], per-step counter totals uint32 [n_counters], info)."""
+    o = opts or SchedOpts()
+    if S < 1:
+        raise ValueError("sm_count must be >= 1")
+    tiles, cnt, R = enumerate_tiles(cfg, o)
+    by_wave: Dict[int, List[Tile]] = {}
+    for t in tiles:
+        by_wave.setdefault(t.wave, []).append(t)
+    rng = SplitMix64(o.shuffle_seed) if o.shuffle_seed else None
+    heap = [(0, s) for s in range(S)]
+    per_sm: List[List[Tile]] = [[] for _ in range(S)]
+    for wv in sorted(by_wave):
+        mem = [t for t in by_wave[wv] if t.memory]
+        cmp_ = [t for t in by_wave[wv] if not t.memory]
+        if rng is None:
+            order = (sorted(mem, key=lambda t: (-t.cost, t.tid))
+                     + sorted(cmp_, key=lambda t: (-t.cost, t.tid)))
+        else:
+            order = _shuffle(mem, rng) + _shuffle(cmp_, rng)
+        for t in order:
+            acc, s = heapq.heappop(heap)
+            per_sm[s].append(t)
+            heapq.heappush(heap, (acc + t.cost, s))
+    Q = 1 + max(len(q) for q in per_sm)
+    queues = np.zeros((S, Q, WORDS), dtype=np.int32)
+    for s in range(S):
+        for i, t in enumerate(per_sm[s]):
+            queues[s, i] = encode(t, ceil_div(t.stream_bytes, o.page_bytes))
+    totals = np.zeros(cnt.n, dtype=np.uint64)
+    for t in tiles:
+        for c, dl in t.pubs:
+            totals[c] += dl
+    info = dict(rows=R, n_tiles=len(tiles), counters=cnt, tiles=tiles,
+                n_chunks=ceil_div(cfg.max_seq, o.attn_chunk))
+    return queues, totals.astype(np.uint32), info
+
+
+# --------------------------------------------------------------------------------------
+# Validator
+# --------------------------------------------------------------------------------------
+
+def _decode(w) -> Tile:
+    waits = [(int(w[7 + 2 * i]), int(w[8 + 2 * i])) for i in range(int(w[6]))]
+    pubs = [(int(w[16 + 2 * i]), int(w[17 + 2 * i])) for i in range(int(w[15]))]
+    t = Tile(int(w[0]), int(w[1]), int(w[2]), int(w[3]), int(w[4]), int(w[5]), int(w[22]),
+             waits, pubs, 0, int(w[21]))
+    return t
+
+
+def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOpts] = None,
+             page_bytes_capacity: Optional[int] = None) -> List[str]:
+    """Checks the contract a schedule must satisfy; returns a list of violations (empty = valid).
+
+    * every tile of the model appears exactly once; END only as padding, at least one END per SM;
+    * each counter's per-step total equals the sum of the deltas published into it, and every
+      wait asks for exactly that total (a consumer waits for all producers of its counter);
+    * waits point only at counters produced in strictly lower waves, and each SM's queue is in
+      non-decreasing wave order (the forward-progress rule: a waiter never holds an SM that a
+      producer it waits on still needs);
+    * (DAG + per-SM program order) is acyclic -- implied by the two previous points;
+    * capacity: at most 4 waits and 2 completions per instruction; no instruction needs more pages
+      than the ring holds.
+    """
+    o = opts or SchedOpts()
+    errs: List[str] = []
+    S, Q, W = queues.shape
+    if W != WORDS:
+        return [f"instruction width {W} != {WORDS}"]
+    ref_tiles, cnt, _ = enumerate_tiles(cfg, o)
+    seen: Dict[int, Tuple[int, int]] = {}
+    pub_sum = np.zeros(cnt.n, dtype=np.int64)
+    producer_wave: Dict[int, int] = {}
+    for s in range(S):
+        ended = False
+        last_wave = -1
+        for i in range(Q):
+            w = queues[s, i]
+            if w[0] == END:
+                if np.any(w != 0):
+                    errs.append(f"sm {s} slot {i}: END with non-zero words")
+                ended = True
+                continue
+            if ended:
+                errs.append(f"sm {s} slot {i}: instruction after END")
+            t = _decode(w)
+            if not (0 < t.op <= ARGMAX):
+                errs.append(f"sm {s} slot {i}: bad opcode {t.op}")
+                continue
+            if t.tid in seen:
+                errs.append(f"tile {t.tid} appears twice")
+            seen[t.tid] = (s, i)
+            if t.wave < last_wave:
+                errs.append(f"sm {s} slot {i}: wave {t.wave} after wave {last_wave}")
+            last_wave = t.wave
+            if len(t.waits) > MAX_WAIT or len(t.pubs) > MAX_PUB:
+                errs.append(f"tile {t.tid}: too many waits/completions")
+            for c, dl in t.pubs:
+                pub_sum[c] += dl
+                pw = producer_wave.setdefault(c, t.wave)
+                if pw != t.wave:
+                    errs.append(f"counter {c} produced in waves {pw} and {t.wave}")
+            if page_bytes_capacity is not None and w[20] * o.page_bytes > page_bytes_capacity:
+                errs.append(f"tile {t.tid}: needs {w[20]} pages, ring too small")
+            ref = ref_tiles[t.tid] if 0 <= t.tid < len(ref_tiles) else None
+            if ref is None or (ref.op, ref.layer, ref.b, ref.a0, ref.a1, ref.a2) != \
+                    (t.op, t.layer, t.b, t.a0, t.a1, t.a2):
+                errs.append(f"tile {t.tid}: fields do not match the model's tile")
+        if not ended:
+            errs.append(f"sm {s}: queue not END-terminated")
+    if len(seen) != len(ref_tiles):
+        errs.append(f"{len(seen)} tiles scheduled, model has {len(ref_tiles)}")
+    if not np.array_equal(pub_sum.astype(np.uint32), np.asarray(totals, dtype=np.uint32)):
+        errs.append("per-step counter totals differ from the sum of published deltas")
+    for s in range(S):
+        for i in range(Q):
+            w = queues[s, i]
+            if w[0] == END:
+                continue
+            t = _decode(w)
+            for c, need in t.waits:
+                if c not in producer_wave:
+                    errs.append(f"tile {t.tid}: waits on counter {c} that nobody produces")
+                    continue
+                if producer_wave[c] >= t.wave:
+                    errs.append(f"tile {t.tid}: waits on counter {c} of wave {producer_wave[c]}")
+                if need != pub_sum[c]:
+                    errs.append(f"tile {t.tid}: waits for {need} on counter {c}, total {pub_sum[c]}")
+    return errs
+
+
+# --------------------------------------------------------------------------------------
+# Host simulator of the queue interpreter (page section "principle, scheduling and data flow":
+# fetch instruction -> END? -> wait counters -> lease pages -> run body -> fence ->
+# add completions -> release pages -> next), with abstract data tracking.
+# --------------------------------------------------------------------------------------
+
+def _reads_writes(t: Tile, cfg):
+    """Abstract buffers a tile reads and writes, as (key, rows) pairs: a write adds its rows to
+    the key's count; a read requires the key's count to have reached the given number of rows
+    (its writers have all run).  Used to check every read follows its write."""
+    L, H, nq, nkv, d = cfg.n_layers, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    F, hpg = cfg.ffn, nq // nkv
+    l, op = t.layer, t.op
+    R, W = [], []
+    if op == QKV:
+        if l > 0:
+            R.append((("x_out", l - 1), H))
+        qd, kvd = nq * d, nkv * d
+        r = t.a0
+        g = (r // d) // hpg if r < qd else ((r - qd) // d if r < qd + kvd else (r - qd - kvd) // d)
+        W.append((("qkv", l, g), t.a1))
+    elif op == ATTN:
+        R.append((("qkv", l, t.a0), (hpg + 2) * d))
+        W.append((("part", l, t.b, t.a0), 1))
+    elif op == COMB:
+        R.append((("part", l, t.b, t.a0), t.a1))
+        W.append((("o", l), 1))
+    elif op == OPROJ:
+        R.append((("o", l), cfg.batch * nkv))
+        if l > 0:
+            R.append((("x_out", l - 1), H))
+        W.append((("x_attn", l), t.a1))
+    elif op == UPGATE:
+        R.append((("x_attn", l), H))
+        W.append((("h", l), t.a1))
+    elif op == DOWN:
+        R.append((("h", l), F))
+        R.append((("x_attn", l), H))
+        W.append((("x_out", l), t.a1))
+    elif op == LMHEAD:
+        R.append((("x_out", L - 1), H))
+        W.append((("lmpart",), 1))
+    elif op == ARGMAX:
+        R.append((("lmpart",), t.a1))
+        W.append((("token", t.b), 1))
+    return R, W
+
+
+def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, seed: int = 0,
+             track_data: bool = True) -> List[str]:
+    """Runs the S queues on the host under a random interleaving, for n_epochs consecutive steps
+    with epoch-offset counter targets (target = epoch * total + need, compared modulo 2^32).
+    Reports a deadlock (no SM can progress before all reach END) and any read of a buffer whose
+    writer has not yet run in the current step."""
+    S, Q, _ = queues.shape
+    rng = random.Random(seed)
+    counters = np.zeros(len(totals), dtype=np.int64)
+    errs: List[str] = []
+    decoded = [[_decode(queues[s, i]) if queues[s, i, 0] != END else None for i in range(Q)]
+               for s in range(S)]
+    rw_cache: Dict[int, Tuple[list, list]] = {}
+    for epoch in range(n_epochs):
+        pc = [0] * S
+        written: Dict[tuple, int] = {}
+        live = [s for s in range(S)]
+        while live:
+            rng.shuffle(live)
+            progressed = False
+            nxt = []
+            for s in live:
+                t = decoded[s][pc[s]]
+                if t is None:
+                    continue  # reached END
+                ok = all(((int(counters[c]) - (epoch * int(totals[c]) + need)) % U32) < (U32 >> 1)
+                         for c, need in t.waits)
+                if ok:
+                    if track_data:
+                        if t.tid not in rw_cache:
+                            rw_cache[t.tid] = _reads_writes(t, cfg)
+                        rd, wr = rw_cache[t.tid]
+                        for key, need_rows in rd:
+                            if written.get(key, 0) < need_rows:
+                                errs.append(f"epoch {epoch}: tile {t.tid} ({OPNAMES[t.op]}) read "
+                                            f"{key} before all of it was written")
+                                return errs
+                        for key, n in wr:
+                            written[key] = written.get(key, 0) + n
+                    for c, dl in t.pubs:
+                        counters[c] += dl
+                    pc[s] += 1
+                    progressed = True
+                nxt.append(s)
+            live = [s for s in nxt if decoded[s][pc[s]] is not None]
+            if live and not progressed:
+                blocked = live[0]
+                return errs + [f"epoch {epoch}: deadlock, sm {blocked} stuck at slot {pc[blocked]}"]
+    return errs
