@@ -1,0 +1,297 @@
+#!/usr/bin/env python3
+"""Benchmark of the persistent decode megakernel: batch-1 decode of the Llama-3.2-1B-shaped
+decoder (16 layers, hidden 2048, 32/8 heads, FFN 8192, vocab 128256, tied, bf16 weights),
+KV cache prefilled to 512 positions.
+
+One "step" = one decode step of the whole model = one launch of the resident grid.
+Prints one JSON line.
+
+  value     device time per token (us/token) from CUDA events around each launch on the
+            launching stream, inputs resident in HBM (weights 2.47 GB >> 129 MB L2, so every
+            step streams its weights from HBM; no L2 flush is needed)
+  e2e       the same metric through the synchronous C-ABI call mk_decode_step: host token and
+            position in, greedy next token (and the device error word) copied back each step
+  roofline  algorithmic bytes per step (weights + KV read + KV written) / median step time,
+            against the measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle on the host cores, on a bounded sample (whole decode steps)
+
+--impl reference runs the CPU oracle (the reference arm of this build) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "llama1b_ctx512"
+METRIC = "batch-1 decode us/token (Llama-3.2-1B shape, bf16 weights/KV); achieved HBM GB/s vs GB300 peak"
+KERNEL_SRC = os.path.join(ROOT, "persistent_megakernel_decode_sm_gb300", "csrc", "mk_kernel.cu")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("mk_kernel.cu", "mk_internal.h"):
+        with open(os.path.join(os.path.dirname(KERNEL_SRC), name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+    p = os.path.join(ROOT, "profiles", "megakernel_llama1b_ctx512_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_step_timer(cfg, kv_len, seed, threads, steps, warmup):
+    """Times whole oracle decode steps of the workload on the host; returns (us per token list, cores)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    from oracle import HostWeights, Oracle, kv_to_host
+    from workload import make_weights, prefilled_kv, token_ids
+    cores = oracle.set_threads(threads)
+    w = make_weights(cfg, seed=seed, device="cpu")
+    hw = HostWeights(w)
+    kh, vh = kv_to_host(prefilled_kv(cfg, [kv_len], seed=seed))
+    del w
+    orc = Oracle("f32")
+    toks = token_ids(cfg, warmup + steps, seed=seed, tag="bench")
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        orc.decode_step(cfg, hw, kh, vh, [toks[i]], [kv_len + (i % (cfg.max_seq - kv_len))])
+        dt = time.perf_counter() - t0
+        if i >= warmup:
+            times.append(dt * 1e6 / cfg.batch)
+    return times, cores
+
+
+def run_reference(args, rank, world):
+    from workload import get_workload
+    wl = get_workload(WORKLOAD)
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    # bounded sample: whole decode steps of the workload, capped so the run stays within minutes
+    cap = int(os.environ.get("MK_REF_MAX_STEPS", "20"))
+    steps = min(steps, cap)
+    warm = min(warm, 1)
+    times, cores = oracle_step_timer(wl.cfg, wl.kv_len[0], 0, threads, steps, warm)
+    v = statistics.mean(times)
+    sample = f"{len(times)} whole decode steps (+{warm} warm-up) of {WORKLOAD} at pos 512+"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us/token", "n_gpus": args.gpus,
+            "steps": len(times), "warmup": warm, "ms_per_step": v * wl.cfg.batch / 1000.0,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "batch": 1, "kv_len": 512,
+                                            "weights": "bf16", "kv": "bf16"},
+            "cpu_baseline": {"value": v, "unit": "us/token", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "us/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-steps", type=int, default=3)
+    ap.add_argument("--workload", default=WORKLOAD)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    W = max(3, args.warmup)
+    K = max(1, args.steps)
+
+    import persistent_megakernel_decode_sm_gb300 as mk
+    from workload import get_workload, make_weights, prefilled_kv, token_ids
+
+    wl = get_workload(args.workload)
+    cfg = wl.cfg
+    w = make_weights(cfg, seed=0, device="cuda")
+    kv = prefilled_kv(cfg, wl.kv_len, seed=0, device="cuda")
+    S = mk.device_sm_count()
+    stream = torch.cuda.Stream()
+    dec = mk.Decoder(mk.Schedule(cfg, S), w, kv, stream=stream)
+    span = cfg.max_seq - max(wl.kv_len)
+    toks = token_ids(cfg, (W + K) * cfg.batch, seed=1, tag="bench")
+
+    def args_for(i):
+        t = toks[i * cfg.batch:(i + 1) * cfg.batch]
+        p = [l + (i % span) for l in wl.kv_len]
+        return t, p
+
+    # ---- device-timed region: K launches, an event pair around each, on the launching stream
+    for i in range(W):
+        dec.launch(*args_for(i))
+    dec.status()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            dec.launch(*args_for(W + i))
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    dec.status()
+    total_ms = t_start.elapsed_time(t_end)
+    per = [a.elapsed_time(b) * 1000.0 for a, b in ev]   # us per launch
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        if world > 1:
+            dist.barrier()
+    med = statistics.median(per)
+    p10 = sorted(per)[max(0, int(0.1 * K) - 1)]
+    p90 = sorted(per)[min(K - 1, int(0.9 * K))]
+
+    # ---- end-to-end through mk_decode_step (host token in, greedy token out)
+    tok = toks[:cfg.batch]
+    torch.cuda.synchronize()
+    e2e_times = []
+    for i in range(W + K):
+        p = [l + (i % span) for l in wl.kv_len]
+        t0 = time.perf_counter()
+        tok = dec.step(tok, p)
+        dt = time.perf_counter() - t0
+        if i >= W:
+            e2e_times.append(dt * 1e6)
+    e2e_us = statistics.mean(e2e_times) / cfg.batch
+
+    pos_mid = [l + 0 for l in wl.kv_len]
+    step_bytes = cfg.step_bytes(pos_mid)
+    peak, peak_kind = peaks()
+    achieved = step_bytes / (med * 1e-6) / 1e9
+    value = total_ms * 1000.0 / K / (cfg.batch * world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "us/token", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": total_ms / K, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": cfg.batch, "kv_len": wl.kv_len[0] if cfg.batch == 1 else wl.kv_len,
+                   "weights": "bf16", "kv": "bf16", "sm_count": S, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (2.47 GB of weights streamed per step)",
+                   "step_us_median": med, "step_us_p10": p10, "step_us_p90": p90},
+        "e2e": {"value": e2e_us, "unit": "us/token", "h2d_bytes_per_step": 8 * cfg.batch,
+                "d2h_bytes_per_step": 96},
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic_record(), "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_step": step_bytes, "vs_nominal_8000": achieved / 8000.0},
+        "clocks": clk.summary(),
+    }
+    dec.close()
+    del w, kv
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        times, cores = oracle_step_timer(cfg, wl.kv_len[0], 0, os.cpu_count() or 1, args.cpu_steps, 1)
+        line["cpu_baseline"] = {"value": statistics.mean(times), "unit": "us/token", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{len(times)} whole decode steps (+1 warm-up) of {args.workload}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * mk.h -- C ABI of the persistent decode megakernel for GB300 (sm_103a).
+ *
+ * One decode step of a whole Llama-style decoder runs as ONE resident kernel launch: a grid of
+ * S CTAs (one per SM) in which every CTA interprets its own queue of tile instructions, waits on
+ * global completion counters before an instruction, streams the instruction's weights / KV rows
+ * through leased shared-memory pages, runs the operator body and publishes its completions.
+ * The design follows the "Inference MegaKernel" page, section "Hand-written whole-model
+ * MegaKernel" (principle, scheduling and data flow; its control-flow pseudocode; its object
+ * table), and the four device-protocol contracts of its section "Unified framework" (data
+ * visibility, forward progress, capacity, resources).
+ *
+ * Conventions
+ *  - Every call returns an mk_status; nothing aborts or throws across the ABI.  After a non-OK
+ *    status mk_last_error() holds a message (thread-local).
+ *  - All device memory of the model (weights, KV cache, completion counters, scratch, logits)
+ *    is allocated and owned by the caller; the library only borrows the pointers for the
+ *    lifetime of the bound context.  The library owns its host schedule objects and, per bound
+ *    context, one small device copy of the queues, counter totals and layer pointer table.
+ *  - Weights and KV cache are bf16, row-major, every pointer 16-byte aligned.
+ *  - "pos" is the position the step's token occupies; the step appends its K/V at pos and
+ *    attends over positions 0..pos inclusive.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MK_OK = 0,
+    MK_ERR_ARG = 1,        /* a bad argument (null, misaligned, out of range, unsupported shape) */
+    MK_ERR_CAPACITY = 2,   /* queue / page ring / KV capacity cannot hold the configuration     */
+    MK_ERR_RESOURCES = 3,  /* the kernel cannot be made resident with one CTA on S SMs          */
+    MK_ERR_CUDA = 4,       /* a CUDA runtime call failed                                        */
+    MK_ERR_TIMEOUT = 5,    /* a device wait ran out its time budget (the step was abandoned)    */
+    MK_ERR_OPCODE = 6,     /* the device met an invalid opcode in a queue                       */
+    MK_ERR_BOUNDS = 7,     /* the device met an instruction whose fields are out of range       */
+    MK_ERR_POISONED = 8    /* an earlier device error poisoned this context; unbind and re-bind */
+} mk_status;
+
+/* Model configuration (a Llama-style decoder).  batch <= 8; n_q_heads % n_kv_heads == 0 with
+ * at most 8 query heads per KV head; head_dim a multiple of 16 and <= 128; hidden, ffn and
+ * n_q_heads * head_dim multiples of 8 and <= 16384. */
+typedef struct {
+    int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+    int32_t tied_embeddings; /* informational: the LM head pointer may equal the embedding  */
+    int32_t batch;           /* sequences decoded together in one step                      */
+    int32_t max_seq;         /* KV capacity in positions; every pos must be < max_seq       */
+    double rms_eps, rope_theta;
+} mk_model_cfg;
+
+/* Schedule knobs; pass NULL to mk_build_schedule for the defaults (each 0 field = default).
+ * Tile geometry depends only on the model configuration and these knobs, never on sm_count. */
+typedef struct {
+    int32_t page_bytes;  /* shared-memory page size; default 16384                              */
+    int32_t tile_bytes;  /* target weight bytes per matvec tile; default 32768                  */
+    int32_t attn_chunk;  /* KV positions per split-K attention tile; default 64                 */
+    int32_t rows_qkv, rows_o, pairs_up, rows_down, rows_lm; /* explicit rows per tile (<= 8;
+                            pairs_up <= 4; rows_qkv must divide head_dim); 0 = from tile_bytes   */
+    uint64_t shuffle_seed; /* 0: cost-ordered placement; otherwise a seeded shuffled placement  */
+} mk_sched_opts;
+
+typedef struct mk_schedule mk_schedule; /* opaque, library-owned host object */
+typedef struct mk_ctx mk_ctx;           /* opaque, library-owned bound context */
+
+/* Host scheduler (page section "Hand-written whole-model MegaKernel": cut every operator into
+ * tiles, build the tile dependency DAG, assign waves and a memory/compute pool, place tiles on
+ * the SMs' instruction queues, tensorise each queue as [S, Q, 32] int32).
+ * Tiles: per layer QKV rows (RMSNorm prologue), split-K attention chunks (RoPE + KV append in
+ * the chunk that holds pos), per-group log-sum-exp combine, O rows (+ residual), gate/up row
+ * pairs (SiLU(gate)*up), down rows (+ residual); then LM-head rows (final RMSNorm prologue,
+ * per-tile max/argmax) and one argmax per sequence.
+ * sm_count: number of queues (= CTAs launched), 1 <= sm_count <= 4096.
+ * opts: NULL for defaults.  On success *out receives a new schedule (free with
+ * mk_schedule_free).  Errors: MK_ERR_ARG (bad cfg/opts), MK_ERR_CAPACITY (a tile needs more
+ * than 2^20 bytes of pages, or the model exceeds the encoding's ranges). */
+mk_status mk_build_schedule(const mk_model_cfg* cfg, int32_t sm_count, const mk_sched_opts* opts,
+                            mk_schedule** out);
+
+/* The queues: a read-only pointer to S*Q*32 int32 (row-major [S, Q, 32]) valid until the
+ * schedule is freed.  Word layout of one instruction:
+ *   [0] opcode (0 END, 1 QKV, 2 ATTN, 3 COMB, 4 OPROJ, 5 UPGATE, 6 DOWN, 7 LMHEAD, 8 ARGMAX)
+ *   [1] layer (n_layers for LMHEAD / ARGMAX)   [2] sequence b (attention, combine, argmax)
+ *   [3] a0: first row | KV group             [4] a1: rows (pairs for UPGATE) | chunk | #chunks | #LM tiles
+ *   [5] a2: chunk length (ATTN, COMB) | LM tile index (LMHEAD)
+ *   [6] number of waits (<= 4)   [7..14] (counter, need) pairs
+ *   [15] number of completions (<= 2)   [16..19] (counter, delta) pairs
+ *   [20] pages of the largest stream the tile may need   [21] tile id   [22] wave   [23..31] 0
+ * A wait is satisfied when counter - (epoch * total[counter] + need) >= 0 (mod 2^32).  END is
+ * all zeros and pads every queue. */
+mk_status mk_schedule_queues(const mk_schedule* s, const int32_t** queues, int32_t* sm_count,
+                             int32_t* queue_len);
+
+/* Per-step counter totals: total[c] = sum of the deltas published into counter c in one step
+ * (read-only pointer to n uint32, valid until the schedule is freed). */
+mk_status mk_schedule_counters(const mk_schedule* s, const uint32_t** totals, int32_t* n_counters);
+
+/* Overwrites one word of the host queue copy (for fault-injection tests of the device runtime's
+ * checks; contexts bound earlier are not affected).  MK_ERR_ARG if an index is out of range. */
+mk_status mk_schedule_patch(mk_schedule* s, int32_t sm, int32_t slot, int32_t word, int32_t value);
+
+/* Bytes of device scratch a context of this schedule needs (activations, attention partials,
+ * LM-head partials, RoPE table, error word, output tokens).  0 if s is NULL. */
+size_t mk_scratch_bytes(const mk_schedule* s);
+
+void mk_schedule_free(mk_schedule* s);
+
+/* Device weights, bf16 row-major, caller-owned.  Per-layer fields are HOST arrays of n_layers
+ * DEVICE pointers (copied at bind).  Layouts:
+ *   embed      [vocab, hidden]
+ *   lm_head    [vocab, hidden]          (may equal embed when tied)
+ *   final_norm, attn_norm[l], mlp_norm[l]   [hidden]
+ *   wqkv[l]    [(n_q_heads + 2 n_kv_heads) head_dim, hidden]   rows: q heads, k heads, v heads
+ *   wo[l]      [hidden, n_q_heads head_dim]
+ *   wgate_up[l][2 ffn, hidden]          rows: gate rows, then up rows
+ *   wdown[l]   [hidden, ffn] */
+typedef struct {
+    const void* embed;
+    const void* lm_head;
+    const void* final_norm;
+    const void* const* attn_norm;
+    const void* const* wqkv;
+    const void* const* wo;
+    const void* const* mlp_norm;
+    const void* const* wgate_up;
+    const void* const* wdown;
+} mk_weights;
+
+/* KV cache, bf16, caller-owned (page object table: "layered, paged K/V", lifetime = request).
+ * Element (b, l, g, p, e) of K lives at k + b*batch_stride + l*layer_stride + g*head_stride
+ * + p*head_dim + e (strides in elements, each a multiple of 8); V likewise. */
+typedef struct {
+    void* k;
+    void* v;
+    int64_t batch_stride, layer_stride, head_stride;
+} mk_kv;
+
+/* Binds a schedule to one model instance on the current CUDA device (page: "llama.cu performs
+ * one model-specific binding; weights, KV cache, activations and counters are all passed in as
+ * objects of this resident execution").
+ * counters: device uint32[n_counters], caller-owned; zeroed by mk_bind.
+ * scratch:  device buffer of >= mk_scratch_bytes(s) bytes, 256-byte aligned, caller-owned.
+ * stream:   a cudaStream_t (NULL = legacy default stream); every launch of the context goes on it.
+ * Checks shapes against the configuration, pointer alignment, that the largest tile fits the
+ * shared-memory page ring (capacity contract) and that one CTA per SM can be resident with the
+ * kernel's registers and shared memory (resources contract).  The schedule may be freed after
+ * binding.  Errors: MK_ERR_ARG, MK_ERR_CAPACITY, MK_ERR_RESOURCES, MK_ERR_CUDA. */
+mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, uint32_t* counters,
+                  void* scratch, void* stream, mk_ctx** out);
+
+/* Time budget, in nanoseconds, of every single device wait (counter spin, page / slot barrier).
+ * When one runs out the kernel records MK_ERR_TIMEOUT, every CTA leaves its loop after draining
+ * its copies in flight, and the context is poisoned.  Default 2e9 (2 s). */
+mk_status mk_set_timeout(mk_ctx* c, uint64_t ns);
+
+/* One decode step, synchronous: tokens and pos are HOST arrays of `batch` int32; logits is a
+ * DEVICE fp32 buffer [batch, vocab] (caller-owned) that receives the step's logits;
+ * next_tokens is a HOST array of `batch` int32 that receives the greedy (argmax, lowest index
+ * on ties) next tokens.  Launches the resident grid once on the bound stream, then waits for it.
+ * Errors: MK_ERR_ARG (token or pos out of range), MK_ERR_POISONED, MK_ERR_TIMEOUT,
+ * MK_ERR_OPCODE, MK_ERR_BOUNDS (device-detected; they poison the context), MK_ERR_CUDA. */
+mk_status mk_decode_step(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
+                         int32_t* next_tokens);
+
+/* Asynchronous form: enqueues one step on the bound stream and returns.  next_tokens_dev is a
+ * DEVICE int32[batch] buffer or NULL.  Device-side errors surface at the next mk_ctx_status or
+ * mk_decode_step. */
+mk_status mk_launch_step(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
+                         int32_t* next_tokens_dev);
+
+/* Waits for the bound stream and returns the device error state (MK_OK when no step failed).
+ * info (optional, 8 int32): code, CTA, queue slot, counter, value seen, value wanted, role, 0. */
+mk_status mk_ctx_status(mk_ctx* c, int32_t* info);
+
+/* Number of SMs of the current CUDA device (the natural sm_count), or MK_ERR_CUDA. */
+mk_status mk_device_sm_count(int32_t* out);
+
+const char* mk_last_error(void);
+
+void mk_unbind(mk_ctx* c);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

@@ -1,0 +1,277 @@
+// C ABI: bind a schedule to one model instance, launch the resident grid, read back status.
+//
+// Binding follows the page "Inference MegaKernel" (section "Hand-written whole-model
+// MegaKernel": one model-specific binding passes weights, KV cache, activations and counters
+// as objects of the resident execution) and checks two of its four device-protocol contracts
+// (section "Unified framework") before any launch:
+//   capacity  -- the largest tile's stream fits the shared-memory page ring, every pos < max_seq;
+//   resources -- one CTA with the kernel's registers and shared memory is resident on each of
+//                the S SMs (the launch is cooperative, so an oversubscribed grid fails instead of
+//                deadlocking: the forward-progress contract).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "mk_internal.h"
+
+namespace mk {
+const void* megakernel_fn(int nch);
+cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st);
+}  // namespace mk
+
+using namespace mk;
+
+struct mk_ctx {
+    Params base;
+    const void* fn;
+    int grid, smem;
+    cudaStream_t stream;
+    int device;
+    int32_t* d_queues;
+    uint32_t* d_totals;
+    LayerPtrs* d_layers;
+    int32_t* h_result;   // pinned: err[16] then tokens[8]
+    uint32_t epoch;
+    bool poisoned;
+    mk_model_cfg cfg;
+};
+
+static mk_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+#define CK(call)                                    \
+    do {                                            \
+        cudaError_t e_ = (call);                    \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+    } while (0)
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static void free_ctx(mk_ctx* c) {
+    if (!c) return;
+    if (c->d_queues) cudaFree(c->d_queues);
+    if (c->d_totals) cudaFree(c->d_totals);
+    if (c->d_layers) cudaFree(c->d_layers);
+    if (c->h_result) cudaFreeHost(c->h_result);
+    delete c;
+}
+
+extern "C" mk_status mk_device_sm_count(int32_t* out) {
+    if (!out) return fail(MK_ERR_ARG, "null argument");
+    int dev = 0, n = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+    *out = n;
+    return MK_OK;
+}
+
+extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, uint32_t* counters,
+                             void* scratch, void* stream, mk_ctx** out) {
+    if (!s || !w || !kv || !counters || !scratch || !out) return fail(MK_ERR_ARG, "null argument");
+    *out = nullptr;
+    const mk_model_cfg& c = s->cfg;
+    const Geometry& g = s->geo;
+    const int L = c.n_layers, H = c.hidden, d = c.head_dim, hpg = c.n_q_heads / c.n_kv_heads;
+    const int qd = c.n_q_heads * d;
+
+    // ---- arguments ----
+    if (!w->embed || !w->lm_head || !w->final_norm || !w->attn_norm || !w->wqkv || !w->wo || !w->mlp_norm ||
+        !w->wgate_up || !w->wdown)
+        return fail(MK_ERR_ARG, "mk_weights has a null field");
+    const void* ptrs[3] = {w->embed, w->lm_head, w->final_norm};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(MK_ERR_ARG, "weight pointer not 16-byte aligned");
+    for (int l = 0; l < L; ++l) {
+        const void* lp[6] = {w->attn_norm[l], w->wqkv[l], w->wo[l], w->mlp_norm[l], w->wgate_up[l], w->wdown[l]};
+        for (const void* p : lp)
+            if (!p || !aligned16(p)) return fail(MK_ERR_ARG, "layer %d weight pointer null or not 16-byte aligned", l);
+    }
+    if (!kv->k || !kv->v || !aligned16(kv->k) || !aligned16(kv->v))
+        return fail(MK_ERR_ARG, "KV pointers null or not 16-byte aligned");
+    if (kv->batch_stride % 8 || kv->layer_stride % 8 || kv->head_stride % 8 || kv->head_stride < int64_t(c.max_seq) * d ||
+        kv->layer_stride < kv->head_stride * c.n_kv_heads || (c.batch > 1 && kv->batch_stride < kv->layer_stride * L))
+        return fail(MK_ERR_ARG, "KV strides must be multiples of 8 elements and cover [max_seq, head_dim] per head");
+    if (reinterpret_cast<uintptr_t>(scratch) & 255u) return fail(MK_ERR_ARG, "scratch must be 256-byte aligned");
+    if (reinterpret_cast<uintptr_t>(counters) & 3u) return fail(MK_ERR_ARG, "counters must be 4-byte aligned");
+    if (g.page_bytes & (g.page_bytes - 1)) return fail(MK_ERR_ARG, "page_bytes must be a power of two");
+
+    // ---- device and resources ----
+    int dev = 0, sms = 0, optin = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+    if (s->S > sms) return fail(MK_ERR_RESOURCES, "schedule has %d queues but the device has %d SMs", s->S, sms);
+    const int maxK = std::max(std::max(H, qd), c.ffn);
+    const int nch = (maxK / 8 + kConsumerThreads - 1) / kConsumerThreads;
+    const void* fn = megakernel_fn(nch);
+    if (!fn) return fail(MK_ERR_ARG, "matvec rows longer than %d elements", 8 * 8 * kConsumerThreads);
+    int asf = std::max(hpg * g.attn_chunk, hpg * g.n_chunk);
+    asf = (asf + 3) & ~3;
+    const int misc0 = smem_misc_bytes(0, asf);
+    int n_pages = (optin - misc0 - 1024) / (g.page_bytes + 16);
+    if (n_pages < 1) return fail(MK_ERR_CAPACITY, "no room for a page ring");
+    int misc = smem_misc_bytes(n_pages, asf);
+    while (n_pages > 0 && int64_t(n_pages) * g.page_bytes + misc > optin) misc = smem_misc_bytes(--n_pages, asf);
+    if (n_pages < std::max(2, s->max_pages))
+        return fail(MK_ERR_CAPACITY, "page ring of %d pages cannot hold a tile of %d pages", n_pages, s->max_pages);
+    const int smem = n_pages * g.page_bytes + misc;
+    CK(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    int per_sm = 0;
+    CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem));
+    if (per_sm < 1) return fail(MK_ERR_RESOURCES, "the kernel cannot be resident (%d B shared memory)", smem);
+
+    // ---- context ----
+    mk_ctx* x = new mk_ctx();
+    std::memset(x, 0, sizeof(*x));
+    x->cfg = c;
+    x->fn = fn;
+    x->grid = s->S;
+    x->smem = smem;
+    x->stream = static_cast<cudaStream_t>(stream);
+    x->device = dev;
+    auto bail = [&](mk_status st) { free_ctx(x); return st; };
+    cudaError_t e;
+    const size_t qbytes = s->queues.size() * sizeof(int32_t);
+    if ((e = cudaMalloc(&x->d_queues, qbytes)) != cudaSuccess) return bail(cuda_fail(e, "cudaMalloc(queues)"));
+    if ((e = cudaMalloc(&x->d_totals, s->totals.size() * 4)) != cudaSuccess) return bail(cuda_fail(e, "cudaMalloc(totals)"));
+    if ((e = cudaMalloc(&x->d_layers, sizeof(LayerPtrs) * L)) != cudaSuccess) return bail(cuda_fail(e, "cudaMalloc(layers)"));
+    if ((e = cudaMallocHost(&x->h_result, 256)) != cudaSuccess) return bail(cuda_fail(e, "cudaMallocHost"));
+    std::vector<LayerPtrs> lp(L);
+    for (int l = 0; l < L; ++l)
+        lp[l] = {static_cast<const uint16_t*>(w->attn_norm[l]), static_cast<const uint16_t*>(w->wqkv[l]),
+                 static_cast<const uint16_t*>(w->wo[l]), static_cast<const uint16_t*>(w->mlp_norm[l]),
+                 static_cast<const uint16_t*>(w->wgate_up[l]), static_cast<const uint16_t*>(w->wdown[l])};
+    if ((e = cudaMemcpy(x->d_queues, s->queues.data(), qbytes, cudaMemcpyHostToDevice)) != cudaSuccess ||
+        (e = cudaMemcpy(x->d_totals, s->totals.data(), s->totals.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess ||
+        (e = cudaMemcpy(x->d_layers, lp.data(), sizeof(LayerPtrs) * L, cudaMemcpyHostToDevice)) != cudaSuccess)
+        return bail(cuda_fail(e, "cudaMemcpy(bind tables)"));
+
+    const ScratchLayout sl = scratch_layout(c, g);
+    uint8_t* sb = static_cast<uint8_t*>(scratch);
+    Params& p = x->base;
+    p.L = L; p.H = H; p.nq = c.n_q_heads; p.nkv = c.n_kv_heads; p.d = d; p.F = c.ffn; p.V = c.vocab;
+    p.B = c.batch; p.max_seq = c.max_seq; p.hpg = hpg; p.qd = qd; p.kvd = c.n_kv_heads * d;
+    p.nqkv = qd + 2 * p.kvd;
+    p.rms_eps = float(c.rms_eps);
+    p.attn_scale = float(1.0 / std::sqrt(double(d)));
+    p.page_bytes = g.page_bytes;
+    p.page_shift = 0;
+    while ((1 << p.page_shift) < g.page_bytes) ++p.page_shift;
+    p.n_pages = n_pages;
+    p.attn_chunk = g.attn_chunk;
+    p.n_chunk = g.n_chunk;
+    p.n_lm = g.n_lm;
+    p.queues = x->d_queues;
+    p.Q = s->Q;
+    p.n_counters = g.n_counters;
+    p.totals = x->d_totals;
+    p.counters = counters;
+    p.embed = static_cast<const uint16_t*>(w->embed);
+    p.lm_head = static_cast<const uint16_t*>(w->lm_head);
+    p.final_norm = static_cast<const uint16_t*>(w->final_norm);
+    p.layers = x->d_layers;
+    p.kc = static_cast<uint16_t*>(kv->k);
+    p.vc = static_cast<uint16_t*>(kv->v);
+    p.kv_bstride = kv->batch_stride;
+    p.kv_lstride = kv->layer_stride;
+    p.kv_hstride = kv->head_stride;
+    p.err = reinterpret_cast<int32_t*>(sb + sl.err);
+    p.tokens_out = reinterpret_cast<int32_t*>(sb + sl.tokens);
+    p.x_attn = reinterpret_cast<float*>(sb + sl.x_attn);
+    p.x_out = reinterpret_cast<float*>(sb + sl.x_out);
+    p.qkv = reinterpret_cast<float*>(sb + sl.qkv);
+    p.part = reinterpret_cast<float*>(sb + sl.part);
+    p.o = reinterpret_cast<float*>(sb + sl.o);
+    p.h = reinterpret_cast<float*>(sb + sl.h);
+    p.lm_part = reinterpret_cast<float2*>(sb + sl.lm_part);
+    p.rope = reinterpret_cast<const float2*>(sb + sl.rope);
+    p.timeout_ns = 2000000000ull;
+    p.smem_misc_off = n_pages * g.page_bytes;
+    p.attn_scratch_floats = asf;
+
+    if ((e = cudaMemsetAsync(counters, 0, s->totals.size() * 4, x->stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(sb + sl.err, 0, 256, x->stream)) != cudaSuccess)
+        return bail(cuda_fail(e, "cudaMemsetAsync"));
+    if ((e = launch_rope_table(reinterpret_cast<float2*>(sb + sl.rope), c.max_seq, d, c.rope_theta, x->stream)) !=
+        cudaSuccess)
+        return bail(cuda_fail(e, "rope table kernel"));
+    if ((e = cudaStreamSynchronize(x->stream)) != cudaSuccess) return bail(cuda_fail(e, "bind synchronize"));
+    *out = x;
+    return MK_OK;
+}
+
+extern "C" mk_status mk_set_timeout(mk_ctx* c, uint64_t ns) {
+    if (!c || ns == 0) return fail(MK_ERR_ARG, "bad argument");
+    c->base.timeout_ns = ns;
+    return MK_OK;
+}
+
+extern "C" mk_status mk_launch_step(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
+                                    int32_t* next_tokens_dev) {
+    if (!c || !tokens || !pos || !logits) return fail(MK_ERR_ARG, "null argument");
+    if (c->poisoned) return fail(MK_ERR_POISONED, "context poisoned by an earlier device error");
+    if (reinterpret_cast<uintptr_t>(logits) & 3u) return fail(MK_ERR_ARG, "logits not 4-byte aligned");
+    Params p = c->base;
+    for (int b = 0; b < c->cfg.batch; ++b) {
+        if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab) return fail(MK_ERR_ARG, "token %d out of range", tokens[b]);
+        if (pos[b] < 0 || pos[b] >= c->cfg.max_seq)
+            return fail(MK_ERR_ARG, "pos %d outside the KV capacity [0, %d)", pos[b], c->cfg.max_seq);
+        p.tok[b] = tokens[b];
+        p.pos[b] = pos[b];
+    }
+    p.epoch = c->epoch;
+    p.logits = logits;
+    p.next_dev = next_tokens_dev;
+    void* args[] = {&p};
+    cudaError_t e = cudaLaunchCooperativeKernel(c->fn, dim3(c->grid), dim3(kThreads), args, size_t(c->smem), c->stream);
+    if (e == cudaErrorCooperativeLaunchTooLarge)
+        return fail(MK_ERR_RESOURCES, "cooperative launch of %d CTAs does not fit the device", c->grid);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
+    c->epoch += 1;
+    return MK_OK;
+}
+
+static mk_status read_status(mk_ctx* c, int32_t* info) {
+    cudaError_t e = cudaMemcpyAsync(c->h_result, c->base.err, 96, cudaMemcpyDeviceToHost, c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) {
+        c->poisoned = true;
+        return cuda_fail(e, "step readback");
+    }
+    if (info)
+        for (int i = 0; i < 8; ++i) info[i] = c->h_result[i];
+    const int code = c->h_result[0];
+    if (code != 0) {
+        c->poisoned = true;
+        return fail(mk_status(code), "device error %d (CTA %d, queue slot %d, counter %d, seen %d, wanted %d, role %d)",
+                    code, c->h_result[1], c->h_result[2], c->h_result[3], c->h_result[4], c->h_result[5],
+                    c->h_result[6]);
+    }
+    return MK_OK;
+}
+
+extern "C" mk_status mk_decode_step(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
+                                    int32_t* next_tokens) {
+    if (!next_tokens) return fail(MK_ERR_ARG, "null next_tokens");
+    mk_status st = mk_launch_step(c, tokens, pos, logits, nullptr);
+    if (st != MK_OK) return st;
+    st = read_status(c, nullptr);
+    if (st != MK_OK) return st;
+    for (int b = 0; b < c->cfg.batch; ++b) next_tokens[b] = c->h_result[16 + b];
+    return MK_OK;
+}
+
+extern "C" mk_status mk_ctx_status(mk_ctx* c, int32_t* info) {
+    if (!c) return fail(MK_ERR_ARG, "null context");
+    if (c->poisoned && !info) return fail(MK_ERR_POISONED, "context poisoned by an earlier device error");
+    return read_status(c, info);
+}
+
+extern "C" void mk_unbind(mk_ctx* c) {
+    if (!c) return;
+    cudaStreamSynchronize(c->stream);
+    free_ctx(c);
+}

@@ -1,0 +1,324 @@
+// Host scheduler: operator -> tiles -> dependency DAG (counters) -> waves -> memory/compute pool
+// placement on S queues -> [S, Q, 32] int32 encoding.
+//
+// Follows the "Inference MegaKernel" page, section "Hand-written whole-model MegaKernel"
+// (principle, scheduling and data flow): every operator of a fixed Llama configuration is cut
+// into tiles, the tile dependency DAG is built, waves and a memory/compute pool are assigned,
+// and each SM's plan is tensorised into an instruction queue held in HBM for the life of the
+// kernel (object table: "per-SM instruction queue, [S,Q,32] int32-style encoding").
+// The page fixes none of the concrete rules; this file states them:
+//  * tiles per layer: QKV row tiles (rows divide head_dim, so a tile lies inside one KV group's
+//    q, k or v range), attention chunks (sequence, group, chunk of attn_chunk positions),
+//    combine per (sequence, group), O row tiles, gate/up row-pair tiles, down row tiles; then
+//    LM-head row tiles and one argmax per sequence;
+//  * DAG: a consumer waits on one counter per producer set -- QKV(l) on down(l-1), attention
+//    chunks of group g on the QKV tiles of group g, combine on its chunks, O on all combines,
+//    up/gate on O, down on up/gate, LM head on the last layer's down, argmax on the LM head;
+//  * waves = longest-path level (6 per layer, then LM head, then argmax); the waits of a tile
+//    point only at lower waves (forward-progress contract);
+//  * pools: memory = tiles that stream weights or KV, compute = combine and argmax; within a
+//    wave memory tiles are placed first;
+//  * placement: within a wave, tiles in (cost desc, id asc) order -- or a seeded splitmix64
+//    Fisher-Yates order when shuffle_seed != 0 -- each to the queue with the smallest
+//    accumulated cost (ties to the lowest SM), the accumulated cost carried across waves;
+//    cost = streamed bytes + a fixed per-tile overhead.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <queue>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+static thread_local std::string g_last_error;
+
+mk_status fail(mk_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+namespace {
+
+struct Tile {
+    int32_t op, layer, b, a0, a1, a2, wave;
+    int32_t nwait, npub;
+    int32_t wait[kMaxWait][2];
+    int32_t pub[kMaxPub][2];
+    int64_t stream_bytes;
+    int32_t id;
+    bool memory() const { return op != OP_COMB && op != OP_ARGMAX; }
+    int64_t cost() const { return stream_bytes + kTileOverhead; }
+};
+
+int32_t cdiv(int64_t a, int64_t b) { return int32_t((a + b - 1) / b); }
+
+int32_t fit(int32_t limit, int64_t tile_bytes, int64_t row_bytes) {
+    int64_t r = tile_bytes / row_bytes;
+    if (r > limit) r = limit;
+    if (r < 1) r = 1;
+    return int32_t(r);
+}
+
+struct SplitMix64 {
+    uint64_t s;
+    uint64_t next() {
+        s += 0x9E3779B97F4A7C15ull;
+        uint64_t z = s;
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        return z ^ (z >> 31);
+    }
+};
+
+mk_status check_cfg(const mk_model_cfg& c) {
+    if (c.n_layers < 1 || c.hidden < 8 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 16 ||
+        c.ffn < 8 || c.vocab < 1 || c.batch < 1 || c.max_seq < 1)
+        return fail(MK_ERR_ARG, "model config: every size must be positive");
+    if (c.batch > kMaxBatch) return fail(MK_ERR_ARG, "batch %d > %d", c.batch, kMaxBatch);
+    if (c.n_q_heads % c.n_kv_heads) return fail(MK_ERR_ARG, "n_q_heads %% n_kv_heads != 0");
+    if (c.n_q_heads / c.n_kv_heads > kMaxHpg)
+        return fail(MK_ERR_ARG, "more than %d query heads per KV head", kMaxHpg);
+    if (c.head_dim % 16 || c.head_dim > kMaxHeadDim)
+        return fail(MK_ERR_ARG, "head_dim must be a multiple of 16 and <= %d", kMaxHeadDim);
+    const int64_t qd = int64_t(c.n_q_heads) * c.head_dim;
+    if (c.hidden % 8 || c.ffn % 8 || qd % 8 || c.hidden > kMaxK || c.ffn > kMaxK || qd > kMaxK)
+        return fail(MK_ERR_ARG, "hidden, ffn and n_q_heads*head_dim must be multiples of 8 and <= %d",
+                    kMaxK);
+    if (!(c.rms_eps >= 0.0) || !(c.rope_theta > 0.0)) return fail(MK_ERR_ARG, "bad rms_eps / rope_theta");
+    if (int64_t(c.vocab) * c.hidden > (int64_t(1) << 40)) return fail(MK_ERR_CAPACITY, "vocab too large");
+    return MK_OK;
+}
+
+}  // namespace
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, const mk_sched_opts* opts,
+                                       mk_schedule** out) {
+    if (!cfgp || !out) return fail(MK_ERR_ARG, "null argument");
+    *out = nullptr;
+    const mk_model_cfg c = *cfgp;
+    mk_status st = check_cfg(c);
+    if (st != MK_OK) return st;
+    if (S < 1 || S > 4096) return fail(MK_ERR_ARG, "sm_count %d out of [1, 4096]", S);
+    mk_sched_opts o{};
+    if (opts) o = *opts;
+    Geometry g{};
+    g.page_bytes = o.page_bytes ? o.page_bytes : 16384;
+    g.tile_bytes = o.tile_bytes ? o.tile_bytes : 32768;
+    g.attn_chunk = o.attn_chunk ? o.attn_chunk : 64;
+    g.shuffle_seed = o.shuffle_seed;
+    if (g.page_bytes < 1024 || g.page_bytes % 128 || g.page_bytes > (1 << 20))
+        return fail(MK_ERR_ARG, "page_bytes must be a multiple of 128 in [1024, 1 MiB]");
+    if (g.tile_bytes < 16) return fail(MK_ERR_ARG, "tile_bytes too small");
+    if (g.attn_chunk < 1 || g.attn_chunk > 1024) return fail(MK_ERR_ARG, "attn_chunk out of [1, 1024]");
+
+    const int32_t L = c.n_layers, H = c.hidden, F = c.ffn, V = c.vocab, B = c.batch;
+    const int32_t nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim, hpg = nq / nkv;
+    const int32_t qd = nq * d, kvd = nkv * d, nqkv = qd + 2 * kvd;
+
+    g.r_qkv = o.rows_qkv ? o.rows_qkv : fit(kMaxRows, g.tile_bytes, 2ll * H);
+    if (!o.rows_qkv)
+        while (d % g.r_qkv) --g.r_qkv;
+    g.r_o = o.rows_o ? o.rows_o : fit(kMaxRows, g.tile_bytes, 2ll * qd);
+    g.r_up = o.pairs_up ? o.pairs_up : fit(kMaxRows / 2, g.tile_bytes, 4ll * H);
+    g.r_dn = o.rows_down ? o.rows_down : fit(kMaxRows, g.tile_bytes, 2ll * F);
+    g.r_lm = o.rows_lm ? o.rows_lm : fit(kMaxRows, g.tile_bytes, 2ll * H);
+    if (g.r_qkv < 1 || g.r_qkv > kMaxRows || d % g.r_qkv) return fail(MK_ERR_ARG, "rows_qkv must divide head_dim, <= 8");
+    if (g.r_o < 1 || g.r_o > kMaxRows || g.r_dn < 1 || g.r_dn > kMaxRows || g.r_lm < 1 || g.r_lm > kMaxRows ||
+        g.r_up < 1 || g.r_up > kMaxRows / 2)
+        return fail(MK_ERR_ARG, "rows per tile out of range");
+    g.n_qkv = cdiv(nqkv, g.r_qkv);
+    g.n_o = cdiv(H, g.r_o);
+    g.n_up = cdiv(F, g.r_up);
+    g.n_dn = cdiv(H, g.r_dn);
+    g.n_lm = cdiv(V, g.r_lm);
+    g.n_chunk = cdiv(c.max_seq, g.attn_chunk);
+    CounterMap cm(c);
+    g.n_counters = cm.count();
+    const int32_t per_group_qkv = (hpg * d + 2 * d) / g.r_qkv;
+
+    // ---- tiles in enumeration order (ids) ------------------------------------------------
+    std::vector<Tile> tiles;
+    tiles.reserve(size_t(L) * (g.n_qkv + B * nkv * (g.n_chunk + 1) + g.n_o + g.n_up + g.n_dn) + g.n_lm + B);
+    auto add = [&](int32_t op, int32_t layer, int32_t b, int32_t a0, int32_t a1, int32_t a2, int32_t wave,
+                   std::initializer_list<std::pair<int32_t, int32_t>> waits,
+                   std::pair<int32_t, int32_t> pub, int64_t bytes) {
+        Tile t{};
+        t.op = op; t.layer = layer; t.b = b; t.a0 = a0; t.a1 = a1; t.a2 = a2; t.wave = wave;
+        for (auto& w : waits) { t.wait[t.nwait][0] = w.first; t.wait[t.nwait][1] = w.second; ++t.nwait; }
+        t.pub[0][0] = pub.first; t.pub[0][1] = pub.second; t.npub = 1;
+        t.stream_bytes = bytes;
+        t.id = int32_t(tiles.size());
+        tiles.push_back(t);
+    };
+    auto group_of_row = [&](int32_t r) {
+        if (r < qd) return (r / d) / hpg;
+        if (r < qd + kvd) return (r - qd) / d;
+        return (r - qd - kvd) / d;
+    };
+    for (int32_t l = 0; l < L; ++l) {
+        for (int32_t t = 0; t < g.n_qkv; ++t) {
+            int32_t r0 = t * g.r_qkv, n = std::min(g.r_qkv, nqkv - r0);
+            Tile tmp{};
+            (void)tmp;
+            if (l == 0)
+                add(OP_QKV, l, 0, r0, n, 0, 6 * l, {}, {cm.qkv(l, group_of_row(r0)), 1}, int64_t(n) * H * 2);
+            else
+                add(OP_QKV, l, 0, r0, n, 0, 6 * l, {{cm.down(l - 1), g.n_dn}}, {cm.qkv(l, group_of_row(r0)), 1},
+                    int64_t(n) * H * 2);
+        }
+        for (int32_t b = 0; b < B; ++b)
+            for (int32_t gr = 0; gr < nkv; ++gr)
+                for (int32_t ch = 0; ch < g.n_chunk; ++ch)
+                    add(OP_ATTN, l, b, gr, ch, g.attn_chunk, 6 * l + 1, {{cm.qkv(l, gr), per_group_qkv}},
+                        {cm.attn(l, b, gr), 1}, int64_t(2) * g.attn_chunk * d * 2);
+        for (int32_t b = 0; b < B; ++b)
+            for (int32_t gr = 0; gr < nkv; ++gr)
+                add(OP_COMB, l, b, gr, g.n_chunk, g.attn_chunk, 6 * l + 2, {{cm.attn(l, b, gr), g.n_chunk}},
+                    {cm.comb(l), 1}, 0);
+        for (int32_t t = 0; t < g.n_o; ++t) {
+            int32_t r0 = t * g.r_o, n = std::min(g.r_o, H - r0);
+            add(OP_OPROJ, l, 0, r0, n, 0, 6 * l + 3, {{cm.comb(l), B * nkv}}, {cm.o(l), 1}, int64_t(n) * qd * 2);
+        }
+        for (int32_t t = 0; t < g.n_up; ++t) {
+            int32_t r0 = t * g.r_up, n = std::min(g.r_up, F - r0);
+            add(OP_UPGATE, l, 0, r0, n, 0, 6 * l + 4, {{cm.o(l), g.n_o}}, {cm.up(l), 1}, int64_t(2) * n * H * 2);
+        }
+        for (int32_t t = 0; t < g.n_dn; ++t) {
+            int32_t r0 = t * g.r_dn, n = std::min(g.r_dn, H - r0);
+            add(OP_DOWN, l, 0, r0, n, 0, 6 * l + 5, {{cm.up(l), g.n_up}}, {cm.down(l), 1}, int64_t(n) * F * 2);
+        }
+    }
+    for (int32_t t = 0; t < g.n_lm; ++t) {
+        int32_t r0 = t * g.r_lm, n = std::min(g.r_lm, V - r0);
+        add(OP_LMHEAD, L, 0, r0, n, t, 6 * L, {{cm.down(L - 1), g.n_dn}}, {cm.lm(), 1}, int64_t(n) * H * 2);
+    }
+    for (int32_t b = 0; b < B; ++b)
+        add(OP_ARGMAX, L, b, 0, g.n_lm, 0, 6 * L + 1, {{cm.lm(), g.n_lm}}, {cm.fin(), 1}, 0);
+
+    // ---- placement ------------------------------------------------------------------------
+    using Slot = std::pair<int64_t, int32_t>;  // (accumulated cost, sm)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t s = 0; s < S; ++s) heap.push({0, s});
+    std::vector<std::vector<int32_t>> per_sm(S);
+    SplitMix64 rng{g.shuffle_seed};
+    size_t i = 0;
+    while (i < tiles.size()) {
+        size_t j = i;
+        while (j < tiles.size() && tiles[j].wave == tiles[i].wave) ++j;  // tiles of one wave are contiguous
+        std::vector<int32_t> mem, cmp;
+        for (size_t k = i; k < j; ++k) (tiles[k].memory() ? mem : cmp).push_back(tiles[k].id);
+        auto order = [&](std::vector<int32_t>& v) {
+            if (g.shuffle_seed == 0) {
+                std::stable_sort(v.begin(), v.end(), [&](int32_t a, int32_t b) {
+                    if (tiles[a].cost() != tiles[b].cost()) return tiles[a].cost() > tiles[b].cost();
+                    return a < b;
+                });
+            } else {
+                for (size_t k = v.size(); k-- > 1;) {
+                    size_t r = size_t(rng.next() % uint64_t(k + 1));
+                    std::swap(v[k], v[r]);
+                }
+            }
+        };
+        order(mem);
+        order(cmp);
+        for (auto* v : {&mem, &cmp})
+            for (int32_t id : *v) {
+                Slot sl = heap.top();
+                heap.pop();
+                per_sm[sl.second].push_back(id);
+                heap.push({sl.first + tiles[id].cost(), sl.second});
+            }
+        i = j;
+    }
+
+    // ---- encoding -------------------------------------------------------------------------
+    auto* sch = new mk_schedule();
+    sch->cfg = c;
+    sch->geo = g;
+    sch->S = S;
+    size_t qmax = 0;
+    for (auto& v : per_sm) qmax = std::max(qmax, v.size());
+    sch->Q = int32_t(qmax + 1);
+    sch->queues.assign(size_t(S) * sch->Q * kWords, 0);
+    sch->totals.assign(g.n_counters, 0u);
+    sch->max_pages = 0;
+    for (int32_t s = 0; s < S; ++s)
+        for (size_t k = 0; k < per_sm[s].size(); ++k) {
+            const Tile& t = tiles[per_sm[s][k]];
+            int32_t* w = &sch->queues[(size_t(s) * sch->Q + k) * kWords];
+            w[W_OP] = t.op; w[W_LAYER] = t.layer; w[W_B] = t.b;
+            w[W_A0] = t.a0; w[W_A1] = t.a1; w[W_A2] = t.a2;
+            w[W_NWAIT] = t.nwait;
+            for (int q = 0; q < t.nwait; ++q) { w[W_WAIT + 2 * q] = t.wait[q][0]; w[W_WAIT + 2 * q + 1] = t.wait[q][1]; }
+            w[W_NPUB] = t.npub;
+            for (int q = 0; q < t.npub; ++q) { w[W_PUB + 2 * q] = t.pub[q][0]; w[W_PUB + 2 * q + 1] = t.pub[q][1]; }
+            int64_t pages = (t.stream_bytes + g.page_bytes - 1) / g.page_bytes;
+            if (pages > (1 << 20)) { delete sch; return fail(MK_ERR_CAPACITY, "tile too large"); }
+            w[W_NPAGES] = int32_t(pages);
+            w[W_TILE] = t.id;
+            w[W_WAVE] = t.wave;
+            sch->max_pages = std::max(sch->max_pages, int32_t(pages));
+        }
+    for (const Tile& t : tiles)
+        for (int q = 0; q < t.npub; ++q) sch->totals[t.pub[q][0]] += uint32_t(t.pub[q][1]);
+
+    // ---- structural validation (waits point at lower waves; queues in wave order) ------------
+    std::vector<int32_t> prod_wave(g.n_counters, -1);
+    for (const Tile& t : tiles) prod_wave[t.pub[0][0]] = t.wave;
+    for (const Tile& t : tiles)
+        for (int q = 0; q < t.nwait; ++q) {
+            int32_t cid = t.wait[q][0];
+            if (prod_wave[cid] < 0 || prod_wave[cid] >= t.wave || uint32_t(t.wait[q][1]) != sch->totals[cid]) {
+                delete sch;
+                return fail(MK_ERR_CAPACITY, "internal: tile %d waits on a counter outside lower waves", t.id);
+            }
+        }
+    *out = sch;
+    return MK_OK;
+}
+
+extern "C" mk_status mk_schedule_queues(const mk_schedule* s, const int32_t** q, int32_t* S, int32_t* Q) {
+    if (!s || !q || !S || !Q) return fail(MK_ERR_ARG, "null argument");
+    *q = s->queues.data();
+    *S = s->S;
+    *Q = s->Q;
+    return MK_OK;
+}
+
+extern "C" mk_status mk_schedule_counters(const mk_schedule* s, const uint32_t** t, int32_t* n) {
+    if (!s || !t || !n) return fail(MK_ERR_ARG, "null argument");
+    *t = s->totals.data();
+    *n = int32_t(s->totals.size());
+    return MK_OK;
+}
+
+extern "C" mk_status mk_schedule_patch(mk_schedule* s, int32_t sm, int32_t slot, int32_t word, int32_t value) {
+    if (!s) return fail(MK_ERR_ARG, "null schedule");
+    if (sm < 0 || sm >= s->S || slot < 0 || slot >= s->Q || word < 0 || word >= kWords)
+        return fail(MK_ERR_ARG, "patch index out of range");
+    s->queues[(size_t(sm) * s->Q + slot) * kWords + word] = value;
+    return MK_OK;
+}
+
+extern "C" size_t mk_scratch_bytes(const mk_schedule* s) {
+    if (!s) return 0;
+    return scratch_layout(s->cfg, s->geo).total;
+}
+
+extern "C" void mk_schedule_free(mk_schedule* s) { delete s; }
+
+extern "C" const char* mk_last_error(void) { return mk::g_last_error.c_str(); }
