@@ -54,16 +54,24 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_record():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
-    p = os.path.join(ROOT, "profiles", "megakernel_llama1b_ctx512_traffic.json")
+def traffic_record(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this very kernel
+    source (its hash is recorded beside the figure); None otherwise."""
+    p = os.path.join(ROOT, "profiles", f"megakernel_{workload}_traffic.txt")
     if not os.path.exists(p):
         return None
+    rec = {}
     with open(p) as f:
-        d = json.load(f)
-    if d.get("kernel_hash") != kernel_hash():
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("kernel_hash") != kernel_hash():
         return None
-    return d.get("dram_bytes_per_launch")
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 class ClockSampler:
@@ -80,7 +88,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "25"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -172,7 +180,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -275,7 +283,7 @@ def main():
                 "d2h_bytes_per_step": 96},
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic_record(), "peak_kind": peak_kind,
+                     "frac": achieved / peak, "traffic": traffic_record(args.workload), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_step": step_bytes, "vs_nominal_8000": achieved / 8000.0},
         "clocks": clk.summary(),
     }

@@ -57,11 +57,12 @@ typedef struct {
 /* Schedule knobs; pass NULL to mk_build_schedule for the defaults (each 0 field = default).
  * Tile geometry depends only on the model configuration and these knobs, never on sm_count. */
 typedef struct {
-    int32_t page_bytes;  /* shared-memory page size; default 16384                              */
-    int32_t tile_bytes;  /* target weight bytes per matvec tile; default 32768                  */
+    int32_t page_bytes;  /* shared-memory page size (a power of two); default 32768             */
+    int32_t tile_bytes;  /* target weight bytes per matvec tile; default 131072                 */
     int32_t attn_chunk;  /* KV positions per split-K attention tile; default 64                 */
-    int32_t rows_qkv, rows_o, pairs_up, rows_down, rows_lm; /* explicit rows per tile (<= 8;
-                            pairs_up <= 4; rows_qkv must divide head_dim); 0 = from tile_bytes   */
+    int32_t rows_qkv, rows_o, pairs_up, rows_down, rows_lm; /* explicit rows per tile (<= 32;
+                            pairs_up <= 16; rows_qkv must divide head_dim); 0 = from tile_bytes,
+                            capped at 8 rows for QKV, O and down, 16 pairs, 32 LM-head rows    */
     uint64_t shuffle_seed; /* 0: cost-ordered placement; otherwise a seeded shuffled placement  */
 } mk_sched_opts;
 
@@ -72,9 +73,10 @@ typedef struct mk_ctx mk_ctx;           /* opaque, library-owned bound context *
  * tiles, build the tile dependency DAG, assign waves and a memory/compute pool, place tiles on
  * the SMs' instruction queues, tensorise each queue as [S, Q, 32] int32).
  * Tiles: per layer QKV rows (RMSNorm prologue), split-K attention chunks (RoPE + KV append in
- * the chunk that holds pos), per-group log-sum-exp combine, O rows (+ residual), gate/up row
- * pairs (SiLU(gate)*up), down rows (+ residual); then LM-head rows (final RMSNorm prologue,
- * per-tile max/argmax) and one argmax per sequence.
+ * the chunk that holds pos; the chunk that completes its KV group also does the group's
+ * log-sum-exp combine), O rows (+ residual), gate/up row pairs (SiLU(gate)*up), down rows
+ * (+ residual); then LM-head rows (final RMSNorm prologue, running max/argmax) and one argmax
+ * per sequence.
  * sm_count: number of queues (= CTAs launched), 1 <= sm_count <= 4096.
  * opts: NULL for defaults.  On success *out receives a new schedule (free with
  * mk_schedule_free).  Errors: MK_ERR_ARG (bad cfg/opts), MK_ERR_CAPACITY (a tile needs more
@@ -84,13 +86,17 @@ mk_status mk_build_schedule(const mk_model_cfg* cfg, int32_t sm_count, const mk_
 
 /* The queues: a read-only pointer to S*Q*32 int32 (row-major [S, Q, 32]) valid until the
  * schedule is freed.  Word layout of one instruction:
- *   [0] opcode (0 END, 1 QKV, 2 ATTN, 3 COMB, 4 OPROJ, 5 UPGATE, 6 DOWN, 7 LMHEAD, 8 ARGMAX)
- *   [1] layer (n_layers for LMHEAD / ARGMAX)   [2] sequence b (attention, combine, argmax)
- *   [3] a0: first row | KV group             [4] a1: rows (pairs for UPGATE) | chunk | #chunks | #LM tiles
- *   [5] a2: chunk length (ATTN, COMB) | LM tile index (LMHEAD)
+ *   [0] opcode (0 END, 1 QKV, 2 ATTN, 4 OPROJ, 5 UPGATE, 6 DOWN, 7 LMHEAD, 8 ARGMAX; 3 is
+ *       reserved and rejected)
+ *   [1] layer (n_layers for LMHEAD / ARGMAX)   [2] sequence b (attention, argmax)
+ *   [3] a0: first row | KV group             [4] a1: rows (pairs for UPGATE) | chunk | #LM tiles
+ *   [5] a2: chunk length (ATTN) | LM tile index (LMHEAD)
  *   [6] number of waits (<= 4)   [7..14] (counter, need) pairs
  *   [15] number of completions (<= 2)   [16..19] (counter, delta) pairs
- *   [20] pages of the largest stream the tile may need   [21] tile id   [22] wave   [23..31] 0
+ *   [20] pages of the largest stream the tile may need   [21] tile id   [22] wave
+ *   [23] 1 = conditional completions: the tile adds 1 to arrival counter [24] itself and its
+ *        completions fire only if it is the last of [25] arrivals (ATTN: the group's combine)
+ *   [26..31] 0 (the bound device copy carries the tile's resolved stream addresses here)
  * A wait is satisfied when counter - (epoch * total[counter] + need) >= 0 (mod 2^32).  END is
  * all zeros and pads every queue. */
 mk_status mk_schedule_queues(const mk_schedule* s, const int32_t** queues, int32_t* sm_count,
@@ -157,6 +163,14 @@ mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, ui
  * When one runs out the kernel records MK_ERR_TIMEOUT, every CTA leaves its loop after draining
  * its copies in flight, and the context is poisoned.  Default 2e9 (2 s). */
 mk_status mk_set_timeout(mk_ctx* c, uint64_t ns);
+
+/* Per-instruction timeline for profiling (the page's "scheduling ledger": scheduler cycles,
+ * dependency waits).  buf: DEVICE uint64[S * Q * 8] (caller-owned) or NULL to switch tracing off.
+ * While on, every launch writes globaltimer stamps (ns) for instruction (sm, slot) at
+ * buf[(sm * Q + slot) * 8 + k]: k = 0 slot published by the loader, 1 its pages issued,
+ * 2 dependencies satisfied, 3 body done, 4 completions published; buf[sm * Q * 8 + 5] = CTA
+ * start.  Entries of slots a CTA never reached keep their old contents. */
+mk_status mk_set_trace(mk_ctx* c, uint64_t* buf);
 
 /* One decode step, synchronous: tokens and pos are HOST arrays of `batch` int32; logits is a
  * DEVICE fp32 buffer [batch, vocab] (caller-owned) that receives the step's logits;

@@ -13,17 +13,19 @@ Tiles (per layer l, in this order; ids are assigned in enumeration order):
   QKV     rows [r, r+R_qkv) of Wqkv (q heads, k heads, v heads); R_qkv divides head_dim, so a
           tile lies in one KV group's q, k or v range.  RMSNorm of the layer input is its prologue.
   ATTN    (b, g, c): sequence b, KV group g, KV positions [c*C, (c+1)*C) -- split-K decode
-          attention; c runs over ceil(max_seq / C) chunks (chunks past pos do no work).
-  COMB    (b, g): fixed-order log-sum-exp combine of the chunk partials of group g.
+          attention; c runs over ceil(max_seq / C) chunks (chunks past pos do no work).  Every
+          chunk tile adds 1 to the group's arrival counter itself; the tile that completes the
+          group (the last arriver) also does the fixed-order log-sum-exp combine of the group's
+          chunk partials and alone carries the tile's completion (a conditional completion).
   OPROJ   rows of Wo, residual add.
   UPGATE  row pairs [r, r+R_up) of gate and of up, SiLU(gate)*up epilogue.
   DOWN    rows of Wdown, residual add.
 then LMHEAD (rows of the LM head, final RMSNorm prologue, per-tile max/argmax partial) and
 ARGMAX (b).
-Waves: the DAG's longest-path level; per layer QKV=6l, ATTN=6l+1, COMB=6l+2, OPROJ=6l+3,
-UPGATE=6l+4, DOWN=6l+5; LMHEAD=6L, ARGMAX=6L+1.
+Waves: the DAG's longest-path level; per layer QKV=5l, ATTN=5l+1, OPROJ=5l+2, UPGATE=5l+3,
+DOWN=5l+4; LMHEAD=5L, ARGMAX=5L+1.
 Pools: memory pool = tiles that stream weights or KV (QKV, ATTN, OPROJ, UPGATE, DOWN,
-LMHEAD); compute pool = COMB, ARGMAX.  Within a wave memory tiles are placed before compute tiles.
+LMHEAD); compute pool = ARGMAX.  Within a wave memory tiles are placed before compute tiles.
 Assignment, wave by wave: memory tiles sorted by (cost desc, tile id asc), then compute tiles
 likewise; each tile goes to the SM with the smallest accumulated cost (ties: lowest SM id);
 the accumulated cost carries across waves.  cost = streamed bytes + TILE_OVERHEAD.
@@ -54,8 +56,8 @@ M64 = (1 << 64) - 1
 
 @dataclass
 class SchedOpts:
-    page_bytes: int = 16384
-    tile_bytes: int = 32768
+    page_bytes: int = 32768
+    tile_bytes: int = 131072
     attn_chunk: int = 64
     shuffle_seed: int = 0
     rows_qkv: int = 0   # 0: derived from tile_bytes
@@ -74,8 +76,8 @@ def tile_rows(cfg, o: SchedOpts) -> Dict[str, int]:
     r_qkv = o.rows_qkv or fit(8, 2 * H)
     while d % r_qkv:
         r_qkv -= 1
-    return dict(qkv=r_qkv, o=o.rows_o or fit(8, 2 * qd), up=o.pairs_up or fit(4, 4 * H),
-                down=o.rows_down or fit(8, 2 * F), lm=o.rows_lm or fit(8, 2 * H))
+    return dict(qkv=r_qkv, o=o.rows_o or fit(8, 2 * qd), up=o.pairs_up or fit(16, 4 * H),
+                down=o.rows_down or fit(8, 2 * F), lm=o.rows_lm or fit(32, 2 * H))
 
 
 def ceil_div(a, b):
@@ -112,6 +114,8 @@ class Tile:
     pubs: List[Tuple[int, int]]
     stream_bytes: int
     tid: int = -1
+    arrive: int = -1     # ATTN: arrival counter the tile increments itself; pubs then belong
+    arrive_n: int = 0    # to the last of arrive_n arrivals only
 
     @property
     def memory(self) -> bool:
@@ -152,40 +156,37 @@ def enumerate_tiles(cfg, o: SchedOpts) -> Tuple[List[Tile], Counters, Dict[str, 
         for t in range(n_qkv):
             r0 = t * R["qkv"]
             n = min(R["qkv"], n_qkv_rows - r0)
-            tiles.append(Tile(QKV, l, 0, r0, n, 0, 6 * l, list(wq),
+            tiles.append(Tile(QKV, l, 0, r0, n, 0, 5 * l, list(wq),
                               [(cnt.qkv(l, group_of_row(r0)), 1)], n * H * 2))
         for b in range(B):
             for g in range(nkv):
                 for c in range(nchunk):
-                    tiles.append(Tile(ATTN, l, b, g, c, C, 6 * l + 1,
+                    tiles.append(Tile(ATTN, l, b, g, c, C, 5 * l + 1,
                                       [(cnt.qkv(l, g), per_group_qkv)],
-                                      [(cnt.attn(l, b, g), 1)], 2 * C * d * 2))
-        for b in range(B):
-            for g in range(nkv):
-                tiles.append(Tile(COMB, l, b, g, nchunk, C, 6 * l + 2,
-                                  [(cnt.attn(l, b, g), nchunk)], [(cnt.comb(l), 1)], 0))
+                                      [(cnt.comb(l), 1)], 2 * C * d * 2,
+                                      arrive=cnt.attn(l, b, g), arrive_n=nchunk))
         for t in range(n_o):
             r0 = t * R["o"]
             n = min(R["o"], H - r0)
-            tiles.append(Tile(OPROJ, l, 0, r0, n, 0, 6 * l + 3, [(cnt.comb(l), B * nkv)],
+            tiles.append(Tile(OPROJ, l, 0, r0, n, 0, 5 * l + 2, [(cnt.comb(l), B * nkv)],
                               [(cnt.o(l), 1)], n * qd * 2))
         for t in range(n_up):
             r0 = t * R["up"]
             n = min(R["up"], F - r0)
-            tiles.append(Tile(UPGATE, l, 0, r0, n, 0, 6 * l + 4, [(cnt.o(l), n_o)],
+            tiles.append(Tile(UPGATE, l, 0, r0, n, 0, 5 * l + 3, [(cnt.o(l), n_o)],
                               [(cnt.up(l), 1)], 2 * n * H * 2))
         for t in range(n_dn):
             r0 = t * R["down"]
             n = min(R["down"], H - r0)
-            tiles.append(Tile(DOWN, l, 0, r0, n, 0, 6 * l + 5, [(cnt.up(l), n_up)],
+            tiles.append(Tile(DOWN, l, 0, r0, n, 0, 5 * l + 4, [(cnt.up(l), n_up)],
                               [(cnt.down(l), 1)], n * F * 2))
     for t in range(n_lm):
         r0 = t * R["lm"]
         n = min(R["lm"], V - r0)
-        tiles.append(Tile(LMHEAD, L, 0, r0, n, t, 6 * L, [(cnt.down(L - 1), n_dn)],
+        tiles.append(Tile(LMHEAD, L, 0, r0, n, t, 5 * L, [(cnt.down(L - 1), n_dn)],
                           [(cnt.lm(), 1)], n * H * 2))
     for b in range(B):
-        tiles.append(Tile(ARGMAX, L, b, 0, n_lm, 0, 6 * L + 1, [(cnt.lm(), n_lm)],
+        tiles.append(Tile(ARGMAX, L, b, 0, n_lm, 0, 5 * L + 1, [(cnt.lm(), n_lm)],
                           [(cnt.final(), 1)], 0))
     for i, t in enumerate(tiles):
         t.tid = i
@@ -224,6 +225,8 @@ def encode(t: Tile, n_pages: int) -> List[int]:
     w[20] = n_pages
     w[21] = t.tid
     w[22] = t.wave
+    if t.arrive >= 0:   # completions only from the last of arrive_n arrivals on counter `arrive`
+        w[23], w[24], w[25] = 1, t.arrive, t.arrive_n
     return w
 
 
@@ -258,8 +261,14 @@ def build_schedule(cfg, S: int, opts: Optional[SchedOpts] = None):
             queues[s, i] = encode(t, ceil_div(t.stream_bytes, o.page_bytes))
     totals = np.zeros(cnt.n, dtype=np.uint64)
     for t in tiles:
-        for c, dl in t.pubs:
-            totals[c] += dl
+        if t.arrive >= 0:
+            totals[t.arrive] += 1                 # each tile arrives once
+            if t.a1 == t.arrive_n - 1:            # the group's completion counts once
+                for c, dl in t.pubs:
+                    totals[c] += dl
+        else:
+            for c, dl in t.pubs:
+                totals[c] += dl
     info = dict(rows=R, n_tiles=len(tiles), counters=cnt, tiles=tiles,
                 n_chunks=ceil_div(cfg.max_seq, o.attn_chunk))
     return queues, totals.astype(np.uint32), info
@@ -274,6 +283,8 @@ def _decode(w) -> Tile:
     pubs = [(int(w[16 + 2 * i]), int(w[17 + 2 * i])) for i in range(int(w[15]))]
     t = Tile(int(w[0]), int(w[1]), int(w[2]), int(w[3]), int(w[4]), int(w[5]), int(w[22]),
              waits, pubs, 0, int(w[21]))
+    if w[23] == 1:
+        t.arrive, t.arrive_n = int(w[24]), int(w[25])
     return t
 
 
@@ -300,6 +311,8 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
     seen: Dict[int, Tuple[int, int]] = {}
     pub_sum = np.zeros(cnt.n, dtype=np.int64)
     producer_wave: Dict[int, int] = {}
+    arrivals: Dict[int, int] = {}
+    cond_pubs: Dict[int, Tuple[int, list, int]] = {}
     for s in range(S):
         ended = False
         last_wave = -1
@@ -324,7 +337,12 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
             last_wave = t.wave
             if len(t.waits) > MAX_WAIT or len(t.pubs) > MAX_PUB:
                 errs.append(f"tile {t.tid}: too many waits/completions")
-            for c, dl in t.pubs:
+            produced = list(t.pubs)
+            if t.arrive >= 0:
+                arrivals[t.arrive] = arrivals.get(t.arrive, 0) + 1
+                produced = [(t.arrive, 1)]
+                cond_pubs.setdefault(t.arrive, (t.arrive_n, list(t.pubs), t.wave))
+            for c, dl in produced:
                 pub_sum[c] += dl
                 pw = producer_wave.setdefault(c, t.wave)
                 if pw != t.wave:
@@ -339,6 +357,14 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
             errs.append(f"sm {s}: queue not END-terminated")
     if len(seen) != len(ref_tiles):
         errs.append(f"{len(seen)} tiles scheduled, model has {len(ref_tiles)}")
+    for a, (n_arr, pubs, wave) in cond_pubs.items():   # each completed group publishes once
+        if arrivals.get(a, 0) != n_arr:
+            errs.append(f"arrival counter {a}: {arrivals.get(a, 0)} tiles arrive, {n_arr} expected")
+        for c, dl in pubs:
+            pub_sum[c] += dl
+            pw = producer_wave.setdefault(c, wave)
+            if pw != wave:
+                errs.append(f"counter {c} produced in waves {pw} and {wave}")
     if not np.array_equal(pub_sum.astype(np.uint32), np.asarray(totals, dtype=np.uint32)):
         errs.append("per-step counter totals differ from the sum of published deltas")
     for s in range(S):
@@ -382,9 +408,6 @@ def _reads_writes(t: Tile, cfg):
     elif op == ATTN:
         R.append((("qkv", l, t.a0), (hpg + 2) * d))
         W.append((("part", l, t.b, t.a0), 1))
-    elif op == COMB:
-        R.append((("part", l, t.b, t.a0), t.a1))
-        W.append((("o", l), 1))
     elif op == OPROJ:
         R.append((("o", l), cfg.batch * nkv))
         if l > 0:
@@ -445,7 +468,18 @@ def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, see
                                 return errs
                         for key, n in wr:
                             written[key] = written.get(key, 0) + n
-                    for c, dl in t.pubs:
+                    pubs = t.pubs
+                    if t.arrive >= 0:
+                        counters[t.arrive] += 1
+                        last = ((int(counters[t.arrive]) - epoch * t.arrive_n) % U32) == t.arrive_n
+                        pubs = t.pubs if last else []
+                        if last and track_data:   # the last arriver combines the group's partials
+                            key = ("part", t.layer, t.b, t.a0)
+                            if written.get(key, 0) < t.arrive_n:
+                                errs.append(f"epoch {epoch}: combine of {key} before all chunks")
+                                return errs
+                            written[("o", t.layer)] = written.get(("o", t.layer), 0) + 1
+                    for c, dl in pubs:
                         counters[c] += dl
                     pc[s] += 1
                     progressed = True

@@ -32,7 +32,7 @@ STATUS_NAMES = ["MK_OK", "MK_ERR_ARG", "MK_ERR_CAPACITY", "MK_ERR_RESOURCES", "M
                 "MK_ERR_OPCODE", "MK_ERR_BOUNDS", "MK_ERR_POISONED"]
 EXPORTS = ["mk_build_schedule", "mk_schedule_queues", "mk_schedule_counters", "mk_schedule_patch",
            "mk_scratch_bytes", "mk_schedule_free", "mk_bind", "mk_set_timeout", "mk_decode_step",
-           "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind"]
+           "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind", "mk_set_trace"]
 
 
 class MkError(RuntimeError):
@@ -94,6 +94,8 @@ lib.mk_device_sm_count.restype = ctypes.c_int
 lib.mk_device_sm_count.argtypes = [_I32P]
 lib.mk_last_error.restype = ctypes.c_char_p
 lib.mk_last_error.argtypes = []
+lib.mk_set_trace.restype = ctypes.c_int
+lib.mk_set_trace.argtypes = [_P, _P]
 lib.mk_unbind.restype = None
 lib.mk_unbind.argtypes = [_P]
 
@@ -229,6 +231,10 @@ class Decoder:
         if st != MK_OK:
             raise MkError(st, lib.mk_last_error().decode(errors="replace"))
         return list(info)
+
+    def set_trace(self, buf):
+        """mk_set_trace: buf is a CUDA int64 tensor of S*Q*8 elements, or None to stop tracing."""
+        _check(lib.mk_set_trace(self.handle, _ptr(buf) if buf is not None else None))
 
     def status_code(self):
         info = (ctypes.c_int32 * 8)()

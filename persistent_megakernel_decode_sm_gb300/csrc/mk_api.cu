@@ -18,7 +18,7 @@
 #include "mk_internal.h"
 
 namespace mk {
-const void* megakernel_fn(int nch);
+const void* megakernel_fn(int cpl);
 cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st);
 }  // namespace mk
 
@@ -68,6 +68,90 @@ extern "C" mk_status mk_device_sm_count(int32_t* out) {
     return MK_OK;
 }
 
+// Device copy of the queues: validates every instruction of a known opcode against the model (the
+// device then trusts those fields) and writes the resolved weight stream of each matvec tile into
+// words 26..31 (source addresses and byte counts), so the loader on the device does no decoding.
+// Unknown opcodes are copied as they are: the device rejects them (MK_ERR_OPCODE).
+static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, std::vector<int32_t>& dq) {
+    const mk_model_cfg& c = s->cfg;
+    const Geometry& g = s->geo;
+    const int L = c.n_layers, H = c.hidden, F = c.ffn, V = c.vocab, B = c.batch, nkv = c.n_kv_heads;
+    const int qd = c.n_q_heads * c.head_dim, nqkv = qd + 2 * nkv * c.head_dim;
+    dq = s->queues;
+    auto put64 = [](int32_t* w2, const void* ptr) {
+        const uint64_t v = reinterpret_cast<uint64_t>(ptr);
+        w2[0] = int32_t(uint32_t(v));
+        w2[1] = int32_t(uint32_t(v >> 32));
+    };
+    for (size_t i = 0; i < dq.size(); i += kWords) {
+        int32_t* x = &dq[i];
+        const int op = x[W_OP];
+        if (op == OP_END || op < 0 || op >= OP_COUNT || op == OP_COMB) continue;
+        const int l = x[W_LAYER], b = x[W_B], a0 = x[W_A0], a1 = x[W_A1], a2 = x[W_A2];
+        const long slot = long(i / kWords);
+        auto bad = [&](const char* what) {
+            return fail(MK_ERR_BOUNDS, "queue %ld slot %ld: %s", slot / s->Q, slot % s->Q, what);
+        };
+        if (x[W_NWAIT] < 0 || x[W_NWAIT] > kMaxWait || x[W_NPUB] < 0 || x[W_NPUB] > kMaxPub) return bad("wait/completion count");
+        for (int k = 0; k < x[W_NWAIT]; ++k)
+            if (unsigned(x[W_WAIT + 2 * k]) >= unsigned(g.n_counters)) return bad("counter id");
+        for (int k = 0; k < x[W_NPUB]; ++k)
+            if (unsigned(x[W_PUB + 2 * k]) >= unsigned(g.n_counters)) return bad("counter id");
+        const bool head = op == OP_LMHEAD || op == OP_ARGMAX;
+        if (head ? l != L : unsigned(l) >= unsigned(L)) return bad("layer");
+        if (unsigned(b) >= unsigned(B)) return bad("sequence");
+        auto rows = [&](int total, int maxn) { return a0 >= 0 && a1 >= 1 && a1 <= maxn && a0 + a1 <= total; };
+        const void* src0 = nullptr;
+        const void* src1 = nullptr;
+        int64_t b0 = 0, b1 = 0;
+        switch (op) {
+            case OP_QKV:
+                if (!rows(nqkv, kMaxRows)) return bad("rows");
+                src0 = static_cast<const uint8_t*>(w->wqkv[l]) + int64_t(a0) * H * 2;
+                b0 = int64_t(a1) * H * 2;
+                break;
+            case OP_OPROJ:
+                if (!rows(H, kMaxRows)) return bad("rows");
+                src0 = static_cast<const uint8_t*>(w->wo[l]) + int64_t(a0) * qd * 2;
+                b0 = int64_t(a1) * qd * 2;
+                break;
+            case OP_UPGATE:
+                if (!rows(F, kMaxRows / 2)) return bad("rows");
+                src0 = static_cast<const uint8_t*>(w->wgate_up[l]) + int64_t(a0) * H * 2;
+                src1 = static_cast<const uint8_t*>(w->wgate_up[l]) + int64_t(F + a0) * H * 2;
+                b0 = b1 = int64_t(a1) * H * 2;
+                break;
+            case OP_DOWN:
+                if (!rows(H, kMaxRows)) return bad("rows");
+                src0 = static_cast<const uint8_t*>(w->wdown[l]) + int64_t(a0) * F * 2;
+                b0 = int64_t(a1) * F * 2;
+                break;
+            case OP_LMHEAD:
+                if (!rows(V, kMaxRows) || unsigned(a2) >= unsigned(g.n_lm)) return bad("rows");
+                src0 = static_cast<const uint8_t*>(w->lm_head) + int64_t(a0) * H * 2;
+                b0 = int64_t(a1) * H * 2;
+                break;
+            case OP_ATTN:
+                if (unsigned(a0) >= unsigned(nkv) || unsigned(a1) >= unsigned(g.n_chunk) || a2 != g.attn_chunk ||
+                    x[W_COND] != 1 || unsigned(x[W_ARRIVE]) >= unsigned(g.n_counters) || x[W_ARRIVE_N] != g.n_chunk)
+                    return bad("attention fields");
+                break;
+            case OP_ARGMAX:
+                if (a1 != g.n_lm) return bad("argmax fields");
+                break;
+            default: break;
+        }
+        if (src0) {
+            if ((b0 + b1 + g.page_bytes - 1) / g.page_bytes > x[W_NPAGES]) return bad("page count");
+            put64(x + W_SRC0, src0);
+            put64(x + W_SRC1, src1);
+            x[W_BYTES0] = int32_t(b0);
+            x[W_BYTES1] = int32_t(b1);
+        }
+    }
+    return MK_OK;
+}
+
 extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, uint32_t* counters,
                              void* scratch, void* stream, mk_ctx** out) {
     if (!s || !w || !kv || !counters || !scratch || !out) return fail(MK_ERR_ARG, "null argument");
@@ -97,6 +181,7 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
     if (reinterpret_cast<uintptr_t>(scratch) & 255u) return fail(MK_ERR_ARG, "scratch must be 256-byte aligned");
     if (reinterpret_cast<uintptr_t>(counters) & 3u) return fail(MK_ERR_ARG, "counters must be 4-byte aligned");
     if (g.page_bytes & (g.page_bytes - 1)) return fail(MK_ERR_ARG, "page_bytes must be a power of two");
+    if (L > kMaxLayersSmem) return fail(MK_ERR_ARG, "more than %d layers", kMaxLayersSmem);
 
     // ---- device and resources ----
     int dev = 0, sms = 0, optin = 0;
@@ -104,17 +189,25 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
     CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
     if (s->S > sms) return fail(MK_ERR_RESOURCES, "schedule has %d queues but the device has %d SMs", s->S, sms);
-    const int maxK = std::max(std::max(H, qd), c.ffn);
-    const int nch = (maxK / 8 + kConsumerThreads - 1) / kConsumerThreads;
-    const void* fn = megakernel_fn(nch);
-    if (!fn) return fail(MK_ERR_ARG, "matvec rows longer than %d elements", 8 * 8 * kConsumerThreads);
+    // matvec rows are cut into <= 2048-element segments (a power-of-two count, <= 8); the kernel
+    // is instantiated for the largest number of 16-byte chunks a lane holds of one segment
+    int cpl = 1;
+    for (int K : {H, qd, c.ffn}) {
+        int nseg = 1;
+        while (K > 2048 * nseg) nseg <<= 1;
+        if (nseg > 8 || K % (8 * nseg)) return fail(MK_ERR_ARG, "matvec row length %d cannot be cut into segments", K);
+        cpl = std::max(cpl, (K / nseg / 8 + 31) / 32);
+    }
+    const void* fn = megakernel_fn(cpl);
+    if (!fn) return fail(MK_ERR_ARG, "no kernel for %d chunks per lane", cpl);
     int asf = std::max(hpg * g.attn_chunk, hpg * g.n_chunk);
     asf = (asf + 3) & ~3;
-    const int misc0 = smem_misc_bytes(0, asf);
+    const int qrf = (hpg * d + 3) & ~3;
+    const int misc0 = smem_misc_bytes(0, asf, qrf);
     int n_pages = (optin - misc0 - 1024) / (g.page_bytes + 16);
     if (n_pages < 1) return fail(MK_ERR_CAPACITY, "no room for a page ring");
-    int misc = smem_misc_bytes(n_pages, asf);
-    while (n_pages > 0 && int64_t(n_pages) * g.page_bytes + misc > optin) misc = smem_misc_bytes(--n_pages, asf);
+    int misc = smem_misc_bytes(n_pages, asf, qrf);
+    while (n_pages > 0 && int64_t(n_pages) * g.page_bytes + misc > optin) misc = smem_misc_bytes(--n_pages, asf, qrf);
     if (n_pages < std::max(2, s->max_pages))
         return fail(MK_ERR_CAPACITY, "page ring of %d pages cannot hold a tile of %d pages", n_pages, s->max_pages);
     const int smem = n_pages * g.page_bytes + misc;
@@ -144,14 +237,25 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
         lp[l] = {static_cast<const uint16_t*>(w->attn_norm[l]), static_cast<const uint16_t*>(w->wqkv[l]),
                  static_cast<const uint16_t*>(w->wo[l]), static_cast<const uint16_t*>(w->mlp_norm[l]),
                  static_cast<const uint16_t*>(w->wgate_up[l]), static_cast<const uint16_t*>(w->wdown[l])};
-    if ((e = cudaMemcpy(x->d_queues, s->queues.data(), qbytes, cudaMemcpyHostToDevice)) != cudaSuccess ||
+    std::vector<int32_t> dq;
+    {
+        const mk_status rs = resolve_queues(s, w, dq);
+        if (rs != MK_OK) return bail(rs);
+    }
+    if ((e = cudaMemcpy(x->d_queues, dq.data(), qbytes, cudaMemcpyHostToDevice)) != cudaSuccess ||
         (e = cudaMemcpy(x->d_totals, s->totals.data(), s->totals.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess ||
         (e = cudaMemcpy(x->d_layers, lp.data(), sizeof(LayerPtrs) * L, cudaMemcpyHostToDevice)) != cudaSuccess)
         return bail(cuda_fail(e, "cudaMemcpy(bind tables)"));
 
-    const ScratchLayout sl = scratch_layout(c, g);
+    const ScratchLayout sl = scratch_layout(c, g, s->S);
     uint8_t* sb = static_cast<uint8_t*>(scratch);
     Params& p = x->base;
+    for (int op = 0; op < OP_COUNT; ++op) {
+        const int K = op == OP_OPROJ ? qd : (op == OP_DOWN ? c.ffn : H);
+        int nseg = 1, lg = 0;
+        while (K > 2048 * nseg) { nseg <<= 1; ++lg; }
+        p.mv[op] = {K, nseg, lg, uint32_t(K) * 2u, (uint32_t(K) * 2u) >> lg, int32_t(((uint32_t(K) * 2u) >> lg) >> 4)};
+    }
     p.L = L; p.H = H; p.nq = c.n_q_heads; p.nkv = c.n_kv_heads; p.d = d; p.F = c.ffn; p.V = c.vocab;
     p.B = c.batch; p.max_seq = c.max_seq; p.hpg = hpg; p.qd = qd; p.kvd = c.n_kv_heads * d;
     p.nqkv = qd + 2 * p.kvd;
@@ -186,14 +290,16 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
     p.part = reinterpret_cast<float*>(sb + sl.part);
     p.o = reinterpret_cast<float*>(sb + sl.o);
     p.h = reinterpret_cast<float*>(sb + sl.h);
-    p.lm_part = reinterpret_cast<float2*>(sb + sl.lm_part);
+    p.lm_part = reinterpret_cast<int4*>(sb + sl.lm_part);
     p.rope = reinterpret_cast<const float2*>(sb + sl.rope);
     p.timeout_ns = 2000000000ull;
     p.smem_misc_off = n_pages * g.page_bytes;
     p.attn_scratch_floats = asf;
+    p.qrot_floats = qrf;
 
     if ((e = cudaMemsetAsync(counters, 0, s->totals.size() * 4, x->stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(sb + sl.err, 0, 256, x->stream)) != cudaSuccess)
+        (e = cudaMemsetAsync(sb + sl.err, 0, 256, x->stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(sb + sl.lm_part, 0xFF, size_t(c.batch) * s->S * kNumConsumerWarps * 16, x->stream)) != cudaSuccess)
         return bail(cuda_fail(e, "cudaMemsetAsync"));
     if ((e = launch_rope_table(reinterpret_cast<float2*>(sb + sl.rope), c.max_seq, d, c.rope_theta, x->stream)) !=
         cudaSuccess)
@@ -206,6 +312,13 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
 extern "C" mk_status mk_set_timeout(mk_ctx* c, uint64_t ns) {
     if (!c || ns == 0) return fail(MK_ERR_ARG, "bad argument");
     c->base.timeout_ns = ns;
+    return MK_OK;
+}
+
+extern "C" mk_status mk_set_trace(mk_ctx* c, uint64_t* buf) {
+    if (!c) return fail(MK_ERR_ARG, "null context");
+    if (reinterpret_cast<uintptr_t>(buf) & 7u) return fail(MK_ERR_ARG, "trace buffer not 8-byte aligned");
+    c->base.trace = buf;
     return MK_OK;
 }
 

@@ -14,17 +14,34 @@ enum Op : int32_t { OP_END = 0, OP_QKV = 1, OP_ATTN = 2, OP_COMB = 3, OP_OPROJ =
                     OP_DOWN = 6, OP_LMHEAD = 7, OP_ARGMAX = 8, OP_COUNT = 9 };
 enum Word : int {
     W_OP = 0, W_LAYER = 1, W_B = 2, W_A0 = 3, W_A1 = 4, W_A2 = 5, W_NWAIT = 6, W_WAIT = 7,
-    W_NPUB = 15, W_PUB = 16, W_NPAGES = 20, W_TILE = 21, W_WAVE = 22
+    W_NPUB = 15, W_PUB = 16, W_NPAGES = 20, W_TILE = 21, W_WAVE = 22,
+    W_COND = 23, W_ARRIVE = 24, W_ARRIVE_N = 25,  // completions only from the last of N arrivals
+    W_SRC0 = 26, W_SRC1 = 28, W_BYTES0 = 30, W_BYTES1 = 31   // device copy: resolved weight stream (matvec)
 };
 constexpr int kWords = 32;
 constexpr int kMaxWait = 4;
 constexpr int kMaxPub = 2;
 constexpr int kMaxBatch = 8;
-constexpr int kMaxRows = 8;        // rows of one matvec tile
+constexpr int kMaxRows = 32;       // rows of one matvec tile (pairs of gate/up rows: half)
 constexpr int kMaxHpg = 8;         // query heads per KV head
 constexpr int kMaxHeadDim = 128;
 constexpr int kMaxK = 16384;       // longest matvec row (elements)
 constexpr int64_t kTileOverhead = 1024;
+
+// shared-memory layout of one CTA (after the page ring)
+constexpr int kNumConsumerWarps = 8;
+constexpr int kConsumerThreads = kNumConsumerWarps * 32;
+constexpr int kLoaderWarp = 8;
+constexpr int kPublisherWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kSlots = 16;   // instruction slots in flight
+constexpr int kQWin = 16;    // instructions per queue-window buffer (two buffers, bulk-copied)
+constexpr int kMaxLayersSmem = 40;   // layer pointer table cached in shared memory
+constexpr int kDone = 64;            // completion records the publisher may lag behind
+constexpr int kTraceWords = 8;       // trace stamps per instruction
+constexpr int kCombStride = 64;      // split-row partials per instruction slot (rows x segments x 2 <= 64)
+constexpr int kXBuf = 2048;          // floats of the shared matvec input buffer (one x per CTA)
+
 
 // ---- resolved schedule parameters -----------------------------------------------------------
 struct Geometry {
@@ -59,7 +76,7 @@ struct ScratchLayout {
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-inline ScratchLayout scratch_layout(const mk_model_cfg& c, const Geometry& g) {
+inline ScratchLayout scratch_layout(const mk_model_cfg& c, const Geometry& g, int S) {
     const size_t L = c.n_layers, B = c.batch, H = c.hidden, d = c.head_dim;
     const size_t qd = size_t(c.n_q_heads) * d, kvd = size_t(c.n_kv_heads) * d;
     const size_t hpg = c.n_q_heads / c.n_kv_heads;
@@ -74,7 +91,7 @@ inline ScratchLayout scratch_layout(const mk_model_cfg& c, const Geometry& g) {
     s.part = take(L * B * size_t(c.n_kv_heads) * g.n_chunk * hpg * (d + 2) * 4);
     s.o = take(L * B * qd * 4);
     s.h = take(L * B * size_t(c.ffn) * 4);
-    s.lm_part = take(B * size_t(g.n_lm) * 8);
+    s.lm_part = take(B * size_t(S) * kNumConsumerWarps * 2 * 16);   // per (sequence, CTA, warp half): max, index, epoch
     s.rope = take(size_t(c.max_seq) * (d / 2) * 8);
     s.total = off;
     return s;
@@ -90,8 +107,17 @@ struct LayerPtrs {
     const uint16_t* wdown;
 };
 
+// matvec shape per opcode, resolved at bind
+struct MvShape {
+    int32_t K;               // row length (elements)
+    int32_t nseg, lognseg;   // segments per row (each <= 2048 elements), log2
+    uint32_t rowbytes, segbytes;
+    int32_t segch;           // 16-byte chunks per segment
+};
+
 // ---- kernel parameters (passed by value) ----------------------------------------------------
 struct Params {
+    MvShape mv[OP_COUNT];
     // model
     int32_t L, H, nq, nkv, d, F, V, B, max_seq, hpg, qd, kvd, nqkv;
     float rms_eps, attn_scale;
@@ -120,7 +146,7 @@ struct Params {
     float* part;
     float* o;
     float* h;
-    float2* lm_part;   // (value, index bits)
+    int4* lm_part;     // [B][S][16]: (max bits, index, epoch, 0)
     const float2* rope; // [max_seq][d/2] (cos, sin)
     // step
     uint32_t epoch;
@@ -129,38 +155,69 @@ struct Params {
     float* logits;
     int32_t* next_dev;
     uint64_t timeout_ns;
+    uint64_t* trace;         // optional [S][Q][8] globaltimer stamps (null: off)
     // shared-memory carve-up
     int32_t smem_misc_off;   // byte offset of the non-ring area
     int32_t attn_scratch_floats;
+    int32_t qrot_floats;
 };
 
-// shared-memory layout of one CTA (after the page ring)
-constexpr int kNumConsumerWarps = 8;
-constexpr int kConsumerThreads = kNumConsumerWarps * 32;
-constexpr int kLoaderWarp = 8;
-constexpr int kPublisherWarp = 9;
-constexpr int kThreads = 320;
-constexpr int kSlots = 16;   // instruction slots in flight
-
-struct SlotInfo {            // one instruction slot: words + where its stream sits in the ring
+struct SlotInfo {            // one instruction slot: words + where its stream sits + decoded matvec shape
     int32_t w[kWords];
-    int32_t first_page;
+    int32_t first_page;      // global page sequence number of the stream's first page
     int32_t n_pages;
-    int32_t pad[2];
+    int32_t first_slot;      // ring slot of the first page
+    int32_t K;               // matvec: row length (elements)
+    int32_t nseg, lognseg;   // segments per row (<= 2048 elements each), log2
+    int32_t units;           // row units (rows, or gate/up pairs) x segments when split, else row units
+    int32_t split;           // 1: the segments of a row go to different warps (batch 1)
+    uint32_t rowbytes, segbytes;
+    int32_t segch;           // 16-byte chunks per segment
+    int32_t first_phase;     // mbarrier phase parity of the first page
 };
 
-// bytes of the non-ring shared memory (slots, barriers, reduction and attention scratch)
-inline int smem_misc_bytes(int n_pages, int attn_scratch_floats) {
-    size_t b = 0;
-    b += sizeof(SlotInfo) * kSlots;
-    b += 8 * (2 * size_t(n_pages) + 3 * kSlots);   // mbarriers
-    b += 4 * (2 * kNumConsumerWarps * kMaxRows);   // matvec reduction (double buffered)
-    b += 4 * 64;                                   // norm reduction, flags, misc
-    b += 4 * size_t(kMaxHpg) * kMaxHeadDim;        // rotated q
-    b += 4 * size_t(attn_scratch_floats);          // scores / combine factors
-    b += 2 * 2 * kMaxHeadDim;                      // new k, v (bf16)
-    b += 4 * 2 * kMaxHpg * 2;                      // (m, l) per head, combine (M, L)
-    return int(align256(b + 256));
+#ifdef __CUDACC__
+#define MK_HD __host__ __device__
+#else
+#define MK_HD
+#endif
+
+// byte offsets of the non-ring shared memory (after the page ring); shared by host and device
+struct MiscLayout {
+    uint32_t slots, qwin, layers, bars, lmbest, comb, combcnt, pubinfo, red, qrot, ascr, ml, kv, xbuf, total;
+};
+
+MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qrot_floats) {
+    MiscLayout m{};
+    uint32_t o = 0;
+    auto take = [&o](uint32_t bytes, uint32_t align) {
+        o = (o + align - 1) & ~(align - 1);
+        const uint32_t r = o;
+        o += bytes;
+        return r;
+    };
+    m.slots = take(uint32_t(sizeof(SlotInfo)) * kSlots, 16);
+    m.qwin = take(2u * kQWin * kWords * 4u, 16);
+    m.layers = take(uint32_t(sizeof(LayerPtrs)) * kMaxLayersSmem, 16);
+    m.bars = take(8u * (2u + 2u * uint32_t(n_pages) + 2u * kSlots + kDone + 3u), 8);  // qfull, full, empty, ins, done, cbar, xfull, xfree
+    m.lmbest = take(8u * kNumConsumerWarps * 2u * kMaxBatch, 8);   // LM-head running (max, index) per warp half / sequence
+    m.comb = take(4u * kSlots * kCombStride, 16);   // split-row segment partials
+    m.combcnt = take(4u * kSlots * kMaxRows, 16);
+    m.pubinfo = take(4u * kDone * 8u, 16);            // completion words of in-flight instructions
+    m.red = take(4u * 64u, 16);                     // argmax scratch [16]; abort flag [32], published count [33],
+                                                    // stream bytes the loader has issued [34..35] (u64),
+                                                    // last-arrival flag [40], shared x scale [41]
+    m.qrot = take(4u * uint32_t(qrot_floats), 16);
+    m.ascr = take(4u * uint32_t(attn_scratch_floats), 16);
+    m.ml = take(4u * 4u * kMaxHpg, 16);             // (m, l) per head, combine L per head
+    m.kv = take(2u * 2u * kMaxHeadDim, 16);         // new k, v (bf16)
+    m.xbuf = take(4u * kXBuf, 16);                  // shared matvec input (raw), one per CTA
+    m.total = (o + 255u) & ~255u;
+    return m;
+}
+
+inline int smem_misc_bytes(int n_pages, int attn_scratch_floats, int qrot_floats) {
+    return int(misc_layout(n_pages, attn_scratch_floats, qrot_floats).total);
 }
 
 // records a message for mk_last_error() and returns st

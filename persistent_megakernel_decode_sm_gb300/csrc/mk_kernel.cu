@@ -54,6 +54,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// waits up to ~hint_ns for the phase (the thread is suspended, not spinning; completion wakes it)
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ uint64_t evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -71,7 +91,14 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// acquire / release halves of the counter protocol (cheaper than a full acq_rel fence)
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_release_gpu() { asm volatile("fence.release.gpu;" ::: "memory"); }
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 __device__ __forceinline__ void red_add_relaxed_gpu(uint32_t* p, uint32_t v) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -80,20 +107,8 @@ __device__ __forceinline__ uint64_t globaltimer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// named barrier 1 over the 256 consumer threads (non-.aligned form: lanes may arrive apart)
-__device__ __forceinline__ void cons_sync() { asm volatile("barrier.sync 1, 256;" ::: "memory"); }
 // whole-CTA barrier reached by warps whose lanes diverged (loader / publisher lane 0 arrives late)
 __device__ __forceinline__ void cta_sync_divergent() { asm volatile("barrier.sync 0;" ::: "memory"); }
-// same barrier, returning the OR of every consumer thread's predicate (uniform result)
-__device__ __forceinline__ bool cons_sync_or(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(uint32_t(pred))
-        : "memory");
-    return r != 0;
-}
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -126,46 +141,75 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
+// optional per-instruction timeline: [0] slot published by the loader, [1] its pages issued,
+// [2] dependencies satisfied, [3] body done, [4] completions published, [5] CTA start
+__device__ __forceinline__ void stamp(const Params& p, int pc, int k) {
+    if (p.trace) p.trace[(size_t(blockIdx.x) * p.Q + pc) * kTraceWords + k] = globaltimer();
+}
+
 // ------------------------------------------------------------------------- shared memory ----
 struct Shared {
     uint8_t* ring;
     SlotInfo* slots;
-    uint64_t* full;
-    uint64_t* empty;
+    int32_t* qwin;     // [2][kQWin][32] queue window
+    LayerPtrs* layers; // [L]
+    uint64_t* qfull;   // [2]
+    uint64_t* full;    // [n_pages]
+    uint64_t* empty;   // [n_pages]
     uint64_t* ins_full;
     uint64_t* ins_empty;
     uint64_t* done;
-    float* red;      // [2][8 warps][8 rows]
-    float* normred;  // [8]
-    int* abort;      // [1]
-    float* qrot;     // [8][128]
-    float* ascr;     // [attn_scratch_floats]
-    uint16_t* knew;  // [128]
-    uint16_t* vnew;  // [128]
-    float* ml;       // [8][2]
-    float* cml;      // [8]
+    uint64_t* cbar;    // consumer-warp barrier (8 arrivals)
+    uint64_t* xfull;   // shared x written (1 arrival: warp 0)
+    uint64_t* xfree;   // shared x taken by every warp (8 arrivals)
+    float* xbuf;       // [kXBuf] shared matvec input
+    float2* lmbest;    // [8 warps][kMaxBatch] LM-head running (max, index)
+    float* comb;       // [kSlots][64] split-row segment partials
+    int* combcnt;      // [kSlots][8]
+    int* pubinfo;      // [kDone][8]: opcode, #completions, (counter, delta) x 2
+    float* red;        // [16] argmax scratch
+    int* abort;        // [1]
+    int* published;    // [1] instructions the publisher has retired
+    unsigned long long* issued;   // [1] stream bytes the loader has staged into pages
+    float* qrot;       // [8][128]
+    float* ascr;       // [attn_scratch_floats]
+    float* ml;         // [8][2]
+    float* cml;        // [8]
+    uint16_t* knew;    // [128]
+    uint16_t* vnew;    // [128]
 };
 
 __device__ __forceinline__ Shared carve(uint8_t* base, const Params& p) {
+    const MiscLayout m = misc_layout(p.n_pages, p.attn_scratch_floats, p.qrot_floats);
+    uint8_t* b = base + p.smem_misc_off;
     Shared s;
     s.ring = base;
-    uint8_t* m = base + p.smem_misc_off;
-    s.slots = reinterpret_cast<SlotInfo*>(m);
-    m += sizeof(SlotInfo) * kSlots;
-    s.full = reinterpret_cast<uint64_t*>(m);
+    s.slots = reinterpret_cast<SlotInfo*>(b + m.slots);
+    s.qwin = reinterpret_cast<int32_t*>(b + m.qwin);
+    s.layers = reinterpret_cast<LayerPtrs*>(b + m.layers);
+    s.qfull = reinterpret_cast<uint64_t*>(b + m.bars);
+    s.full = s.qfull + 2;
     s.empty = s.full + p.n_pages;
     s.ins_full = s.empty + p.n_pages;
     s.ins_empty = s.ins_full + kSlots;
     s.done = s.ins_empty + kSlots;
-    m = reinterpret_cast<uint8_t*>(s.done + kSlots);
-    s.red = reinterpret_cast<float*>(m);
-    s.normred = s.red + 2 * kNumConsumerWarps * kMaxRows;
-    s.abort = reinterpret_cast<int*>(s.normred + 8);
-    s.qrot = reinterpret_cast<float*>(s.abort + 56);
-    s.ascr = s.qrot + kMaxHpg * kMaxHeadDim;
-    s.ml = s.ascr + p.attn_scratch_floats;
+    s.cbar = s.done + kDone;
+    s.xfull = s.cbar + 1;
+    s.xfree = s.cbar + 2;
+    s.xbuf = reinterpret_cast<float*>(b + m.xbuf);
+    s.lmbest = reinterpret_cast<float2*>(b + m.lmbest);
+    s.comb = reinterpret_cast<float*>(b + m.comb);
+    s.combcnt = reinterpret_cast<int*>(b + m.combcnt);
+    s.pubinfo = reinterpret_cast<int*>(b + m.pubinfo);
+    s.red = reinterpret_cast<float*>(b + m.red);
+    s.abort = reinterpret_cast<int*>(b + m.red) + 32;
+    s.published = reinterpret_cast<int*>(b + m.red) + 33;
+    s.issued = reinterpret_cast<unsigned long long*>(reinterpret_cast<int*>(b + m.red) + 34);
+    s.qrot = reinterpret_cast<float*>(b + m.qrot);
+    s.ascr = reinterpret_cast<float*>(b + m.ascr);
+    s.ml = reinterpret_cast<float*>(b + m.ml);
     s.cml = s.ml + 2 * kMaxHpg;
-    s.knew = reinterpret_cast<uint16_t*>(s.cml + 2 * kMaxHpg);
+    s.knew = reinterpret_cast<uint16_t*>(b + m.kv);
     s.vnew = s.knew + kMaxHeadDim;
     return s;
 }
@@ -185,17 +229,22 @@ __device__ void raise_error(const Params& p, const Shared& sh, int code, int rol
 }
 
 // bounded mbarrier wait: false when the CTA aborts or the budget runs out (error recorded)
-__device__ bool wait_bar(const Params& p, const Shared& sh, uint64_t* bar, uint32_t parity, int role, int pc) {
-    if (mbar_try_wait(bar, parity)) return true;
+// (the waiting thread sleeps in hardware between checks of the abort flag and the time budget)
+__device__ bool wait_bar_slow(const Params& p, const Shared& sh, uint64_t* bar, uint32_t parity, int role,
+                                           int pc) {
     const uint64_t t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*reinterpret_cast<volatile int*>(sh.abort)) return false;
         if (globaltimer() - t0 > p.timeout_ns) {
             raise_error(p, sh, MK_ERR_TIMEOUT, role, pc, -1, 0, 0);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_bar(const Params& p, const Shared& sh, uint64_t* bar, uint32_t parity, int role,
+                                         int pc) {
+    return mbar_try_wait(bar, parity) || wait_bar_slow(p, sh, bar, parity, role, pc);
 }
 
 // ------------------------------------------------------------------------- streams ----------
@@ -217,79 +266,47 @@ __device__ __forceinline__ int attn_old_rows(const Params& p, int b, int c, int 
     return min(c0 + chunk, pos) - c0;        // cached positions strictly before pos
 }
 
-// validates an instruction and describes the bytes its body streams; returns an mk_status
-__device__ int describe(const Params& p, const int32_t* w, Stream& st) {
+__device__ __forceinline__ const uint8_t* word_ptr(const int32_t* w) {
+    return reinterpret_cast<const uint8_t*>((uint64_t(uint32_t(w[1])) << 32) | uint64_t(uint32_t(w[0])));
+}
+__device__ __forceinline__ bool is_matvec(int op) {
+    return op == OP_QKV || op == OP_OPROJ || op == OP_UPGATE || op == OP_DOWN || op == OP_LMHEAD;
+}
+
+// The bytes an instruction's body streams.  Matvec tiles carry their resolved weight stream in
+// words 26..31 (written and validated at bind); an attention chunk's cached KV rows depend on pos
+// and are computed here (with the chunk's bounds checked).  Returns an mk_status.
+__device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
     st.nseg = 0;
     st.total = 0;
     st.pages = 0;
     const int op = w[W_OP];
-    if (op == OP_END) return MK_OK;
-    if (op <= 0 || op >= OP_COUNT) return MK_ERR_OPCODE;
-    const int l = w[W_LAYER], b = w[W_B], a0 = w[W_A0], a1 = w[W_A1], a2 = w[W_A2];
-    if (w[W_NWAIT] < 0 || w[W_NWAIT] > kMaxWait || w[W_NPUB] < 0 || w[W_NPUB] > kMaxPub) return MK_ERR_BOUNDS;
-    for (int i = 0; i < w[W_NWAIT]; ++i)
-        if (unsigned(w[W_WAIT + 2 * i]) >= unsigned(p.n_counters)) return MK_ERR_BOUNDS;
-    for (int i = 0; i < w[W_NPUB]; ++i)
-        if (unsigned(w[W_PUB + 2 * i]) >= unsigned(p.n_counters)) return MK_ERR_BOUNDS;
-    const bool head = (op == OP_LMHEAD || op == OP_ARGMAX);
-    if (head ? (l != p.L) : (unsigned(l) >= unsigned(p.L))) return MK_ERR_BOUNDS;
-    if (unsigned(b) >= unsigned(p.B)) return MK_ERR_BOUNDS;
-    auto rows = [&](int nrows_total, int maxn) { return a0 >= 0 && a1 >= 1 && a1 <= maxn && a0 + a1 <= nrows_total; };
-    const LayerPtrs* lp = head ? nullptr : &p.layers[l];
-    switch (op) {
-        case OP_QKV:
-            if (!rows(p.nqkv, kMaxRows)) return MK_ERR_BOUNDS;
-            st.seg[0] = {reinterpret_cast<const uint8_t*>(lp->wqkv) + size_t(a0) * p.H * 2, 0, uint32_t(a1 * p.H * 2)};
-            st.nseg = 1;
-            break;
-        case OP_OPROJ:
-            if (!rows(p.H, kMaxRows)) return MK_ERR_BOUNDS;
-            st.seg[0] = {reinterpret_cast<const uint8_t*>(lp->wo) + size_t(a0) * p.qd * 2, 0, uint32_t(a1 * p.qd * 2)};
-            st.nseg = 1;
-            break;
-        case OP_UPGATE: {
-            if (!rows(p.F, kMaxRows / 2)) return MK_ERR_BOUNDS;
-            const uint32_t nb = uint32_t(a1 * p.H * 2);
-            st.seg[0] = {reinterpret_cast<const uint8_t*>(lp->wgate_up) + size_t(a0) * p.H * 2, 0, nb};
-            st.seg[1] = {reinterpret_cast<const uint8_t*>(lp->wgate_up) + size_t(p.F + a0) * p.H * 2, nb, nb};
+    if (is_matvec(op)) {
+        const uint32_t b0 = uint32_t(w[W_BYTES0]), b1 = uint32_t(w[W_BYTES1]);
+        st.seg[0] = {word_ptr(w + W_SRC0), 0u, b0};
+        st.seg[1] = {word_ptr(w + W_SRC1), b0, b1};
+        st.nseg = b1 ? 2 : 1;
+        st.total = b0 + b1;
+        if (b0 == 0) return MK_ERR_BOUNDS;
+    } else if (op == OP_ATTN) {
+        const int l = w[W_LAYER], b = w[W_B], g = w[W_A0], c = w[W_A1], C = w[W_A2];
+        if (unsigned(l) >= unsigned(p.L) || unsigned(b) >= unsigned(p.B) || unsigned(g) >= unsigned(p.nkv) ||
+            unsigned(c) >= unsigned(p.n_chunk) || C != p.attn_chunk)
+            return MK_ERR_BOUNDS;
+        const int n_old = attn_old_rows(p, b, c, C);
+        if (n_old > 0) {
+            const size_t base = size_t(b) * p.kv_bstride + size_t(l) * p.kv_lstride + size_t(g) * p.kv_hstride +
+                                size_t(c) * C * p.d;
+            const uint32_t nb = uint32_t(n_old * p.d * 2);
+            st.seg[0] = {reinterpret_cast<const uint8_t*>(p.kc + base), 0u, nb};
+            st.seg[1] = {reinterpret_cast<const uint8_t*>(p.vc + base), nb, nb};
             st.nseg = 2;
-            break;
+            st.total = 2 * nb;
         }
-        case OP_DOWN:
-            if (!rows(p.H, kMaxRows)) return MK_ERR_BOUNDS;
-            st.seg[0] = {reinterpret_cast<const uint8_t*>(lp->wdown) + size_t(a0) * p.F * 2, 0, uint32_t(a1 * p.F * 2)};
-            st.nseg = 1;
-            break;
-        case OP_LMHEAD:
-            if (!rows(p.V, kMaxRows) || unsigned(a2) >= unsigned(p.n_lm)) return MK_ERR_BOUNDS;
-            st.seg[0] = {reinterpret_cast<const uint8_t*>(p.lm_head) + size_t(a0) * p.H * 2, 0, uint32_t(a1 * p.H * 2)};
-            st.nseg = 1;
-            break;
-        case OP_ATTN: {
-            if (unsigned(a0) >= unsigned(p.nkv) || unsigned(a1) >= unsigned(p.n_chunk) || a2 != p.attn_chunk)
-                return MK_ERR_BOUNDS;
-            const int n_old = attn_old_rows(p, b, a1, a2);
-            if (n_old > 0) {
-                const size_t base = size_t(b) * p.kv_bstride + size_t(l) * p.kv_lstride + size_t(a0) * p.kv_hstride +
-                                    size_t(a1) * a2 * p.d;
-                const uint32_t nb = uint32_t(n_old * p.d * 2);
-                st.seg[0] = {reinterpret_cast<const uint8_t*>(p.kc + base), 0, nb};
-                st.seg[1] = {reinterpret_cast<const uint8_t*>(p.vc + base), nb, nb};
-                st.nseg = 2;
-            }
-            break;
-        }
-        case OP_COMB:
-            if (unsigned(a0) >= unsigned(p.nkv) || a1 != p.n_chunk || a2 != p.attn_chunk) return MK_ERR_BOUNDS;
-            break;
-        case OP_ARGMAX:
-            if (a1 != p.n_lm) return MK_ERR_BOUNDS;
-            break;
-        default:
-            return MK_ERR_OPCODE;
+    } else if (op != OP_ARGMAX && op != OP_END) {
+        return MK_ERR_OPCODE;
     }
-    for (int i = 0; i < st.nseg; ++i) st.total += st.seg[i].bytes;
-    st.pages = int((st.total + uint32_t(p.page_bytes) - 1) / uint32_t(p.page_bytes));
+    st.pages = int((st.total + uint32_t(p.page_bytes) - 1u) >> p.page_shift);
     if (st.pages > w[W_NPAGES] || st.pages > p.n_pages) return MK_ERR_CAPACITY;
     return MK_OK;
 }
@@ -300,45 +317,112 @@ __device__ void loader(const Params& p, const Shared& sh) {
     const uint64_t pol = evict_first_policy();
     const uint32_t PB = uint32_t(p.page_bytes);
     const uint32_t NP = uint32_t(p.n_pages);
-    uint32_t page_seq = 0;
+    const int n_chunks = (p.Q + kQWin - 1) / kQWin;
+    // the queue is read through a two-buffer shared-memory window, kQWin instructions per bulk copy
+    auto fetch_chunk = [&](int chunk) {
+        const int n = min(kQWin, p.Q - chunk * kQWin);
+        uint64_t* bar = sh.qfull + (chunk & 1);
+        mbar_arrive_expect_tx(bar, uint32_t(n * kWords * 4));
+        bulk_g2s(sh.qwin + (chunk & 1) * kQWin * kWords, q + size_t(chunk) * kQWin * kWords, uint32_t(n * kWords * 4),
+                 bar, pol);
+    };
+    fetch_chunk(0);
+    if (n_chunks > 1) fetch_chunk(1);
+    int chunks_issued = n_chunks > 1 ? 2 : 1;
+    int chunks_waited = 0;
+    uint32_t page_seq = 0;                   // pages issued so far
+    uint32_t cur_slot = 0, cur_phase = 0;    // ring slot and phase parity of the next page
     for (int pc = 0; pc < p.Q; ++pc) {
         const int slot = pc % kSlots;
+        const int chunk = pc / kQWin;
+        if (pc % kQWin == 0) {
+            if (!wait_bar(p, sh, sh.qfull + (chunk & 1), (chunk >> 1) & 1, ROLE_LOADER, pc)) break;
+            chunks_waited = chunk + 1;
+        }
         if (pc >= kSlots && !wait_bar(p, sh, sh.ins_empty + slot, ((pc / kSlots) - 1) & 1, ROLE_LOADER, pc)) break;
         SlotInfo& si = sh.slots[slot];
-        const int4* src = reinterpret_cast<const int4*>(q + size_t(pc) * kWords);
+        const int4* src = reinterpret_cast<const int4*>(sh.qwin + ((chunk & 1) * kQWin + pc % kQWin) * kWords);
 #pragma unroll
-        for (int i = 0; i < kWords / 4; ++i) reinterpret_cast<int4*>(si.w)[i] = __ldg(src + i);
+        for (int i = 0; i < kWords / 4; ++i) reinterpret_cast<int4*>(si.w)[i] = src[i];
+        if (pc % kQWin == kQWin - 1 && chunks_issued < n_chunks) {
+            fence_proxy_async_smem();   // generic reads of this buffer before the async refill
+            fetch_chunk(chunks_issued++);
+        }
         Stream st;
-        const int e = describe(p, si.w, st);
+        const int e = stream_of(p, si.w, st);
         if (e != MK_OK) {
             raise_error(p, sh, e, ROLE_LOADER, pc, -1, uint32_t(si.w[W_OP]), 0);
             break;
         }
         si.first_page = int32_t(page_seq);
         si.n_pages = st.pages;
+        si.first_slot = int32_t(cur_slot);
+        si.first_phase = int32_t(cur_phase);
+        if (is_matvec(si.w[W_OP])) {   // shape of the op (bind-time table) and of this tile
+            const MvShape& m = p.mv[si.w[W_OP]];
+            const int n = si.w[W_A1];
+            const bool split = p.B == 1 && m.nseg > 1 && n * m.nseg * (si.w[W_OP] == OP_UPGATE ? 2 : 1) <= kCombStride;
+            si.K = m.K;
+            si.nseg = m.nseg;
+            si.lognseg = m.lognseg;
+            si.split = split;
+            si.units = split ? n * m.nseg : n;
+            si.rowbytes = m.rowbytes;
+            si.segbytes = m.segbytes;
+            si.segch = m.segch;
+        }
+        {   // completion words for the publisher, which may lag up to kDone instructions behind
+            const uint64_t t0 = globaltimer();
+            bool stalled = false;
+            while (pc - *reinterpret_cast<volatile int*>(sh.published) >= kDone) {
+                __nanosleep(200);
+                if (*reinterpret_cast<volatile int*>(sh.abort)) { stalled = true; break; }
+                if (globaltimer() - t0 > p.timeout_ns) {
+                    raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_LOADER, pc, -1, 0, 0);
+                    stalled = true;
+                    break;
+                }
+            }
+            if (stalled) break;
+            int* pi = sh.pubinfo + (pc % kDone) * 8;
+            pi[0] = si.w[W_OP];
+            pi[1] = si.w[W_NPUB];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pi[2 + i] = si.w[W_PUB + i];
+            pi[6] = si.w[W_COND];   // 1: completions only if the consumer marks the tile as the group's last
+            pi[7] = 0;              // set by the consumer: this tile completed its group
+        }
+        stamp(p, pc, 0);
         mbar_arrive(sh.ins_full + slot);   // release: the slot's words are visible to the consumers
         if (si.w[W_OP] == OP_END) break;
         bool stop = false;
         for (int pg = 0; pg < st.pages; ++pg) {
-            const uint32_t k = page_seq + uint32_t(pg);
-            const uint32_t ps = k % NP;
-            if (k >= NP && !wait_bar(p, sh, sh.empty + ps, ((k / NP) - 1) & 1, ROLE_LOADER, pc)) {
+            const uint32_t ps = cur_slot;
+            if (page_seq >= NP && !wait_bar(p, sh, sh.empty + ps, cur_phase ^ 1u, ROLE_LOADER, pc)) {
                 stop = true;
-                page_seq = k;   // pages before k were issued
                 break;
             }
             const uint32_t lo = uint32_t(pg) * PB;
             const uint32_t hi = min(lo + PB, st.total);
             mbar_arrive_expect_tx(sh.full + ps, hi - lo);
-            uint8_t* dst = sh.ring + size_t(ps) * PB;
+            uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
             for (int s = 0; s < st.nseg; ++s) {
                 const uint32_t a = max(lo, st.seg[s].off);
                 const uint32_t z = min(hi, st.seg[s].off + st.seg[s].bytes);
                 if (a < z) bulk_g2s(dst + (a - lo), st.seg[s].src + (a - st.seg[s].off), z - a, sh.full + ps, pol);
             }
+            ++page_seq;
+            if (++cur_slot == NP) { cur_slot = 0; cur_phase ^= 1u; }
         }
         if (stop) break;
-        page_seq += uint32_t(st.pages);
+        stamp(p, pc, 1);
+        *reinterpret_cast<volatile unsigned long long*>(sh.issued) += st.total;
+    }
+    // queue-window copies still in flight (prefetched past END, or abandoned on abort)
+    for (int c = chunks_waited; c < chunks_issued; ++c) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(sh.qfull + (c & 1), (c >> 1) & 1))
+            if (globaltimer() - t0 > 1000000000ull) break;   // copies always land; 1 s cap
     }
     if (*reinterpret_cast<volatile int*>(sh.abort)) {
         // drain: wait for the last copy issued into every page so no bulk copy outlives the CTA
@@ -355,24 +439,58 @@ __device__ void loader(const Params& p, const Shared& sh) {
 
 // ------------------------------------------------------------------------- publisher --------
 __device__ void publisher(const Params& p, const Shared& sh) {
-    for (int pc = 0;; ++pc) {
-        const int slot = pc % kSlots;
-        if (!wait_bar(p, sh, sh.done + slot, (pc / kSlots) & 1, ROLE_PUBLISHER, pc)) break;
-        const SlotInfo& si = sh.slots[slot];
-        if (si.w[W_OP] == OP_END) break;
-        const int np = si.w[W_NPUB];
-        fence_acq_rel_gpu();   // everything the consumers wrote for this instruction, then the counters
-        for (int i = 0; i < np; ++i) red_add_relaxed_gpu(p.counters + si.w[W_PUB + 2 * i], uint32_t(si.w[W_PUB + 2 * i + 1]));
-        mbar_arrive(sh.ins_empty + slot);
+    // Retires instructions in queue order.  Every instruction the consumer warps have finished is
+    // taken into one batch: one release fence, then one add per distinct counter.  The publisher
+    // owns its own completion ring (kDone deep), so a slow fence never holds up the loader.
+    constexpr int kBatch = 32;
+    int pc = 0;
+    bool finished = false;
+    while (!finished) {
+        if (!wait_bar(p, sh, sh.done + (pc % kDone), (pc / kDone) & 1, ROLE_PUBLISHER, pc)) break;
+        int n = 1;
+        while (n < kBatch && sh.pubinfo[((pc + n - 1) % kDone) * 8] != OP_END &&
+               mbar_test_wait(sh.done + ((pc + n) % kDone), ((pc + n) / kDone) & 1))
+            ++n;
+        int cid[2 * kBatch], cnt = 0;
+        uint32_t dl[2 * kBatch];
+        for (int i = 0; i < n; ++i) {
+            const int* pi = sh.pubinfo + ((pc + i) % kDone) * 8;
+            if (pi[0] == OP_END) { finished = true; n = i + 1; break; }
+            if (pi[6] && !pi[7]) continue;   // conditional completion not fired by this tile
+            for (int k = 0; k < pi[1]; ++k) {
+                const int c = pi[2 + 2 * k];
+                const uint32_t d = uint32_t(pi[3 + 2 * k]);
+                int j = 0;
+                while (j < cnt && cid[j] != c) ++j;
+                if (j == cnt) { cid[cnt] = c; dl[cnt] = 0; ++cnt; }
+                dl[j] += d;
+            }
+        }
+        if (cnt) {
+            fence_release_gpu();   // everything the consumers wrote for these instructions, then the counters
+            for (int j = 0; j < cnt; ++j) red_add_relaxed_gpu(p.counters + cid[j], dl[j]);
+        }
+        if (p.trace)
+            for (int i = 0; i < n; ++i) stamp(p, pc + i, 4);
+        pc += n;
+        *reinterpret_cast<volatile int*>(sh.published) = pc;
     }
 }
 
-// ------------------------------------------------------------------------- consumer bodies --
-struct Cons {
+// ------------------------------------------------------------------------- consumer warps ---
+// The 8 consumer warps walk the instruction stream independently.  A matvec tile needs no
+// block-level synchronisation: each warp owns whole (row, segment) units with its segment of x
+// in registers; a row split into segments is summed by its last-arriving warp in shared memory,
+// always in segment order.  Attention, combine and argmax cooperate through an mbarrier-based
+// consumer barrier whose waits are bounded and give up when the CTA aborts.
+
+struct Cw {
     const Params& p;
     const Shared& sh;
-    int tid, warp, lane;
-    int rbuf;
+    int warp, lane;
+    uint32_t cb_phase;   // consumer-barrier uses so far
+    uint32_t rot;        // running count of row units (mod 8): rotates units across warps
+    uint32_t xphase;     // shared-x loads so far
 };
 
 __device__ __forceinline__ const uint8_t* ring_ptr(const Shared& sh, const Params& p, uint32_t first_slot, uint32_t off) {
@@ -381,377 +499,509 @@ __device__ __forceinline__ const uint8_t* ring_ptr(const Shared& sh, const Param
     return sh.ring + (size_t(s) << p.page_shift) + (off & (uint32_t(p.page_bytes) - 1u));
 }
 
-// waits every page of the instruction; a failed wait only marks the thread (uniform exit later)
-__device__ bool wait_pages(const Cons& c, const SlotInfo& si, int pc) {
-    bool ok = true;
-    for (int i = 0; i < si.n_pages && ok; ++i) {
-        const uint32_t k = uint32_t(si.first_page) + uint32_t(i);
-        ok = wait_bar(c.p, c.sh, c.sh.full + (k % uint32_t(c.p.n_pages)), (k / uint32_t(c.p.n_pages)) & 1,
-                      ROLE_CONSUMER, pc);
+// Every warp waits for every page of the instruction before it may release them: an early
+// release could otherwise count toward the previous use of the same page slot.
+__device__ bool wait_pages(const Cw& c, const SlotInfo& si, int pc) {
+    uint32_t slot = uint32_t(si.first_slot), ph = uint32_t(si.first_phase);
+    for (int i = 0; i < si.n_pages; ++i) {
+        if (!wait_bar(c.p, c.sh, c.sh.full + slot, ph, ROLE_CONSUMER, pc)) return false;
+        if (++slot == uint32_t(c.p.n_pages)) { slot = 0; ph ^= 1u; }
     }
+    return true;
+}
+__device__ void release_pages(const Cw& c, const SlotInfo& si) {
+    __syncwarp();
+    if (c.lane == 0) {
+        uint32_t slot = uint32_t(si.first_slot);
+        for (int i = 0; i < si.n_pages; ++i) {
+            mbar_arrive(c.sh.empty + slot);
+            if (++slot == uint32_t(c.p.n_pages)) slot = 0;
+        }
+    }
+}
+
+// barrier over the 8 consumer warps; false when the CTA aborted while waiting
+__device__ bool cbar(Cw& c, int pc) {
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(c.sh.cbar);
+    const bool ok = wait_bar(c.p, c.sh, c.sh.cbar, c.cb_phase & 1u, ROLE_CONSUMER, pc);
+    ++c.cb_phase;
+    __syncwarp();
     return ok;
 }
-__device__ void release_pages(const Cons& c, const SlotInfo& si) {
-    __syncwarp();
-    if (c.lane == 0)
-        for (int i = 0; i < si.n_pages; ++i)
-            mbar_arrive(c.sh.empty + ((uint32_t(si.first_page) + uint32_t(i)) % uint32_t(c.p.n_pages)));
+
+__device__ __forceinline__ void load8(const float* srcf, const uint16_t* srcb, int e0, float* v) {
+    if (srcf) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(srcf + e0));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(srcf + e0 + 4));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(srcb + e0));
+        v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+        v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+    }
 }
 
-// block sum over the 256 consumer threads, same fixed order in every thread
-__device__ float cons_block_sum(const Cons& c, float v) {
-    v = warp_sum(v);
-    if (c.lane == 0) c.sh.normred[c.warp] = v;
-    cons_sync();
-    float s = 0.f;
+// This warp's segment `seg` of the length-K input (lane owns chunks lane + 32 i), optionally
+// RMS-normalised: the sum of squares runs over all segments in a fixed order, so every warp
+// derives the same scale.
+template <int CPL>
+__device__ void load_xw(const Cw& c, float (&xr)[8 * CPL], int K, int nseg, int seg, const float* srcf,
+                        const uint16_t* srcb, const uint16_t* gain) {
+    const int seglen = K / nseg, segch = seglen / 8;
 #pragma unroll
-    for (int w = 0; w < kNumConsumerWarps; ++w) s += c.sh.normred[w];
-    return s;
-}
-
-// loads this thread's x chunks (tid + 256 j) of a length-K input, optionally RMS-normalised
-template <int NCH>
-__device__ void load_x(const Cons& c, float (&xr)[64], int K, const float* srcf, const uint16_t* srcb,
-                       const uint16_t* gain) {
-    const int rowchunks = K / 8;
+    for (int i = 0; i < CPL; ++i) {
+        const int ch = c.lane + 32 * i;
+        if (ch < segch) load8(srcf, srcb, seg * seglen + ch * 8, &xr[8 * i]);
+        else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
+        }
+    }
+    if (!gain) return;
     float ss = 0.f;
+    for (int s = 0; s < nseg; ++s) {
 #pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-        const int ch = c.tid + 256 * j;
-        if (ch < rowchunks) {
-            if (srcf) {
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(srcf) + 2 * ch);
-                const float4 b = __ldcg(reinterpret_cast<const float4*>(srcf) + 2 * ch + 1);
-                xr[j * 8 + 0] = a.x; xr[j * 8 + 1] = a.y; xr[j * 8 + 2] = a.z; xr[j * 8 + 3] = a.w;
-                xr[j * 8 + 4] = b.x; xr[j * 8 + 5] = b.y; xr[j * 8 + 6] = b.z; xr[j * 8 + 7] = b.w;
-            } else {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(srcb) + ch);
-                xr[j * 8 + 0] = bf_lo(v.x); xr[j * 8 + 1] = bf_hi(v.x);
-                xr[j * 8 + 2] = bf_lo(v.y); xr[j * 8 + 3] = bf_hi(v.y);
-                xr[j * 8 + 4] = bf_lo(v.z); xr[j * 8 + 5] = bf_hi(v.z);
-                xr[j * 8 + 6] = bf_lo(v.w); xr[j * 8 + 7] = bf_hi(v.w);
+        for (int i = 0; i < CPL; ++i) {
+            const int ch = c.lane + 32 * i;
+            if (ch < segch) {
+                float v[8];
+                if (s == seg) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = xr[8 * i + e];
+                } else {
+                    load8(srcf, srcb, s * seglen + ch * 8, v);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
             }
+        }
+    }
+    ss = warp_sum(ss);
+    const float scale = rsqrtf(ss / float(K) + c.p.rms_eps);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(xr[j * 8 + e], xr[j * 8 + e], ss);
+    for (int i = 0; i < CPL; ++i) {
+        const int ch = c.lane + 32 * i;
+        if (ch < segch) {
+            const uint4 g = __ldg(reinterpret_cast<const uint4*>(gain + seg * seglen + ch * 8));
+            xr[8 * i + 0] = (xr[8 * i + 0] * scale) * bf_lo(g.x);
+            xr[8 * i + 1] = (xr[8 * i + 1] * scale) * bf_hi(g.x);
+            xr[8 * i + 2] = (xr[8 * i + 2] * scale) * bf_lo(g.y);
+            xr[8 * i + 3] = (xr[8 * i + 3] * scale) * bf_hi(g.y);
+            xr[8 * i + 4] = (xr[8 * i + 4] * scale) * bf_lo(g.z);
+            xr[8 * i + 5] = (xr[8 * i + 5] * scale) * bf_hi(g.z);
+            xr[8 * i + 6] = (xr[8 * i + 6] * scale) * bf_lo(g.w);
+            xr[8 * i + 7] = (xr[8 * i + 7] * scale) * bf_hi(g.w);
+        }
+    }
+}
+
+// One input vector per CTA: warp 0 reads x (K <= kXBuf elements) from L2 once, computes the RMS
+// scale, and publishes both in shared memory; every warp then takes its chunks (lane + 32 i).
+// Cuts the L2 reads of a vector all 152 CTAs want at the same moment eightfold.  Every warp runs
+// this at every change of input (the key sequence is the same in all warps).
+template <int CPL>
+__device__ bool shared_x(Cw& c, float (&xr)[8 * CPL], int K, const float* srcf, const uint16_t* srcb,
+                         const uint16_t* gain, int pc) {
+    const int segch = K / 8;
+    if (c.warp == 0) {
+        if (c.xphase > 0 && !wait_bar(c.p, c.sh, c.sh.xfree, (c.xphase - 1u) & 1u, ROLE_CONSUMER, pc)) return false;
+        float ss = 0.f;
+        for (int ch = c.lane; ch < segch; ch += 32) {
+            float v[8];
+            load8(srcf, srcb, ch * 8, v);
+            *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+        }
+        ss = warp_sum(ss);
+        if (c.lane == 0) c.sh.red[41] = gain ? rsqrtf(ss / float(K) + c.p.rms_eps) : 1.0f;
+        __syncwarp();
+        if (c.lane == 0) mbar_arrive(c.sh.xfull);
+    }
+    if (!wait_bar(c.p, c.sh, c.sh.xfull, c.xphase & 1u, ROLE_CONSUMER, pc)) return false;
+    const float scale = c.sh.red[41];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int ch = c.lane + 32 * i;
+        if (ch < segch) {
+            const float4 a = *reinterpret_cast<const float4*>(c.sh.xbuf + ch * 8);
+            const float4 b = *reinterpret_cast<const float4*>(c.sh.xbuf + ch * 8 + 4);
+            float* x = &xr[8 * i];
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+            if (gain) {
+                const uint4 g = __ldg(reinterpret_cast<const uint4*>(gain + ch * 8));
+                x[0] = (x[0] * scale) * bf_lo(g.x); x[1] = (x[1] * scale) * bf_hi(g.x);
+                x[2] = (x[2] * scale) * bf_lo(g.y); x[3] = (x[3] * scale) * bf_hi(g.y);
+                x[4] = (x[4] * scale) * bf_lo(g.z); x[5] = (x[5] * scale) * bf_hi(g.z);
+                x[6] = (x[6] * scale) * bf_lo(g.w); x[7] = (x[7] * scale) * bf_hi(g.w);
+            }
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xr[j * 8 + e] = 0.f;
+            for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
         }
     }
-    if (gain) {
-        const float tot = cons_block_sum(c, ss);
-        const float scale = rsqrtf(tot / float(K) + c.p.rms_eps);
-#pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-            const int ch = c.tid + 256 * j;
-            if (ch < rowchunks) {
-                const uint4 g = __ldg(reinterpret_cast<const uint4*>(gain) + ch);
-                xr[j * 8 + 0] = (xr[j * 8 + 0] * scale) * bf_lo(g.x);
-                xr[j * 8 + 1] = (xr[j * 8 + 1] * scale) * bf_hi(g.x);
-                xr[j * 8 + 2] = (xr[j * 8 + 2] * scale) * bf_lo(g.y);
-                xr[j * 8 + 3] = (xr[j * 8 + 3] * scale) * bf_hi(g.y);
-                xr[j * 8 + 4] = (xr[j * 8 + 4] * scale) * bf_lo(g.z);
-                xr[j * 8 + 5] = (xr[j * 8 + 5] * scale) * bf_hi(g.z);
-                xr[j * 8 + 6] = (xr[j * 8 + 6] * scale) * bf_lo(g.w);
-                xr[j * 8 + 7] = (xr[j * 8 + 7] * scale) * bf_hi(g.w);
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(c.sh.xfree);
+    ++c.xphase;
+    return true;
+}
+
+// output of one matvec row (run by one lane); `half` tells the two row units a warp carries apart
+__device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int b, int ru, int half, float s0, float s1) {
+    const Params& p = c.p;
+    const int op = si.w[W_OP], l = si.w[W_LAYER], a0 = si.w[W_A0];
+    const size_t lb = size_t(l) * p.B + b;
+    const int row = a0 + ru;
+    switch (op) {
+        case OP_QKV: p.qkv[lb * p.nqkv + row] = s0; break;
+        case OP_OPROJ: {
+            const float res = (l == 0) ? bf16f(p.embed[size_t(p.tok[b]) * p.H + row]) : __ldcg(p.x_out + (lb - p.B) * p.H + row);
+            p.x_attn[lb * p.H + row] = res + s0;
+            break;
+        }
+        case OP_UPGATE: p.h[lb * p.F + row] = s0 / (1.0f + expf(-s0)) * s1; break;
+        case OP_DOWN: p.x_out[lb * p.H + row] = __ldcg(p.x_attn + lb * p.H + row) + s0; break;
+        default: {   // LM head: logit, then this warp half's running (max, lowest index) for the argmax
+            p.logits[size_t(b) * p.V + row] = s0;
+            const int slot = (c.warp * 2 + half) * kMaxBatch + b;
+            float2 best = c.sh.lmbest[slot];
+            if (s0 > best.x || (s0 == best.x && row < __float_as_int(best.y))) {
+                best = make_float2(s0, __int_as_float(row));
+                c.sh.lmbest[slot] = best;
             }
+            p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * (2 * kNumConsumerWarps) + c.warp * 2 + half] =
+                make_int4(__float_as_int(best.x), __float_as_int(best.y), int(p.epoch), 0);
+            break;
         }
     }
 }
 
-// Matvec tile: rows of a row-major bf16 matrix (the stream in the leased pages) times the
-// thread-distributed input x.  Thread t owns the 16-byte column chunks t, t+256, ... of every
-// row, so x stays in registers across rows and across consecutive tiles with the same input.
-// Row sums: per-thread partials -> an 8-row butterfly inside the warp -> fixed-order sum over
-// the 8 warps.  The order depends only on K, never on the tile or the SM.
-template <int NCH>
-__device__ void matvec_tile(Cons& c, const SlotInfo& si, int pc, float (&xr)[64], int& xkey) {
-    const Params& p = c.p;
-    const int op = si.w[W_OP], l = si.w[W_LAYER], a0 = si.w[W_A0], n = si.w[W_A1];
-    int K, nrows;
-    switch (op) {
-        case OP_QKV: K = p.H; nrows = n; break;
-        case OP_OPROJ: K = p.qd; nrows = n; break;
-        case OP_UPGATE: K = p.H; nrows = 2 * n; break;
-        case OP_DOWN: K = p.F; nrows = n; break;
-        default: K = p.H; nrows = n; break;   // LM head
+// row unit u's sum is done: emit it, or (split rows) leave this segment's partial and let the
+// last-arriving segment warp add the partials in segment order and emit the row
+__device__ void mv_finish(const Cw& c, const SlotInfo& si, int pc, int b, int u, int half, float s0, float s1) {
+    const bool pair = si.w[W_OP] == OP_UPGATE;
+    if (!si.split) {
+        mv_epilogue(c, si, b, u, half, s0, s1);
+        return;
     }
-    const int rowchunks = K / 8;
-    const uint32_t rowbytes = uint32_t(K) * 2u;
-    const uint32_t first_slot = uint32_t(si.first_page) % uint32_t(p.n_pages);
-    const bool pages_ok = wait_pages(c, si, pc);
-    (void)pages_ok;   // a failed wait already set the abort flag; the loop exits at the next barrier
+    const int nseg = si.nseg, seg = u & (nseg - 1), ru = u >> si.lognseg;
+    const int slot = pc % kSlots;
+    float* part = c.sh.comb + slot * kCombStride;
+    if (pair) { part[(ru * nseg + seg) * 2] = s0; part[(ru * nseg + seg) * 2 + 1] = s1; }
+    else part[ru * nseg + seg] = s0;
+    __threadfence_block();
+    if (atomicAdd(c.sh.combcnt + slot * kMaxRows + ru, 1) == nseg - 1) {
+        __threadfence_block();
+        float u0 = 0.f, u1 = 0.f;
+        for (int s = 0; s < nseg; ++s) {
+            if (pair) { u0 += part[(ru * nseg + s) * 2]; u1 += part[(ru * nseg + s) * 2 + 1]; }
+            else u0 += part[ru * nseg + s];
+        }
+        c.sh.combcnt[slot * kMaxRows + ru] = 0;
+        mv_epilogue(c, si, b, ru, half, u0, u1);
+    }
+}
+
+// two row segments (stream offsets o0, o1) dotted with x at once: 2*CPL independent 16-byte loads
+// per lane, then one butterfly that leaves the first sum in lanes 0-15 and the second in lanes
+// 16-31 (each bit-identical to a plain xor butterfly of that sum).
+template <int CPL>
+__device__ __forceinline__ float seg_dot2(const Cw& c, const SlotInfo& si, uint32_t o0, uint32_t o1, bool has1,
+                                          const float (&xr)[8 * CPL]) {
+    const int segch = si.segch;
+    const uint32_t first = uint32_t(si.first_slot), sb = si.segbytes;
+    const bool p0 = (o0 >> c.p.page_shift) == ((o0 + sb - 1u) >> c.p.page_shift);
+    const bool p1 = (o1 >> c.p.page_shift) == ((o1 + sb - 1u) >> c.p.page_shift);
+    const uint8_t* b0 = ring_ptr(c.sh, c.p, first, o0) + c.lane * 16;
+    const uint8_t* b1 = ring_ptr(c.sh, c.p, first, o1) + c.lane * 16;
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+    if (p0 && p1 && segch == 32 * CPL) {   // whole segments inside one page each: plain strided loads
+        if (has1) {
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                const uint4 w0 = *reinterpret_cast<const uint4*>(b0 + i * 512);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(b1 + i * 512);
+                a[i & 3] = dot8(w0, &xr[8 * i], a[i & 3]);
+                e[i & 3] = dot8(w1, &xr[8 * i], e[i & 3]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) a[i & 3] = dot8(*reinterpret_cast<const uint4*>(b0 + i * 512), &xr[8 * i], a[i & 3]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            const int ch = c.lane + 32 * i;
+            const bool ok = ch < segch;
+            const uint4 w0 = ok ? *reinterpret_cast<const uint4*>(p0 ? b0 + i * 512 : ring_ptr(c.sh, c.p, first, o0 + uint32_t(ch) * 16u))
+                                : make_uint4(0, 0, 0, 0);
+            const uint4 w1 = (ok && has1) ? *reinterpret_cast<const uint4*>(p1 ? b1 + i * 512 : ring_ptr(c.sh, c.p, first, o1 + uint32_t(ch) * 16u))
+                                          : make_uint4(0, 0, 0, 0);
+            a[i & 3] = dot8(w0, &xr[8 * i], a[i & 3]);
+            e[i & 3] = dot8(w1, &xr[8 * i], e[i & 3]);
+        }
+    }
+    const float s0 = (a[0] + a[1]) + (a[2] + a[3]);
+    const float s1 = (e[0] + e[1]) + (e[2] + e[3]);
+    const bool hi = c.lane & 16;
+    float v = (hi ? s1 : s0) + __shfl_xor_sync(0xFFFFFFFFu, hi ? s0 : s1, 16);
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Matvec tile (QKV / O / gate-up / down / LM-head rows).  Unit u of the tile (a row, a gate/up
+// pair, or a row segment) goes to warp (u + rot) mod 8, where rot rotates with every tile so
+// short tiles spread over all warps; a warp handles its units two row segments at a time.
+template <int CPL>
+__device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc, float (&xr)[8 * CPL], int& xkey) {
+    const Params& p = c.p;
+    const int op = si.w[W_OP], l = si.w[W_LAYER], n = si.w[W_A1];
+    const bool pair = op == OP_UPGATE;
+    const int U = si.units, nseg = si.nseg;
+    const uint32_t rowbytes = si.rowbytes, segbytes = si.segbytes;
+    if (!wait_pages(c, si, pc)) return false;
+    if (c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
+    const int ufirst = (c.warp - int(c.rot)) & 7;
     for (int b = 0; b < p.B; ++b) {
-        // ---- input vector (cached across tiles with the same key) ----
         const float* srcf = nullptr;
         const uint16_t* srcb = nullptr;
         const uint16_t* gain = nullptr;
         const size_t lb = size_t(l) * p.B + b;
         switch (op) {
             case OP_QKV:
-                gain = p.layers[l].attn_norm;
+                gain = c.sh.layers[l].attn_norm;
                 if (l == 0) srcb = p.embed + size_t(p.tok[b]) * p.H;
                 else srcf = p.x_out + (lb - p.B) * p.H;
                 break;
             case OP_OPROJ: srcf = p.o + lb * p.qd; break;
-            case OP_UPGATE: gain = p.layers[l].mlp_norm; srcf = p.x_attn + lb * p.H; break;
+            case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; srcf = p.x_attn + lb * p.H; break;
             case OP_DOWN: srcf = p.h + lb * p.F; break;
             default: gain = p.final_norm; srcf = p.x_out + (size_t(p.L - 1) * p.B + b) * p.H; break;
         }
-        const int key = ((op * 64 + (l & 63)) * kMaxBatch + b) + 1;
-        if (key != xkey) {
-            load_x<NCH>(c, xr, K, srcf, srcb, gain);
-            xkey = key;
+        if (nseg == 1 && si.K <= kXBuf) {   // every warp, even one without units in this tile
+            const int key = (((op * 64 + (l & 63)) * kMaxBatch + b) * 8) + 1;
+            if (key != xkey) {
+                if (!shared_x<CPL>(c, xr, si.K, srcf, srcb, gain, pc)) return false;
+                xkey = key;
+            }
         }
-        // ---- accumulate ----
-        float acc[kMaxRows];
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
-            acc[r] = 0.f;
-            if (r < nrows) {
-#pragma unroll
-                for (int j = 0; j < NCH; ++j) {
-                    const int ch = c.tid + 256 * j;
-                    if (ch < rowchunks) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(
-                            ring_ptr(c.sh, p, first_slot, uint32_t(r) * rowbytes + uint32_t(ch) * 16u));
-                        acc[r] = dot8(v, &xr[j * 8], acc[r]);
-                    }
+        // (a gate/up pair is already two row segments: one unit per step; otherwise units u, u+8)
+        for (int u = ufirst; u < U; u += pair ? 8 : 16) {
+            const int u1 = u + 8;
+            const bool two = !pair && u1 < U;
+            const int s_lo = si.split ? (u & (nseg - 1)) : 0;
+            const int s_hi = si.split ? s_lo + 1 : nseg;
+            float t0 = 0.f, t1 = 0.f;
+            for (int s = s_lo; s < s_hi; ++s) {
+                const int key = (((op * 64 + (l & 63)) * kMaxBatch + b) * 8 + s) + 1;
+                if (key != xkey) {
+                    load_xw<CPL>(c, xr, si.K, nseg, s, srcf, srcb, gain);
+                    xkey = key;
                 }
+                const int r0 = si.split ? (u >> si.lognseg) : u;
+                const uint32_t off0 = uint32_t(r0) * rowbytes + uint32_t(s) * segbytes;
+                uint32_t off1;
+                if (pair) off1 = off0 + uint32_t(n) * rowbytes;                 // the up row of the pair
+                else off1 = uint32_t(si.split ? (u1 >> si.lognseg) : u1) * rowbytes + uint32_t(s) * segbytes;
+                const float v = seg_dot2<CPL>(c, si, off0, off1, pair || two, xr);
+                // lanes 0-15 hold the first sum, lanes 16-31 the second
+                t0 += __shfl_sync(0xFFFFFFFFu, v, 0);
+                t1 += __shfl_sync(0xFFFFFFFFu, v, 16);
             }
-        }
-        if (b == p.B - 1) release_pages(c, si);
-        // ---- 8-row butterfly: lane ends with the warp sum of row (lane >> 2) & 7 ----
-        {
-            const bool b4 = (c.lane >> 4) & 1, b3 = (c.lane >> 3) & 1, b2 = (c.lane >> 2) & 1;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float send = b4 ? acc[i] : acc[i + 4];
-                const float keep = b4 ? acc[i + 4] : acc[i];
-                acc[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+            if (pair) {
+                if (c.lane == 0) mv_finish(c, si, pc, b, u, 0, t0, t1);
+            } else {
+                if (c.lane == 0) mv_finish(c, si, pc, b, u, 0, t0, 0.f);
+                if (two && c.lane == 16) mv_finish(c, si, pc, b, u1, 1, t1, 0.f);
             }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float send = b3 ? acc[i] : acc[i + 2];
-                const float keep = b3 ? acc[i + 2] : acc[i];
-                acc[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
-            }
-            {
-                const float send = b2 ? acc[0] : acc[1];
-                const float keep = b2 ? acc[1] : acc[0];
-                acc[0] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
-            }
-            acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], 2);
-            acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], 1);
-        }
-        float* red = c.sh.red + c.rbuf * (kNumConsumerWarps * kMaxRows);
-        if ((c.lane & 3) == 0) red[c.warp * kMaxRows + ((c.lane >> 2) & 7)] = acc[0];
-        cons_sync();
-        c.rbuf ^= 1;
-        auto rowsum = [&](int r) {
-            float s = 0.f;
-#pragma unroll
-            for (int w = 0; w < kNumConsumerWarps; ++w) s += red[w * kMaxRows + r];
-            return s;
-        };
-        // ---- epilogue (warp 0) ----
-        if (c.warp == 0) {
-            const int r = c.lane;
-            switch (op) {
-                case OP_QKV:
-                    if (r < n) p.qkv[lb * p.nqkv + a0 + r] = rowsum(r);
-                    break;
-                case OP_OPROJ:
-                    if (r < n) {
-                        const int row = a0 + r;
-                        const float res = (l == 0) ? bf16f(p.embed[size_t(p.tok[b]) * p.H + row])
-                                                   : __ldcg(p.x_out + (lb - p.B) * p.H + row);
-                        p.x_attn[lb * p.H + row] = res + rowsum(r);
-                    }
-                    break;
-                case OP_UPGATE:
-                    if (r < n) {
-                        const float gt = rowsum(r), up = rowsum(n + r);
-                        p.h[lb * p.F + a0 + r] = gt / (1.0f + expf(-gt)) * up;
-                    }
-                    break;
-                case OP_DOWN:
-                    if (r < n) {
-                        const int row = a0 + r;
-                        p.x_out[lb * p.H + row] = __ldcg(p.x_attn + lb * p.H + row) + rowsum(r);
-                    }
-                    break;
-                default: {   // LM head
-                    if (r < n) p.logits[size_t(b) * p.V + a0 + r] = rowsum(r);
-                    if (r == 0) {
-                        float best = rowsum(0);
-                        int bi = 0;
-                        for (int k = 1; k < n; ++k) {
-                            const float v = rowsum(k);
-                            if (v > best) { best = v; bi = k; }
-                        }
-                        p.lm_part[size_t(b) * p.n_lm + si.w[W_A2]] = make_float2(best, __int_as_float(a0 + bi));
-                    }
-                    break;
-                }
-            }
+            __syncwarp();
         }
     }
+    if (c.warp == 0 && c.lane == 0) stamp(p, pc, 7);
+    c.rot = (c.rot + uint32_t(U)) & 7u;
+    release_pages(c, si);
+    return true;
 }
 
 // Split-K decode attention over one chunk of KV positions for one (sequence, KV group); the
 // chunk that holds pos also applies RoPE to the new k, rounds k and v to bf16 and appends them
-// to the cache.  Writes the chunk partial (o[d] unnormalised, m, l) for each query head.
-__device__ void attn_tile(Cons& c, const SlotInfo& si, int pc) {
+// to the cache.  Writes the chunk partial (o[d] unnormalised, m, l) for each query head, then
+// arrives on the group's arrival counter; the tile that arrives last combines the group's
+// partials (fixed chunk order) into o and alone fires the completion the O projection waits on.
+__device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     const Params& p = c.p;
     const int l = si.w[W_LAYER], b = si.w[W_B], g = si.w[W_A0], ch = si.w[W_A1], C = si.w[W_A2];
     const int d = p.d, half = d / 2, hpg = p.hpg;
+    const int tid = c.warp * 32 + c.lane;
     const int n_old = attn_old_rows(p, b, ch, C);
-    if (n_old < 0) return;   // chunk past pos: no work, no pages
-    const int pos = p.pos[b];
-    const bool has_new = pos < ch * C + C;
-    const int n = n_old + (has_new ? 1 : 0);
     const size_t lb = size_t(l) * p.B + b;
     const float* qkv = p.qkv + lb * p.nqkv;
-    const float2* rp = p.rope + size_t(pos) * half;
-    // 1. rotate q of the group's heads; RoPE k, round k and v, append them
-    for (int idx = c.tid; idx < hpg * half; idx += kConsumerThreads) {
-        const int h = idx / half, i = idx % half;
-        const float* qh = qkv + size_t(g * hpg + h) * d;
-        const float q0 = __ldcg(qh + i), q1 = __ldcg(qh + i + half);
-        const float2 cs = rp[i];
-        c.sh.qrot[h * d + i] = q0 * cs.x - q1 * cs.y;
-        c.sh.qrot[h * d + i + half] = q0 * cs.y + q1 * cs.x;
-    }
-    if (has_new) {
-        const size_t cache = size_t(b) * p.kv_bstride + size_t(l) * p.kv_lstride + size_t(g) * p.kv_hstride +
-                             size_t(pos) * d;
-        for (int i = c.tid; i < half; i += kConsumerThreads) {
-            const float* kh = qkv + p.qd + size_t(g) * d;
-            const float k0 = __ldcg(kh + i), k1 = __ldcg(kh + i + half);
+    float* sc = c.sh.ascr;   // [hpg][C] scores, then [hpg][n_chunk] combine factors
+    if (n_old >= 0) {
+        const int pos = p.pos[b];
+        const bool has_new = pos < ch * C + C;
+        const int n = n_old + (has_new ? 1 : 0);
+        const float2* rp = p.rope + size_t(pos) * half;
+        if (!cbar(c, pc)) return false;   // the previous block-level body is done with the scratch
+        // 1. rotate q of the group's heads; RoPE k, round k and v, append them
+        for (int idx = tid; idx < hpg * half; idx += kConsumerThreads) {
+            const int h = idx / half, i = idx % half;
+            const float* qh = qkv + size_t(g * hpg + h) * d;
+            const float q0 = __ldcg(qh + i), q1 = __ldcg(qh + i + half);
             const float2 cs = rp[i];
-            const uint16_t r0 = f2bf_rn(k0 * cs.x - k1 * cs.y), r1 = f2bf_rn(k0 * cs.y + k1 * cs.x);
-            c.sh.knew[i] = r0;
-            c.sh.knew[i + half] = r1;
-            p.kc[cache + i] = r0;
-            p.kc[cache + i + half] = r1;
+            c.sh.qrot[h * d + i] = q0 * cs.x - q1 * cs.y;
+            c.sh.qrot[h * d + i + half] = q0 * cs.y + q1 * cs.x;
         }
-        for (int i = c.tid; i < d; i += kConsumerThreads) {
-            const uint16_t r = f2bf_rn(__ldcg(qkv + p.qd + p.kvd + size_t(g) * d + i));
-            c.sh.vnew[i] = r;
-            p.vc[cache + i] = r;
+        if (has_new) {
+            const size_t cache = size_t(b) * p.kv_bstride + size_t(l) * p.kv_lstride + size_t(g) * p.kv_hstride +
+                                 size_t(pos) * d;
+            for (int i = tid; i < half; i += kConsumerThreads) {
+                const float* kh = qkv + p.qd + size_t(g) * d;
+                const float k0 = __ldcg(kh + i), k1 = __ldcg(kh + i + half);
+                const float2 cs = rp[i];
+                const uint16_t r0 = f2bf_rn(k0 * cs.x - k1 * cs.y), r1 = f2bf_rn(k0 * cs.y + k1 * cs.x);
+                c.sh.knew[i] = r0;
+                c.sh.knew[i + half] = r1;
+                p.kc[cache + i] = r0;
+                p.kc[cache + i + half] = r1;
+            }
+            for (int i = tid; i < d; i += kConsumerThreads) {
+                const uint16_t r = f2bf_rn(__ldcg(qkv + p.qd + p.kvd + size_t(g) * d + i));
+                c.sh.vnew[i] = r;
+                p.vc[cache + i] = r;
+            }
         }
-    }
-    cons_sync();
-    wait_pages(c, si, pc);
-    const uint32_t first_slot = uint32_t(si.first_page) % uint32_t(p.n_pages);
-    const uint32_t rowb = uint32_t(d) * 2u;
-    const uint32_t voff = uint32_t(n_old) * rowb;
-    float* sc = c.sh.ascr;   // [hpg][C]
-    // 2. scores s[h][t] = (q_h . k_t) * scale; d/8 consecutive lanes share a position
-    const int cpr = d / 8;
-    for (int base = 0; base < n * cpr; base += kConsumerThreads) {
-        const int idx = base + c.tid;
-        const bool valid = idx < n * cpr;
-        const int t = idx / cpr, j = idx % cpr;
-        float part[kMaxHpg];
+        if (!wait_pages(c, si, pc)) return false;
+        if (!cbar(c, pc)) return false;
+        const uint32_t first_slot = uint32_t(si.first_slot);
+        const uint32_t rowb = uint32_t(d) * 2u;
+        const uint32_t voff = uint32_t(n_old) * rowb;
+        const uint32_t kbytes = voff;
+        // the K block and the V block each sit inside one page (the common case): direct pointers
+        const bool k1p = n_old == 0 || (0u >> p.page_shift) == ((kbytes - 1u) >> p.page_shift);
+        const bool v1p = n_old == 0 || (voff >> p.page_shift) == ((voff + kbytes - 1u) >> p.page_shift);
+        const uint8_t* kbase = ring_ptr(c.sh, p, first_slot, 0u);
+        const uint8_t* vbase = ring_ptr(c.sh, p, first_slot, voff);
+        // 2. scores s[h][t] = (q_h . k_t) * scale; d/8 consecutive lanes share a position
+        const int cpr = d / 8;
+        for (int base = 0; base < n * cpr; base += kConsumerThreads) {
+            const int idx = base + tid;
+            const bool valid = idx < n * cpr;
+            const int t = idx / cpr, j = idx % cpr;
+            float part[kMaxHpg];
 #pragma unroll
-        for (int h = 0; h < kMaxHpg; ++h) part[h] = 0.f;
-        if (valid) {
-            const uint4 kv = (t < n_old) ? *reinterpret_cast<const uint4*>(ring_ptr(c.sh, p, first_slot, uint32_t(t) * rowb + uint32_t(j) * 16u))
-                                         : *reinterpret_cast<const uint4*>(c.sh.knew + j * 8);
+            for (int h = 0; h < kMaxHpg; ++h) part[h] = 0.f;
+            if (valid) {
+                const uint32_t off = uint32_t(t) * rowb + uint32_t(j) * 16u;
+                const uint4 kv = (t < n_old) ? *reinterpret_cast<const uint4*>(k1p ? kbase + off : ring_ptr(c.sh, p, first_slot, off))
+                                             : *reinterpret_cast<const uint4*>(c.sh.knew + j * 8);
 #pragma unroll
-            for (int h = 0; h < kMaxHpg; ++h)
-                if (h < hpg) part[h] = dot8(kv, c.sh.qrot + h * d + j * 8, 0.f);
-        }
-        for (int o = 1; o < cpr; o <<= 1)
+                for (int h = 0; h < kMaxHpg; ++h)
+                    if (h < hpg) part[h] = dot8(kv, c.sh.qrot + h * d + j * 8, 0.f);
+            }
+            for (int o = 1; o < cpr; o <<= 1)
 #pragma unroll
-            for (int h = 0; h < kMaxHpg; ++h) part[h] += __shfl_xor_sync(0xFFFFFFFFu, part[h], o);
-        if (valid && j == 0)
+                for (int h = 0; h < kMaxHpg; ++h)
+                    if (h < hpg) part[h] += __shfl_xor_sync(0xFFFFFFFFu, part[h], o);
+            if (valid && j == 0)
 #pragma unroll
-            for (int h = 0; h < kMaxHpg; ++h)
-                if (h < hpg) sc[h * C + t] = part[h] * p.attn_scale;
-    }
-    cons_sync();
-    // 3. softmax pieces per head (warp h): m, w_t = exp(s_t - m), l = sum w_t
-    if (c.warp < hpg) {
-        const int h = c.warp;
-        float m = -INFINITY;
-        for (int t = c.lane; t < n; t += 32) m = fmaxf(m, sc[h * C + t]);
-        m = warp_max(m);
-        float s = 0.f;
-        for (int t = c.lane; t < n; t += 32) {
-            const float e = expf(sc[h * C + t] - m);
-            sc[h * C + t] = e;
-            s += e;
+                for (int h = 0; h < kMaxHpg; ++h)
+                    if (h < hpg) sc[h * C + t] = part[h] * p.attn_scale;
         }
-        s = warp_sum(s);
-        if (c.lane == 0) { c.sh.ml[2 * h] = m; c.sh.ml[2 * h + 1] = s; }
-    }
-    cons_sync();
-    // 4. o[h][e] = sum_t w_t v_t[e]
-    float* dst = p.part + ((lb * p.nkv + g) * p.n_chunk + ch) * size_t(hpg) * (d + 2);
-    for (int idx = c.tid; idx < hpg * d; idx += kConsumerThreads) {
-        const int h = idx / d, e = idx % d;
-        float acc = 0.f;
-        for (int t = 0; t < n; ++t) {
-            const float v = (t < n_old) ? bf16f(*reinterpret_cast<const uint16_t*>(ring_ptr(c.sh, p, first_slot, voff + uint32_t(t) * rowb + uint32_t(e) * 2u)))
-                                        : bf16f(c.sh.vnew[e]);
-            acc = fmaf(sc[h * C + t], v, acc);
+        if (!cbar(c, pc)) return false;
+        // 3. softmax pieces per head (warp h): m, w_t = exp(s_t - m), l = sum w_t
+        if (c.warp < hpg) {
+            const int h = c.warp;
+            float m = -INFINITY;
+            for (int t = c.lane; t < n; t += 32) m = fmaxf(m, sc[h * C + t]);
+            m = warp_max(m);
+            float s = 0.f;
+            for (int t = c.lane; t < n; t += 32) {
+                const float e = expf(sc[h * C + t] - m);
+                sc[h * C + t] = e;
+                s += e;
+            }
+            s = warp_sum(s);
+            if (c.lane == 0) { c.sh.ml[2 * h] = m; c.sh.ml[2 * h + 1] = s; }
         }
-        float* dh = dst + size_t(h) * (d + 2);
-        dh[e] = acc;
-        if (e == 0) { dh[d] = c.sh.ml[2 * h]; dh[d + 1] = c.sh.ml[2 * h + 1]; }
+        if (!cbar(c, pc)) return false;
+        // 4. o[h][e] = sum_t w_t v_t[e]
+        float* dst = p.part + ((lb * p.nkv + g) * p.n_chunk + ch) * size_t(hpg) * (d + 2);
+        for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
+            const int h = idx / d, e = idx % d;
+            const float* wts = sc + h * C;
+            float acc = 0.f;
+            if (v1p) {
+                const uint16_t* vcol = reinterpret_cast<const uint16_t*>(vbase) + e;
+                for (int t = 0; t < n_old; ++t) acc = fmaf(wts[t], bf16f(vcol[t * d]), acc);
+            } else {
+                for (int t = 0; t < n_old; ++t)
+                    acc = fmaf(wts[t], bf16f(*reinterpret_cast<const uint16_t*>(ring_ptr(c.sh, p, first_slot, voff + uint32_t(t) * rowb + uint32_t(e) * 2u))), acc);
+            }
+            if (has_new) acc = fmaf(wts[n_old], bf16f(c.sh.vnew[e]), acc);
+            float* dh = dst + size_t(h) * (d + 2);
+            dh[e] = acc;
+            if (e == 0) { dh[d] = c.sh.ml[2 * h]; dh[d + 1] = c.sh.ml[2 * h + 1]; }
+        }
+        release_pages(c, si);
     }
-    release_pages(c, si);
-}
-
-// Fixed-order log-sum-exp combine of the active chunks of one (sequence, group):
-// M = max_c m_c, f_c = exp(m_c - M), L = sum_c f_c l_c, o = sum_c f_c o_c / L.
-__device__ void comb_tile(Cons& c, const SlotInfo& si) {
-    const Params& p = c.p;
-    const int l = si.w[W_LAYER], b = si.w[W_B], g = si.w[W_A0], nch = si.w[W_A1], C = si.w[W_A2];
-    const int d = p.d, hpg = p.hpg;
-    const int nact = min(nch, p.pos[b] / C + 1);
-    const size_t lb = size_t(l) * p.B + b;
-    const float* base = p.part + (lb * p.nkv + g) * size_t(p.n_chunk) * hpg * (d + 2);
-    float* fac = c.sh.ascr;   // [hpg][n_chunk]
+    // 5. arrive on the group; the last arrival combines M = max_c m_c, f_c = exp(m_c - M),
+    //    L = sum_c f_c l_c, o = sum_c f_c o_c / L over the active chunks, in chunk order
+    if (!cbar(c, pc)) return false;   // every thread's partial is written (CTA scope) before the release
+    if (tid == 0) {
+        const uint32_t nch = uint32_t(si.w[W_ARRIVE_N]);
+        const uint32_t old = atom_add_acq_rel_gpu(p.counters + si.w[W_ARRIVE], 1u);
+        const bool last = old - p.epoch * nch == nch - 1u;
+        reinterpret_cast<volatile int*>(c.sh.red)[40] = last ? 1 : 0;
+        if (last) c.sh.pubinfo[(pc % kDone) * 8 + 7] = 1;   // fire this tile's completion
+    }
+    if (!cbar(c, pc)) return false;
+    if (!reinterpret_cast<volatile int*>(c.sh.red)[40]) return true;
+    const int nact = min(p.n_chunk, p.pos[b] / C + 1);
+    const float* pbase = p.part + (lb * p.nkv + g) * size_t(p.n_chunk) * hpg * (d + 2);
     if (c.warp < hpg) {
         const int h = c.warp;
         float M = -INFINITY;
-        for (int k = c.lane; k < nact; k += 32) M = fmaxf(M, __ldcg(base + (size_t(k) * hpg + h) * (d + 2) + d));
+        for (int k = c.lane; k < nact; k += 32) M = fmaxf(M, __ldcg(pbase + (size_t(k) * hpg + h) * (d + 2) + d));
         M = warp_max(M);
         float Ls = 0.f;
         for (int k = c.lane; k < nact; k += 32) {
-            const float* ph = base + (size_t(k) * hpg + h) * (d + 2);
+            const float* ph = pbase + (size_t(k) * hpg + h) * (d + 2);
             const float f = expf(__ldcg(ph + d) - M);
-            fac[h * p.n_chunk + k] = f;
+            sc[h * p.n_chunk + k] = f;
             Ls = fmaf(f, __ldcg(ph + d + 1), Ls);
         }
         Ls = warp_sum(Ls);
         if (c.lane == 0) c.sh.cml[h] = Ls;
     }
-    cons_sync();
+    if (!cbar(c, pc)) return false;
     float* out = p.o + lb * p.qd + size_t(g) * hpg * d;
-    for (int idx = c.tid; idx < hpg * d; idx += kConsumerThreads) {
+    for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
         const int h = idx / d, e = idx % d;
         float acc = 0.f;
-        for (int k = 0; k < nact; ++k) acc = fmaf(fac[h * p.n_chunk + k], __ldcg(base + (size_t(k) * hpg + h) * (d + 2) + e), acc);
+        for (int k = 0; k < nact; ++k) acc = fmaf(sc[h * p.n_chunk + k], __ldcg(pbase + (size_t(k) * hpg + h) * (d + 2) + e), acc);
         out[idx] = acc / c.sh.cml[h];
     }
+    return true;
 }
 
 // Greedy token: argmax over the LM-head tile partials (largest value, lowest index on ties).
-__device__ void argmax_tile(Cons& c, const SlotInfo& si) {
+__device__ bool argmax_tile(Cw& c, const SlotInfo& si, int pc) {
     const Params& p = c.p;
-    const int b = si.w[W_B], n = si.w[W_A1];
-    const float2* parts = p.lm_part + size_t(b) * p.n_lm;
+    const int b = si.w[W_B];
+    const int tid = c.warp * 32 + c.lane;
+    const int n = int(gridDim.x) * kNumConsumerWarps * 2;   // one running partial per (CTA, warp half)
+    const int4* parts = p.lm_part + size_t(b) * n;
     float bv = -INFINITY;
     int bi = 0x7FFFFFFF;
-    for (int i = c.tid; i < n; i += kConsumerThreads) {
-        const float2 v = __ldcg(parts + i);
-        const int idx = __float_as_int(v.y);
-        if (v.x > bv || (v.x == bv && idx < bi)) { bv = v.x; bi = idx; }
+    for (int i = tid; i < n; i += kConsumerThreads) {
+        const int4 v = __ldcg(parts + i);
+        if (uint32_t(v.z) != p.epoch) continue;   // written in an earlier step: this warp had no LM rows
+        const float val = __int_as_float(v.x);
+        if (val > bv || (val == bv && v.y < bi)) { bv = val; bi = v.y; }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
@@ -759,77 +1009,108 @@ __device__ void argmax_tile(Cons& c, const SlotInfo& si) {
         const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
         if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
     }
-    float* red = c.sh.red + c.rbuf * (kNumConsumerWarps * kMaxRows);
-    if (c.lane == 0) { red[2 * c.warp] = bv; red[2 * c.warp + 1] = __int_as_float(bi); }
-    cons_sync();
-    c.rbuf ^= 1;
-    if (c.tid == 0) {
+    if (!cbar(c, pc)) return false;   // the previous user of the scratch is done
+    if (c.lane == 0) { c.sh.red[2 * c.warp] = bv; c.sh.red[2 * c.warp + 1] = __int_as_float(bi); }
+    if (!cbar(c, pc)) return false;
+    if (tid == 0) {
         for (int w = 0; w < kNumConsumerWarps; ++w) {
-            const float ov = red[2 * w];
-            const int oi = __float_as_int(red[2 * w + 1]);
+            const float ov = c.sh.red[2 * w];
+            const int oi = __float_as_int(c.sh.red[2 * w + 1]);
             if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
         }
         p.tokens_out[b] = bi;
         if (p.next_dev) p.next_dev[b] = bi;
     }
-}
-
-__device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* w, int pc) {
-    const int nw = w[W_NWAIT];
-    for (int i = 0; i < nw; ++i) {
-        const int cid = w[W_WAIT + 2 * i];
-        const uint32_t target = p.epoch * __ldg(p.totals + cid) + uint32_t(w[W_WAIT + 2 * i + 1]);
-        uint32_t v = ld_relaxed_gpu(p.counters + cid);
-        if (int32_t(v - target) >= 0) continue;
-        const uint64_t t0 = globaltimer();
-        while (true) {
-            v = ld_relaxed_gpu(p.counters + cid);
-            if (int32_t(v - target) >= 0) break;
-            if (*reinterpret_cast<volatile int*>(sh.abort) || ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(p.err))) {
-                *reinterpret_cast<volatile int*>(sh.abort) = 1;
-                return false;
-            }
-            if (globaltimer() - t0 > p.timeout_ns) {
-                raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_COUNTER, pc, cid, v, target);
-                return false;
-            }
-        }
-    }
-    fence_acq_rel_gpu();   // acquire: producers' data is visible before any consumer reads it
     return true;
 }
 
-template <int NCH>
-__device__ void consumer_loop(const Params& p, const Shared& sh) {
-    Cons c{p, sh, int(threadIdx.x), int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0};
-    float xr[64];
+// Counters seen satisfied by this warp: counters only grow within a launch, so a wait whose
+// target an earlier observation already covers needs neither a poll nor another acquire fence.
+struct CounterCache {
+    int32_t id[4];
+    int32_t need[4];
+    int next;
+};
+
+__device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* w, int pc, CounterCache& cc) {
+    const int nw = w[W_NWAIT];
+    bool polled = false;
+    for (int i = 0; i < nw; ++i) {
+        const int cid = w[W_WAIT + 2 * i], need = w[W_WAIT + 2 * i + 1];
+        bool known = false;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) known |= (cc.id[k] == cid) && (cc.need[k] == need);
+        if (known) continue;
+        polled = true;
+        const uint32_t target = p.epoch * __ldg(p.totals + cid) + uint32_t(need);
+        uint32_t v = ld_relaxed_gpu(p.counters + cid);
+        if (int32_t(v - target) < 0) {
+            const uint64_t t0 = globaltimer();
+            while (true) {
+                v = ld_relaxed_gpu(p.counters + cid);
+                if (int32_t(v - target) >= 0) break;
+                if (*reinterpret_cast<volatile int*>(sh.abort) ||
+                    ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(p.err))) {
+                    *reinterpret_cast<volatile int*>(sh.abort) = 1;
+                    return false;
+                }
+                if (globaltimer() - t0 > p.timeout_ns) {
+                    raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_COUNTER, pc, cid, v, target);
+                    return false;
+                }
+            }
+        }
+        cc.id[cc.next] = cid;
+        cc.need[cc.next] = need;
+        cc.next = (cc.next + 1) & 3;
+    }
+    if (polled) fence_acquire_gpu();   // acquire: producers' data is visible before this warp reads it
+    return true;
+}
+
+template <int CPL>
+__device__ void consumer_warp(const Params& p, const Shared& sh) {
+    Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u, 0u};
+    float xr[8 * CPL];
     int xkey = -1;
+    CounterCache cc{{-1, -1, -1, -1}, {-1, -1, -1, -1}, 0};
     for (int pc = 0;; ++pc) {
         const int slot = pc % kSlots;
-        bool ok = wait_bar(p, sh, sh.ins_full + slot, (pc / kSlots) & 1, ROLE_CONSUMER, pc);
+        if (!wait_bar(p, sh, sh.ins_full + slot, (pc / kSlots) & 1, ROLE_CONSUMER, pc)) break;
         const SlotInfo& si = sh.slots[slot];
-        const int op = ok ? si.w[W_OP] : OP_END;
-        if (ok && op != OP_END && c.tid == 0) ok = wait_counters(p, sh, si.w, pc);
-        const bool stop = cons_sync_or(!ok || *reinterpret_cast<volatile int*>(sh.abort) != 0);
-        if (stop) break;
-        switch (op) {
-            case OP_QKV:
-            case OP_OPROJ:
-            case OP_UPGATE:
-            case OP_DOWN:
-            case OP_LMHEAD: matvec_tile<NCH>(c, si, pc, xr, xkey); break;
-            case OP_ATTN: attn_tile(c, si, pc); break;
-            case OP_COMB: comb_tile(c, si); break;
-            case OP_ARGMAX: argmax_tile(c, si); break;
-            default: break;   // END
+        const int op = si.w[W_OP];
+        if (op != OP_END) {
+            // the RMSNorm gain of a new input depends on no counter: start fetching it into L1
+            // before waiting, so the normalisation after the wait does not pay a second round trip
+            const uint16_t* gain = op == OP_QKV ? sh.layers[si.w[W_LAYER]].attn_norm
+                                 : op == OP_UPGATE ? sh.layers[si.w[W_LAYER]].mlp_norm
+                                 : op == OP_LMHEAD ? p.final_norm : nullptr;
+            if (gain && c.lane * 64 < p.H * 2)
+                for (int off = c.lane * 64; off < p.H * 2; off += 32 * 64)
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(gain) + off));
+            int ok = 1;
+            if (c.lane == 0) ok = wait_counters(p, sh, si.w, pc, cc);
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+            if (threadIdx.x == 0) stamp(p, pc, 2);
+            bool good;
+            switch (op) {
+                case OP_ATTN: good = attn_tile(c, si, pc); break;
+                case OP_ARGMAX: good = argmax_tile(c, si, pc); break;
+                default: good = matvec_warp<CPL>(c, si, pc, xr, xkey); break;
+            }
+            if (!good) break;
+            if (threadIdx.x == 0) stamp(p, pc, 3);
         }
         __syncwarp();
-        if (c.lane == 0) mbar_arrive(sh.done + slot);
+        if (c.lane == 0) {
+            mbar_arrive(sh.ins_empty + slot);
+            mbar_arrive(sh.done + (pc % kDone));
+        }
         if (op == OP_END) break;
     }
 }
 
-template <int NCH>
+template <int CPL>
 __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Shared sh = carve(smem, p);
@@ -840,15 +1121,27 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
         }
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(sh.ins_full + i, 1);
-            mbar_init(sh.ins_empty + i, 1);
-            mbar_init(sh.done + i, kNumConsumerWarps);
+            mbar_init(sh.ins_empty + i, kNumConsumerWarps);
         }
+        for (int i = 0; i < kDone; ++i) mbar_init(sh.done + i, kNumConsumerWarps);
+        *sh.published = 0;
+        mbar_init(sh.qfull + 0, 1);
+        mbar_init(sh.qfull + 1, 1);
+        mbar_init(sh.cbar, kNumConsumerWarps);
+        mbar_init(sh.xfull, 1);
+        mbar_init(sh.xfree, kNumConsumerWarps);
         *sh.abort = 0;
+        *sh.issued = 0ull;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    for (int i = threadIdx.x; i < kNumConsumerWarps * 2 * kMaxBatch; i += blockDim.x)
+        sh.lmbest[i] = make_float2(-INFINITY, __int_as_float(0x7FFFFFFF));
+    for (int i = threadIdx.x; i < kSlots * kMaxRows; i += blockDim.x) sh.combcnt[i] = 0;
+    for (int i = threadIdx.x; i < p.L; i += blockDim.x) sh.layers[i] = p.layers[i];
+    if (threadIdx.x == 0) stamp(p, 0, 5);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < kNumConsumerWarps) consumer_loop<NCH>(p, sh);
+    if (warp < kNumConsumerWarps) consumer_warp<CPL>(p, sh);
     else if (warp == kLoaderWarp) { if (lane == 0) loader(p, sh); }
     else if (lane == 0) publisher(p, sh);
     cta_sync_divergent();
@@ -865,9 +1158,9 @@ __global__ void rope_table_kernel(float2* out, int max_seq, int d, double theta)
     }
 }
 
-// x chunks per thread: ceil(K / 8 / 256) for the longest matvec row of the model
-static const void* kernel_for(int nch) {
-    switch (nch) {
+// CPL = 16-byte chunks per lane of the longest row segment (segments hold <= 2048 elements)
+static const void* kernel_for(int cpl) {
+    switch (cpl) {
         case 1: return reinterpret_cast<const void*>(&megakernel<1>);
         case 2: return reinterpret_cast<const void*>(&megakernel<2>);
         case 3: return reinterpret_cast<const void*>(&megakernel<3>);
@@ -880,7 +1173,7 @@ static const void* kernel_for(int nch) {
     }
 }
 
-const void* megakernel_fn(int nch) { return kernel_for(nch); }
+const void* megakernel_fn(int cpl) { return kernel_for(cpl); }
 
 cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st) {
     const int n = max_seq * (d / 2);

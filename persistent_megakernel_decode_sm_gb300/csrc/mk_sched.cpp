@@ -12,12 +12,14 @@
 //    combine per (sequence, group), O row tiles, gate/up row-pair tiles, down row tiles; then
 //    LM-head row tiles and one argmax per sequence;
 //  * DAG: a consumer waits on one counter per producer set -- QKV(l) on down(l-1), attention
-//    chunks of group g on the QKV tiles of group g, combine on its chunks, O on all combines,
-//    up/gate on O, down on up/gate, LM head on the last layer's down, argmax on the LM head;
-//  * waves = longest-path level (6 per layer, then LM head, then argmax); the waits of a tile
+//    chunks of group g on the QKV tiles of group g, O on the combined attention of every group,
+//    up/gate on O, down on up/gate, LM head on the last layer's down, argmax on the LM head.
+//    The combine of a group's chunk partials is done by the chunk tile that arrives last on the
+//    group's arrival counter, which alone carries the completion O waits on;
+//  * waves = longest-path level (5 per layer, then LM head, then argmax); the waits of a tile
 //    point only at lower waves (forward-progress contract);
-//  * pools: memory = tiles that stream weights or KV, compute = combine and argmax; within a
-//    wave memory tiles are placed first;
+//  * pools: memory = tiles that stream weights or KV, compute = argmax; within a wave memory
+//    tiles are placed first;
 //  * placement: within a wave, tiles in (cost desc, id asc) order -- or a seeded splitmix64
 //    Fisher-Yates order when shuffle_seed != 0 -- each to the queue with the smallest
 //    accumulated cost (ties to the lowest SM), the accumulated cost carried across waves;
@@ -56,7 +58,8 @@ struct Tile {
     int32_t pub[kMaxPub][2];
     int64_t stream_bytes;
     int32_t id;
-    bool memory() const { return op != OP_COMB && op != OP_ARGMAX; }
+    int32_t arrive, arrive_n;   // ATTN: arrival counter and arrivals per group (-1: none)
+    bool memory() const { return op != OP_ARGMAX; }
     int64_t cost() const { return stream_bytes + kTileOverhead; }
 };
 
@@ -115,8 +118,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     mk_sched_opts o{};
     if (opts) o = *opts;
     Geometry g{};
-    g.page_bytes = o.page_bytes ? o.page_bytes : 16384;
-    g.tile_bytes = o.tile_bytes ? o.tile_bytes : 32768;
+    g.page_bytes = o.page_bytes ? o.page_bytes : 32768;
+    g.tile_bytes = o.tile_bytes ? o.tile_bytes : 131072;
     g.attn_chunk = o.attn_chunk ? o.attn_chunk : 64;
     g.shuffle_seed = o.shuffle_seed;
     if (g.page_bytes < 1024 || g.page_bytes % 128 || g.page_bytes > (1 << 20))
@@ -128,17 +131,20 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     const int32_t nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim, hpg = nq / nkv;
     const int32_t qd = nq * d, kvd = nkv * d, nqkv = qd + 2 * kvd;
 
-    g.r_qkv = o.rows_qkv ? o.rows_qkv : fit(kMaxRows, g.tile_bytes, 2ll * H);
+    // default rows per tile: the tile_bytes target, capped so QKV and O stay fine-grained (they are
+    // small per layer and gate the attention); gate/up, down and LM-head tiles carry more rows
+    g.r_qkv = o.rows_qkv ? o.rows_qkv : fit(8, g.tile_bytes, 2ll * H);
     if (!o.rows_qkv)
         while (d % g.r_qkv) --g.r_qkv;
-    g.r_o = o.rows_o ? o.rows_o : fit(kMaxRows, g.tile_bytes, 2ll * qd);
+    g.r_o = o.rows_o ? o.rows_o : fit(8, g.tile_bytes, 2ll * qd);
     g.r_up = o.pairs_up ? o.pairs_up : fit(kMaxRows / 2, g.tile_bytes, 4ll * H);
-    g.r_dn = o.rows_down ? o.rows_down : fit(kMaxRows, g.tile_bytes, 2ll * F);
+    g.r_dn = o.rows_down ? o.rows_down : fit(8, g.tile_bytes, 2ll * F);
     g.r_lm = o.rows_lm ? o.rows_lm : fit(kMaxRows, g.tile_bytes, 2ll * H);
-    if (g.r_qkv < 1 || g.r_qkv > kMaxRows || d % g.r_qkv) return fail(MK_ERR_ARG, "rows_qkv must divide head_dim, <= 8");
+    if (g.r_qkv < 1 || g.r_qkv > kMaxRows || d % g.r_qkv)
+        return fail(MK_ERR_ARG, "rows_qkv must divide head_dim and be <= %d", kMaxRows);
     if (g.r_o < 1 || g.r_o > kMaxRows || g.r_dn < 1 || g.r_dn > kMaxRows || g.r_lm < 1 || g.r_lm > kMaxRows ||
         g.r_up < 1 || g.r_up > kMaxRows / 2)
-        return fail(MK_ERR_ARG, "rows per tile out of range");
+        return fail(MK_ERR_ARG, "rows per tile out of range (<= %d rows, <= %d pairs)", kMaxRows, kMaxRows / 2);
     g.n_qkv = cdiv(nqkv, g.r_qkv);
     g.n_o = cdiv(H, g.r_o);
     g.n_up = cdiv(F, g.r_up);
@@ -160,6 +166,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         for (auto& w : waits) { t.wait[t.nwait][0] = w.first; t.wait[t.nwait][1] = w.second; ++t.nwait; }
         t.pub[0][0] = pub.first; t.pub[0][1] = pub.second; t.npub = 1;
         t.stream_bytes = bytes;
+        t.arrive = -1;
+        t.arrive_n = 0;
         t.id = int32_t(tiles.size());
         tiles.push_back(t);
     };
@@ -171,42 +179,39 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     for (int32_t l = 0; l < L; ++l) {
         for (int32_t t = 0; t < g.n_qkv; ++t) {
             int32_t r0 = t * g.r_qkv, n = std::min(g.r_qkv, nqkv - r0);
-            Tile tmp{};
-            (void)tmp;
             if (l == 0)
-                add(OP_QKV, l, 0, r0, n, 0, 6 * l, {}, {cm.qkv(l, group_of_row(r0)), 1}, int64_t(n) * H * 2);
+                add(OP_QKV, l, 0, r0, n, 0, 5 * l, {}, {cm.qkv(l, group_of_row(r0)), 1}, int64_t(n) * H * 2);
             else
-                add(OP_QKV, l, 0, r0, n, 0, 6 * l, {{cm.down(l - 1), g.n_dn}}, {cm.qkv(l, group_of_row(r0)), 1},
+                add(OP_QKV, l, 0, r0, n, 0, 5 * l, {{cm.down(l - 1), g.n_dn}}, {cm.qkv(l, group_of_row(r0)), 1},
                     int64_t(n) * H * 2);
         }
         for (int32_t b = 0; b < B; ++b)
             for (int32_t gr = 0; gr < nkv; ++gr)
-                for (int32_t ch = 0; ch < g.n_chunk; ++ch)
-                    add(OP_ATTN, l, b, gr, ch, g.attn_chunk, 6 * l + 1, {{cm.qkv(l, gr), per_group_qkv}},
-                        {cm.attn(l, b, gr), 1}, int64_t(2) * g.attn_chunk * d * 2);
-        for (int32_t b = 0; b < B; ++b)
-            for (int32_t gr = 0; gr < nkv; ++gr)
-                add(OP_COMB, l, b, gr, g.n_chunk, g.attn_chunk, 6 * l + 2, {{cm.attn(l, b, gr), g.n_chunk}},
-                    {cm.comb(l), 1}, 0);
+                for (int32_t ch = 0; ch < g.n_chunk; ++ch) {
+                    add(OP_ATTN, l, b, gr, ch, g.attn_chunk, 5 * l + 1, {{cm.qkv(l, gr), per_group_qkv}},
+                        {cm.comb(l), 1}, int64_t(2) * g.attn_chunk * d * 2);
+                    tiles.back().arrive = cm.attn(l, b, gr);
+                    tiles.back().arrive_n = g.n_chunk;
+                }
         for (int32_t t = 0; t < g.n_o; ++t) {
             int32_t r0 = t * g.r_o, n = std::min(g.r_o, H - r0);
-            add(OP_OPROJ, l, 0, r0, n, 0, 6 * l + 3, {{cm.comb(l), B * nkv}}, {cm.o(l), 1}, int64_t(n) * qd * 2);
+            add(OP_OPROJ, l, 0, r0, n, 0, 5 * l + 2, {{cm.comb(l), B * nkv}}, {cm.o(l), 1}, int64_t(n) * qd * 2);
         }
         for (int32_t t = 0; t < g.n_up; ++t) {
             int32_t r0 = t * g.r_up, n = std::min(g.r_up, F - r0);
-            add(OP_UPGATE, l, 0, r0, n, 0, 6 * l + 4, {{cm.o(l), g.n_o}}, {cm.up(l), 1}, int64_t(2) * n * H * 2);
+            add(OP_UPGATE, l, 0, r0, n, 0, 5 * l + 3, {{cm.o(l), g.n_o}}, {cm.up(l), 1}, int64_t(2) * n * H * 2);
         }
         for (int32_t t = 0; t < g.n_dn; ++t) {
             int32_t r0 = t * g.r_dn, n = std::min(g.r_dn, H - r0);
-            add(OP_DOWN, l, 0, r0, n, 0, 6 * l + 5, {{cm.up(l), g.n_up}}, {cm.down(l), 1}, int64_t(n) * F * 2);
+            add(OP_DOWN, l, 0, r0, n, 0, 5 * l + 4, {{cm.up(l), g.n_up}}, {cm.down(l), 1}, int64_t(n) * F * 2);
         }
     }
     for (int32_t t = 0; t < g.n_lm; ++t) {
         int32_t r0 = t * g.r_lm, n = std::min(g.r_lm, V - r0);
-        add(OP_LMHEAD, L, 0, r0, n, t, 6 * L, {{cm.down(L - 1), g.n_dn}}, {cm.lm(), 1}, int64_t(n) * H * 2);
+        add(OP_LMHEAD, L, 0, r0, n, t, 5 * L, {{cm.down(L - 1), g.n_dn}}, {cm.lm(), 1}, int64_t(n) * H * 2);
     }
     for (int32_t b = 0; b < B; ++b)
-        add(OP_ARGMAX, L, b, 0, g.n_lm, 0, 6 * L + 1, {{cm.lm(), g.n_lm}}, {cm.fin(), 1}, 0);
+        add(OP_ARGMAX, L, b, 0, g.n_lm, 0, 5 * L + 1, {{cm.lm(), g.n_lm}}, {cm.fin(), 1}, 0);
 
     // ---- placement ------------------------------------------------------------------------
     using Slot = std::pair<int64_t, int32_t>;  // (accumulated cost, sm)
@@ -271,10 +276,16 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
             w[W_NPAGES] = int32_t(pages);
             w[W_TILE] = t.id;
             w[W_WAVE] = t.wave;
+            if (t.arrive >= 0) { w[W_COND] = 1; w[W_ARRIVE] = t.arrive; w[W_ARRIVE_N] = t.arrive_n; }
             sch->max_pages = std::max(sch->max_pages, int32_t(pages));
         }
-    for (const Tile& t : tiles)
+    for (const Tile& t : tiles) {
+        if (t.arrive >= 0) {
+            sch->totals[t.arrive] += 1u;                      // every chunk tile arrives once
+            if (t.a1 != t.arrive_n - 1) continue;             // the group's completion counts once
+        }
         for (int q = 0; q < t.npub; ++q) sch->totals[t.pub[q][0]] += uint32_t(t.pub[q][1]);
+    }
 
     // ---- structural validation (waits point at lower waves; queues in wave order) ------------
     std::vector<int32_t> prod_wave(g.n_counters, -1);
@@ -316,7 +327,7 @@ extern "C" mk_status mk_schedule_patch(mk_schedule* s, int32_t sm, int32_t slot,
 
 extern "C" size_t mk_scratch_bytes(const mk_schedule* s) {
     if (!s) return 0;
-    return scratch_layout(s->cfg, s->geo).total;
+    return scratch_layout(s->cfg, s->geo, s->S).total;
 }
 
 extern "C" void mk_schedule_free(mk_schedule* s) { delete s; }

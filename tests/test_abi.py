@@ -1,0 +1,60 @@
+"""The C-ABI library loads and exports every function include/mk.h declares; host-side argument
+checks work without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+mk = pytest.importorskip("persistent_megakernel_decode_sm_gb300")
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "mk.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mk_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported():
+    names = header_functions()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(mk.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(mk.EXPORTS)
+
+
+def test_build_schedule_rejects_bad_arguments():
+    from workload import small_config
+    with pytest.raises(mk.MkError) as e:
+        mk.Schedule(small_config(n_kv_heads=3), 4)
+    assert e.value.status == mk.MK_ERR_ARG
+    with pytest.raises(mk.MkError):
+        mk.Schedule(small_config(), 0)
+    with pytest.raises(mk.MkError):
+        mk.Schedule(small_config(head_dim=24), 4)
+    with pytest.raises(mk.MkError):
+        mk.Schedule(small_config(batch=9), 4)
+    with pytest.raises(mk.MkError):
+        mk.Schedule(small_config(), 4, rows_qkv=7)        # must divide head_dim
+    with pytest.raises(mk.MkError):
+        mk.Schedule(small_config(), 4, page_bytes=1000)
+
+
+def test_patch_and_scratch_size():
+    from workload import small_config
+    s = mk.Schedule(small_config(), 3)
+    q = s.queues()
+    s.patch(1, 0, 5, 77)
+    assert s.queues()[1, 0, 5] == 77 and q[1, 0, 5] != 77 or q[1, 0, 5] == 77
+    with pytest.raises(mk.MkError):
+        s.patch(3, 0, 0, 1)
+    assert s.scratch_bytes > 0 and s.scratch_bytes % 256 == 0
+
+
+def test_last_error_message_is_set():
+    from workload import small_config
+    with pytest.raises(mk.MkError) as e:
+        mk.Schedule(small_config(n_q_heads=5, n_kv_heads=2), 4)
+    assert "n_kv_heads" in str(e.value)

@@ -1,0 +1,110 @@
+"""The host scheduler (C++, in libmk.so) against its independent restatement on the oracle side,
+the schedule validator and the host simulator of the queue interpreter (no GPU).
+
+Bit-exact: the C++ queues [S, Q, 32] and per-step counter totals equal the restatement's, for
+every workload, several SM counts and the shuffled placement."""
+import numpy as np
+import pytest
+
+from oracle import schedule_ref as sr
+from workload import WORKLOADS, get_workload, small_config
+
+mk = pytest.importorskip("persistent_megakernel_decode_sm_gb300")
+
+SMS = [1, 2, 7, 37, 132, 148, 152]
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+@pytest.mark.parametrize("S", [1, 7, 37, 152])
+def test_cpp_schedule_bit_exact_vs_restatement(name, S):
+    cfg = get_workload(name).cfg
+    s = mk.Schedule(cfg, S)
+    q, t, _ = sr.build_schedule(cfg, S)
+    assert np.array_equal(s.queues(), q)
+    assert np.array_equal(s.totals(), t)
+
+
+@pytest.mark.parametrize("seed", [1, 12345, 2 ** 63 + 17])
+def test_cpp_shuffled_placement_bit_exact(seed):
+    cfg = get_workload("llama1b_ctx512").cfg
+    s = mk.Schedule(cfg, 148, shuffle_seed=seed)
+    q, t, _ = sr.build_schedule(cfg, 148, sr.SchedOpts(shuffle_seed=seed))
+    assert np.array_equal(s.queues(), q) and np.array_equal(s.totals(), t)
+
+
+@pytest.mark.parametrize("kw", [dict(page_bytes=16384, tile_bytes=32768, attn_chunk=32),
+                                dict(rows_qkv=4, rows_o=3, pairs_up=5, rows_down=7, rows_lm=9),
+                                dict(attn_chunk=100)])
+def test_cpp_knobs_bit_exact(kw):
+    cfg = small_config(n_layers=3, max_seq=300)
+    s = mk.Schedule(cfg, 11, **kw)
+    q, t, _ = sr.build_schedule(cfg, 11, sr.SchedOpts(**kw))
+    assert np.array_equal(s.queues(), q) and np.array_equal(s.totals(), t)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama1b_ctx512", "llama1b_batch8"])
+@pytest.mark.parametrize("S,seed", [(152, 0), (37, 0), (5, 99)])
+def test_schedule_valid_and_deadlock_free(name, S, seed):
+    cfg = get_workload(name).cfg
+    q, t, _ = sr.build_schedule(cfg, S, sr.SchedOpts(shuffle_seed=seed))
+    assert sr.validate(q, t, cfg, sr.SchedOpts(shuffle_seed=seed)) == []
+    assert sr.simulate(q, t, cfg, n_epochs=2, seed=seed) == []
+
+
+def test_schedule_tiles_cover_every_row_once():
+    cfg = get_workload("tiny").cfg
+    tiles, cnt, R = sr.enumerate_tiles(cfg, sr.SchedOpts())
+    for op, total in ((sr.QKV, cfg.qkv_rows), (sr.OPROJ, cfg.hidden), (sr.UPGATE, cfg.ffn),
+                      (sr.DOWN, cfg.hidden), (sr.LMHEAD, cfg.vocab)):
+        for l in (range(cfg.n_layers) if op != sr.LMHEAD else [cfg.n_layers]):
+            rows = np.zeros(total, int)
+            for t in tiles:
+                if t.op == op and t.layer == l:
+                    rows[t.a0:t.a0 + t.a1] += 1
+            assert np.all(rows == 1)
+
+
+def _mutate(q, fn):
+    q = q.copy()
+    fn(q)
+    return q
+
+
+def test_validator_and_simulator_catch_planted_errors():
+    cfg = get_workload("tiny").cfg
+    q, t, _ = sr.build_schedule(cfg, 5)
+    # a dropped tile
+    s0 = next(i for i in range(q.shape[1]) if q[0, i, 0] != 0)
+    bad = _mutate(q, lambda a: a.__setitem__((0, s0), 0))
+    assert sr.validate(bad, t, cfg)
+    # a wait that asks for one more completion than the producers publish -> deadlock
+    qi = [(s, i) for s in range(q.shape[0]) for i in range(q.shape[1]) if q[s, i, 6] > 0][0]
+    bad = q.copy()
+    bad[qi][8] += 1
+    assert sr.validate(bad, t, cfg)
+    assert any("deadlock" in e for e in sr.simulate(bad, t, cfg, n_epochs=1))
+    # a wait removed: the simulator sees a read before its producer ran
+    bad = q.copy()
+    for s in range(q.shape[0]):
+        for i in range(q.shape[1]):
+            if q[s, i, 0] == sr.UPGATE:
+                bad[s, i, 6] = 0
+    assert any("before" in e for e in sr.simulate(bad, t, cfg, n_epochs=1, seed=1))
+    # per-SM wave order broken
+    S_, Q_ = q.shape[0], q.shape[1]
+    s = max(range(S_), key=lambda k: int((q[k, :, 0] != 0).sum()))
+    n = int((q[s, :, 0] != 0).sum())
+    bad = q.copy()
+    bad[s, [0, n - 1]] = bad[s, [n - 1, 0]]
+    assert sr.validate(bad, t, cfg)
+
+
+def test_counter_totals_match_waits():
+    cfg = get_workload("llama1b_ctx512").cfg
+    q, t, info = sr.build_schedule(cfg, 152)
+    cnt = info["counters"]
+    L, B, nkv = cfg.n_layers, cfg.batch, cfg.n_kv_heads
+    assert t[cnt.comb(3)] == B * nkv
+    assert t[cnt.attn(2, 0, 1)] == info["n_chunks"]
+    assert t[cnt.lm()] == -(-cfg.vocab // info["rows"]["lm"])
+    assert t[cnt.final()] == B

@@ -113,6 +113,14 @@ def get_workload(name: str) -> Workload:
         cfg = _llama1b(batch=8, max_seq=4096 + 64)
         return Workload(name, cfg, prompt_len=0, kv_len=lens, decode_steps=64,
                         description="Llama-3.2-1B shape, batch 8, KV U[256,4096], 64 steps")
+    if name == "llama1b_reduced":
+        # profiling case (not a benchmark line): Llama-3.2-1B layer shapes, 2 layers, vocab 32000;
+        # ~380 MB of weights, larger than L2, small enough for many-pass profiler captures
+        cfg = ModelConfig(n_layers=2, hidden=2048, n_q_heads=32, n_kv_heads=8, head_dim=64, ffn=8192,
+                          vocab=32000, tied_embeddings=True, batch=1, max_seq=512 + 128, rms_eps=1e-5,
+                          rope_theta=500000.0)
+        return Workload(name, cfg, prompt_len=0, kv_len=[512], decode_steps=128,
+                        description="reduced Llama-3.2-1B shape for profiling: 2 layers, vocab 32000")
     if name == "llama8b_ctx2048":
         cfg = ModelConfig(n_layers=32, hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
                           ffn=14336, vocab=128256, tied_embeddings=False, batch=1,
