@@ -181,6 +181,25 @@ mk_status mk_set_trace(mk_ctx* c, uint64_t* buf);
 mk_status mk_decode_step(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
                          int32_t* next_tokens);
 
+/* One decode step like mk_decode_step, for callers that cannot allocate device memory: code
+ * under a framework whose caching allocator owns the GPU's memory, or a latency-critical loop
+ * where cudaMalloc / cudaFree may synchronise the device.  (The page has no counterpart: this is
+ * an interface convenience of this library.)  Allocates nothing.  Instead of the scratch bound
+ * with the context it uses one library-owned device array of MK_STATIC_SCRATCH_BYTES (16 MiB),
+ * which every GPU that loads the library holds until the process exits.
+ *  - The first call on a device sets the array up for that device (looks up its device
+ *    address); make that first call before any stream capture.
+ *  - A step that needs more scratch than the array holds is rejected with MK_ERR_CAPACITY
+ *    (e.g. long contexts, whose attention partials grow with max_seq).
+ *  - Every call shares the array and finds the previous call's contents; the call resets what
+ *    must start fresh.  Calls that overlap on the GPU (other streams, other contexts at the same
+ *    time) race on the array.
+ * Arguments, results and errors as mk_decode_step (the context's counters and stream are used;
+ * its bound scratch is not touched). */
+#define MK_STATIC_SCRATCH_BYTES (16u << 20)
+mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
+                                int32_t* next_tokens);
+
 /* Asynchronous form: enqueues one step on the bound stream and returns.  next_tokens_dev is a
  * DEVICE int32[batch] buffer or NULL.  Device-side errors surface at the next mk_ctx_status or
  * mk_decode_step. */

@@ -32,7 +32,8 @@ STATUS_NAMES = ["MK_OK", "MK_ERR_ARG", "MK_ERR_CAPACITY", "MK_ERR_RESOURCES", "M
                 "MK_ERR_OPCODE", "MK_ERR_BOUNDS", "MK_ERR_POISONED"]
 EXPORTS = ["mk_build_schedule", "mk_schedule_queues", "mk_schedule_counters", "mk_schedule_patch",
            "mk_scratch_bytes", "mk_schedule_free", "mk_bind", "mk_set_timeout", "mk_decode_step",
-           "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind", "mk_set_trace"]
+           "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind", "mk_set_trace",
+           "mk_decode_step_static"]
 
 
 class MkError(RuntimeError):
@@ -94,6 +95,8 @@ lib.mk_device_sm_count.restype = ctypes.c_int
 lib.mk_device_sm_count.argtypes = [_I32P]
 lib.mk_last_error.restype = ctypes.c_char_p
 lib.mk_last_error.argtypes = []
+lib.mk_decode_step_static.restype = ctypes.c_int
+lib.mk_decode_step_static.argtypes = [_P, _I32P, _I32P, _P, _I32P]
 lib.mk_set_trace.restype = ctypes.c_int
 lib.mk_set_trace.argtypes = [_P, _P]
 lib.mk_unbind.restype = None
@@ -216,6 +219,14 @@ class Decoder:
         t, p = self._arrays(tokens, pos)
         out = (ctypes.c_int32 * self.cfg.batch)()
         _check(lib.mk_decode_step(self.handle, t, p, _ptr(lg), out))
+        return list(out)
+
+    def step_static(self, tokens: Sequence[int], pos: Sequence[int], logits=None) -> List[int]:
+        """mk_decode_step_static: one synchronous step using the library's static device scratch."""
+        lg = self.logits if logits is None else logits
+        t, p = self._arrays(tokens, pos)
+        out = (ctypes.c_int32 * self.cfg.batch)()
+        _check(lib.mk_decode_step_static(self.handle, t, p, _ptr(lg), out))
         return list(out)
 
     def launch(self, tokens: Sequence[int], pos: Sequence[int], logits=None, next_dev=None):

@@ -14,6 +14,8 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <type_traits>
 
 #include "mk_internal.h"
 
@@ -387,4 +389,100 @@ extern "C" void mk_unbind(mk_ctx* c) {
     if (!c) return;
     cudaStreamSynchronize(c->stream);
     free_ctx(c);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Decode step without caller scratch.  Some callers cannot allocate device memory themselves:
+// code that runs under a framework whose caching allocator owns the GPU's memory (a direct
+// cudaMalloc bypasses its accounting and can fail once the pool has reserved the device), or a
+// latency-critical serving loop where a cudaMalloc / cudaFree may synchronise the whole device.
+// For them this entry point keeps the step's scratch in a library-owned array of fixed size that
+// every GPU loading the library holds until the process exits.  Calls share the array: two calls
+// that overlap on the GPU (different streams, or different contexts at once) race on it.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // MK_STATIC_SCRATCH_BYTES
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+static uint8_t* g_static_scratch_dev[64];                    // device address, per device
+static std::mutex g_static_mutex;
+
+extern "C" mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
+                                           int32_t* next_tokens) {
+    if (!c || !tokens || !pos || !logits || !next_tokens) return fail(MK_ERR_ARG, "null argument");
+    if (c->poisoned) return fail(MK_ERR_POISONED, "context poisoned by an earlier device error");
+    int dev = -1;
+    CK(cudaGetDevice(&dev));
+    if (dev != c->device) return fail(MK_ERR_ARG, "the context is bound to device %d, device %d is current", c->device, dev);
+    if (dev < 0 || dev >= 64) return fail(MK_ERR_ARG, "device ordinal %d out of range", dev);
+    uint8_t* base;
+    {   // set-up, once per device, with that device current: the array's device address
+        std::lock_guard<std::mutex> lock(g_static_mutex);
+        if (!g_static_scratch_dev[dev]) {
+            void* ptr = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+            g_static_scratch_dev[dev] = static_cast<uint8_t*>(ptr);
+        }
+        base = g_static_scratch_dev[dev];
+    }
+    // the bound scratch layout, moved onto the static array (the error word leads the layout and
+    // the RoPE table ends it)
+    Params p = c->base;
+    uint8_t* bound = reinterpret_cast<uint8_t*>(p.err);
+    const size_t half = size_t(p.d / 2);
+    const size_t need = size_t(reinterpret_cast<const uint8_t*>(p.rope) - bound) + size_t(p.max_seq) * half * 8;
+    if (need > kStaticScratchBytes)
+        return fail(MK_ERR_CAPACITY, "step needs %zu bytes of scratch, the static array holds %zu", need,
+                    kStaticScratchBytes);
+    auto move = [&](auto* ptr) {
+        using T = std::remove_pointer_t<decltype(ptr)>;
+        return reinterpret_cast<T*>(base + (reinterpret_cast<const uint8_t*>(ptr) - bound));
+    };
+    p.err = move(p.err);
+    p.tokens_out = move(p.tokens_out);
+    p.x_attn = move(p.x_attn);
+    p.x_out = move(p.x_out);
+    p.qkv = move(p.qkv);
+    p.part = move(p.part);
+    p.o = move(p.o);
+    p.h = move(p.h);
+    p.lm_part = move(p.lm_part);
+    p.rope = move(const_cast<float2*>(p.rope));
+    for (int b = 0; b < c->cfg.batch; ++b) {
+        if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab) return fail(MK_ERR_ARG, "token %d out of range", tokens[b]);
+        if (pos[b] < 0 || pos[b] >= c->cfg.max_seq)
+            return fail(MK_ERR_ARG, "pos %d outside the KV capacity [0, %d)", pos[b], c->cfg.max_seq);
+        p.tok[b] = tokens[b];
+        p.pos[b] = pos[b];
+    }
+    // the array keeps the previous call's contents: reset what must start fresh (error word and
+    // output tokens, the LM-head partials' epoch tags) and rebuild the RoPE table for this model
+    const size_t lm_bytes = size_t(c->cfg.batch) * size_t(c->grid) * kNumConsumerWarps * 2 * 16;
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(p.err, 0, 256, c->stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(p.lm_part, 0xFF, lm_bytes, c->stream)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(static scratch)");
+    if ((e = launch_rope_table(const_cast<float2*>(p.rope), c->cfg.max_seq, c->cfg.head_dim, c->cfg.rope_theta,
+                               c->stream)) != cudaSuccess)
+        return cuda_fail(e, "rope table kernel");
+    p.epoch = c->epoch;
+    p.logits = logits;
+    p.next_dev = nullptr;
+    void* args[] = {&p};
+    e = cudaLaunchCooperativeKernel(c->fn, dim3(c->grid), dim3(kThreads), args, size_t(c->smem), c->stream);
+    if (e == cudaErrorCooperativeLaunchTooLarge)
+        return fail(MK_ERR_RESOURCES, "cooperative launch of %d CTAs does not fit the device", c->grid);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
+    c->epoch += 1;
+    e = cudaMemcpyAsync(c->h_result, p.err, 96, cudaMemcpyDeviceToHost, c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) {
+        c->poisoned = true;
+        return cuda_fail(e, "step readback");
+    }
+    if (c->h_result[0] != 0) {
+        c->poisoned = true;
+        return fail(mk_status(c->h_result[0]), "device error %d (CTA %d, queue slot %d)", c->h_result[0],
+                    c->h_result[1], c->h_result[2]);
+    }
+    for (int b = 0; b < c->cfg.batch; ++b) next_tokens[b] = c->h_result[16 + b];
+    return MK_OK;
 }
