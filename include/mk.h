@@ -137,7 +137,8 @@ typedef struct {
     const void* const* wdown;
 } mk_weights;
 
-/* KV cache, bf16, caller-owned (page object table: "layered, paged K/V", lifetime = request).
+/* KV cache, bf16, caller-owned (the page's object table lists the K/V cache as a per-layer
+ * object in HBM that lives as long as the request).
  * Element (b, l, g, p, e) of K lives at k + b*batch_stride + l*layer_stride + g*head_stride
  * + p*head_dim + e (strides in elements, each a multiple of 8); V likewise. */
 typedef struct {
@@ -146,9 +147,9 @@ typedef struct {
     int64_t batch_stride, layer_stride, head_stride;
 } mk_kv;
 
-/* Binds a schedule to one model instance on the current CUDA device (page: "llama.cu performs
- * one model-specific binding; weights, KV cache, activations and counters are all passed in as
- * objects of this resident execution").
+/* Binds a schedule to one model instance on the current CUDA device (the page's model binding:
+ * weights, KV cache, activations and counters become objects of the one resident execution,
+ * bound once).
  * counters: device uint32[n_counters], caller-owned; zeroed by mk_bind.
  * scratch:  device buffer of >= mk_scratch_bytes(s) bytes, 256-byte aligned, caller-owned.
  * stream:   a cudaStream_t (NULL = legacy default stream); every launch of the context goes on it.
@@ -159,12 +160,30 @@ typedef struct {
 mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, uint32_t* counters,
                   void* scratch, void* stream, mk_ctx** out);
 
-/* Time budget, in nanoseconds, of every single device wait (counter spin, page / slot barrier).
+/* Time budget, in nanoseconds, of every single device wait (counter spin, tagged-data poll, page /
+ * slot barrier).
  * When one runs out the kernel records MK_ERR_TIMEOUT, every CTA leaves its loop after draining
  * its copies in flight, and the context is poisoned.  Default 2e9 (2 s). */
 mk_status mk_set_timeout(mk_ctx* c, uint64_t ns);
 
-/* Per-instruction timeline for profiling (the page's "scheduling ledger": scheduler cycles,
+/* How a consumer learns that the inputs of its instruction are ready.
+ *  MK_SYNC_TAGS (default): the activation vectors one operator hands to the next (q/k/v,
+ *    attention output, both residual streams, SwiGLU output) are epoch-tagged -- every element is
+ *    one 64-bit word holding the fp32 value and the step's tag -- and a consumer polls the
+ *    elements it reads until each carries this step's tag.  One read both proves readiness and
+ *    fetches the data, so a dependency costs one memory round trip instead of the publisher's
+ *    release fence, the counter add, the consumer's counter poll and then the data read.
+ *    Counters are still published; they are awaited only where no tagged vector carries the
+ *    dependency (the greedy argmax over the LM-head partials).
+ *  MK_SYNC_COUNTERS: every instruction first waits all of its counters with acquire semantics
+ *    (the page's protocol: wait the counters, run the body, fence, then add the completions); the tag checks then
+ *    pass at the first read.
+ * Both modes run the same arithmetic in the same order: their results are bit-identical.
+ * Takes effect at the next launch.  Errors: MK_ERR_ARG (null context, unknown mode). */
+typedef enum { MK_SYNC_TAGS = 0, MK_SYNC_COUNTERS = 1 } mk_sync_mode;
+mk_status mk_set_sync(mk_ctx* c, int32_t mode);
+
+/* Per-instruction timeline for profiling (the page's scheduling ledger: scheduler cycles,
  * dependency waits).  buf: DEVICE uint64[S * Q * 8] (caller-owned) or NULL to switch tracing off.
  * While on, every launch writes globaltimer stamps (ns) for instruction (sm, slot) at
  * buf[(sm * Q + slot) * 8 + k]: k = 0 slot published by the loader, 1 its pages issued,
@@ -207,7 +226,9 @@ mk_status mk_launch_step(mk_ctx* c, const int32_t* tokens, const int32_t* pos, f
                          int32_t* next_tokens_dev);
 
 /* Waits for the bound stream and returns the device error state (MK_OK when no step failed).
- * info (optional, 8 int32): code, CTA, queue slot, counter, value seen, value wanted, role, 0. */
+ * info (optional, 8 int32): code, CTA, queue slot, counter, value seen, value wanted, role, 0.
+ * role: 1 loader, 2 consumer (page / slot / CTA barrier), 3 publisher, 4 counter wait,
+ * 5 tagged-data poll (counter, seen, wanted: -1, tag seen, tag wanted). */
 mk_status mk_ctx_status(mk_ctx* c, int32_t* info);
 
 /* Number of SMs of the current CUDA device (the natural sm_count), or MK_ERR_CUDA. */

@@ -30,10 +30,12 @@ MK_OK, MK_ERR_ARG, MK_ERR_CAPACITY, MK_ERR_RESOURCES, MK_ERR_CUDA, MK_ERR_TIMEOU
     MK_ERR_BOUNDS, MK_ERR_POISONED = range(9)
 STATUS_NAMES = ["MK_OK", "MK_ERR_ARG", "MK_ERR_CAPACITY", "MK_ERR_RESOURCES", "MK_ERR_CUDA", "MK_ERR_TIMEOUT",
                 "MK_ERR_OPCODE", "MK_ERR_BOUNDS", "MK_ERR_POISONED"]
+SYNC_TAGS, SYNC_COUNTERS = 0, 1   # mk_sync_mode
+
 EXPORTS = ["mk_build_schedule", "mk_schedule_queues", "mk_schedule_counters", "mk_schedule_patch",
            "mk_scratch_bytes", "mk_schedule_free", "mk_bind", "mk_set_timeout", "mk_decode_step",
            "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind", "mk_set_trace",
-           "mk_decode_step_static"]
+           "mk_decode_step_static", "mk_set_sync"]
 
 
 class MkError(RuntimeError):
@@ -99,6 +101,8 @@ lib.mk_decode_step_static.restype = ctypes.c_int
 lib.mk_decode_step_static.argtypes = [_P, _I32P, _I32P, _P, _I32P]
 lib.mk_set_trace.restype = ctypes.c_int
 lib.mk_set_trace.argtypes = [_P, _P]
+lib.mk_set_sync.restype = ctypes.c_int
+lib.mk_set_sync.argtypes = [_P, ctypes.c_int32]
 lib.mk_unbind.restype = None
 lib.mk_unbind.argtypes = [_P]
 
@@ -242,6 +246,14 @@ class Decoder:
         if st != MK_OK:
             raise MkError(st, lib.mk_last_error().decode(errors="replace"))
         return list(info)
+
+    def set_sync(self, mode: str):
+        """mk_set_sync: "tags" (epoch-tagged activations, the default) or "counters" (every
+        instruction waits its completion counters first)."""
+        modes = {"tags": SYNC_TAGS, "counters": SYNC_COUNTERS}
+        if mode not in modes:
+            raise ValueError(f"sync mode {mode!r}: expected one of {sorted(modes)}")
+        _check(lib.mk_set_sync(self.handle, modes[mode]))
 
     def set_trace(self, buf):
         """mk_set_trace: buf is a CUDA int64 tensor of S*Q*8 elements, or None to stop tracing."""

@@ -14,6 +14,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <type_traits>
 
@@ -286,21 +287,39 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
     p.kv_hstride = kv->head_stride;
     p.err = reinterpret_cast<int32_t*>(sb + sl.err);
     p.tokens_out = reinterpret_cast<int32_t*>(sb + sl.tokens);
-    p.x_attn = reinterpret_cast<float*>(sb + sl.x_attn);
-    p.x_out = reinterpret_cast<float*>(sb + sl.x_out);
-    p.qkv = reinterpret_cast<float*>(sb + sl.qkv);
+    p.x_attn = reinterpret_cast<uint64_t*>(sb + sl.x_attn);
+    p.x_out = reinterpret_cast<uint64_t*>(sb + sl.x_out);
+    p.qkv = reinterpret_cast<uint64_t*>(sb + sl.qkv);
     p.part = reinterpret_cast<float*>(sb + sl.part);
-    p.o = reinterpret_cast<float*>(sb + sl.o);
+    p.o = reinterpret_cast<uint64_t*>(sb + sl.o);
     p.h = reinterpret_cast<float*>(sb + sl.h);
     p.lm_part = reinterpret_cast<int4*>(sb + sl.lm_part);
     p.rope = reinterpret_cast<const float2*>(sb + sl.rope);
+    // Readers without tags: the argmax (LM-head partials), the MLP down projection (the SwiGLU
+    // output is plain fp32) and every matvec whose rows are cut into segments (its per-warp input
+    // segment is read after an acquiring wait); their producers publish after a release fence.
+    p.acquire_ops = (1u << OP_ARGMAX) | (1u << OP_DOWN);
+    p.release_ops = (1u << OP_LMHEAD) | (1u << OP_UPGATE);
+    auto untagged = [&](int op, std::initializer_list<int> producers) {
+        if (p.mv[op].nseg <= 1) return;
+        p.acquire_ops |= 1u << op;
+        for (int q : producers) p.release_ops |= 1u << q;
+    };
+    untagged(OP_QKV, {OP_DOWN});
+    untagged(OP_OPROJ, {OP_ATTN});
+    untagged(OP_UPGATE, {OP_OPROJ});
+    untagged(OP_DOWN, {OP_UPGATE});
+    untagged(OP_LMHEAD, {OP_DOWN});
     p.timeout_ns = 2000000000ull;
     p.smem_misc_off = n_pages * g.page_bytes;
     p.attn_scratch_floats = asf;
     p.qrot_floats = qrf;
 
+    // tags start at 0 (never a step's tag): words left in the scratch by an earlier binding must
+    // not pass for this context's first steps
     if ((e = cudaMemsetAsync(counters, 0, s->totals.size() * 4, x->stream)) != cudaSuccess ||
         (e = cudaMemsetAsync(sb + sl.err, 0, 256, x->stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(sb + sl.x_attn, 0, sl.lm_part - sl.x_attn, x->stream)) != cudaSuccess ||
         (e = cudaMemsetAsync(sb + sl.lm_part, 0xFF, size_t(c.batch) * s->S * kNumConsumerWarps * 16, x->stream)) != cudaSuccess)
         return bail(cuda_fail(e, "cudaMemsetAsync"));
     if ((e = launch_rope_table(reinterpret_cast<float2*>(sb + sl.rope), c.max_seq, d, c.rope_theta, x->stream)) !=
@@ -314,6 +333,13 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
 extern "C" mk_status mk_set_timeout(mk_ctx* c, uint64_t ns) {
     if (!c || ns == 0) return fail(MK_ERR_ARG, "bad argument");
     c->base.timeout_ns = ns;
+    return MK_OK;
+}
+
+extern "C" mk_status mk_set_sync(mk_ctx* c, int32_t mode) {
+    if (!c) return fail(MK_ERR_ARG, "null context");
+    if (mode != MK_SYNC_TAGS && mode != MK_SYNC_COUNTERS) return fail(MK_ERR_ARG, "unknown sync mode %d", mode);
+    c->base.sync_counters = mode == MK_SYNC_COUNTERS ? 1 : 0;
     return MK_OK;
 }
 
@@ -338,6 +364,7 @@ extern "C" mk_status mk_launch_step(mk_ctx* c, const int32_t* tokens, const int3
         p.pos[b] = pos[b];
     }
     p.epoch = c->epoch;
+    p.tag = c->epoch + 1u;
     p.logits = logits;
     p.next_dev = next_tokens_dev;
     void* args[] = {&p};
@@ -454,16 +481,20 @@ extern "C" mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, con
         p.pos[b] = pos[b];
     }
     // the array keeps the previous call's contents: reset what must start fresh (error word and
-    // output tokens, the LM-head partials' epoch tags) and rebuild the RoPE table for this model
+    // output tokens, the activation words -- another context may have left its own tags there --,
+    // the LM-head partials' epoch tags) and rebuild the RoPE table for this model
     const size_t lm_bytes = size_t(c->cfg.batch) * size_t(c->grid) * kNumConsumerWarps * 2 * 16;
     cudaError_t e;
     if ((e = cudaMemsetAsync(p.err, 0, 256, c->stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(p.x_attn, 0, size_t(reinterpret_cast<uint8_t*>(p.lm_part) - reinterpret_cast<uint8_t*>(p.x_attn)),
+                             c->stream)) != cudaSuccess ||
         (e = cudaMemsetAsync(p.lm_part, 0xFF, lm_bytes, c->stream)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync(static scratch)");
     if ((e = launch_rope_table(const_cast<float2*>(p.rope), c->cfg.max_seq, c->cfg.head_dim, c->cfg.rope_theta,
                                c->stream)) != cudaSuccess)
         return cuda_fail(e, "rope table kernel");
     p.epoch = c->epoch;
+    p.tag = c->epoch + 1u;
     p.logits = logits;
     p.next_dev = nullptr;
     void* args[] = {&p};

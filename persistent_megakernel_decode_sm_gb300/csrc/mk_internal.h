@@ -69,7 +69,11 @@ struct CounterMap {
     int32_t count() const { return base2 + 4 * L + 2; }
 };
 
-// ---- scratch layout (fp32 activations unless noted), each region 256-byte aligned -----------
+// ---- scratch layout, each region 256-byte aligned ----------------------------------------------
+// The activation vectors a step hands from one operator to the next (qkv, o, x_attn, x_out) are
+// epoch-tagged: one 64-bit word per element, fp32 value in the low half, the step's tag in the high
+// half, written and read as single 64-bit accesses.  A reader that sees this step's tag has the
+// value of this step -- the element needs no separate flag, fence or counter to be consumed.
 struct ScratchLayout {
     size_t err, tokens, x_attn, x_out, qkv, part, o, h, lm_part, rope, total;
 };
@@ -85,12 +89,12 @@ inline ScratchLayout scratch_layout(const mk_model_cfg& c, const Geometry& g, in
     auto take = [&](size_t bytes) { size_t r = off; off = align256(off + bytes); return r; };
     s.err = take(256);            // int32 err[16] at 0, int32 tokens[8] at byte 64 (one readback)
     s.tokens = s.err + 64;
-    s.x_attn = take(L * B * H * 4);
-    s.x_out = take(L * B * H * 4);
-    s.qkv = take(L * B * (qd + 2 * kvd) * 4);
-    s.part = take(L * B * size_t(c.n_kv_heads) * g.n_chunk * hpg * (d + 2) * 4);
-    s.o = take(L * B * qd * 4);
-    s.h = take(L * B * size_t(c.ffn) * 4);
+    s.x_attn = take(L * B * H * 8);                   // tagged
+    s.x_out = take(L * B * H * 8);                    // tagged
+    s.qkv = take(L * B * (qd + 2 * kvd) * 8);         // tagged
+    s.part = take(L * B * size_t(c.n_kv_heads) * g.n_chunk * hpg * (d + 2) * 4);   // fp32 chunk partials
+    s.o = take(L * B * qd * 8);                       // tagged
+    s.h = take(L * B * size_t(c.ffn) * 4);            // fp32 (its reader waits with acquire)
     s.lm_part = take(B * size_t(S) * kNumConsumerWarps * 2 * 16);   // per (sequence, CTA, warp half): max, index, epoch
     s.rope = take(size_t(c.max_seq) * (d / 2) * 8);
     s.total = off;
@@ -140,16 +144,20 @@ struct Params {
     // scratch
     int32_t* err;
     int32_t* tokens_out;
-    float* x_attn;
-    float* x_out;
-    float* qkv;
-    float* part;
-    float* o;
-    float* h;
+    uint64_t* x_attn;   // tagged [L][B][H]: residual stream after attention
+    uint64_t* x_out;    // tagged [L][B][H]: residual stream after the MLP
+    uint64_t* qkv;      // tagged [L][B][nqkv]
+    float* part;        // [L][B][nkv][n_chunk][hpg][d + 2] attention chunk partials
+    uint64_t* o;        // tagged [L][B][qd]: attention output
+    float* h;           // [L][B][F]: SwiGLU output (plain fp32, read after an acquiring wait)
     int4* lm_part;     // [B][S][16]: (max bits, index, epoch, 0)
     const float2* rope; // [max_seq][d/2] (cos, sin)
     // step
     uint32_t epoch;
+    uint32_t tag;            // epoch + 1: the tag of this step's activation words (0 = never written)
+    int32_t sync_counters;   // 1: every counter wait acquires, every publish releases (MK_SYNC_COUNTERS)
+    uint32_t acquire_ops;    // bit op: its counter waits acquire (it reads untagged inputs)
+    uint32_t release_ops;    // bit op: its completions are published after a release fence
     int32_t tok[kMaxBatch];
     int32_t pos[kMaxBatch];
     float* logits;
@@ -184,7 +192,7 @@ struct SlotInfo {            // one instruction slot: words + where its stream s
 
 // byte offsets of the non-ring shared memory (after the page ring); shared by host and device
 struct MiscLayout {
-    uint32_t slots, qwin, layers, bars, lmbest, comb, combcnt, pubinfo, red, qrot, ascr, ml, kv, xbuf, total;
+    uint32_t slots, qwin, layers, bars, lmbest, comb, combcnt, pubinfo, red, qrot, ascr, ml, kv, xbuf, gbuf, total;
 };
 
 MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qrot_floats) {
@@ -206,12 +214,14 @@ MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qr
     m.pubinfo = take(4u * kDone * 8u, 16);            // completion words of in-flight instructions
     m.red = take(4u * 64u, 16);                     // argmax scratch [16]; abort flag [32], published count [33],
                                                     // stream bytes the loader has issued [34..35] (u64),
-                                                    // last-arrival flag [40], shared x scale [41]
+                                                    // last-arrival flag [40], per-warp sums of
+                                                    // squares of the shared x [48..55]
     m.qrot = take(4u * uint32_t(qrot_floats), 16);
     m.ascr = take(4u * uint32_t(attn_scratch_floats), 16);
     m.ml = take(4u * 4u * kMaxHpg, 16);             // (m, l) per head, combine L per head
     m.kv = take(2u * 2u * kMaxHeadDim, 16);         // new k, v (bf16)
     m.xbuf = take(4u * kXBuf, 16);                  // shared matvec input (raw), one per CTA
+    m.gbuf = take(2u * kXBuf, 16);                  // its RMSNorm gain (bf16)
     m.total = (o + 255u) & ~255u;
     return m;
 }

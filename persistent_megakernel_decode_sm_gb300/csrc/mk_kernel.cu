@@ -26,7 +26,7 @@
 
 namespace mk {
 
-enum Role : int { ROLE_LOADER = 1, ROLE_CONSUMER = 2, ROLE_PUBLISHER = 3, ROLE_COUNTER = 4 };
+enum Role : int { ROLE_LOADER = 1, ROLE_CONSUMER = 2, ROLE_PUBLISHER = 3, ROLE_COUNTER = 4, ROLE_DATA = 5 };
 
 // ------------------------------------------------------------------------- PTX helpers ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -107,6 +107,38 @@ __device__ __forceinline__ uint64_t globaltimer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// epoch-tagged activation words: fp32 bits low, tag high, one single-copy-atomic 64-bit access
+__device__ __forceinline__ void st_tag(uint64_t* a, float v, uint32_t tag) {
+    const uint64_t w = (uint64_t(tag) << 32) | uint64_t(__float_as_uint(v));
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_tag(const uint64_t* a) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(a));
+    return w;
+}
+// two consecutive words (16-byte aligned); each 64-bit element is read atomically
+__device__ __forceinline__ void ld_tag2(const uint64_t* a, uint64_t& w0, uint64_t& w1) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(a));
+}
+__device__ __forceinline__ float tag_val(uint64_t w) { return __uint_as_float(uint32_t(w)); }
+__device__ __forceinline__ uint32_t tag_of(uint64_t w) { return uint32_t(w >> 32); }
+// eight consecutive tagged elements (64-byte aligned): values into v, true when all carry `tag`
+__device__ __forceinline__ bool ld8_tagged(const uint64_t* a, float* v, uint32_t tag) {
+    uint64_t w[8];
+    ld_tag2(a, w[0], w[1]);
+    ld_tag2(a + 2, w[2], w[3]);
+    ld_tag2(a + 4, w[4], w[5]);
+    ld_tag2(a + 6, w[6], w[7]);
+    bool ok = true;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        v[e] = tag_val(w[e]);
+        ok &= tag_of(w[e]) == tag;
+    }
+    return ok;
+}
+
 // whole-CTA barrier reached by warps whose lanes diverged (loader / publisher lane 0 arrives late)
 __device__ __forceinline__ void cta_sync_divergent() { asm volatile("barrier.sync 0;" ::: "memory"); }
 
@@ -163,6 +195,7 @@ struct Shared {
     uint64_t* xfull;   // shared x written (1 arrival: warp 0)
     uint64_t* xfree;   // shared x taken by every warp (8 arrivals)
     float* xbuf;       // [kXBuf] shared matvec input
+    uint16_t* gbuf;    // [kXBuf] its RMSNorm gain (bf16)
     float2* lmbest;    // [8 warps][kMaxBatch] LM-head running (max, index)
     float* comb;       // [kSlots][64] split-row segment partials
     int* combcnt;      // [kSlots][8]
@@ -197,6 +230,7 @@ __device__ __forceinline__ Shared carve(uint8_t* base, const Params& p) {
     s.xfull = s.cbar + 1;
     s.xfree = s.cbar + 2;
     s.xbuf = reinterpret_cast<float*>(b + m.xbuf);
+    s.gbuf = reinterpret_cast<uint16_t*>(b + m.gbuf);
     s.lmbest = reinterpret_cast<float2*>(b + m.lmbest);
     s.comb = reinterpret_cast<float*>(b + m.comb);
     s.combcnt = reinterpret_cast<int*>(b + m.combcnt);
@@ -230,7 +264,7 @@ __device__ void raise_error(const Params& p, const Shared& sh, int code, int rol
 
 // bounded mbarrier wait: false when the CTA aborts or the budget runs out (error recorded)
 // (the waiting thread sleeps in hardware between checks of the abort flag and the time budget)
-__device__ bool wait_bar_slow(const Params& p, const Shared& sh, uint64_t* bar, uint32_t parity, int role,
+__device__ __noinline__ bool wait_bar_slow(const Params& p, const Shared& sh, uint64_t* bar, uint32_t parity, int role,
                                            int pc) {
     const uint64_t t0 = globaltimer();
     while (true) {
@@ -406,7 +440,9 @@ __device__ void loader(const Params& p, const Shared& sh) {
             const uint32_t hi = min(lo + PB, st.total);
             mbar_arrive_expect_tx(sh.full + ps, hi - lo);
             uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
-            for (int s = 0; s < st.nseg; ++s) {
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {   // (static indexes: the stream stays in registers)
+                if (s >= st.nseg) break;
                 const uint32_t a = max(lo, st.seg[s].off);
                 const uint32_t z = min(hi, st.seg[s].off + st.seg[s].bytes);
                 if (a < z) bulk_g2s(dst + (a - lo), st.seg[s].src + (a - st.seg[s].off), z - a, sh.full + ps, pol);
@@ -451,25 +487,37 @@ __device__ void publisher(const Params& p, const Shared& sh) {
         while (n < kBatch && sh.pubinfo[((pc + n - 1) % kDone) * 8] != OP_END &&
                mbar_test_wait(sh.done + ((pc + n) % kDone), ((pc + n) / kDone) & 1))
             ++n;
-        int cid[2 * kBatch], cnt = 0;
-        uint32_t dl[2 * kBatch];
+        // pass 1: the batch's extent (END closes it), whether it needs the release fence, and
+        // whether it adds anything at all
+        bool release = p.sync_counters != 0, any = false;
         for (int i = 0; i < n; ++i) {
             const int* pi = sh.pubinfo + ((pc + i) % kDone) * 8;
             if (pi[0] == OP_END) { finished = true; n = i + 1; break; }
+            release |= (p.release_ops >> pi[0]) & 1;   // its output is read after an acquire, untagged
+            any |= pi[1] > 0 && !(pi[6] && !pi[7]);
+        }
+        // counters mode (and outputs read untagged): everything the consumers wrote for these
+        // instructions, then the counters.  Otherwise the data is tagged: no fence
+        if (any && release) fence_release_gpu();
+        // pass 2: the adds, one per run of completions to the same counter (queue order keeps
+        // the tiles of one operator together), accumulated in registers
+        int run_c = -1;
+        uint32_t run_d = 0;
+        for (int i = 0; i < n; ++i) {
+            const int* pi = sh.pubinfo + ((pc + i) % kDone) * 8;
+            if (pi[0] == OP_END) break;
             if (pi[6] && !pi[7]) continue;   // conditional completion not fired by this tile
             for (int k = 0; k < pi[1]; ++k) {
                 const int c = pi[2 + 2 * k];
-                const uint32_t d = uint32_t(pi[3 + 2 * k]);
-                int j = 0;
-                while (j < cnt && cid[j] != c) ++j;
-                if (j == cnt) { cid[cnt] = c; dl[cnt] = 0; ++cnt; }
-                dl[j] += d;
+                if (c != run_c) {
+                    if (run_c >= 0) red_add_relaxed_gpu(p.counters + run_c, run_d);
+                    run_c = c;
+                    run_d = 0;
+                }
+                run_d += uint32_t(pi[3 + 2 * k]);
             }
         }
-        if (cnt) {
-            fence_release_gpu();   // everything the consumers wrote for these instructions, then the counters
-            for (int j = 0; j < cnt; ++j) red_add_relaxed_gpu(p.counters + cid[j], dl[j]);
-        }
+        if (run_c >= 0) red_add_relaxed_gpu(p.counters + run_c, run_d);
         if (p.trace)
             for (int i = 0; i < n; ++i) stamp(p, pc + i, 4);
         pc += n;
@@ -530,48 +578,137 @@ __device__ bool cbar(Cw& c, int pc) {
     return ok;
 }
 
-__device__ __forceinline__ void load8(const float* srcf, const uint16_t* srcb, int e0, float* v) {
-    if (srcf) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(srcf + e0));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(srcf + e0 + 4));
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+// Bounded wait on tagged data, by a whole warp: call after a poll in which some lane did not yet
+// see this step's tag.  False (warp-uniform) once the CTA aborts, another CTA has recorded an
+// error, or the time budget runs out (then the timeout is recorded here).
+struct Spin {
+    uint64_t t0 = 0;
+    bool started = false;
+};
+__device__ bool spin_more(const Cw& c, Spin& sp, int pc) {
+    int stop = 0;
+    if (c.lane == 0) {
+        if (*reinterpret_cast<volatile int*>(c.sh.abort) || ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(c.p.err))) {
+            *reinterpret_cast<volatile int*>(c.sh.abort) = 1;
+            stop = 1;
+        } else {
+            const uint64_t now = globaltimer();
+            if (!sp.started) {
+                sp.t0 = now;
+                sp.started = true;
+            } else if (now - sp.t0 > c.p.timeout_ns) {
+                raise_error(c.p, c.sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, 0, c.p.tag);
+                stop = 1;
+            }
+        }
+    }
+    return __shfl_sync(0xFFFFFFFFu, stop, 0) == 0;
+}
+// warp-wide: lanes with `valid` read the tagged words a0 and a1 until both carry this step's tag
+__device__ bool wpoll2(const Cw& c, bool valid, const uint64_t* a0, const uint64_t* a1, float& v0, float& v1, int pc) {
+    Spin sp;
+    while (true) {
+        bool ok = true;
+        if (valid) {
+            const uint64_t w0 = ld_tag(a0), w1 = ld_tag(a1);
+            v0 = tag_val(w0);
+            v1 = tag_val(w1);
+            ok = tag_of(w0) == c.p.tag && tag_of(w1) == c.p.tag;
+        }
+        if (__all_sync(0xFFFFFFFFu, ok)) return true;
+        if (!spin_more(c, sp, pc)) return false;
+    }
+}
+// one thread: one tagged element (a thread of a divergent branch).  On abort or timeout the CTA's
+// abort flag is set and the value read last is returned; the caller's next wait then gives up.
+__device__ float poll1(const Params& p, const Shared& sh, const uint64_t* a, int pc) {
+    uint64_t w = ld_tag(a);
+    if (tag_of(w) == p.tag) return tag_val(w);
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        w = ld_tag(a);
+        if (tag_of(w) == p.tag) break;
+        if (*reinterpret_cast<volatile int*>(sh.abort) || ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(p.err))) {
+            *reinterpret_cast<volatile int*>(sh.abort) = 1;
+            break;
+        }
+        if (globaltimer() - t0 > p.timeout_ns) {
+            raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, tag_of(w), p.tag);
+            break;
+        }
+    }
+    return tag_val(w);
+}
+
+__device__ __forceinline__ void load8_bf16(const uint16_t* src, float* v) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+    v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+    v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+}
+// where a matvec input comes from: epoch-tagged activations (t), plain fp32 activations read after
+// an acquiring counter wait (f), or the bf16 embedding row of the step's token (b)
+struct XSrc {
+    const uint64_t* t;
+    const float* f;
+    const uint16_t* b;
+};
+__device__ __forceinline__ void load8f(const float* src, float* v) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+// eight elements from element e0 on; false when a tagged element does not yet carry `tag`
+__device__ __forceinline__ bool load8x(const XSrc& x, int e0, float* v, uint32_t tag) {
+    if (x.t) return ld8_tagged(x.t + e0, v, tag);
+    if (x.f) load8f(x.f + e0, v);
+    else load8_bf16(x.b + e0, v);
+    return true;
+}
+// eight elements' values, for a reader whose counter wait acquired (tagged words: values only,
+// four 16-byte loads of (value, tag, value, tag))
+__device__ __forceinline__ void load8v(const XSrc& x, int e0, float* v) {
+    if (x.t) {
+        const uint4* f = reinterpret_cast<const uint4*>(x.t + e0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 w = __ldcg(f + j);
+            v[2 * j] = __uint_as_float(w.x);
+            v[2 * j + 1] = __uint_as_float(w.z);
+        }
+    } else if (x.f) {
+        load8f(x.f + e0, v);
     } else {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(srcb + e0));
-        v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
-        v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+        load8_bf16(x.b + e0, v);
     }
 }
 
 // This warp's segment `seg` of the length-K input (lane owns chunks lane + 32 i), optionally
 // RMS-normalised: the sum of squares runs over all segments in a fixed order, so every warp
-// derives the same scale.
+// derives the same scale.  Segmented inputs are read after an acquiring counter wait (a tag poll
+// of a whole segment would not fit the registers next to x): values only, no tags.
 template <int CPL>
-__device__ void load_xw(const Cw& c, float (&xr)[8 * CPL], int K, int nseg, int seg, const float* srcf,
-                        const uint16_t* srcb, const uint16_t* gain) {
+__device__ bool load_xw(const Cw& c, float (&xr)[8 * CPL], int K, int nseg, int seg, const XSrc& src,
+                        const uint16_t* gain) {
     const int seglen = K / nseg, segch = seglen / 8;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
         const int ch = c.lane + 32 * i;
-        if (ch < segch) load8(srcf, srcb, seg * seglen + ch * 8, &xr[8 * i]);
+        if (ch < segch) load8v(src, seg * seglen + ch * 8, &xr[8 * i]);
         else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
         }
     }
-    if (!gain) return;
+    if (!gain) return true;
     float ss = 0.f;
-    for (int s = 0; s < nseg; ++s) {
+#pragma unroll 1
+    for (int s = 0; s < nseg; ++s) {   // (this warp's own segment is read again: same values)
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
             const int ch = c.lane + 32 * i;
             if (ch < segch) {
                 float v[8];
-                if (s == seg) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = xr[8 * i + e];
-                } else {
-                    load8(srcf, srcb, s * seglen + ch * 8, v);
-                }
+                load8v(src, s * seglen + ch * 8, v);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
             }
@@ -594,34 +731,53 @@ __device__ void load_xw(const Cw& c, float (&xr)[8 * CPL], int K, int nseg, int 
             xr[8 * i + 7] = (xr[8 * i + 7] * scale) * bf_hi(g.w);
         }
     }
+    return true;
 }
 
-// One input vector per CTA: warp 0 reads x (K <= kXBuf elements) from L2 once, computes the RMS
-// scale, and publishes both in shared memory; every warp then takes its chunks (lane + 32 i).
-// Cuts the L2 reads of a vector all 152 CTAs want at the same moment eightfold.  Every warp runs
-// this at every change of input (the key sequence is the same in all warps).
+// One input vector per CTA: the 8 consumer warps read x (K <= kXBuf elements) from L2 together --
+// thread t takes the 8-element chunks t, t + 256, ... and its RMSNorm gain in the same round
+// trip -- into shared memory, with one sum of squares per warp; after the CTA-wide arrival every
+// warp adds the 8 sums in warp order (the same scale everywhere) and takes its chunks
+// (lane + 32 i).  Every warp runs this at every change of input (the key sequence is the same in
+// all warps); xfree keeps a warp from overwriting a buffer another warp still reads.
 template <int CPL>
-__device__ bool shared_x(Cw& c, float (&xr)[8 * CPL], int K, const float* srcf, const uint16_t* srcb,
-                         const uint16_t* gain, int pc) {
+__device__ bool shared_x(Cw& c, float (&xr)[8 * CPL], int K, const XSrc& src, const uint16_t* gain, int pc) {
     const int segch = K / 8;
-    if (c.warp == 0) {
-        if (c.xphase > 0 && !wait_bar(c.p, c.sh, c.sh.xfree, (c.xphase - 1u) & 1u, ROLE_CONSUMER, pc)) return false;
-        float ss = 0.f;
-        for (int ch = c.lane; ch < segch; ch += 32) {
-            float v[8];
-            load8(srcf, srcb, ch * 8, v);
+    const int tid = c.warp * 32 + c.lane;
+    if (c.xphase > 0 && !wait_bar(c.p, c.sh, c.sh.xfree, (c.xphase - 1u) & 1u, ROLE_CONSUMER, pc)) return false;
+    float ss = 0.f;
+    for (int base = 0; base < segch; base += kConsumerThreads) {   // warp-uniform trip count
+        const int ch = base + tid;
+        const bool valid = ch < segch;
+        uint4 g = make_uint4(0u, 0u, 0u, 0u);
+        if (gain && valid) g = __ldg(reinterpret_cast<const uint4*>(gain + ch * 8));
+        float v[8];
+        Spin sp;
+        while (true) {
+            const bool ok = valid ? load8x(src, ch * 8, v, c.p.tag) : true;
+            if (__all_sync(0xFFFFFFFFu, ok)) break;
+            if (!spin_more(c, sp, pc)) return false;
+        }
+        if (valid) {
             *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8) = make_float4(v[0], v[1], v[2], v[3]);
             *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+            if (gain) *reinterpret_cast<uint4*>(c.sh.gbuf + ch * 8) = g;
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
         }
-        ss = warp_sum(ss);
-        if (c.lane == 0) c.sh.red[41] = gain ? rsqrtf(ss / float(K) + c.p.rms_eps) : 1.0f;
-        __syncwarp();
-        if (c.lane == 0) mbar_arrive(c.sh.xfull);
     }
+    ss = warp_sum(ss);
+    if (c.lane == 0) c.sh.red[48 + c.warp] = ss;
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(c.sh.xfull);
     if (!wait_bar(c.p, c.sh, c.sh.xfull, c.xphase & 1u, ROLE_CONSUMER, pc)) return false;
-    const float scale = c.sh.red[41];
+    float scale = 1.0f;
+    if (gain) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNumConsumerWarps; ++w) tot += c.sh.red[48 + w];
+        scale = rsqrtf(tot / float(K) + c.p.rms_eps);
+    }
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
         const int ch = c.lane + 32 * i;
@@ -631,7 +787,7 @@ __device__ bool shared_x(Cw& c, float (&xr)[8 * CPL], int K, const float* srcf, 
             float* x = &xr[8 * i];
             x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
             if (gain) {
-                const uint4 g = __ldg(reinterpret_cast<const uint4*>(gain + ch * 8));
+                const uint4 g = *reinterpret_cast<const uint4*>(c.sh.gbuf + ch * 8);
                 x[0] = (x[0] * scale) * bf_lo(g.x); x[1] = (x[1] * scale) * bf_hi(g.x);
                 x[2] = (x[2] * scale) * bf_lo(g.y); x[3] = (x[3] * scale) * bf_hi(g.y);
                 x[4] = (x[4] * scale) * bf_lo(g.z); x[5] = (x[5] * scale) * bf_hi(g.z);
@@ -649,20 +805,21 @@ __device__ bool shared_x(Cw& c, float (&xr)[8 * CPL], int K, const float* srcf, 
 }
 
 // output of one matvec row (run by one lane); `half` tells the two row units a warp carries apart
-__device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int b, int ru, int half, float s0, float s1) {
+__device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int ru, int half, float s0, float s1) {
     const Params& p = c.p;
     const int op = si.w[W_OP], l = si.w[W_LAYER], a0 = si.w[W_A0];
     const size_t lb = size_t(l) * p.B + b;
     const int row = a0 + ru;
     switch (op) {
-        case OP_QKV: p.qkv[lb * p.nqkv + row] = s0; break;
+        case OP_QKV: st_tag(p.qkv + lb * p.nqkv + row, s0, p.tag); break;
         case OP_OPROJ: {
-            const float res = (l == 0) ? bf16f(p.embed[size_t(p.tok[b]) * p.H + row]) : __ldcg(p.x_out + (lb - p.B) * p.H + row);
-            p.x_attn[lb * p.H + row] = res + s0;
+            const float res = (l == 0) ? bf16f(p.embed[size_t(p.tok[b]) * p.H + row])
+                                       : poll1(p, c.sh, p.x_out + (lb - p.B) * p.H + row, pc);
+            st_tag(p.x_attn + lb * p.H + row, res + s0, p.tag);
             break;
         }
-        case OP_UPGATE: p.h[lb * p.F + row] = s0 / (1.0f + expf(-s0)) * s1; break;
-        case OP_DOWN: p.x_out[lb * p.H + row] = __ldcg(p.x_attn + lb * p.H + row) + s0; break;
+        case OP_UPGATE: p.h[lb * p.F + row] = s0 / (1.0f + expf(-s0)) * s1; break;   // plain: read after acquire
+        case OP_DOWN: st_tag(p.x_out + lb * p.H + row, poll1(p, c.sh, p.x_attn + lb * p.H + row, pc) + s0, p.tag); break;
         default: {   // LM head: logit, then this warp half's running (max, lowest index) for the argmax
             p.logits[size_t(b) * p.V + row] = s0;
             const int slot = (c.warp * 2 + half) * kMaxBatch + b;
@@ -681,66 +838,67 @@ __device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int b, int ru, int 
 // row unit u's sum is done: emit it, or (split rows) leave this segment's partial and let the
 // last-arriving segment warp add the partials in segment order and emit the row
 __device__ void mv_finish(const Cw& c, const SlotInfo& si, int pc, int b, int u, int half, float s0, float s1) {
-    const bool pair = si.w[W_OP] == OP_UPGATE;
-    if (!si.split) {
-        mv_epilogue(c, si, b, u, half, s0, s1);
-        return;
-    }
-    const int nseg = si.nseg, seg = u & (nseg - 1), ru = u >> si.lognseg;
-    const int slot = pc % kSlots;
-    float* part = c.sh.comb + slot * kCombStride;
-    if (pair) { part[(ru * nseg + seg) * 2] = s0; part[(ru * nseg + seg) * 2 + 1] = s1; }
-    else part[ru * nseg + seg] = s0;
-    __threadfence_block();
-    if (atomicAdd(c.sh.combcnt + slot * kMaxRows + ru, 1) == nseg - 1) {
+    int ru = u;
+    if (si.split) {
+        const bool pair = si.w[W_OP] == OP_UPGATE;
+        const int nseg = si.nseg, seg = u & (nseg - 1);
+        ru = u >> si.lognseg;
+        const int slot = pc % kSlots;
+        float* part = c.sh.comb + slot * kCombStride;
+        if (pair) { part[(ru * nseg + seg) * 2] = s0; part[(ru * nseg + seg) * 2 + 1] = s1; }
+        else part[ru * nseg + seg] = s0;
         __threadfence_block();
-        float u0 = 0.f, u1 = 0.f;
+        if (atomicAdd(c.sh.combcnt + slot * kMaxRows + ru, 1) != nseg - 1) return;
+        __threadfence_block();
+        s0 = 0.f;
+        s1 = 0.f;
+#pragma unroll 1
         for (int s = 0; s < nseg; ++s) {
-            if (pair) { u0 += part[(ru * nseg + s) * 2]; u1 += part[(ru * nseg + s) * 2 + 1]; }
-            else u0 += part[ru * nseg + s];
+            if (pair) { s0 += part[(ru * nseg + s) * 2]; s1 += part[(ru * nseg + s) * 2 + 1]; }
+            else s0 += part[ru * nseg + s];
         }
         c.sh.combcnt[slot * kMaxRows + ru] = 0;
-        mv_epilogue(c, si, b, ru, half, u0, u1);
     }
+    mv_epilogue(c, si, pc, b, ru, half, s0, s1);
 }
 
 // two row segments (stream offsets o0, o1) dotted with x at once: 2*CPL independent 16-byte loads
 // per lane, then one butterfly that leaves the first sum in lanes 0-15 and the second in lanes
-// 16-31 (each bit-identical to a plain xor butterfly of that sum).
+// 16-31 (each bit-identical to a plain xor butterfly of that sum).  Without a second segment
+// (has1 false) the first one is dotted twice and the copy is dropped.
 template <int CPL>
 __device__ __forceinline__ float seg_dot2(const Cw& c, const SlotInfo& si, uint32_t o0, uint32_t o1, bool has1,
                                           const float (&xr)[8 * CPL]) {
     const int segch = si.segch;
     const uint32_t first = uint32_t(si.first_slot), sb = si.segbytes;
+    if (!has1) o1 = o0;
     const bool p0 = (o0 >> c.p.page_shift) == ((o0 + sb - 1u) >> c.p.page_shift);
     const bool p1 = (o1 >> c.p.page_shift) == ((o1 + sb - 1u) >> c.p.page_shift);
-    const uint8_t* b0 = ring_ptr(c.sh, c.p, first, o0) + c.lane * 16;
-    const uint8_t* b1 = ring_ptr(c.sh, c.p, first, o1) + c.lane * 16;
     float a[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
     if (p0 && p1 && segch == 32 * CPL) {   // whole segments inside one page each: plain strided loads
-        if (has1) {
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                const uint4 w0 = *reinterpret_cast<const uint4*>(b0 + i * 512);
-                const uint4 w1 = *reinterpret_cast<const uint4*>(b1 + i * 512);
-                a[i & 3] = dot8(w0, &xr[8 * i], a[i & 3]);
-                e[i & 3] = dot8(w1, &xr[8 * i], e[i & 3]);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) a[i & 3] = dot8(*reinterpret_cast<const uint4*>(b0 + i * 512), &xr[8 * i], a[i & 3]);
-        }
-    } else {
+        const uint8_t* b0 = ring_ptr(c.sh, c.p, first, o0) + c.lane * 16;
+        const uint8_t* b1 = ring_ptr(c.sh, c.p, first, o1) + c.lane * 16;
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
-            const int ch = c.lane + 32 * i;
-            const bool ok = ch < segch;
-            const uint4 w0 = ok ? *reinterpret_cast<const uint4*>(p0 ? b0 + i * 512 : ring_ptr(c.sh, c.p, first, o0 + uint32_t(ch) * 16u))
-                                : make_uint4(0, 0, 0, 0);
-            const uint4 w1 = (ok && has1) ? *reinterpret_cast<const uint4*>(p1 ? b1 + i * 512 : ring_ptr(c.sh, c.p, first, o1 + uint32_t(ch) * 16u))
-                                          : make_uint4(0, 0, 0, 0);
+            const uint4 w0 = *reinterpret_cast<const uint4*>(b0 + i * 512);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(b1 + i * 512);
             a[i & 3] = dot8(w0, &xr[8 * i], a[i & 3]);
             e[i & 3] = dot8(w1, &xr[8 * i], e[i & 3]);
+        }
+    } else {   // a segment crosses a page or is ragged: one segment at a time, chunk by chunk
+#pragma unroll 1
+        for (int r = 0; r < 2; ++r) {
+            const uint32_t o = r ? o1 : o0;
+            float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                const int ch = c.lane + 32 * i;
+                if (ch < segch)
+                    t[i & 3] = dot8(*reinterpret_cast<const uint4*>(ring_ptr(c.sh, c.p, first, o + uint32_t(ch) * 16u)),
+                                    &xr[8 * i], t[i & 3]);
+            }
+            if (r) { e[0] = t[0]; e[1] = t[1]; e[2] = t[2]; e[3] = t[3]; }
+            else { a[0] = t[0]; a[1] = t[1]; a[2] = t[2]; a[3] = t[3]; }
         }
     }
     const float s0 = (a[0] + a[1]) + (a[2] + a[3]);
@@ -766,25 +924,24 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc, float (&xr)[8 * C
     if (c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
     const int ufirst = (c.warp - int(c.rot)) & 7;
     for (int b = 0; b < p.B; ++b) {
-        const float* srcf = nullptr;
-        const uint16_t* srcb = nullptr;
+        XSrc src{nullptr, nullptr, nullptr};
         const uint16_t* gain = nullptr;
         const size_t lb = size_t(l) * p.B + b;
         switch (op) {
             case OP_QKV:
                 gain = c.sh.layers[l].attn_norm;
-                if (l == 0) srcb = p.embed + size_t(p.tok[b]) * p.H;
-                else srcf = p.x_out + (lb - p.B) * p.H;
+                if (l == 0) src.b = p.embed + size_t(p.tok[b]) * p.H;
+                else src.t = p.x_out + (lb - p.B) * p.H;
                 break;
-            case OP_OPROJ: srcf = p.o + lb * p.qd; break;
-            case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; srcf = p.x_attn + lb * p.H; break;
-            case OP_DOWN: srcf = p.h + lb * p.F; break;
-            default: gain = p.final_norm; srcf = p.x_out + (size_t(p.L - 1) * p.B + b) * p.H; break;
+            case OP_OPROJ: src.t = p.o + lb * p.qd; break;
+            case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; src.t = p.x_attn + lb * p.H; break;
+            case OP_DOWN: src.f = p.h + lb * p.F; break;
+            default: gain = p.final_norm; src.t = p.x_out + (size_t(p.L - 1) * p.B + b) * p.H; break;
         }
         if (nseg == 1 && si.K <= kXBuf) {   // every warp, even one without units in this tile
             const int key = (((op * 64 + (l & 63)) * kMaxBatch + b) * 8) + 1;
             if (key != xkey) {
-                if (!shared_x<CPL>(c, xr, si.K, srcf, srcb, gain, pc)) return false;
+                if (!shared_x<CPL>(c, xr, si.K, src, gain, pc)) return false;
                 xkey = key;
             }
         }
@@ -798,7 +955,7 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc, float (&xr)[8 * C
             for (int s = s_lo; s < s_hi; ++s) {
                 const int key = (((op * 64 + (l & 63)) * kMaxBatch + b) * 8 + s) + 1;
                 if (key != xkey) {
-                    load_xw<CPL>(c, xr, si.K, nseg, s, srcf, srcb, gain);
+                    load_xw<CPL>(c, xr, si.K, nseg, s, src, gain);
                     xkey = key;
                 }
                 const int r0 = si.split ? (u >> si.lognseg) : u;
@@ -811,11 +968,10 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc, float (&xr)[8 * C
                 t0 += __shfl_sync(0xFFFFFFFFu, v, 0);
                 t1 += __shfl_sync(0xFFFFFFFFu, v, 16);
             }
-            if (pair) {
-                if (c.lane == 0) mv_finish(c, si, pc, b, u, 0, t0, t1);
-            } else {
-                if (c.lane == 0) mv_finish(c, si, pc, b, u, 0, t0, 0.f);
-                if (two && c.lane == 16) mv_finish(c, si, pc, b, u1, 1, t1, 0.f);
+            // lane 0 emits unit u (with the up sum of a pair), lane 16 the second unit u1
+            if (c.lane == 0 || (two && c.lane == 16)) {
+                const bool lo = c.lane == 0;
+                mv_finish(c, si, pc, b, lo ? u : u1, lo ? 0 : 1, lo ? t0 : t1, pair ? t1 : 0.f);
             }
             __syncwarp();
         }
@@ -838,7 +994,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     const int tid = c.warp * 32 + c.lane;
     const int n_old = attn_old_rows(p, b, ch, C);
     const size_t lb = size_t(l) * p.B + b;
-    const float* qkv = p.qkv + lb * p.nqkv;
+    const uint64_t* qkv = p.qkv + lb * p.nqkv;
     float* sc = c.sh.ascr;   // [hpg][C] scores, then [hpg][n_chunk] combine factors
     if (n_old >= 0) {
         const int pos = p.pos[b];
@@ -846,32 +1002,50 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         const int n = n_old + (has_new ? 1 : 0);
         const float2* rp = p.rope + size_t(pos) * half;
         if (!cbar(c, pc)) return false;   // the previous block-level body is done with the scratch
-        // 1. rotate q of the group's heads; RoPE k, round k and v, append them
-        for (int idx = tid; idx < hpg * half; idx += kConsumerThreads) {
+        // 1. rotate q of the group's heads; RoPE k, round k and v, append them (q, k, v are
+        //    read until they carry this step's tag; loops run warp-uniform trip counts)
+        for (int base = c.warp * 32; base < hpg * half; base += kConsumerThreads) {
+            const int idx = base + c.lane;
+            const bool valid = idx < hpg * half;
             const int h = idx / half, i = idx % half;
-            const float* qh = qkv + size_t(g * hpg + h) * d;
-            const float q0 = __ldcg(qh + i), q1 = __ldcg(qh + i + half);
-            const float2 cs = rp[i];
-            c.sh.qrot[h * d + i] = q0 * cs.x - q1 * cs.y;
-            c.sh.qrot[h * d + i + half] = q0 * cs.y + q1 * cs.x;
+            const uint64_t* qh = qkv + size_t(g * hpg + h) * d;
+            float q0 = 0.f, q1 = 0.f;
+            if (!wpoll2(c, valid, qh + i, qh + i + half, q0, q1, pc)) return false;
+            if (valid) {
+                const float2 cs = rp[i];
+                c.sh.qrot[h * d + i] = q0 * cs.x - q1 * cs.y;
+                c.sh.qrot[h * d + i + half] = q0 * cs.y + q1 * cs.x;
+            }
         }
         if (has_new) {
             const size_t cache = size_t(b) * p.kv_bstride + size_t(l) * p.kv_lstride + size_t(g) * p.kv_hstride +
                                  size_t(pos) * d;
-            for (int i = tid; i < half; i += kConsumerThreads) {
-                const float* kh = qkv + p.qd + size_t(g) * d;
-                const float k0 = __ldcg(kh + i), k1 = __ldcg(kh + i + half);
-                const float2 cs = rp[i];
-                const uint16_t r0 = f2bf_rn(k0 * cs.x - k1 * cs.y), r1 = f2bf_rn(k0 * cs.y + k1 * cs.x);
-                c.sh.knew[i] = r0;
-                c.sh.knew[i + half] = r1;
-                p.kc[cache + i] = r0;
-                p.kc[cache + i + half] = r1;
+            const uint64_t* kh = qkv + p.qd + size_t(g) * d;
+            const uint64_t* vh = qkv + p.qd + p.kvd + size_t(g) * d;
+            for (int base = c.warp * 32; base < half; base += kConsumerThreads) {
+                const int i = base + c.lane;
+                const bool valid = i < half;
+                float k0 = 0.f, k1 = 0.f;
+                if (!wpoll2(c, valid, kh + i, kh + i + half, k0, k1, pc)) return false;
+                if (valid) {
+                    const float2 cs = rp[i];
+                    const uint16_t r0 = f2bf_rn(k0 * cs.x - k1 * cs.y), r1 = f2bf_rn(k0 * cs.y + k1 * cs.x);
+                    c.sh.knew[i] = r0;
+                    c.sh.knew[i + half] = r1;
+                    p.kc[cache + i] = r0;
+                    p.kc[cache + i + half] = r1;
+                }
             }
-            for (int i = tid; i < d; i += kConsumerThreads) {
-                const uint16_t r = f2bf_rn(__ldcg(qkv + p.qd + p.kvd + size_t(g) * d + i));
-                c.sh.vnew[i] = r;
-                p.vc[cache + i] = r;
+            for (int base = c.warp * 32; base < d; base += kConsumerThreads) {
+                const int i = base + c.lane;
+                const bool valid = i < d;
+                float v0 = 0.f, v1 = 0.f;
+                if (!wpoll2(c, valid, vh + i, vh + i, v0, v1, pc)) return false;
+                if (valid) {
+                    const uint16_t r = f2bf_rn(v0);
+                    c.sh.vnew[i] = r;
+                    p.vc[cache + i] = r;
+                }
             }
         }
         if (!wait_pages(c, si, pc)) return false;
@@ -916,9 +1090,11 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         if (c.warp < hpg) {
             const int h = c.warp;
             float m = -INFINITY;
+#pragma unroll 1
             for (int t = c.lane; t < n; t += 32) m = fmaxf(m, sc[h * C + t]);
             m = warp_max(m);
             float s = 0.f;
+#pragma unroll 1
             for (int t = c.lane; t < n; t += 32) {
                 const float e = expf(sc[h * C + t] - m);
                 sc[h * C + t] = e;
@@ -965,9 +1141,11 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     if (c.warp < hpg) {
         const int h = c.warp;
         float M = -INFINITY;
+#pragma unroll 1
         for (int k = c.lane; k < nact; k += 32) M = fmaxf(M, __ldcg(pbase + (size_t(k) * hpg + h) * (d + 2) + d));
         M = warp_max(M);
         float Ls = 0.f;
+#pragma unroll 1
         for (int k = c.lane; k < nact; k += 32) {
             const float* ph = pbase + (size_t(k) * hpg + h) * (d + 2);
             const float f = expf(__ldcg(ph + d) - M);
@@ -978,12 +1156,12 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         if (c.lane == 0) c.sh.cml[h] = Ls;
     }
     if (!cbar(c, pc)) return false;
-    float* out = p.o + lb * p.qd + size_t(g) * hpg * d;
+    uint64_t* out = p.o + lb * p.qd + size_t(g) * hpg * d;
     for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
         const int h = idx / d, e = idx % d;
         float acc = 0.f;
         for (int k = 0; k < nact; ++k) acc = fmaf(sc[h * p.n_chunk + k], __ldcg(pbase + (size_t(k) * hpg + h) * (d + 2) + e), acc);
-        out[idx] = acc / c.sh.cml[h];
+        st_tag(out + idx, acc / c.sh.cml[h], p.tag);
     }
     return true;
 }
@@ -1026,13 +1204,13 @@ __device__ bool argmax_tile(Cw& c, const SlotInfo& si, int pc) {
 
 // Counters seen satisfied by this warp: counters only grow within a launch, so a wait whose
 // target an earlier observation already covers needs neither a poll nor another acquire fence.
-struct CounterCache {
+struct CounterCache {   // the four waits seen last, newest first (static indexes: registers)
     int32_t id[4];
     int32_t need[4];
-    int next;
 };
 
-__device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* w, int pc, CounterCache& cc) {
+__device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* w, int pc, CounterCache& cc,
+                              bool acquire) {
     const int nw = w[W_NWAIT];
     bool polled = false;
     for (int i = 0; i < nw; ++i) {
@@ -1060,11 +1238,15 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
                 }
             }
         }
-        cc.id[cc.next] = cid;
-        cc.need[cc.next] = need;
-        cc.next = (cc.next + 1) & 3;
+#pragma unroll
+        for (int k = 3; k > 0; --k) {
+            cc.id[k] = cc.id[k - 1];
+            cc.need[k] = cc.need[k - 1];
+        }
+        cc.id[0] = cid;
+        cc.need[0] = need;
     }
-    if (polled) fence_acquire_gpu();   // acquire: producers' data is visible before this warp reads it
+    if (polled && acquire) fence_acquire_gpu();   // acquire: producers' data is visible before this warp reads it
     return true;
 }
 
@@ -1073,7 +1255,7 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
     Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u, 0u};
     float xr[8 * CPL];
     int xkey = -1;
-    CounterCache cc{{-1, -1, -1, -1}, {-1, -1, -1, -1}, 0};
+    CounterCache cc{{-1, -1, -1, -1}, {-1, -1, -1, -1}};
     for (int pc = 0;; ++pc) {
         const int slot = pc % kSlots;
         if (!wait_bar(p, sh, sh.ins_full + slot, (pc / kSlots) & 1, ROLE_CONSUMER, pc)) break;
@@ -1088,8 +1270,13 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
             if (gain && c.lane * 64 < p.H * 2)
                 for (int off = c.lane * 64; off < p.H * 2; off += 32 * 64)
                     asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(gain) + off));
+            // counters with acquire semantics in the counters mode and for the consumers that read
+            // their inputs without tags (the argmax over the LM-head partials; matvecs whose rows
+            // are cut into segments); otherwise the counters only say when to start reading -- the
+            // tags of the data decide, and a word read too early is read again
             int ok = 1;
-            if (c.lane == 0) ok = wait_counters(p, sh, si.w, pc, cc);
+            if (c.lane == 0)
+                ok = wait_counters(p, sh, si.w, pc, cc, p.sync_counters || ((p.acquire_ops >> op) & 1));
             if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
             if (threadIdx.x == 0) stamp(p, pc, 2);
             bool good;
@@ -1128,7 +1315,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
         mbar_init(sh.qfull + 0, 1);
         mbar_init(sh.qfull + 1, 1);
         mbar_init(sh.cbar, kNumConsumerWarps);
-        mbar_init(sh.xfull, 1);
+        mbar_init(sh.xfull, kNumConsumerWarps);
         mbar_init(sh.xfree, kNumConsumerWarps);
         *sh.abort = 0;
         *sh.issued = 0ull;

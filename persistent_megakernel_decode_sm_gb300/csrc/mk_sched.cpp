@@ -5,7 +5,7 @@
 // (principle, scheduling and data flow): every operator of a fixed Llama configuration is cut
 // into tiles, the tile dependency DAG is built, waves and a memory/compute pool are assigned,
 // and each SM's plan is tensorised into an instruction queue held in HBM for the life of the
-// kernel (object table: "per-SM instruction queue, [S,Q,32] int32-style encoding").
+// kernel (the page's object table gives the queue only as an int32 tensor of shape [S, Q, 32]).
 // The page fixes none of the concrete rules; this file states them:
 //  * tiles per layer: QKV row tiles (rows divide head_dim, so a tile lies inside one KV group's
 //    q, k or v range), attention chunks (sequence, group, chunk of attn_chunk positions),

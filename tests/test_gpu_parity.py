@@ -1,10 +1,11 @@
 """GPU parity of the megakernel against the CPU oracle, through the C ABI (libmk.so).
 
-Tolerances (stated by the task's success criterion for this decoder): logits within
+Tolerances (the parity criterion of this decoder): logits within
 max |error| <= 1e-2 * max |oracle logit| per sequence; the greedy token equal wherever the
 oracle's top-2 logit margin exceeds 0.05; appended K/V equal to the oracle's bf16 codes up to one
 unit in the last place (the fp32 sums behind them are ordered differently).  Outputs are
-bit-identical across SM counts and queue placements.
+bit-identical across SM counts, queue placements and the two synchronisation modes
+(epoch-tagged activations, completion counters).
 """
 import numpy as np
 import pytest
@@ -80,6 +81,7 @@ def test_device_timeout_is_reported_and_gpu_stays_usable():
     sm, slot = [(i, j) for i in range(q.shape[0]) for j in range(q.shape[1]) if q[i, j, 6] > 0][0]
     sched.patch(sm, slot, 8, int(q[sm, slot, 8]) + 1)
     dec = mk.Decoder(sched, s.weights, s.kv, timeout_ns=20_000_000)
+    dec.set_sync("counters")   # every instruction waits its counters
     with pytest.raises(mk.MkError) as ei:
         dec.step(s.tokens, s.pos)
     assert ei.value.status == mk.MK_ERR_TIMEOUT
@@ -101,6 +103,59 @@ def test_invalid_opcode_is_reported():
     with pytest.raises(mk.MkError) as ei:
         dec.step(s.tokens, s.pos)
     assert ei.value.status == mk.MK_ERR_OPCODE
+    dec.close()
+    s2 = make_setup("tiny")
+    dec2 = mk.Decoder(mk.Schedule(s2.cfg, mk.device_sm_count()), s2.weights, s2.kv)
+    _assert_parity(run_parity(s2, dec2, steps=1))
+
+
+def _steps(dec, s, n):
+    toks, pos = list(s.tokens), list(s.pos)
+    res = []
+    for _ in range(n):
+        nxt = dec.step(toks, pos)
+        res.append(dec.logits.cpu().clone())
+        toks, pos = nxt, [p + 1 for p in pos]
+    res.append(s.kv.k.cpu().clone())
+    res.append(s.kv.v.cpu().clone())
+    return res
+
+
+@pytest.mark.parametrize("name,steps", [("tiny", 3), ("llama1b_ctx512", 2)])
+def test_sync_modes_bit_identical(name, steps):
+    outs = []
+    for mode in ("tags", "counters"):
+        s = make_setup(name)
+        dec = mk.Decoder(mk.Schedule(s.cfg, mk.device_sm_count()), s.weights, s.kv)
+        dec.set_sync(mode)
+        outs.append(_steps(dec, s, steps))
+        dec.close()
+        del s
+        torch.cuda.empty_cache()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_tagged_wait_timeout_is_reported():
+    # shift the rows of one last-layer MLP-down tile onto its neighbour's: the tile still
+    # publishes its completion, so the LM-head tiles pass their counter waits, but some words of
+    # the final residual stream never receive this step's tag and the LM-head tiles, reading
+    # them, give up after the time budget (the argmax sits behind them: no other wait is open)
+    s = make_setup("tiny")
+    sched = mk.Schedule(s.cfg, 16)   # 16 queues: every one holds LM-head tiles
+    q = sched.queues()
+    am = [(i, j) for i in range(q.shape[0]) for j in range(q.shape[1]) if q[i, j, 0] == 8][0]
+    assert 7 in q[am[0], :am[1], 0], "the argmax must queue behind an LM-head tile"
+    last = s.cfg.n_layers - 1
+    sm, slot = [(i, j) for i in range(q.shape[0]) for j in range(q.shape[1])
+                if q[i, j, 0] == 6 and q[i, j, 1] == last and q[i, j, 3] == 0][0]
+    sched.patch(sm, slot, 3, int(q[sm, slot, 4]))
+    dec = mk.Decoder(sched, s.weights, s.kv, timeout_ns=20_000_000)
+    with pytest.raises(mk.MkError) as ei:
+        dec.step(s.tokens, s.pos)
+    assert ei.value.status == mk.MK_ERR_TIMEOUT
+    st, info = dec.status_code()
+    assert st == mk.MK_ERR_TIMEOUT and info[6] == 5, (st, info)   # a tagged-data poll gave up
     dec.close()
     s2 = make_setup("tiny")
     dec2 = mk.Decoder(mk.Schedule(s2.cfg, mk.device_sm_count()), s2.weights, s2.kv)
