@@ -55,14 +55,17 @@ typedef struct {
 } mk_model_cfg;
 
 /* Schedule knobs; pass NULL to mk_build_schedule for the defaults (each 0 field = default).
- * Tile geometry depends only on the model configuration and these knobs, never on sm_count. */
+ * At batch 1 with tile_bytes 0 every matvec operator is cut into about sm_count tiles (QKV tiles
+ * at most head_dim rows), each streamed through the page ring step by step; otherwise tiles hold
+ * about tile_bytes and must fit the ring.  A row's arithmetic never depends on the tiling. */
 typedef struct {
     int32_t page_bytes;  /* shared-memory page size (a power of two); default 32768             */
-    int32_t tile_bytes;  /* target weight bytes per matvec tile; default 131072                 */
+    int32_t tile_bytes;  /* 0: per-SM tiles at batch 1, 131072 at batch > 1; else the target
+                            weight bytes per matvec tile (capped at 8 rows for QKV, O and down,
+                            16 gate/up pairs, 32 LM-head rows)                                   */
     int32_t attn_chunk;  /* KV positions per split-K attention tile; default 64                 */
-    int32_t rows_qkv, rows_o, pairs_up, rows_down, rows_lm; /* explicit rows per tile (<= 32;
-                            pairs_up <= 16; rows_qkv must divide head_dim); 0 = from tile_bytes,
-                            capped at 8 rows for QKV, O and down, 16 pairs, 32 LM-head rows    */
+    int32_t rows_qkv, rows_o, pairs_up, rows_down, rows_lm; /* explicit rows (pairs) per tile,
+                            overriding the above; rows_qkv <= head_dim                           */
     uint64_t shuffle_seed; /* 0: cost-ordered placement; otherwise a seeded shuffled placement  */
 } mk_sched_opts;
 
@@ -160,21 +163,23 @@ typedef struct {
 mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, uint32_t* counters,
                   void* scratch, void* stream, mk_ctx** out);
 
-/* Time budget, in nanoseconds, of every single device wait (counter spin, tagged-data poll, page /
- * slot barrier).
+/* Time budget, in nanoseconds, of a single device wait: counter spins and tagged-data polls get
+ * ns, waits of the consumer warps on one another 2 ns, the loader's and publisher's waits (which
+ * only follow the consumers) 4 ns -- so the wait nearest the cause of a stall is the one recorded.
  * When one runs out the kernel records MK_ERR_TIMEOUT, every CTA leaves its loop after draining
  * its copies in flight, and the context is poisoned.  Default 2e9 (2 s). */
 mk_status mk_set_timeout(mk_ctx* c, uint64_t ns);
 
 /* How a consumer learns that the inputs of its instruction are ready.
  *  MK_SYNC_TAGS (default): the activation vectors one operator hands to the next (q/k/v,
- *    attention output, both residual streams, SwiGLU output) are epoch-tagged -- every element is
+ *    attention output, both residual streams) are epoch-tagged -- every element is
  *    one 64-bit word holding the fp32 value and the step's tag -- and a consumer polls the
  *    elements it reads until each carries this step's tag.  One read both proves readiness and
  *    fetches the data, so a dependency costs one memory round trip instead of the publisher's
  *    release fence, the counter add, the consumer's counter poll and then the data read.
- *    Counters are still published; they are awaited only where no tagged vector carries the
- *    dependency (the greedy argmax over the LM-head partials).
+ *    Counters are still polled first, as cheap doorbells; they keep acquire/release semantics
+ *    where a reader has no tag to check (the argmax over the LM-head partials, the MLP down
+ *    projection's SwiGLU input, matvec inputs cut into segments).
  *  MK_SYNC_COUNTERS: every instruction first waits all of its counters with acquire semantics
  *    (the page's protocol: wait the counters, run the body, fence, then add the completions); the tag checks then
  *    pass at the first read.

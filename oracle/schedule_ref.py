@@ -10,8 +10,9 @@ before an instruction and adds to counters after it.  The exact rules below are 
 reading of that outline (the page fixes none of them):
 
 Tiles (per layer l, in this order; ids are assigned in enumeration order):
-  QKV     rows [r, r+R_qkv) of Wqkv (q heads, k heads, v heads); R_qkv divides head_dim, so a
-          tile lies in one KV group's q, k or v range.  RMSNorm of the layer input is its prologue.
+  QKV     rows [r, r+R_qkv) of Wqkv (q heads, k heads, v heads); R_qkv <= head_dim, so a tile
+          touches one or two KV groups' q, k or v ranges and completes each group it touches.
+          RMSNorm of the layer input is its prologue.
   ATTN    (b, g, c): sequence b, KV group g, KV positions [c*C, (c+1)*C) -- split-K decode
           attention; c runs over ceil(max_seq / C) chunks (chunks past pos do no work).  Every
           chunk tile adds 1 to the group's arrival counter itself; the tile that completes the
@@ -26,9 +27,12 @@ Waves: the DAG's longest-path level; per layer QKV=5l, ATTN=5l+1, OPROJ=5l+2, UP
 DOWN=5l+4; LMHEAD=5L, ARGMAX=5L+1.
 Pools: memory pool = tiles that stream weights or KV (QKV, ATTN, OPROJ, UPGATE, DOWN,
 LMHEAD); compute pool = ARGMAX.  Within a wave memory tiles are placed before compute tiles.
+Rows per tile: at batch 1 (tile_bytes 0) about one tile per operator per SM -- such a tile
+streams through the page ring page by page; otherwise tiles of about tile_bytes.
 Assignment, wave by wave: memory tiles sorted by (cost desc, tile id asc), then compute tiles
-likewise; each tile goes to the SM with the smallest accumulated cost (ties: lowest SM id);
-the accumulated cost carries across waves.  cost = streamed bytes + TILE_OVERHEAD.
+likewise; each tile goes to the SM with the smallest accumulated cost (ties: lowest SM id) among
+the SMs holding fewer than ceil(n / S) of the n tiles of its pool in this wave; the accumulated
+cost carries across waves.  cost = streamed bytes + TILE_OVERHEAD.
 With a non-zero shuffle seed the wave's tiles are instead put in a splitmix64 Fisher-Yates
 order (pools still kept apart) -- the "shuffled assignment" used to test determinism.
 Queue of an SM: its tiles in assignment order, padded with END (all-zero words).
@@ -57,7 +61,7 @@ M64 = (1 << 64) - 1
 @dataclass
 class SchedOpts:
     page_bytes: int = 32768
-    tile_bytes: int = 131072
+    tile_bytes: int = 0     # 0: per-SM tiles at batch 1, 131072-byte tiles at batch > 1
     attn_chunk: int = 64
     shuffle_seed: int = 0
     rows_qkv: int = 0   # 0: derived from tile_bytes
@@ -67,17 +71,31 @@ class SchedOpts:
     rows_lm: int = 0
 
 
-def tile_rows(cfg, o: SchedOpts) -> Dict[str, int]:
-    H, F, d, qd = cfg.hidden, cfg.ffn, cfg.head_dim, cfg.n_q_heads * cfg.head_dim
+def tile_rows(cfg, o: SchedOpts, S: int) -> Dict[str, int]:
+    """Rows (pairs for gate/up) per matvec tile.  Batch 1 with tile_bytes 0: about one tile per
+    operator per SM (QKV tiles at most head_dim rows, so a tile touches one or two KV groups).
+    Otherwise tiles of about tile_bytes (default 131072).  Explicit rows_* override either."""
+    H, F, V, d = cfg.hidden, cfg.ffn, cfg.vocab, cfg.head_dim
+    qd = cfg.n_q_heads * cfg.head_dim
+    nqkv = qd + 2 * cfg.n_kv_heads * d
+    if cfg.batch == 1 and o.tile_bytes == 0:
+        R = dict(qkv=min(d, ceil_div(nqkv, S)), o=ceil_div(H, S), up=ceil_div(F, S),
+                 down=ceil_div(H, S), lm=ceil_div(V, S))
+    else:
+        tb = o.tile_bytes or 131072
 
-    def fit(limit, nbytes_per_row):
-        return max(1, min(limit, o.tile_bytes // nbytes_per_row))
+        def fit(limit, nbytes_per_row):
+            return max(1, min(limit, tb // nbytes_per_row))
 
-    r_qkv = o.rows_qkv or fit(8, 2 * H)
-    while d % r_qkv:
-        r_qkv -= 1
-    return dict(qkv=r_qkv, o=o.rows_o or fit(8, 2 * qd), up=o.pairs_up or fit(16, 4 * H),
-                down=o.rows_down or fit(8, 2 * F), lm=o.rows_lm or fit(32, 2 * H))
+        r_qkv = fit(8, 2 * H)
+        while d % r_qkv:
+            r_qkv -= 1
+        R = dict(qkv=r_qkv, o=fit(8, 2 * qd), up=fit(16, 4 * H), down=fit(8, 2 * F), lm=fit(32, 2 * H))
+    for k, v in (("qkv", o.rows_qkv), ("o", o.rows_o), ("up", o.pairs_up), ("down", o.rows_down),
+                 ("lm", o.rows_lm)):
+        if v:
+            R[k] = v
+    return R
 
 
 def ceil_div(a, b):
@@ -126,12 +144,12 @@ class Tile:
         return self.stream_bytes + TILE_OVERHEAD
 
 
-def enumerate_tiles(cfg, o: SchedOpts) -> Tuple[List[Tile], Counters, Dict[str, int]]:
+def enumerate_tiles(cfg, o: SchedOpts, S: int) -> Tuple[List[Tile], Counters, Dict[str, int]]:
     L, H, F, V, B = cfg.n_layers, cfg.hidden, cfg.ffn, cfg.vocab, cfg.batch
     nq, nkv, d = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     qd, kvd = nq * d, nkv * d
     hpg = nq // nkv
-    R = tile_rows(cfg, o)
+    R = tile_rows(cfg, o, S)
     C = o.attn_chunk
     nchunk = ceil_div(cfg.max_seq, C)
     cnt = Counters(cfg)
@@ -141,7 +159,6 @@ def enumerate_tiles(cfg, o: SchedOpts) -> Tuple[List[Tile], Counters, Dict[str, 
     n_up = ceil_div(F, R["up"])
     n_dn = ceil_div(H, R["down"])
     n_lm = ceil_div(V, R["lm"])
-    per_group_qkv = (hpg * d + 2 * d) // R["qkv"]
     tiles: List[Tile] = []
 
     def group_of_row(r):
@@ -151,18 +168,29 @@ def enumerate_tiles(cfg, o: SchedOpts) -> Tuple[List[Tile], Counters, Dict[str, 
             return (r - qd) // d
         return (r - qd - kvd) // d
 
+    # a QKV tile (<= head_dim rows) touches one or two KV groups and completes each of them
+    def groups_of_tile(r0, n):
+        g0, g1 = group_of_row(r0), group_of_row(r0 + n - 1)
+        return [g0] if g0 == g1 else [g0, g1]
+
+    qkv_tiles_of_group = [0] * nkv
+    for t in range(n_qkv):
+        r0 = t * R["qkv"]
+        for g in groups_of_tile(r0, min(R["qkv"], n_qkv_rows - r0)):
+            qkv_tiles_of_group[g] += 1
+
     for l in range(L):
         wq = [] if l == 0 else [(cnt.down(l - 1), n_dn)]
         for t in range(n_qkv):
             r0 = t * R["qkv"]
             n = min(R["qkv"], n_qkv_rows - r0)
             tiles.append(Tile(QKV, l, 0, r0, n, 0, 5 * l, list(wq),
-                              [(cnt.qkv(l, group_of_row(r0)), 1)], n * H * 2))
+                              [(cnt.qkv(l, g), 1) for g in groups_of_tile(r0, n)], n * H * 2))
         for b in range(B):
             for g in range(nkv):
                 for c in range(nchunk):
                     tiles.append(Tile(ATTN, l, b, g, c, C, 5 * l + 1,
-                                      [(cnt.qkv(l, g), per_group_qkv)],
+                                      [(cnt.qkv(l, g), qkv_tiles_of_group[g])],
                                       [(cnt.comb(l), 1)], 2 * C * d * 2,
                                       arrive=cnt.attn(l, b, g), arrive_n=nchunk))
         for t in range(n_o):
@@ -213,6 +241,15 @@ def _shuffle(xs: List[Tile], rng: SplitMix64) -> List[Tile]:
     return xs
 
 
+def tile_pages(t: Tile, cfg, o: SchedOpts) -> int:
+    """Pages of a tile's stream: gate/up tiles stream page-sized row groups, gate and up pages
+    alternating; every other tile streams its bytes contiguously."""
+    if t.op == UPGATE:
+        rpp = o.page_bytes // (2 * cfg.hidden)
+        return 2 * ceil_div(t.a1, rpp)
+    return ceil_div(t.stream_bytes, o.page_bytes)
+
+
 def encode(t: Tile, n_pages: int) -> List[int]:
     w = [0] * WORDS
     w[0], w[1], w[2], w[3], w[4], w[5] = t.op, t.layer, t.b, t.a0, t.a1, t.a2
@@ -235,30 +272,36 @@ def build_schedule(cfg, S: int, opts: Optional[SchedOpts] = None):
     o = opts or SchedOpts()
     if S < 1:
         raise ValueError("sm_count must be >= 1")
-    tiles, cnt, R = enumerate_tiles(cfg, o)
+    tiles, cnt, R = enumerate_tiles(cfg, o, S)
     by_wave: Dict[int, List[Tile]] = {}
     for t in tiles:
         by_wave.setdefault(t.wave, []).append(t)
     rng = SplitMix64(o.shuffle_seed) if o.shuffle_seed else None
-    heap = [(0, s) for s in range(S)]
+    # each tile, in order, to the SM with the smallest accumulated cost (ties: lowest SM) among
+    # those holding fewer than ceil(n / S) of the wave's tiles of its pool
+    acc = np.zeros(S, dtype=np.int64)
     per_sm: List[List[Tile]] = [[] for _ in range(S)]
     for wv in sorted(by_wave):
         mem = [t for t in by_wave[wv] if t.memory]
         cmp_ = [t for t in by_wave[wv] if not t.memory]
         if rng is None:
-            order = (sorted(mem, key=lambda t: (-t.cost, t.tid))
-                     + sorted(cmp_, key=lambda t: (-t.cost, t.tid)))
+            pools = [sorted(mem, key=lambda t: (-t.cost, t.tid)), sorted(cmp_, key=lambda t: (-t.cost, t.tid))]
         else:
-            order = _shuffle(mem, rng) + _shuffle(cmp_, rng)
-        for t in order:
-            acc, s = heapq.heappop(heap)
-            per_sm[s].append(t)
-            heapq.heappush(heap, (acc + t.cost, s))
+            pools = [_shuffle(mem, rng), _shuffle(cmp_, rng)]
+        for pool in pools:
+            cap = ceil_div(len(pool), S)
+            in_wave = np.zeros(S, dtype=np.int64)
+            big = np.iinfo(np.int64).max
+            for t in pool:
+                s = int(np.argmin(np.where(in_wave < cap, acc, big)))   # first minimum: lowest SM
+                per_sm[s].append(t)
+                acc[s] += t.cost
+                in_wave[s] += 1
     Q = 1 + max(len(q) for q in per_sm)
     queues = np.zeros((S, Q, WORDS), dtype=np.int32)
     for s in range(S):
         for i, t in enumerate(per_sm[s]):
-            queues[s, i] = encode(t, ceil_div(t.stream_bytes, o.page_bytes))
+            queues[s, i] = encode(t, tile_pages(t, cfg, o))
     totals = np.zeros(cnt.n, dtype=np.uint64)
     for t in tiles:
         if t.arrive >= 0:
@@ -299,15 +342,15 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
       non-decreasing wave order (the forward-progress rule: a waiter never holds an SM that a
       producer it waits on still needs);
     * (DAG + per-SM program order) is acyclic -- implied by the two previous points;
-    * capacity: at most 4 waits and 2 completions per instruction; no instruction needs more pages
-      than the ring holds.
+    * capacity: at most 4 waits and 2 completions per instruction; at batch > 1 no instruction
+      needs more pages than the ring holds.
     """
     o = opts or SchedOpts()
     errs: List[str] = []
     S, Q, W = queues.shape
     if W != WORDS:
         return [f"instruction width {W} != {WORDS}"]
-    ref_tiles, cnt, _ = enumerate_tiles(cfg, o)
+    ref_tiles, cnt, _ = enumerate_tiles(cfg, o, S)
     seen: Dict[int, Tuple[int, int]] = {}
     pub_sum = np.zeros(cnt.n, dtype=np.int64)
     producer_wave: Dict[int, int] = {}
@@ -347,7 +390,9 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
                 pw = producer_wave.setdefault(c, t.wave)
                 if pw != t.wave:
                     errs.append(f"counter {c} produced in waves {pw} and {t.wave}")
-            if page_bytes_capacity is not None and w[20] * o.page_bytes > page_bytes_capacity:
+            # batch > 1 consumers hold a tile's pages until the tile is done: it must fit the ring
+            # (at batch 1 a tile streams through the ring page by page)
+            if page_bytes_capacity is not None and cfg.batch > 1 and w[20] * o.page_bytes > page_bytes_capacity:
                 errs.append(f"tile {t.tid}: needs {w[20]} pages, ring too small")
             ref = ref_tiles[t.tid] if 0 <= t.tid < len(ref_tiles) else None
             if ref is None or (ref.op, ref.layer, ref.b, ref.a0, ref.a1, ref.a2) != \
@@ -402,9 +447,12 @@ def _reads_writes(t: Tile, cfg):
         if l > 0:
             R.append((("x_out", l - 1), H))
         qd, kvd = nq * d, nkv * d
-        r = t.a0
-        g = (r // d) // hpg if r < qd else ((r - qd) // d if r < qd + kvd else (r - qd - kvd) // d)
-        W.append((("qkv", l, g), t.a1))
+
+        def group(r):
+            return (r // d) // hpg if r < qd else ((r - qd) // d if r < qd + kvd else (r - qd - kvd) // d)
+
+        for r in range(t.a0, t.a0 + t.a1):   # rows counted per KV group (a tile may touch two)
+            W.append((("qkv", l, group(r)), 1))
     elif op == ATTN:
         R.append((("qkv", l, t.a0), (hpg + 2) * d))
         W.append((("part", l, t.b, t.a0), 1))

@@ -103,34 +103,34 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, std::
         const bool head = op == OP_LMHEAD || op == OP_ARGMAX;
         if (head ? l != L : unsigned(l) >= unsigned(L)) return bad("layer");
         if (unsigned(b) >= unsigned(B)) return bad("sequence");
-        auto rows = [&](int total, int maxn) { return a0 >= 0 && a1 >= 1 && a1 <= maxn && a0 + a1 <= total; };
+        auto rows = [&](int total, int maxn) { return a0 >= 0 && a1 >= 1 && a1 <= maxn && int64_t(a0) + a1 <= total; };
         const void* src0 = nullptr;
         const void* src1 = nullptr;
         int64_t b0 = 0, b1 = 0;
         switch (op) {
             case OP_QKV:
-                if (!rows(nqkv, kMaxRows)) return bad("rows");
+                if (!rows(nqkv, c.head_dim)) return bad("rows");
                 src0 = static_cast<const uint8_t*>(w->wqkv[l]) + int64_t(a0) * H * 2;
                 b0 = int64_t(a1) * H * 2;
                 break;
             case OP_OPROJ:
-                if (!rows(H, kMaxRows)) return bad("rows");
+                if (!rows(H, H)) return bad("rows");
                 src0 = static_cast<const uint8_t*>(w->wo[l]) + int64_t(a0) * qd * 2;
                 b0 = int64_t(a1) * qd * 2;
                 break;
             case OP_UPGATE:
-                if (!rows(F, kMaxRows / 2)) return bad("rows");
+                if (!rows(F, F)) return bad("rows");
                 src0 = static_cast<const uint8_t*>(w->wgate_up[l]) + int64_t(a0) * H * 2;
                 src1 = static_cast<const uint8_t*>(w->wgate_up[l]) + int64_t(F + a0) * H * 2;
                 b0 = b1 = int64_t(a1) * H * 2;
                 break;
             case OP_DOWN:
-                if (!rows(H, kMaxRows)) return bad("rows");
+                if (!rows(H, H)) return bad("rows");
                 src0 = static_cast<const uint8_t*>(w->wdown[l]) + int64_t(a0) * F * 2;
                 b0 = int64_t(a1) * F * 2;
                 break;
             case OP_LMHEAD:
-                if (!rows(V, kMaxRows) || unsigned(a2) >= unsigned(g.n_lm)) return bad("rows");
+                if (!rows(V, V) || unsigned(a2) >= unsigned(g.n_lm)) return bad("rows");
                 src0 = static_cast<const uint8_t*>(w->lm_head) + int64_t(a0) * H * 2;
                 b0 = int64_t(a1) * H * 2;
                 break;
@@ -145,7 +145,9 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, std::
             default: break;
         }
         if (src0) {
-            if ((b0 + b1 + g.page_bytes - 1) / g.page_bytes > x[W_NPAGES]) return bad("page count");
+            const int64_t rpp = g.page_bytes / (2ll * H);   // gate/up: row groups, gate and up pages alternating
+            const int64_t pages = op == OP_UPGATE ? 2 * ((a1 + rpp - 1) / rpp) : (b0 + b1 + g.page_bytes - 1) / g.page_bytes;
+            if (pages != x[W_NPAGES] || b0 + b1 > (int64_t(1) << 31) - 1) return bad("page count");
             put64(x + W_SRC0, src0);
             put64(x + W_SRC1, src1);
             x[W_BYTES0] = int32_t(b0);
@@ -211,8 +213,28 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
     if (n_pages < 1) return fail(MK_ERR_CAPACITY, "no room for a page ring");
     int misc = smem_misc_bytes(n_pages, asf, qrf);
     while (n_pages > 0 && int64_t(n_pages) * g.page_bytes + misc > optin) misc = smem_misc_bytes(--n_pages, asf, qrf);
-    if (n_pages < std::max(2, s->max_pages))
-        return fail(MK_ERR_CAPACITY, "page ring of %d pages cannot hold a tile of %d pages", n_pages, s->max_pages);
+    // capacity: at batch > 1 a tile's pages are held until it is done, so the ring must hold the
+    // largest tile; at batch 1 matvec tiles stream step by step (16 row segments, or 8 gate/up
+    // pairs, per step): the ring must hold the pages of one step (+1 for a straddled boundary) and
+    // an attention tile
+    int need_pages = 2;
+    if (c.batch > 1) {
+        need_pages = std::max(need_pages, s->max_pages);
+    } else {
+        auto seg_bytes = [&](int K) {
+            int nseg = 1;
+            while (K > 2048 * nseg) nseg <<= 1;
+            return int64_t(K) * 2 / nseg;
+        };
+        const int64_t pb = g.page_bytes;
+        for (int K : {H, qd, c.ffn})   // non-pair steps: 16 units of at most one row segment each
+            need_pages = std::max<int64_t>(need_pages, (16 * seg_bytes(K) + pb - 1) / pb + 1);
+        const int64_t rpp = pb / (2ll * H);   // gate/up: 8 pairs -> row groups of rpp rows, two pages each
+        need_pages = std::max<int64_t>(need_pages, 2 * ((8 + rpp - 1) / rpp + 1));
+        need_pages = std::max<int64_t>(need_pages, (2ll * g.attn_chunk * d * 2 + pb - 1) / pb);
+    }
+    if (n_pages < need_pages)
+        return fail(MK_ERR_CAPACITY, "page ring of %d pages cannot hold the %d pages a step needs", n_pages, need_pages);
     const int smem = n_pages * g.page_bytes + misc;
     CK(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     int per_sm = 0;

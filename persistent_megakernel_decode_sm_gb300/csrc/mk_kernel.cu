@@ -198,7 +198,7 @@ struct Shared {
     uint16_t* gbuf;    // [kXBuf] its RMSNorm gain (bf16)
     float2* lmbest;    // [8 warps][kMaxBatch] LM-head running (max, index)
     float* comb;       // [kSlots][64] split-row segment partials
-    int* combcnt;      // [kSlots][8]
+    int* combcnt;      // [kSlots][kMaxRows] split-row slot: owning row << 8 | arrivals, -1 free
     int* pubinfo;      // [kDone][8]: opcode, #completions, (counter, delta) x 2
     float* red;        // [16] argmax scratch
     int* abort;        // [1]
@@ -262,6 +262,15 @@ __device__ void raise_error(const Params& p, const Shared& sh, int code, int rol
     *reinterpret_cast<volatile int*>(sh.abort) = 1;
 }
 
+// Time budget of a wait by its role.  Waits that can name the cause of a stall (a counter, a
+// tagged element) get the configured budget; waits on this CTA's own consumers (consumer
+// barriers) twice that, and the loader's and publisher's waits, which only follow the consumers,
+// four times: the wait closest to the cause runs out first and is the one recorded.
+__device__ __forceinline__ uint64_t budget(const Params& p, int role) {
+    return role == ROLE_LOADER || role == ROLE_PUBLISHER ? 4ull * p.timeout_ns
+         : role == ROLE_CONSUMER ? 2ull * p.timeout_ns : p.timeout_ns;
+}
+
 // bounded mbarrier wait: false when the CTA aborts or the budget runs out (error recorded)
 // (the waiting thread sleeps in hardware between checks of the abort flag and the time budget)
 __device__ __noinline__ bool wait_bar_slow(const Params& p, const Shared& sh, uint64_t* bar, uint32_t parity, int role,
@@ -270,7 +279,7 @@ __device__ __noinline__ bool wait_bar_slow(const Params& p, const Shared& sh, ui
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*reinterpret_cast<volatile int*>(sh.abort)) return false;
-        if (globaltimer() - t0 > p.timeout_ns) {
+        if (globaltimer() - t0 > budget(p, role)) {
             raise_error(p, sh, MK_ERR_TIMEOUT, role, pc, -1, 0, 0);
             return false;
         }
@@ -291,6 +300,8 @@ struct Stream {
     int nseg;
     uint32_t total;
     int pages;
+    int inter;                       // gate/up tile: page 2j = gate rows [j rpp, (j+1) rpp), 2j+1 = up rows
+    uint32_t rows, rowbytes, rpp;    // (interleaved streams)
 };
 
 __device__ __forceinline__ int attn_old_rows(const Params& p, int b, int c, int chunk) {
@@ -314,6 +325,8 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
     st.nseg = 0;
     st.total = 0;
     st.pages = 0;
+    st.inter = 0;
+    st.rows = st.rowbytes = st.rpp = 0;
     const int op = w[W_OP];
     if (is_matvec(op)) {
         const uint32_t b0 = uint32_t(w[W_BYTES0]), b1 = uint32_t(w[W_BYTES1]);
@@ -322,6 +335,16 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
         st.nseg = b1 ? 2 : 1;
         st.total = b0 + b1;
         if (b0 == 0) return MK_ERR_BOUNDS;
+        if (op == OP_UPGATE) {   // pair rows of gate and up in adjacent pages
+            st.inter = 1;
+            st.rows = uint32_t(w[W_A1]);
+            st.rowbytes = uint32_t(p.H) * 2u;
+            st.rpp = uint32_t(p.page_bytes) / st.rowbytes;
+            if (st.rpp == 0 || b0 != st.rows * st.rowbytes || b1 != b0) return MK_ERR_BOUNDS;
+            st.pages = int(2u * ((st.rows + st.rpp - 1u) / st.rpp));
+            if (st.pages > w[W_NPAGES]) return MK_ERR_CAPACITY;
+            return MK_OK;
+        }
     } else if (op == OP_ATTN) {
         const int l = w[W_LAYER], b = w[W_B], g = w[W_A0], c = w[W_A1], C = w[W_A2];
         if (unsigned(l) >= unsigned(p.L) || unsigned(b) >= unsigned(p.B) || unsigned(g) >= unsigned(p.nkv) ||
@@ -341,7 +364,9 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
         return MK_ERR_OPCODE;
     }
     st.pages = int((st.total + uint32_t(p.page_bytes) - 1u) >> p.page_shift);
-    if (st.pages > w[W_NPAGES] || st.pages > p.n_pages) return MK_ERR_CAPACITY;
+    // a tile whose consumers hold all its pages at once (attention; every tile at batch > 1) must
+    // fit the ring; batch-1 matvec tiles stream through it
+    if (st.pages > w[W_NPAGES] || ((op == OP_ATTN || p.B > 1) && st.pages > p.n_pages)) return MK_ERR_CAPACITY;
     return MK_OK;
 }
 
@@ -395,7 +420,7 @@ __device__ void loader(const Params& p, const Shared& sh) {
         if (is_matvec(si.w[W_OP])) {   // shape of the op (bind-time table) and of this tile
             const MvShape& m = p.mv[si.w[W_OP]];
             const int n = si.w[W_A1];
-            const bool split = p.B == 1 && m.nseg > 1 && n * m.nseg * (si.w[W_OP] == OP_UPGATE ? 2 : 1) <= kCombStride;
+            const bool split = p.B == 1 && m.nseg > 1;   // segments of a row on different warps
             si.K = m.K;
             si.nseg = m.nseg;
             si.lognseg = m.lognseg;
@@ -411,7 +436,7 @@ __device__ void loader(const Params& p, const Shared& sh) {
             while (pc - *reinterpret_cast<volatile int*>(sh.published) >= kDone) {
                 __nanosleep(200);
                 if (*reinterpret_cast<volatile int*>(sh.abort)) { stalled = true; break; }
-                if (globaltimer() - t0 > p.timeout_ns) {
+                if (globaltimer() - t0 > budget(p, ROLE_LOADER)) {
                     raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_LOADER, pc, -1, 0, 0);
                     stalled = true;
                     break;
@@ -436,16 +461,24 @@ __device__ void loader(const Params& p, const Shared& sh) {
                 stop = true;
                 break;
             }
-            const uint32_t lo = uint32_t(pg) * PB;
-            const uint32_t hi = min(lo + PB, st.total);
-            mbar_arrive_expect_tx(sh.full + ps, hi - lo);
             uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
+            if (st.inter) {   // one row group of gate (even page) or up (odd page)
+                const uint32_t r0 = uint32_t(pg >> 1) * st.rpp;
+                const uint32_t bytes = min(st.rpp, st.rows - r0) * st.rowbytes;
+                mbar_arrive_expect_tx(sh.full + ps, bytes);
+                bulk_g2s(dst, ((pg & 1) ? st.seg[1].src : st.seg[0].src) + size_t(r0) * st.rowbytes, bytes, sh.full + ps,
+                         pol);
+            } else {
+                const uint32_t lo = uint32_t(pg) * PB;
+                const uint32_t hi = min(lo + PB, st.total);
+                mbar_arrive_expect_tx(sh.full + ps, hi - lo);
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {   // (static indexes: the stream stays in registers)
-                if (s >= st.nseg) break;
-                const uint32_t a = max(lo, st.seg[s].off);
-                const uint32_t z = min(hi, st.seg[s].off + st.seg[s].bytes);
-                if (a < z) bulk_g2s(dst + (a - lo), st.seg[s].src + (a - st.seg[s].off), z - a, sh.full + ps, pol);
+                for (int s = 0; s < 2; ++s) {   // (static indexes: the stream stays in registers)
+                    if (s >= st.nseg) break;
+                    const uint32_t a = max(lo, st.seg[s].off);
+                    const uint32_t z = min(hi, st.seg[s].off + st.seg[s].bytes);
+                    if (a < z) bulk_g2s(dst + (a - lo), st.seg[s].src + (a - st.seg[s].off), z - a, sh.full + ps, pol);
+                }
             }
             ++page_seq;
             if (++cur_slot == NP) { cur_slot = 0; cur_phase ^= 1u; }
@@ -824,40 +857,55 @@ __device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int 
             p.logits[size_t(b) * p.V + row] = s0;
             const int slot = (c.warp * 2 + half) * kMaxBatch + b;
             float2 best = c.sh.lmbest[slot];
-            if (s0 > best.x || (s0 == best.x && row < __float_as_int(best.y))) {
-                best = make_float2(s0, __int_as_float(row));
-                c.sh.lmbest[slot] = best;
-            }
-            p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * (2 * kNumConsumerWarps) + c.warp * 2 + half] =
-                make_int4(__float_as_int(best.x), __float_as_int(best.y), int(p.epoch), 0);
-            break;
+            if (s0 > best.x || (s0 == best.x && row < __float_as_int(best.y)))
+                c.sh.lmbest[slot] = make_float2(s0, __int_as_float(row));
+            break;   // (the tile's end writes the warp half's running best to lm_part)
         }
     }
 }
 
 // row unit u's sum is done: emit it, or (split rows) leave this segment's partial and let the
-// last-arriving segment warp add the partials in segment order and emit the row
+// last-arriving segment warp add the partials in segment order and emit the row.  Split rows use
+// slot ru mod cap of the instruction's partial area; the slot's word holds the owning row (high
+// bits) and the arrivals so far (low 8 bits), -1 when free.  A warp that runs ahead waits
+// (bounded) for an earlier row to free its slot; the slowest warp never waits: every row of an
+// earlier step already has all its segments.
 __device__ void mv_finish(const Cw& c, const SlotInfo& si, int pc, int b, int u, int half, float s0, float s1) {
     int ru = u;
     if (si.split) {
         const bool pair = si.w[W_OP] == OP_UPGATE;
-        const int nseg = si.nseg, seg = u & (nseg - 1);
+        const int nseg = si.nseg, seg = u & (nseg - 1), per = pair ? 2 : 1;
         ru = u >> si.lognseg;
         const int slot = pc % kSlots;
-        float* part = c.sh.comb + slot * kCombStride;
-        if (pair) { part[(ru * nseg + seg) * 2] = s0; part[(ru * nseg + seg) * 2 + 1] = s1; }
-        else part[ru * nseg + seg] = s0;
+        const int cap = kCombStride / (nseg * per);            // a power of two, <= kMaxRows
+        const int rs = ru & (cap - 1);
+        int* word = c.sh.combcnt + slot * kMaxRows + rs;
+        float* part = c.sh.comb + slot * kCombStride + rs * nseg * per;
+        uint64_t t0 = 0;
+        while (true) {
+            const int w = atomicCAS(word, -1, ru << 8);
+            if (w == -1 || (w >> 8) == ru) break;
+            if (*reinterpret_cast<volatile int*>(c.sh.abort)) return;
+            if (t0 == 0) t0 = globaltimer();
+            else if (globaltimer() - t0 > budget(c.p, ROLE_CONSUMER)) {
+                raise_error(c.p, c.sh, MK_ERR_TIMEOUT, ROLE_CONSUMER, pc, -1, uint32_t(w), uint32_t(ru));
+                return;
+            }
+        }
+        if (pair) { part[seg * 2] = s0; part[seg * 2 + 1] = s1; }
+        else part[seg] = s0;
         __threadfence_block();
-        if (atomicAdd(c.sh.combcnt + slot * kMaxRows + ru, 1) != nseg - 1) return;
+        if ((atomicAdd(word, 1) & 0xFF) != nseg - 1) return;
         __threadfence_block();
         s0 = 0.f;
         s1 = 0.f;
 #pragma unroll 1
         for (int s = 0; s < nseg; ++s) {
-            if (pair) { s0 += part[(ru * nseg + s) * 2]; s1 += part[(ru * nseg + s) * 2 + 1]; }
-            else s0 += part[ru * nseg + s];
+            if (pair) { s0 += part[s * 2]; s1 += part[s * 2 + 1]; }
+            else s0 += part[s];
         }
-        c.sh.combcnt[slot * kMaxRows + ru] = 0;
+        __threadfence_block();
+        atomicExch(word, -1);   // the slot is free for the row cap rows later
     }
     mv_epilogue(c, si, pc, b, ru, half, s0, s1);
 }
@@ -867,10 +915,10 @@ __device__ void mv_finish(const Cw& c, const SlotInfo& si, int pc, int b, int u,
 // 16-31 (each bit-identical to a plain xor butterfly of that sum).  Without a second segment
 // (has1 false) the first one is dotted twice and the copy is dropped.
 template <int CPL>
-__device__ __forceinline__ float seg_dot2(const Cw& c, const SlotInfo& si, uint32_t o0, uint32_t o1, bool has1,
-                                          const float (&xr)[8 * CPL]) {
+__device__ __forceinline__ float seg_dot2(const Cw& c, const SlotInfo& si, uint32_t first, uint32_t o0, uint32_t o1,
+                                          bool has1, const float (&xr)[8 * CPL]) {
     const int segch = si.segch;
-    const uint32_t first = uint32_t(si.first_slot), sb = si.segbytes;
+    const uint32_t sb = si.segbytes;
     if (!has1) o1 = o0;
     const bool p0 = (o0 >> c.p.page_shift) == ((o0 + sb - 1u) >> c.p.page_shift);
     const bool p1 = (o1 >> c.p.page_shift) == ((o1 + sb - 1u) >> c.p.page_shift);
@@ -912,17 +960,46 @@ __device__ __forceinline__ float seg_dot2(const Cw& c, const SlotInfo& si, uint3
 
 // Matvec tile (QKV / O / gate-up / down / LM-head rows).  Unit u of the tile (a row, a gate/up
 // pair, or a row segment) goes to warp (u + rot) mod 8, where rot rotates with every tile so
-// short tiles spread over all warps; a warp handles its units two row segments at a time.
+// short tiles spread over all warps; a warp handles its units two row segments at a time, in
+// steps of 16 units (8 gate/up pairs) taken in stream order.  At batch 1 the tile streams: a warp
+// waits only for the pages of its next step and gives back every page no later step reads, so a
+// tile may be far larger than the page ring.  At batch > 1 every sequence reads every page: the
+// tile's pages are held until it is done.  Gate/up tiles arrive interleaved: page 2j holds gate
+// rows [j rpp, (j + 1) rpp), page 2j + 1 the matching up rows.
 template <int CPL>
 __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc, float (&xr)[8 * CPL], int& xkey) {
     const Params& p = c.p;
-    const int op = si.w[W_OP], l = si.w[W_LAYER], n = si.w[W_A1];
+    const int op = si.w[W_OP], l = si.w[W_LAYER];
     const bool pair = op == OP_UPGATE;
     const int U = si.units, nseg = si.nseg;
     const uint32_t rowbytes = si.rowbytes, segbytes = si.segbytes;
-    if (!wait_pages(c, si, pc)) return false;
+    const uint32_t PB = uint32_t(p.page_bytes), NP = uint32_t(p.n_pages);
+    const uint32_t rpp = PB / rowbytes;   // gate/up: rows per page
+    const bool stream = p.B == 1;
+    if (!stream && !wait_pages(c, si, pc)) return false;
     if (c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
     const int ufirst = (c.warp - int(c.rot)) & 7;
+    const int per_step = pair ? 8 : 16;
+    const int nsteps = (U + per_step - 1) / per_step;
+    // stream offset of segment s of unit u's row (a pair: its gate row; the up row is a page later)
+    auto unit_off = [&](int u, int s) -> uint32_t {
+        const uint32_t row = uint32_t(si.split ? (u >> si.lognseg) : u);
+        if (pair) return (row / rpp) * 2u * PB + (row % rpp) * rowbytes + uint32_t(s) * segbytes;
+        return row * rowbytes + uint32_t(s) * segbytes;
+    };
+    auto first_page = [&](int k) -> int {   // first page step k reads
+        const int u0 = k * per_step;
+        return int(unit_off(u0, si.split ? (u0 & (nseg - 1)) : 0) >> p.page_shift);
+    };
+    auto last_page = [&](int k) -> int {    // last page step k reads
+        const int u1 = min(U, (k + 1) * per_step) - 1;
+        if (pair) return int(unit_off(u1, si.split ? (u1 & (nseg - 1)) : 0) >> p.page_shift) + 1;
+        return int((unit_off(u1, si.split ? (u1 & (nseg - 1)) : nseg - 1) + segbytes - 1u) >> p.page_shift);
+    };
+    // page trackers (batch 1): next page to wait, next page to release, page whose slot is `bslot`
+    int waited = 0, released = 0, based = 0;
+    uint32_t wslot = uint32_t(si.first_slot), wph = uint32_t(si.first_phase);
+    uint32_t rslot = wslot, bslot = wslot;
     for (int b = 0; b < p.B; ++b) {
         XSrc src{nullptr, nullptr, nullptr};
         const uint16_t* gain = nullptr;
@@ -945,40 +1022,87 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc, float (&xr)[8 * C
                 xkey = key;
             }
         }
-        // (a gate/up pair is already two row segments: one unit per step; otherwise units u, u+8)
-        for (int u = ufirst; u < U; u += pair ? 8 : 16) {
-            const int u1 = u + 8;
-            const bool two = !pair && u1 < U;
-            const int s_lo = si.split ? (u & (nseg - 1)) : 0;
-            const int s_hi = si.split ? s_lo + 1 : nseg;
-            float t0 = 0.f, t1 = 0.f;
-            for (int s = s_lo; s < s_hi; ++s) {
-                const int key = (((op * 64 + (l & 63)) * kMaxBatch + b) * 8 + s) + 1;
-                if (key != xkey) {
-                    load_xw<CPL>(c, xr, si.K, nseg, s, src, gain);
-                    xkey = key;
+        for (int k = 0; k < nsteps; ++k) {
+            uint32_t first = uint32_t(si.first_slot), obase = 0;
+            if (stream) {   // this step's pages
+                const int pa = first_page(k), pb = last_page(k);
+                for (; waited <= pb; ++waited) {
+                    if (!wait_bar(p, c.sh, c.sh.full + wslot, wph, ROLE_CONSUMER, pc)) return false;
+                    if (++wslot == NP) { wslot = 0; wph ^= 1u; }
                 }
-                const int r0 = si.split ? (u >> si.lognseg) : u;
-                const uint32_t off0 = uint32_t(r0) * rowbytes + uint32_t(s) * segbytes;
-                uint32_t off1;
-                if (pair) off1 = off0 + uint32_t(n) * rowbytes;                 // the up row of the pair
-                else off1 = uint32_t(si.split ? (u1 >> si.lognseg) : u1) * rowbytes + uint32_t(s) * segbytes;
-                const float v = seg_dot2<CPL>(c, si, off0, off1, pair || two, xr);
-                // lanes 0-15 hold the first sum, lanes 16-31 the second
-                t0 += __shfl_sync(0xFFFFFFFFu, v, 0);
-                t1 += __shfl_sync(0xFFFFFFFFu, v, 16);
+                for (; based < pa; ++based)
+                    if (++bslot == NP) bslot = 0;
+                first = bslot;
+                obase = uint32_t(pa) * PB;
             }
-            // lane 0 emits unit u (with the up sum of a pair), lane 16 the second unit u1
-            if (c.lane == 0 || (two && c.lane == 16)) {
-                const bool lo = c.lane == 0;
-                mv_finish(c, si, pc, b, lo ? u : u1, lo ? 0 : 1, lo ? t0 : t1, pair ? t1 : 0.f);
+            // (a gate/up pair is already two row segments: one unit per step; otherwise u, u + 8)
+            const int u = k * per_step + ufirst;
+            if (u < U) {
+                const int u1 = u + 8;
+                const bool two = !pair && u1 < U;
+                const int s_lo = si.split ? (u & (nseg - 1)) : 0;
+                const int s_hi = si.split ? s_lo + 1 : nseg;
+                float t0 = 0.f, t1 = 0.f;
+                for (int s = s_lo; s < s_hi; ++s) {
+                    const int key = (((op * 64 + (l & 63)) * kMaxBatch + b) * 8 + s) + 1;
+                    if (key != xkey) {
+                        load_xw<CPL>(c, xr, si.K, nseg, s, src, gain);
+                        xkey = key;
+                    }
+                    const uint32_t off0 = unit_off(u, s) - obase;
+                    const uint32_t off1 = pair ? off0 + PB : (two ? unit_off(u1, s) - obase : off0);
+                    const float v = seg_dot2<CPL>(c, si, first, off0, off1, pair || two, xr);
+                    // lanes 0-15 hold the first sum, lanes 16-31 the second
+                    t0 += __shfl_sync(0xFFFFFFFFu, v, 0);
+                    t1 += __shfl_sync(0xFFFFFFFFu, v, 16);
+                }
+                // lane 0 emits unit u (with the up sum of a pair), lane 16 the second unit u1
+                if (c.lane == 0 || (two && c.lane == 16)) {
+                    const bool lo = c.lane == 0;
+                    mv_finish(c, si, pc, b, lo ? u : u1, lo ? 0 : 1, lo ? t0 : t1, pair ? t1 : 0.f);
+                }
+            }
+            if (stream) {   // give back the pages no later step of this tile reads
+                const int pn = min(k + 1 < nsteps ? first_page(k + 1) : si.n_pages, waited);
+                __syncwarp();
+                if (c.lane == 0) {
+                    uint32_t rs = rslot;
+                    for (int i = released; i < pn; ++i) {
+                        mbar_arrive(c.sh.empty + rs);
+                        if (++rs == NP) rs = 0;
+                    }
+                }
+                for (; released < pn; ++released)
+                    if (++rslot == NP) rslot = 0;
             }
             __syncwarp();
         }
     }
     if (c.warp == 0 && c.lane == 0) stamp(p, pc, 7);
+    if (stream) {   // pages no step read (none in a well-formed tile): wait for them, then give back
+        for (; waited < si.n_pages; ++waited) {
+            if (!wait_bar(p, c.sh, c.sh.full + wslot, wph, ROLE_CONSUMER, pc)) return false;
+            if (++wslot == NP) { wslot = 0; wph ^= 1u; }
+        }
+        __syncwarp();
+        if (c.lane == 0)
+            for (int i = released; i < si.n_pages; ++i) {
+                mbar_arrive(c.sh.empty + rslot);
+                if (++rslot == NP) rslot = 0;
+            }
+        __syncwarp();
+    } else {
+        release_pages(c, si);
+    }
+    if (op == OP_LMHEAD && (c.lane & 15) == 0) {   // this warp half's running (max, lowest index)
+        const int half = c.lane >> 4;
+        for (int b = 0; b < p.B; ++b) {
+            const float2 best = c.sh.lmbest[(c.warp * 2 + half) * kMaxBatch + b];
+            p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * (2 * kNumConsumerWarps) + c.warp * 2 + half] =
+                make_int4(__float_as_int(best.x), __float_as_int(best.y), int(p.epoch), 0);
+        }
+    }
     c.rot = (c.rot + uint32_t(U)) & 7u;
-    release_pages(c, si);
     return true;
 }
 
@@ -1323,7 +1447,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
     }
     for (int i = threadIdx.x; i < kNumConsumerWarps * 2 * kMaxBatch; i += blockDim.x)
         sh.lmbest[i] = make_float2(-INFINITY, __int_as_float(0x7FFFFFFF));
-    for (int i = threadIdx.x; i < kSlots * kMaxRows; i += blockDim.x) sh.combcnt[i] = 0;
+    for (int i = threadIdx.x; i < kSlots * kMaxRows; i += blockDim.x) sh.combcnt[i] = -1;   // split-row slots free
     for (int i = threadIdx.x; i < p.L; i += blockDim.x) sh.layers[i] = p.layers[i];
     if (threadIdx.x == 0) stamp(p, 0, 5);
     __syncthreads();

@@ -7,8 +7,8 @@
 // and each SM's plan is tensorised into an instruction queue held in HBM for the life of the
 // kernel (the page's object table gives the queue only as an int32 tensor of shape [S, Q, 32]).
 // The page fixes none of the concrete rules; this file states them:
-//  * tiles per layer: QKV row tiles (rows divide head_dim, so a tile lies inside one KV group's
-//    q, k or v range), attention chunks (sequence, group, chunk of attn_chunk positions),
+//  * tiles per layer: QKV row tiles (<= head_dim rows: a tile touches one or two KV groups and
+//    completes each), attention chunks (sequence, group, chunk of attn_chunk positions),
 //    combine per (sequence, group), O row tiles, gate/up row-pair tiles, down row tiles; then
 //    LM-head row tiles and one argmax per sequence;
 //  * DAG: a consumer waits on one counter per producer set -- QKV(l) on down(l-1), attention
@@ -20,9 +20,12 @@
 //    point only at lower waves (forward-progress contract);
 //  * pools: memory = tiles that stream weights or KV, compute = argmax; within a wave memory
 //    tiles are placed first;
+//  * rows per tile: at batch 1 about one tile per operator per SM (streamed through the page
+//    ring page by page), otherwise about tile_bytes per tile;
 //  * placement: within a wave, tiles in (cost desc, id asc) order -- or a seeded splitmix64
 //    Fisher-Yates order when shuffle_seed != 0 -- each to the queue with the smallest
-//    accumulated cost (ties to the lowest SM), the accumulated cost carried across waves;
+//    accumulated cost (ties to the lowest SM) among the queues holding fewer than ceil(n / S)
+//    of the wave's n tiles of that pool, the accumulated cost carried across waves;
 //    cost = streamed bytes + a fixed per-tile overhead.
 #include <algorithm>
 #include <cstdarg>
@@ -119,32 +122,47 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     if (opts) o = *opts;
     Geometry g{};
     g.page_bytes = o.page_bytes ? o.page_bytes : 32768;
-    g.tile_bytes = o.tile_bytes ? o.tile_bytes : 131072;
+    g.tile_bytes = o.tile_bytes;   // 0: matvec tiles sized per SM (batch 1) / 131072 bytes (batch > 1)
     g.attn_chunk = o.attn_chunk ? o.attn_chunk : 64;
     g.shuffle_seed = o.shuffle_seed;
     if (g.page_bytes < 1024 || g.page_bytes % 128 || g.page_bytes > (1 << 20))
         return fail(MK_ERR_ARG, "page_bytes must be a multiple of 128 in [1024, 1 MiB]");
-    if (g.tile_bytes < 16) return fail(MK_ERR_ARG, "tile_bytes too small");
+    if (g.tile_bytes != 0 && g.tile_bytes < 16) return fail(MK_ERR_ARG, "tile_bytes too small");
     if (g.attn_chunk < 1 || g.attn_chunk > 1024) return fail(MK_ERR_ARG, "attn_chunk out of [1, 1024]");
 
     const int32_t L = c.n_layers, H = c.hidden, F = c.ffn, V = c.vocab, B = c.batch;
     const int32_t nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim, hpg = nq / nkv;
     const int32_t qd = nq * d, kvd = nkv * d, nqkv = qd + 2 * kvd;
 
-    // default rows per tile: the tile_bytes target, capped so QKV and O stay fine-grained (they are
-    // small per layer and gate the attention); gate/up, down and LM-head tiles carry more rows
-    g.r_qkv = o.rows_qkv ? o.rows_qkv : fit(8, g.tile_bytes, 2ll * H);
-    if (!o.rows_qkv)
+    // rows per tile.  Batch 1 (tile_bytes 0): about one tile per operator per SM -- a tile streams
+    // through the page ring page by page, so it need not fit the ring, and the per-tile costs
+    // (dispatch, input vector, first touch of its pages, completion) are paid once per operator
+    // and SM.  QKV tiles keep <= head_dim rows (a tile then touches at most two KV groups).
+    // Batch > 1 or an explicit tile_bytes: tiles of about tile_bytes, which must fit the ring.
+    if (B == 1 && g.tile_bytes == 0) {
+        g.r_qkv = std::min(d, cdiv(nqkv, S));
+        g.r_o = cdiv(H, S);
+        g.r_up = cdiv(F, S);
+        g.r_dn = cdiv(H, S);
+        g.r_lm = cdiv(V, S);
+    } else {
+        const int64_t tb = g.tile_bytes ? g.tile_bytes : 131072;
+        g.r_qkv = fit(8, tb, 2ll * H);
         while (d % g.r_qkv) --g.r_qkv;
-    g.r_o = o.rows_o ? o.rows_o : fit(8, g.tile_bytes, 2ll * qd);
-    g.r_up = o.pairs_up ? o.pairs_up : fit(kMaxRows / 2, g.tile_bytes, 4ll * H);
-    g.r_dn = o.rows_down ? o.rows_down : fit(8, g.tile_bytes, 2ll * F);
-    g.r_lm = o.rows_lm ? o.rows_lm : fit(kMaxRows, g.tile_bytes, 2ll * H);
-    if (g.r_qkv < 1 || g.r_qkv > kMaxRows || d % g.r_qkv)
-        return fail(MK_ERR_ARG, "rows_qkv must divide head_dim and be <= %d", kMaxRows);
-    if (g.r_o < 1 || g.r_o > kMaxRows || g.r_dn < 1 || g.r_dn > kMaxRows || g.r_lm < 1 || g.r_lm > kMaxRows ||
-        g.r_up < 1 || g.r_up > kMaxRows / 2)
-        return fail(MK_ERR_ARG, "rows per tile out of range (<= %d rows, <= %d pairs)", kMaxRows, kMaxRows / 2);
+        g.r_o = fit(8, tb, 2ll * qd);
+        g.r_up = fit(16, tb, 4ll * H);
+        g.r_dn = fit(8, tb, 2ll * F);
+        g.r_lm = fit(32, tb, 2ll * H);
+    }
+    if (o.rows_qkv) g.r_qkv = o.rows_qkv;
+    if (o.rows_o) g.r_o = o.rows_o;
+    if (o.pairs_up) g.r_up = o.pairs_up;
+    if (o.rows_down) g.r_dn = o.rows_down;
+    if (o.rows_lm) g.r_lm = o.rows_lm;
+    if (g.r_qkv < 1 || g.r_qkv > d) return fail(MK_ERR_ARG, "rows_qkv must be in [1, head_dim]");
+    if (g.r_o < 1 || g.r_up < 1 || g.r_lm < 1 || g.r_dn < 1) return fail(MK_ERR_ARG, "rows per tile must be >= 1");
+    if (g.page_bytes < 2 * H)   // gate/up tiles stream whole rows per page
+        return fail(MK_ERR_ARG, "page_bytes %d holds no gate/up row (%d bytes)", g.page_bytes, 2 * H);
     g.n_qkv = cdiv(nqkv, g.r_qkv);
     g.n_o = cdiv(H, g.r_o);
     g.n_up = cdiv(F, g.r_up);
@@ -153,7 +171,6 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     g.n_chunk = cdiv(c.max_seq, g.attn_chunk);
     CounterMap cm(c);
     g.n_counters = cm.count();
-    const int32_t per_group_qkv = (hpg * d + 2 * d) / g.r_qkv;
 
     // ---- tiles in enumeration order (ids) ------------------------------------------------
     std::vector<Tile> tiles;
@@ -176,19 +193,35 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         if (r < qd + kvd) return (r - qd) / d;
         return (r - qd - kvd) / d;
     };
+    // QKV tiles of <= head_dim rows touch one or two KV groups (ranges are >= head_dim rows):
+    // a tile completes every group it touches; attention of a group waits for all of them
+    std::vector<int32_t> qkv_tiles_of_group(nkv, 0);
+    for (int32_t t = 0; t < g.n_qkv; ++t) {
+        const int32_t r0 = t * g.r_qkv, n = std::min(g.r_qkv, nqkv - r0);
+        const int32_t g0 = group_of_row(r0), g1 = group_of_row(r0 + n - 1);
+        ++qkv_tiles_of_group[g0];
+        if (g1 != g0) ++qkv_tiles_of_group[g1];
+    }
     for (int32_t l = 0; l < L; ++l) {
         for (int32_t t = 0; t < g.n_qkv; ++t) {
             int32_t r0 = t * g.r_qkv, n = std::min(g.r_qkv, nqkv - r0);
+            const int32_t g0 = group_of_row(r0), g1 = group_of_row(r0 + n - 1);
             if (l == 0)
-                add(OP_QKV, l, 0, r0, n, 0, 5 * l, {}, {cm.qkv(l, group_of_row(r0)), 1}, int64_t(n) * H * 2);
+                add(OP_QKV, l, 0, r0, n, 0, 5 * l, {}, {cm.qkv(l, g0), 1}, int64_t(n) * H * 2);
             else
-                add(OP_QKV, l, 0, r0, n, 0, 5 * l, {{cm.down(l - 1), g.n_dn}}, {cm.qkv(l, group_of_row(r0)), 1},
+                add(OP_QKV, l, 0, r0, n, 0, 5 * l, {{cm.down(l - 1), g.n_dn}}, {cm.qkv(l, g0), 1},
                     int64_t(n) * H * 2);
+            if (g1 != g0) {
+                Tile& tq = tiles.back();
+                tq.pub[1][0] = cm.qkv(l, g1);
+                tq.pub[1][1] = 1;
+                tq.npub = 2;
+            }
         }
         for (int32_t b = 0; b < B; ++b)
             for (int32_t gr = 0; gr < nkv; ++gr)
                 for (int32_t ch = 0; ch < g.n_chunk; ++ch) {
-                    add(OP_ATTN, l, b, gr, ch, g.attn_chunk, 5 * l + 1, {{cm.qkv(l, gr), per_group_qkv}},
+                    add(OP_ATTN, l, b, gr, ch, g.attn_chunk, 5 * l + 1, {{cm.qkv(l, gr), qkv_tiles_of_group[gr]}},
                         {cm.comb(l), 1}, int64_t(2) * g.attn_chunk * d * 2);
                     tiles.back().arrive = cm.attn(l, b, gr);
                     tiles.back().arrive_n = g.n_chunk;
@@ -214,9 +247,11 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         add(OP_ARGMAX, L, b, 0, g.n_lm, 0, 5 * L + 1, {{cm.lm(), g.n_lm}}, {cm.fin(), 1}, 0);
 
     // ---- placement ------------------------------------------------------------------------
-    using Slot = std::pair<int64_t, int32_t>;  // (accumulated cost, sm)
-    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-    for (int32_t s = 0; s < S; ++s) heap.push({0, s});
+    // each tile, in order, to the SM with the smallest accumulated cost (ties: lowest SM) among
+    // those holding fewer than ceil(n / S) of the wave's tiles of this pool (a wave is spread over
+    // the SMs before any SM takes a second tile of it)
+    std::vector<int64_t> acc(S, 0);
+    std::vector<int32_t> in_wave(S, 0);
     std::vector<std::vector<int32_t>> per_sm(S);
     SplitMix64 rng{g.shuffle_seed};
     size_t i = 0;
@@ -240,13 +275,18 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         };
         order(mem);
         order(cmp);
-        for (auto* v : {&mem, &cmp})
+        for (auto* v : {&mem, &cmp}) {
+            const int32_t cap = cdiv(int64_t(v->size()), S);
+            std::fill(in_wave.begin(), in_wave.end(), 0);
             for (int32_t id : *v) {
-                Slot sl = heap.top();
-                heap.pop();
-                per_sm[sl.second].push_back(id);
-                heap.push({sl.first + tiles[id].cost(), sl.second});
+                int32_t best = -1;
+                for (int32_t s = 0; s < S; ++s)
+                    if (in_wave[s] < cap && (best < 0 || acc[s] < acc[best])) best = s;
+                per_sm[best].push_back(id);
+                acc[best] += tiles[id].cost();
+                ++in_wave[best];
             }
+        }
         i = j;
     }
 
@@ -271,7 +311,10 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
             for (int q = 0; q < t.nwait; ++q) { w[W_WAIT + 2 * q] = t.wait[q][0]; w[W_WAIT + 2 * q + 1] = t.wait[q][1]; }
             w[W_NPUB] = t.npub;
             for (int q = 0; q < t.npub; ++q) { w[W_PUB + 2 * q] = t.pub[q][0]; w[W_PUB + 2 * q + 1] = t.pub[q][1]; }
-            int64_t pages = (t.stream_bytes + g.page_bytes - 1) / g.page_bytes;
+            // gate/up tiles stream page-sized row groups, gate and up pages alternating
+            const int64_t rpp = g.page_bytes / (2ll * H);
+            int64_t pages = t.op == OP_UPGATE ? 2 * ((t.a1 + rpp - 1) / rpp)
+                                              : (t.stream_bytes + g.page_bytes - 1) / g.page_bytes;
             if (pages > (1 << 20)) { delete sch; return fail(MK_ERR_CAPACITY, "tile too large"); }
             w[W_NPAGES] = int32_t(pages);
             w[W_TILE] = t.id;
@@ -289,7 +332,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
 
     // ---- structural validation (waits point at lower waves; queues in wave order) ------------
     std::vector<int32_t> prod_wave(g.n_counters, -1);
-    for (const Tile& t : tiles) prod_wave[t.pub[0][0]] = t.wave;
+    for (const Tile& t : tiles)
+        for (int q = 0; q < t.npub; ++q) prod_wave[t.pub[q][0]] = t.wave;
     for (const Tile& t : tiles)
         for (int q = 0; q < t.nwait; ++q) {
             int32_t cid = t.wait[q][0];

@@ -37,7 +37,9 @@ def test_build_schedule_rejects_bad_arguments():
     with pytest.raises(mk.MkError):
         mk.Schedule(small_config(batch=9), 4)
     with pytest.raises(mk.MkError):
-        mk.Schedule(small_config(), 4, rows_qkv=7)        # must divide head_dim
+        mk.Schedule(small_config(), 4, rows_qkv=65)       # more rows than head_dim
+    with pytest.raises(mk.MkError):
+        mk.Schedule(small_config(hidden=1024), 4, page_bytes=1024)   # holds no gate/up row
     with pytest.raises(mk.MkError):
         mk.Schedule(small_config(), 4, page_bytes=1000)
 

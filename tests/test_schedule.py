@@ -51,9 +51,10 @@ def test_schedule_valid_and_deadlock_free(name, S, seed):
     assert sr.simulate(q, t, cfg, n_epochs=2, seed=seed) == []
 
 
-def test_schedule_tiles_cover_every_row_once():
-    cfg = get_workload("tiny").cfg
-    tiles, cnt, R = sr.enumerate_tiles(cfg, sr.SchedOpts())
+@pytest.mark.parametrize("name,S", [("tiny", 152), ("tiny", 7), ("llama1b_ctx512", 152), ("llama1b_batch8", 152)])
+def test_schedule_tiles_cover_every_row_once(name, S):
+    cfg = get_workload(name).cfg
+    tiles, cnt, R = sr.enumerate_tiles(cfg, sr.SchedOpts(), S)
     for op, total in ((sr.QKV, cfg.qkv_rows), (sr.OPROJ, cfg.hidden), (sr.UPGATE, cfg.ffn),
                       (sr.DOWN, cfg.hidden), (sr.LMHEAD, cfg.vocab)):
         for l in (range(cfg.n_layers) if op != sr.LMHEAD else [cfg.n_layers]):
@@ -62,6 +63,18 @@ def test_schedule_tiles_cover_every_row_once():
                 if t.op == op and t.layer == l:
                     rows[t.a0:t.a0 + t.a1] += 1
             assert np.all(rows == 1)
+
+
+def test_batch1_wave_spread_one_matvec_tile_per_sm():
+    # at batch 1 every matvec operator has at most S tiles and no SM holds two tiles of a wave
+    cfg = get_workload("llama1b_ctx512").cfg
+    S = 152
+    q, t, _ = sr.build_schedule(cfg, S)
+    for s in range(S):
+        waves = [int(w[22]) for w in q[s] if w[0] != sr.END]
+        assert len(waves) == len(set(waves)), f"sm {s} holds two tiles of one wave"
+    n_up = sum(1 for s in range(S) for w in q[s] if w[0] == sr.UPGATE and w[1] == 0)
+    assert n_up == S
 
 
 def _mutate(q, fn):
