@@ -227,10 +227,17 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
             return int64_t(K) * 2 / nseg;
         };
         const int64_t pb = g.page_bytes;
-        for (int K : {H, qd, c.ffn})   // non-pair steps: 16 units of at most one row segment each
-            need_pages = std::max<int64_t>(need_pages, (16 * seg_bytes(K) + pb - 1) / pb + 1);
+        // pages one step can touch: a span of `bytes` starting at a multiple of `bytes` covers
+        // ceil(bytes / pb) pages when the two sizes divide one another, else one more
+        auto span = [&](int64_t bytes) {
+            const int64_t n = (bytes + pb - 1) / pb;
+            return (bytes % pb == 0 || pb % bytes == 0) ? n : n + 1;
+        };
+        for (int K : {H, qd, c.ffn})   // non-pair steps: 16 units of one row segment each
+            need_pages = std::max<int64_t>(need_pages, span(16 * seg_bytes(K)));
         const int64_t rpp = pb / (2ll * H);   // gate/up: 8 pairs -> row groups of rpp rows, two pages each
-        need_pages = std::max<int64_t>(need_pages, 2 * ((8 + rpp - 1) / rpp + 1));
+        need_pages = std::max<int64_t>(need_pages, 2 * ((rpp % 8 == 0 || 8 % rpp == 0) ? std::max<int64_t>(1, 8 / rpp)
+                                                                                       : (8 + rpp - 1) / rpp + 1));
         need_pages = std::max<int64_t>(need_pages, (2ll * g.attn_chunk * d * 2 + pb - 1) / pb);
     }
     if (n_pages < need_pages)

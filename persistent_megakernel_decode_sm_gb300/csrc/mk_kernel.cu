@@ -967,7 +967,11 @@ __device__ __forceinline__ float seg_dot2(const Cw& c, const SlotInfo& si, uint3
 // tile's pages are held until it is done.  Gate/up tiles arrive interleaved: page 2j holds gate
 // rows [j rpp, (j + 1) rpp), page 2j + 1 the matching up rows.
 template <int CPL>
-__device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc, float (&xr)[8 * CPL], int& xkey) {
+__device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc) {
+    // this warp's input in registers, (re)loaded by the tile: its registers are free outside
+    // matvec tiles (a batch-1 SM runs about one tile per operator, each with a new input)
+    float xr[8 * CPL];
+    int xkey = -1;
     const Params& p = c.p;
     const int op = si.w[W_OP], l = si.w[W_LAYER];
     const bool pair = op == OP_UPGATE;
@@ -1262,19 +1266,30 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     if (!reinterpret_cast<volatile int*>(c.sh.red)[40]) return true;
     const int nact = min(p.n_chunk, p.pos[b] / C + 1);
     const float* pbase = p.part + (lb * p.nkv + g) * size_t(p.n_chunk) * hpg * (d + 2);
+    // the group's active partials are one contiguous block; when it fits the shared-x and gain
+    // buffers (free during attention: the tile began with every warp past its previous input) it
+    // is staged there in one round trip, and the combine below reads shared memory
+    const int blk = nact * hpg * (d + 2);
+    const float* pb = pbase;
+    if (blk <= kXBuf * 3 / 2) {
+        float* stage = c.sh.xbuf;   // xbuf and gbuf are adjacent: 1.5 * kXBuf floats
+        for (int i = tid; i < blk; i += kConsumerThreads) stage[i] = __ldcg(pbase + i);
+        if (!cbar(c, pc)) return false;
+        pb = stage;
+    }
     if (c.warp < hpg) {
         const int h = c.warp;
         float M = -INFINITY;
 #pragma unroll 1
-        for (int k = c.lane; k < nact; k += 32) M = fmaxf(M, __ldcg(pbase + (size_t(k) * hpg + h) * (d + 2) + d));
+        for (int k = c.lane; k < nact; k += 32) M = fmaxf(M, pb[(size_t(k) * hpg + h) * (d + 2) + d]);
         M = warp_max(M);
         float Ls = 0.f;
 #pragma unroll 1
         for (int k = c.lane; k < nact; k += 32) {
-            const float* ph = pbase + (size_t(k) * hpg + h) * (d + 2);
-            const float f = expf(__ldcg(ph + d) - M);
+            const float* ph = pb + (size_t(k) * hpg + h) * (d + 2);
+            const float f = expf(ph[d] - M);
             sc[h * p.n_chunk + k] = f;
-            Ls = fmaf(f, __ldcg(ph + d + 1), Ls);
+            Ls = fmaf(f, ph[d + 1], Ls);
         }
         Ls = warp_sum(Ls);
         if (c.lane == 0) c.sh.cml[h] = Ls;
@@ -1284,9 +1299,11 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
         const int h = idx / d, e = idx % d;
         float acc = 0.f;
-        for (int k = 0; k < nact; ++k) acc = fmaf(sc[h * p.n_chunk + k], __ldcg(pbase + (size_t(k) * hpg + h) * (d + 2) + e), acc);
+        for (int k = 0; k < nact; ++k) acc = fmaf(sc[h * p.n_chunk + k], pb[(size_t(k) * hpg + h) * (d + 2) + e], acc);
         st_tag(out + idx, acc / c.sh.cml[h], p.tag);
     }
+    // staged: no warp may refill the shared-x buffer (next instruction) while others still read it
+    if (pb != pbase && !cbar(c, pc)) return false;
     return true;
 }
 
@@ -1377,8 +1394,6 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
 template <int CPL>
 __device__ void consumer_warp(const Params& p, const Shared& sh) {
     Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u, 0u};
-    float xr[8 * CPL];
-    int xkey = -1;
     CounterCache cc{{-1, -1, -1, -1}, {-1, -1, -1, -1}};
     for (int pc = 0;; ++pc) {
         const int slot = pc % kSlots;
@@ -1407,7 +1422,7 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
             switch (op) {
                 case OP_ATTN: good = attn_tile(c, si, pc); break;
                 case OP_ARGMAX: good = argmax_tile(c, si, pc); break;
-                default: good = matvec_warp<CPL>(c, si, pc, xr, xkey); break;
+                default: good = matvec_warp<CPL>(c, si, pc); break;
             }
             if (!good) break;
             if (threadIdx.x == 0) stamp(p, pc, 3);
