@@ -177,9 +177,9 @@ mk_status mk_set_timeout(mk_ctx* c, uint64_t ns);
  *    elements it reads until each carries this step's tag.  One read both proves readiness and
  *    fetches the data, so a dependency costs one memory round trip instead of the publisher's
  *    release fence, the counter add, the consumer's counter poll and then the data read.
- *    Counters are still polled first, as cheap doorbells; they keep acquire/release semantics
- *    where a reader has no tag to check (the argmax over the LM-head partials, the MLP down
- *    projection's SwiGLU input, matvec inputs cut into segments).
+ *    Such a consumer reads no counter at all.  Counters are still published, and they keep
+ *    acquire/release semantics where a reader has no tag to check (the argmax over the LM-head
+ *    partials, the MLP down projection's SwiGLU input, matvec inputs cut into segments).
  *  MK_SYNC_COUNTERS: every instruction first waits all of its counters with acquire semantics
  *    (the page's protocol: wait the counters, run the body, fence, then add the completions); the tag checks then
  *    pass at the first read.

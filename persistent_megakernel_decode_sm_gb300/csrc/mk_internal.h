@@ -39,6 +39,7 @@ constexpr int kQWin = 16;    // instructions per queue-window buffer (two buffer
 constexpr int kMaxLayersSmem = 40;   // layer pointer table cached in shared memory
 constexpr int kDone = 64;            // completion records the publisher may lag behind
 constexpr int kTraceWords = 8;       // trace stamps per instruction
+constexpr unsigned kPollBackoffNs = 128;   // pause between two polling rounds of tagged data
 constexpr int kCombStride = 64;      // split-row partials per instruction slot (rows x segments x 2 <= 64)
 constexpr int kXBuf = 2048;          // floats of the shared matvec input buffer (one x per CTA)
 

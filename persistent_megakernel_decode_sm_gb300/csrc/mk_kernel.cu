@@ -633,6 +633,7 @@ __device__ bool spin_more(const Cw& c, Spin& sp, int pc) {
                 raise_error(c.p, c.sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, 0, c.p.tag);
                 stop = 1;
             }
+            if (!stop) __nanosleep(kPollBackoffNs);   // spaces a warp's polling rounds out in L2
         }
     }
     return __shfl_sync(0xFFFFFFFFu, stop, 0) == 0;
@@ -1350,8 +1351,7 @@ struct CounterCache {   // the four waits seen last, newest first (static indexe
     int32_t need[4];
 };
 
-__device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* w, int pc, CounterCache& cc,
-                              bool acquire) {
+__device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* w, int pc, CounterCache& cc) {
     const int nw = w[W_NWAIT];
     bool polled = false;
     for (int i = 0; i < nw; ++i) {
@@ -1387,7 +1387,7 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
         cc.id[0] = cid;
         cc.need[0] = need;
     }
-    if (polled && acquire) fence_acquire_gpu();   // acquire: producers' data is visible before this warp reads it
+    if (polled) fence_acquire_gpu();   // acquire: producers' data is visible before this warp reads it
     return true;
 }
 
@@ -1409,13 +1409,14 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
             if (gain && c.lane * 64 < p.H * 2)
                 for (int off = c.lane * 64; off < p.H * 2; off += 32 * 64)
                     asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(gain) + off));
-            // counters with acquire semantics in the counters mode and for the consumers that read
-            // their inputs without tags (the argmax over the LM-head partials; matvecs whose rows
-            // are cut into segments); otherwise the counters only say when to start reading -- the
-            // tags of the data decide, and a word read too early is read again
+            // counters (with acquire semantics) in the counters mode and for the consumers that read
+            // their inputs without tags (the argmax over the LM-head partials, the MLP down
+            // projection's SwiGLU input, matvecs whose rows are cut into segments); every other
+            // consumer polls the tagged words it reads until they carry this step's tag, with no
+            // counter in between: a counter poll before the data read would add a round trip
             int ok = 1;
-            if (c.lane == 0)
-                ok = wait_counters(p, sh, si.w, pc, cc, p.sync_counters || ((p.acquire_ops >> op) & 1));
+            if (c.lane == 0 && (p.sync_counters || ((p.acquire_ops >> op) & 1)))
+                ok = wait_counters(p, sh, si.w, pc, cc);
             if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
             if (threadIdx.x == 0) stamp(p, pc, 2);
             bool good;
