@@ -321,14 +321,15 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
     p.qkv = reinterpret_cast<uint64_t*>(sb + sl.qkv);
     p.part = reinterpret_cast<float*>(sb + sl.part);
     p.o = reinterpret_cast<uint64_t*>(sb + sl.o);
-    p.h = reinterpret_cast<float*>(sb + sl.h);
+    p.h = reinterpret_cast<uint32_t*>(sb + sl.h);
     p.lm_part = reinterpret_cast<int4*>(sb + sl.lm_part);
     p.rope = reinterpret_cast<const float2*>(sb + sl.rope);
-    // Readers without tags: the argmax (LM-head partials), the MLP down projection (the SwiGLU
-    // output is plain fp32) and every matvec whose rows are cut into segments (its per-warp input
-    // segment is read after an acquiring wait); their producers publish after a release fence.
-    p.acquire_ops = (1u << OP_ARGMAX) | (1u << OP_DOWN);
-    p.release_ops = (1u << OP_LMHEAD) | (1u << OP_UPGATE);
+    // Readers without tags: the argmax (LM-head partials) and every matvec whose 64-bit tagged
+    // rows are cut into segments (its per-warp input segment is read after an acquiring wait);
+    // their producers publish after a release fence.  The MLP down projection polls its
+    // 3-bit-tagged input like any tagged reader.
+    p.acquire_ops = 1u << OP_ARGMAX;
+    p.release_ops = 1u << OP_LMHEAD;
     auto untagged = [&](int op, std::initializer_list<int> producers) {
         if (p.mv[op].nseg <= 1) return;
         p.acquire_ops |= 1u << op;
@@ -337,7 +338,6 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
     untagged(OP_QKV, {OP_DOWN});
     untagged(OP_OPROJ, {OP_ATTN});
     untagged(OP_UPGATE, {OP_OPROJ});
-    untagged(OP_DOWN, {OP_UPGATE});
     untagged(OP_LMHEAD, {OP_DOWN});
     p.timeout_ns = 2000000000ull;
     p.smem_misc_off = n_pages * g.page_bytes;

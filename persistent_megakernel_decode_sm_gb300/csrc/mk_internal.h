@@ -95,7 +95,7 @@ inline ScratchLayout scratch_layout(const mk_model_cfg& c, const Geometry& g, in
     s.qkv = take(L * B * (qd + 2 * kvd) * 8);         // tagged
     s.part = take(L * B * size_t(c.n_kv_heads) * g.n_chunk * hpg * (d + 2) * 4);   // fp32 chunk partials
     s.o = take(L * B * qd * 8);                       // tagged
-    s.h = take(L * B * size_t(c.ffn) * 4);            // fp32 (its reader waits with acquire)
+    s.h = take(L * B * size_t(c.ffn) * 4);            // fp32 with a 3-bit tag
     s.lm_part = take(B * size_t(S) * kNumConsumerWarps * 2 * 16);   // per (sequence, CTA, warp half): max, index, epoch
     s.rope = take(size_t(c.max_seq) * (d / 2) * 8);
     s.total = off;
@@ -150,7 +150,7 @@ struct Params {
     uint64_t* qkv;      // tagged [L][B][nqkv]
     float* part;        // [L][B][nkv][n_chunk][hpg][d + 2] attention chunk partials
     uint64_t* o;        // tagged [L][B][qd]: attention output
-    float* h;           // [L][B][F]: SwiGLU output (plain fp32, read after an acquiring wait)
+    uint32_t* h;        // [L][B][F]: SwiGLU output, fp32 with a 3-bit step tag in the low mantissa bits
     int4* lm_part;     // [B][S][16]: (max bits, index, epoch, 0)
     const float2* rope; // [max_seq][d/2] (cos, sin)
     // step

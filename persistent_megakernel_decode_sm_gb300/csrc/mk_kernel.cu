@@ -139,6 +139,31 @@ __device__ __forceinline__ bool ld8_tagged(const uint64_t* a, float* v, uint32_t
     return ok;
 }
 
+// The SwiGLU output is read by the down projection a whole 2048-element segment per warp, where
+// 64-bit words would not fit the registers next to x: its elements are 32-bit words, fp32 with
+// the three low mantissa bits replaced by a 3-bit step tag, (epoch mod 7) + 1 -- never 0 (the
+// cleared scratch) and never the previous step's.  The stored value is the fp32 result with those
+// bits cleared (a relative change below 2^-20).
+__device__ __forceinline__ uint32_t htag(uint32_t tag) { return (tag - 1u) % 7u + 1u; }
+__device__ __forceinline__ void st_htag(uint32_t* a, float v, uint32_t ht) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(a), "r"((__float_as_uint(v) & ~7u) | ht) : "memory");
+}
+// eight consecutive h-tagged elements (32-byte aligned): values into v, true when all carry ht
+__device__ __forceinline__ bool ld8_htagged(const uint32_t* a, float* v, uint32_t ht) {
+    uint32_t w[8];
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(a));
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "l"(a + 4));
+    uint32_t bad = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        v[e] = __uint_as_float(w[e] & ~7u);
+        bad |= w[e] ^ ht;
+    }
+    return (bad & 7u) == 0;
+}
+
 // whole-CTA barrier reached by warps whose lanes diverged (loader / publisher lane 0 arrives late)
 __device__ __forceinline__ void cta_sync_divergent() { asm volatile("barrier.sync 0;" ::: "memory"); }
 
@@ -680,22 +705,17 @@ __device__ __forceinline__ void load8_bf16(const uint16_t* src, float* v) {
     v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
 }
 // where a matvec input comes from: epoch-tagged activations (t), plain fp32 activations read after
-// an acquiring counter wait (f), or the bf16 embedding row of the step's token (b)
+// the 3-bit tagged SwiGLU output (h), or the bf16 embedding row of the step's token (b)
 struct XSrc {
     const uint64_t* t;
-    const float* f;
+    const uint32_t* h;
     const uint16_t* b;
 };
-__device__ __forceinline__ void load8f(const float* src, float* v) {
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-// eight elements from element e0 on; false when a tagged element does not yet carry `tag`
+// eight elements from element e0 on; false when a tagged element does not yet carry this step's tag
 __device__ __forceinline__ bool load8x(const XSrc& x, int e0, float* v, uint32_t tag) {
     if (x.t) return ld8_tagged(x.t + e0, v, tag);
-    if (x.f) load8f(x.f + e0, v);
-    else load8_bf16(x.b + e0, v);
+    if (x.h) return ld8_htagged(x.h + e0, v, htag(tag));
+    load8_bf16(x.b + e0, v);
     return true;
 }
 // eight elements' values, for a reader whose counter wait acquired (tagged words: values only,
@@ -709,8 +729,13 @@ __device__ __forceinline__ void load8v(const XSrc& x, int e0, float* v) {
             v[2 * j] = __uint_as_float(w.x);
             v[2 * j + 1] = __uint_as_float(w.z);
         }
-    } else if (x.f) {
-        load8f(x.f + e0, v);
+    } else if (x.h) {
+        const uint4 a = __ldcg(reinterpret_cast<const uint4*>(x.h + e0));
+        const uint4 b = __ldcg(reinterpret_cast<const uint4*>(x.h + e0 + 4));
+        v[0] = __uint_as_float(a.x & ~7u); v[1] = __uint_as_float(a.y & ~7u);
+        v[2] = __uint_as_float(a.z & ~7u); v[3] = __uint_as_float(a.w & ~7u);
+        v[4] = __uint_as_float(b.x & ~7u); v[5] = __uint_as_float(b.y & ~7u);
+        v[6] = __uint_as_float(b.z & ~7u); v[7] = __uint_as_float(b.w & ~7u);
     } else {
         load8_bf16(x.b + e0, v);
     }
@@ -718,20 +743,30 @@ __device__ __forceinline__ void load8v(const XSrc& x, int e0, float* v) {
 
 // This warp's segment `seg` of the length-K input (lane owns chunks lane + 32 i), optionally
 // RMS-normalised: the sum of squares runs over all segments in a fixed order, so every warp
-// derives the same scale.  Segmented inputs are read after an acquiring counter wait (a tag poll
-// of a whole segment would not fit the registers next to x): values only, no tags.
+// derives the same scale.  The SwiGLU output (32-bit words with a 3-bit tag) is polled until
+// every element carries this step's tag; 64-bit tagged inputs cut into segments are read after an
+// acquiring counter wait (a tag poll of a whole segment would not fit the registers next to x):
+// values only, no tags.  False when the CTA aborts or the poll runs out of time.
 template <int CPL>
 __device__ bool load_xw(const Cw& c, float (&xr)[8 * CPL], int K, int nseg, int seg, const XSrc& src,
-                        const uint16_t* gain) {
+                        const uint16_t* gain, int pc) {
     const int seglen = K / nseg, segch = seglen / 8;
+    Spin sp;
+    while (true) {
+        bool ok = true;
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        const int ch = c.lane + 32 * i;
-        if (ch < segch) load8v(src, seg * seglen + ch * 8, &xr[8 * i]);
-        else {
+        for (int i = 0; i < CPL; ++i) {
+            const int ch = c.lane + 32 * i;
+            if (ch < segch) {
+                if (src.h) ok &= ld8_htagged(src.h + seg * seglen + ch * 8, &xr[8 * i], htag(c.p.tag));
+                else load8v(src, seg * seglen + ch * 8, &xr[8 * i]);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
+                for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
+            }
         }
+        if (__all_sync(0xFFFFFFFFu, ok)) break;
+        if (!spin_more(c, sp, pc)) return false;
     }
     if (!gain) return true;
     float ss = 0.f;
@@ -852,7 +887,7 @@ __device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int 
             st_tag(p.x_attn + lb * p.H + row, res + s0, p.tag);
             break;
         }
-        case OP_UPGATE: p.h[lb * p.F + row] = s0 / (1.0f + expf(-s0)) * s1; break;   // plain: read after acquire
+        case OP_UPGATE: st_htag(p.h + lb * p.F + row, s0 / (1.0f + expf(-s0)) * s1, htag(p.tag)); break;
         case OP_DOWN: st_tag(p.x_out + lb * p.H + row, poll1(p, c.sh, p.x_attn + lb * p.H + row, pc) + s0, p.tag); break;
         default: {   // LM head: logit, then this warp half's running (max, lowest index) for the argmax
             p.logits[size_t(b) * p.V + row] = s0;
@@ -1017,7 +1052,7 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc) {
                 break;
             case OP_OPROJ: src.t = p.o + lb * p.qd; break;
             case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; src.t = p.x_attn + lb * p.H; break;
-            case OP_DOWN: src.f = p.h + lb * p.F; break;
+            case OP_DOWN: src.h = p.h + lb * p.F; break;
             default: gain = p.final_norm; src.t = p.x_out + (size_t(p.L - 1) * p.B + b) * p.H; break;
         }
         if (nseg == 1 && si.K <= kXBuf) {   // every warp, even one without units in this tile
@@ -1051,7 +1086,7 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc) {
                 for (int s = s_lo; s < s_hi; ++s) {
                     const int key = (((op * 64 + (l & 63)) * kMaxBatch + b) * 8 + s) + 1;
                     if (key != xkey) {
-                        load_xw<CPL>(c, xr, si.K, nseg, s, src, gain);
+                        if (!load_xw<CPL>(c, xr, si.K, nseg, s, src, gain, pc)) return false;
                         xkey = key;
                     }
                     const uint32_t off0 = unit_off(u, s) - obase;
