@@ -1146,6 +1146,41 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc) {
     return true;
 }
 
+// Scores of one attention chunk: sc[h][t] = (q_h . k_t) * scale for t < n (row n_old is the new
+// key), d/8 consecutive lanes sharing a position.  HPG heads are unrolled at compile time; a head
+// count other than 4 runs the kMaxHpg variant with heads past hpg computed on a clamped head and
+// not stored.
+template <int HPG>
+__device__ __forceinline__ void attn_scores(const Cw& c, int tid, int n, int n_old, int hpg, int C, const uint8_t* kbase,
+                                            bool k1p, uint32_t first_slot, float* sc) {
+    const Params& p = c.p;
+    const int d = p.d, cpr = d / 8;
+    const uint32_t rowb = uint32_t(d) * 2u;
+    for (int base = 0; base < n * cpr; base += kConsumerThreads) {
+        const int idx = base + tid;
+        const bool valid = idx < n * cpr;
+        const int t = idx / cpr, j = idx - t * cpr;
+        float part[HPG];
+        if (valid) {
+            const uint32_t off = uint32_t(t) * rowb + uint32_t(j) * 16u;
+            const uint4 kv = (t < n_old) ? *reinterpret_cast<const uint4*>(k1p ? kbase + off : ring_ptr(c.sh, p, first_slot, off))
+                                         : *reinterpret_cast<const uint4*>(c.sh.knew + j * 8);
+#pragma unroll
+            for (int h = 0; h < HPG; ++h) part[h] = dot8(kv, c.sh.qrot + min(h, hpg - 1) * d + j * 8, 0.f);
+        } else {
+#pragma unroll
+            for (int h = 0; h < HPG; ++h) part[h] = 0.f;
+        }
+        for (int o = 1; o < cpr; o <<= 1)
+#pragma unroll
+            for (int h = 0; h < HPG; ++h) part[h] += __shfl_xor_sync(0xFFFFFFFFu, part[h], o);
+        if (valid && j == 0)
+#pragma unroll
+            for (int h = 0; h < HPG; ++h)
+                if (h < hpg) sc[h * C + t] = part[h] * p.attn_scale;
+    }
+}
+
 // Split-K decode attention over one chunk of KV positions for one (sequence, KV group); the
 // chunk that holds pos also applies RoPE to the new k, rounds k and v to bf16 and appends them
 // to the cache.  Writes the chunk partial (o[d] unnormalised, m, l) for each query head, then
@@ -1166,49 +1201,42 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         const int n = n_old + (has_new ? 1 : 0);
         const float2* rp = p.rope + size_t(pos) * half;
         if (!cbar(c, pc)) return false;   // the previous block-level body is done with the scratch
-        // 1. rotate q of the group's heads; RoPE k, round k and v, append them (q, k, v are
-        //    read until they carry this step's tag; loops run warp-uniform trip counts)
-        for (int base = c.warp * 32; base < hpg * half; base += kConsumerThreads) {
-            const int idx = base + c.lane;
-            const bool valid = idx < hpg * half;
-            const int h = idx / half, i = idx % half;
-            const uint64_t* qh = qkv + size_t(g * hpg + h) * d;
-            float q0 = 0.f, q1 = 0.f;
-            if (!wpoll2(c, valid, qh + i, qh + i + half, q0, q1, pc)) return false;
-            if (valid) {
-                const float2 cs = rp[i];
-                c.sh.qrot[h * d + i] = q0 * cs.x - q1 * cs.y;
-                c.sh.qrot[h * d + i + half] = q0 * cs.y + q1 * cs.x;
-            }
-        }
-        if (has_new) {
+        // 1. rotate q of the group's heads; RoPE k, round k and v, append them.  q, k and v are
+        //    read until they carry this step's tag, in one pass whose items (q pairs, then k pairs,
+        //    then v elements) are spread over all warps, so no warp waits on two round trips
+        {
             const size_t cache = size_t(b) * p.kv_bstride + size_t(l) * p.kv_lstride + size_t(g) * p.kv_hstride +
                                  size_t(pos) * d;
             const uint64_t* kh = qkv + p.qd + size_t(g) * d;
             const uint64_t* vh = qkv + p.qd + p.kvd + size_t(g) * d;
-            for (int base = c.warp * 32; base < half; base += kConsumerThreads) {
-                const int i = base + c.lane;
-                const bool valid = i < half;
-                float k0 = 0.f, k1 = 0.f;
-                if (!wpoll2(c, valid, kh + i, kh + i + half, k0, k1, pc)) return false;
-                if (valid) {
-                    const float2 cs = rp[i];
-                    const uint16_t r0 = f2bf_rn(k0 * cs.x - k1 * cs.y), r1 = f2bf_rn(k0 * cs.y + k1 * cs.x);
-                    c.sh.knew[i] = r0;
-                    c.sh.knew[i + half] = r1;
-                    p.kc[cache + i] = r0;
-                    p.kc[cache + i + half] = r1;
-                }
-            }
-            for (int base = c.warp * 32; base < d; base += kConsumerThreads) {
-                const int i = base + c.lane;
-                const bool valid = i < d;
+            const int nq = hpg * half, nk = has_new ? half : 0, nitems = nq + nk + (has_new ? d : 0);
+            for (int base = c.warp * 32; base < nitems; base += kConsumerThreads) {   // warp-uniform
+                const int it = base + c.lane;
+                const bool valid = it < nitems;
+                const int kind = it < nq ? 0 : it < nq + nk ? 1 : 2;
+                const int i = kind == 0 ? it % half : kind == 1 ? it - nq : it - nq - nk;
+                const int h = kind == 0 ? it / half : 0;
+                const uint64_t* a0 = kind == 0 ? qkv + size_t(g * hpg + h) * d + i : kind == 1 ? kh + i : vh + i;
+                const uint64_t* a1 = kind == 2 ? a0 : a0 + half;
                 float v0 = 0.f, v1 = 0.f;
-                if (!wpoll2(c, valid, vh + i, vh + i, v0, v1, pc)) return false;
+                if (!wpoll2(c, valid, a0, a1, v0, v1, pc)) return false;
                 if (valid) {
-                    const uint16_t r = f2bf_rn(v0);
-                    c.sh.vnew[i] = r;
-                    p.vc[cache + i] = r;
+                    if (kind == 0) {
+                        const float2 cs = rp[i];
+                        c.sh.qrot[h * d + i] = v0 * cs.x - v1 * cs.y;
+                        c.sh.qrot[h * d + i + half] = v0 * cs.y + v1 * cs.x;
+                    } else if (kind == 1) {
+                        const float2 cs = rp[i];
+                        const uint16_t r0 = f2bf_rn(v0 * cs.x - v1 * cs.y), r1 = f2bf_rn(v0 * cs.y + v1 * cs.x);
+                        c.sh.knew[i] = r0;
+                        c.sh.knew[i + half] = r1;
+                        p.kc[cache + i] = r0;
+                        p.kc[cache + i + half] = r1;
+                    } else {
+                        const uint16_t r = f2bf_rn(v0);
+                        c.sh.vnew[i] = r;
+                        p.vc[cache + i] = r;
+                    }
                 }
             }
         }
@@ -1224,31 +1252,8 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         const uint8_t* kbase = ring_ptr(c.sh, p, first_slot, 0u);
         const uint8_t* vbase = ring_ptr(c.sh, p, first_slot, voff);
         // 2. scores s[h][t] = (q_h . k_t) * scale; d/8 consecutive lanes share a position
-        const int cpr = d / 8;
-        for (int base = 0; base < n * cpr; base += kConsumerThreads) {
-            const int idx = base + tid;
-            const bool valid = idx < n * cpr;
-            const int t = idx / cpr, j = idx % cpr;
-            float part[kMaxHpg];
-#pragma unroll
-            for (int h = 0; h < kMaxHpg; ++h) part[h] = 0.f;
-            if (valid) {
-                const uint32_t off = uint32_t(t) * rowb + uint32_t(j) * 16u;
-                const uint4 kv = (t < n_old) ? *reinterpret_cast<const uint4*>(k1p ? kbase + off : ring_ptr(c.sh, p, first_slot, off))
-                                             : *reinterpret_cast<const uint4*>(c.sh.knew + j * 8);
-#pragma unroll
-                for (int h = 0; h < kMaxHpg; ++h)
-                    if (h < hpg) part[h] = dot8(kv, c.sh.qrot + h * d + j * 8, 0.f);
-            }
-            for (int o = 1; o < cpr; o <<= 1)
-#pragma unroll
-                for (int h = 0; h < kMaxHpg; ++h)
-                    if (h < hpg) part[h] += __shfl_xor_sync(0xFFFFFFFFu, part[h], o);
-            if (valid && j == 0)
-#pragma unroll
-                for (int h = 0; h < kMaxHpg; ++h)
-                    if (h < hpg) sc[h * C + t] = part[h] * p.attn_scale;
-        }
+        if (hpg == 4) attn_scores<4>(c, tid, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
+        else attn_scores<kMaxHpg>(c, tid, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
         if (!cbar(c, pc)) return false;
         // 3. softmax pieces per head (warp h): m, w_t = exp(s_t - m), l = sum w_t
         if (c.warp < hpg) {
@@ -1273,14 +1278,20 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
             const int h = idx / d, e = idx % d;
             const float* wts = sc + h * C;
-            float acc = 0.f;
+            // four interleaved partial sums (positions t mod 4), added pairwise at the end
+            float a4[4] = {0.f, 0.f, 0.f, 0.f};
             if (v1p) {
                 const uint16_t* vcol = reinterpret_cast<const uint16_t*>(vbase) + e;
-                for (int t = 0; t < n_old; ++t) acc = fmaf(wts[t], bf16f(vcol[t * d]), acc);
+                int t = 0;
+                for (; t + 4 <= n_old; t += 4)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) a4[r] = fmaf(wts[t + r], bf16f(vcol[(t + r) * d]), a4[r]);
+                for (; t < n_old; ++t) a4[t & 3] = fmaf(wts[t], bf16f(vcol[t * d]), a4[t & 3]);
             } else {
                 for (int t = 0; t < n_old; ++t)
-                    acc = fmaf(wts[t], bf16f(*reinterpret_cast<const uint16_t*>(ring_ptr(c.sh, p, first_slot, voff + uint32_t(t) * rowb + uint32_t(e) * 2u))), acc);
+                    a4[t & 3] = fmaf(wts[t], bf16f(*reinterpret_cast<const uint16_t*>(ring_ptr(c.sh, p, first_slot, voff + uint32_t(t) * rowb + uint32_t(e) * 2u))), a4[t & 3]);
             }
+            float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
             if (has_new) acc = fmaf(wts[n_old], bf16f(c.sh.vnew[e]), acc);
             float* dh = dst + size_t(h) * (d + 2);
             dh[e] = acc;
@@ -1334,9 +1345,16 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     uint64_t* out = p.o + lb * p.qd + size_t(g) * hpg * d;
     for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
         const int h = idx / d, e = idx % d;
-        float acc = 0.f;
-        for (int k = 0; k < nact; ++k) acc = fmaf(sc[h * p.n_chunk + k], pb[(size_t(k) * hpg + h) * (d + 2) + e], acc);
-        st_tag(out + idx, acc / c.sh.cml[h], p.tag);
+        const float* f = sc + h * p.n_chunk;
+        const float* ph = pb + size_t(h) * (d + 2) + e;
+        const size_t cs = size_t(hpg) * (d + 2);   // stride of one chunk's partials
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+        int k = 0;
+        for (; k + 4 <= nact; k += 4)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) a4[r] = fmaf(f[k + r], ph[(k + r) * cs], a4[r]);
+        for (; k < nact; ++k) a4[k & 3] = fmaf(f[k], ph[k * cs], a4[k & 3]);
+        st_tag(out + idx, ((a4[0] + a4[1]) + (a4[2] + a4[3])) / c.sh.cml[h], p.tag);
     }
     // staged: no warp may refill the shared-x buffer (next instruction) while others still read it
     if (pb != pbase && !cbar(c, pc)) return false;
