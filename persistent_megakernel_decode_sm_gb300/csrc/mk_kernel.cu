@@ -1092,9 +1092,10 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc) {
                     const uint32_t off0 = unit_off(u, s) - obase;
                     const uint32_t off1 = pair ? off0 + PB : (two ? unit_off(u1, s) - obase : off0);
                     const float v = seg_dot2<CPL>(c, si, first, off0, off1, pair || two, xr);
-                    // lanes 0-15 hold the first sum, lanes 16-31 the second
-                    t0 += __shfl_sync(0xFFFFFFFFu, v, 0);
-                    t1 += __shfl_sync(0xFFFFFFFFu, v, 16);
+                    // lanes 0-15 hold the first sum, lanes 16-31 the second: lane 0 keeps its own (and
+                    // takes the up sum of a pair from lane 16), lane 16 keeps its own
+                    t0 += v;
+                    t1 += pair ? __shfl_sync(0xFFFFFFFFu, v, 16) : v;
                 }
                 // lane 0 emits unit u (with the up sum of a pair), lane 16 the second unit u1
                 if (c.lane == 0 || (two && c.lane == 16)) {
@@ -1115,7 +1116,6 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc) {
                 for (; released < pn; ++released)
                     if (++rslot == NP) rslot = 0;
             }
-            __syncwarp();
         }
     }
     if (c.warp == 0 && c.lane == 0) stamp(p, pc, 7);
