@@ -11,6 +11,8 @@ Prints one JSON line.
             step streams its weights from HBM; no L2 flush is needed)
   e2e       the same metric through the synchronous C-ABI call mk_decode_step: host token and
             position in, greedy next token (and the device error word) copied back each step
+  e2e_chained  the same through mk_decode_steps: all timed steps in one call, each step's greedy
+            token feeding the next on the device, tokens copied back once at the end
   roofline  algorithmic bytes per step (weights + KV read + KV written) / median step time,
             against the measured HBM copy bandwidth
   cpu_baseline  the CPU oracle on the host cores, on a bounded sample (whole decode steps)
@@ -285,6 +287,16 @@ def main():
             e2e_times.append(dt * 1e6)
     e2e_us = statistics.mean(e2e_times) / cfg.batch
 
+    # ---- end-to-end through mk_decode_steps: n chained steps per call (each step's greedy token
+    # feeds the next on the device), one host synchronisation per call
+    n_chain = min(K, span)
+    tokens_dev = torch.empty(n_chain * cfg.batch, dtype=torch.int32, device=dec.logits.device)
+    dec.steps(toks[:cfg.batch], list(wl.kv_len), min(W, n_chain), tokens_dev=tokens_dev)   # warm-up call
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    dec.steps(toks[:cfg.batch], list(wl.kv_len), n_chain, tokens_dev=tokens_dev)
+    chained_us = (time.perf_counter() - t0) * 1e6 / n_chain / cfg.batch
+
     pos_mid = [l + 0 for l in wl.kv_len]
     step_bytes = cfg.step_bytes(pos_mid)
     peak, peak_kind = peaks()
@@ -303,6 +315,9 @@ def main():
                    "step_us_mean": mean_us, "step_us_median": med, "step_us_p10": p10, "step_us_p90": p90},
         "e2e": {"value": e2e_us, "unit": "us/token", "h2d_bytes_per_step": 8 * cfg.batch,
                 "d2h_bytes_per_step": 96},
+        "e2e_chained": {"value": chained_us, "unit": "us/token", "steps_per_call": n_chain,
+                        "h2d_bytes_per_step": 8 * cfg.batch / n_chain,
+                        "d2h_bytes_per_step": (4 * cfg.batch * n_chain + 96) / n_chain},
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic_record(args.workload), "peak_kind": peak_kind,

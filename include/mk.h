@@ -224,6 +224,26 @@ mk_status mk_decode_step(mk_ctx* c, const int32_t* tokens, const int32_t* pos, f
 mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
                                 int32_t* next_tokens);
 
+/* n_steps greedy decode steps in one call, each step's token fed to the next step's embedding on
+ * the device (the chained, multi-step form of decoding; the page's "online" megakernel keeps
+ * generating without returning to the host).  Step i (0-based) decodes sequence b at position
+ * pos[b] + i; step 0 takes tokens[b] (host), step i > 0 the greedy token of step i - 1.  The
+ * steps are launched back to back on the bound stream, one launch each, with no host round trip
+ * in between; the host synchronises once, at the end.
+ *  tokens, pos   HOST int32[batch]: the first step's tokens (in [0, vocab)) and positions
+ *                (pos[b] + n_steps <= max_seq).
+ *  n_steps       >= 1.
+ *  logits        DEVICE fp32[batch, vocab], caller-owned: every step writes it; the last step's
+ *                logits remain.
+ *  tokens_dev    DEVICE int32[n_steps * batch], caller-owned, 4-byte aligned: step i's greedy
+ *                tokens at [i * batch, (i + 1) * batch).
+ *  tokens_out    HOST int32[n_steps * batch]: a copy of tokens_dev, read back once at the end.
+ * Errors: MK_ERR_ARG (null or misaligned pointer, n_steps < 1, a token or position out of range:
+ * nothing is launched), MK_ERR_POISONED; a device error in any step is reported as by
+ * mk_decode_step and poisons the context (later steps then stop at their first wait). */
+mk_status mk_decode_steps(mk_ctx* c, const int32_t* tokens, const int32_t* pos, int32_t n_steps, float* logits,
+                          int32_t* tokens_dev, int32_t* tokens_out);
+
 /* Asynchronous form: enqueues one step on the bound stream and returns.  next_tokens_dev is a
  * DEVICE int32[batch] buffer or NULL.  Device-side errors surface at the next mk_ctx_status or
  * mk_decode_step. */

@@ -35,7 +35,7 @@ SYNC_TAGS, SYNC_COUNTERS = 0, 1   # mk_sync_mode
 EXPORTS = ["mk_build_schedule", "mk_schedule_queues", "mk_schedule_counters", "mk_schedule_patch",
            "mk_scratch_bytes", "mk_schedule_free", "mk_bind", "mk_set_timeout", "mk_decode_step",
            "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind", "mk_set_trace",
-           "mk_decode_step_static", "mk_set_sync"]
+           "mk_decode_step_static", "mk_set_sync", "mk_decode_steps"]
 
 
 class MkError(RuntimeError):
@@ -91,6 +91,8 @@ lib.mk_decode_step.restype = ctypes.c_int
 lib.mk_decode_step.argtypes = [_P, _I32P, _I32P, _P, _I32P]
 lib.mk_launch_step.restype = ctypes.c_int
 lib.mk_launch_step.argtypes = [_P, _I32P, _I32P, _P, _P]
+lib.mk_decode_steps.restype = ctypes.c_int
+lib.mk_decode_steps.argtypes = [_P, _I32P, _I32P, ctypes.c_int32, _P, _P, _I32P]
 lib.mk_ctx_status.restype = ctypes.c_int
 lib.mk_ctx_status.argtypes = [_P, _I32P]
 lib.mk_device_sm_count.restype = ctypes.c_int
@@ -232,6 +234,21 @@ class Decoder:
         out = (ctypes.c_int32 * self.cfg.batch)()
         _check(lib.mk_decode_step_static(self.handle, t, p, _ptr(lg), out))
         return list(out)
+
+    def steps(self, tokens: Sequence[int], pos: Sequence[int], n_steps: int, logits=None,
+              tokens_dev=None) -> List[List[int]]:
+        """mk_decode_steps: n_steps chained greedy steps (each step's token feeds the next on the
+        device), one host synchronisation.  Returns the greedy tokens per step ([n_steps][batch]);
+        ``logits`` (default self.logits) holds the last step's logits."""
+        import torch
+        B = self.cfg.batch
+        lg = self.logits if logits is None else logits
+        if tokens_dev is None:
+            tokens_dev = torch.empty(n_steps * B, dtype=torch.int32, device=lg.device)
+        t, p = self._arrays(tokens, pos)
+        out = (ctypes.c_int32 * (max(n_steps, 1) * B))()
+        _check(lib.mk_decode_steps(self.handle, t, p, int(n_steps), _ptr(lg), _ptr(tokens_dev), out))
+        return [list(out[i * B:(i + 1) * B]) for i in range(n_steps)]
 
     def launch(self, tokens: Sequence[int], pos: Sequence[int], logits=None, next_dev=None):
         """mk_launch_step: enqueue one step on the bound stream."""

@@ -379,19 +379,17 @@ extern "C" mk_status mk_set_trace(mk_ctx* c, uint64_t* buf) {
     return MK_OK;
 }
 
-extern "C" mk_status mk_launch_step(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
-                                    int32_t* next_tokens_dev) {
-    if (!c || !tokens || !pos || !logits) return fail(MK_ERR_ARG, "null argument");
-    if (c->poisoned) return fail(MK_ERR_POISONED, "context poisoned by an earlier device error");
-    if (reinterpret_cast<uintptr_t>(logits) & 3u) return fail(MK_ERR_ARG, "logits not 4-byte aligned");
+// One step on the bound stream.  Its tokens come from the host (tokens) or, when tok_dev is set,
+// from device memory (a chained step: the previous step's greedy tokens); pos[b] + dpos is its
+// position.  The caller has checked the arguments.
+static mk_status launch(mk_ctx* c, const int32_t* tokens, const int32_t* pos, int32_t dpos, float* logits,
+                        int32_t* next_tokens_dev, const int32_t* tok_dev) {
     Params p = c->base;
     for (int b = 0; b < c->cfg.batch; ++b) {
-        if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab) return fail(MK_ERR_ARG, "token %d out of range", tokens[b]);
-        if (pos[b] < 0 || pos[b] >= c->cfg.max_seq)
-            return fail(MK_ERR_ARG, "pos %d outside the KV capacity [0, %d)", pos[b], c->cfg.max_seq);
-        p.tok[b] = tokens[b];
-        p.pos[b] = pos[b];
+        p.tok[b] = tok_dev ? 0 : tokens[b];
+        p.pos[b] = pos[b] + dpos;
     }
+    p.tok_dev = tok_dev;
     p.epoch = c->epoch;
     p.tag = c->epoch + 1u;
     p.logits = logits;
@@ -403,6 +401,27 @@ extern "C" mk_status mk_launch_step(mk_ctx* c, const int32_t* tokens, const int3
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
     c->epoch += 1;
     return MK_OK;
+}
+
+static mk_status check_step_args(mk_ctx* c, const int32_t* tokens, const int32_t* pos, int32_t n_steps,
+                                 const float* logits) {
+    if (!c || !tokens || !pos || !logits) return fail(MK_ERR_ARG, "null argument");
+    if (c->poisoned) return fail(MK_ERR_POISONED, "context poisoned by an earlier device error");
+    if (reinterpret_cast<uintptr_t>(logits) & 3u) return fail(MK_ERR_ARG, "logits not 4-byte aligned");
+    for (int b = 0; b < c->cfg.batch; ++b) {
+        if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab) return fail(MK_ERR_ARG, "token %d out of range", tokens[b]);
+        if (pos[b] < 0 || int64_t(pos[b]) + n_steps > c->cfg.max_seq)
+            return fail(MK_ERR_ARG, "positions %d..%d outside the KV capacity [0, %d)", pos[b], pos[b] + n_steps - 1,
+                        c->cfg.max_seq);
+    }
+    return MK_OK;
+}
+
+extern "C" mk_status mk_launch_step(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
+                                    int32_t* next_tokens_dev) {
+    const mk_status st = check_step_args(c, tokens, pos, 1, logits);
+    if (st != MK_OK) return st;
+    return launch(c, tokens, pos, 0, logits, next_tokens_dev, nullptr);
 }
 
 static mk_status read_status(mk_ctx* c, int32_t* info) {
@@ -433,6 +452,30 @@ extern "C" mk_status mk_decode_step(mk_ctx* c, const int32_t* tokens, const int3
     if (st != MK_OK) return st;
     for (int b = 0; b < c->cfg.batch; ++b) next_tokens[b] = c->h_result[16 + b];
     return MK_OK;
+}
+
+extern "C" mk_status mk_decode_steps(mk_ctx* c, const int32_t* tokens, const int32_t* pos, int32_t n_steps,
+                                     float* logits, int32_t* tokens_dev, int32_t* tokens_out) {
+    if (n_steps < 1) return fail(MK_ERR_ARG, "n_steps %d < 1", n_steps);
+    if (!tokens_dev || !tokens_out) return fail(MK_ERR_ARG, "null argument");
+    if (reinterpret_cast<uintptr_t>(tokens_dev) & 3u) return fail(MK_ERR_ARG, "tokens_dev not 4-byte aligned");
+    mk_status st = check_step_args(c, tokens, pos, n_steps, logits);
+    if (st != MK_OK) return st;
+    const int B = c->cfg.batch;
+    for (int i = 0; i < n_steps; ++i) {   // back to back on the stream: no host round trip in between
+        st = launch(c, tokens, pos, i, logits, tokens_dev + size_t(i) * B, i ? tokens_dev + size_t(i - 1) * B : nullptr);
+        if (st != MK_OK) {
+            c->poisoned = true;   // steps already enqueued have advanced the counters
+            return st;
+        }
+    }
+    const cudaError_t e =
+        cudaMemcpyAsync(tokens_out, tokens_dev, size_t(n_steps) * B * sizeof(int32_t), cudaMemcpyDeviceToHost, c->stream);
+    if (e != cudaSuccess) {
+        c->poisoned = true;
+        return cuda_fail(e, "token readback");
+    }
+    return read_status(c, nullptr);
 }
 
 extern "C" mk_status mk_ctx_status(mk_ctx* c, int32_t* info) {

@@ -163,6 +163,7 @@ struct Params {
     int32_t pos[kMaxBatch];
     float* logits;
     int32_t* next_dev;
+    const int32_t* tok_dev;  // optional DEVICE int32[B]: this step's tokens (a chained step), else tok
     uint64_t timeout_ns;
     uint64_t* trace;         // optional [S][Q][8] globaltimer stamps (null: off)
     // shared-memory carve-up

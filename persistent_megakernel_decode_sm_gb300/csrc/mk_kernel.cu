@@ -873,6 +873,14 @@ __device__ bool shared_x(Cw& c, float (&xr)[8 * CPL], int K, const XSrc& src, co
     return true;
 }
 
+// the step's input token of sequence b: from the host, or in a chained multi-step call the
+// previous step's greedy token in device memory -- clamped to the vocabulary, since a step that
+// failed may have left no token (its recorded error is what the host then reports)
+__device__ __forceinline__ int step_token(const Params& p, int b) {
+    if (!p.tok_dev) return p.tok[b];
+    return min(max(__ldcg(p.tok_dev + b), 0), p.V - 1);
+}
+
 // output of one matvec row (run by one lane); `half` tells the two row units a warp carries apart
 __device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int ru, int half, float s0, float s1) {
     const Params& p = c.p;
@@ -882,7 +890,7 @@ __device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int 
     switch (op) {
         case OP_QKV: st_tag(p.qkv + lb * p.nqkv + row, s0, p.tag); break;
         case OP_OPROJ: {
-            const float res = (l == 0) ? bf16f(p.embed[size_t(p.tok[b]) * p.H + row])
+            const float res = (l == 0) ? bf16f(p.embed[size_t(step_token(p, b)) * p.H + row])
                                        : poll1(p, c.sh, p.x_out + (lb - p.B) * p.H + row, pc);
             st_tag(p.x_attn + lb * p.H + row, res + s0, p.tag);
             break;
@@ -1047,7 +1055,7 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc) {
         switch (op) {
             case OP_QKV:
                 gain = c.sh.layers[l].attn_norm;
-                if (l == 0) src.b = p.embed + size_t(p.tok[b]) * p.H;
+                if (l == 0) src.b = p.embed + size_t(step_token(p, b)) * p.H;
                 else src.t = p.x_out + (lb - p.B) * p.H;
                 break;
             case OP_OPROJ: src.t = p.o + lb * p.qd; break;

@@ -60,3 +60,18 @@ def test_last_error_message_is_set():
     with pytest.raises(mk.MkError) as e:
         mk.Schedule(small_config(n_q_heads=5, n_kv_heads=2), 4)
     assert "n_kv_heads" in str(e.value)
+
+
+def test_step_calls_reject_null_and_bad_arguments_without_a_device():
+    lib = mk.lib
+    B = 1
+    t = (ctypes.c_int32 * B)(1)
+    p = (ctypes.c_int32 * B)(0)
+    out = (ctypes.c_int32 * 8)()
+    dummy = ctypes.c_void_p(256)   # never dereferenced: every call below fails its host checks first
+    assert lib.mk_decode_steps(None, t, p, 0, dummy, dummy, out) == mk.MK_ERR_ARG      # n_steps < 1
+    assert lib.mk_decode_steps(None, t, p, 2, dummy, None, out) == mk.MK_ERR_ARG       # no token buffer
+    assert lib.mk_decode_steps(None, t, p, 2, dummy, dummy, None) == mk.MK_ERR_ARG     # no host copy
+    assert lib.mk_decode_steps(None, t, p, 2, dummy, dummy, out) == mk.MK_ERR_ARG      # no context
+    assert lib.mk_launch_step(None, t, p, dummy, None) == mk.MK_ERR_ARG
+    assert lib.mk_decode_step(None, t, p, dummy, out) == mk.MK_ERR_ARG
