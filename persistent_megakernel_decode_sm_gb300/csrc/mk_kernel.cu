@@ -704,8 +704,8 @@ __device__ __forceinline__ void load8_bf16(const uint16_t* src, float* v) {
     v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
     v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
 }
-// where a matvec input comes from: epoch-tagged activations (t), plain fp32 activations read after
-// the 3-bit tagged SwiGLU output (h), or the bf16 embedding row of the step's token (b)
+// where a matvec input comes from: epoch-tagged activations (t), the 3-bit tagged SwiGLU output
+// (h), or the bf16 embedding row of the step's token (b)
 struct XSrc {
     const uint64_t* t;
     const uint32_t* h;
@@ -1405,11 +1405,12 @@ __device__ bool argmax_tile(Cw& c, const SlotInfo& si, int pc) {
     return true;
 }
 
-// Counters seen satisfied by this warp: counters only grow within a launch, so a wait whose
-// target an earlier observation already covers needs neither a poll nor another acquire fence.
-struct CounterCache {   // the four waits seen last, newest first (static indexes: registers)
-    int32_t id[4];
-    int32_t need[4];
+// The counter wait this warp saw satisfied last: counters only grow within a launch, so the same
+// wait again (consecutive tiles of one operator) needs neither a poll nor another acquire fence.
+// One entry only: the cache stays in registers live across the matvec loop, where every register
+// counts.
+struct CounterCache {
+    int32_t id, need;
 };
 
 __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* w, int pc, CounterCache& cc) {
@@ -1417,10 +1418,7 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
     bool polled = false;
     for (int i = 0; i < nw; ++i) {
         const int cid = w[W_WAIT + 2 * i], need = w[W_WAIT + 2 * i + 1];
-        bool known = false;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) known |= (cc.id[k] == cid) && (cc.need[k] == need);
-        if (known) continue;
+        if (cc.id == cid && cc.need == need) continue;
         polled = true;
         const uint32_t target = p.epoch * __ldg(p.totals + cid) + uint32_t(need);
         uint32_t v = ld_relaxed_gpu(p.counters + cid);
@@ -1440,13 +1438,8 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
                 }
             }
         }
-#pragma unroll
-        for (int k = 3; k > 0; --k) {
-            cc.id[k] = cc.id[k - 1];
-            cc.need[k] = cc.need[k - 1];
-        }
-        cc.id[0] = cid;
-        cc.need[0] = need;
+        cc.id = cid;
+        cc.need = need;
     }
     if (polled) fence_acquire_gpu();   // acquire: producers' data is visible before this warp reads it
     return true;
@@ -1455,7 +1448,7 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
 template <int CPL>
 __device__ void consumer_warp(const Params& p, const Shared& sh) {
     Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u, 0u};
-    CounterCache cc{{-1, -1, -1, -1}, {-1, -1, -1, -1}};
+    CounterCache cc{-1, -1};
     for (int pc = 0;; ++pc) {
         const int slot = pc % kSlots;
         if (!wait_bar(p, sh, sh.ins_full + slot, (pc / kSlots) & 1, ROLE_CONSUMER, pc)) break;
