@@ -150,6 +150,25 @@ typedef struct {
     int64_t batch_stride, layer_stride, head_stride;
 } mk_kv;
 
+/* Paged KV cache (optional, see mk_bind_paged).  The K (and V) cache is a pool of blocks of
+ * block_size positions per (layer, KV head); sequence b's positions [j*block_size,
+ * (j+1)*block_size) live in pool block block_table[b*max_blocks + j].  Element (b, l, g, p, e) of
+ * K lives at k + l*layer_stride + g*head_stride + (block_table[b*max_blocks + p/block_size]*
+ * block_size + p % block_size)*head_dim + e (mk_kv's batch_stride is not used).  The page calls
+ * the KV cache paged and per layer; one block is one split-K attention chunk, so a chunk's rows
+ * are one contiguous copy.
+ *  block_table  DEVICE int32[batch * max_blocks], caller-owned, 4-byte aligned; read by every
+ *               step (the caller may rewrite it between steps).  An entry outside [0, n_blocks)
+ *               that a step needs stops the step with MK_ERR_BOUNDS (nothing is accessed there).
+ *  block_size   positions per block: must equal the schedule's attention chunk
+ *               (mk_sched_opts.attn_chunk, default 64).
+ *  max_blocks   table entries per sequence, max_blocks * block_size >= max_seq.
+ *  n_blocks     blocks in the pool per (layer, KV head): head_stride >= n_blocks*block_size*head_dim. */
+typedef struct {
+    const int32_t* block_table;
+    int32_t block_size, max_blocks, n_blocks;
+} mk_kv_pages;
+
 /* Binds a schedule to one model instance on the current CUDA device (the page's model binding:
  * weights, KV cache, activations and counters become objects of the one resident execution,
  * bound once).
@@ -162,6 +181,12 @@ typedef struct {
  * binding.  Errors: MK_ERR_ARG, MK_ERR_CAPACITY, MK_ERR_RESOURCES, MK_ERR_CUDA. */
 mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, uint32_t* counters,
                   void* scratch, void* stream, mk_ctx** out);
+
+/* mk_bind with a paged KV cache (pages non-NULL; NULL binds the contiguous layout exactly as
+ * mk_bind).  Errors as mk_bind, plus MK_ERR_ARG for a block size other than the schedule's
+ * attention chunk, a table that cannot cover max_seq, or strides that do not cover the pool. */
+mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, const mk_kv_pages* pages,
+                        uint32_t* counters, void* scratch, void* stream, mk_ctx** out);
 
 /* Time budget, in nanoseconds, of a single device wait: counter spins and tagged-data polls get
  * ns, waits of the consumer warps on one another 2 ns, the loader's and publisher's waits (which

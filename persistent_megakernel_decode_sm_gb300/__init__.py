@@ -35,7 +35,7 @@ SYNC_TAGS, SYNC_COUNTERS = 0, 1   # mk_sync_mode
 EXPORTS = ["mk_build_schedule", "mk_schedule_queues", "mk_schedule_counters", "mk_schedule_patch",
            "mk_scratch_bytes", "mk_schedule_free", "mk_bind", "mk_set_timeout", "mk_decode_step",
            "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind", "mk_set_trace",
-           "mk_decode_step_static", "mk_set_sync", "mk_decode_steps"]
+           "mk_decode_step_static", "mk_set_sync", "mk_decode_steps", "mk_bind_paged"]
 
 
 class MkError(RuntimeError):
@@ -69,6 +69,11 @@ class mk_kv(ctypes.Structure):
                 ("head_stride", ctypes.c_int64)]
 
 
+class mk_kv_pages(ctypes.Structure):
+    _fields_ = [("block_table", _P), ("block_size", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+                ("n_blocks", ctypes.c_int32)]
+
+
 _I32P = ctypes.POINTER(ctypes.c_int32)
 lib.mk_build_schedule.restype = ctypes.c_int
 lib.mk_build_schedule.argtypes = [ctypes.POINTER(mk_model_cfg), ctypes.c_int32, ctypes.POINTER(mk_sched_opts),
@@ -85,6 +90,9 @@ lib.mk_schedule_free.restype = None
 lib.mk_schedule_free.argtypes = [_P]
 lib.mk_bind.restype = ctypes.c_int
 lib.mk_bind.argtypes = [_P, ctypes.POINTER(mk_weights), ctypes.POINTER(mk_kv), _P, _P, _P, ctypes.POINTER(_P)]
+lib.mk_bind_paged.restype = ctypes.c_int
+lib.mk_bind_paged.argtypes = [_P, ctypes.POINTER(mk_weights), ctypes.POINTER(mk_kv), ctypes.POINTER(mk_kv_pages), _P,
+                              _P, _P, ctypes.POINTER(_P)]
 lib.mk_set_timeout.restype = ctypes.c_int
 lib.mk_set_timeout.argtypes = [_P, ctypes.c_uint64]
 lib.mk_decode_step.restype = ctypes.c_int
@@ -172,9 +180,13 @@ def _ptr(t) -> int:
 
 
 class Decoder:
-    """A bound context: borrows the weights / KV tensors, owns counters, scratch and logits (torch)."""
+    """A bound context: borrows the weights / KV tensors, owns counters, scratch and logits (torch).
 
-    def __init__(self, sched: Schedule, weights, kv, stream=None, timeout_ns: Optional[int] = None):
+    ``pages`` (optional) binds a paged KV cache: a tuple (block_table, block_size, n_blocks) with
+    block_table a CUDA int32 tensor [batch, max_blocks]; kv.k / kv.v are then the block pools,
+    shaped [n_layers, n_kv_heads, n_blocks * block_size, head_dim]."""
+
+    def __init__(self, sched: Schedule, weights, kv, stream=None, timeout_ns: Optional[int] = None, pages=None):
         import torch
         cfg = sched.cfg
         dev = weights.embed.device
@@ -189,14 +201,23 @@ class Decoder:
         for t in (kv.k, kv.v):
             assert t.is_contiguous() and t.dtype == torch.bfloat16 and t.device == dev
         st = kv.k.stride()
-        self._kv = mk_kv(_ptr(kv.k), _ptr(kv.v), st[0], st[1], st[2])
+        if pages is None:
+            self._kv = mk_kv(_ptr(kv.k), _ptr(kv.v), st[0], st[1], st[2])
+            self._pages = None
+        else:
+            table, block_size, n_blocks = pages
+            assert table.dtype == torch.int32 and table.device == dev and table.is_contiguous()
+            self._kv = mk_kv(_ptr(kv.k), _ptr(kv.v), 0, st[0], st[1])
+            self._pages = mk_kv_pages(_ptr(table), int(block_size), int(table.shape[-1]), int(n_blocks))
+            self._table = table
         self.counters = torch.zeros(sched.n_counters, dtype=torch.int32, device=dev)
         self.scratch = torch.empty(sched.scratch_bytes // 4 + 64, dtype=torch.int32, device=dev)
         self.logits = torch.empty((cfg.batch, cfg.vocab), dtype=torch.float32, device=dev)
         self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
         h = _P()
-        _check(lib.mk_bind(sched.handle, ctypes.byref(self._w), ctypes.byref(self._kv), _ptr(self.counters),
-                           _ptr(self.scratch), ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h)))
+        _check(lib.mk_bind_paged(sched.handle, ctypes.byref(self._w), ctypes.byref(self._kv),
+                                 ctypes.byref(self._pages) if self._pages is not None else None, _ptr(self.counters),
+                                 _ptr(self.scratch), ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h)))
         self.handle = h
         if timeout_ns is not None:
             self.set_timeout(timeout_ns)

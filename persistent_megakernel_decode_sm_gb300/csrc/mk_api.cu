@@ -159,6 +159,12 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, std::
 
 extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, uint32_t* counters,
                              void* scratch, void* stream, mk_ctx** out) {
+    return mk_bind_paged(s, w, kv, nullptr, counters, scratch, stream, out);
+}
+
+extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, const mk_kv* kv,
+                                   const mk_kv_pages* pages, uint32_t* counters, void* scratch, void* stream,
+                                   mk_ctx** out) {
     if (!s || !w || !kv || !counters || !scratch || !out) return fail(MK_ERR_ARG, "null argument");
     *out = nullptr;
     const mk_model_cfg& c = s->cfg;
@@ -180,9 +186,23 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
     }
     if (!kv->k || !kv->v || !aligned16(kv->k) || !aligned16(kv->v))
         return fail(MK_ERR_ARG, "KV pointers null or not 16-byte aligned");
-    if (kv->batch_stride % 8 || kv->layer_stride % 8 || kv->head_stride % 8 || kv->head_stride < int64_t(c.max_seq) * d ||
-        kv->layer_stride < kv->head_stride * c.n_kv_heads || (c.batch > 1 && kv->batch_stride < kv->layer_stride * L))
+    if (pages) {   // a pool of blocks per (layer, KV head), reached through the block table
+        if (!pages->block_table || (reinterpret_cast<uintptr_t>(pages->block_table) & 3u))
+            return fail(MK_ERR_ARG, "block table null or not 4-byte aligned");
+        if (pages->block_size != g.attn_chunk)
+            return fail(MK_ERR_ARG, "block_size %d must equal the schedule's attention chunk %d", pages->block_size,
+                        g.attn_chunk);
+        if (pages->n_blocks < 1 || int64_t(pages->max_blocks) * pages->block_size < c.max_seq)
+            return fail(MK_ERR_ARG, "the block table must cover max_seq positions and the pool hold a block");
+        if (kv->layer_stride % 8 || kv->head_stride % 8 ||
+            kv->head_stride < int64_t(pages->n_blocks) * pages->block_size * d ||
+            kv->layer_stride < kv->head_stride * c.n_kv_heads)
+            return fail(MK_ERR_ARG, "KV strides must be multiples of 8 elements and cover the pool per head");
+    } else if (kv->batch_stride % 8 || kv->layer_stride % 8 || kv->head_stride % 8 ||
+               kv->head_stride < int64_t(c.max_seq) * d || kv->layer_stride < kv->head_stride * c.n_kv_heads ||
+               (c.batch > 1 && kv->batch_stride < kv->layer_stride * L)) {
         return fail(MK_ERR_ARG, "KV strides must be multiples of 8 elements and cover [max_seq, head_dim] per head");
+    }
     if (reinterpret_cast<uintptr_t>(scratch) & 255u) return fail(MK_ERR_ARG, "scratch must be 256-byte aligned");
     if (reinterpret_cast<uintptr_t>(counters) & 3u) return fail(MK_ERR_ARG, "counters must be 4-byte aligned");
     if (g.page_bytes & (g.page_bytes - 1)) return fail(MK_ERR_ARG, "page_bytes must be a power of two");
@@ -314,6 +334,9 @@ extern "C" mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk
     p.kv_bstride = kv->batch_stride;
     p.kv_lstride = kv->layer_stride;
     p.kv_hstride = kv->head_stride;
+    p.kv_table = pages ? pages->block_table : nullptr;
+    p.kv_max_blocks = pages ? pages->max_blocks : 0;
+    p.kv_n_blocks = pages ? pages->n_blocks : 0;
     p.err = reinterpret_cast<int32_t*>(sb + sl.err);
     p.tokens_out = reinterpret_cast<int32_t*>(sb + sl.tokens);
     p.x_attn = reinterpret_cast<uint64_t*>(sb + sl.x_attn);

@@ -142,6 +142,8 @@ struct Params {
     uint16_t* kc;
     uint16_t* vc;
     int64_t kv_bstride, kv_lstride, kv_hstride;
+    const int32_t* kv_table;   // paged cache: DEVICE int32[B][kv_max_blocks] block table (null: contiguous)
+    int32_t kv_max_blocks, kv_n_blocks;
     // scratch
     int32_t* err;
     int32_t* tokens_out;
@@ -172,7 +174,9 @@ struct Params {
     int32_t qrot_floats;
 };
 
-struct SlotInfo {            // one instruction slot: words + where its stream sits + decoded matvec shape
+// one instruction slot: words + where its stream sits + decoded matvec shape.  16-byte aligned
+// and sized: the loader fills the words of each slot of the array with 16-byte stores
+struct alignas(16) SlotInfo {
     int32_t w[kWords];
     int32_t first_page;      // global page sequence number of the stream's first page
     int32_t n_pages;
@@ -184,7 +188,9 @@ struct SlotInfo {            // one instruction slot: words + where its stream s
     uint32_t rowbytes, segbytes;
     int32_t segch;           // 16-byte chunks per segment
     int32_t first_phase;     // mbarrier phase parity of the first page
+    int64_t kv_off;          // attention: element offset of the chunk's first K/V row in the cache
 };
+static_assert(sizeof(SlotInfo) % 16 == 0 && offsetof(SlotInfo, w) == 0, "slot words must stay 16-byte aligned");
 
 #ifdef __CUDACC__
 #define MK_HD __host__ __device__

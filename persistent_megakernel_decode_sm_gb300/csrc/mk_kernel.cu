@@ -321,6 +321,7 @@ struct Seg {
     uint32_t off, bytes;   // offset of the segment inside the tile's stream
 };
 struct Stream {
+    int64_t kv_off;                  // attention: element offset of the chunk's first K/V row
     Seg seg[2];
     int nseg;
     uint32_t total;
@@ -334,6 +335,21 @@ __device__ __forceinline__ int attn_old_rows(const Params& p, int b, int c, int 
     const int c0 = c * chunk;
     if (c0 > pos) return -1;                 // chunk past pos: inactive
     return min(c0 + chunk, pos) - c0;        // cached positions strictly before pos
+}
+
+// Element offset of the first K/V row of attention chunk c (positions [c C, c C + C)) of
+// sequence b, layer l, KV head g.  Contiguous cache: rows of a head are consecutive.  Paged cache:
+// the chunk is one block of the pool, found through the block table; false when the table entry
+// is outside the pool (nothing is read or written then).
+__device__ __forceinline__ bool kv_chunk_off(const Params& p, int b, int l, int g, int c, int C, int64_t& off) {
+    if (!p.kv_table) {
+        off = int64_t(b) * p.kv_bstride + int64_t(l) * p.kv_lstride + int64_t(g) * p.kv_hstride + int64_t(c) * C * p.d;
+        return true;
+    }
+    const int blk = __ldg(p.kv_table + size_t(b) * p.kv_max_blocks + c);
+    if (unsigned(blk) >= unsigned(p.kv_n_blocks)) return false;
+    off = int64_t(l) * p.kv_lstride + int64_t(g) * p.kv_hstride + int64_t(blk) * C * p.d;
+    return true;
 }
 
 __device__ __forceinline__ const uint8_t* word_ptr(const int32_t* w) {
@@ -350,6 +366,7 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
     st.nseg = 0;
     st.total = 0;
     st.pages = 0;
+    st.kv_off = 0;
     st.inter = 0;
     st.rows = st.rowbytes = st.rpp = 0;
     const int op = w[W_OP];
@@ -376,9 +393,9 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
             unsigned(c) >= unsigned(p.n_chunk) || C != p.attn_chunk)
             return MK_ERR_BOUNDS;
         const int n_old = attn_old_rows(p, b, c, C);
+        if (n_old >= 0 && !kv_chunk_off(p, b, l, g, c, C, st.kv_off)) return MK_ERR_BOUNDS;
         if (n_old > 0) {
-            const size_t base = size_t(b) * p.kv_bstride + size_t(l) * p.kv_lstride + size_t(g) * p.kv_hstride +
-                                size_t(c) * C * p.d;
+            const size_t base = size_t(st.kv_off);
             const uint32_t nb = uint32_t(n_old * p.d * 2);
             st.seg[0] = {reinterpret_cast<const uint8_t*>(p.kc + base), 0u, nb};
             st.seg[1] = {reinterpret_cast<const uint8_t*>(p.vc + base), nb, nb};
@@ -440,6 +457,7 @@ __device__ void loader(const Params& p, const Shared& sh) {
         }
         si.first_page = int32_t(page_seq);
         si.n_pages = st.pages;
+        si.kv_off = st.kv_off;
         si.first_slot = int32_t(cur_slot);
         si.first_phase = int32_t(cur_phase);
         if (is_matvec(si.w[W_OP])) {   // shape of the op (bind-time table) and of this tile
@@ -1213,8 +1231,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         //    read until they carry this step's tag, in one pass whose items (q pairs, then k pairs,
         //    then v elements) are spread over all warps, so no warp waits on two round trips
         {
-            const size_t cache = size_t(b) * p.kv_bstride + size_t(l) * p.kv_lstride + size_t(g) * p.kv_hstride +
-                                 size_t(pos) * d;
+            const size_t cache = size_t(si.kv_off) + size_t(pos - ch * C) * d;   // row pos (this chunk holds it)
             const uint64_t* kh = qkv + p.qd + size_t(g) * d;
             const uint64_t* vh = qkv + p.qd + p.kvd + size_t(g) * d;
             const int nq = hpg * half, nk = has_new ? half : 0, nitems = nq + nk + (has_new ? d : 0);
