@@ -48,11 +48,34 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank space: edits to comments do not change the code."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':   # string literal, kept whole
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_hash() -> str:
+    """Hash of the kernel's code (mk_kernel.cu + mk_internal.h, comments and spacing ignored)."""
     h = hashlib.sha256()
     for name in ("mk_kernel.cu", "mk_internal.h"):
-        with open(os.path.join(os.path.dirname(KERNEL_SRC), name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(os.path.dirname(KERNEL_SRC), name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -206,8 +206,8 @@ mk_status mk_set_timeout(mk_ctx* c, uint64_t ns);
  *    acquire/release semantics where a reader has no tag to check (the argmax over the LM-head
  *    partials, the MLP down projection's SwiGLU input, matvec inputs cut into segments).
  *  MK_SYNC_COUNTERS: every instruction first waits all of its counters with acquire semantics
- *    (the page's protocol: wait the counters, run the body, fence, then add the completions); the tag checks then
- *    pass at the first read.
+ *    (the page's protocol: wait the counters, run the body, fence, then add the completions);
+ *    the tag checks then pass at the first read.
  * Both modes run the same arithmetic in the same order: their results are bit-identical.
  * Takes effect at the next launch.  Errors: MK_ERR_ARG (null context, unknown mode). */
 typedef enum { MK_SYNC_TAGS = 0, MK_SYNC_COUNTERS = 1 } mk_sync_mode;

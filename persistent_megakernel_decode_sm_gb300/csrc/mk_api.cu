@@ -253,7 +253,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
             const int64_t n = (bytes + pb - 1) / pb;
             return (bytes % pb == 0 || pb % bytes == 0) ? n : n + 1;
         };
-        for (int K : {H, qd, c.ffn})   // non-pair steps: 16 units of one row segment each
+        for (int K : {H, qd, c.ffn})   // non-pair steps: 16 units (two per consumer warp) of one row segment each
             need_pages = std::max<int64_t>(need_pages, span(16 * seg_bytes(K)));
         const int64_t rpp = pb / (2ll * H);   // gate/up: 8 pairs -> row groups of rpp rows, two pages each
         need_pages = std::max<int64_t>(need_pages, 2 * ((rpp % 8 == 0 || 8 % rpp == 0) ? std::max<int64_t>(1, 8 / rpp)

@@ -10,12 +10,15 @@
 //     with cp.async.bulk global->shared copies (evict-first L2 policy) completed on the page's
 //     mbarrier.  Weights and old KV rows do not depend on any counter, so they are fetched
 //     before the instruction's dependencies resolve -- the page ring absorbs dependency stalls.
-//  * 8 consumer warps: wait the instruction's counters (one thread spins with relaxed loads,
-//     then an acquire fence), run the body on the leased pages, release the pages (mbarrier
-//     arrive), write outputs, and hand the instruction to the publisher.
-//  * publisher warp (one thread): fence.acq_rel.gpu, then adds the completions to the global
-//     counters -- data first, then the fence, then the counter (the page's data-visibility
-//     contract), without stalling the consumers on the fence.
+//  * 8 consumer warps: learn that the instruction's inputs are ready, run the body on the leased
+//     pages, release the pages (mbarrier arrive), write outputs, and hand the instruction to
+//     the publisher.  By default (epoch-tagged activations) a consumer polls the tagged words it
+//     reads until they carry this step's tag; inputs without a tag (the argmax's partials,
+//     segmented 64-bit inputs) and the counters mode wait the instruction's counters instead
+//     (one thread spins with relaxed loads, then an acquire fence).
+//  * publisher warp (one thread): adds the completions to the global counters, after a
+//     fence.release.gpu where a reader will rely on the counter (data first, then the fence,
+//     then the counter: the page's data-visibility contract), without stalling the consumers.
 // Every wait (counter spin, page / slot barrier) has a time budget; when it runs out the CTA
 // records the error, all roles leave their loops, the loader drains its copies in flight and
 // the kernel returns (no trap, no endless spin).
