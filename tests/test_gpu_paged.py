@@ -93,3 +93,26 @@ def test_paged_bind_rejects_a_block_size_other_than_the_chunk():
     with pytest.raises(mk.MkError) as e:
         mk.Decoder(mk.Schedule(s.cfg, mk.device_sm_count()), s.weights, pool, pages=(table, 32, n_blocks))
     assert e.value.status == mk.MK_ERR_ARG
+
+
+def test_paged_chained_counters_mode_matches_contiguous_tags_mode():
+    """The paged cache, chained steps and the counters synchronisation together give the same
+    tokens and logits as the contiguous cache stepped one call at a time in the default mode."""
+    s = make_setup("tiny")
+    S = mk.device_sm_count()
+    pool, table, n_blocks = to_paged(s.kv, spare=3, seed=11)
+    a = mk.Decoder(mk.Schedule(s.cfg, S), s.weights, s.kv)
+    b = mk.Decoder(mk.Schedule(s.cfg, S), s.weights, pool, pages=(table, BLOCK, n_blocks))
+    b.set_sync("counters")
+    n = 5
+    toks_b = b.steps(s.tokens, s.pos, n)
+    t, toks_a = list(s.tokens), []
+    for i in range(n):
+        t = a.step(t, [p + i for p in s.pos])
+        toks_a.append(t)
+    assert toks_a == toks_b
+    assert torch.equal(a.logits, b.logits)
+    back = from_paged(pool, table, tuple(s.kv.k.shape))
+    assert torch.equal(back.k, s.kv.k) and torch.equal(back.v, s.kv.v)
+    a.close()
+    b.close()
