@@ -63,7 +63,10 @@ typedef struct {
     int32_t tile_bytes;  /* 0: per-SM tiles at batch 1, 131072 at batch > 1; else the target
                             weight bytes per matvec tile (capped at 8 rows for QKV, O and down,
                             16 gate/up pairs, 32 LM-head rows)                                   */
-    int32_t attn_chunk;  /* KV positions per split-K attention tile; default 64                 */
+    int32_t attn_chunk;  /* KV positions per split-K attention tile; 0: 64, doubled (up to 256)
+                            while batch * n_kv_heads * ceil(max_seq / chunk) > 152 (a property
+                            of the configuration, not of sm_count);
+                            n_q_heads / n_kv_heads * attn_chunk <= 2048 (checked at bind)        */
     int32_t rows_qkv, rows_o, pairs_up, rows_down, rows_lm; /* explicit rows (pairs) per tile,
                             overriding the above; rows_qkv <= head_dim                           */
     uint64_t shuffle_seed; /* 0: cost-ordered placement; otherwise a seeded shuffled placement  */
@@ -108,6 +111,11 @@ mk_status mk_schedule_queues(const mk_schedule* s, const int32_t** queues, int32
 /* Per-step counter totals: total[c] = sum of the deltas published into counter c in one step
  * (read-only pointer to n uint32, valid until the schedule is freed). */
 mk_status mk_schedule_counters(const mk_schedule* s, const uint32_t** totals, int32_t* n_counters);
+
+/* The schedule's attention chunk (KV positions per split-K attention tile: the option, or the
+ * default the scheduler chose); a paged KV cache must use it as its block size.  MK_ERR_ARG on
+ * null arguments. */
+mk_status mk_schedule_attn_chunk(const mk_schedule* s, int32_t* out);
 
 /* Overwrites one word of the host queue copy (for fault-injection tests of the device runtime's
  * checks; contexts bound earlier are not affected).  MK_ERR_ARG if an index is out of range. */
@@ -161,7 +169,7 @@ typedef struct {
  *               step (the caller may rewrite it between steps).  An entry outside [0, n_blocks)
  *               that a step needs stops the step with MK_ERR_BOUNDS (nothing is accessed there).
  *  block_size   positions per block: must equal the schedule's attention chunk
- *               (mk_sched_opts.attn_chunk, default 64).
+ *               (mk_schedule_attn_chunk).
  *  max_blocks   table entries per sequence, max_blocks * block_size >= max_seq.
  *  n_blocks     blocks in the pool per (layer, KV head): head_stride >= n_blocks*block_size*head_dim. */
 typedef struct {

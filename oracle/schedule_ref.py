@@ -62,7 +62,7 @@ M64 = (1 << 64) - 1
 class SchedOpts:
     page_bytes: int = 32768
     tile_bytes: int = 0     # 0: per-SM tiles at batch 1, 131072-byte tiles at batch > 1
-    attn_chunk: int = 64
+    attn_chunk: int = 0     # 0: 64 positions, doubled up to 256 while B * n_kv * chunks > 152
     shuffle_seed: int = 0
     rows_qkv: int = 0   # 0: derived from tile_bytes
     rows_o: int = 0
@@ -144,13 +144,28 @@ class Tile:
         return self.stream_bytes + TILE_OVERHEAD
 
 
+ATTN_CHUNK_TILES = 152   # the default chunk grows while a layer has more chunks than this
+
+
+def attn_chunk(cfg, o: SchedOpts, S: int) -> int:
+    """KV positions per split-K attention tile: the option, else 64 doubled (at most to 256) as
+    long as the chunks of all sequences and KV heads outnumber ATTN_CHUNK_TILES -- a property of
+    the configuration, independent of the queue count S."""
+    if o.attn_chunk:
+        return o.attn_chunk
+    C = 64
+    while C < 256 and cfg.batch * cfg.n_kv_heads * ceil_div(cfg.max_seq, C) > ATTN_CHUNK_TILES:
+        C *= 2
+    return C
+
+
 def enumerate_tiles(cfg, o: SchedOpts, S: int) -> Tuple[List[Tile], Counters, Dict[str, int]]:
     L, H, F, V, B = cfg.n_layers, cfg.hidden, cfg.ffn, cfg.vocab, cfg.batch
     nq, nkv, d = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     qd, kvd = nq * d, nkv * d
     hpg = nq // nkv
     R = tile_rows(cfg, o, S)
-    C = o.attn_chunk
+    C = attn_chunk(cfg, o, S)
     nchunk = ceil_div(cfg.max_seq, C)
     cnt = Counters(cfg)
     n_qkv_rows = qd + 2 * kvd
@@ -313,7 +328,7 @@ def build_schedule(cfg, S: int, opts: Optional[SchedOpts] = None):
             for c, dl in t.pubs:
                 totals[c] += dl
     info = dict(rows=R, n_tiles=len(tiles), counters=cnt, tiles=tiles,
-                n_chunks=ceil_div(cfg.max_seq, o.attn_chunk))
+                n_chunks=ceil_div(cfg.max_seq, attn_chunk(cfg, o, S)))
     return queues, totals.astype(np.uint32), info
 
 

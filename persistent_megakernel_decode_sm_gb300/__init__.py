@@ -35,7 +35,7 @@ SYNC_TAGS, SYNC_COUNTERS = 0, 1   # mk_sync_mode
 EXPORTS = ["mk_build_schedule", "mk_schedule_queues", "mk_schedule_counters", "mk_schedule_patch",
            "mk_scratch_bytes", "mk_schedule_free", "mk_bind", "mk_set_timeout", "mk_decode_step",
            "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind", "mk_set_trace",
-           "mk_decode_step_static", "mk_set_sync", "mk_decode_steps", "mk_bind_paged"]
+           "mk_decode_step_static", "mk_set_sync", "mk_decode_steps", "mk_bind_paged", "mk_schedule_attn_chunk"]
 
 
 class MkError(RuntimeError):
@@ -82,6 +82,8 @@ lib.mk_schedule_queues.restype = ctypes.c_int
 lib.mk_schedule_queues.argtypes = [_P, ctypes.POINTER(_I32P), _I32P, _I32P]
 lib.mk_schedule_counters.restype = ctypes.c_int
 lib.mk_schedule_counters.argtypes = [_P, ctypes.POINTER(ctypes.POINTER(ctypes.c_uint32)), _I32P]
+lib.mk_schedule_attn_chunk.restype = ctypes.c_int
+lib.mk_schedule_attn_chunk.argtypes = [_P, _I32P]
 lib.mk_schedule_patch.restype = ctypes.c_int
 lib.mk_schedule_patch.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
 lib.mk_scratch_bytes.restype = ctypes.c_size_t
@@ -166,6 +168,13 @@ class Schedule:
     @property
     def n_counters(self) -> int:
         return int(self.totals().size)
+
+    @property
+    def attn_chunk(self) -> int:
+        """KV positions per split-K attention tile (the block size of a paged KV cache)."""
+        v = ctypes.c_int32()
+        _check(lib.mk_schedule_attn_chunk(self.handle, ctypes.byref(v)))
+        return v.value
 
     @property
     def scratch_bytes(self) -> int:

@@ -225,7 +225,10 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     }
     const void* fn = megakernel_fn(cpl);
     if (!fn) return fail(MK_ERR_ARG, "no kernel for %d chunks per lane", cpl);
-    int asf = std::max(hpg * g.attn_chunk, hpg * g.n_chunk);
+    // the attention scratch holds the combine factors; a chunk's scores use the shared-x buffer
+    if (hpg * g.attn_chunk > kXBuf)
+        return fail(MK_ERR_ARG, "attn_chunk %d: the scores of %d heads do not fit %d floats", g.attn_chunk, hpg, kXBuf);
+    int asf = hpg * g.n_chunk;
     asf = (asf + 3) & ~3;
     const int qrf = (hpg * d + 3) & ~3;
     const int misc0 = smem_misc_bytes(0, asf, qrf);

@@ -42,6 +42,7 @@ constexpr int kTraceWords = 8;       // trace stamps per instruction
 constexpr unsigned kPollBackoffNs = 128;   // pause between two polling rounds of tagged data
 constexpr int kCombStride = 64;      // split-row partials per instruction slot (rows x segments x 2 <= 64)
 constexpr int kXBuf = 2048;          // floats of the shared matvec input buffer (one x per CTA)
+constexpr int kAttnChunkTiles = 152; // default attention chunk: grown while a layer has more chunks
 
 
 // ---- resolved schedule parameters -----------------------------------------------------------

@@ -1223,7 +1223,12 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     const int n_old = attn_old_rows(p, b, ch, C);
     const size_t lb = size_t(l) * p.B + b;
     const uint64_t* qkv = p.qkv + lb * p.nqkv;
-    float* sc = c.sh.ascr;   // [hpg][C] scores, then [hpg][n_chunk] combine factors
+    // [hpg][C] scores in the shared-x buffer: no warp reads a matvec input while the tile runs
+    // (every warp passed its previous instruction at the first barrier, and the next
+    // instruction's input is written only after the arrival barrier below); [hpg][n_chunk]
+    // combine factors in the attention scratch
+    float* sc = c.sh.xbuf;
+    float* cf = c.sh.ascr;
     if (n_old >= 0) {
         const int pos = p.pos[b];
         const bool has_new = pos < ch * C + C;
@@ -1363,7 +1368,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         for (int k = c.lane; k < nact; k += 32) {
             const float* ph = pb + (size_t(k) * hpg + h) * (d + 2);
             const float f = expf(ph[d] - M);
-            sc[h * p.n_chunk + k] = f;
+            cf[h * p.n_chunk + k] = f;
             Ls = fmaf(f, ph[d + 1], Ls);
         }
         Ls = warp_sum(Ls);
@@ -1373,7 +1378,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     uint64_t* out = p.o + lb * p.qd + size_t(g) * hpg * d;
     for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
         const int h = idx / d, e = idx % d;
-        const float* f = sc + h * p.n_chunk;
+        const float* f = cf + h * p.n_chunk;
         const float* ph = pb + size_t(h) * (d + 2) + e;
         const size_t cs = size_t(hpg) * (d + 2);   // stride of one chunk's partials
         float a4[4] = {0.f, 0.f, 0.f, 0.f};

@@ -123,7 +123,17 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     Geometry g{};
     g.page_bytes = o.page_bytes ? o.page_bytes : 32768;
     g.tile_bytes = o.tile_bytes;   // 0: matvec tiles sized per SM (batch 1) / 131072 bytes (batch > 1)
-    g.attn_chunk = o.attn_chunk ? o.attn_chunk : 64;
+    // attention chunk: 64 positions, doubled (up to 256) while the chunks of all sequences and KV
+    // heads would outnumber the 152 SMs of a GB300 (long contexts, batches): fewer, larger split-K
+    // tiles.  A property of the model configuration alone, like every tile shape: the results do
+    // not depend on the SM count the schedule is built for.
+    g.attn_chunk = o.attn_chunk;
+    if (g.attn_chunk == 0) {
+        g.attn_chunk = 64;
+        while (g.attn_chunk < 256 &&
+               int64_t(c.batch) * c.n_kv_heads * cdiv(c.max_seq, g.attn_chunk) > kAttnChunkTiles)
+            g.attn_chunk *= 2;
+    }
     g.shuffle_seed = o.shuffle_seed;
     if (g.page_bytes < 1024 || g.page_bytes % 128 || g.page_bytes > (1 << 20))
         return fail(MK_ERR_ARG, "page_bytes must be a multiple of 128 in [1024, 1 MiB]");
@@ -351,6 +361,12 @@ extern "C" mk_status mk_schedule_queues(const mk_schedule* s, const int32_t** q,
     *q = s->queues.data();
     *S = s->S;
     *Q = s->Q;
+    return MK_OK;
+}
+
+extern "C" mk_status mk_schedule_attn_chunk(const mk_schedule* s, int32_t* out) {
+    if (!s || !out) return fail(MK_ERR_ARG, "null argument");
+    *out = s->geo.attn_chunk;
     return MK_OK;
 }
 
