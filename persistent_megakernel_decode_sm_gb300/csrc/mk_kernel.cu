@@ -1234,10 +1234,14 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         const bool has_new = pos < ch * C + C;
         const int n = n_old + (has_new ? 1 : 0);
         const float2* rp = p.rope + size_t(pos) * half;
-        if (!cbar(c, pc)) return false;   // the previous block-level body is done with the scratch
         // 1. rotate q of the group's heads; RoPE k, round k and v, append them.  q, k and v are
         //    read until they carry this step's tag, in one pass whose items (q pairs, then k pairs,
-        //    then v elements) are spread over all warps, so no warp waits on two round trips
+        //    then v elements) are spread over all warps, so no warp waits on two round trips.  No
+        //    barrier first: what this phase writes (rotated q, new k and v) is read only by
+        //    attention phases 2-4, and every warp left those of an earlier attention tile before
+        //    that tile's arrival barrier; a warp still finishing another kind of instruction
+        //    touches none of it (the scores, which reuse the shared-x buffer, wait for the barrier
+        //    after this phase)
         {
             const size_t cache = size_t(si.kv_off) + size_t(pos - ch * C) * d;   // row pos (this chunk holds it)
             const uint64_t* kh = qkv + p.qd + size_t(g) * d;
