@@ -24,6 +24,19 @@ def test_cpp_schedule_bit_exact_vs_restatement(name, S):
     assert np.array_equal(s.totals(), t)
 
 
+def test_default_attention_chunk_depends_on_the_configuration_only():
+    """64 positions, doubled up to 256 while a layer has more than 152 chunks -- whatever the SM
+    count, so outputs stay bit-identical across SM counts."""
+    expect = {"tiny": 64, "llama1b_ctx512": 64, "llama1b_reduced": 64, "llama8b_ctx2048": 128,
+              "llama1b_ctx8192": 256, "llama1b_batch8": 256}
+    for name, C in expect.items():
+        cfg = get_workload(name).cfg
+        for S in (1, 37, 152, 1000):
+            assert mk.Schedule(cfg, S).attn_chunk == C, (name, S)
+            assert sr.attn_chunk(cfg, sr.SchedOpts(), S) == C, (name, S)
+        assert mk.Schedule(cfg, 152, attn_chunk=32).attn_chunk == 32
+
+
 @pytest.mark.parametrize("seed", [1, 12345, 2 ** 63 + 17])
 def test_cpp_shuffled_placement_bit_exact(seed):
     cfg = get_workload("llama1b_ctx512").cfg
