@@ -134,3 +134,30 @@ def test_counter_totals_match_waits():
     assert t[cnt.attn(2, 0, 1)] == info["n_chunks"]
     assert t[cnt.lm()] == -(-cfg.vocab // info["rows"]["lm"])
     assert t[cnt.final()] == B
+
+
+def test_random_small_configs_bit_exact_valid_and_deadlock_free():
+    """Seeded random small shapes and SM counts: the C++ schedule equals the restatement, passes
+    the validator, and the host simulator runs it without a deadlock or an early read."""
+    rng = np.random.default_rng(2024)
+    checked = 0
+    for _ in range(60):
+        nkv = int(rng.choice([1, 2, 4]))
+        hpg = int(rng.choice([1, 2, 4]))
+        d = int(rng.choice([64, 128]))
+        cfg = small_config(n_layers=int(rng.integers(1, 4)), hidden=int(rng.choice([128, 256, 512])),
+                           n_q_heads=nkv * hpg, n_kv_heads=nkv, head_dim=d,
+                           ffn=8 * int(rng.integers(16, 120)), vocab=8 * int(rng.integers(64, 600)),
+                           batch=int(rng.choice([1, 1, 2, 3])), max_seq=int(rng.integers(8, 400)))
+        S = int(rng.choice([1, 3, 7, 16, 37]))
+        try:
+            s = mk.Schedule(cfg, S)
+        except mk.MkError:
+            continue
+        q, t, _ = sr.build_schedule(cfg, S)
+        assert np.array_equal(s.queues(), q), cfg
+        assert np.array_equal(s.totals(), t), cfg
+        assert sr.validate(q, t, cfg) == [], cfg
+        assert sr.simulate(q, t, cfg, n_epochs=1, seed=checked) == [], cfg
+        checked += 1
+    assert checked >= 40
