@@ -207,12 +207,13 @@ mk_status mk_set_timeout(mk_ctx* c, uint64_t ns);
  *  MK_SYNC_TAGS (default): the activation vectors one operator hands to the next (q/k/v,
  *    attention output, both residual streams) are epoch-tagged -- every element is
  *    one 64-bit word holding the fp32 value and the step's tag -- and a consumer polls the
- *    elements it reads until each carries this step's tag.  One read both proves readiness and
- *    fetches the data, so a dependency costs one memory round trip instead of the publisher's
- *    release fence, the counter add, the consumer's counter poll and then the data read.
- *    Such a consumer reads no counter at all.  Counters are still published, and they keep
- *    acquire/release semantics where a reader has no tag to check (the argmax over the LM-head
- *    partials, the MLP down projection's SwiGLU input, matvec inputs cut into segments).
+ *    elements it reads until each carries this step's tag.  The SwiGLU output is 32-bit fp32
+ *    words whose three low mantissa bits hold a 3-bit step tag, polled the same way.  One read
+ *    both proves readiness and fetches the data, so a dependency costs one memory round trip
+ *    instead of the publisher's release fence, the counter add, the consumer's counter poll and
+ *    then the data read.  Such a consumer reads no counter at all.  Counters are still
+ *    published, and they keep acquire/release semantics where a reader has no tag to check (the
+ *    argmax over the LM-head partials, matvec inputs of 64-bit words cut into segments).
  *  MK_SYNC_COUNTERS: every instruction first waits all of its counters with acquire semantics
  *    (the page's protocol: wait the counters, run the body, fence, then add the completions);
  *    the tag checks then pass at the first read.
