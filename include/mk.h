@@ -2,9 +2,10 @@
  * mk.h -- C ABI of the persistent decode megakernel for GB300 (sm_103a).
  *
  * One decode step of a whole Llama-style decoder runs as ONE resident kernel launch: a grid of
- * S CTAs (one per SM) in which every CTA interprets its own queue of tile instructions, waits on
- * global completion counters before an instruction, streams the instruction's weights / KV rows
- * through leased shared-memory pages, runs the operator body and publishes its completions.
+ * S CTAs (one per SM) in which every CTA interprets its own queue of tile instructions, waits
+ * for an instruction's inputs (epoch-tagged data, or global completion counters: mk_set_sync),
+ * streams the instruction's weights / KV rows through leased shared-memory pages, runs the
+ * operator body and publishes its completions.
  * The design follows the "Inference MegaKernel" page, section "Hand-written whole-model
  * MegaKernel" (principle, scheduling and data flow; its control-flow pseudocode; its object
  * table), and the four device-protocol contracts of its section "Unified framework" (data
