@@ -193,9 +193,12 @@ class Decoder:
 
     ``pages`` (optional) binds a paged KV cache: a tuple (block_table, block_size, n_blocks) with
     block_table a CUDA int32 tensor [batch, max_blocks]; kv.k / kv.v are then the block pools,
-    shaped [n_layers, n_kv_heads, n_blocks * block_size, head_dim]."""
+    shaped [n_layers, n_kv_heads, n_blocks * block_size, head_dim].  ``scratch`` (optional) is the
+    caller's device scratch (at least ``sched.scratch_bytes`` bytes, 256-byte aligned); by default
+    one is allocated."""
 
-    def __init__(self, sched: Schedule, weights, kv, stream=None, timeout_ns: Optional[int] = None, pages=None):
+    def __init__(self, sched: Schedule, weights, kv, stream=None, timeout_ns: Optional[int] = None, pages=None,
+                 scratch=None):
         import torch
         cfg = sched.cfg
         dev = weights.embed.device
@@ -220,7 +223,10 @@ class Decoder:
             self._pages = mk_kv_pages(_ptr(table), int(block_size), int(table.shape[-1]), int(n_blocks))
             self._table = table
         self.counters = torch.zeros(sched.n_counters, dtype=torch.int32, device=dev)
-        self.scratch = torch.empty(sched.scratch_bytes // 4 + 64, dtype=torch.int32, device=dev)
+        if scratch is None:
+            scratch = torch.empty(sched.scratch_bytes // 4 + 64, dtype=torch.int32, device=dev)
+        assert scratch.device == dev and scratch.numel() * scratch.element_size() >= sched.scratch_bytes
+        self.scratch = scratch
         self.logits = torch.empty((cfg.batch, cfg.vocab), dtype=torch.float32, device=dev)
         self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
         h = _P()

@@ -39,6 +39,10 @@ struct mk_ctx {
     int32_t* h_result;   // pinned: err[16] then tokens[8]
     uint32_t epoch;
     bool poisoned;
+    // a step ran on the static scratch: the bound scratch's activation words did not advance with
+    // the epoch (the 3-bit SwiGLU tag repeats every 7 steps), so it is cleared before its next use
+    bool bound_stale;
+    const int32_t* last_err;   // error word of the last launched step (bound or static scratch)
     mk_model_cfg cfg;
 };
 
@@ -366,6 +370,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     untagged(OP_UPGATE, {OP_OPROJ});
     untagged(OP_LMHEAD, {OP_DOWN});
     p.timeout_ns = 2000000000ull;
+    x->last_err = p.err;
     p.smem_misc_off = n_pages * g.page_bytes;
     p.attn_scratch_floats = asf;
     p.qrot_floats = qrf;
@@ -375,7 +380,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     if ((e = cudaMemsetAsync(counters, 0, s->totals.size() * 4, x->stream)) != cudaSuccess ||
         (e = cudaMemsetAsync(sb + sl.err, 0, 256, x->stream)) != cudaSuccess ||
         (e = cudaMemsetAsync(sb + sl.x_attn, 0, sl.lm_part - sl.x_attn, x->stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(sb + sl.lm_part, 0xFF, size_t(c.batch) * s->S * kNumConsumerWarps * 16, x->stream)) != cudaSuccess)
+        (e = cudaMemsetAsync(sb + sl.lm_part, 0xFF, sl.rope - sl.lm_part, x->stream)) != cudaSuccess)
         return bail(cuda_fail(e, "cudaMemsetAsync"));
     if ((e = launch_rope_table(reinterpret_cast<float2*>(sb + sl.rope), c.max_seq, d, c.rope_theta, x->stream)) !=
         cudaSuccess)
@@ -405,28 +410,50 @@ extern "C" mk_status mk_set_trace(mk_ctx* c, uint64_t* buf) {
     return MK_OK;
 }
 
+// Clears the activation words, attention partials and LM-head partials of a scratch (tag 0 is
+// never a step's tag; LM-head partial epochs 0xFFFFFFFF are never a step's epoch).
+static cudaError_t clear_scratch(const Params& p, cudaStream_t st) {
+    const size_t act = size_t(reinterpret_cast<const uint8_t*>(p.lm_part) - reinterpret_cast<const uint8_t*>(p.x_attn));
+    const size_t lm = size_t(reinterpret_cast<const uint8_t*>(p.rope) - reinterpret_cast<const uint8_t*>(p.lm_part));
+    cudaError_t e = cudaMemsetAsync(p.x_attn, 0, act, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.lm_part, 0xFF, lm, st);
+    return e;
+}
+
+// Launches the resident grid with fully prepared parameters (scratch pointers, tokens,
+// positions) at the context's epoch, then advances the epoch.
+static mk_status launch_params(mk_ctx* c, Params& p) {
+    p.epoch = c->epoch;
+    p.tag = c->epoch + 1u;
+    void* args[] = {&p};
+    cudaError_t e = cudaLaunchCooperativeKernel(c->fn, dim3(c->grid), dim3(kThreads), args, size_t(c->smem), c->stream);
+    if (e == cudaErrorCooperativeLaunchTooLarge)
+        return fail(MK_ERR_RESOURCES, "cooperative launch of %d CTAs does not fit the device", c->grid);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
+    c->last_err = p.err;
+    c->epoch += 1;
+    return MK_OK;
+}
+
 // One step on the bound stream.  Its tokens come from the host (tokens) or, when tok_dev is set,
 // from device memory (a chained step: the previous step's greedy tokens); pos[b] + dpos is its
 // position.  The caller has checked the arguments.
 static mk_status launch(mk_ctx* c, const int32_t* tokens, const int32_t* pos, int32_t dpos, float* logits,
                         int32_t* next_tokens_dev, const int32_t* tok_dev) {
     Params p = c->base;
+    if (c->bound_stale) {   // steps ran on the static scratch since this scratch was last used
+        const cudaError_t e = clear_scratch(p, c->stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(bound scratch)");
+        c->bound_stale = false;
+    }
     for (int b = 0; b < c->cfg.batch; ++b) {
         p.tok[b] = tok_dev ? 0 : tokens[b];
         p.pos[b] = pos[b] + dpos;
     }
     p.tok_dev = tok_dev;
-    p.epoch = c->epoch;
-    p.tag = c->epoch + 1u;
     p.logits = logits;
     p.next_dev = next_tokens_dev;
-    void* args[] = {&p};
-    cudaError_t e = cudaLaunchCooperativeKernel(c->fn, dim3(c->grid), dim3(kThreads), args, size_t(c->smem), c->stream);
-    if (e == cudaErrorCooperativeLaunchTooLarge)
-        return fail(MK_ERR_RESOURCES, "cooperative launch of %d CTAs does not fit the device", c->grid);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
-    c->epoch += 1;
-    return MK_OK;
+    return launch_params(c, p);
 }
 
 static mk_status check_step_args(mk_ctx* c, const int32_t* tokens, const int32_t* pos, int32_t n_steps,
@@ -450,8 +477,10 @@ extern "C" mk_status mk_launch_step(mk_ctx* c, const int32_t* tokens, const int3
     return launch(c, tokens, pos, 0, logits, next_tokens_dev, nullptr);
 }
 
+// Reads back the error word (and output tokens) of the context's last step -- from the scratch
+// that step used -- and poisons the context on a device error.
 static mk_status read_status(mk_ctx* c, int32_t* info) {
-    cudaError_t e = cudaMemcpyAsync(c->h_result, c->base.err, 96, cudaMemcpyDeviceToHost, c->stream);
+    cudaError_t e = cudaMemcpyAsync(c->h_result, c->last_err, 96, cudaMemcpyDeviceToHost, c->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) {
         c->poisoned = true;
@@ -557,6 +586,13 @@ extern "C" mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, con
     if (need > kStaticScratchBytes)
         return fail(MK_ERR_CAPACITY, "step needs %zu bytes of scratch, the static array holds %zu", need,
                     kStaticScratchBytes);
+    for (int b = 0; b < c->cfg.batch; ++b) {
+        if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab) return fail(MK_ERR_ARG, "token %d out of range", tokens[b]);
+        if (pos[b] < 0 || pos[b] >= c->cfg.max_seq)
+            return fail(MK_ERR_ARG, "pos %d outside the KV capacity [0, %d)", pos[b], c->cfg.max_seq);
+        p.tok[b] = tokens[b];
+        p.pos[b] = pos[b];
+    }
     auto move = [&](auto* ptr) {
         using T = std::remove_pointer_t<decltype(ptr)>;
         return reinterpret_cast<T*>(base + (reinterpret_cast<const uint8_t*>(ptr) - bound));
@@ -571,47 +607,24 @@ extern "C" mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, con
     p.h = move(p.h);
     p.lm_part = move(p.lm_part);
     p.rope = move(const_cast<float2*>(p.rope));
-    for (int b = 0; b < c->cfg.batch; ++b) {
-        if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab) return fail(MK_ERR_ARG, "token %d out of range", tokens[b]);
-        if (pos[b] < 0 || pos[b] >= c->cfg.max_seq)
-            return fail(MK_ERR_ARG, "pos %d outside the KV capacity [0, %d)", pos[b], c->cfg.max_seq);
-        p.tok[b] = tokens[b];
-        p.pos[b] = pos[b];
-    }
     // the array keeps the previous call's contents: reset what must start fresh (error word and
-    // output tokens, the activation words -- another context may have left its own tags there --,
-    // the LM-head partials' epoch tags) and rebuild the RoPE table for this model
-    const size_t lm_bytes = size_t(c->cfg.batch) * size_t(c->grid) * kNumConsumerWarps * 2 * 16;
+    // output tokens; the activation words -- another context may have left its own tags there --;
+    // the LM-head partials' epochs) and rebuild the RoPE table for this model
     cudaError_t e;
-    if ((e = cudaMemsetAsync(p.err, 0, 256, c->stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(p.x_attn, 0, size_t(reinterpret_cast<uint8_t*>(p.lm_part) - reinterpret_cast<uint8_t*>(p.x_attn)),
-                             c->stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(p.lm_part, 0xFF, lm_bytes, c->stream)) != cudaSuccess)
+    if ((e = cudaMemsetAsync(p.err, 0, 256, c->stream)) != cudaSuccess || (e = clear_scratch(p, c->stream)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync(static scratch)");
     if ((e = launch_rope_table(const_cast<float2*>(p.rope), c->cfg.max_seq, c->cfg.head_dim, c->cfg.rope_theta,
                                c->stream)) != cudaSuccess)
         return cuda_fail(e, "rope table kernel");
-    p.epoch = c->epoch;
-    p.tag = c->epoch + 1u;
     p.logits = logits;
     p.next_dev = nullptr;
-    void* args[] = {&p};
-    e = cudaLaunchCooperativeKernel(c->fn, dim3(c->grid), dim3(kThreads), args, size_t(c->smem), c->stream);
-    if (e == cudaErrorCooperativeLaunchTooLarge)
-        return fail(MK_ERR_RESOURCES, "cooperative launch of %d CTAs does not fit the device", c->grid);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
-    c->epoch += 1;
-    e = cudaMemcpyAsync(c->h_result, p.err, 96, cudaMemcpyDeviceToHost, c->stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
-    if (e != cudaSuccess) {
-        c->poisoned = true;
-        return cuda_fail(e, "step readback");
-    }
-    if (c->h_result[0] != 0) {
-        c->poisoned = true;
-        return fail(mk_status(c->h_result[0]), "device error %d (CTA %d, queue slot %d)", c->h_result[0],
-                    c->h_result[1], c->h_result[2]);
-    }
+    p.tok_dev = nullptr;
+    const mk_status st = launch_params(c, p);
+    if (st != MK_OK) return st;
+    // the bound scratch's activation tags fell behind the epoch: its next step clears them first
+    c->bound_stale = true;
+    const mk_status rs = read_status(c, nullptr);
+    if (rs != MK_OK) return rs;
     for (int b = 0; b < c->cfg.batch; ++b) next_tokens[b] = c->h_result[16 + b];
     return MK_OK;
 }

@@ -160,3 +160,35 @@ def test_tagged_wait_timeout_is_reported():
     s2 = make_setup("tiny")
     dec2 = mk.Decoder(mk.Schedule(s2.cfg, mk.device_sm_count()), s2.weights, s2.kv)
     _assert_parity(run_parity(s2, dec2, steps=1))
+
+
+def test_lm_partials_of_ctas_without_lm_rows_are_cleared_at_bind():
+    # only four CTAs hold LM-head tiles; every other CTA's per-warp (max, index, epoch) partials
+    # must come from the bind's clearing, not from whatever the scratch held before: fill the
+    # scratch with entries (1e30, index 0, epoch 0) -- they would win the first step's argmax if
+    # the bind left any of them in place
+    s = make_setup("tiny")
+    sched = mk.Schedule(s.cfg, mk.device_sm_count(), rows_lm=s.cfg.vocab // 4)
+    poison = torch.zeros((sched.scratch_bytes // 16 + 16, 4), dtype=torch.int32, device="cuda")
+    poison[:, 0] = int(np.array([1e30], dtype=np.float32).view(np.int32)[0])
+    dec = mk.Decoder(sched, s.weights, s.kv, scratch=poison.view(-1))
+    r = run_parity(s, dec, steps=2)
+    _assert_parity(r)
+    assert r["token_checked"] >= 1
+    dec.close()
+
+
+def test_decode_from_position_zero():
+    # an empty cache: the first position attends to itself only (the attention output is v0)
+    s = make_setup("tiny")
+    from workload import empty_kv
+    s.kv = empty_kv(s.cfg, device="cuda")
+    s.kh[...] = 0
+    s.vh[...] = 0
+    s.pos = [0]
+    dec = mk.Decoder(mk.Schedule(s.cfg, mk.device_sm_count()), s.weights, s.kv)
+    r = run_parity(s, dec, steps=4)
+    _assert_parity(r)
+    kv = kv_agreement(s, [[0, 1, 2, 3]])
+    assert kv["worst_in_steps"] <= 1.0 and kv["frac_equal"] > 0.97, kv
+    dec.close()
