@@ -21,7 +21,7 @@
 #include "mk_internal.h"
 
 namespace mk {
-const void* megakernel_fn(int cpl);
+const void* megakernel_fn();
 cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st);
 }  // namespace mk
 
@@ -148,9 +148,11 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, std::
                 break;
             default: break;
         }
-        if (src0) {
-            const int64_t rpp = g.page_bytes / (2ll * H);   // gate/up: row groups, gate and up pages alternating
-            const int64_t pages = op == OP_UPGATE ? 2 * ((a1 + rpp - 1) / rpp) : (b0 + b1 + g.page_bytes - 1) / g.page_bytes;
+        if (src0) {   // whole rows per page; gate/up: gate and up row groups in alternate pages
+            const int64_t K = op == OP_OPROJ ? qd : (op == OP_DOWN ? F : H);
+            const int64_t rpp = g.page_bytes / (2 * K);
+            if (rpp < 1) return bad("a page holds no row");
+            const int64_t pages = ((a1 + rpp - 1) / rpp) * (op == OP_UPGATE ? 2 : 1);
             if (pages != x[W_NPAGES] || b0 + b1 > (int64_t(1) << 31) - 1) return bad("page count");
             put64(x + W_SRC0, src0);
             put64(x + W_SRC1, src1);
@@ -218,55 +220,38 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
     if (s->S > sms) return fail(MK_ERR_RESOURCES, "schedule has %d queues but the device has %d SMs", s->S, sms);
-    // matvec rows are cut into <= 2048-element segments (a power-of-two count, <= 8); the kernel
-    // is instantiated for the largest number of 16-byte chunks a lane holds of one segment
-    int cpl = 1;
-    for (int K : {H, qd, c.ffn}) {
-        int nseg = 1;
-        while (K > 2048 * nseg) nseg <<= 1;
-        if (nseg > 8 || K % (8 * nseg)) return fail(MK_ERR_ARG, "matvec row length %d cannot be cut into segments", K);
-        cpl = std::max(cpl, (K / nseg / 8 + 31) / 32);
+    // shared input buffer: the hidden size (the normed inputs) and at least kMinXBuf floats (the
+    // attention's scores and combine); matvec inputs longer than it are polled per warp
+    const int xbuf = std::max(kMinXBuf, H);
+    if (hpg * g.attn_chunk > xbuf)
+        return fail(MK_ERR_ARG, "attn_chunk %d: the scores of %d heads do not fit %d floats", g.attn_chunk, hpg, xbuf);
+    // matvec shapes: whole rows per page, segments per row (a property of the row length only)
+    MvShape mv[OP_COUNT] = {};
+    int comb_stride = 1;
+    for (int op : {int(OP_QKV), int(OP_OPROJ), int(OP_UPGATE), int(OP_DOWN), int(OP_LMHEAD)}) {
+        const int K = op == OP_OPROJ ? qd : (op == OP_DOWN ? c.ffn : H);
+        mv[op] = mv_shape(K, g.page_bytes, xbuf);
+        if (mv[op].rpp < 1)
+            return fail(MK_ERR_CAPACITY, "a %d-byte page holds no %d-element row", g.page_bytes, K);
+        if (mv[op].segch > 32 * kCpl)
+            return fail(MK_ERR_ARG, "matvec row length %d cannot be cut into %d segments", K, kMaxSeg);
+        if (mv[op].G > 1) comb_stride = std::max(comb_stride, mv[op].rpp * mv[op].G);
     }
-    const void* fn = megakernel_fn(cpl);
-    if (!fn) return fail(MK_ERR_ARG, "no kernel for %d chunks per lane", cpl);
-    // the attention scratch holds the combine factors; a chunk's scores use the shared-x buffer
-    if (hpg * g.attn_chunk > kXBuf)
-        return fail(MK_ERR_ARG, "attn_chunk %d: the scores of %d heads do not fit %d floats", g.attn_chunk, hpg, kXBuf);
+    const void* fn = megakernel_fn();
     int asf = hpg * g.n_chunk;
     asf = (asf + 3) & ~3;
     const int qrf = (hpg * d + 3) & ~3;
-    const int misc0 = smem_misc_bytes(0, asf, qrf);
-    int n_pages = (optin - misc0 - 1024) / (g.page_bytes + 16);
+    int n_pages = 0;
+    while (int64_t(n_pages + 1) * g.page_bytes + smem_misc_bytes(n_pages + 1, asf, qrf, xbuf, comb_stride) <= optin)
+        ++n_pages;
     if (n_pages < 1) return fail(MK_ERR_CAPACITY, "no room for a page ring");
-    int misc = smem_misc_bytes(n_pages, asf, qrf);
-    while (n_pages > 0 && int64_t(n_pages) * g.page_bytes + misc > optin) misc = smem_misc_bytes(--n_pages, asf, qrf);
+    const int misc = smem_misc_bytes(n_pages, asf, qrf, xbuf, comb_stride);
     // capacity: at batch > 1 a tile's pages are held until it is done, so the ring must hold the
-    // largest tile; at batch 1 matvec tiles stream step by step (16 row segments, or 8 gate/up
-    // pairs, per step): the ring must hold the pages of one step (+1 for a straddled boundary) and
-    // an attention tile
+    // largest tile; at batch 1 a matvec tile streams through the ring one group of two pages at a
+    // time, and an attention tile holds its K and V rows
     int need_pages = 2;
-    if (c.batch > 1) {
-        need_pages = std::max(need_pages, s->max_pages);
-    } else {
-        auto seg_bytes = [&](int K) {
-            int nseg = 1;
-            while (K > 2048 * nseg) nseg <<= 1;
-            return int64_t(K) * 2 / nseg;
-        };
-        const int64_t pb = g.page_bytes;
-        // pages one step can touch: a span of `bytes` starting at a multiple of `bytes` covers
-        // ceil(bytes / pb) pages when the two sizes divide one another, else one more
-        auto span = [&](int64_t bytes) {
-            const int64_t n = (bytes + pb - 1) / pb;
-            return (bytes % pb == 0 || pb % bytes == 0) ? n : n + 1;
-        };
-        for (int K : {H, qd, c.ffn})   // non-pair steps: 16 units (two per consumer warp) of one row segment each
-            need_pages = std::max<int64_t>(need_pages, span(16 * seg_bytes(K)));
-        const int64_t rpp = pb / (2ll * H);   // gate/up: 8 pairs -> row groups of rpp rows, two pages each
-        need_pages = std::max<int64_t>(need_pages, 2 * ((rpp % 8 == 0 || 8 % rpp == 0) ? std::max<int64_t>(1, 8 / rpp)
-                                                                                       : (8 + rpp - 1) / rpp + 1));
-        need_pages = std::max<int64_t>(need_pages, (2ll * g.attn_chunk * d * 2 + pb - 1) / pb);
-    }
+    if (c.batch > 1) need_pages = std::max(need_pages, s->max_pages);
+    else need_pages = std::max<int>(need_pages, int((2ll * g.attn_chunk * d * 2 + g.page_bytes - 1) / g.page_bytes));
     if (n_pages < need_pages)
         return fail(MK_ERR_CAPACITY, "page ring of %d pages cannot hold the %d pages a step needs", n_pages, need_pages);
     const int smem = n_pages * g.page_bytes + misc;
@@ -309,12 +294,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     const ScratchLayout sl = scratch_layout(c, g, s->S);
     uint8_t* sb = static_cast<uint8_t*>(scratch);
     Params& p = x->base;
-    for (int op = 0; op < OP_COUNT; ++op) {
-        const int K = op == OP_OPROJ ? qd : (op == OP_DOWN ? c.ffn : H);
-        int nseg = 1, lg = 0;
-        while (K > 2048 * nseg) { nseg <<= 1; ++lg; }
-        p.mv[op] = {K, nseg, lg, uint32_t(K) * 2u, (uint32_t(K) * 2u) >> lg, int32_t(((uint32_t(K) * 2u) >> lg) >> 4)};
-    }
+    for (int op = 0; op < OP_COUNT; ++op) p.mv[op] = mv[op];
     p.L = L; p.H = H; p.nq = c.n_q_heads; p.nkv = c.n_kv_heads; p.d = d; p.F = c.ffn; p.V = c.vocab;
     p.B = c.batch; p.max_seq = c.max_seq; p.hpg = hpg; p.qd = qd; p.kvd = c.n_kv_heads * d;
     p.nqkv = qd + 2 * p.kvd;
@@ -354,26 +334,17 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     p.h = reinterpret_cast<uint32_t*>(sb + sl.h);
     p.lm_part = reinterpret_cast<int4*>(sb + sl.lm_part);
     p.rope = reinterpret_cast<const float2*>(sb + sl.rope);
-    // Readers without tags: the argmax (LM-head partials) and every matvec whose 64-bit tagged
-    // rows are cut into segments (its per-warp input segment is read after an acquiring wait);
-    // their producers publish after a release fence.  The MLP down projection polls its
-    // 3-bit-tagged input like any tagged reader.
+    // The one reader without tags: the argmax over the LM-head partials, after an acquiring wait
+    // on the counter the LM-head tiles publish after a release fence.
     p.acquire_ops = 1u << OP_ARGMAX;
     p.release_ops = 1u << OP_LMHEAD;
-    auto untagged = [&](int op, std::initializer_list<int> producers) {
-        if (p.mv[op].nseg <= 1) return;
-        p.acquire_ops |= 1u << op;
-        for (int q : producers) p.release_ops |= 1u << q;
-    };
-    untagged(OP_QKV, {OP_DOWN});
-    untagged(OP_OPROJ, {OP_ATTN});
-    untagged(OP_UPGATE, {OP_OPROJ});
-    untagged(OP_LMHEAD, {OP_DOWN});
     p.timeout_ns = 2000000000ull;
     x->last_err = p.err;
     p.smem_misc_off = n_pages * g.page_bytes;
     p.attn_scratch_floats = asf;
     p.qrot_floats = qrf;
+    p.xbuf_floats = xbuf;
+    p.comb_stride = comb_stride;
 
     // tags start at 0 (never a step's tag): words left in the scratch by an earlier binding must
     // not pass for this context's first steps

@@ -7,6 +7,12 @@
 
 #include "mk.h"
 
+#ifdef __CUDACC__
+#define MK_HD __host__ __device__
+#else
+#define MK_HD
+#endif
+
 namespace mk {
 
 // ---- instruction encoding ([S, Q, 32] int32, see mk_schedule_queues) ---------------------
@@ -22,26 +28,28 @@ constexpr int kWords = 32;
 constexpr int kMaxWait = 4;
 constexpr int kMaxPub = 2;
 constexpr int kMaxBatch = 8;
-constexpr int kMaxRows = 32;       // rows of one matvec tile (pairs of gate/up rows: half)
 constexpr int kMaxHpg = 8;         // query heads per KV head
 constexpr int kMaxHeadDim = 128;
 constexpr int kMaxK = 16384;       // longest matvec row (elements)
 constexpr int64_t kTileOverhead = 1024;
 
 // shared-memory layout of one CTA (after the page ring)
-constexpr int kNumConsumerWarps = 8;
+constexpr int kNumConsumerWarps = 16;
 constexpr int kConsumerThreads = kNumConsumerWarps * 32;
-constexpr int kLoaderWarp = 8;
-constexpr int kPublisherWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kLoaderWarp = 16;
+constexpr int kPublisherWarp = 17;
+constexpr int kThreads = 576;
 constexpr int kSlots = 16;   // instruction slots in flight
 constexpr int kQWin = 16;    // instructions per queue-window buffer (two buffers, bulk-copied)
 constexpr int kMaxLayersSmem = 40;   // layer pointer table cached in shared memory
 constexpr int kDone = 64;            // completion records the publisher may lag behind
 constexpr int kTraceWords = 8;       // trace stamps per instruction
 constexpr unsigned kPollBackoffNs = 128;   // pause between two polling rounds of tagged data
-constexpr int kCombStride = 64;      // split-row partials per instruction slot (rows x segments x 2 <= 64)
-constexpr int kXBuf = 2048;          // floats of the shared matvec input buffer (one x per CTA)
+constexpr int kCpl = 4;              // 16-byte chunks a lane holds of its row segment (at most)
+constexpr int kMaxSeg = 16;          // row segments of a matvec (a power of two dividing the warp count)
+constexpr int kDirectMinK = 4097;    // rows this long take their input per warp, not through the shared buffer
+constexpr int kResBuf = 64;          // residual words of a tile's rows staged in shared memory (per buffer)
+constexpr int kMinXBuf = 3072;       // floats of the shared input buffer at least (attention scores, combine)
 constexpr int kAttnChunkTiles = 152; // default attention chunk: grown while a layer has more chunks
 
 
@@ -97,7 +105,7 @@ inline ScratchLayout scratch_layout(const mk_model_cfg& c, const Geometry& g, in
     s.part = take(L * B * size_t(c.n_kv_heads) * g.n_chunk * hpg * (d + 2) * 4);   // fp32 chunk partials
     s.o = take(L * B * qd * 8);                       // tagged
     s.h = take(L * B * size_t(c.ffn) * 4);            // fp32 with a 3-bit tag
-    s.lm_part = take(B * size_t(S) * kNumConsumerWarps * 2 * 16);   // per (sequence, CTA, warp half): max, index, epoch
+    s.lm_part = take(B * size_t(S) * kNumConsumerWarps * 16);   // per (sequence, CTA, warp): max, index, epoch
     s.rope = take(size_t(c.max_seq) * (d / 2) * 8);
     s.total = off;
     return s;
@@ -113,17 +121,38 @@ struct LayerPtrs {
     const uint16_t* wdown;
 };
 
-// matvec shape per opcode, resolved at bind
+// Matvec shape per opcode, resolved at bind.  A row of K elements is cut into G segments of
+// segch 16-byte chunks (the last one may be shorter); warp w always computes segment w mod G of
+// every row, holding that segment of the input vector in registers (at most kCpl chunks per lane).
+// G is the smallest power of two that keeps a segment within 32 * kCpl chunks: a property of K
+// alone, so the arithmetic of a row never depends on the tiling or the SM count.  Pages hold whole
+// rows (rpp per page).
 struct MvShape {
-    int32_t K;               // row length (elements)
-    int32_t nseg, lognseg;   // segments per row (each <= 2048 elements), log2
-    uint32_t rowbytes, segbytes;
-    int32_t segch;           // 16-byte chunks per segment
+    int32_t K, chunks;       // row length: elements, 16-byte chunks
+    int32_t G, logG;         // segments per row, log2
+    int32_t segch;           // chunks per segment
+    uint32_t rowbytes;       // 2 K
+    int32_t rpp;             // whole rows per page
+    int32_t direct;          // 1: each warp polls its own input segment (no shared input buffer)
 };
+
+MK_HD inline MvShape mv_shape(int K, int page_bytes, int xbuf_floats) {
+    MvShape m{};
+    m.K = K;
+    m.chunks = K / 8;
+    m.G = 1;
+    m.logG = 0;
+    while ((m.chunks + m.G - 1) / m.G > 32 * kCpl && m.G < kMaxSeg) { m.G *= 2; ++m.logG; }
+    m.segch = (m.chunks + m.G - 1) / m.G;
+    m.rowbytes = uint32_t(K) * 2u;
+    m.rpp = page_bytes / int(m.rowbytes);
+    m.direct = K > xbuf_floats ? 1 : 0;
+    return m;
+}
 
 // ---- kernel parameters (passed by value) ----------------------------------------------------
 struct Params {
-    MvShape mv[OP_COUNT];
+    MvShape mv[OP_COUNT];    // matvec shapes by opcode (unused entries zero)
     // model
     int32_t L, H, nq, nkv, d, F, V, B, max_seq, hpg, qd, kvd, nqkv;
     float rms_eps, attn_scale;
@@ -154,7 +183,7 @@ struct Params {
     float* part;        // [L][B][nkv][n_chunk][hpg][d + 2] attention chunk partials
     uint64_t* o;        // tagged [L][B][qd]: attention output
     uint32_t* h;        // [L][B][F]: SwiGLU output, fp32 with a 3-bit step tag in the low mantissa bits
-    int4* lm_part;     // [B][S][16]: (max bits, index, epoch, 0)
+    int4* lm_part;      // [B][S][kNumConsumerWarps]: (max bits, index, epoch, 0)
     const float2* rope; // [max_seq][d/2] (cos, sin)
     // step
     uint32_t epoch;
@@ -173,38 +202,32 @@ struct Params {
     int32_t smem_misc_off;   // byte offset of the non-ring area
     int32_t attn_scratch_floats;
     int32_t qrot_floats;
+    int32_t xbuf_floats;     // shared input buffer (floats)
+    int32_t comb_stride;     // segment partials per page slot
 };
 
-// one instruction slot: words + where its stream sits + decoded matvec shape.  16-byte aligned
-// and sized: the loader fills the words of each slot of the array with 16-byte stores
+// one instruction slot: words + where its stream sits + the matvec shape.  16-byte aligned and
+// sized: the loader fills the words of each slot of the array with 16-byte stores
 struct alignas(16) SlotInfo {
     int32_t w[kWords];
     int32_t first_page;      // global page sequence number of the stream's first page
     int32_t n_pages;
     int32_t first_slot;      // ring slot of the first page
-    int32_t K;               // matvec: row length (elements)
-    int32_t nseg, lognseg;   // segments per row (<= 2048 elements each), log2
-    int32_t units;           // row units (rows, or gate/up pairs) x segments when split, else row units
-    int32_t split;           // 1: the segments of a row go to different warps (batch 1)
-    uint32_t rowbytes, segbytes;
-    int32_t segch;           // 16-byte chunks per segment
     int32_t first_phase;     // mbarrier phase parity of the first page
     int64_t kv_off;          // attention: element offset of the chunk's first K/V row in the cache
+    int32_t rows;            // matvec: rows (gate/up: pairs) of the tile
+    int32_t inter;           // matvec: 1 = gate/up, pages alternate gate rows and up rows
+    MvShape mv;              // matvec: the operator's shape
 };
 static_assert(sizeof(SlotInfo) % 16 == 0 && offsetof(SlotInfo, w) == 0, "slot words must stay 16-byte aligned");
 
-#ifdef __CUDACC__
-#define MK_HD __host__ __device__
-#else
-#define MK_HD
-#endif
-
 // byte offsets of the non-ring shared memory (after the page ring); shared by host and device
 struct MiscLayout {
-    uint32_t slots, qwin, layers, bars, lmbest, comb, combcnt, pubinfo, red, qrot, ascr, ml, kv, xbuf, gbuf, total;
+    uint32_t slots, qwin, layers, bars, comb, combcnt, pubinfo, red, qrot, ascr, ml, kv, res, xbuf, total;
 };
 
-MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qrot_floats) {
+MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qrot_floats, int xbuf_floats,
+                                    int comb_stride) {
     MiscLayout m{};
     uint32_t o = 0;
     auto take = [&o](uint32_t bytes, uint32_t align) {
@@ -217,26 +240,25 @@ MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qr
     m.qwin = take(2u * kQWin * kWords * 4u, 16);
     m.layers = take(uint32_t(sizeof(LayerPtrs)) * kMaxLayersSmem, 16);
     m.bars = take(8u * (2u + 2u * uint32_t(n_pages) + 2u * kSlots + kDone + 3u), 8);  // qfull, full, empty, ins, done, cbar, xfull, xfree
-    m.lmbest = take(8u * kNumConsumerWarps * 2u * kMaxBatch, 8);   // LM-head running (max, index) per warp half / sequence
-    m.comb = take(4u * kSlots * kCombStride, 16);   // split-row segment partials
-    m.combcnt = take(4u * kSlots * kMaxRows, 16);
+    m.comb = take(4u * 2u * uint32_t(n_pages) * uint32_t(comb_stride), 16);   // segment partials per (page slot, unit)
+    m.combcnt = take(4u * uint32_t(n_pages) * uint32_t(comb_stride), 16);    // arrivals per (page slot, row)
     m.pubinfo = take(4u * kDone * 8u, 16);            // completion words of in-flight instructions
-    m.red = take(4u * 64u, 16);                     // argmax scratch [16]; abort flag [32], published count [33],
+    m.red = take(4u * 64u, 16);                     // argmax scratch [0..31]; abort flag [32], published count [33],
                                                     // stream bytes the loader has issued [34..35] (u64),
                                                     // last-arrival flag [40], per-warp sums of
-                                                    // squares of the shared x [48..55]
+                                                    // squares of the shared input [48..63]
     m.qrot = take(4u * uint32_t(qrot_floats), 16);
     m.ascr = take(4u * uint32_t(attn_scratch_floats), 16);
     m.ml = take(4u * 4u * kMaxHpg, 16);             // (m, l) per head, combine L per head
     m.kv = take(2u * 2u * kMaxHeadDim, 16);         // new k, v (bf16)
-    m.xbuf = take(4u * kXBuf, 16);                  // shared matvec input (raw), one per CTA
-    m.gbuf = take(2u * kXBuf, 16);                  // its RMSNorm gain (bf16)
+    m.res = take(4u * 2u * kResBuf, 16);            // residual words of the tile's rows, two buffers
+    m.xbuf = take(4u * uint32_t(xbuf_floats), 16);  // shared matvec input (raw), one per CTA
     m.total = (o + 255u) & ~255u;
     return m;
 }
 
-inline int smem_misc_bytes(int n_pages, int attn_scratch_floats, int qrot_floats) {
-    return int(misc_layout(n_pages, attn_scratch_floats, qrot_floats).total);
+inline int smem_misc_bytes(int n_pages, int attn_scratch_floats, int qrot_floats, int xbuf_floats, int comb_stride) {
+    return int(misc_layout(n_pages, attn_scratch_floats, qrot_floats, xbuf_floats, comb_stride).total);
 }
 
 // records a message for mk_last_error() and returns st

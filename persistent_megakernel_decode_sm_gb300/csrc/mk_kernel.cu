@@ -219,16 +219,15 @@ struct Shared {
     uint64_t* ins_full;
     uint64_t* ins_empty;
     uint64_t* done;
-    uint64_t* cbar;    // consumer-warp barrier (8 arrivals)
-    uint64_t* xfull;   // shared x written (1 arrival: warp 0)
-    uint64_t* xfree;   // shared x taken by every warp (8 arrivals)
-    float* xbuf;       // [kXBuf] shared matvec input
-    uint16_t* gbuf;    // [kXBuf] its RMSNorm gain (bf16)
-    float2* lmbest;    // [8 warps][kMaxBatch] LM-head running (max, index)
-    float* comb;       // [kSlots][64] split-row segment partials
-    int* combcnt;      // [kSlots][kMaxRows] split-row slot: owning row << 8 | arrivals, -1 free
+    uint64_t* cbar;    // consumer-warp barrier (16 arrivals)
+    uint64_t* xfull;   // shared input written (16 arrivals)
+    uint64_t* xfree;   // shared input taken by every warp (16 arrivals)
+    float* xbuf;       // [xbuf_floats] shared matvec input
+    float* res;        // [2][kResBuf] residual words of a tile's rows
+    float* comb;       // [n_pages][comb_stride][2] row-segment partials
+    int* combcnt;      // [n_pages][comb_stride] segment arrivals per row
     int* pubinfo;      // [kDone][8]: opcode, #completions, (counter, delta) x 2
-    float* red;        // [16] argmax scratch
+    float* red;        // [32] argmax scratch
     int* abort;        // [1]
     int* published;    // [1] instructions the publisher has retired
     unsigned long long* issued;   // [1] stream bytes the loader has staged into pages
@@ -241,7 +240,7 @@ struct Shared {
 };
 
 __device__ __forceinline__ Shared carve(uint8_t* base, const Params& p) {
-    const MiscLayout m = misc_layout(p.n_pages, p.attn_scratch_floats, p.qrot_floats);
+    const MiscLayout m = misc_layout(p.n_pages, p.attn_scratch_floats, p.qrot_floats, p.xbuf_floats, p.comb_stride);
     uint8_t* b = base + p.smem_misc_off;
     Shared s;
     s.ring = base;
@@ -258,8 +257,7 @@ __device__ __forceinline__ Shared carve(uint8_t* base, const Params& p) {
     s.xfull = s.cbar + 1;
     s.xfree = s.cbar + 2;
     s.xbuf = reinterpret_cast<float*>(b + m.xbuf);
-    s.gbuf = reinterpret_cast<uint16_t*>(b + m.gbuf);
-    s.lmbest = reinterpret_cast<float2*>(b + m.lmbest);
+    s.res = reinterpret_cast<float*>(b + m.res);
     s.comb = reinterpret_cast<float*>(b + m.comb);
     s.combcnt = reinterpret_cast<int*>(b + m.combcnt);
     s.pubinfo = reinterpret_cast<int*>(b + m.pubinfo);
@@ -330,7 +328,7 @@ struct Stream {
     uint32_t total;
     int pages;
     int inter;                       // gate/up tile: page 2j = gate rows [j rpp, (j+1) rpp), 2j+1 = up rows
-    uint32_t rows, rowbytes, rpp;    // (interleaved streams)
+    uint32_t rows, rowbytes, rpp;    // matvec: whole rows per page (0 rows: a plain byte stream)
 };
 
 __device__ __forceinline__ int attn_old_rows(const Params& p, int b, int c, int chunk) {
@@ -373,23 +371,20 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
     st.inter = 0;
     st.rows = st.rowbytes = st.rpp = 0;
     const int op = w[W_OP];
-    if (is_matvec(op)) {
+    if (is_matvec(op)) {   // whole rows per page; gate/up: gate and up row groups in alternate pages
         const uint32_t b0 = uint32_t(w[W_BYTES0]), b1 = uint32_t(w[W_BYTES1]);
         st.seg[0] = {word_ptr(w + W_SRC0), 0u, b0};
         st.seg[1] = {word_ptr(w + W_SRC1), b0, b1};
         st.nseg = b1 ? 2 : 1;
         st.total = b0 + b1;
-        if (b0 == 0) return MK_ERR_BOUNDS;
-        if (op == OP_UPGATE) {   // pair rows of gate and up in adjacent pages
-            st.inter = 1;
-            st.rows = uint32_t(w[W_A1]);
-            st.rowbytes = uint32_t(p.H) * 2u;
-            st.rpp = uint32_t(p.page_bytes) / st.rowbytes;
-            if (st.rpp == 0 || b0 != st.rows * st.rowbytes || b1 != b0) return MK_ERR_BOUNDS;
-            st.pages = int(2u * ((st.rows + st.rpp - 1u) / st.rpp));
-            if (st.pages > w[W_NPAGES]) return MK_ERR_CAPACITY;
-            return MK_OK;
-        }
+        st.inter = op == OP_UPGATE;
+        st.rows = uint32_t(w[W_A1]);
+        st.rowbytes = p.mv[op].rowbytes;
+        st.rpp = uint32_t(p.mv[op].rpp);
+        if (b0 == 0 || st.rpp == 0 || b0 != st.rows * st.rowbytes || b1 != (st.inter ? b0 : 0u)) return MK_ERR_BOUNDS;
+        st.pages = int((st.rows + st.rpp - 1u) / st.rpp) * (st.inter ? 2 : 1);
+        if (st.pages > w[W_NPAGES] || (p.B > 1 && st.pages > p.n_pages)) return MK_ERR_CAPACITY;
+        return MK_OK;
     } else if (op == OP_ATTN) {
         const int l = w[W_LAYER], b = w[W_B], g = w[W_A0], c = w[W_A1], C = w[W_A2];
         if (unsigned(l) >= unsigned(p.L) || unsigned(b) >= unsigned(p.B) || unsigned(g) >= unsigned(p.nkv) ||
@@ -464,17 +459,9 @@ __device__ void loader(const Params& p, const Shared& sh) {
         si.first_slot = int32_t(cur_slot);
         si.first_phase = int32_t(cur_phase);
         if (is_matvec(si.w[W_OP])) {   // shape of the op (bind-time table) and of this tile
-            const MvShape& m = p.mv[si.w[W_OP]];
-            const int n = si.w[W_A1];
-            const bool split = p.B == 1 && m.nseg > 1;   // segments of a row on different warps
-            si.K = m.K;
-            si.nseg = m.nseg;
-            si.lognseg = m.lognseg;
-            si.split = split;
-            si.units = split ? n * m.nseg : n;
-            si.rowbytes = m.rowbytes;
-            si.segbytes = m.segbytes;
-            si.segch = m.segch;
+            si.rows = int32_t(st.rows);
+            si.inter = st.inter;
+            si.mv = p.mv[si.w[W_OP]];
         }
         {   // completion words for the publisher, which may lag up to kDone instructions behind
             const uint64_t t0 = globaltimer();
@@ -508,12 +495,12 @@ __device__ void loader(const Params& p, const Shared& sh) {
                 break;
             }
             uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
-            if (st.inter) {   // one row group of gate (even page) or up (odd page)
-                const uint32_t r0 = uint32_t(pg >> 1) * st.rpp;
+            if (st.rows) {   // matvec: a group of whole rows (gate/up: gate rows on even pages, up rows on odd)
+                const uint32_t r0 = uint32_t(st.inter ? pg >> 1 : pg) * st.rpp;
                 const uint32_t bytes = min(st.rpp, st.rows - r0) * st.rowbytes;
                 mbar_arrive_expect_tx(sh.full + ps, bytes);
-                bulk_g2s(dst, ((pg & 1) ? st.seg[1].src : st.seg[0].src) + size_t(r0) * st.rowbytes, bytes, sh.full + ps,
-                         pol);
+                bulk_g2s(dst, ((st.inter && (pg & 1)) ? st.seg[1].src : st.seg[0].src) + size_t(r0) * st.rowbytes, bytes,
+                         sh.full + ps, pol);
             } else {
                 const uint32_t lo = uint32_t(pg) * PB;
                 const uint32_t hi = min(lo + PB, st.total);
@@ -605,19 +592,20 @@ __device__ void publisher(const Params& p, const Shared& sh) {
 }
 
 // ------------------------------------------------------------------------- consumer warps ---
-// The 8 consumer warps walk the instruction stream independently.  A matvec tile needs no
-// block-level synchronisation: each warp owns whole (row, segment) units with its segment of x
-// in registers; a row split into segments is summed by its last-arriving warp in shared memory,
-// always in segment order.  Attention, combine and argmax cooperate through an mbarrier-based
-// consumer barrier whose waits are bounded and give up when the CTA aborts.
+// The 16 consumer warps walk the instruction stream independently.  A matvec tile needs one
+// consumer barrier per input vector (every warp takes its segment of the input once it is
+// complete in shared memory) and none per row: warp w computes segment w mod G of the rows of
+// each page group, with its segment of the input in registers; the G segment sums of a row meet
+// in shared memory, where the last-arriving warp adds them in segment order and writes the row.
+// Attention and argmax cooperate through an mbarrier-based consumer barrier whose waits are
+// bounded and give up when the CTA aborts.
 
 struct Cw {
     const Params& p;
     const Shared& sh;
     int warp, lane;
     uint32_t cb_phase;   // consumer-barrier uses so far
-    uint32_t rot;        // running count of row units (mod 8): rotates units across warps
-    uint32_t xphase;     // shared-x loads so far
+    uint32_t xphase;     // input loads so far
 };
 
 __device__ __forceinline__ const uint8_t* ring_ptr(const Shared& sh, const Params& p, uint32_t first_slot, uint32_t off) {
@@ -739,161 +727,6 @@ __device__ __forceinline__ bool load8x(const XSrc& x, int e0, float* v, uint32_t
     load8_bf16(x.b + e0, v);
     return true;
 }
-// eight elements' values, for a reader whose counter wait acquired (tagged words: values only,
-// four 16-byte loads of (value, tag, value, tag))
-__device__ __forceinline__ void load8v(const XSrc& x, int e0, float* v) {
-    if (x.t) {
-        const uint4* f = reinterpret_cast<const uint4*>(x.t + e0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 w = __ldcg(f + j);
-            v[2 * j] = __uint_as_float(w.x);
-            v[2 * j + 1] = __uint_as_float(w.z);
-        }
-    } else if (x.h) {
-        const uint4 a = __ldcg(reinterpret_cast<const uint4*>(x.h + e0));
-        const uint4 b = __ldcg(reinterpret_cast<const uint4*>(x.h + e0 + 4));
-        v[0] = __uint_as_float(a.x & ~7u); v[1] = __uint_as_float(a.y & ~7u);
-        v[2] = __uint_as_float(a.z & ~7u); v[3] = __uint_as_float(a.w & ~7u);
-        v[4] = __uint_as_float(b.x & ~7u); v[5] = __uint_as_float(b.y & ~7u);
-        v[6] = __uint_as_float(b.z & ~7u); v[7] = __uint_as_float(b.w & ~7u);
-    } else {
-        load8_bf16(x.b + e0, v);
-    }
-}
-
-// This warp's segment `seg` of the length-K input (lane owns chunks lane + 32 i), optionally
-// RMS-normalised: the sum of squares runs over all segments in a fixed order, so every warp
-// derives the same scale.  The SwiGLU output (32-bit words with a 3-bit tag) is polled until
-// every element carries this step's tag; 64-bit tagged inputs cut into segments are read after an
-// acquiring counter wait (a tag poll of a whole segment would not fit the registers next to x):
-// values only, no tags.  False when the CTA aborts or the poll runs out of time.
-template <int CPL>
-__device__ bool load_xw(const Cw& c, float (&xr)[8 * CPL], int K, int nseg, int seg, const XSrc& src,
-                        const uint16_t* gain, int pc) {
-    const int seglen = K / nseg, segch = seglen / 8;
-    Spin sp;
-    while (true) {
-        bool ok = true;
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-            const int ch = c.lane + 32 * i;
-            if (ch < segch) {
-                if (src.h) ok &= ld8_htagged(src.h + seg * seglen + ch * 8, &xr[8 * i], htag(c.p.tag));
-                else load8v(src, seg * seglen + ch * 8, &xr[8 * i]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
-            }
-        }
-        if (__all_sync(0xFFFFFFFFu, ok)) break;
-        if (!spin_more(c, sp, pc)) return false;
-    }
-    if (!gain) return true;
-    float ss = 0.f;
-#pragma unroll 1
-    for (int s = 0; s < nseg; ++s) {   // (this warp's own segment is read again: same values)
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-            const int ch = c.lane + 32 * i;
-            if (ch < segch) {
-                float v[8];
-                load8v(src, s * seglen + ch * 8, v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
-            }
-        }
-    }
-    ss = warp_sum(ss);
-    const float scale = rsqrtf(ss / float(K) + c.p.rms_eps);
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        const int ch = c.lane + 32 * i;
-        if (ch < segch) {
-            const uint4 g = __ldg(reinterpret_cast<const uint4*>(gain + seg * seglen + ch * 8));
-            xr[8 * i + 0] = (xr[8 * i + 0] * scale) * bf_lo(g.x);
-            xr[8 * i + 1] = (xr[8 * i + 1] * scale) * bf_hi(g.x);
-            xr[8 * i + 2] = (xr[8 * i + 2] * scale) * bf_lo(g.y);
-            xr[8 * i + 3] = (xr[8 * i + 3] * scale) * bf_hi(g.y);
-            xr[8 * i + 4] = (xr[8 * i + 4] * scale) * bf_lo(g.z);
-            xr[8 * i + 5] = (xr[8 * i + 5] * scale) * bf_hi(g.z);
-            xr[8 * i + 6] = (xr[8 * i + 6] * scale) * bf_lo(g.w);
-            xr[8 * i + 7] = (xr[8 * i + 7] * scale) * bf_hi(g.w);
-        }
-    }
-    return true;
-}
-
-// One input vector per CTA: the 8 consumer warps read x (K <= kXBuf elements) from L2 together --
-// thread t takes the 8-element chunks t, t + 256, ... and its RMSNorm gain in the same round
-// trip -- into shared memory, with one sum of squares per warp; after the CTA-wide arrival every
-// warp adds the 8 sums in warp order (the same scale everywhere) and takes its chunks
-// (lane + 32 i).  Every warp runs this at every change of input (the key sequence is the same in
-// all warps); xfree keeps a warp from overwriting a buffer another warp still reads.
-template <int CPL>
-__device__ bool shared_x(Cw& c, float (&xr)[8 * CPL], int K, const XSrc& src, const uint16_t* gain, int pc) {
-    const int segch = K / 8;
-    const int tid = c.warp * 32 + c.lane;
-    if (c.xphase > 0 && !wait_bar(c.p, c.sh, c.sh.xfree, (c.xphase - 1u) & 1u, ROLE_CONSUMER, pc)) return false;
-    float ss = 0.f;
-    for (int base = 0; base < segch; base += kConsumerThreads) {   // warp-uniform trip count
-        const int ch = base + tid;
-        const bool valid = ch < segch;
-        uint4 g = make_uint4(0u, 0u, 0u, 0u);
-        if (gain && valid) g = __ldg(reinterpret_cast<const uint4*>(gain + ch * 8));
-        float v[8];
-        Spin sp;
-        while (true) {
-            const bool ok = valid ? load8x(src, ch * 8, v, c.p.tag) : true;
-            if (__all_sync(0xFFFFFFFFu, ok)) break;
-            if (!spin_more(c, sp, pc)) return false;
-        }
-        if (valid) {
-            *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8) = make_float4(v[0], v[1], v[2], v[3]);
-            *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
-            if (gain) *reinterpret_cast<uint4*>(c.sh.gbuf + ch * 8) = g;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
-        }
-    }
-    ss = warp_sum(ss);
-    if (c.lane == 0) c.sh.red[48 + c.warp] = ss;
-    __syncwarp();
-    if (c.lane == 0) mbar_arrive(c.sh.xfull);
-    if (!wait_bar(c.p, c.sh, c.sh.xfull, c.xphase & 1u, ROLE_CONSUMER, pc)) return false;
-    float scale = 1.0f;
-    if (gain) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kNumConsumerWarps; ++w) tot += c.sh.red[48 + w];
-        scale = rsqrtf(tot / float(K) + c.p.rms_eps);
-    }
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        const int ch = c.lane + 32 * i;
-        if (ch < segch) {
-            const float4 a = *reinterpret_cast<const float4*>(c.sh.xbuf + ch * 8);
-            const float4 b = *reinterpret_cast<const float4*>(c.sh.xbuf + ch * 8 + 4);
-            float* x = &xr[8 * i];
-            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-            if (gain) {
-                const uint4 g = *reinterpret_cast<const uint4*>(c.sh.gbuf + ch * 8);
-                x[0] = (x[0] * scale) * bf_lo(g.x); x[1] = (x[1] * scale) * bf_hi(g.x);
-                x[2] = (x[2] * scale) * bf_lo(g.y); x[3] = (x[3] * scale) * bf_hi(g.y);
-                x[4] = (x[4] * scale) * bf_lo(g.z); x[5] = (x[5] * scale) * bf_hi(g.z);
-                x[6] = (x[6] * scale) * bf_lo(g.w); x[7] = (x[7] * scale) * bf_hi(g.w);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
-        }
-    }
-    __syncwarp();
-    if (c.lane == 0) mbar_arrive(c.sh.xfree);
-    ++c.xphase;
-    return true;
-}
-
 // the step's input token of sequence b: from the host, or in a chained multi-step call the
 // previous step's greedy token in device memory -- clamped to the vocabulary, since a step that
 // failed may have left no token (its recorded error is what the host then reports)
@@ -902,176 +735,220 @@ __device__ __forceinline__ int step_token(const Params& p, int b) {
     return min(max(__ldcg(p.tok_dev + b), 0), p.V - 1);
 }
 
-// output of one matvec row (run by one lane); `half` tells the two row units a warp carries apart
-__device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int ru, int half, float s0, float s1) {
+// where an epilogue's residual comes from: epoch-tagged words, or the bf16 embedding row (layer 0)
+struct RSrc {
+    const uint64_t* t;
+    const uint16_t* b;
+};
+
+// The input vector of a matvec tile (sequence b) into this warp's registers: its segment g of the
+// row length, RMS-normalised where the operator has a norm.  Rows up to the shared buffer's length
+// take their input cooperatively: thread t polls the 8-element chunks t, t + 512, ... into shared
+// memory with one sum of squares per warp; after the CTA-wide arrival every warp adds the 16 sums
+// in warp order (the same scale everywhere) and takes its segment.  Longer rows (the MLP down
+// projection's input) are polled by each warp for its own segment, straight into registers.  In
+// the same polling round thread t < nres fetches the residual word of the tile's row t into the
+// shared residual buffer (O projection, MLP down).  Every warp runs this for every matvec tile
+// (the instruction sequence is the same in all warps); xfree keeps a warp from overwriting a
+// buffer another warp still reads: the shared input until every warp has taken its segment, a
+// residual buffer (there are two, alternating) until every warp has finished the tile before.
+__device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uint16_t* gain, const RSrc& rs, int nres,
+                           float (&xr)[8 * kCpl], float*& res, int pc) {
     const Params& p = c.p;
-    const int op = si.w[W_OP], l = si.w[W_LAYER], a0 = si.w[W_A0];
+    const MvShape& m = si.mv;
+    const int tid = c.warp * 32 + c.lane;
+    const int g = c.warp & (m.G - 1);
+    const int cg0 = g * m.segch;
+    const int nch = min(m.segch, m.chunks - cg0);   // chunks of this warp's segment (the last may be short)
+    if (c.xphase > 0 && !wait_bar(p, c.sh, c.sh.xfree, (c.xphase - 1u) & 1u, ROLE_CONSUMER, pc)) return false;
+    res = c.sh.res + (c.xphase & 1u) * kResBuf;
+    bool rdone = tid >= nres;
+    auto poll_res = [&]() {
+        if (!rdone) {
+            if (rs.b) {
+                res[tid] = bf16f(rs.b[tid]);
+                rdone = true;
+            } else {
+                const uint64_t w = ld_tag(rs.t + tid);
+                if (tag_of(w) == p.tag) {
+                    res[tid] = tag_val(w);
+                    rdone = true;
+                }
+            }
+        }
+        return rdone;
+    };
+    float ss = 0.f;
+    Spin sp;
+    if (!m.direct) {
+        for (int base = 0; base < m.chunks; base += kConsumerThreads) {   // warp-uniform trip count
+            const int ch = base + tid;
+            const bool valid = ch < m.chunks;
+            float v[8];
+            while (true) {
+                bool ok = valid ? load8x(src, ch * 8, v, p.tag) : true;
+                if (base == 0) ok &= poll_res();
+                if (__all_sync(0xFFFFFFFFu, ok)) break;
+                if (!spin_more(c, sp, pc)) return false;
+            }
+            if (valid) {
+                *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+            }
+        }
+    } else {
+        while (true) {
+            bool ok = poll_res();
+#pragma unroll
+            for (int i = 0; i < kCpl; ++i) {
+                const int ch = c.lane + 32 * i;
+                if (ch < nch) {
+                    ok &= load8x(src, (cg0 + ch) * 8, &xr[8 * i], p.tag);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
+                }
+            }
+            if (__all_sync(0xFFFFFFFFu, ok)) break;
+            if (!spin_more(c, sp, pc)) return false;
+        }
+    }
+    if (gain) {
+        ss = warp_sum(ss);
+        if (c.lane == 0) c.sh.red[48 + c.warp] = ss;
+    }
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(c.sh.xfull);
+    if (!wait_bar(p, c.sh, c.sh.xfull, c.xphase & 1u, ROLE_CONSUMER, pc)) return false;
+    if (!m.direct) {
+        float scale = 1.0f;
+        if (gain) {
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kNumConsumerWarps; ++w) tot += c.sh.red[48 + w];
+            scale = rsqrtf(tot / float(m.K) + p.rms_eps);
+        }
+#pragma unroll
+        for (int i = 0; i < kCpl; ++i) {
+            const int ch = c.lane + 32 * i;
+            float* x = &xr[8 * i];
+            if (ch < nch) {
+                const int cg = cg0 + ch;
+                const float4 a = *reinterpret_cast<const float4*>(c.sh.xbuf + cg * 8);
+                const float4 b = *reinterpret_cast<const float4*>(c.sh.xbuf + cg * 8 + 4);
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+                if (gain) {
+                    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(gain + cg * 8));
+                    x[0] = (x[0] * scale) * bf_lo(gw.x); x[1] = (x[1] * scale) * bf_hi(gw.x);
+                    x[2] = (x[2] * scale) * bf_lo(gw.y); x[3] = (x[3] * scale) * bf_hi(gw.y);
+                    x[4] = (x[4] * scale) * bf_lo(gw.z); x[5] = (x[5] * scale) * bf_hi(gw.z);
+                    x[6] = (x[6] * scale) * bf_lo(gw.w); x[7] = (x[7] * scale) * bf_hi(gw.w);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = 0.f;
+            }
+        }
+    }
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(c.sh.xfree);
+    ++c.xphase;
+    return true;
+}
+
+// Output of one matvec row (tile row ru, run by one lane).  The LM head keeps this lane's running
+// (max, lowest index) in bv / bi.
+__device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int ru, float s0, float s1,
+                            const float* res, float& bv, int& bi) {
+    const Params& p = c.p;
+    const int op = si.w[W_OP], l = si.w[W_LAYER];
     const size_t lb = size_t(l) * p.B + b;
-    const int row = a0 + ru;
+    const int row = si.w[W_A0] + ru;
     switch (op) {
         case OP_QKV: st_tag(p.qkv + lb * p.nqkv + row, s0, p.tag); break;
         case OP_OPROJ: {
-            const float res = (l == 0) ? bf16f(p.embed[size_t(step_token(p, b)) * p.H + row])
-                                       : poll1(p, c.sh, p.x_out + (lb - p.B) * p.H + row, pc);
-            st_tag(p.x_attn + lb * p.H + row, res + s0, p.tag);
+            const float r = ru < kResBuf ? res[ru]
+                          : (l == 0) ? bf16f(p.embed[size_t(step_token(p, b)) * p.H + row])
+                                     : poll1(p, c.sh, p.x_out + (lb - p.B) * p.H + row, pc);
+            st_tag(p.x_attn + lb * p.H + row, r + s0, p.tag);
             break;
         }
         case OP_UPGATE: st_htag(p.h + lb * p.F + row, s0 / (1.0f + expf(-s0)) * s1, htag(p.tag)); break;
-        case OP_DOWN: st_tag(p.x_out + lb * p.H + row, poll1(p, c.sh, p.x_attn + lb * p.H + row, pc) + s0, p.tag); break;
-        default: {   // LM head: logit, then this warp half's running (max, lowest index) for the argmax
+        case OP_DOWN: {
+            const float r = ru < kResBuf ? res[ru] : poll1(p, c.sh, p.x_attn + lb * p.H + row, pc);
+            st_tag(p.x_out + lb * p.H + row, r + s0, p.tag);
+            break;
+        }
+        default:   // LM head: the logit, then this lane's running (max, lowest index)
             p.logits[size_t(b) * p.V + row] = s0;
-            const int slot = (c.warp * 2 + half) * kMaxBatch + b;
-            float2 best = c.sh.lmbest[slot];
-            if (s0 > best.x || (s0 == best.x && row < __float_as_int(best.y)))
-                c.sh.lmbest[slot] = make_float2(s0, __int_as_float(row));
-            break;   // (the tile's end writes the warp half's running best to lm_part)
-        }
-    }
-}
-
-// row unit u's sum is done: emit it, or (split rows) leave this segment's partial and let the
-// last-arriving segment warp add the partials in segment order and emit the row.  Split rows use
-// slot ru mod cap of the instruction's partial area; the slot's word holds the owning row (high
-// bits) and the arrivals so far (low 8 bits), -1 when free.  A warp that runs ahead waits
-// (bounded) for an earlier row to free its slot; the slowest warp never waits: every row of an
-// earlier step already has all its segments.
-__device__ void mv_finish(const Cw& c, const SlotInfo& si, int pc, int b, int u, int half, float s0, float s1) {
-    int ru = u;
-    if (si.split) {
-        const bool pair = si.w[W_OP] == OP_UPGATE;
-        const int nseg = si.nseg, seg = u & (nseg - 1), per = pair ? 2 : 1;
-        ru = u >> si.lognseg;
-        const int slot = pc % kSlots;
-        const int cap = kCombStride / (nseg * per);            // a power of two, <= kMaxRows
-        const int rs = ru & (cap - 1);
-        int* word = c.sh.combcnt + slot * kMaxRows + rs;
-        float* part = c.sh.comb + slot * kCombStride + rs * nseg * per;
-        uint64_t t0 = 0;
-        while (true) {
-            const int w = atomicCAS(word, -1, ru << 8);
-            if (w == -1 || (w >> 8) == ru) break;
-            if (*reinterpret_cast<volatile int*>(c.sh.abort)) return;
-            if (t0 == 0) t0 = globaltimer();
-            else if (globaltimer() - t0 > budget(c.p, ROLE_CONSUMER)) {
-                raise_error(c.p, c.sh, MK_ERR_TIMEOUT, ROLE_CONSUMER, pc, -1, uint32_t(w), uint32_t(ru));
-                return;
+            if (s0 > bv || (s0 == bv && row < bi)) {
+                bv = s0;
+                bi = row;
             }
-        }
-        if (pair) { part[seg * 2] = s0; part[seg * 2 + 1] = s1; }
-        else part[seg] = s0;
-        __threadfence_block();
-        if ((atomicAdd(word, 1) & 0xFF) != nseg - 1) return;
-        __threadfence_block();
-        s0 = 0.f;
-        s1 = 0.f;
-#pragma unroll 1
-        for (int s = 0; s < nseg; ++s) {
-            if (pair) { s0 += part[s * 2]; s1 += part[s * 2 + 1]; }
-            else s0 += part[s];
-        }
-        __threadfence_block();
-        atomicExch(word, -1);   // the slot is free for the row cap rows later
+            break;
     }
-    mv_epilogue(c, si, pc, b, ru, half, s0, s1);
 }
 
-// two row segments (stream offsets o0, o1) dotted with x at once: 2*CPL independent 16-byte loads
-// per lane, then one butterfly that leaves the first sum in lanes 0-15 and the second in lanes
-// 16-31 (each bit-identical to a plain xor butterfly of that sum).  Without a second segment
-// (has1 false) the first one is dotted twice and the copy is dropped.
-template <int CPL>
-__device__ __forceinline__ float seg_dot2(const Cw& c, const SlotInfo& si, uint32_t first, uint32_t o0, uint32_t o1,
-                                          bool has1, const float (&xr)[8 * CPL]) {
-    const int segch = si.segch;
-    const uint32_t sb = si.segbytes;
-    if (!has1) o1 = o0;
-    const bool p0 = (o0 >> c.p.page_shift) == ((o0 + sb - 1u) >> c.p.page_shift);
-    const bool p1 = (o1 >> c.p.page_shift) == ((o1 + sb - 1u) >> c.p.page_shift);
-    float a[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-    if (p0 && p1 && segch == 32 * CPL) {   // whole segments inside one page each: plain strided loads
-        const uint8_t* b0 = ring_ptr(c.sh, c.p, first, o0) + c.lane * 16;
-        const uint8_t* b1 = ring_ptr(c.sh, c.p, first, o1) + c.lane * 16;
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-            const uint4 w0 = *reinterpret_cast<const uint4*>(b0 + i * 512);
-            const uint4 w1 = *reinterpret_cast<const uint4*>(b1 + i * 512);
-            a[i & 3] = dot8(w0, &xr[8 * i], a[i & 3]);
-            e[i & 3] = dot8(w1, &xr[8 * i], e[i & 3]);
-        }
-    } else {   // a segment crosses a page or is ragged: one segment at a time, chunk by chunk
+// Segment g's sum of unit j of the page in ring slot `slot` (a row, or a gate/up pair: s0 gate,
+// s1 up).  With one segment per row the row is done; otherwise the sum waits in the slot's
+// partial area and the last of the row's G segments to arrive adds them in segment order and
+// writes the row.  A page slot's partials and counters are reused only after every warp has
+// released the page, so no row ever meets another row's partials.
+__device__ void mv_finish(const Cw& c, const SlotInfo& si, int pc, int b, uint32_t slot, int j, int ru, float s0,
+                          float s1, const float* res, float& bv, int& bi) {
+    const int G = si.mv.G;
+    if (G > 1) {
+        const int lg = si.mv.logG;
+        float* part = c.sh.comb + (size_t(slot) * c.p.comb_stride + j) * 2;
+        part[0] = s0;
+        part[1] = s1;
+        __threadfence_block();
+        int* cnt = c.sh.combcnt + slot * c.p.comb_stride + (j >> lg);
+        if (atomicAdd(cnt, 1) != G - 1) return;
+        __threadfence_block();
+        const float* q = c.sh.comb + (size_t(slot) * c.p.comb_stride + (j & ~(G - 1))) * 2;
+        s0 = q[0];
+        s1 = q[1];
 #pragma unroll 1
-        for (int r = 0; r < 2; ++r) {
-            const uint32_t o = r ? o1 : o0;
-            float t[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                const int ch = c.lane + 32 * i;
-                if (ch < segch)
-                    t[i & 3] = dot8(*reinterpret_cast<const uint4*>(ring_ptr(c.sh, c.p, first, o + uint32_t(ch) * 16u)),
-                                    &xr[8 * i], t[i & 3]);
-            }
-            if (r) { e[0] = t[0]; e[1] = t[1]; e[2] = t[2]; e[3] = t[3]; }
-            else { a[0] = t[0]; a[1] = t[1]; a[2] = t[2]; a[3] = t[3]; }
+        for (int k = 1; k < G; ++k) {
+            s0 += q[2 * k];
+            s1 += q[2 * k + 1];
         }
+        *cnt = 0;   // (visible to the page slot's next user through the ring's mbarriers)
     }
-    const float s0 = (a[0] + a[1]) + (a[2] + a[3]);
-    const float s1 = (e[0] + e[1]) + (e[2] + e[3]);
-    const bool hi = c.lane & 16;
-    float v = (hi ? s1 : s0) + __shfl_xor_sync(0xFFFFFFFFu, hi ? s0 : s1, 16);
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
+    mv_epilogue(c, si, pc, b, ru, s0, s1, res, bv, bi);
 }
 
-// Matvec tile (QKV / O / gate-up / down / LM-head rows).  Unit u of the tile (a row, a gate/up
-// pair, or a row segment) goes to warp (u + rot) mod 8, where rot rotates with every tile so
-// short tiles spread over all warps; a warp handles its units two row segments at a time, in
-// steps of 16 units (8 gate/up pairs) taken in stream order.  At batch 1 the tile streams: a warp
-// waits only for the pages of its next step and gives back every page no later step reads, so a
-// tile may be far larger than the page ring.  At batch > 1 every sequence reads every page: the
-// tile's pages are held until it is done.  Gate/up tiles arrive interleaved: page 2j holds gate
-// rows [j rpp, (j + 1) rpp), page 2j + 1 the matching up rows.
-template <int CPL>
-__device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc) {
-    // this warp's input in registers, (re)loaded by the tile: its registers are free outside
-    // matvec tiles (a batch-1 SM runs about one tile per operator, each with a new input)
-    float xr[8 * CPL];
-    int xkey = -1;
+// Matvec tile (QKV / O / gate-up / down / LM-head rows).  Pages hold whole rows; the tile is
+// walked in groups of two pages: two row pages, or for gate/up the gate page and the up page of
+// the same row group.  A page holds units (row, segment) in row-major order; warp w takes units
+// j = w, w + 16, ... of the group, always its own segment, two row dots at a time (the unit in the
+// first page and the unit in the second).  At batch 1 the tile streams: a warp waits only for the
+// pages of its current group and gives them back when done with them, so a tile may be far larger
+// than the page ring.  At batch > 1 every sequence reads every page: the tile's pages are held
+// until it is done.
+__device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     const Params& p = c.p;
-    const int op = si.w[W_OP], l = si.w[W_LAYER];
-    const bool pair = op == OP_UPGATE;
-    const int U = si.units, nseg = si.nseg;
-    const uint32_t rowbytes = si.rowbytes, segbytes = si.segbytes;
-    const uint32_t PB = uint32_t(p.page_bytes), NP = uint32_t(p.n_pages);
-    const uint32_t rpp = PB / rowbytes;   // gate/up: rows per page
+    const int op = si.w[W_OP], l = si.w[W_LAYER], a0 = si.w[W_A0];
+    const bool pair = si.inter != 0;
+    const MvShape& m = si.mv;
+    const int R = si.rows, rpp = m.rpp, lg = m.logG;
+    const int g = c.warp & (m.G - 1);
+    const int nch = min(m.segch, m.chunks - g * m.segch);
+    const uint32_t rowbytes = m.rowbytes, NP = uint32_t(p.n_pages);
+    const int npg = si.n_pages;
     const bool stream = p.B == 1;
     if (!stream && !wait_pages(c, si, pc)) return false;
     if (c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
-    const int ufirst = (c.warp - int(c.rot)) & 7;
-    const int per_step = pair ? 8 : 16;
-    const int nsteps = (U + per_step - 1) / per_step;
-    // stream offset of segment s of unit u's row (a pair: its gate row; the up row is a page later)
-    auto unit_off = [&](int u, int s) -> uint32_t {
-        const uint32_t row = uint32_t(si.split ? (u >> si.lognseg) : u);
-        if (pair) return (row / rpp) * 2u * PB + (row % rpp) * rowbytes + uint32_t(s) * segbytes;
-        return row * rowbytes + uint32_t(s) * segbytes;
-    };
-    auto first_page = [&](int k) -> int {   // first page step k reads
-        const int u0 = k * per_step;
-        return int(unit_off(u0, si.split ? (u0 & (nseg - 1)) : 0) >> p.page_shift);
-    };
-    auto last_page = [&](int k) -> int {    // last page step k reads
-        const int u1 = min(U, (k + 1) * per_step) - 1;
-        if (pair) return int(unit_off(u1, si.split ? (u1 & (nseg - 1)) : 0) >> p.page_shift) + 1;
-        return int((unit_off(u1, si.split ? (u1 & (nseg - 1)) : nseg - 1) + segbytes - 1u) >> p.page_shift);
-    };
-    // page trackers (batch 1): next page to wait, next page to release, page whose slot is `bslot`
-    int waited = 0, released = 0, based = 0;
-    uint32_t wslot = uint32_t(si.first_slot), wph = uint32_t(si.first_phase);
-    uint32_t rslot = wslot, bslot = wslot;
+    float xr[8 * kCpl];
+    const size_t lane_off = size_t(g * m.segch + c.lane) * 16u;   // this lane's first chunk within a row
     for (int b = 0; b < p.B; ++b) {
         XSrc src{nullptr, nullptr, nullptr};
+        RSrc rs{nullptr, nullptr};
         const uint16_t* gain = nullptr;
+        int nres = 0;
         const size_t lb = size_t(l) * p.B + b;
         switch (op) {
             case OP_QKV:
@@ -1079,99 +956,108 @@ __device__ bool matvec_warp(Cw& c, const SlotInfo& si, int pc) {
                 if (l == 0) src.b = p.embed + size_t(step_token(p, b)) * p.H;
                 else src.t = p.x_out + (lb - p.B) * p.H;
                 break;
-            case OP_OPROJ: src.t = p.o + lb * p.qd; break;
+            case OP_OPROJ:
+                src.t = p.o + lb * p.qd;
+                if (l == 0) rs.b = p.embed + size_t(step_token(p, b)) * p.H + a0;
+                else rs.t = p.x_out + (lb - p.B) * p.H + a0;
+                nres = min(R, kResBuf);
+                break;
             case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; src.t = p.x_attn + lb * p.H; break;
-            case OP_DOWN: src.h = p.h + lb * p.F; break;
+            case OP_DOWN:
+                src.h = p.h + lb * p.F;
+                rs.t = p.x_attn + lb * p.H + a0;
+                nres = min(R, kResBuf);
+                break;
             default: gain = p.final_norm; src.t = p.x_out + (size_t(p.L - 1) * p.B + b) * p.H; break;
         }
-        if (nseg == 1 && si.K <= kXBuf) {   // every warp, even one without units in this tile
-            const int key = (((op * 64 + (l & 63)) * kMaxBatch + b) * 8) + 1;
-            if (key != xkey) {
-                if (!shared_x<CPL>(c, xr, si.K, src, gain, pc)) return false;
-                xkey = key;
+        float* res;
+        if (!load_input(c, si, src, gain, rs, nres, xr, res, pc)) return false;
+        float bv = -INFINITY;   // LM head: this lane's running best (lanes 0 and 16)
+        int bi = 0x7FFFFFFF;
+        uint32_t slot = uint32_t(si.first_slot), ph = uint32_t(si.first_phase);
+        for (int k = 0; 2 * k < npg; ++k) {
+            const bool two = 2 * k + 1 < npg;
+            const uint32_t slot1 = slot + 1u == NP ? 0u : slot + 1u;
+            const uint32_t ph1 = slot + 1u == NP ? ph ^ 1u : ph;
+            if (stream) {
+                if (!wait_bar(p, c.sh, c.sh.full + slot, ph, ROLE_CONSUMER, pc)) return false;
+                if (two && !wait_bar(p, c.sh, c.sh.full + slot1, ph1, ROLE_CONSUMER, pc)) return false;
             }
-        }
-        for (int k = 0; k < nsteps; ++k) {
-            uint32_t first = uint32_t(si.first_slot), obase = 0;
-            if (stream) {   // this step's pages
-                const int pa = first_page(k), pb = last_page(k);
-                for (; waited <= pb; ++waited) {
-                    if (!wait_bar(p, c.sh, c.sh.full + wslot, wph, ROLE_CONSUMER, pc)) return false;
-                    if (++wslot == NP) { wslot = 0; wph ^= 1u; }
-                }
-                for (; based < pa; ++based)
-                    if (++bslot == NP) bslot = 0;
-                first = bslot;
-                obase = uint32_t(pa) * PB;
+            int r0, n0, r1, n1;   // first tile row and rows of each page of the group
+            if (pair) {
+                r0 = r1 = k * rpp;
+                n0 = n1 = min(rpp, R - r0);
+            } else {
+                r0 = 2 * k * rpp;
+                n0 = min(rpp, R - r0);
+                r1 = r0 + rpp;
+                n1 = two ? min(rpp, R - r1) : 0;
             }
-            // (a gate/up pair is already two row segments: one unit per step; otherwise u, u + 8)
-            const int u = k * per_step + ufirst;
-            if (u < U) {
-                const int u1 = u + 8;
-                const bool two = !pair && u1 < U;
-                const int s_lo = si.split ? (u & (nseg - 1)) : 0;
-                const int s_hi = si.split ? s_lo + 1 : nseg;
-                float t0 = 0.f, t1 = 0.f;
-                for (int s = s_lo; s < s_hi; ++s) {
-                    const int key = (((op * 64 + (l & 63)) * kMaxBatch + b) * 8 + s) + 1;
-                    if (key != xkey) {
-                        if (!load_xw<CPL>(c, xr, si.K, nseg, s, src, gain, pc)) return false;
-                        xkey = key;
+            const int u0 = n0 << lg, u1 = n1 << lg;
+            const uint8_t* base0 = c.sh.ring + (size_t(slot) << p.page_shift) + lane_off;
+            const uint8_t* base1 = c.sh.ring + (size_t(slot1) << p.page_shift) + lane_off;
+            for (int j = c.warp; j < max(u0, u1); j += kNumConsumerWarps) {   // warp-uniform
+                const int r = j >> lg;
+                const bool h0 = j < u0, h1 = j < u1;
+                const uint8_t* w0 = base0 + size_t(r) * rowbytes;
+                const uint8_t* w1 = base1 + size_t(r) * rowbytes;
+                float a[kCpl], e[kCpl];
+#pragma unroll
+                for (int i = 0; i < kCpl; ++i) {
+                    a[i] = 0.f;
+                    e[i] = 0.f;
+                    if (c.lane + 32 * i < nch) {
+                        if (h0) a[i] = dot8(*reinterpret_cast<const uint4*>(w0 + i * 512), &xr[8 * i], 0.f);
+                        if (h1) e[i] = dot8(*reinterpret_cast<const uint4*>(w1 + i * 512), &xr[8 * i], 0.f);
                     }
-                    const uint32_t off0 = unit_off(u, s) - obase;
-                    const uint32_t off1 = pair ? off0 + PB : (two ? unit_off(u1, s) - obase : off0);
-                    const float v = seg_dot2<CPL>(c, si, first, off0, off1, pair || two, xr);
-                    // lanes 0-15 hold the first sum, lanes 16-31 the second: lane 0 keeps its own (and
-                    // takes the up sum of a pair from lane 16), lane 16 keeps its own
-                    t0 += v;
-                    t1 += pair ? __shfl_sync(0xFFFFFFFFu, v, 16) : v;
                 }
-                // lane 0 emits unit u (with the up sum of a pair), lane 16 the second unit u1
-                if (c.lane == 0 || (two && c.lane == 16)) {
-                    const bool lo = c.lane == 0;
-                    mv_finish(c, si, pc, b, lo ? u : u1, lo ? 0 : 1, lo ? t0 : t1, pair ? t1 : 0.f);
+                const float s0 = (a[0] + a[1]) + (a[2] + a[3]);
+                const float s1 = (e[0] + e[1]) + (e[2] + e[3]);
+                // one butterfly for both sums: the first lands in lanes 0-15, the second in 16-31
+                const bool hi = c.lane & 16;
+                float v = (hi ? s1 : s0) + __shfl_xor_sync(0xFFFFFFFFu, hi ? s0 : s1, 16);
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                if (pair) {
+                    const float up = __shfl_sync(0xFFFFFFFFu, v, 16);
+                    if (c.lane == 0) mv_finish(c, si, pc, b, slot, j, r0 + r, v, up, res, bv, bi);
+                } else if (c.lane == 0) {
+                    if (h0) mv_finish(c, si, pc, b, slot, j, r0 + r, v, 0.f, res, bv, bi);
+                } else if (c.lane == 16) {
+                    if (h1) mv_finish(c, si, pc, b, slot1, j, r1 + r, v, 0.f, res, bv, bi);
                 }
             }
-            if (stream) {   // give back the pages no later step of this tile reads
-                const int pn = min(k + 1 < nsteps ? first_page(k + 1) : si.n_pages, waited);
+            if (stream) {   // this group's pages are done for this warp
                 __syncwarp();
                 if (c.lane == 0) {
-                    uint32_t rs = rslot;
-                    for (int i = released; i < pn; ++i) {
-                        mbar_arrive(c.sh.empty + rs);
-                        if (++rs == NP) rs = 0;
-                    }
+                    mbar_arrive(c.sh.empty + slot);
+                    if (two) mbar_arrive(c.sh.empty + slot1);
                 }
-                for (; released < pn; ++released)
-                    if (++rslot == NP) rslot = 0;
+            }
+            if (two) {
+                slot = slot1 + 1u == NP ? 0u : slot1 + 1u;
+                ph = slot1 + 1u == NP ? ph1 ^ 1u : ph1;
+            } else {
+                slot = slot1;
+                ph = ph1;
             }
         }
+        if (op == OP_LMHEAD) {   // this warp's running (max, lowest index) from lanes 0 and 16
+            const float ov = __shfl_sync(0xFFFFFFFFu, bv, 16);
+            const int oi = __shfl_sync(0xFFFFFFFFu, bi, 16);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+            if (c.lane == 0)
+                p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * kNumConsumerWarps + c.warp] =
+                    make_int4(__float_as_int(bv), bi, int(p.epoch), 0);
+        }
+        // batch > 1: the page slots' partials and counters serve the next sequence
+        if (!stream && !cbar(c, pc)) return false;
     }
     if (c.warp == 0 && c.lane == 0) stamp(p, pc, 7);
-    if (stream) {   // pages no step read (none in a well-formed tile): wait for them, then give back
-        for (; waited < si.n_pages; ++waited) {
-            if (!wait_bar(p, c.sh, c.sh.full + wslot, wph, ROLE_CONSUMER, pc)) return false;
-            if (++wslot == NP) { wslot = 0; wph ^= 1u; }
-        }
-        __syncwarp();
-        if (c.lane == 0)
-            for (int i = released; i < si.n_pages; ++i) {
-                mbar_arrive(c.sh.empty + rslot);
-                if (++rslot == NP) rslot = 0;
-            }
-        __syncwarp();
-    } else {
-        release_pages(c, si);
-    }
-    if (op == OP_LMHEAD && (c.lane & 15) == 0) {   // this warp half's running (max, lowest index)
-        const int half = c.lane >> 4;
-        for (int b = 0; b < p.B; ++b) {
-            const float2 best = c.sh.lmbest[(c.warp * 2 + half) * kMaxBatch + b];
-            p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * (2 * kNumConsumerWarps) + c.warp * 2 + half] =
-                make_int4(__float_as_int(best.x), __float_as_int(best.y), int(p.epoch), 0);
-        }
-    }
-    c.rot = (c.rot + uint32_t(U)) & 7u;
+    if (!stream) release_pages(c, si);
     return true;
 }
 
@@ -1350,13 +1236,13 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     if (!reinterpret_cast<volatile int*>(c.sh.red)[40]) return true;
     const int nact = min(p.n_chunk, p.pos[b] / C + 1);
     const float* pbase = p.part + (lb * p.nkv + g) * size_t(p.n_chunk) * hpg * (d + 2);
-    // the group's active partials are one contiguous block; when it fits the shared-x and gain
-    // buffers (free during attention: the tile began with every warp past its previous input) it
-    // is staged there in one round trip, and the combine below reads shared memory
+    // the group's active partials are one contiguous block; when it fits the shared input buffer
+    // (free during attention: the tile began with every warp past its previous input) it is staged
+    // there in one round trip, and the combine below reads shared memory
     const int blk = nact * hpg * (d + 2);
     const float* pb = pbase;
-    if (blk <= kXBuf * 3 / 2) {
-        float* stage = c.sh.xbuf;   // xbuf and gbuf are adjacent: 1.5 * kXBuf floats
+    if (blk <= p.xbuf_floats) {
+        float* stage = c.sh.xbuf;
         for (int i = tid; i < blk; i += kConsumerThreads) stage[i] = __ldcg(pbase + i);
         if (!cbar(c, pc)) return false;
         pb = stage;
@@ -1403,7 +1289,7 @@ __device__ bool argmax_tile(Cw& c, const SlotInfo& si, int pc) {
     const Params& p = c.p;
     const int b = si.w[W_B];
     const int tid = c.warp * 32 + c.lane;
-    const int n = int(gridDim.x) * kNumConsumerWarps * 2;   // one running partial per (CTA, warp half)
+    const int n = int(gridDim.x) * kNumConsumerWarps;   // one running partial per (CTA, warp)
     const int4* parts = p.lm_part + size_t(b) * n;
     float bv = -INFINITY;
     int bi = 0x7FFFFFFF;
@@ -1474,9 +1360,8 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
     return true;
 }
 
-template <int CPL>
 __device__ void consumer_warp(const Params& p, const Shared& sh) {
-    Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u, 0u};
+    Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u};
     CounterCache cc{-1, -1};
     for (int pc = 0;; ++pc) {
         const int slot = pc % kSlots;
@@ -1506,7 +1391,7 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
             switch (op) {
                 case OP_ATTN: good = attn_tile(c, si, pc); break;
                 case OP_ARGMAX: good = argmax_tile(c, si, pc); break;
-                default: good = matvec_warp<CPL>(c, si, pc); break;
+                default: good = matvec_tile(c, si, pc); break;
             }
             if (!good) break;
             if (threadIdx.x == 0) stamp(p, pc, 3);
@@ -1520,7 +1405,6 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
     }
 }
 
-template <int CPL>
 __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Shared sh = carve(smem, p);
@@ -1544,14 +1428,12 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
         *sh.issued = 0ull;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int i = threadIdx.x; i < kNumConsumerWarps * 2 * kMaxBatch; i += blockDim.x)
-        sh.lmbest[i] = make_float2(-INFINITY, __int_as_float(0x7FFFFFFF));
-    for (int i = threadIdx.x; i < kSlots * kMaxRows; i += blockDim.x) sh.combcnt[i] = -1;   // split-row slots free
+    for (int i = threadIdx.x; i < p.n_pages * p.comb_stride; i += blockDim.x) sh.combcnt[i] = 0;
     for (int i = threadIdx.x; i < p.L; i += blockDim.x) sh.layers[i] = p.layers[i];
     if (threadIdx.x == 0) stamp(p, 0, 5);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < kNumConsumerWarps) consumer_warp<CPL>(p, sh);
+    if (warp < kNumConsumerWarps) consumer_warp(p, sh);
     else if (warp == kLoaderWarp) { if (lane == 0) loader(p, sh); }
     else if (lane == 0) publisher(p, sh);
     cta_sync_divergent();
@@ -1568,22 +1450,7 @@ __global__ void rope_table_kernel(float2* out, int max_seq, int d, double theta)
     }
 }
 
-// CPL = 16-byte chunks per lane of the longest row segment (segments hold <= 2048 elements)
-static const void* kernel_for(int cpl) {
-    switch (cpl) {
-        case 1: return reinterpret_cast<const void*>(&megakernel<1>);
-        case 2: return reinterpret_cast<const void*>(&megakernel<2>);
-        case 3: return reinterpret_cast<const void*>(&megakernel<3>);
-        case 4: return reinterpret_cast<const void*>(&megakernel<4>);
-        case 5: return reinterpret_cast<const void*>(&megakernel<5>);
-        case 6: return reinterpret_cast<const void*>(&megakernel<6>);
-        case 7: return reinterpret_cast<const void*>(&megakernel<7>);
-        case 8: return reinterpret_cast<const void*>(&megakernel<8>);
-        default: return nullptr;
-    }
-}
-
-const void* megakernel_fn(int cpl) { return kernel_for(cpl); }
+const void* megakernel_fn() { return reinterpret_cast<const void*>(&megakernel); }
 
 cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st) {
     const int n = max_seq * (d / 2);

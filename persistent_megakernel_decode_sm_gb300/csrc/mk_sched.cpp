@@ -21,7 +21,7 @@
 //  * pools: memory = tiles that stream weights or KV, compute = argmax; within a wave memory
 //    tiles are placed first;
 //  * rows per tile: at batch 1 about one tile per operator per SM (streamed through the page
-//    ring page by page), otherwise about tile_bytes per tile;
+//    ring page by page, whole rows per page), otherwise about tile_bytes per tile;
 //  * placement: within a wave, tiles in (cost desc, id asc) order -- or a seeded splitmix64
 //    Fisher-Yates order when shuffle_seed != 0 -- each to the queue with the smallest
 //    accumulated cost (ties to the lowest SM) among the queues holding fewer than ceil(n / S)
@@ -171,8 +171,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     if (o.rows_lm) g.r_lm = o.rows_lm;
     if (g.r_qkv < 1 || g.r_qkv > d) return fail(MK_ERR_ARG, "rows_qkv must be in [1, head_dim]");
     if (g.r_o < 1 || g.r_up < 1 || g.r_lm < 1 || g.r_dn < 1) return fail(MK_ERR_ARG, "rows per tile must be >= 1");
-    if (g.page_bytes < 2 * H)   // gate/up tiles stream whole rows per page
-        return fail(MK_ERR_ARG, "page_bytes %d holds no gate/up row (%d bytes)", g.page_bytes, 2 * H);
+    if (g.page_bytes < 2 * std::max(H, std::max(qd, F)))   // matvec tiles stream whole rows per page
+        return fail(MK_ERR_ARG, "page_bytes %d holds no matvec row (%d bytes)", g.page_bytes, 2 * std::max(H, std::max(qd, F)));
     g.n_qkv = cdiv(nqkv, g.r_qkv);
     g.n_o = cdiv(H, g.r_o);
     g.n_up = cdiv(F, g.r_up);
@@ -321,10 +321,14 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
             for (int q = 0; q < t.nwait; ++q) { w[W_WAIT + 2 * q] = t.wait[q][0]; w[W_WAIT + 2 * q + 1] = t.wait[q][1]; }
             w[W_NPUB] = t.npub;
             for (int q = 0; q < t.npub; ++q) { w[W_PUB + 2 * q] = t.pub[q][0]; w[W_PUB + 2 * q + 1] = t.pub[q][1]; }
-            // gate/up tiles stream page-sized row groups, gate and up pages alternating
-            const int64_t rpp = g.page_bytes / (2ll * H);
-            int64_t pages = t.op == OP_UPGATE ? 2 * ((t.a1 + rpp - 1) / rpp)
-                                              : (t.stream_bytes + g.page_bytes - 1) / g.page_bytes;
+            // matvec tiles stream whole rows per page (gate/up: gate and up row groups in alternate
+            // pages); an attention tile streams its K rows, then its V rows
+            int64_t pages = (t.stream_bytes + g.page_bytes - 1) / g.page_bytes;
+            if (t.op == OP_QKV || t.op == OP_OPROJ || t.op == OP_UPGATE || t.op == OP_DOWN || t.op == OP_LMHEAD) {
+                const int64_t K = t.op == OP_OPROJ ? qd : (t.op == OP_DOWN ? F : H);
+                const int64_t rpp = g.page_bytes / (2 * K);
+                pages = ((t.a1 + rpp - 1) / rpp) * (t.op == OP_UPGATE ? 2 : 1);
+            }
             if (pages > (1 << 20)) { delete sch; return fail(MK_ERR_CAPACITY, "tile too large"); }
             w[W_NPAGES] = int32_t(pages);
             w[W_TILE] = t.id;

@@ -1,14 +1,16 @@
 """Host check of the batch-1 streaming contract between the loader, the consumer warps and the
 bind-time capacity rule (no GPU).
 
-At batch 1 a matvec tile streams through the page ring: a consumer warp waits for the pages of
-its next step and gives back every page no later step reads, so the slowest warp can always
-progress as long as the pages one step touches fit the ring.  The bind accepts a schedule only
-when its rule for those pages fits; this test walks every batch-1 matvec tile of every workload
-(rows per tile from the scheduler's restatement) through the unit -> byte -> page mapping the
-consumer warps use -- 16 row segments or 8 gate/up pairs per step, gate/up rows interleaved by
-page -- and checks that every step's page span stays within the rule, that the steps cover the
-tile's pages in order, and that the rule fits the 6-page ring of the default 32 KB pages.
+At batch 1 a matvec tile streams through the page ring: every page holds whole rows (gate/up:
+the gate rows and the up rows of one row group in two consecutive pages), and the consumer warps
+walk the pages in groups of two, each warp waiting for the group's pages and giving them back
+when done.  Warp w computes segment w mod G of every row it touches (G, the segments per row,
+depends on the row length only) and units (row, segment) j = w, w + 16, ... of each page.  This
+test restates that mapping for every batch-1 matvec tile of every workload (rows per tile from the
+scheduler's restatement) and checks that the pages cover the rows exactly once in order, that
+every (row, segment) unit is computed by exactly one warp that always holds the same segment, that
+a page's units fit the shared partial area the bind sizes, and that the bind's page rule (two
+pages per step, plus an attention tile) fits the 6-page ring of the default 32 KB pages.
 """
 import pytest
 
@@ -17,86 +19,84 @@ from workload import WORKLOADS, get_workload
 
 PB = 32768          # default page bytes
 N_PAGES = 6         # pages the 1B / 8B configurations get from the 227 KB of shared memory
+WARPS = 16          # consumer warps
+CPL = 4             # 16-byte chunks a lane holds of its segment, at most
+MAX_SEG = 16
 
 
-def nseg_of(K):
-    n = 1
-    while K > 2048 * n:
-        n *= 2
-    return n
+def segments(K):
+    """Segments per row: the smallest power of two keeping a segment within 32 * CPL chunks."""
+    chunks, G = K // 8, 1
+    while -(-chunks // G) > 32 * CPL and G < MAX_SEG:
+        G *= 2
+    return G
+
+
+def tile_groups(op, rows, K):
+    """Yields, per two-page group, the tile rows in each page (a list of two lists)."""
+    rpp = PB // (2 * K)
+    assert rpp >= 1
+    pair = op == sr.UPGATE
+    n_pages = -(-rows // rpp) * (2 if pair else 1)
+    for k in range(0, n_pages, 2):
+        pages = []
+        for pg in (k, k + 1):
+            if pg >= n_pages:
+                pages.append([])
+                continue
+            grp = pg // 2 if pair else pg
+            pages.append(list(range(grp * rpp, min(rows, (grp + 1) * rpp))))
+        yield pages
+    return n_pages
 
 
 def bind_rule_pages(cfg, chunk):
-    """The bind's upper bound of the pages one batch-1 step can touch (restated)."""
-    def span(nbytes):
-        n = -(-nbytes // PB)
-        return n if (nbytes % PB == 0 or PB % nbytes == 0) else n + 1
-    need = 2
-    for K in (cfg.hidden, cfg.q_dim, cfg.ffn):
-        need = max(need, span(16 * (2 * K // nseg_of(K))))
-    rpp = PB // (2 * cfg.hidden)
-    groups = max(1, 8 // rpp) if (rpp % 8 == 0 or 8 % rpp == 0) else -(-8 // rpp) + 1
-    need = max(need, 2 * groups)
-    need = max(need, -(-(2 * chunk * cfg.head_dim * 2) // PB))
-    return need
-
-
-def step_spans(op, rows, K):
-    """(first page, last page) of every step of a batch-1 tile of `rows` rows (pairs for gate/up)
-    of length K, and the tile's page count, as the loader lays the stream out."""
-    pair = op == sr.UPGATE
-    nseg = nseg_of(K)
-    split = nseg > 1
-    lognseg = nseg.bit_length() - 1
-    rowbytes = 2 * K
-    segbytes = rowbytes // nseg
-    rpp = PB // rowbytes
-    U = rows * nseg if split else rows
-    per_step = 8 if pair else 16
-
-    def unit_off(u, s):
-        row = (u >> lognseg) if split else u
-        if pair:
-            return (row // rpp) * 2 * PB + (row % rpp) * rowbytes + s * segbytes
-        return row * rowbytes + s * segbytes
-
-    spans = []
-    for k in range(-(-U // per_step)):
-        u0 = k * per_step
-        first = unit_off(u0, (u0 & (nseg - 1)) if split else 0) // PB
-        u1 = min(U, (k + 1) * per_step) - 1
-        if pair:
-            last = unit_off(u1, (u1 & (nseg - 1)) if split else 0) // PB + 1
-        else:
-            last = (unit_off(u1, (u1 & (nseg - 1)) if split else nseg - 1) + segbytes - 1) // PB
-        spans.append((first, last))
-    n_pages = 2 * -(-rows // rpp) if pair else -(-(rows * rowbytes) // PB)
-    return spans, n_pages
+    """The bind's page rule at batch 1 (restated): a group of two pages, or an attention tile."""
+    return max(2, -(-(2 * chunk * cfg.head_dim * 2) // PB))
 
 
 @pytest.mark.parametrize("name", [w for w in WORKLOADS if get_workload(w).cfg.batch == 1])
 @pytest.mark.parametrize("S", [1, 37, 152])
-def test_batch1_steps_fit_the_bind_rule(name, S):
+def test_batch1_groups_cover_every_unit_once(name, S):
     cfg = get_workload(name).cfg
     o = sr.SchedOpts()
     tiles, _, _ = sr.enumerate_tiles(cfg, o, S)
-    need = bind_rule_pages(cfg, sr.attn_chunk(cfg, o, S))
     K = {sr.QKV: cfg.hidden, sr.OPROJ: cfg.q_dim, sr.UPGATE: cfg.hidden, sr.DOWN: cfg.ffn,
          sr.LMHEAD: cfg.hidden}
+    comb_stride = max([1] + [(PB // (2 * k)) * segments(k) for k in K.values() if segments(k) > 1])
     seen = 0
     for t in tiles:
         if t.op not in K:
             continue
-        if 2 * K[t.op] > PB and t.op == sr.UPGATE:
-            continue   # (rejected at schedule time: a page must hold a gate/up row)
-        spans, n_pages = step_spans(t.op, t.a1, K[t.op])
-        prev_first = 0
-        for first, last in spans:
-            assert first >= prev_first and first <= last < n_pages, (t, first, last, n_pages)
-            assert last - first + 1 <= need, (name, t.op, t.a1, first, last, need)
-            prev_first = first
-        assert spans[0][0] == 0 and spans[-1][1] == n_pages - 1
+        k_len = K[t.op]
+        G = segments(k_len)
+        lg = G.bit_length() - 1
+        chunks = k_len // 8
+        segch = -(-chunks // G)
+        assert segch <= 32 * CPL and WARPS % G == 0
+        done = {}
+        pages_seen = 0
+        for pages in tile_groups(t.op, t.a1, k_len):
+            pages_seen += sum(1 for p in pages if p)
+            for pi, prow in enumerate(pages):
+                units = len(prow) << lg
+                if G > 1:
+                    assert units <= comb_stride
+                for w in range(WARPS):
+                    for j in range(w, units, WARPS):
+                        assert j % G == w % G            # a warp keeps its own segment
+                        key = (pi if t.op == sr.UPGATE else 0, prow[j >> lg], j % G)
+                        done[key] = done.get(key, 0) + 1
+        # every (row, segment) -- for gate/up, of the gate and the up row -- exactly once
+        sides = 2 if t.op == sr.UPGATE else 1
+        assert sorted(done) == sorted((side, r, s) for side in range(sides) for r in range(t.a1)
+                                      for s in range(G))
+        assert set(done.values()) == {1}
+        assert pages_seen == sr.tile_pages(t, cfg, o)
         seen += 1
     assert seen > 0
-    if name != "tiny":
-        assert need <= N_PAGES
+    assert bind_rule_pages(cfg, sr.attn_chunk(cfg, o, S)) <= N_PAGES
+
+
+def test_segments_depend_on_the_row_length_only():
+    assert [segments(k) for k in (256, 688, 1024, 2048, 4096, 8192, 14336, 16384)] == [1, 1, 1, 2, 4, 8, 16, 16]
