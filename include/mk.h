@@ -227,8 +227,10 @@ mk_status mk_set_sync(mk_ctx* c, int32_t mode);
  * dependency waits).  buf: DEVICE uint64[S * Q * 8] (caller-owned) or NULL to switch tracing off.
  * While on, every launch writes globaltimer stamps (ns) for instruction (sm, slot) at
  * buf[(sm * Q + slot) * 8 + k]: k = 0 slot published by the loader, 1 its pages issued,
- * 2 dependencies satisfied, 3 body done, 4 completions published; buf[sm * Q * 8 + 5] = CTA
- * start.  Entries of slots a CTA never reached keep their old contents. */
+ * 2 dependencies satisfied, 3 body done, 4 completions published, 6 (matvec) input vector
+ * loaded, 7 (matvec) rows done -- 2, 3, 6 and 7 as seen by consumer warp 0;
+ * buf[sm * Q * 8 + 5] = CTA start.  Entries of slots a CTA never reached keep their old
+ * contents. */
 mk_status mk_set_trace(mk_ctx* c, uint64_t* buf);
 
 /* One decode step, synchronous: tokens and pos are HOST arrays of `batch` int32; logits is a

@@ -223,7 +223,7 @@ static_assert(sizeof(SlotInfo) % 16 == 0 && offsetof(SlotInfo, w) == 0, "slot wo
 
 // byte offsets of the non-ring shared memory (after the page ring); shared by host and device
 struct MiscLayout {
-    uint32_t slots, qwin, layers, bars, comb, combcnt, pubinfo, red, qrot, ascr, ml, kv, res, xbuf, total;
+    uint32_t slots, qwin, layers, bars, comb, combcnt, pubinfo, red, lmbest, qrot, ascr, ml, kv, res, xbuf, total;
 };
 
 MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qrot_floats, int xbuf_floats,
@@ -247,6 +247,7 @@ MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qr
                                                     // stream bytes the loader has issued [34..35] (u64),
                                                     // last-arrival flag [40], per-warp sums of
                                                     // squares of the shared input [48..63]
+    m.lmbest = take(8u * kNumConsumerWarps * kMaxBatch, 8);   // LM-head running (max, index) per warp / sequence
     m.qrot = take(4u * uint32_t(qrot_floats), 16);
     m.ascr = take(4u * uint32_t(attn_scratch_floats), 16);
     m.ml = take(4u * 4u * kMaxHpg, 16);             // (m, l) per head, combine L per head

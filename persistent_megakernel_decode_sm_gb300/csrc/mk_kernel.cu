@@ -228,6 +228,7 @@ struct Shared {
     int* combcnt;      // [n_pages][comb_stride] segment arrivals per row
     int* pubinfo;      // [kDone][8]: opcode, #completions, (counter, delta) x 2
     float* red;        // [32] argmax scratch
+    float2* lmbest;    // [kNumConsumerWarps][kMaxBatch] LM-head running (max, index) of the CTA's tiles
     int* abort;        // [1]
     int* published;    // [1] instructions the publisher has retired
     unsigned long long* issued;   // [1] stream bytes the loader has staged into pages
@@ -262,6 +263,7 @@ __device__ __forceinline__ Shared carve(uint8_t* base, const Params& p) {
     s.combcnt = reinterpret_cast<int*>(b + m.combcnt);
     s.pubinfo = reinterpret_cast<int*>(b + m.pubinfo);
     s.red = reinterpret_cast<float*>(b + m.red);
+    s.lmbest = reinterpret_cast<float2*>(b + m.lmbest);
     s.abort = reinterpret_cast<int*>(b + m.red) + 32;
     s.published = reinterpret_cast<int*>(b + m.red) + 33;
     s.issued = reinterpret_cast<unsigned long long*>(reinterpret_cast<int*>(b + m.red) + 34);
@@ -941,7 +943,6 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     const int npg = si.n_pages;
     const bool stream = p.B == 1;
     if (!stream && !wait_pages(c, si, pc)) return false;
-    if (c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
     float xr[8 * kCpl];
     const size_t lane_off = size_t(g * m.segch + c.lane) * 16u;   // this lane's first chunk within a row
     for (int b = 0; b < p.B; ++b) {
@@ -972,6 +973,7 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
         }
         float* res;
         if (!load_input(c, si, src, gain, rs, nres, xr, res, pc)) return false;
+        if (b == 0 && c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
         float bv = -INFINITY;   // LM head: this lane's running best (lanes 0 and 16)
         int bi = 0x7FFFFFFF;
         uint32_t slot = uint32_t(si.first_slot), ph = uint32_t(si.first_phase);
@@ -1042,16 +1044,19 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 ph = ph1;
             }
         }
-        if (op == OP_LMHEAD) {   // this warp's running (max, lowest index) from lanes 0 and 16
+        if (op == OP_LMHEAD) {   // this warp's running (max, lowest index) over its LM-head tiles so far
             const float ov = __shfl_sync(0xFFFFFFFFu, bv, 16);
             const int oi = __shfl_sync(0xFFFFFFFFu, bi, 16);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-            if (c.lane == 0)
+            if (c.lane == 0) {
+                float2& run = c.sh.lmbest[c.warp * kMaxBatch + b];
+                int ri = __float_as_int(run.y);
+                float rv = run.x;
+                if (ov > rv || (ov == rv && oi < ri)) { rv = ov; ri = oi; }
+                if (bv > rv || (bv == rv && bi < ri)) { rv = bv; ri = bi; }
+                run = make_float2(rv, __int_as_float(ri));
                 p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * kNumConsumerWarps + c.warp] =
-                    make_int4(__float_as_int(bv), bi, int(p.epoch), 0);
+                    make_int4(__float_as_int(rv), ri, int(p.epoch), 0);
+            }
         }
         // batch > 1: the page slots' partials and counters serve the next sequence
         if (!stream && !cbar(c, pc)) return false;
@@ -1429,6 +1434,8 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     for (int i = threadIdx.x; i < p.n_pages * p.comb_stride; i += blockDim.x) sh.combcnt[i] = 0;
+    for (int i = threadIdx.x; i < kNumConsumerWarps * kMaxBatch; i += blockDim.x)
+        sh.lmbest[i] = make_float2(-INFINITY, __int_as_float(0x7FFFFFFF));
     for (int i = threadIdx.x; i < p.L; i += blockDim.x) sh.layers[i] = p.layers[i];
     if (threadIdx.x == 0) stamp(p, 0, 5);
     __syncthreads();
