@@ -653,20 +653,28 @@ __device__ bool cbar(Cw& c, int pc) {
 struct Spin {
     uint64_t t0 = 0;
     bool started = false;
+    uint32_t rounds = 0;
 };
-__device__ bool spin_more(const Cw& c, Spin& sp, int pc) {
+// Another CTA's error reaches this CTA through the global error word; reading it costs a memory
+// round trip, so a poll reads it only every kErrCheckRounds rounds (its own CTA's abort flag, in
+// shared memory, every round).
+constexpr uint32_t kErrCheckRounds = 64;
+__device__ __forceinline__ bool other_cta_failed(const Params& p, uint32_t& rounds) {
+    return (++rounds % kErrCheckRounds) == 0 && ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(p.err)) != 0;
+}
+__device__ bool spin_more(const Params& p, const Shared& sh, int lane, Spin& sp, int pc) {
     int stop = 0;
-    if (c.lane == 0) {
-        if (*reinterpret_cast<volatile int*>(c.sh.abort) || ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(c.p.err))) {
-            *reinterpret_cast<volatile int*>(c.sh.abort) = 1;
+    if (lane == 0) {
+        if (*reinterpret_cast<volatile int*>(sh.abort) || other_cta_failed(p, sp.rounds)) {
+            *reinterpret_cast<volatile int*>(sh.abort) = 1;
             stop = 1;
         } else {
             const uint64_t now = globaltimer();
             if (!sp.started) {
                 sp.t0 = now;
                 sp.started = true;
-            } else if (now - sp.t0 > c.p.timeout_ns) {
-                raise_error(c.p, c.sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, 0, c.p.tag);
+            } else if (now - sp.t0 > p.timeout_ns) {
+                raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, 0, p.tag);
                 stop = 1;
             }
             if (!stop) __nanosleep(kPollBackoffNs);   // spaces a warp's polling rounds out in L2
@@ -674,6 +682,7 @@ __device__ bool spin_more(const Cw& c, Spin& sp, int pc) {
     }
     return __shfl_sync(0xFFFFFFFFu, stop, 0) == 0;
 }
+__device__ __forceinline__ bool spin_more(const Cw& c, Spin& sp, int pc) { return spin_more(c.p, c.sh, c.lane, sp, pc); }
 // warp-wide: lanes with `valid` read the tagged words a0 and a1 until both carry this step's tag
 __device__ bool wpoll2(const Cw& c, bool valid, const uint64_t* a0, const uint64_t* a1, float& v0, float& v1, int pc) {
     Spin sp;
@@ -695,10 +704,11 @@ __device__ float poll1(const Params& p, const Shared& sh, const uint64_t* a, int
     uint64_t w = ld_tag(a);
     if (tag_of(w) == p.tag) return tag_val(w);
     const uint64_t t0 = globaltimer();
+    uint32_t rounds = 0;
     while (true) {
         w = ld_tag(a);
         if (tag_of(w) == p.tag) break;
-        if (*reinterpret_cast<volatile int*>(sh.abort) || ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(p.err))) {
+        if (*reinterpret_cast<volatile int*>(sh.abort) || other_cta_failed(p, rounds)) {
             *reinterpret_cast<volatile int*>(sh.abort) = 1;
             break;
         }
@@ -754,6 +764,25 @@ struct RSrc {
 // (the instruction sequence is the same in all warps); xfree keeps a warp from overwriting a
 // buffer another warp still reads: the shared input until every warp has taken its segment, a
 // residual buffer (there are two, alternating) until every warp has finished the tile before.
+// Residual word of tile row `tid` into res[tid] (tid < nres): true once it is there.
+__device__ __forceinline__ bool poll_res(const Params& p, const RSrc& rs, int tid, int nres, float* res, bool& rdone) {
+    if (!rdone) {
+        if (tid >= nres) {
+            rdone = true;
+        } else if (rs.b) {
+            res[tid] = bf16f(rs.b[tid]);
+            rdone = true;
+        } else {
+            const uint64_t w = ld_tag(rs.t + tid);
+            if (tag_of(w) == p.tag) {
+                res[tid] = tag_val(w);
+                rdone = true;
+            }
+        }
+    }
+    return rdone;
+}
+
 __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uint16_t* gain, const RSrc& rs, int nres,
                            float (&xr)[8 * kCpl], float*& res, int pc) {
     const Params& p = c.p;
@@ -764,32 +793,17 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
     const int nch = min(m.segch, m.chunks - cg0);   // chunks of this warp's segment (the last may be short)
     if (c.xphase > 0 && !wait_bar(p, c.sh, c.sh.xfree, (c.xphase - 1u) & 1u, ROLE_CONSUMER, pc)) return false;
     res = c.sh.res + (c.xphase & 1u) * kResBuf;
-    bool rdone = tid >= nres;
-    auto poll_res = [&]() {
-        if (!rdone) {
-            if (rs.b) {
-                res[tid] = bf16f(rs.b[tid]);
-                rdone = true;
-            } else {
-                const uint64_t w = ld_tag(rs.t + tid);
-                if (tag_of(w) == p.tag) {
-                    res[tid] = tag_val(w);
-                    rdone = true;
-                }
-            }
-        }
-        return rdone;
-    };
-    float ss = 0.f;
+    bool rdone = false;
     Spin sp;
     if (!m.direct) {
+        float ss = 0.f;
         for (int base = 0; base < m.chunks; base += kConsumerThreads) {   // warp-uniform trip count
             const int ch = base + tid;
             const bool valid = ch < m.chunks;
             float v[8];
             while (true) {
                 bool ok = valid ? load8x(src, ch * 8, v, p.tag) : true;
-                if (base == 0) ok &= poll_res();
+                if (base == 0) ok &= poll_res(p, rs, tid, nres, res, rdone);
                 if (__all_sync(0xFFFFFFFFu, ok)) break;
                 if (!spin_more(c, sp, pc)) return false;
             }
@@ -800,9 +814,13 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
                 for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
             }
         }
+        if (gain) {
+            ss = warp_sum(ss);
+            if (c.lane == 0) c.sh.red[48 + c.warp] = ss;
+        }
     } else {
         while (true) {
-            bool ok = poll_res();
+            bool ok = poll_res(p, rs, tid, nres, res, rdone);
 #pragma unroll
             for (int i = 0; i < kCpl; ++i) {
                 const int ch = c.lane + 32 * i;
@@ -816,10 +834,6 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
             if (__all_sync(0xFFFFFFFFu, ok)) break;
             if (!spin_more(c, sp, pc)) return false;
         }
-    }
-    if (gain) {
-        ss = warp_sum(ss);
-        if (c.lane == 0) c.sh.red[48 + c.warp] = ss;
     }
     __syncwarp();
     if (c.lane == 0) mbar_arrive(c.sh.xfull);
@@ -862,8 +876,8 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
 
 // Output of one matvec row (tile row ru, run by one lane).  The LM head keeps this lane's running
 // (max, lowest index) in bv / bi.
-__device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int ru, float s0, float s1,
-                            const float* res, float& bv, int& bi) {
+__device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int ru, float s0,
+                                            float s1, const float* res, float& bv, int& bi) {
     const Params& p = c.p;
     const int op = si.w[W_OP], l = si.w[W_LAYER];
     const size_t lb = size_t(l) * p.B + b;
@@ -893,44 +907,59 @@ __device__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int 
     }
 }
 
-// Segment g's sum of unit j of the page in ring slot `slot` (a row, or a gate/up pair: s0 gate,
-// s1 up).  With one segment per row the row is done; otherwise the sum waits in the slot's
-// partial area and the last of the row's G segments to arrive adds them in segment order and
-// writes the row.  A page slot's partials and counters are reused only after every warp has
-// released the page, so no row ever meets another row's partials.
-__device__ void mv_finish(const Cw& c, const SlotInfo& si, int pc, int b, uint32_t slot, int j, int ru, float s0,
-                          float s1, const float* res, float& bv, int& bi) {
-    const int G = si.mv.G;
-    if (G > 1) {
-        const int lg = si.mv.logG;
-        float* part = c.sh.comb + (size_t(slot) * c.p.comb_stride + j) * 2;
-        part[0] = s0;
-        part[1] = s1;
-        __threadfence_block();
-        int* cnt = c.sh.combcnt + slot * c.p.comb_stride + (j >> lg);
-        if (atomicAdd(cnt, 1) != G - 1) return;
-        __threadfence_block();
-        const float* q = c.sh.comb + (size_t(slot) * c.p.comb_stride + (j & ~(G - 1))) * 2;
-        s0 = q[0];
-        s1 = q[1];
+// The rows of one page group, once every consumer warp has left its segment sums: run by the warp
+// that arrived last, one lane per row.  A row's G segment sums are added in segment order (the
+// same order whichever warp runs this, so the result does not depend on timing or SM count).
+// Page 0 holds tile rows [r0, r0 + n0), page 1 rows [r1, r1 + n1); for gate/up both pages hold
+// the same n0 rows (gate sums in word 0 of a unit's partial, up sums in word 1).
+__device__ void group_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, uint32_t slot, uint32_t slot1, int r0,
+                               int n0, int r1, int n1, const float* res) {
+    const Params& p = c.p;
+    const int G = si.mv.G, lg = si.mv.logG;
+    const bool pair = si.inter != 0;
+    const int nrows = pair ? n0 : n0 + n1;
+    const float* cb0 = c.sh.comb + size_t(slot) * p.comb_stride * 2;
+    const float* cb1 = c.sh.comb + size_t(slot1) * p.comb_stride * 2;
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int i = c.lane; i < nrows; i += 32) {
+        const bool second = !pair && i >= n0;
+        const int r = second ? i - n0 : i;
+        const float* q = (second ? cb1 : cb0) + (size_t(r) << lg) * 2;
+        float s0 = q[0], s1 = q[1];
 #pragma unroll 1
         for (int k = 1; k < G; ++k) {
             s0 += q[2 * k];
             s1 += q[2 * k + 1];
         }
-        *cnt = 0;   // (visible to the page slot's next user through the ring's mbarriers)
+        mv_epilogue(c, si, pc, b, (second ? r1 : r0) + r, s0, s1, res, bv, bi);
     }
-    mv_epilogue(c, si, pc, b, ru, s0, s1, res, bv, bi);
+    if (si.w[W_OP] == OP_LMHEAD) {   // the group's best, merged into this warp's running best
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (c.lane == 0) {
+            float2& run = c.sh.lmbest[c.warp * kMaxBatch + b];
+            if (bv > run.x || (bv == run.x && bi < __float_as_int(run.y))) run = make_float2(bv, __int_as_float(bi));
+        }
+    }
 }
 
 // Matvec tile (QKV / O / gate-up / down / LM-head rows).  Pages hold whole rows; the tile is
 // walked in groups of two pages: two row pages, or for gate/up the gate page and the up page of
 // the same row group.  A page holds units (row, segment) in row-major order; warp w takes units
 // j = w, w + 16, ... of the group, always its own segment, two row dots at a time (the unit in the
-// first page and the unit in the second).  At batch 1 the tile streams: a warp waits only for the
-// pages of its current group and gives them back when done with them, so a tile may be far larger
-// than the page ring.  At batch > 1 every sequence reads every page: the tile's pages are held
-// until it is done.
+// first page and the unit in the second), and leaves each sum in the page slot's partial area.
+// The warp that arrives last on the group's counter writes the group's rows.  At batch 1 the tile
+// streams: a warp waits only for the pages of its current group and gives them back when done with
+// them, so a tile may be far larger than the page ring.  At batch > 1 every sequence reads every
+// page: the tile's pages are held until it is done.
 __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     const Params& p = c.p;
     const int op = si.w[W_OP], l = si.w[W_LAYER], a0 = si.w[W_A0];
@@ -945,6 +974,9 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     if (!stream && !wait_pages(c, si, pc)) return false;
     float xr[8 * kCpl];
     const size_t lane_off = size_t(g * m.segch + c.lane) * 16u;   // this lane's first chunk within a row
+    // this lane's partial word within a unit: lane 0 the first sum (word 0), lane 16 the second
+    // (gate/up: word 1 of the same unit; otherwise word 0 of the second page's unit)
+    const int pword = (pair && c.lane == 16) ? 1 : 0;
     for (int b = 0; b < p.B; ++b) {
         XSrc src{nullptr, nullptr, nullptr};
         RSrc rs{nullptr, nullptr};
@@ -974,8 +1006,6 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
         float* res;
         if (!load_input(c, si, src, gain, rs, nres, xr, res, pc)) return false;
         if (b == 0 && c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
-        float bv = -INFINITY;   // LM head: this lane's running best (lanes 0 and 16)
-        int bi = 0x7FFFFFFF;
         uint32_t slot = uint32_t(si.first_slot), ph = uint32_t(si.first_phase);
         for (int k = 0; 2 * k < npg; ++k) {
             const bool two = 2 * k + 1 < npg;
@@ -995,39 +1025,52 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 r1 = r0 + rpp;
                 n1 = two ? min(rpp, R - r1) : 0;
             }
-            const int u0 = n0 << lg, u1 = n1 << lg;
-            const uint8_t* base0 = c.sh.ring + (size_t(slot) << p.page_shift) + lane_off;
-            const uint8_t* base1 = c.sh.ring + (size_t(slot1) << p.page_shift) + lane_off;
-            for (int j = c.warp; j < max(u0, u1); j += kNumConsumerWarps) {   // warp-uniform
-                const int r = j >> lg;
-                const bool h0 = j < u0, h1 = j < u1;
-                const uint8_t* w0 = base0 + size_t(r) * rowbytes;
-                const uint8_t* w1 = base1 + size_t(r) * rowbytes;
-                float a[kCpl], e[kCpl];
+            {
+                const int u0 = n0 << lg, u1 = n1 << lg;
+                const uint8_t* base0 = c.sh.ring + (size_t(slot) << p.page_shift) + lane_off;
+                const uint8_t* base1 = c.sh.ring + (size_t(slot1) << p.page_shift) + lane_off;
+                // partial word this lane writes: lane 0 -> (slot, unit), lane 16 -> (slot1 or slot, unit)
+                float* pbase = c.sh.comb + (size_t((c.lane == 16 && !pair) ? slot1 : slot) * p.comb_stride) * 2 + pword;
+                const bool writer = (c.lane & 15) == 0;
+                for (int j = c.warp; j < max(u0, u1); j += kNumConsumerWarps) {   // warp-uniform
+                    const int r = j >> lg;
+                    const bool h0 = j < u0, h1 = j < u1;
+                    const uint8_t* w0 = base0 + size_t(r) * rowbytes;
+                    const uint8_t* w1 = base1 + size_t(r) * rowbytes;
+                    float a[kCpl], e[kCpl];
 #pragma unroll
-                for (int i = 0; i < kCpl; ++i) {
-                    a[i] = 0.f;
-                    e[i] = 0.f;
-                    if (c.lane + 32 * i < nch) {
-                        if (h0) a[i] = dot8(*reinterpret_cast<const uint4*>(w0 + i * 512), &xr[8 * i], 0.f);
-                        if (h1) e[i] = dot8(*reinterpret_cast<const uint4*>(w1 + i * 512), &xr[8 * i], 0.f);
+                    for (int i = 0; i < kCpl; ++i) {
+                        a[i] = 0.f;
+                        e[i] = 0.f;
+                        if (c.lane + 32 * i < nch) {
+                            if (h0) a[i] = dot8(*reinterpret_cast<const uint4*>(w0 + i * 512), &xr[8 * i], 0.f);
+                            if (h1) e[i] = dot8(*reinterpret_cast<const uint4*>(w1 + i * 512), &xr[8 * i], 0.f);
+                        }
                     }
-                }
-                const float s0 = (a[0] + a[1]) + (a[2] + a[3]);
-                const float s1 = (e[0] + e[1]) + (e[2] + e[3]);
-                // one butterfly for both sums: the first lands in lanes 0-15, the second in 16-31
-                const bool hi = c.lane & 16;
-                float v = (hi ? s1 : s0) + __shfl_xor_sync(0xFFFFFFFFu, hi ? s0 : s1, 16);
+                    const float s0 = (a[0] + a[1]) + (a[2] + a[3]);
+                    const float s1 = (e[0] + e[1]) + (e[2] + e[3]);
+                    // one butterfly for both sums: the first lands in lanes 0-15, the second in 16-31
+                    const bool hi = c.lane & 16;
+                    float v = (hi ? s1 : s0) + __shfl_xor_sync(0xFFFFFFFFu, hi ? s0 : s1, 16);
 #pragma unroll
-                for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                if (pair) {
-                    const float up = __shfl_sync(0xFFFFFFFFu, v, 16);
-                    if (c.lane == 0) mv_finish(c, si, pc, b, slot, j, r0 + r, v, up, res, bv, bi);
-                } else if (c.lane == 0) {
-                    if (h0) mv_finish(c, si, pc, b, slot, j, r0 + r, v, 0.f, res, bv, bi);
-                } else if (c.lane == 16) {
-                    if (h1) mv_finish(c, si, pc, b, slot1, j, r1 + r, v, 0.f, res, bv, bi);
+                    for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                    if (writer && (hi ? h1 : h0)) pbase[size_t(j) * 2] = v;
                 }
+            }
+            // every warp arrives on the group's counter; the last one writes the group's rows
+            __syncwarp();
+            int last = 0;
+            if (c.lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(c.sh.combcnt + slot, 1) == kNumConsumerWarps - 1;
+                if (last) __threadfence_block();
+            }
+            last = __shfl_sync(0xFFFFFFFFu, last, 0);
+            if (last) {
+                __syncwarp();
+                group_epilogue(c, si, pc, b, slot, slot1, r0, n0, r1, n1, res);
+                __syncwarp();
+                if (c.lane == 0) c.sh.combcnt[slot] = 0;   // (seen by the slot's next group through the ring's mbarriers)
             }
             if (stream) {   // this group's pages are done for this warp
                 __syncwarp();
@@ -1044,19 +1087,10 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 ph = ph1;
             }
         }
-        if (op == OP_LMHEAD) {   // this warp's running (max, lowest index) over its LM-head tiles so far
-            const float ov = __shfl_sync(0xFFFFFFFFu, bv, 16);
-            const int oi = __shfl_sync(0xFFFFFFFFu, bi, 16);
-            if (c.lane == 0) {
-                float2& run = c.sh.lmbest[c.warp * kMaxBatch + b];
-                int ri = __float_as_int(run.y);
-                float rv = run.x;
-                if (ov > rv || (ov == rv && oi < ri)) { rv = ov; ri = oi; }
-                if (bv > rv || (bv == rv && bi < ri)) { rv = bv; ri = bi; }
-                run = make_float2(rv, __int_as_float(ri));
-                p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * kNumConsumerWarps + c.warp] =
-                    make_int4(__float_as_int(rv), ri, int(p.epoch), 0);
-            }
+        if (op == OP_LMHEAD && c.lane == 0) {   // this warp's running best over the CTA's LM-head rows so far
+            const float2 run = c.sh.lmbest[c.warp * kMaxBatch + b];
+            p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * kNumConsumerWarps + c.warp] =
+                make_int4(__float_as_int(run.x), __float_as_int(run.y), int(p.epoch), 0);
         }
         // batch > 1: the page slots' partials and counters serve the next sequence
         if (!stream && !cbar(c, pc)) return false;
@@ -1344,11 +1378,11 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
         uint32_t v = ld_relaxed_gpu(p.counters + cid);
         if (int32_t(v - target) < 0) {
             const uint64_t t0 = globaltimer();
+            uint32_t rounds = 0;
             while (true) {
                 v = ld_relaxed_gpu(p.counters + cid);
                 if (int32_t(v - target) >= 0) break;
-                if (*reinterpret_cast<volatile int*>(sh.abort) ||
-                    ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(p.err))) {
+                if (*reinterpret_cast<volatile int*>(sh.abort) || other_cta_failed(p, rounds)) {
                     *reinterpret_cast<volatile int*>(sh.abort) = 1;
                     return false;
                 }
