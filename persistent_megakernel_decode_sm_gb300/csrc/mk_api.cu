@@ -235,7 +235,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
             return fail(MK_ERR_CAPACITY, "a %d-byte page holds no %d-element row", g.page_bytes, K);
         if (mv[op].segch > 32 * kCpl)
             return fail(MK_ERR_ARG, "matvec row length %d cannot be cut into %d segments", K, kMaxSeg);
-        if (mv[op].G > 1) comb_stride = std::max(comb_stride, mv[op].rpp * mv[op].G);
+        comb_stride = std::max(comb_stride, mv[op].rpp * mv[op].G);   // (row, segment) units of a page
     }
     const void* fn = megakernel_fn();
     int asf = hpg * g.n_chunk;

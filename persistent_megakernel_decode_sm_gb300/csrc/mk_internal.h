@@ -203,7 +203,7 @@ struct Params {
     int32_t attn_scratch_floats;
     int32_t qrot_floats;
     int32_t xbuf_floats;     // shared input buffer (floats)
-    int32_t comb_stride;     // segment partials per page slot
+    int32_t comb_stride;     // (row, segment) units of a page, at most: partial words per page slot
 };
 
 // one instruction slot: words + where its stream sits + the matvec shape.  16-byte aligned and

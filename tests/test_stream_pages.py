@@ -9,7 +9,7 @@ depends on the row length only) and units (row, segment) j = w, w + 16, ... of e
 test restates that mapping for every batch-1 matvec tile of every workload (rows per tile from the
 scheduler's restatement) and checks that the pages cover the rows exactly once in order, that
 every (row, segment) unit is computed by exactly one warp that always holds the same segment, that
-a page's units fit the shared partial area the bind sizes, and that the bind's page rule (two
+a page's units fit the shared partial area the bind sizes (every unit leaves a partial), and that the bind's page rule (two
 pages per step, plus an attention tile) fits the 6-page ring of the default 32 KB pages.
 """
 import pytest
@@ -63,7 +63,7 @@ def test_batch1_groups_cover_every_unit_once(name, S):
     tiles, _, _ = sr.enumerate_tiles(cfg, o, S)
     K = {sr.QKV: cfg.hidden, sr.OPROJ: cfg.q_dim, sr.UPGATE: cfg.hidden, sr.DOWN: cfg.ffn,
          sr.LMHEAD: cfg.hidden}
-    comb_stride = max([1] + [(PB // (2 * k)) * segments(k) for k in K.values() if segments(k) > 1])
+    comb_stride = max((PB // (2 * k)) * segments(k) for k in K.values())
     seen = 0
     for t in tiles:
         if t.op not in K:
@@ -80,8 +80,7 @@ def test_batch1_groups_cover_every_unit_once(name, S):
             pages_seen += sum(1 for p in pages if p)
             for pi, prow in enumerate(pages):
                 units = len(prow) << lg
-                if G > 1:
-                    assert units <= comb_stride
+                assert units <= comb_stride   # the page slot's partial area holds every unit
                 for w in range(WARPS):
                     for j in range(w, units, WARPS):
                         assert j % G == w % G            # a warp keeps its own segment
