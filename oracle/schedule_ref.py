@@ -257,15 +257,12 @@ def _shuffle(xs: List[Tile], rng: SplitMix64) -> List[Tile]:
 
 
 def tile_pages(t: Tile, cfg, o: SchedOpts) -> int:
-    """Pages of a tile's stream: a matvec tile streams whole rows per page (a gate/up page holds
-    the gate rows of its pairs, then their up rows); an attention tile streams its bytes
-    contiguously."""
+    """Pages of a tile's stream: a matvec tile streams whole rows per page (gate/up: gate and up
+    row groups in alternate pages); an attention tile streams its bytes contiguously."""
     if t.op in (QKV, OPROJ, UPGATE, DOWN, LMHEAD):
         K = cfg.q_dim if t.op == OPROJ else (cfg.ffn if t.op == DOWN else cfg.hidden)
         rpp = o.page_bytes // (2 * K)
-        if t.op == UPGATE:
-            rpp //= 2
-        return ceil_div(t.a1, rpp)
+        return ceil_div(t.a1, rpp) * (2 if t.op == UPGATE else 1)
     return ceil_div(t.stream_bytes, o.page_bytes)
 
 

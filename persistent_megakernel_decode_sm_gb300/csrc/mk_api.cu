@@ -148,11 +148,11 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, std::
                 break;
             default: break;
         }
-        if (src0) {   // whole rows per page; a gate/up page: the gate rows of its pairs, then their up rows
+        if (src0) {   // whole rows per page; gate/up: gate and up row groups in alternate pages
             const int64_t K = op == OP_OPROJ ? qd : (op == OP_DOWN ? F : H);
-            const int64_t rpp = (g.page_bytes / (2 * K)) >> (op == OP_UPGATE ? 1 : 0);
+            const int64_t rpp = g.page_bytes / (2 * K);
             if (rpp < 1) return bad("a page holds no row");
-            const int64_t pages = (a1 + rpp - 1) / rpp;
+            const int64_t pages = ((a1 + rpp - 1) / rpp) * (op == OP_UPGATE ? 2 : 1);
             if (pages != x[W_NPAGES] || b0 + b1 > (int64_t(1) << 31) - 1) return bad("page count");
             put64(x + W_SRC0, src0);
             put64(x + W_SRC1, src1);
@@ -231,7 +231,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     for (int op : {int(OP_QKV), int(OP_OPROJ), int(OP_UPGATE), int(OP_DOWN), int(OP_LMHEAD)}) {
         const int K = op == OP_OPROJ ? qd : (op == OP_DOWN ? c.ffn : H);
         mv[op] = mv_shape(K, g.page_bytes, xbuf);
-        if (mv[op].rpp < (op == OP_UPGATE ? 2 : 1))
+        if (mv[op].rpp < 1)
             return fail(MK_ERR_CAPACITY, "a %d-byte page holds no %d-element row", g.page_bytes, K);
         if (mv[op].segch > 32 * kCpl)
             return fail(MK_ERR_ARG, "matvec row length %d cannot be cut into %d segments", K, kMaxSeg);
@@ -247,9 +247,9 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     if (n_pages < 1) return fail(MK_ERR_CAPACITY, "no room for a page ring");
     const int misc = smem_misc_bytes(n_pages, asf, qrf, xbuf, comb_stride);
     // capacity: at batch > 1 a tile's pages are held until it is done, so the ring must hold the
-    // largest tile; at batch 1 a matvec tile streams through the ring one page at a time, and an
-    // attention tile holds its K and V rows
-    int need_pages = 1;
+    // largest tile; at batch 1 a matvec tile streams through the ring one group of two pages at a
+    // time, and an attention tile holds its K and V rows
+    int need_pages = 2;
     if (c.batch > 1) need_pages = std::max(need_pages, s->max_pages);
     else need_pages = std::max<int>(need_pages, int((2ll * g.attn_chunk * d * 2 + g.page_bytes - 1) / g.page_bytes));
     if (n_pages < need_pages)

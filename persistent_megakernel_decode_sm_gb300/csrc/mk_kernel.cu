@@ -329,8 +329,8 @@ struct Stream {
     int nseg;
     uint32_t total;
     int pages;
-    int inter;                       // gate/up tile: page j holds gate rows [j rpp, (j+1) rpp), then the same up rows
-    uint32_t rows, rowbytes, rpp;    // matvec: rows (pairs) per page (0 rows: a plain byte stream)
+    int inter;                       // gate/up tile: page 2j = gate rows [j rpp, (j+1) rpp), 2j+1 = up rows
+    uint32_t rows, rowbytes, rpp;    // matvec: whole rows per page (0 rows: a plain byte stream)
 };
 
 __device__ __forceinline__ int attn_old_rows(const Params& p, int b, int c, int chunk) {
@@ -373,7 +373,7 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
     st.inter = 0;
     st.rows = st.rowbytes = st.rpp = 0;
     const int op = w[W_OP];
-    if (is_matvec(op)) {   // whole rows per page; gate/up: a page holds the gate rows, then the up rows, of its pairs
+    if (is_matvec(op)) {   // whole rows per page; gate/up: gate and up row groups in alternate pages
         const uint32_t b0 = uint32_t(w[W_BYTES0]), b1 = uint32_t(w[W_BYTES1]);
         st.seg[0] = {word_ptr(w + W_SRC0), 0u, b0};
         st.seg[1] = {word_ptr(w + W_SRC1), b0, b1};
@@ -382,9 +382,9 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
         st.inter = op == OP_UPGATE;
         st.rows = uint32_t(w[W_A1]);
         st.rowbytes = p.mv[op].rowbytes;
-        st.rpp = uint32_t(p.mv[op].rpp) >> (st.inter ? 1 : 0);   // rows (gate/up: pairs) per page
+        st.rpp = uint32_t(p.mv[op].rpp);
         if (b0 == 0 || st.rpp == 0 || b0 != st.rows * st.rowbytes || b1 != (st.inter ? b0 : 0u)) return MK_ERR_BOUNDS;
-        st.pages = int((st.rows + st.rpp - 1u) / st.rpp);
+        st.pages = int((st.rows + st.rpp - 1u) / st.rpp) * (st.inter ? 2 : 1);
         if (st.pages > w[W_NPAGES] || (p.B > 1 && st.pages > p.n_pages)) return MK_ERR_CAPACITY;
         return MK_OK;
     } else if (op == OP_ATTN) {
@@ -497,12 +497,12 @@ __device__ void loader(const Params& p, const Shared& sh) {
                 break;
             }
             uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
-            if (st.rows) {   // matvec: whole rows (gate/up: the gate rows of the page's pairs, then their up rows)
-                const uint32_t r0 = uint32_t(pg) * st.rpp;
+            if (st.rows) {   // matvec: a group of whole rows (gate/up: gate rows on even pages, up rows on odd)
+                const uint32_t r0 = uint32_t(st.inter ? pg >> 1 : pg) * st.rpp;
                 const uint32_t bytes = min(st.rpp, st.rows - r0) * st.rowbytes;
-                mbar_arrive_expect_tx(sh.full + ps, st.inter ? 2u * bytes : bytes);
-                bulk_g2s(dst, st.seg[0].src + size_t(r0) * st.rowbytes, bytes, sh.full + ps, pol);
-                if (st.inter) bulk_g2s(dst + bytes, st.seg[1].src + size_t(r0) * st.rowbytes, bytes, sh.full + ps, pol);
+                mbar_arrive_expect_tx(sh.full + ps, bytes);
+                bulk_g2s(dst, ((st.inter && (pg & 1)) ? st.seg[1].src : st.seg[0].src) + size_t(r0) * st.rowbytes, bytes,
+                         sh.full + ps, pol);
             } else {
                 const uint32_t lo = uint32_t(pg) * PB;
                 const uint32_t hi = min(lo + PB, st.total);
@@ -783,40 +783,6 @@ __device__ __forceinline__ bool poll_res(const Params& p, const RSrc& rs, int ti
     return rdone;
 }
 
-// Cooperative part of an input load: thread t polls the 8-element chunks t, t + 512, ... of the
-// input into the shared buffer and (t < nres) the residual word of tile row t; one sum of squares
-// per warp into red[48 + warp] when `norm`.  Not inlined: its polling loop must not compete for
-// registers with the state a matvec tile keeps across it.
-__device__ __noinline__ bool poll_shared_input(const Params& p, const Shared& sh, int pc, XSrc src, RSrc rs, int nres,
-                                               int chunks, float* res, int norm) {
-    const int tid = int(threadIdx.x), lane = tid & 31;
-    bool rdone = false;
-    float ss = 0.f;
-    Spin sp;
-    for (int base = 0; base < chunks; base += kConsumerThreads) {   // warp-uniform trip count
-        const int ch = base + tid;
-        const bool valid = ch < chunks;
-        float v[8];
-        while (true) {
-            bool ok = valid ? load8x(src, ch * 8, v, p.tag) : true;
-            if (base == 0) ok &= poll_res(p, rs, tid, nres, res, rdone);
-            if (__all_sync(0xFFFFFFFFu, ok)) break;
-            if (!spin_more(p, sh, lane, sp, pc)) return false;
-        }
-        if (valid) {
-            *reinterpret_cast<float4*>(sh.xbuf + ch * 8) = make_float4(v[0], v[1], v[2], v[3]);
-            *reinterpret_cast<float4*>(sh.xbuf + ch * 8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
-        }
-    }
-    if (norm) {
-        ss = warp_sum(ss);
-        if (lane == 0) sh.red[48 + (tid >> 5)] = ss;
-    }
-    return true;
-}
-
 __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uint16_t* gain, const RSrc& rs, int nres,
                            float (&xr)[8 * kCpl], float*& res, int pc) {
     const Params& p = c.p;
@@ -827,11 +793,32 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
     const int nch = min(m.segch, m.chunks - cg0);   // chunks of this warp's segment (the last may be short)
     if (c.xphase > 0 && !wait_bar(p, c.sh, c.sh.xfree, (c.xphase - 1u) & 1u, ROLE_CONSUMER, pc)) return false;
     res = c.sh.res + (c.xphase & 1u) * kResBuf;
+    bool rdone = false;
+    Spin sp;
     if (!m.direct) {
-        if (!poll_shared_input(p, c.sh, pc, src, rs, nres, m.chunks, res, gain != nullptr)) return false;
+        float ss = 0.f;
+        for (int base = 0; base < m.chunks; base += kConsumerThreads) {   // warp-uniform trip count
+            const int ch = base + tid;
+            const bool valid = ch < m.chunks;
+            float v[8];
+            while (true) {
+                bool ok = valid ? load8x(src, ch * 8, v, p.tag) : true;
+                if (base == 0) ok &= poll_res(p, rs, tid, nres, res, rdone);
+                if (__all_sync(0xFFFFFFFFu, ok)) break;
+                if (!spin_more(c, sp, pc)) return false;
+            }
+            if (valid) {
+                *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+            }
+        }
+        if (gain) {
+            ss = warp_sum(ss);
+            if (c.lane == 0) c.sh.red[48 + c.warp] = ss;
+        }
     } else {
-        bool rdone = false;
-        Spin sp;
         while (true) {
             bool ok = poll_res(p, rs, tid, nres, res, rdone);
 #pragma unroll
@@ -920,30 +907,34 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
     }
 }
 
-// The rows of one page, once every consumer warp has left its segment sums: run by the warp that
-// arrived last, one lane per row.  A row's G segment sums are added in segment order (the same
-// order whichever warp runs this, so the result does not depend on timing or SM count).  The page
-// holds tile rows [r0, r0 + n); a gate/up page holds pairs [r0, r0 + n): n gate rows, then n up rows.
-__device__ void page_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, uint32_t slot, int r0, int n,
-                              const float* res) {
+// The rows of one page group, once every consumer warp has left its segment sums: run by the warp
+// that arrived last, one lane per row.  A row's G segment sums are added in segment order (the
+// same order whichever warp runs this, so the result does not depend on timing or SM count).
+// Page 0 holds tile rows [r0, r0 + n0), page 1 rows [r1, r1 + n1); for gate/up both pages hold
+// the same n0 rows (gate sums in word 0 of a unit's partial, up sums in word 1).
+__device__ void group_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, uint32_t slot, uint32_t slot1, int r0,
+                               int n0, int r1, int n1, const float* res) {
     const Params& p = c.p;
     const int G = si.mv.G, lg = si.mv.logG;
     const bool pair = si.inter != 0;
-    const float* cb = c.sh.comb + size_t(slot) * p.comb_stride;
+    const int nrows = pair ? n0 : n0 + n1;
+    const float* cb0 = c.sh.comb + size_t(slot) * p.comb_stride * 2;
+    const float* cb1 = c.sh.comb + size_t(slot1) * p.comb_stride * 2;
     float bv = -INFINITY;
     int bi = 0x7FFFFFFF;
-    for (int i = c.lane; i < n; i += 32) {
-        const float* q = cb + (size_t(i) << lg);
-        const float* u = cb + (size_t(n + i) << lg);
-        float s0 = q[0], s1 = pair ? u[0] : 0.f;
+    for (int i = c.lane; i < nrows; i += 32) {
+        const bool second = !pair && i >= n0;
+        const int r = second ? i - n0 : i;
+        const float* q = (second ? cb1 : cb0) + (size_t(r) << lg) * 2;
+        float s0 = q[0], s1 = q[1];
 #pragma unroll 1
         for (int k = 1; k < G; ++k) {
-            s0 += q[k];
-            if (pair) s1 += u[k];
+            s0 += q[2 * k];
+            s1 += q[2 * k + 1];
         }
-        mv_epilogue(c, si, pc, b, r0 + i, s0, s1, res, bv, bi);
+        mv_epilogue(c, si, pc, b, (second ? r1 : r0) + r, s0, s1, res, bv, bi);
     }
-    if (si.w[W_OP] == OP_LMHEAD) {   // the page's best, merged into this warp's running best
+    if (si.w[W_OP] == OP_LMHEAD) {   // the group's best, merged into this warp's running best
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
             const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
@@ -960,22 +951,21 @@ __device__ void page_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, ui
     }
 }
 
-// Matvec tile (QKV / O / gate-up / down / LM-head rows).  Pages hold whole rows (a gate/up page:
-// the gate rows of its pairs, then their up rows).  A page's rows are cut into units (row,
-// segment), in row-major order; warp w takes units j = w, w + 16, ... of each page -- always its
-// own segment -- two at a time (one butterfly for both sums), and leaves each sum in the page
-// slot's partial area.  The warp that arrives last on the page's counter writes the page's rows.
-// At batch 1 the tile streams: a warp waits only for its current page and gives it back when done
-// with it, so a tile may be far larger than the page ring and all but one page of the ring are
-// free to be in flight.  At batch > 1 every sequence reads every page: the tile's pages are held
-// until it is done.
+// Matvec tile (QKV / O / gate-up / down / LM-head rows).  Pages hold whole rows; the tile is
+// walked in groups of two pages: two row pages, or for gate/up the gate page and the up page of
+// the same row group.  A page holds units (row, segment) in row-major order; warp w takes units
+// j = w, w + 16, ... of the group, always its own segment, two row dots at a time (the unit in the
+// first page and the unit in the second), and leaves each sum in the page slot's partial area.
+// The warp that arrives last on the group's counter writes the group's rows.  At batch 1 the tile
+// streams: a warp waits only for the pages of its current group and gives them back when done with
+// them, so a tile may be far larger than the page ring.  At batch > 1 every sequence reads every
+// page: the tile's pages are held until it is done.
 __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     const Params& p = c.p;
     const int op = si.w[W_OP], l = si.w[W_LAYER], a0 = si.w[W_A0];
     const bool pair = si.inter != 0;
     const MvShape& m = si.mv;
-    const int R = si.rows, lg = m.logG;
-    const int rpp = pair ? m.rpp >> 1 : m.rpp;   // rows (pairs) per page
+    const int R = si.rows, rpp = m.rpp, lg = m.logG;
     const int g = c.warp & (m.G - 1);
     const int nch = min(m.segch, m.chunks - g * m.segch);
     const uint32_t rowbytes = m.rowbytes, NP = uint32_t(p.n_pages);
@@ -983,8 +973,10 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     const bool stream = p.B == 1;
     if (!stream && !wait_pages(c, si, pc)) return false;
     float xr[8 * kCpl];
-    const uint32_t lane_off = uint32_t(g * m.segch + c.lane) * 16u;   // this lane's first chunk within a row
-    const uint32_t jstep = uint32_t(kNumConsumerWarps >> lg) * rowbytes; // from unit j's row to unit j + 16's row
+    const size_t lane_off = size_t(g * m.segch + c.lane) * 16u;   // this lane's first chunk within a row
+    // this lane's partial word within a unit: lane 0 the first sum (word 0), lane 16 the second
+    // (gate/up: word 1 of the same unit; otherwise word 0 of the second page's unit)
+    const int pword = (pair && c.lane == 16) ? 1 : 0;
     for (int b = 0; b < p.B; ++b) {
         XSrc src{nullptr, nullptr, nullptr};
         RSrc rs{nullptr, nullptr};
@@ -1015,25 +1007,43 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
         if (!load_input(c, si, src, gain, rs, nres, xr, res, pc)) return false;
         if (b == 0 && c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
         uint32_t slot = uint32_t(si.first_slot), ph = uint32_t(si.first_phase);
-        for (int k = 0; k < npg; ++k) {
-            if (stream && !wait_bar(p, c.sh, c.sh.full + slot, ph, ROLE_CONSUMER, pc)) return false;
-            const int r0 = k * rpp;
-            const int n = min(rpp, R - r0);
+        for (int k = 0; 2 * k < npg; ++k) {
+            const bool two = 2 * k + 1 < npg;
+            const uint32_t slot1 = slot + 1u == NP ? 0u : slot + 1u;
+            const uint32_t ph1 = slot + 1u == NP ? ph ^ 1u : ph;
+            if (stream) {
+                if (!wait_bar(p, c.sh, c.sh.full + slot, ph, ROLE_CONSUMER, pc)) return false;
+                if (two && !wait_bar(p, c.sh, c.sh.full + slot1, ph1, ROLE_CONSUMER, pc)) return false;
+            }
+            int r0, n0, r1, n1;   // first tile row and rows of each page of the group
+            if (pair) {
+                r0 = r1 = k * rpp;
+                n0 = n1 = min(rpp, R - r0);
+            } else {
+                r0 = 2 * k * rpp;
+                n0 = min(rpp, R - r0);
+                r1 = r0 + rpp;
+                n1 = two ? min(rpp, R - r1) : 0;
+            }
             {
-                const int units = (pair ? 2 * n : n) << lg;
-                const uint8_t* base = c.sh.ring + (size_t(slot) << p.page_shift) + lane_off;
-                float* pw = c.sh.comb + size_t(slot) * p.comb_stride;
-                for (int j = c.warp; j < units; j += 2 * kNumConsumerWarps) {   // warp-uniform
-                    const bool h1 = j + kNumConsumerWarps < units;
-                    const uint8_t* w0 = base + uint32_t(j >> lg) * rowbytes;
-                    const uint8_t* w1 = w0 + jstep;
+                const int u0 = n0 << lg, u1 = n1 << lg;
+                const uint8_t* base0 = c.sh.ring + (size_t(slot) << p.page_shift) + lane_off;
+                const uint8_t* base1 = c.sh.ring + (size_t(slot1) << p.page_shift) + lane_off;
+                // partial word this lane writes: lane 0 -> (slot, unit), lane 16 -> (slot1 or slot, unit)
+                float* pbase = c.sh.comb + (size_t((c.lane == 16 && !pair) ? slot1 : slot) * p.comb_stride) * 2 + pword;
+                const bool writer = (c.lane & 15) == 0;
+                for (int j = c.warp; j < max(u0, u1); j += kNumConsumerWarps) {   // warp-uniform
+                    const int r = j >> lg;
+                    const bool h0 = j < u0, h1 = j < u1;
+                    const uint8_t* w0 = base0 + size_t(r) * rowbytes;
+                    const uint8_t* w1 = base1 + size_t(r) * rowbytes;
                     float a[kCpl], e[kCpl];
 #pragma unroll
                     for (int i = 0; i < kCpl; ++i) {
                         a[i] = 0.f;
                         e[i] = 0.f;
                         if (c.lane + 32 * i < nch) {
-                            a[i] = dot8(*reinterpret_cast<const uint4*>(w0 + i * 512), &xr[8 * i], 0.f);
+                            if (h0) a[i] = dot8(*reinterpret_cast<const uint4*>(w0 + i * 512), &xr[8 * i], 0.f);
                             if (h1) e[i] = dot8(*reinterpret_cast<const uint4*>(w1 + i * 512), &xr[8 * i], 0.f);
                         }
                     }
@@ -1044,11 +1054,10 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                     float v = (hi ? s1 : s0) + __shfl_xor_sync(0xFFFFFFFFu, hi ? s0 : s1, 16);
 #pragma unroll
                     for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                    if (c.lane == 0) pw[j] = v;
-                    else if (c.lane == 16 && h1) pw[j + kNumConsumerWarps] = v;
+                    if (writer && (hi ? h1 : h0)) pbase[size_t(j) * 2] = v;
                 }
             }
-            // every warp arrives on the page's counter; the last one writes the page's rows
+            // every warp arrives on the group's counter; the last one writes the group's rows
             __syncwarp();
             int last = 0;
             if (c.lane == 0) {
@@ -1059,17 +1068,23 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
             last = __shfl_sync(0xFFFFFFFFu, last, 0);
             if (last) {
                 __syncwarp();
-                page_epilogue(c, si, pc, b, slot, r0, n, res);
+                group_epilogue(c, si, pc, b, slot, slot1, r0, n0, r1, n1, res);
                 __syncwarp();
-                if (c.lane == 0) c.sh.combcnt[slot] = 0;   // (seen by the slot's next page through the ring's mbarriers)
+                if (c.lane == 0) c.sh.combcnt[slot] = 0;   // (seen by the slot's next group through the ring's mbarriers)
             }
-            if (stream) {   // this page is done for this warp
+            if (stream) {   // this group's pages are done for this warp
                 __syncwarp();
-                if (c.lane == 0) mbar_arrive(c.sh.empty + slot);
+                if (c.lane == 0) {
+                    mbar_arrive(c.sh.empty + slot);
+                    if (two) mbar_arrive(c.sh.empty + slot1);
+                }
             }
-            if (++slot == NP) {
-                slot = 0;
-                ph ^= 1u;
+            if (two) {
+                slot = slot1 + 1u == NP ? 0u : slot1 + 1u;
+                ph = slot1 + 1u == NP ? ph1 ^ 1u : ph1;
+            } else {
+                slot = slot1;
+                ph = ph1;
             }
         }
         if (op == OP_LMHEAD && c.lane == 0) {   // this warp's running best over the CTA's LM-head rows so far

@@ -171,10 +171,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     if (o.rows_lm) g.r_lm = o.rows_lm;
     if (g.r_qkv < 1 || g.r_qkv > d) return fail(MK_ERR_ARG, "rows_qkv must be in [1, head_dim]");
     if (g.r_o < 1 || g.r_up < 1 || g.r_lm < 1 || g.r_dn < 1) return fail(MK_ERR_ARG, "rows per tile must be >= 1");
-    // matvec tiles stream whole rows per page, gate/up tiles a gate row and its up row at least
-    if (g.page_bytes < 2 * std::max(2 * H, std::max(qd, F)))
-        return fail(MK_ERR_ARG, "page_bytes %d holds no matvec row (%d bytes)", g.page_bytes,
-                    2 * std::max(2 * H, std::max(qd, F)));
+    if (g.page_bytes < 2 * std::max(H, std::max(qd, F)))   // matvec tiles stream whole rows per page
+        return fail(MK_ERR_ARG, "page_bytes %d holds no matvec row (%d bytes)", g.page_bytes, 2 * std::max(H, std::max(qd, F)));
     g.n_qkv = cdiv(nqkv, g.r_qkv);
     g.n_o = cdiv(H, g.r_o);
     g.n_up = cdiv(F, g.r_up);
@@ -323,13 +321,13 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
             for (int q = 0; q < t.nwait; ++q) { w[W_WAIT + 2 * q] = t.wait[q][0]; w[W_WAIT + 2 * q + 1] = t.wait[q][1]; }
             w[W_NPUB] = t.npub;
             for (int q = 0; q < t.npub; ++q) { w[W_PUB + 2 * q] = t.pub[q][0]; w[W_PUB + 2 * q + 1] = t.pub[q][1]; }
-            // matvec tiles stream whole rows per page (a gate/up page: the gate rows of its pairs,
-            // then their up rows); an attention tile streams its K rows, then its V rows
+            // matvec tiles stream whole rows per page (gate/up: gate and up row groups in alternate
+            // pages); an attention tile streams its K rows, then its V rows
             int64_t pages = (t.stream_bytes + g.page_bytes - 1) / g.page_bytes;
             if (t.op == OP_QKV || t.op == OP_OPROJ || t.op == OP_UPGATE || t.op == OP_DOWN || t.op == OP_LMHEAD) {
                 const int64_t K = t.op == OP_OPROJ ? qd : (t.op == OP_DOWN ? F : H);
-                const int64_t rpp = (g.page_bytes / (2 * K)) >> (t.op == OP_UPGATE ? 1 : 0);
-                pages = (t.a1 + rpp - 1) / rpp;
+                const int64_t rpp = g.page_bytes / (2 * K);
+                pages = ((t.a1 + rpp - 1) / rpp) * (t.op == OP_UPGATE ? 2 : 1);
             }
             if (pages > (1 << 20)) { delete sch; return fail(MK_ERR_CAPACITY, "tile too large"); }
             w[W_NPAGES] = int32_t(pages);

@@ -1,16 +1,16 @@
 """Host check of the batch-1 streaming contract between the loader, the consumer warps and the
 bind-time capacity rule (no GPU).
 
-At batch 1 a matvec tile streams through the page ring: every page holds whole rows (a gate/up
-page: the gate rows of its pairs, then their up rows), and each consumer warp waits for one page
-at a time and gives it back when done.  Warp w computes segment w mod G of every row it touches (G, the segments per row,
+At batch 1 a matvec tile streams through the page ring: every page holds whole rows (gate/up:
+the gate rows and the up rows of one row group in two consecutive pages), and the consumer warps
+walk the pages in groups of two, each warp waiting for the group's pages and giving them back
+when done.  Warp w computes segment w mod G of every row it touches (G, the segments per row,
 depends on the row length only) and units (row, segment) j = w, w + 16, ... of each page.  This
 test restates that mapping for every batch-1 matvec tile of every workload (rows per tile from the
 scheduler's restatement) and checks that the pages cover the rows exactly once in order, that
 every (row, segment) unit is computed by exactly one warp that always holds the same segment, that
-a page's units fit the shared partial area the bind sizes (every unit leaves a partial), and
-that the bind's page rule (one page, or an attention tile) fits the 6-page ring of the default
-32 KB pages.
+a page's units fit the shared partial area the bind sizes (every unit leaves a partial), and that the bind's page rule (two
+pages per step, plus an attention tile) fits the 6-page ring of the default 32 KB pages.
 """
 import pytest
 
@@ -32,22 +32,27 @@ def segments(K):
     return G
 
 
-def tile_pages(op, rows, K):
-    """Yields, per page, the (side, tile row) pairs it holds in page order: side 0 a row (or a gate
-    row), side 1 an up row."""
+def tile_groups(op, rows, K):
+    """Yields, per two-page group, the tile rows in each page (a list of two lists)."""
     rpp = PB // (2 * K)
-    pair = op == sr.UPGATE
-    if pair:
-        rpp //= 2
     assert rpp >= 1
-    for r0 in range(0, rows, rpp):
-        n = min(rpp, rows - r0)
-        yield [(0, r) for r in range(r0, r0 + n)] + ([(1, r) for r in range(r0, r0 + n)] if pair else [])
+    pair = op == sr.UPGATE
+    n_pages = -(-rows // rpp) * (2 if pair else 1)
+    for k in range(0, n_pages, 2):
+        pages = []
+        for pg in (k, k + 1):
+            if pg >= n_pages:
+                pages.append([])
+                continue
+            grp = pg // 2 if pair else pg
+            pages.append(list(range(grp * rpp, min(rows, (grp + 1) * rpp))))
+        yield pages
+    return n_pages
 
 
 def bind_rule_pages(cfg, chunk):
-    """The bind's page rule at batch 1 (restated): one page, or an attention tile's K and V rows."""
-    return max(1, -(-(2 * chunk * cfg.head_dim * 2) // PB))
+    """The bind's page rule at batch 1 (restated): a group of two pages, or an attention tile."""
+    return max(2, -(-(2 * chunk * cfg.head_dim * 2) // PB))
 
 
 @pytest.mark.parametrize("name", [w for w in WORKLOADS if get_workload(w).cfg.batch == 1])
@@ -71,17 +76,16 @@ def test_batch1_groups_cover_every_unit_once(name, S):
         assert segch <= 32 * CPL and WARPS % G == 0
         done = {}
         pages_seen = 0
-        for prow in tile_pages(t.op, t.a1, k_len):
-            pages_seen += 1
-            units = len(prow) << lg
-            assert units <= comb_stride   # the page slot's partial area holds every unit
-            assert len(prow) * 2 * k_len <= PB
-            for w in range(WARPS):
-                for j in range(w, units, WARPS):
-                    assert j % G == w % G            # a warp keeps its own segment
-                    side, row = prow[j >> lg]
-                    key = (side, row, j % G)
-                    done[key] = done.get(key, 0) + 1
+        for pages in tile_groups(t.op, t.a1, k_len):
+            pages_seen += sum(1 for p in pages if p)
+            for pi, prow in enumerate(pages):
+                units = len(prow) << lg
+                assert units <= comb_stride   # the page slot's partial area holds every unit
+                for w in range(WARPS):
+                    for j in range(w, units, WARPS):
+                        assert j % G == w % G            # a warp keeps its own segment
+                        key = (pi if t.op == sr.UPGATE else 0, prow[j >> lg], j % G)
+                        done[key] = done.get(key, 0) + 1
         # every (row, segment) -- for gate/up, of the gate and the up row -- exactly once
         sides = 2 if t.op == sr.UPGATE else 1
         assert sorted(done) == sorted((side, r, s) for side in range(sides) for r in range(t.a1)
