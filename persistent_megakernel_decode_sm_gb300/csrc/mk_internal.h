@@ -49,6 +49,7 @@ constexpr int kCpl = 4;              // 16-byte chunks a lane holds of its row s
 constexpr int kMaxSeg = 16;          // row segments of a matvec (a power of two dividing the warp count)
 constexpr int kDirectMinK = 4097;    // rows this long take their input per warp, not through the shared buffer
 constexpr int kResBuf = 64;          // residual words of a tile's rows staged in shared memory (per buffer)
+constexpr int kL2Ahead = 8;          // pages of a matvec stream warmed into L2 ahead of the ring copies
 constexpr int kMinXBuf = 3072;       // floats of the shared input buffer at least (attention scores, combine)
 constexpr int kAttnChunkTiles = 152; // default attention chunk: grown while a layer has more chunks
 

@@ -89,6 +89,10 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
+// warms L2 with `bytes` (a multiple of 16) from global memory; no shared memory, no completion
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -413,6 +417,14 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
 }
 
 // ------------------------------------------------------------------------- loader -----------
+// Page pg of a matvec stream: its source and bytes (whole rows; a gate/up tile alternates gate
+// pages and up pages of the same row group).
+__device__ __forceinline__ const uint8_t* mv_page(const Stream& st, uint32_t pg, uint32_t& bytes) {
+    const uint32_t r0 = (st.inter ? pg >> 1 : pg) * st.rpp;
+    bytes = min(st.rpp, st.rows - r0) * st.rowbytes;
+    return ((st.inter && (pg & 1u)) ? st.seg[1].src : st.seg[0].src) + size_t(r0) * st.rowbytes;
+}
+
 __device__ void loader(const Params& p, const Shared& sh) {
     const int32_t* q = p.queues + size_t(blockIdx.x) * p.Q * kWords;
     const uint64_t pol = evict_first_policy();
@@ -490,19 +502,31 @@ __device__ void loader(const Params& p, const Shared& sh) {
         mbar_arrive(sh.ins_full + slot);   // release: the slot's words are visible to the consumers
         if (si.w[W_OP] == OP_END) break;
         bool stop = false;
+        // a matvec stream is warmed into L2 kL2Ahead pages ahead of the copies into the ring: the
+        // ring's own depth then only has to cover the L2 -> shared memory hop
+        if (st.rows)
+            for (int pg = 0; pg < min(st.pages, kL2Ahead); ++pg) {
+                uint32_t bytes;
+                const uint8_t* src = mv_page(st, uint32_t(pg), bytes);
+                prefetch_l2(src, bytes);
+            }
         for (int pg = 0; pg < st.pages; ++pg) {
             const uint32_t ps = cur_slot;
+            if (st.rows && pg + kL2Ahead < st.pages) {
+                uint32_t bytes;
+                const uint8_t* src = mv_page(st, uint32_t(pg + kL2Ahead), bytes);
+                prefetch_l2(src, bytes);
+            }
             if (page_seq >= NP && !wait_bar(p, sh, sh.empty + ps, cur_phase ^ 1u, ROLE_LOADER, pc)) {
                 stop = true;
                 break;
             }
             uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
             if (st.rows) {   // matvec: a group of whole rows (gate/up: gate rows on even pages, up rows on odd)
-                const uint32_t r0 = uint32_t(st.inter ? pg >> 1 : pg) * st.rpp;
-                const uint32_t bytes = min(st.rpp, st.rows - r0) * st.rowbytes;
+                uint32_t bytes;
+                const uint8_t* src = mv_page(st, uint32_t(pg), bytes);
                 mbar_arrive_expect_tx(sh.full + ps, bytes);
-                bulk_g2s(dst, ((st.inter && (pg & 1)) ? st.seg[1].src : st.seg[0].src) + size_t(r0) * st.rowbytes, bytes,
-                         sh.full + ps, pol);
+                bulk_g2s(dst, src, bytes, sh.full + ps, pol);
             } else {
                 const uint32_t lo = uint32_t(pg) * PB;
                 const uint32_t hi = min(lo + PB, st.total);
@@ -739,6 +763,30 @@ __device__ __forceinline__ bool load8x(const XSrc& x, int e0, float* v, uint32_t
     load8_bf16(x.b + e0, v);
     return true;
 }
+// four elements from element e0 on (e0 a multiple of 4); false when a tagged element does not yet
+// carry this step's tag
+__device__ __forceinline__ bool load4x(const XSrc& x, int e0, float* v, uint32_t tag) {
+    if (x.t) {
+        uint64_t w0, w1, w2, w3;
+        ld_tag2(x.t + e0, w0, w1);
+        ld_tag2(x.t + e0 + 2, w2, w3);
+        v[0] = tag_val(w0); v[1] = tag_val(w1); v[2] = tag_val(w2); v[3] = tag_val(w3);
+        return tag_of(w0) == tag && tag_of(w1) == tag && tag_of(w2) == tag && tag_of(w3) == tag;
+    }
+    if (x.h) {
+        uint32_t w[4];
+        asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(x.h + e0));
+        const uint32_t ht = htag(tag);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(w[e] & ~7u);
+        return (((w[0] ^ ht) | (w[1] ^ ht) | (w[2] ^ ht) | (w[3] ^ ht)) & 7u) == 0;
+    }
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(x.b + e0));
+    v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+    return true;
+}
+
 // the step's input token of sequence b: from the host, or in a chained multi-step call the
 // previous step's greedy token in device memory -- clamped to the vocabulary, since a step that
 // failed may have left no token (its recorded error is what the host then reports)
@@ -755,7 +803,7 @@ struct RSrc {
 
 // The input vector of a matvec tile (sequence b) into this warp's registers: its segment g of the
 // row length, RMS-normalised where the operator has a norm.  Rows up to the shared buffer's length
-// take their input cooperatively: thread t polls the 8-element chunks t, t + 512, ... into shared
+// take their input cooperatively: thread t polls the 4-element pieces t, t + 512, ... into shared
 // memory with one sum of squares per warp; after the CTA-wide arrival every warp adds the 16 sums
 // in warp order (the same scale everywhere) and takes its segment.  Longer rows (the MLP down
 // projection's input) are polled by each warp for its own segment, straight into registers.  In
@@ -764,25 +812,6 @@ struct RSrc {
 // (the instruction sequence is the same in all warps); xfree keeps a warp from overwriting a
 // buffer another warp still reads: the shared input until every warp has taken its segment, a
 // residual buffer (there are two, alternating) until every warp has finished the tile before.
-// Residual word of tile row `tid` into res[tid] (tid < nres): true once it is there.
-__device__ __forceinline__ bool poll_res(const Params& p, const RSrc& rs, int tid, int nres, float* res, bool& rdone) {
-    if (!rdone) {
-        if (tid >= nres) {
-            rdone = true;
-        } else if (rs.b) {
-            res[tid] = bf16f(rs.b[tid]);
-            rdone = true;
-        } else {
-            const uint64_t w = ld_tag(rs.t + tid);
-            if (tag_of(w) == p.tag) {
-                res[tid] = tag_val(w);
-                rdone = true;
-            }
-        }
-    }
-    return rdone;
-}
-
 __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uint16_t* gain, const RSrc& rs, int nres,
                            float (&xr)[8 * kCpl], float*& res, int pc) {
     const Params& p = c.p;
@@ -793,25 +822,32 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
     const int nch = min(m.segch, m.chunks - cg0);   // chunks of this warp's segment (the last may be short)
     if (c.xphase > 0 && !wait_bar(p, c.sh, c.sh.xfree, (c.xphase - 1u) & 1u, ROLE_CONSUMER, pc)) return false;
     res = c.sh.res + (c.xphase & 1u) * kResBuf;
-    bool rdone = false;
+    // the residual word of tile row tid: its load is issued before the input poll, so the two round
+    // trips overlap (the residual was produced an operator earlier: it is almost always ready)
+    const bool rmine = tid < nres;
+    uint64_t rw = 0;
+    float rb = 0.f;
+    if (rmine) {
+        if (rs.b) rb = bf16f(rs.b[tid]);
+        else rw = ld_tag(rs.t + tid);
+    }
     Spin sp;
     if (!m.direct) {
         float ss = 0.f;
-        for (int base = 0; base < m.chunks; base += kConsumerThreads) {   // warp-uniform trip count
-            const int ch = base + tid;
-            const bool valid = ch < m.chunks;
-            float v[8];
+        const int quads = m.K / 4;
+        for (int base = 0; base < quads; base += kConsumerThreads) {   // warp-uniform trip count
+            const int qd = base + tid;
+            const bool valid = qd < quads;
+            float v[4];
             while (true) {
-                bool ok = valid ? load8x(src, ch * 8, v, p.tag) : true;
-                if (base == 0) ok &= poll_res(p, rs, tid, nres, res, rdone);
+                const bool ok = valid ? load4x(src, qd * 4, v, p.tag) : true;
                 if (__all_sync(0xFFFFFFFFu, ok)) break;
                 if (!spin_more(c, sp, pc)) return false;
             }
             if (valid) {
-                *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8) = make_float4(v[0], v[1], v[2], v[3]);
-                *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                *reinterpret_cast<float4*>(c.sh.xbuf + qd * 4) = make_float4(v[0], v[1], v[2], v[3]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+                for (int e = 0; e < 4; ++e) ss = fmaf(v[e], v[e], ss);
             }
         }
         if (gain) {
@@ -820,7 +856,7 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
         }
     } else {
         while (true) {
-            bool ok = poll_res(p, rs, tid, nres, res, rdone);
+            bool ok = true;
 #pragma unroll
             for (int i = 0; i < kCpl; ++i) {
                 const int ch = c.lane + 32 * i;
@@ -835,6 +871,7 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
             if (!spin_more(c, sp, pc)) return false;
         }
     }
+    if (rmine) res[tid] = rs.b ? rb : (tag_of(rw) == p.tag ? tag_val(rw) : poll1(p, c.sh, rs.t + tid, pc));
     __syncwarp();
     if (c.lane == 0) mbar_arrive(c.sh.xfull);
     if (!wait_bar(p, c.sh, c.sh.xfull, c.xphase & 1u, ROLE_CONSUMER, pc)) return false;
