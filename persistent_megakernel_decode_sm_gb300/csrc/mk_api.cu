@@ -21,7 +21,7 @@
 #include "mk_internal.h"
 
 namespace mk {
-const void* megakernel_fn();
+const void* megakernel_fn(int cpl);
 cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st);
 }  // namespace mk
 
@@ -226,18 +226,21 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     if (hpg * g.attn_chunk > xbuf)
         return fail(MK_ERR_ARG, "attn_chunk %d: the scores of %d heads do not fit %d floats", g.attn_chunk, hpg, xbuf);
     // matvec shapes: whole rows per page, segments per row (a property of the row length only)
+    // chunks per lane: 2 when every row fits 16 segments of 64 chunks, else 4
+    const int kmax = std::max(H, std::max(qd, c.ffn));
+    const int cpl = (kmax / 8 + kMaxSeg - 1) / kMaxSeg <= 64 ? 2 : kMaxCpl;
     MvShape mv[OP_COUNT] = {};
     int comb_stride = 1;
     for (int op : {int(OP_QKV), int(OP_OPROJ), int(OP_UPGATE), int(OP_DOWN), int(OP_LMHEAD)}) {
         const int K = op == OP_OPROJ ? qd : (op == OP_DOWN ? c.ffn : H);
-        mv[op] = mv_shape(K, g.page_bytes, xbuf);
+        mv[op] = mv_shape(K, cpl, g.page_bytes, xbuf);
         if (mv[op].rpp < 1)
             return fail(MK_ERR_CAPACITY, "a %d-byte page holds no %d-element row", g.page_bytes, K);
-        if (mv[op].segch > 32 * kCpl)
+        if (mv[op].segch > 32 * cpl)
             return fail(MK_ERR_ARG, "matvec row length %d cannot be cut into %d segments", K, kMaxSeg);
         comb_stride = std::max(comb_stride, mv[op].rpp * mv[op].G);   // (row, segment) units of a page
     }
-    const void* fn = megakernel_fn();
+    const void* fn = megakernel_fn(cpl);
     int asf = hpg * g.n_chunk;
     asf = (asf + 3) & ~3;
     const int qrf = (hpg * d + 3) & ~3;

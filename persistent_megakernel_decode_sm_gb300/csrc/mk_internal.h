@@ -45,7 +45,7 @@ constexpr int kMaxLayersSmem = 40;   // layer pointer table cached in shared mem
 constexpr int kDone = 64;            // completion records the publisher may lag behind
 constexpr int kTraceWords = 8;       // trace stamps per instruction
 constexpr unsigned kPollBackoffNs = 128;   // pause between two polling rounds of tagged data
-constexpr int kCpl = 4;              // 16-byte chunks a lane holds of its row segment (at most)
+constexpr int kMaxCpl = 4;           // 16-byte chunks a lane holds of its row segment (at most)
 constexpr int kMaxSeg = 16;          // row segments of a matvec (a power of two dividing the warp count)
 constexpr int kDirectMinK = 4097;    // rows this long take their input per warp, not through the shared buffer
 constexpr int kResBuf = 64;          // residual words of a tile's rows staged in shared memory (per buffer)
@@ -124,9 +124,11 @@ struct LayerPtrs {
 
 // Matvec shape per opcode, resolved at bind.  A row of K elements is cut into G segments of
 // segch 16-byte chunks (the last one may be shorter); warp w always computes segment w mod G of
-// every row, holding that segment of the input vector in registers (at most kCpl chunks per lane).
-// G is the smallest power of two that keeps a segment within 32 * kCpl chunks: a property of K
-// alone, so the arithmetic of a row never depends on the tiling or the SM count.  Pages hold whole
+// every row, holding that segment of the input vector in registers (at most cpl chunks per lane;
+// the kernel is built for cpl 2 and 4, and a model takes the smallest that holds its longest row in
+// at most kMaxSeg segments).  G is the smallest power of two that keeps a segment within 32 * cpl
+// chunks: a property of K and cpl alone, so the arithmetic of a row never depends on the tiling or
+// the SM count.  Pages hold whole
 // rows (rpp per page).
 struct MvShape {
     int32_t K, chunks;       // row length: elements, 16-byte chunks
@@ -137,13 +139,13 @@ struct MvShape {
     int32_t direct;          // 1: each warp polls its own input segment (no shared input buffer)
 };
 
-MK_HD inline MvShape mv_shape(int K, int page_bytes, int xbuf_floats) {
+MK_HD inline MvShape mv_shape(int K, int cpl, int page_bytes, int xbuf_floats) {
     MvShape m{};
     m.K = K;
     m.chunks = K / 8;
     m.G = 1;
     m.logG = 0;
-    while ((m.chunks + m.G - 1) / m.G > 32 * kCpl && m.G < kMaxSeg) { m.G *= 2; ++m.logG; }
+    while ((m.chunks + m.G - 1) / m.G > 32 * cpl && m.G < kMaxSeg) { m.G *= 2; ++m.logG; }
     m.segch = (m.chunks + m.G - 1) / m.G;
     m.rowbytes = uint32_t(K) * 2u;
     m.rpp = page_bytes / int(m.rowbytes);

@@ -176,6 +176,11 @@ __device__ __forceinline__ void cta_sync_divergent() { asm volatile("barrier.syn
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
 __device__ __forceinline__ uint16_t f2bf_rn(float f) {   // round to nearest even (finite inputs)
     uint32_t u = __float_as_uint(f);
@@ -812,8 +817,9 @@ struct RSrc {
 // (the instruction sequence is the same in all warps); xfree keeps a warp from overwriting a
 // buffer another warp still reads: the shared input until every warp has taken its segment, a
 // residual buffer (there are two, alternating) until every warp has finished the tile before.
+template <int CPL>
 __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uint16_t* gain, const RSrc& rs, int nres,
-                           float (&xr)[8 * kCpl], float*& res, int pc) {
+                           float (&xr)[8 * CPL], float*& res, int pc) {
     const Params& p = c.p;
     const MvShape& m = si.mv;
     const int tid = c.warp * 32 + c.lane;
@@ -858,7 +864,7 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
         while (true) {
             bool ok = true;
 #pragma unroll
-            for (int i = 0; i < kCpl; ++i) {
+            for (int i = 0; i < CPL; ++i) {
                 const int ch = c.lane + 32 * i;
                 if (ch < nch) {
                     ok &= load8x(src, (cg0 + ch) * 8, &xr[8 * i], p.tag);
@@ -884,7 +890,7 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
             scale = rsqrtf(tot / float(m.K) + p.rms_eps);
         }
 #pragma unroll
-        for (int i = 0; i < kCpl; ++i) {
+        for (int i = 0; i < CPL; ++i) {
             const int ch = c.lane + 32 * i;
             float* x = &xr[8 * i];
             if (ch < nch) {
@@ -997,6 +1003,7 @@ __device__ void group_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, u
 // streams: a warp waits only for the pages of its current group and gives them back when done with
 // them, so a tile may be far larger than the page ring.  At batch > 1 every sequence reads every
 // page: the tile's pages are held until it is done.
+template <int CPL>
 __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     const Params& p = c.p;
     const int op = si.w[W_OP], l = si.w[W_LAYER], a0 = si.w[W_A0];
@@ -1009,8 +1016,9 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     const int npg = si.n_pages;
     const bool stream = p.B == 1;
     if (!stream && !wait_pages(c, si, pc)) return false;
-    float xr[8 * kCpl];
-    const size_t lane_off = size_t(g * m.segch + c.lane) * 16u;   // this lane's first chunk within a row
+    float xr[8 * CPL];
+    const uint32_t lane_off = uint32_t(g * m.segch + c.lane) * 16u;   // this lane's first chunk within a row
+    const uint32_t ring_base = smem_u32(c.sh.ring);
     // this lane's partial word within a unit: lane 0 the first sum (word 0), lane 16 the second
     // (gate/up: word 1 of the same unit; otherwise word 0 of the second page's unit)
     const int pword = (pair && c.lane == 16) ? 1 : 0;
@@ -1041,7 +1049,7 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
             default: gain = p.final_norm; src.t = p.x_out + (size_t(p.L - 1) * p.B + b) * p.H; break;
         }
         float* res;
-        if (!load_input(c, si, src, gain, rs, nres, xr, res, pc)) return false;
+        if (!load_input<CPL>(c, si, src, gain, rs, nres, xr, res, pc)) return false;
         if (b == 0 && c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
         uint32_t slot = uint32_t(si.first_slot), ph = uint32_t(si.first_phase);
         for (int k = 0; 2 * k < npg; ++k) {
@@ -1064,28 +1072,32 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
             }
             {
                 const int u0 = n0 << lg, u1 = n1 << lg;
-                const uint8_t* base0 = c.sh.ring + (size_t(slot) << p.page_shift) + lane_off;
-                const uint8_t* base1 = c.sh.ring + (size_t(slot1) << p.page_shift) + lane_off;
+                const uint32_t base0 = ring_base + (slot << p.page_shift) + lane_off;
+                const uint32_t base1 = ring_base + (slot1 << p.page_shift) + lane_off;
                 // partial word this lane writes: lane 0 -> (slot, unit), lane 16 -> (slot1 or slot, unit)
                 float* pbase = c.sh.comb + (size_t((c.lane == 16 && !pair) ? slot1 : slot) * p.comb_stride) * 2 + pword;
                 const bool writer = (c.lane & 15) == 0;
                 for (int j = c.warp; j < max(u0, u1); j += kNumConsumerWarps) {   // warp-uniform
-                    const int r = j >> lg;
+                    const uint32_t roff = uint32_t(j >> lg) * rowbytes;
                     const bool h0 = j < u0, h1 = j < u1;
-                    const uint8_t* w0 = base0 + size_t(r) * rowbytes;
-                    const uint8_t* w1 = base1 + size_t(r) * rowbytes;
-                    float a[kCpl], e[kCpl];
+                    float a[CPL], e[CPL];
 #pragma unroll
-                    for (int i = 0; i < kCpl; ++i) {
+                    for (int i = 0; i < CPL; ++i) {
                         a[i] = 0.f;
                         e[i] = 0.f;
                         if (c.lane + 32 * i < nch) {
-                            if (h0) a[i] = dot8(*reinterpret_cast<const uint4*>(w0 + i * 512), &xr[8 * i], 0.f);
-                            if (h1) e[i] = dot8(*reinterpret_cast<const uint4*>(w1 + i * 512), &xr[8 * i], 0.f);
+                            if (h0) a[i] = dot8(lds128(base0 + roff + i * 512), &xr[8 * i], 0.f);
+                            if (h1) e[i] = dot8(lds128(base1 + roff + i * 512), &xr[8 * i], 0.f);
                         }
                     }
-                    const float s0 = (a[0] + a[1]) + (a[2] + a[3]);
-                    const float s1 = (e[0] + e[1]) + (e[2] + e[3]);
+                    float s0 = a[0], s1 = e[0];
+                    if (CPL == 2) {
+                        s0 += a[CPL - 1];
+                        s1 += e[CPL - 1];
+                    } else {
+                        s0 = (a[0] + a[1 % CPL]) + (a[2 % CPL] + a[3 % CPL]);
+                        s1 = (e[0] + e[1 % CPL]) + (e[2 % CPL] + e[3 % CPL]);
+                    }
                     // one butterfly for both sums: the first lands in lanes 0-15, the second in 16-31
                     const bool hi = c.lane & 16;
                     float v = (hi ? s1 : s0) + __shfl_xor_sync(0xFFFFFFFFu, hi ? s0 : s1, 16);
@@ -1436,6 +1448,7 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
     return true;
 }
 
+template <int CPL>
 __device__ void consumer_warp(const Params& p, const Shared& sh) {
     Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u};
     CounterCache cc{-1, -1};
@@ -1467,7 +1480,7 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
             switch (op) {
                 case OP_ATTN: good = attn_tile(c, si, pc); break;
                 case OP_ARGMAX: good = argmax_tile(c, si, pc); break;
-                default: good = matvec_tile(c, si, pc); break;
+                default: good = matvec_tile<CPL>(c, si, pc); break;
             }
             if (!good) break;
             if (threadIdx.x == 0) stamp(p, pc, 3);
@@ -1481,6 +1494,7 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
     }
 }
 
+template <int CPL>
 __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Shared sh = carve(smem, p);
@@ -1511,7 +1525,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
     if (threadIdx.x == 0) stamp(p, 0, 5);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < kNumConsumerWarps) consumer_warp(p, sh);
+    if (warp < kNumConsumerWarps) consumer_warp<CPL>(p, sh);
     else if (warp == kLoaderWarp) { if (lane == 0) loader(p, sh); }
     else if (lane == 0) publisher(p, sh);
     cta_sync_divergent();
@@ -1528,7 +1542,10 @@ __global__ void rope_table_kernel(float2* out, int max_seq, int d, double theta)
     }
 }
 
-const void* megakernel_fn() { return reinterpret_cast<const void*>(&megakernel); }
+// CPL: 16-byte chunks a lane holds of its row segment (2 or 4)
+const void* megakernel_fn(int cpl) {
+    return cpl == 2 ? reinterpret_cast<const void*>(&megakernel<2>) : reinterpret_cast<const void*>(&megakernel<kMaxCpl>);
+}
 
 cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st) {
     const int n = max_seq * (d / 2);

@@ -20,14 +20,20 @@ from workload import WORKLOADS, get_workload
 PB = 32768          # default page bytes
 N_PAGES = 6         # pages the 1B / 8B configurations get from the 227 KB of shared memory
 WARPS = 16          # consumer warps
-CPL = 4             # 16-byte chunks a lane holds of its segment, at most
 MAX_SEG = 16
 
 
-def segments(K):
-    """Segments per row: the smallest power of two keeping a segment within 32 * CPL chunks."""
+def cpl_of(cfg):
+    """16-byte chunks a lane holds of its segment: 2 when the longest row fits 16 segments of 64
+    chunks, else 4."""
+    kmax = max(cfg.hidden, cfg.q_dim, cfg.ffn)
+    return 2 if -(-(kmax // 8) // MAX_SEG) <= 64 else 4
+
+
+def segments(K, cpl):
+    """Segments per row: the smallest power of two keeping a segment within 32 * cpl chunks."""
     chunks, G = K // 8, 1
-    while -(-chunks // G) > 32 * CPL and G < MAX_SEG:
+    while -(-chunks // G) > 32 * cpl and G < MAX_SEG:
         G *= 2
     return G
 
@@ -63,17 +69,18 @@ def test_batch1_groups_cover_every_unit_once(name, S):
     tiles, _, _ = sr.enumerate_tiles(cfg, o, S)
     K = {sr.QKV: cfg.hidden, sr.OPROJ: cfg.q_dim, sr.UPGATE: cfg.hidden, sr.DOWN: cfg.ffn,
          sr.LMHEAD: cfg.hidden}
-    comb_stride = max((PB // (2 * k)) * segments(k) for k in K.values())
+    cpl = cpl_of(cfg)
+    comb_stride = max((PB // (2 * k)) * segments(k, cpl) for k in K.values())
     seen = 0
     for t in tiles:
         if t.op not in K:
             continue
         k_len = K[t.op]
-        G = segments(k_len)
+        G = segments(k_len, cpl)
         lg = G.bit_length() - 1
         chunks = k_len // 8
         segch = -(-chunks // G)
-        assert segch <= 32 * CPL and WARPS % G == 0
+        assert segch <= 32 * cpl and WARPS % G == 0
         done = {}
         pages_seen = 0
         for pages in tile_groups(t.op, t.a1, k_len):
@@ -97,5 +104,9 @@ def test_batch1_groups_cover_every_unit_once(name, S):
     assert bind_rule_pages(cfg, sr.attn_chunk(cfg, o, S)) <= N_PAGES
 
 
-def test_segments_depend_on_the_row_length_only():
-    assert [segments(k) for k in (256, 688, 1024, 2048, 4096, 8192, 14336, 16384)] == [1, 1, 1, 2, 4, 8, 16, 16]
+def test_segments_depend_on_the_row_length_and_configuration_only():
+    Ks = (256, 688, 1024, 2048, 4096, 8192, 14336, 16384)
+    assert [segments(k, 2) for k in Ks[:6]] == [1, 2, 2, 4, 8, 16]
+    assert [segments(k, 4) for k in Ks] == [1, 1, 1, 2, 4, 8, 16, 16]
+    assert {w: cpl_of(get_workload(w).cfg) for w in WORKLOADS} == {
+        "tiny": 2, "llama1b_ctx512": 2, "llama1b_ctx8192": 2, "llama1b_batch8": 2, "llama8b_ctx2048": 4}
