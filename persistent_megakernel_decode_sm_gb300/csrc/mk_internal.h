@@ -243,8 +243,8 @@ MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qr
     m.qwin = take(2u * kQWin * kWords * 4u, 16);
     m.layers = take(uint32_t(sizeof(LayerPtrs)) * kMaxLayersSmem, 16);
     m.bars = take(8u * (2u + 2u * uint32_t(n_pages) + 2u * kSlots + kDone + 3u), 8);  // qfull, full, empty, ins, done, cbar, xfull, xfree
-    m.comb = take(4u * 2u * uint32_t(n_pages) * uint32_t(comb_stride), 16);   // segment partials per (page slot, unit)
-    m.combcnt = take(4u * uint32_t(n_pages) * uint32_t(comb_stride), 16);    // arrivals per (page slot, row)
+    m.comb = take(4u * 4u * uint32_t(n_pages) * uint32_t(comb_stride), 16);   // partials per (page slot, phase, unit)
+    m.combcnt = take(4u * 2u * uint32_t(n_pages), 16);                        // arrivals per (page slot, phase)
     m.pubinfo = take(4u * kDone * 8u, 16);            // completion words of in-flight instructions
     m.red = take(4u * 64u, 16);                     // argmax scratch [0..31]; abort flag [32], published count [33],
                                                     // stream bytes the loader has issued [34..35] (u64),

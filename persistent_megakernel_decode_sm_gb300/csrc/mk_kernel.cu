@@ -233,8 +233,8 @@ struct Shared {
     uint64_t* xfree;   // shared input taken by every warp (16 arrivals)
     float* xbuf;       // [xbuf_floats] shared matvec input
     float* res;        // [2][kResBuf] residual words of a tile's rows
-    float* comb;       // [n_pages][comb_stride][2] row-segment partials
-    int* combcnt;      // [n_pages][comb_stride] segment arrivals per row
+    float* comb;       // [n_pages][2 phases][comb_stride][2] row-segment partials
+    int* combcnt;      // [n_pages][2 phases] arrivals of the warps on a page group
     int* pubinfo;      // [kDone][8]: opcode, #completions, (counter, delta) x 2
     float* red;        // [32] argmax scratch
     float2* lmbest;    // [kNumConsumerWarps][kMaxBatch] LM-head running (max, index) of the CTA's tiles
@@ -955,14 +955,14 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
 // same order whichever warp runs this, so the result does not depend on timing or SM count).
 // Page 0 holds tile rows [r0, r0 + n0), page 1 rows [r1, r1 + n1); for gate/up both pages hold
 // the same n0 rows (gate sums in word 0 of a unit's partial, up sums in word 1).
-__device__ void group_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, uint32_t slot, uint32_t slot1, int r0,
-                               int n0, int r1, int n1, const float* res) {
+__device__ void group_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, uint32_t slot, uint32_t slot1,
+                               uint32_t par, uint32_t par1, int r0, int n0, int r1, int n1, const float* res) {
     const Params& p = c.p;
     const int G = si.mv.G, lg = si.mv.logG;
     const bool pair = si.inter != 0;
     const int nrows = pair ? n0 : n0 + n1;
-    const float* cb0 = c.sh.comb + size_t(slot) * p.comb_stride * 2;
-    const float* cb1 = c.sh.comb + size_t(slot1) * p.comb_stride * 2;
+    const float* cb0 = c.sh.comb + (size_t(slot) * 2 + par) * p.comb_stride * 2;
+    const float* cb1 = c.sh.comb + (size_t(slot1) * 2 + par1) * p.comb_stride * 2;
     float bv = -INFINITY;
     int bi = 0x7FFFFFFF;
     for (int i = c.lane; i < nrows; i += 32) {
@@ -1074,8 +1074,10 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 const int u0 = n0 << lg, u1 = n1 << lg;
                 const uint32_t base0 = ring_base + (slot << p.page_shift) + lane_off;
                 const uint32_t base1 = ring_base + (slot1 << p.page_shift) + lane_off;
-                // partial word this lane writes: lane 0 -> (slot, unit), lane 16 -> (slot1 or slot, unit)
-                float* pbase = c.sh.comb + (size_t((c.lane == 16 && !pair) ? slot1 : slot) * p.comb_stride) * 2 + pword;
+                // partial word this lane writes: lane 0 -> (slot, unit), lane 16 -> (slot1 or slot, unit);
+                // the partial areas alternate with the page slot's phase (see below)
+                const bool second = c.lane == 16 && !pair;   // this lane writes the second page's units
+                float* pbase = c.sh.comb + (size_t(second ? slot1 : slot) * 2 + ((second ? ph1 : ph) & 1u)) * p.comb_stride * 2 + pword;
                 const bool writer = (c.lane & 15) == 0;
                 for (int j = c.warp; j < max(u0, u1); j += kNumConsumerWarps) {   // warp-uniform
                     const uint32_t roff = uint32_t(j >> lg) * rowbytes;
@@ -1106,27 +1108,34 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                     if (writer && (hi ? h1 : h0)) pbase[size_t(j) * 2] = v;
                 }
             }
-            // every warp arrives on the group's counter; the last one writes the group's rows
-            __syncwarp();
-            int last = 0;
-            if (c.lane == 0) {
-                __threadfence_block();
-                last = atomicAdd(c.sh.combcnt + slot, 1) == kNumConsumerWarps - 1;
-                if (last) __threadfence_block();
-            }
-            last = __shfl_sync(0xFFFFFFFFu, last, 0);
-            if (last) {
-                __syncwarp();
-                group_epilogue(c, si, pc, b, slot, slot1, r0, n0, r1, n1, res);
-                __syncwarp();
-                if (c.lane == 0) c.sh.combcnt[slot] = 0;   // (seen by the slot's next group through the ring's mbarriers)
-            }
-            if (stream) {   // this group's pages are done for this warp
+            // The group's pages are done for this warp: give them back before the group's rows are
+            // written (the rows come from the partial area, not from the pages).  The partial
+            // area and counter of a page slot alternate with its phase: a slot's next use (the
+            // other phase) may start while the last warp still writes this group's rows, and the
+            // use after it (this phase again) cannot start before that warp has given the slot
+            // back once more -- which it does only after these rows.
+            if (stream) {
                 __syncwarp();
                 if (c.lane == 0) {
                     mbar_arrive(c.sh.empty + slot);
                     if (two) mbar_arrive(c.sh.empty + slot1);
                 }
+            }
+            // every warp arrives on the group's counter; the last one writes the group's rows
+            __syncwarp();
+            int* cnt = c.sh.combcnt + slot * 2 + (ph & 1u);
+            int last = 0;
+            if (c.lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(cnt, 1) == kNumConsumerWarps - 1;
+                if (last) __threadfence_block();
+            }
+            last = __shfl_sync(0xFFFFFFFFu, last, 0);
+            if (last) {
+                __syncwarp();
+                group_epilogue(c, si, pc, b, slot, slot1, ph & 1u, ph1 & 1u, r0, n0, r1, n1, res);
+                __syncwarp();
+                if (c.lane == 0) *cnt = 0;
             }
             if (two) {
                 slot = slot1 + 1u == NP ? 0u : slot1 + 1u;
@@ -1518,7 +1527,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
         *sh.issued = 0ull;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int i = threadIdx.x; i < p.n_pages * p.comb_stride; i += blockDim.x) sh.combcnt[i] = 0;
+    for (int i = threadIdx.x; i < 2 * p.n_pages; i += blockDim.x) sh.combcnt[i] = 0;
     for (int i = threadIdx.x; i < kNumConsumerWarps * kMaxBatch; i += blockDim.x)
         sh.lmbest[i] = make_float2(-INFINITY, __int_as_float(0x7FFFFFFF));
     for (int i = threadIdx.x; i < p.L; i += blockDim.x) sh.layers[i] = p.layers[i];
