@@ -1071,56 +1071,92 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 n1 = two ? min(rpp, R - r1) : 0;
             }
             {
-                const int u0 = n0 << lg, u1 = n1 << lg;
+                const int u0 = n0 << lg, u1 = n1 << lg, U = max(u0, u1);
                 const uint32_t base0 = ring_base + (slot << p.page_shift) + lane_off;
                 const uint32_t base1 = ring_base + (slot1 << p.page_shift) + lane_off;
-                // partial word this lane writes: lane 0 -> (slot, unit), lane 16 -> (slot1 or slot, unit);
-                // the partial areas alternate with the page slot's phase (see below)
-                const bool second = c.lane == 16 && !pair;   // this lane writes the second page's units
-                float* pbase = c.sh.comb + (size_t(second ? slot1 : slot) * 2 + ((second ? ph1 : ph) & 1u)) * p.comb_stride * 2 + pword;
-                const bool writer = (c.lane & 15) == 0;
-                for (int j = c.warp; j < max(u0, u1); j += kNumConsumerWarps) {   // warp-uniform
-                    const uint32_t roff = uint32_t(j >> lg) * rowbytes;
-                    const bool h0 = j < u0, h1 = j < u1;
-                    float a[CPL], e[CPL];
+                float* cb0 = c.sh.comb + (size_t(slot) * 2 + (ph & 1u)) * p.comb_stride * 2;
+                float* cb1 = pair ? cb0 + 1 : c.sh.comb + (size_t(slot1) * 2 + (ph1 & 1u)) * p.comb_stride * 2;
+                bool released = !stream;
+                // RPI row units per step: units j and j + 16 of each page (CPL 2), or unit j of each
+                // page (CPL 4).  A step loads its weights first; the pages go back to the loader as
+                // soon as the warp's last loads of the group have landed -- the math runs on registers
+                constexpr int RPI = CPL == 2 ? 4 : 2;
+                constexpr int JSTEP = (RPI / 2) * kNumConsumerWarps;
+                for (int jb = c.warp; jb < U; jb += JSTEP) {   // warp-uniform
+                    bool val[RPI];
+                    uint32_t addr[RPI];
 #pragma unroll
-                    for (int i = 0; i < CPL; ++i) {
-                        a[i] = 0.f;
-                        e[i] = 0.f;
-                        if (c.lane + 32 * i < nch) {
-                            if (h0) a[i] = dot8(lds128(base0 + roff + i * 512), &xr[8 * i], 0.f);
-                            if (h1) e[i] = dot8(lds128(base1 + roff + i * 512), &xr[8 * i], 0.f);
+                    for (int r = 0; r < RPI; ++r) {
+                        const int j = jb + (r % (RPI / 2)) * kNumConsumerWarps;
+                        const bool second = r >= RPI / 2;
+                        val[r] = j < (second ? u1 : u0);
+                        addr[r] = (second ? base1 : base0) + uint32_t(j >> lg) * rowbytes;
+                    }
+                    uint4 w[RPI][CPL];
+#pragma unroll
+                    for (int r = 0; r < RPI; ++r)
+#pragma unroll
+                        for (int i = 0; i < CPL; ++i)
+                            w[r][i] = (val[r] && c.lane + 32 * i < nch) ? lds128(addr[r] + i * 512) : make_uint4(0u, 0u, 0u, 0u);
+                    if (!released && jb + JSTEP >= U) {   // the warp's last loads of the group
+                        __syncwarp();
+                        if (c.lane == 0) {
+                            mbar_arrive(c.sh.empty + slot);
+                            if (two) mbar_arrive(c.sh.empty + slot1);
+                        }
+                        released = true;
+                    }
+                    float sr[RPI];
+#pragma unroll
+                    for (int r = 0; r < RPI; ++r) {
+                        float acc[CPL];
+#pragma unroll
+                        for (int i = 0; i < CPL; ++i) acc[i] = dot8(w[r][i], &xr[8 * i], 0.f);
+                        sr[r] = CPL == 2 ? acc[0] + acc[CPL - 1]
+                                         : (acc[0] + acc[1 % CPL]) + (acc[2 % CPL] + acc[3 % CPL]);
+                    }
+                    // transposed butterfly: every row's 32-lane sum, row r ending in lanes
+                    // [r * 32 / RPI, (r + 1) * 32 / RPI)
+                    const bool b4 = c.lane & 16;
+                    float v;
+                    if (RPI == 4) {
+                        const bool b3 = c.lane & 8;
+                        const float a0 = (b4 ? sr[2 % RPI] : sr[0]) + __shfl_xor_sync(0xFFFFFFFFu, b4 ? sr[0] : sr[2 % RPI], 16);
+                        const float a1 = (b4 ? sr[3 % RPI] : sr[1]) + __shfl_xor_sync(0xFFFFFFFFu, b4 ? sr[1] : sr[3 % RPI], 16);
+                        v = (b3 ? a1 : a0) + __shfl_xor_sync(0xFFFFFFFFu, b3 ? a0 : a1, 8);
+#pragma unroll
+                        for (int o = 4; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                    } else {
+                        v = (b4 ? sr[1] : sr[0]) + __shfl_xor_sync(0xFFFFFFFFu, b4 ? sr[0] : sr[1], 16);
+#pragma unroll
+                        for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                    }
+                    // the first lane of each row's lane group leaves the row's segment sum
+                    const int lr = c.lane / (32 / RPI);   // this lane's row of the step
+                    if ((c.lane & (32 / RPI - 1)) == 0) {
+                        bool ok = false;
+#pragma unroll
+                        for (int r = 0; r < RPI; ++r) ok |= (lr == r) && val[r];
+                        if (ok) {
+                            const int j = jb + (lr % (RPI / 2)) * kNumConsumerWarps;
+                            (lr >= RPI / 2 ? cb1 : cb0)[size_t(j) * 2] = v;
                         }
                     }
-                    float s0 = a[0], s1 = e[0];
-                    if (CPL == 2) {
-                        s0 += a[CPL - 1];
-                        s1 += e[CPL - 1];
-                    } else {
-                        s0 = (a[0] + a[1 % CPL]) + (a[2 % CPL] + a[3 % CPL]);
-                        s1 = (e[0] + e[1 % CPL]) + (e[2 % CPL] + e[3 % CPL]);
+                }
+                if (!released) {   // (a warp without units in this group)
+                    __syncwarp();
+                    if (c.lane == 0) {
+                        mbar_arrive(c.sh.empty + slot);
+                        if (two) mbar_arrive(c.sh.empty + slot1);
                     }
-                    // one butterfly for both sums: the first lands in lanes 0-15, the second in 16-31
-                    const bool hi = c.lane & 16;
-                    float v = (hi ? s1 : s0) + __shfl_xor_sync(0xFFFFFFFFu, hi ? s0 : s1, 16);
-#pragma unroll
-                    for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                    if (writer && (hi ? h1 : h0)) pbase[size_t(j) * 2] = v;
                 }
             }
-            // The group's pages are done for this warp: give them back before the group's rows are
-            // written (the rows come from the partial area, not from the pages).  The partial
-            // area and counter of a page slot alternate with its phase: a slot's next use (the
-            // other phase) may start while the last warp still writes this group's rows, and the
-            // use after it (this phase again) cannot start before that warp has given the slot
-            // back once more -- which it does only after these rows.
-            if (stream) {
-                __syncwarp();
-                if (c.lane == 0) {
-                    mbar_arrive(c.sh.empty + slot);
-                    if (two) mbar_arrive(c.sh.empty + slot1);
-                }
-            }
+            // The group's pages went back to the loader with the last loads above: the rows are
+            // written from the partial area, not from the pages.  The partial area and counter of
+            // a page slot alternate with its phase: a slot's next use (the other phase) may start
+            // while the last warp still writes this group's rows, and the use after it (this phase
+            // again) cannot start before that warp has given the slot back once more -- which it
+            // does only after these rows.
             // every warp arrives on the group's counter; the last one writes the group's rows
             __syncwarp();
             int* cnt = c.sh.combcnt + slot * 2 + (ph & 1u);
