@@ -226,9 +226,9 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     if (hpg * g.attn_chunk > xbuf)
         return fail(MK_ERR_ARG, "attn_chunk %d: the scores of %d heads do not fit %d floats", g.attn_chunk, hpg, xbuf);
     // matvec shapes: whole rows per page, segments per row (a property of the row length only)
-    // chunks per lane: 2 when every row fits 16 segments of 64 chunks, else 4
+    // chunks per lane: 4 when every row fits kMaxSeg segments of 128 chunks, else 8
     const int kmax = std::max(H, std::max(qd, c.ffn));
-    const int cpl = (kmax / 8 + kMaxSeg - 1) / kMaxSeg <= 64 ? 2 : kMaxCpl;
+    const int cpl = (kmax / 8 + kMaxSeg - 1) / kMaxSeg <= 128 ? 4 : kMaxCpl;
     MvShape mv[OP_COUNT] = {};
     int comb_stride = 1;
     for (int op : {int(OP_QKV), int(OP_OPROJ), int(OP_UPGATE), int(OP_DOWN), int(OP_LMHEAD)}) {

@@ -34,20 +34,21 @@ constexpr int kMaxK = 16384;       // longest matvec row (elements)
 constexpr int64_t kTileOverhead = 1024;
 
 // shared-memory layout of one CTA (after the page ring)
-constexpr int kNumConsumerWarps = 16;
+constexpr int kNumConsumerWarps = 8;
 constexpr int kConsumerThreads = kNumConsumerWarps * 32;
-constexpr int kLoaderWarp = 16;
-constexpr int kPublisherWarp = 17;
-constexpr int kThreads = 576;
+constexpr int kLoaderWarp = 8;
+constexpr int kPublisherWarp = 9;
+constexpr int kThreads = 320;
 constexpr int kSlots = 16;   // instruction slots in flight
 constexpr int kQWin = 16;    // instructions per queue-window buffer (two buffers, bulk-copied)
 constexpr int kMaxLayersSmem = 40;   // layer pointer table cached in shared memory
 constexpr int kDone = 64;            // completion records the publisher may lag behind
 constexpr int kTraceWords = 8;       // trace stamps per instruction
 constexpr unsigned kPollBackoffNs = 128;   // pause between two polling rounds of tagged data
-constexpr int kMaxCpl = 4;           // 16-byte chunks a lane holds of its row segment (at most)
-constexpr int kMaxSeg = 16;          // row segments of a matvec (a power of two dividing the warp count)
+constexpr int kMaxCpl = 8;           // 16-byte chunks a lane holds of its row segment (at most)
+constexpr int kMaxSeg = 8;           // row segments of a matvec (a power of two dividing the warp count)
 constexpr int kDirectMinK = 4097;    // rows this long take their input per warp, not through the shared buffer
+constexpr int kXChunks = 2;          // 8-element input chunks a consumer thread polls per round
 constexpr int kResBuf = 64;          // residual words of a tile's rows staged in shared memory (per buffer)
 constexpr int kL2Ahead = 8;          // pages of a matvec stream warmed into L2 ahead of the ring copies
 constexpr int kMinXBuf = 3072;       // floats of the shared input buffer at least (attention scores, combine)
@@ -125,7 +126,7 @@ struct LayerPtrs {
 // Matvec shape per opcode, resolved at bind.  A row of K elements is cut into G segments of
 // segch 16-byte chunks (the last one may be shorter); warp w always computes segment w mod G of
 // every row, holding that segment of the input vector in registers (at most cpl chunks per lane;
-// the kernel is built for cpl 2 and 4, and a model takes the smallest that holds its longest row in
+// the kernel is built for cpl 4 and 8, and a model takes the smallest that holds its longest row in
 // at most kMaxSeg segments).  G is the smallest power of two that keeps a segment within 32 * cpl
 // chunks: a property of K and cpl alone, so the arithmetic of a row never depends on the tiling or
 // the SM count.  Pages hold whole

@@ -808,8 +808,8 @@ struct RSrc {
 
 // The input vector of a matvec tile (sequence b) into this warp's registers: its segment g of the
 // row length, RMS-normalised where the operator has a norm.  Rows up to the shared buffer's length
-// take their input cooperatively: thread t polls the 4-element pieces t, t + 512, ... into shared
-// memory with one sum of squares per warp; after the CTA-wide arrival every warp adds the 16 sums
+// take their input cooperatively: thread t polls the 8-element chunks t, t + 256, ... into shared
+// memory, all of them before checking a tag, with one sum of squares per warp; after the CTA-wide arrival every warp adds the 16 sums
 // in warp order (the same scale everywhere) and takes its segment.  Longer rows (the MLP down
 // projection's input) are polled by each warp for its own segment, straight into registers.  In
 // the same polling round thread t < nres fetches the residual word of the tile's row t into the
@@ -839,21 +839,30 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
     }
     Spin sp;
     if (!m.direct) {
+        // every chunk of this thread is loaded before any tag is checked: one round trip for a row
+        // of up to 8 * kXChunks * 256 elements
         float ss = 0.f;
-        const int quads = m.K / 4;
-        for (int base = 0; base < quads; base += kConsumerThreads) {   // warp-uniform trip count
-            const int qd = base + tid;
-            const bool valid = qd < quads;
-            float v[4];
+        for (int base = 0; base < m.chunks; base += kXChunks * kConsumerThreads) {   // warp-uniform
+            float v[kXChunks][8];
             while (true) {
-                const bool ok = valid ? load4x(src, qd * 4, v, p.tag) : true;
+                bool ok = true;
+#pragma unroll
+                for (int q = 0; q < kXChunks; ++q) {
+                    const int ch = base + q * kConsumerThreads + tid;
+                    if (ch < m.chunks) ok &= load8x(src, ch * 8, v[q], p.tag);
+                }
                 if (__all_sync(0xFFFFFFFFu, ok)) break;
                 if (!spin_more(c, sp, pc)) return false;
             }
-            if (valid) {
-                *reinterpret_cast<float4*>(c.sh.xbuf + qd * 4) = make_float4(v[0], v[1], v[2], v[3]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ss = fmaf(v[e], v[e], ss);
+            for (int q = 0; q < kXChunks; ++q) {
+                const int ch = base + q * kConsumerThreads + tid;
+                if (ch < m.chunks) {
+                    *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8) = make_float4(v[q][0], v[q][1], v[q][2], v[q][3]);
+                    *reinterpret_cast<float4*>(c.sh.xbuf + ch * 8 + 4) = make_float4(v[q][4], v[q][5], v[q][6], v[q][7]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = fmaf(v[q][e], v[q][e], ss);
+                }
             }
         }
         if (gain) {
@@ -1077,10 +1086,10 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 float* cb0 = c.sh.comb + (size_t(slot) * 2 + (ph & 1u)) * p.comb_stride * 2;
                 float* cb1 = pair ? cb0 + 1 : c.sh.comb + (size_t(slot1) * 2 + (ph1 & 1u)) * p.comb_stride * 2;
                 bool released = !stream;
-                // RPI row units per step: units j and j + 16 of each page (CPL 2), or unit j of each
-                // page (CPL 4).  A step loads its weights first; the pages go back to the loader as
-                // soon as the warp's last loads of the group have landed -- the math runs on registers
-                constexpr int RPI = CPL == 2 ? 4 : 2;
+                // RPI row units per step: unit j of each page.  A step loads its weights first; the
+                // pages go back to the loader as soon as the warp's last loads of the group have
+                // landed -- the math runs on registers
+                constexpr int RPI = 2;
                 constexpr int JSTEP = (RPI / 2) * kNumConsumerWarps;
                 for (int jb = c.warp; jb < U; jb += JSTEP) {   // warp-uniform
                     bool val[RPI];
@@ -1112,8 +1121,13 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                         float acc[CPL];
 #pragma unroll
                         for (int i = 0; i < CPL; ++i) acc[i] = dot8(w[r][i], &xr[8 * i], 0.f);
-                        sr[r] = CPL == 2 ? acc[0] + acc[CPL - 1]
-                                         : (acc[0] + acc[1 % CPL]) + (acc[2 % CPL] + acc[3 % CPL]);
+                        float t = acc[0];
+#pragma unroll
+                        for (int h = 1; h < CPL; h *= 2)   // pairwise: ((a0 + a1) + (a2 + a3)) + ...
+#pragma unroll
+                            for (int i = 0; i + h < CPL; i += 2 * h) acc[i] += acc[i + h];
+                        t = acc[0];
+                        sr[r] = t;
                     }
                     // transposed butterfly: every row's 32-lane sum, row r ending in lanes
                     // [r * 32 / RPI, (r + 1) * 32 / RPI)
@@ -1587,9 +1601,9 @@ __global__ void rope_table_kernel(float2* out, int max_seq, int d, double theta)
     }
 }
 
-// CPL: 16-byte chunks a lane holds of its row segment (2 or 4)
+// CPL: 16-byte chunks a lane holds of its row segment (4 or 8)
 const void* megakernel_fn(int cpl) {
-    return cpl == 2 ? reinterpret_cast<const void*>(&megakernel<2>) : reinterpret_cast<const void*>(&megakernel<kMaxCpl>);
+    return cpl == 4 ? reinterpret_cast<const void*>(&megakernel<4>) : reinterpret_cast<const void*>(&megakernel<kMaxCpl>);
 }
 
 cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st) {

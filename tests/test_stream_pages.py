@@ -5,7 +5,7 @@ At batch 1 a matvec tile streams through the page ring: every page holds whole r
 the gate rows and the up rows of one row group in two consecutive pages), and the consumer warps
 walk the pages in groups of two, each warp waiting for the group's pages and giving them back
 when done.  Warp w computes segment w mod G of every row it touches (G, the segments per row,
-depends on the row length only) and units (row, segment) j = w, w + 16, ... of each page.  This
+depends on the row length only) and units (row, segment) j = w, w + 8, ... of each page.  This
 test restates that mapping for every batch-1 matvec tile of every workload (rows per tile from the
 scheduler's restatement) and checks that the pages cover the rows exactly once in order, that
 every (row, segment) unit is computed by exactly one warp that always holds the same segment, that
@@ -19,15 +19,15 @@ from workload import WORKLOADS, get_workload
 
 PB = 32768          # default page bytes
 N_PAGES = 6         # pages the 1B / 8B configurations get from the 227 KB of shared memory
-WARPS = 16          # consumer warps
-MAX_SEG = 16
+WARPS = 8           # consumer warps
+MAX_SEG = 8
 
 
 def cpl_of(cfg):
-    """16-byte chunks a lane holds of its segment: 2 when the longest row fits 16 segments of 64
-    chunks, else 4."""
+    """16-byte chunks a lane holds of its segment: 4 when the longest row fits 8 segments of 128
+    chunks, else 8."""
     kmax = max(cfg.hidden, cfg.q_dim, cfg.ffn)
-    return 2 if -(-(kmax // 8) // MAX_SEG) <= 64 else 4
+    return 4 if -(-(kmax // 8) // MAX_SEG) <= 128 else 8
 
 
 def segments(K, cpl):
@@ -106,7 +106,7 @@ def test_batch1_groups_cover_every_unit_once(name, S):
 
 def test_segments_depend_on_the_row_length_and_configuration_only():
     Ks = (256, 688, 1024, 2048, 4096, 8192, 14336, 16384)
-    assert [segments(k, 2) for k in Ks[:6]] == [1, 2, 2, 4, 8, 16]
-    assert [segments(k, 4) for k in Ks] == [1, 1, 1, 2, 4, 8, 16, 16]
+    assert [segments(k, 4) for k in Ks[:6]] == [1, 1, 1, 2, 4, 8]
+    assert [segments(k, 8) for k in Ks] == [1, 1, 1, 1, 2, 4, 8, 8]
     assert {w: cpl_of(get_workload(w).cfg) for w in WORKLOADS} == {
-        "tiny": 2, "llama1b_ctx512": 2, "llama1b_ctx8192": 2, "llama1b_batch8": 2, "llama8b_ctx2048": 4}
+        "tiny": 4, "llama1b_ctx512": 4, "llama1b_ctx8192": 4, "llama1b_batch8": 4, "llama8b_ctx2048": 8}
