@@ -1086,9 +1086,7 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 float* cb0 = c.sh.comb + (size_t(slot) * 2 + (ph & 1u)) * p.comb_stride * 2;
                 float* cb1 = pair ? cb0 + 1 : c.sh.comb + (size_t(slot1) * 2 + (ph1 & 1u)) * p.comb_stride * 2;
                 bool released = !stream;
-                // RPI row units per step: unit j of each page.  A step loads its weights first; the
-                // pages go back to the loader as soon as the warp's last loads of the group have
-                // landed -- the math runs on registers
+                // RPI row units per step: unit j of each page
                 constexpr int RPI = 2;
                 constexpr int JSTEP = (RPI / 2) * kNumConsumerWarps;
                 for (int jb = c.warp; jb < U; jb += JSTEP) {   // warp-uniform
@@ -1107,14 +1105,6 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
 #pragma unroll
                         for (int i = 0; i < CPL; ++i)
                             w[r][i] = (val[r] && c.lane + 32 * i < nch) ? lds128(addr[r] + i * 512) : make_uint4(0u, 0u, 0u, 0u);
-                    if (!released && jb + JSTEP >= U) {   // the warp's last loads of the group
-                        __syncwarp();
-                        if (c.lane == 0) {
-                            mbar_arrive(c.sh.empty + slot);
-                            if (two) mbar_arrive(c.sh.empty + slot1);
-                        }
-                        released = true;
-                    }
                     float sr[RPI];
 #pragma unroll
                     for (int r = 0; r < RPI; ++r) {
@@ -1128,6 +1118,19 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                             for (int i = 0; i + h < CPL; i += 2 * h) acc[i] += acc[i + h];
                         t = acc[0];
                         sr[r] = t;
+                    }
+                    // The group's pages go back to the loader once the warp's last step has consumed
+                    // every value it loaded from them (the dot products above): an arrival right
+                    // after the loads were issued let the loader's refill overwrite a page before
+                    // all of them had read it (measured: runs no longer bit-identical).  The
+                    // reduction, the partial sums and the rows need no page.
+                    if (!released && jb + JSTEP >= U) {
+                        __syncwarp();
+                        if (c.lane == 0) {
+                            mbar_arrive(c.sh.empty + slot);
+                            if (two) mbar_arrive(c.sh.empty + slot1);
+                        }
+                        released = true;
                     }
                     // transposed butterfly: every row's 32-lane sum, row r ending in lanes
                     // [r * 32 / RPI, (r + 1) * 32 / RPI)

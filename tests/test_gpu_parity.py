@@ -192,3 +192,18 @@ def test_decode_from_position_zero():
     kv = kv_agreement(s, [[0, 1, 2, 3]])
     assert kv["worst_in_steps"] <= 1.0 and kv["frac_equal"] > 0.97, kv
     dec.close()
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama1b_ctx512"])
+def test_repeated_runs_bit_identical(name):
+    # the same steps on fresh contexts, four times: logits and caches must not depend on timing
+    def run():
+        s = make_setup(name)
+        dec = mk.Decoder(mk.Schedule(s.cfg, mk.device_sm_count()), s.weights, s.kv)
+        out = _steps(dec, s, 3)
+        dec.close()
+        return out
+    ref = run()
+    for _ in range(3):
+        for a, b in zip(run(), ref):
+            assert torch.equal(a, b)
