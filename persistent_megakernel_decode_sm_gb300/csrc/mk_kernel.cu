@@ -1086,8 +1086,8 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 float* cb0 = c.sh.comb + (size_t(slot) * 2 + (ph & 1u)) * p.comb_stride * 2;
                 float* cb1 = pair ? cb0 + 1 : c.sh.comb + (size_t(slot1) * 2 + (ph1 & 1u)) * p.comb_stride * 2;
                 bool released = !stream;
-                // RPI row units per step: unit j of each page
-                constexpr int RPI = 2;
+                // RPI row units per step: units j and j + 8 of each page (CPL 4), or unit j of each page
+                constexpr int RPI = CPL == 4 ? 4 : 2;
                 constexpr int JSTEP = (RPI / 2) * kNumConsumerWarps;
                 for (int jb = c.warp; jb < U; jb += JSTEP) {   // warp-uniform
                     bool val[RPI];
