@@ -1,7 +1,7 @@
 """GPU parity of the megakernel against the CPU oracle on the larger configurations, through the
-C ABI (libmk.so): a long context (129 attention chunks per group, the combine over partials in
-L2), batch 8 with uneven KV lengths (tiles held whole in the page ring, one input vector per
-sequence), and the 8B shape (every matvec input cut into segments, untied LM head).
+C ABI (libmk.so): a long context (33 attention chunks of 256 positions per group, combined over
+partials in L2), batch 8 with uneven KV lengths (tiles held whole in the page ring, one input
+vector per sequence), and the 8B shape (8 chunks per lane, untied LM head).
 
 Tolerances as in test_gpu_parity: logits within max |error| <= 1e-2 * max |oracle logit| per
 sequence, the greedy token equal wherever the oracle's top-2 margin exceeds 0.05, appended K/V
@@ -35,6 +35,22 @@ def _run(name: str, steps: int):
 
 def test_llama1b_long_context_parity():
     _run("llama1b_ctx8192", steps=2)
+
+
+def test_llama1b_long_context_bit_identical_across_sm_counts():
+    # 33 attention chunks of 256 positions per group, combined in chunk order
+    outs = []
+    for S in (mk.device_sm_count(), 76):
+        s = make_setup("llama1b_ctx8192")
+        dec = mk.Decoder(mk.Schedule(s.cfg, S), s.weights, s.kv)
+        dec.step(s.tokens, s.pos)
+        outs.append((dec.logits.cpu().clone(), s.kv.k[:, :, :, s.pos[0]].cpu().clone(),
+                     s.kv.v[:, :, :, s.pos[0]].cpu().clone()))
+        dec.close()
+        del s, dec
+        torch.cuda.empty_cache()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
 
 
 def test_llama1b_batch8_parity():
