@@ -943,7 +943,7 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
             st_tag(p.x_attn + lb * p.H + row, r + s0, p.tag);
             break;
         }
-        case OP_UPGATE: st_htag(p.h + lb * p.F + row, s0 / (1.0f + expf(-s0)) * s1, htag(p.tag)); break;
+        case OP_UPGATE: st_htag(p.h + lb * p.F + row, __fdividef(s0, 1.0f + __expf(-s0)) * s1, htag(p.tag)); break;
         case OP_DOWN: {
             const float r = ru < kResBuf ? res[ru] : poll1(p, c.sh, p.x_attn + lb * p.H + row, pc);
             st_tag(p.x_out + lb * p.H + row, r + s0, p.tag);
@@ -959,24 +959,30 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
     }
 }
 
-// The rows of one page group, once every consumer warp has left its segment sums: run by the warp
-// that arrived last, one lane per row.  A row's G segment sums are added in segment order (the
-// same order whichever warp runs this, so the result does not depend on timing or SM count).
-// Page 0 holds tile rows [r0, r0 + n0), page 1 rows [r1, r1 + n1); for gate/up both pages hold
-// the same n0 rows (gate sums in word 0 of a unit's partial, up sums in word 1).
-__device__ void group_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, uint32_t slot, uint32_t slot1,
-                               uint32_t par, uint32_t par1, int r0, int n0, int r1, int n1, const float* res) {
+// A page group of a matvec tile: its pages' ring slots and phase parities, and the tile rows of
+// each page.
+struct GroupRef {
+    uint32_t slot, slot1, par, par1;
+    int r0, n0, r1, n1;
+};
+
+// The rows of one page group, once every consumer warp has left its segment sums, one lane per
+// row.  A row's G segment sums are added in segment order (the same order whichever warp runs
+// this, so the result does not depend on timing or SM count).  Page 0 holds tile rows
+// [r0, r0 + n0), page 1 rows [r1, r1 + n1); for gate/up both pages hold the same n0 rows (gate sums
+// in word 0 of a unit's partial, up sums in word 1).  The LM head keeps each lane's running
+// (max, lowest index) in bv / bi.
+__device__ void group_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, const GroupRef& gr, const float* res,
+                               float& bv, int& bi) {
     const Params& p = c.p;
     const int G = si.mv.G, lg = si.mv.logG;
     const bool pair = si.inter != 0;
-    const int nrows = pair ? n0 : n0 + n1;
-    const float* cb0 = c.sh.comb + (size_t(slot) * 2 + par) * p.comb_stride * 2;
-    const float* cb1 = c.sh.comb + (size_t(slot1) * 2 + par1) * p.comb_stride * 2;
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
+    const int nrows = pair ? gr.n0 : gr.n0 + gr.n1;
+    const float* cb0 = c.sh.comb + (size_t(gr.slot) * 2 + gr.par) * p.comb_stride * 2;
+    const float* cb1 = c.sh.comb + (size_t(gr.slot1) * 2 + gr.par1) * p.comb_stride * 2;
     for (int i = c.lane; i < nrows; i += 32) {
-        const bool second = !pair && i >= n0;
-        const int r = second ? i - n0 : i;
+        const bool second = !pair && i >= gr.n0;
+        const int r = second ? i - gr.n0 : i;
         const float* q = (second ? cb1 : cb0) + (size_t(r) << lg) * 2;
         float s0 = q[0], s1 = q[1];
 #pragma unroll 1
@@ -984,23 +990,35 @@ __device__ void group_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, u
             s0 += q[2 * k];
             s1 += q[2 * k + 1];
         }
-        mv_epilogue(c, si, pc, b, (second ? r1 : r0) + r, s0, s1, res, bv, bi);
+        mv_epilogue(c, si, pc, b, (second ? gr.r1 : gr.r0) + r, s0, s1, res, bv, bi);
     }
-    if (si.w[W_OP] == OP_LMHEAD) {   // the group's best, merged into this warp's running best
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
+}
+
+// Writes a page group's rows once all consumer warps have arrived on its counter (a bounded wait:
+// the group's other warps are at most a step behind), then resets the counter for the slot's
+// next use of this phase.  False when the CTA aborts or the wait runs out.
+__device__ bool finish_group(const Cw& c, const SlotInfo& si, int pc, int b, const GroupRef& gr, const float* res,
+                             float& bv, int& bi) {
+    volatile int* cnt = c.sh.combcnt + gr.slot * 2 + gr.par;
+    int ok = 1;
+    if (c.lane == 0 && *cnt != kNumConsumerWarps) {
+        const uint64_t t0 = globaltimer();
+        while (*cnt != kNumConsumerWarps) {
+            if (*reinterpret_cast<volatile int*>(c.sh.abort)) { ok = 0; break; }
+            if (globaltimer() - t0 > budget(c.p, ROLE_CONSUMER)) {
+                raise_error(c.p, c.sh, MK_ERR_TIMEOUT, ROLE_CONSUMER, pc, -1, uint32_t(*cnt), kNumConsumerWarps);
+                ok = 0;
+                break;
             }
         }
-        if (c.lane == 0) {
-            float2& run = c.sh.lmbest[c.warp * kMaxBatch + b];
-            if (bv > run.x || (bv == run.x && bi < __float_as_int(run.y))) run = make_float2(bv, __int_as_float(bi));
-        }
     }
+    __threadfence_block();
+    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+    __syncwarp();
+    group_epilogue(c, si, pc, b, gr, res, bv, bi);
+    __syncwarp();
+    if (c.lane == 0) *cnt = 0;   // (seen by the slot's next use of this phase through the ring's mbarriers)
+    return true;
 }
 
 // Matvec tile (QKV / O / gate-up / down / LM-head rows).  Pages hold whole rows; the tile is
@@ -1061,7 +1079,11 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
         if (!load_input<CPL>(c, si, src, gain, rs, nres, xr, res, pc)) return false;
         if (b == 0 && c.warp == 0 && c.lane == 0) stamp(p, pc, 6);
         uint32_t slot = uint32_t(si.first_slot), ph = uint32_t(si.first_phase);
-        for (int k = 0; 2 * k < npg; ++k) {
+        GroupRef prev{};
+        float bv = -INFINITY;   // LM head: the running (max, lowest index) of the rows this lane wrote
+        int bi = 0x7FFFFFFF;
+        const int ngroups = (npg + 1) / 2;
+        for (int k = 0; k < ngroups; ++k) {
             const bool two = 2 * k + 1 < npg;
             const uint32_t slot1 = slot + 1u == NP ? 0u : slot + 1u;
             const uint32_t ph1 = slot + 1u == NP ? ph ^ 1u : ph;
@@ -1168,28 +1190,24 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                     }
                 }
             }
-            // The group's pages went back to the loader with the last loads above: the rows are
-            // written from the partial area, not from the pages.  The partial area and counter of
-            // a page slot alternate with its phase: a slot's next use (the other phase) may start
-            // while the last warp still writes this group's rows, and the use after it (this phase
-            // again) cannot start before that warp has given the slot back once more -- which it
-            // does only after these rows.
-            // every warp arrives on the group's counter; the last one writes the group's rows
+            // The group's pages went back to the loader after the warp's dot products: the rows
+            // are written from the partial area, not from the pages.  The partial area and counter
+            // of a page slot alternate with its phase: a slot's next use (the other phase) may
+            // start before this group's rows are written, and the use after it (this phase again)
+            // cannot start before every warp -- the writing one included -- has given the slot
+            // back once more, which the writing warp does only after these rows.
+            // Every warp arrives on the group's counter.  The group's rows are written one group
+            // later by warp k mod 8: the writing rotates over the warps, so no warp carries it on
+            // every group (the warp that arrives last would, and so arrive last again).
             __syncwarp();
-            int* cnt = c.sh.combcnt + slot * 2 + (ph & 1u);
-            int last = 0;
             if (c.lane == 0) {
                 __threadfence_block();
-                last = atomicAdd(cnt, 1) == kNumConsumerWarps - 1;
-                if (last) __threadfence_block();
+                atomicAdd(c.sh.combcnt + slot * 2 + (ph & 1u), 1);
             }
-            last = __shfl_sync(0xFFFFFFFFu, last, 0);
-            if (last) {
-                __syncwarp();
-                group_epilogue(c, si, pc, b, slot, slot1, ph & 1u, ph1 & 1u, r0, n0, r1, n1, res);
-                __syncwarp();
-                if (c.lane == 0) *cnt = 0;
-            }
+            if (k >= 1 && ((k - 1) & (kNumConsumerWarps - 1)) == c.warp &&
+                !finish_group(c, si, pc, b, prev, res, bv, bi))
+                return false;
+            prev = GroupRef{slot, slot1, ph & 1u, ph1 & 1u, r0, n0, r1, n1};
             if (two) {
                 slot = slot1 + 1u == NP ? 0u : slot1 + 1u;
                 ph = slot1 + 1u == NP ? ph1 ^ 1u : ph1;
@@ -1198,10 +1216,25 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 ph = ph1;
             }
         }
-        if (op == OP_LMHEAD && c.lane == 0) {   // this warp's running best over the CTA's LM-head rows so far
-            const float2 run = c.sh.lmbest[c.warp * kMaxBatch + b];
-            p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * kNumConsumerWarps + c.warp] =
-                make_int4(__float_as_int(run.x), __float_as_int(run.y), int(p.epoch), 0);
+        if (ngroups >= 1 && ((ngroups - 1) & (kNumConsumerWarps - 1)) == c.warp &&
+            !finish_group(c, si, pc, b, prev, res, bv, bi))
+            return false;
+        if (op == OP_LMHEAD) {   // this warp's running best over the CTA's LM-head rows so far
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (c.lane == 0) {
+                float2& run = c.sh.lmbest[c.warp * kMaxBatch + b];
+                if (bv > run.x || (bv == run.x && bi < __float_as_int(run.y))) run = make_float2(bv, __int_as_float(bi));
+                p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * kNumConsumerWarps + c.warp] =
+                    make_int4(__float_as_int(run.x), __float_as_int(run.y), int(p.epoch), 0);
+            }
         }
         // batch > 1: the page slots' partials and counters serve the next sequence
         if (!stream && !cbar(c, pc)) return false;
