@@ -51,7 +51,6 @@ constexpr int kDirectMinK = 4097;    // rows this long take their input per warp
 constexpr int kXChunks = 2;          // 8-element input chunks a consumer thread polls per round
 constexpr int kResBuf = 64;          // residual words of a tile's rows staged in shared memory (per buffer)
 constexpr int kL2Ahead = 8;          // pages of a matvec stream warmed into L2 ahead of the ring copies
-constexpr uint32_t kL2NextBytes = 480u << 10;   // bytes of the next matvec instruction's stream warmed into L2
 constexpr int kMinXBuf = 3072;       // floats of the shared input buffer at least (attention scores, combine)
 constexpr int kAttnChunkTiles = 152; // default attention chunk: grown while a layer has more chunks
 

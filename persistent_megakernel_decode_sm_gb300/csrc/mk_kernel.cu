@@ -450,7 +450,6 @@ __device__ void loader(const Params& p, const Shared& sh) {
     int chunks_waited = 0;
     uint32_t page_seq = 0;                   // pages issued so far
     uint32_t cur_slot = 0, cur_phase = 0;    // ring slot and phase parity of the next page
-    int l2_next = 0;                         // instructions before this one have had their L2 warm-up
     for (int pc = 0; pc < p.Q; ++pc) {
         const int slot = pc % kSlots;
         const int chunk = pc / kQWin;
@@ -466,23 +465,6 @@ __device__ void loader(const Params& p, const Shared& sh) {
         if (pc % kQWin == kQWin - 1 && chunks_issued < n_chunks) {
             fence_proxy_async_smem();   // generic reads of this buffer before the async refill
             fetch_chunk(chunks_issued++);
-        }
-        // the next matvec instruction in the window: its weight stream (up to kL2NextBytes) is
-        // warmed into L2 now, so HBM keeps streaming while this SM's consumers wait on the
-        // dependencies in between (the QKV -> attention -> O chain in front of the MLP)
-        for (int j = max(pc + 1, l2_next); j < min(p.Q, (chunk + 1) * kQWin); ++j) {
-            const int32_t* wj = sh.qwin + ((chunk & 1) * kQWin + j % kQWin) * kWords;
-            if (!is_matvec(wj[W_OP])) continue;
-            uint32_t left = kL2NextBytes;
-#pragma unroll 1
-            for (int sgi = 0; sgi < 2; ++sgi) {
-                const uint8_t* src = word_ptr(wj + (sgi ? W_SRC1 : W_SRC0));
-                const uint32_t n = min(uint32_t(wj[sgi ? W_BYTES1 : W_BYTES0]), left);
-                for (uint32_t o = 0; o < n; o += PB) prefetch_l2(src + o, min(PB, n - o));
-                left -= n;
-            }
-            l2_next = j + 1;
-            break;
         }
         Stream st;
         const int e = stream_of(p, si.w, st);
