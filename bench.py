@@ -175,6 +175,26 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def oracle_step_timer(cfg, kv_len, seed, threads, steps, warmup):
     """Times whole oracle decode steps of the workload on the host; returns (us per token list, cores)."""
     import numpy as np  # noqa: F401
@@ -217,7 +237,8 @@ def run_reference(args, rank, world):
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": {"workload": WORKLOAD, "batch": 1, "kv_len": 512,
                                             "weights": "bf16", "kv": "bf16"},
-            "cpu_baseline": {"value": v, "unit": "us/token", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "us/token", "cores": cores, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": v, "unit": "us/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -351,9 +372,14 @@ def main():
     del w, kv
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
+        # the oracle as it stands: OpenMP over matvec rows on every host core (per-row sums in the
+        # same order), and single-threaded (one step)
         times, cores = oracle_step_timer(cfg, wl.kv_len[0], 0, os.cpu_count() or 1, args.cpu_steps, 1)
+        single, _ = oracle_step_timer(cfg, wl.kv_len[0], 0, 1, 1, 0)
         line["cpu_baseline"] = {"value": statistics.mean(times), "unit": "us/token", "cores": cores,
-                                "kind": "oracle",
+                                "kind": "oracle", "cpu_model": cpu_model(),
+                                "single_thread": {"value": statistics.mean(single), "unit": "us/token", "cores": 1,
+                                                  "sample": f"{len(single)} whole decode step of {args.workload}"},
                                 "sample": f"{len(times)} whole decode steps (+1 warm-up) of {args.workload}"}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -92,7 +92,10 @@ mk_status mk_build_schedule(const mk_model_cfg* cfg, int32_t sm_count, const mk_
                             mk_schedule** out);
 
 /* The queues: a read-only pointer to S*Q*32 int32 (row-major [S, Q, 32]) valid until the
- * schedule is freed.  Word layout of one instruction:
+ * schedule is freed.  The page's object table ("Inference MegaKernel", section "Hand-written
+ * whole-model MegaKernel") lists the instruction queue as an int32 tensor of shape [S, Q, 32]
+ * held in HBM for the life of the kernel; the word layout is this library's (the page gives none).
+ * Errors: MK_ERR_ARG on a null argument.  Word layout of one instruction:
  *   [0] opcode (0 END, 1 QKV, 2 ATTN, 4 OPROJ, 5 UPGATE, 6 DOWN, 7 LMHEAD, 8 ARGMAX; 3 is
  *       reserved and rejected)
  *   [1] layer (n_layers for LMHEAD / ARGMAX)   [2] sequence b (attention, argmax)
@@ -110,7 +113,12 @@ mk_status mk_schedule_queues(const mk_schedule* s, const int32_t** queues, int32
                              int32_t* queue_len);
 
 /* Per-step counter totals: total[c] = sum of the deltas published into counter c in one step
- * (read-only pointer to n uint32, valid until the schedule is freed). */
+ * (read-only pointer to n uint32, valid until the schedule is freed).  The page's object table
+ * lists global completion counters beside the queues; its interpreter waits until a counter has
+ * reached what an instruction needs and adds to the counters an instruction completes (section
+ * "Hand-written whole-model MegaKernel", pseudocode and object table).  With counters that keep
+ * growing across steps the wait target is epoch * total + need.  Errors: MK_ERR_ARG on a null
+ * argument. */
 mk_status mk_schedule_counters(const mk_schedule* s, const uint32_t** totals, int32_t* n_counters);
 
 /* The schedule's attention chunk (KV positions per split-K attention tile: the option, or the
@@ -123,7 +131,9 @@ mk_status mk_schedule_attn_chunk(const mk_schedule* s, int32_t* out);
 mk_status mk_schedule_patch(mk_schedule* s, int32_t sm, int32_t slot, int32_t word, int32_t value);
 
 /* Bytes of device scratch a context of this schedule needs (activations, attention partials,
- * LM-head partials, RoPE table, error word, output tokens).  0 if s is NULL. */
+ * LM-head partials, RoPE table, error word, output tokens) -- the activation objects the page's
+ * object table keeps in HBM for the resident execution (section "Hand-written whole-model
+ * MegaKernel").  The caller allocates them (mk_bind).  0 if s is NULL. */
 size_t mk_scratch_bytes(const mk_schedule* s);
 
 void mk_schedule_free(mk_schedule* s);
@@ -233,8 +243,12 @@ mk_status mk_set_sync(mk_ctx* c, int32_t mode);
  * contents. */
 mk_status mk_set_trace(mk_ctx* c, uint64_t* buf);
 
-/* One decode step, synchronous: tokens and pos are HOST arrays of `batch` int32; logits is a
- * DEVICE fp32 buffer [batch, vocab] (caller-owned) that receives the step's logits;
+/* One decode step, synchronous -- the step the page's megakernel runs as one resident execution
+ * per token (section "Hand-written whole-model MegaKernel": the whole decode step of the model
+ * in one launch, instead of about a hundred kernels; section "Why inference still has
+ * bubbles" for the launch and tail costs it removes).  tokens and pos are HOST arrays of `batch`
+ * int32; logits is a DEVICE fp32 buffer [batch, vocab] (caller-owned) that receives the step's
+ * logits;
  * next_tokens is a HOST array of `batch` int32 that receives the greedy (argmax, lowest index
  * on ties) next tokens.  Launches the resident grid once on the bound stream, then waits for it.
  * Errors: MK_ERR_ARG (token or pos out of range), MK_ERR_POISONED, MK_ERR_TIMEOUT,
@@ -296,8 +310,14 @@ mk_status mk_ctx_status(mk_ctx* c, int32_t* info);
 /* Number of SMs of the current CUDA device (the natural sm_count), or MK_ERR_CUDA. */
 mk_status mk_device_sm_count(int32_t* out);
 
+/* The message of the calling thread's last non-OK status (thread-local; empty if none).  A
+ * library convention with no counterpart on the page. */
 const char* mk_last_error(void);
 
+/* Ends a binding: waits for the bound stream, then frees the context's own device copies (queues,
+ * counter totals, layer table) and its pinned readback buffer.  The caller's weights, KV cache,
+ * counters and scratch are not touched (the page's objects live as long as the request that bound
+ * them; section "Hand-written whole-model MegaKernel", object table).  NULL is ignored. */
 void mk_unbind(mk_ctx* c);
 
 #ifdef __cplusplus

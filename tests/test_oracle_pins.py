@@ -339,3 +339,28 @@ def test_decode_batch_sequences_independent():
         lb, nb, kb, vb = _run(one, w, kvb, [toks[b]], [pos[b]])
         assert np.array_equal(lb[0], logits[b]) and nb[0] == nxt[b]
         assert np.array_equal(kb[0], k[b]) and np.array_equal(vb[0], v[b])
+
+
+def test_swiglu_step_tag_stays_inside_the_parity_tolerance(oracle32, oracle64):
+    """The megakernel stores the SwiGLU output in fp32 with its three lowest mantissa bits
+    replaced by a step tag (1..7).  Restated here on the oracle's own swiglu outputs: every tagged
+    value lies within 2^-20 (relative) of the untagged one, and the change it makes to a
+    down-projection row of the 1B shape (8192 inputs, weights ~N(0, 0.02)) is below 1e-5 of the
+    row's magnitude -- three orders of magnitude inside the parity tolerance of 1e-2 * max|logit|."""
+    rng = np.random.default_rng(5)
+    a = rng.normal(0, 2.0, 8192).astype(np.float32)
+    u = rng.normal(0, 2.0, 8192).astype(np.float32)
+    h = oracle32.swiglu(a, u).astype(np.float32)
+    bits = h.view(np.uint32)
+    for tag in range(1, 8):
+        tagged = ((bits & np.uint32(0xFFFFFFF8)) | np.uint32(tag)).view(np.float32)
+        rel = np.abs(tagged.astype(np.float64) - h) / np.maximum(np.abs(h.astype(np.float64)), 1e-30)
+        assert rel.max() < 2.0 ** -20
+        w = rng.normal(0, 0.02, (4, 8192)).astype(np.float32)
+        exact = w.astype(np.float64) @ h.astype(np.float64)
+        moved = w.astype(np.float64) @ tagged.astype(np.float64)
+        scale = np.abs(w.astype(np.float64)) @ np.abs(h.astype(np.float64))
+        assert np.all(np.abs(moved - exact) <= 1e-5 * scale)
+    # (the fp64 oracle agrees with the fp32 one far inside the same bound)
+    h64 = oracle64.swiglu(a.astype(np.float64), u.astype(np.float64))
+    assert np.max(np.abs(h64 - h) / np.maximum(np.abs(h64), 1e-30)) < 2.0 ** -20
