@@ -13,6 +13,9 @@ Prints one JSON line.
             position in, greedy next token (and the device error word) copied back each step
   e2e_chained  the same through mk_decode_steps: all timed steps in one call, each step's greedy
             token feeding the next on the device, tokens copied back once at the end
+  persistent   ONE launch running the same number of steps (mk_decode_persistent_*): device
+            time per token from an event pair around the launch, its end-to-end time, and the
+            HBM fraction of the per-token bytes at that time
   roofline  algorithmic bytes per step (weights + KV read + KV written) / median step time,
             against the measured HBM copy bandwidth
   cpu_baseline  the CPU oracle on the host cores, on a bounded sample (whole decode steps)
@@ -341,6 +344,21 @@ def main():
     dec.steps(toks[:cfg.batch], list(wl.kv_len), n_chain, tokens_dev=tokens_dev)
     chained_us = (time.perf_counter() - t0) * 1e6 / n_chain / cfg.batch
 
+    # ---- one persistent launch of n_chain steps (mk_decode_persistent_*): the resident grid runs
+    # every step, each step's greedy token feeding the next on the device; device time from an
+    # event pair around the launch, end-to-end time around start + wait (tokens read back once)
+    dec.persistent(toks[:cfg.batch], list(wl.kv_len), min(W, n_chain), tokens_dev=tokens_dev)   # warm-up
+    torch.cuda.synchronize()
+    pe0 = torch.cuda.Event(enable_timing=True)
+    pe1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    pe0.record(stream)
+    dec.persistent_start(toks[:cfg.batch], list(wl.kv_len), n_chain, tokens_dev=tokens_dev)
+    pe1.record(stream)
+    ran = len(dec.persistent_wait())
+    persistent_e2e_us = (time.perf_counter() - t0) * 1e6 / ran / cfg.batch
+    persistent_dev_us = pe0.elapsed_time(pe1) * 1000.0 / ran / cfg.batch
+
     pos_mid = [l + 0 for l in wl.kv_len]
     step_bytes = cfg.step_bytes(pos_mid)
     peak, peak_kind = peaks()
@@ -362,6 +380,10 @@ def main():
         "e2e_chained": {"value": chained_us, "unit": "us/token", "steps_per_call": n_chain,
                         "h2d_bytes_per_step": 8 * cfg.batch / n_chain,
                         "d2h_bytes_per_step": (4 * cfg.batch * n_chain + 96) / n_chain},
+        "persistent": {"value": persistent_dev_us, "unit": "us/token", "steps_per_launch": ran,
+                       "e2e": persistent_e2e_us, "h2d_bytes_per_step": 8 * cfg.batch / ran,
+                       "d2h_bytes_per_step": (4 * cfg.batch * ran + 96) / ran,
+                       "frac": step_bytes / (persistent_dev_us * cfg.batch * 1e-6) / 1e9 / peak},
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic_record(args.workload), "peak_kind": peak_kind,

@@ -276,8 +276,8 @@ mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, const int32_t*
                                 int32_t* next_tokens);
 
 /* n_steps greedy decode steps in one call, each step's token fed to the next step's embedding on
- * the device (the chained, multi-step form of decoding; the page's "online" megakernel keeps
- * generating without returning to the host).  Step i (0-based) decodes sequence b at position
+ * the device (the chained, multi-step form of decoding, one launch per step; mk_decode_persistent
+ * below runs all the steps in one launch).  Step i (0-based) decodes sequence b at position
  * pos[b] + i; step 0 takes tokens[b] (host), step i > 0 the greedy token of step i - 1.  The
  * steps are launched back to back on the bound stream, one launch each, with no host round trip
  * in between; the host synchronises once, at the end.
@@ -294,6 +294,45 @@ mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, const int32_t*
  * mk_decode_step and poisons the context (later steps then stop at their first wait). */
 mk_status mk_decode_steps(mk_ctx* c, const int32_t* tokens, const int32_t* pos, int32_t n_steps, float* logits,
                           int32_t* tokens_dev, int32_t* tokens_out);
+
+/* Persistent multi-step decode: ONE resident launch runs up to n_steps greedy steps, each step's
+ * token fed to the next step's embedding on the device, and ends early at a step boundary when
+ * the host asks it to (the "Inference MegaKernel" page, section "MPK compiler and runtime": its
+ * runtime's online mode keeps the kernel resident while tokens are pending and polls a host
+ * shutdown signal instead of returning after every token).  Between steps every CTA waits for
+ * all CTAs to retire the previous step (a grid-wide step word, release/acquire ordered); the
+ * previous step's greedy token, the stop decision and the KV rows it appended are read after it.
+ *
+ * mk_decode_persistent_start enqueues the launch on the bound stream and returns at once.
+ *  tokens, pos   HOST int32[batch]: the first step's tokens (in [0, vocab)) and positions
+ *                (pos[b] + n_steps <= max_seq).  Step i decodes sequence b at pos[b] + i.
+ *  n_steps       >= 1: the most steps the launch runs.
+ *  logits        DEVICE fp32[batch, vocab], caller-owned: every step writes it; the last step's
+ *                logits remain.
+ *  tokens_dev    DEVICE int32[n_steps * batch], caller-owned, 4-byte aligned: step i's greedy
+ *                tokens at [i * batch, (i + 1) * batch).  Must stay allocated until the wait.
+ * While the launch is in flight the context accepts only mk_decode_persistent_stop,
+ * mk_decode_persistent_progress and mk_decode_persistent_wait (other calls: MK_ERR_ARG).
+ * Errors: MK_ERR_ARG (null or misaligned pointer, n_steps < 1, a token or position out of range,
+ * a launch already in flight: nothing is launched), MK_ERR_POISONED, MK_ERR_CUDA. */
+mk_status mk_decode_persistent_start(mk_ctx* c, const int32_t* tokens, const int32_t* pos, int32_t n_steps,
+                                     float* logits, int32_t* tokens_dev);
+
+/* Asks the in-flight launch to stop: the first step whose greedy token is chosen after the
+ * request is the last one the launch runs (one or more steps always run).  A plain store to a
+ * host word the device reads; returns at once.  MK_ERR_ARG if no launch is in flight. */
+mk_status mk_decode_persistent_stop(mk_ctx* c);
+
+/* Steps the in-flight (or last) launch has finished so far, read from a host word the device
+ * writes after every step; does not wait.  MK_ERR_ARG on a null argument. */
+mk_status mk_decode_persistent_progress(mk_ctx* c, int32_t* steps_done);
+
+/* Waits for the launch to end.  steps_done (HOST int32, optional) receives the steps it ran
+ * (1..n_steps); tokens_out (HOST int32[n_steps * batch], optional) their greedy tokens, step i at
+ * [i * batch].  The context's next step continues the epoch after the last step run.  Errors:
+ * MK_ERR_ARG (no launch in flight); a device error is reported as by mk_decode_step and poisons
+ * the context. */
+mk_status mk_decode_persistent_wait(mk_ctx* c, int32_t* steps_done, int32_t* tokens_out);
 
 /* Asynchronous form: enqueues one step on the bound stream and returns.  next_tokens_dev is a
  * DEVICE int32[batch] buffer or NULL.  Device-side errors surface at the next mk_ctx_status or
@@ -314,8 +353,9 @@ mk_status mk_device_sm_count(int32_t* out);
  * library convention with no counterpart on the page. */
 const char* mk_last_error(void);
 
-/* Ends a binding: waits for the bound stream, then frees the context's own device copies (queues,
- * counter totals, layer table) and its pinned readback buffer.  The caller's weights, KV cache,
+/* Ends a binding: asks a persistent launch in flight to stop, waits for the bound stream, then
+ * frees the context's own device copies (queues, counter totals, layer table, step word) and its
+ * pinned readback and control buffers.  The caller's weights, KV cache,
  * counters and scratch are not touched (the page's objects live as long as the request that bound
  * them; section "Hand-written whole-model MegaKernel", object table).  NULL is ignored. */
 void mk_unbind(mk_ctx* c);

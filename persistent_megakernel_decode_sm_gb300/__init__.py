@@ -35,7 +35,9 @@ SYNC_TAGS, SYNC_COUNTERS = 0, 1   # mk_sync_mode
 EXPORTS = ["mk_build_schedule", "mk_schedule_queues", "mk_schedule_counters", "mk_schedule_patch",
            "mk_scratch_bytes", "mk_schedule_free", "mk_bind", "mk_set_timeout", "mk_decode_step",
            "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind", "mk_set_trace",
-           "mk_decode_step_static", "mk_set_sync", "mk_decode_steps", "mk_bind_paged", "mk_schedule_attn_chunk"]
+           "mk_decode_step_static", "mk_set_sync", "mk_decode_steps", "mk_bind_paged", "mk_schedule_attn_chunk",
+           "mk_decode_persistent_start", "mk_decode_persistent_stop", "mk_decode_persistent_progress",
+           "mk_decode_persistent_wait"]
 
 
 class MkError(RuntimeError):
@@ -103,6 +105,14 @@ lib.mk_launch_step.restype = ctypes.c_int
 lib.mk_launch_step.argtypes = [_P, _I32P, _I32P, _P, _P]
 lib.mk_decode_steps.restype = ctypes.c_int
 lib.mk_decode_steps.argtypes = [_P, _I32P, _I32P, ctypes.c_int32, _P, _P, _I32P]
+lib.mk_decode_persistent_start.restype = ctypes.c_int
+lib.mk_decode_persistent_start.argtypes = [_P, _I32P, _I32P, ctypes.c_int32, _P, _P]
+lib.mk_decode_persistent_stop.restype = ctypes.c_int
+lib.mk_decode_persistent_stop.argtypes = [_P]
+lib.mk_decode_persistent_progress.restype = ctypes.c_int
+lib.mk_decode_persistent_progress.argtypes = [_P, _I32P]
+lib.mk_decode_persistent_wait.restype = ctypes.c_int
+lib.mk_decode_persistent_wait.argtypes = [_P, _I32P, _I32P]
 lib.mk_ctx_status.restype = ctypes.c_int
 lib.mk_ctx_status.argtypes = [_P, _I32P]
 lib.mk_device_sm_count.restype = ctypes.c_int
@@ -285,6 +295,49 @@ class Decoder:
         out = (ctypes.c_int32 * (max(n_steps, 1) * B))()
         _check(lib.mk_decode_steps(self.handle, t, p, int(n_steps), _ptr(lg), _ptr(tokens_dev), out))
         return [list(out[i * B:(i + 1) * B]) for i in range(n_steps)]
+
+    def persistent_start(self, tokens: Sequence[int], pos: Sequence[int], n_steps: int, logits=None,
+                         tokens_dev=None):
+        """mk_decode_persistent_start: one resident launch of up to n_steps chained greedy steps,
+        enqueued on the bound stream.  Returns the device token buffer ([n_steps * batch] int32);
+        keep it alive until persistent_wait."""
+        import torch
+        B = self.cfg.batch
+        lg = self.logits if logits is None else logits
+        if tokens_dev is None:
+            tokens_dev = torch.empty(max(int(n_steps), 1) * B, dtype=torch.int32, device=lg.device)
+        t, p = self._arrays(tokens, pos)
+        _check(lib.mk_decode_persistent_start(self.handle, t, p, int(n_steps), _ptr(lg), _ptr(tokens_dev)))
+        self._run = (int(n_steps), tokens_dev)
+        return tokens_dev
+
+    def persistent_stop(self):
+        """mk_decode_persistent_stop: the launch in flight ends after the step it is deciding."""
+        _check(lib.mk_decode_persistent_stop(self.handle))
+
+    def persistent_progress(self) -> int:
+        """mk_decode_persistent_progress: steps finished so far (no wait)."""
+        out = ctypes.c_int32(0)
+        _check(lib.mk_decode_persistent_progress(self.handle, ctypes.byref(out)))
+        return out.value
+
+    def persistent_wait(self) -> List[List[int]]:
+        """mk_decode_persistent_wait: waits for the launch; returns the greedy tokens of the steps
+        it ran ([steps][batch])."""
+        B = self.cfg.batch
+        n_steps = self._run[0] if getattr(self, "_run", None) else 1
+        done = ctypes.c_int32(0)
+        out = (ctypes.c_int32 * (n_steps * B))()
+        st = lib.mk_decode_persistent_wait(self.handle, ctypes.byref(done), out)
+        self._run = None
+        _check(st)
+        return [list(out[i * B:(i + 1) * B]) for i in range(done.value)]
+
+    def persistent(self, tokens: Sequence[int], pos: Sequence[int], n_steps: int, logits=None,
+                   tokens_dev=None) -> List[List[int]]:
+        """One persistent launch of n_steps steps, waited for: the tokens per step."""
+        self.persistent_start(tokens, pos, n_steps, logits, tokens_dev)
+        return self.persistent_wait()
 
     def launch(self, tokens: Sequence[int], pos: Sequence[int], logits=None, next_dev=None):
         """mk_launch_step: enqueue one step on the bound stream."""

@@ -18,6 +18,8 @@
 #include <mutex>
 #include <type_traits>
 
+#include <atomic>
+
 #include "mk_internal.h"
 
 namespace mk {
@@ -43,6 +45,14 @@ struct mk_ctx {
     // the epoch (the 3-bit SwiGLU tag repeats every 7 steps), so it is cleared before its next use
     bool bound_stale;
     const int32_t* last_err;   // error word of the last launched step (bound or static scratch)
+    uint32_t* d_step_bar;      // grid-wide step word: each CTA adds 1 per step it retires
+    volatile int32_t* h_ctl;   // mapped pinned words: [0] stop request (host), [1] steps done (device)
+    int32_t* d_ctl;            // their device address
+    // a persistent launch in flight: its step budget and token buffer (the epoch advances by the
+    // steps it ran, known only once it has ended)
+    bool run_active;
+    int32_t run_steps;
+    const int32_t* run_tokens;
     mk_model_cfg cfg;
 };
 
@@ -63,6 +73,8 @@ static void free_ctx(mk_ctx* c) {
     if (c->d_totals) cudaFree(c->d_totals);
     if (c->d_layers) cudaFree(c->d_layers);
     if (c->h_result) cudaFreeHost(c->h_result);
+    if (c->d_step_bar) cudaFree(c->d_step_bar);
+    if (c->h_ctl) cudaFreeHost(const_cast<int32_t*>(c->h_ctl));
     delete c;
 }
 
@@ -279,6 +291,16 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     if ((e = cudaMalloc(&x->d_totals, s->totals.size() * 4)) != cudaSuccess) return bail(cuda_fail(e, "cudaMalloc(totals)"));
     if ((e = cudaMalloc(&x->d_layers, sizeof(LayerPtrs) * L)) != cudaSuccess) return bail(cuda_fail(e, "cudaMalloc(layers)"));
     if ((e = cudaMallocHost(&x->h_result, 256)) != cudaSuccess) return bail(cuda_fail(e, "cudaMallocHost"));
+    if ((e = cudaMalloc(&x->d_step_bar, 4)) != cudaSuccess) return bail(cuda_fail(e, "cudaMalloc(step word)"));
+    {
+        int32_t* ctl = nullptr;
+        if ((e = cudaHostAlloc(&ctl, 64, cudaHostAllocMapped)) != cudaSuccess)
+            return bail(cuda_fail(e, "cudaHostAlloc(control words)"));
+        x->h_ctl = ctl;
+        ctl[0] = ctl[1] = 0;
+        if ((e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&x->d_ctl), ctl, 0)) != cudaSuccess)
+            return bail(cuda_fail(e, "cudaHostGetDevicePointer(control words)"));
+    }
     std::vector<LayerPtrs> lp(L);
     for (int l = 0; l < L; ++l)
         lp[l] = {static_cast<const uint16_t*>(w->attn_norm[l]), static_cast<const uint16_t*>(w->wqkv[l]),
@@ -342,6 +364,9 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     p.acquire_ops = 1u << OP_ARGMAX;
     p.release_ops = 1u << OP_LMHEAD;
     p.timeout_ns = 2000000000ull;
+    p.n_steps = 1;
+    p.step_bar = x->d_step_bar;
+    p.ctl = nullptr;
     x->last_err = p.err;
     p.smem_misc_off = n_pages * g.page_bytes;
     p.attn_scratch_floats = asf;
@@ -352,6 +377,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     // tags start at 0 (never a step's tag): words left in the scratch by an earlier binding must
     // not pass for this context's first steps
     if ((e = cudaMemsetAsync(counters, 0, s->totals.size() * 4, x->stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(x->d_step_bar, 0, 4, x->stream)) != cudaSuccess ||
         (e = cudaMemsetAsync(sb + sl.err, 0, 256, x->stream)) != cudaSuccess ||
         (e = cudaMemsetAsync(sb + sl.x_attn, 0, sl.lm_part - sl.x_attn, x->stream)) != cudaSuccess ||
         (e = cudaMemsetAsync(sb + sl.lm_part, 0xFF, sl.rope - sl.lm_part, x->stream)) != cudaSuccess)
@@ -433,6 +459,7 @@ static mk_status launch(mk_ctx* c, const int32_t* tokens, const int32_t* pos, in
 static mk_status check_step_args(mk_ctx* c, const int32_t* tokens, const int32_t* pos, int32_t n_steps,
                                  const float* logits) {
     if (!c || !tokens || !pos || !logits) return fail(MK_ERR_ARG, "null argument");
+    if (c->run_active) return fail(MK_ERR_ARG, "a persistent launch is in flight (mk_decode_persistent_wait first)");
     if (c->poisoned) return fail(MK_ERR_POISONED, "context poisoned by an earlier device error");
     if (reinterpret_cast<uintptr_t>(logits) & 3u) return fail(MK_ERR_ARG, "logits not 4-byte aligned");
     for (int b = 0; b < c->cfg.batch; ++b) {
@@ -507,14 +534,101 @@ extern "C" mk_status mk_decode_steps(mk_ctx* c, const int32_t* tokens, const int
     return read_status(c, nullptr);
 }
 
+// ---- persistent multi-step decode: one launch, up to n_steps steps, a host stop request ----
+extern "C" mk_status mk_decode_persistent_start(mk_ctx* c, const int32_t* tokens, const int32_t* pos,
+                                                int32_t n_steps, float* logits, int32_t* tokens_dev) {
+    if (!c) return fail(MK_ERR_ARG, "null context");
+    if (n_steps < 1) return fail(MK_ERR_ARG, "n_steps %d < 1", n_steps);
+    if (!tokens_dev || (reinterpret_cast<uintptr_t>(tokens_dev) & 3u))
+        return fail(MK_ERR_ARG, "tokens_dev null or not 4-byte aligned");
+    mk_status st = check_step_args(c, tokens, pos, n_steps, logits);
+    if (st != MK_OK) return st;
+    Params p = c->base;
+    if (c->bound_stale) {
+        const cudaError_t e = clear_scratch(p, c->stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(bound scratch)");
+        c->bound_stale = false;
+    }
+    for (int b = 0; b < c->cfg.batch; ++b) {
+        p.tok[b] = tokens[b];
+        p.pos[b] = pos[b];
+    }
+    p.tok_dev = nullptr;
+    p.logits = logits;
+    p.next_dev = tokens_dev;
+    p.n_steps = n_steps;
+    p.ctl = c->d_ctl;
+    p.trace = nullptr;   // the trace holds one step's stamps
+    // the control words are written before the launch is enqueued: the device sees them
+    c->h_ctl[0] = 0;
+    c->h_ctl[1] = 0;
+    std::atomic_thread_fence(std::memory_order_seq_cst);
+    p.epoch = c->epoch;
+    p.tag = c->epoch + 1u;
+    void* args[] = {&p};
+    const cudaError_t e =
+        cudaLaunchCooperativeKernel(c->fn, dim3(c->grid), dim3(kThreads), args, size_t(c->smem), c->stream);
+    if (e == cudaErrorCooperativeLaunchTooLarge)
+        return fail(MK_ERR_RESOURCES, "cooperative launch of %d CTAs does not fit the device", c->grid);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
+    c->last_err = p.err;
+    c->run_active = true;
+    c->run_steps = n_steps;
+    c->run_tokens = tokens_dev;
+    return MK_OK;
+}
+
+extern "C" mk_status mk_decode_persistent_stop(mk_ctx* c) {
+    if (!c) return fail(MK_ERR_ARG, "null context");
+    if (!c->run_active) return fail(MK_ERR_ARG, "no persistent launch in flight");
+    c->h_ctl[0] = 1;
+    std::atomic_thread_fence(std::memory_order_seq_cst);
+    return MK_OK;
+}
+
+extern "C" mk_status mk_decode_persistent_progress(mk_ctx* c, int32_t* steps_done) {
+    if (!c || !steps_done) return fail(MK_ERR_ARG, "null argument");
+    std::atomic_thread_fence(std::memory_order_seq_cst);
+    *steps_done = c->h_ctl[1];
+    return MK_OK;
+}
+
+extern "C" mk_status mk_decode_persistent_wait(mk_ctx* c, int32_t* steps_done, int32_t* tokens_out) {
+    if (!c) return fail(MK_ERR_ARG, "null context");
+    if (!c->run_active) return fail(MK_ERR_ARG, "no persistent launch in flight");
+    c->run_active = false;
+    cudaError_t e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) {
+        c->poisoned = true;
+        return cuda_fail(e, "persistent launch");
+    }
+    const int32_t ran = c->h_ctl[1];
+    // the steps run advanced the counters, the step word and the tags by that many epochs
+    c->epoch += uint32_t(ran > 0 ? ran : 0);
+    const mk_status st = read_status(c, nullptr);
+    if (st != MK_OK) return st;
+    if (ran < 1 || ran > c->run_steps) {
+        c->poisoned = true;
+        return fail(MK_ERR_CUDA, "persistent launch reported %d steps of %d", ran, c->run_steps);
+    }
+    if (steps_done) *steps_done = ran;
+    if (tokens_out) {
+        e = cudaMemcpy(tokens_out, c->run_tokens, size_t(ran) * c->cfg.batch * sizeof(int32_t), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "token readback");
+    }
+    return MK_OK;
+}
+
 extern "C" mk_status mk_ctx_status(mk_ctx* c, int32_t* info) {
     if (!c) return fail(MK_ERR_ARG, "null context");
+    if (c->run_active) return fail(MK_ERR_ARG, "a persistent launch is in flight (mk_decode_persistent_wait first)");
     if (c->poisoned && !info) return fail(MK_ERR_POISONED, "context poisoned by an earlier device error");
     return read_status(c, info);
 }
 
 extern "C" void mk_unbind(mk_ctx* c) {
     if (!c) return;
+    if (c->run_active) c->h_ctl[0] = 1;   // a persistent launch ends at its next step boundary
     cudaStreamSynchronize(c->stream);
     free_ctx(c);
 }
@@ -535,6 +649,7 @@ static std::mutex g_static_mutex;
 extern "C" mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, const int32_t* pos, float* logits,
                                            int32_t* next_tokens) {
     if (!c || !tokens || !pos || !logits || !next_tokens) return fail(MK_ERR_ARG, "null argument");
+    if (c->run_active) return fail(MK_ERR_ARG, "a persistent launch is in flight (mk_decode_persistent_wait first)");
     if (c->poisoned) return fail(MK_ERR_POISONED, "context poisoned by an earlier device error");
     int dev = -1;
     CK(cudaGetDevice(&dev));

@@ -198,8 +198,11 @@ struct Params {
     int32_t tok[kMaxBatch];
     int32_t pos[kMaxBatch];
     float* logits;
-    int32_t* next_dev;
-    const int32_t* tok_dev;  // optional DEVICE int32[B]: this step's tokens (a chained step), else tok
+    int32_t* next_dev;       // optional DEVICE int32[n_steps][B]: step s's greedy tokens at [s * B]
+    const int32_t* tok_dev;  // optional DEVICE int32[B]: the first step's tokens (a chained step), else tok
+    int32_t n_steps;         // steps this launch runs (>= 1): step s at epoch + s, positions pos + s
+    uint32_t* step_bar;      // DEVICE word: every CTA adds 1 when it retires a step (e * grid at epoch e's start)
+    volatile int32_t* ctl;   // optional host-mapped words: [0] stop request (host), [1] steps done (device)
     uint64_t timeout_ns;
     uint64_t* trace;         // optional [S][Q][8] globaltimer stamps (null: off)
     // shared-memory carve-up

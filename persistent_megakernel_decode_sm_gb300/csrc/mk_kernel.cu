@@ -109,6 +109,15 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v
 __device__ __forceinline__ void red_add_relaxed_gpu(uint32_t* p, uint32_t v) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// host-mapped words (a multi-step launch's control block): system-scope accesses
+__device__ __forceinline__ int32_t ld_sys(const volatile int32_t* a) {
+    int32_t v;
+    asm volatile("ld.relaxed.sys.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_sys(volatile int32_t* a, int32_t v) {
+    asm volatile("st.relaxed.sys.global.b32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -239,6 +248,7 @@ struct Shared {
     float* red;        // [32] argmax scratch
     float2* lmbest;    // [kNumConsumerWarps][kMaxBatch] LM-head running (max, index) of the CTA's tiles
     int* abort;        // [1]
+    int* stop;         // [1] a multi-step launch ends at a step boundary (not an error)
     int* published;    // [1] instructions the publisher has retired
     unsigned long long* issued;   // [1] stream bytes the loader has staged into pages
     float* qrot;       // [8][128]
@@ -274,6 +284,7 @@ __device__ __forceinline__ Shared carve(uint8_t* base, const Params& p) {
     s.red = reinterpret_cast<float*>(b + m.red);
     s.lmbest = reinterpret_cast<float2*>(b + m.lmbest);
     s.abort = reinterpret_cast<int*>(b + m.red) + 32;
+    s.stop = reinterpret_cast<int*>(b + m.red) + 41;
     s.published = reinterpret_cast<int*>(b + m.red) + 33;
     s.issued = reinterpret_cast<unsigned long long*>(reinterpret_cast<int*>(b + m.red) + 34);
     s.qrot = reinterpret_cast<float*>(b + m.qrot);
@@ -315,7 +326,7 @@ __device__ __noinline__ bool wait_bar_slow(const Params& p, const Shared& sh, ui
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-        if (*reinterpret_cast<volatile int*>(sh.abort)) return false;
+        if (*reinterpret_cast<volatile int*>(sh.abort) || *reinterpret_cast<volatile int*>(sh.stop)) return false;
         if (globaltimer() - t0 > budget(p, role)) {
             raise_error(p, sh, MK_ERR_TIMEOUT, role, pc, -1, 0, 0);
             return false;
@@ -342,8 +353,8 @@ struct Stream {
     uint32_t rows, rowbytes, rpp;    // matvec: whole rows per page (0 rows: a plain byte stream)
 };
 
-__device__ __forceinline__ int attn_old_rows(const Params& p, int b, int c, int chunk) {
-    const int pos = p.pos[b];
+__device__ __forceinline__ int attn_old_rows(const Params& p, int b, int c, int chunk, int dpos) {
+    const int pos = p.pos[b] + dpos;
     const int c0 = c * chunk;
     if (c0 > pos) return -1;                 // chunk past pos: inactive
     return min(c0 + chunk, pos) - c0;        // cached positions strictly before pos
@@ -374,7 +385,7 @@ __device__ __forceinline__ bool is_matvec(int op) {
 // The bytes an instruction's body streams.  Matvec tiles carry their resolved weight stream in
 // words 26..31 (written and validated at bind); an attention chunk's cached KV rows depend on pos
 // and are computed here (with the chunk's bounds checked).  Returns an mk_status.
-__device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
+__device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos) {
     st.nseg = 0;
     st.total = 0;
     st.pages = 0;
@@ -401,7 +412,7 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st) {
         if (unsigned(l) >= unsigned(p.L) || unsigned(b) >= unsigned(p.B) || unsigned(g) >= unsigned(p.nkv) ||
             unsigned(c) >= unsigned(p.n_chunk) || C != p.attn_chunk)
             return MK_ERR_BOUNDS;
-        const int n_old = attn_old_rows(p, b, c, C);
+        const int n_old = attn_old_rows(p, b, c, C, dpos);
         if (n_old >= 0 && !kv_chunk_off(p, b, l, g, c, C, st.kv_off)) return MK_ERR_BOUNDS;
         if (n_old > 0) {
             const size_t base = size_t(st.kv_off);
@@ -430,135 +441,194 @@ __device__ __forceinline__ const uint8_t* mv_page(const Stream& st, uint32_t pg,
     return ((st.inter && (pg & 1u)) ? st.seg[1].src : st.seg[0].src) + size_t(r0) * st.rowbytes;
 }
 
+// Another CTA's error reaches this CTA through the global error word; reading it costs a memory
+// round trip, so a poll reads it only every kErrCheckRounds rounds (its own CTA's abort flag, in
+// shared memory, every round).
+constexpr uint32_t kErrCheckRounds = 64;
+__device__ __forceinline__ bool other_cta_failed(const Params& p, uint32_t& rounds) {
+    return (++rounds % kErrCheckRounds) == 0 && ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(p.err)) != 0;
+}
+
+// The loader's side of a step boundary: before the first copy of KV-cache rows in step s > 0 of a
+// multi-step launch (rows the previous step wrote), every CTA has retired that step and the
+// writes are acquired, then ordered before this thread's bulk (async-proxy) reads.  Weight pages
+// need no wait, so a step's first matvec pages stream in while the consumers are still in the
+// previous step.  False: stop, abort or timeout.
+__device__ bool loader_boundary(const Params& p, const Shared& sh, int s, int pc) {
+    const uint32_t target = (p.epoch + uint32_t(s)) * gridDim.x;
+    const uint64_t t0 = globaltimer();
+    uint32_t rounds = 0;
+    while (int32_t(ld_relaxed_gpu(p.step_bar) - target) < 0) {
+        __nanosleep(100);
+        if (*reinterpret_cast<volatile int*>(sh.abort) || *reinterpret_cast<volatile int*>(sh.stop)) return false;
+        if (other_cta_failed(p, rounds)) {
+            *reinterpret_cast<volatile int*>(sh.abort) = 1;
+            return false;
+        }
+        if (globaltimer() - t0 > p.timeout_ns) {
+            raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_LOADER, pc, -1, ld_relaxed_gpu(p.step_bar), target);
+            return false;
+        }
+    }
+    fence_acquire_gpu();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
 __device__ void loader(const Params& p, const Shared& sh) {
     const int32_t* q = p.queues + size_t(blockIdx.x) * p.Q * kWords;
     const uint64_t pol = evict_first_policy();
     const uint32_t PB = uint32_t(p.page_bytes);
     const uint32_t NP = uint32_t(p.n_pages);
     const int n_chunks = (p.Q + kQWin - 1) / kQWin;
-    // the queue is read through a two-buffer shared-memory window, kQWin instructions per bulk copy
+    // The queue is read through a two-buffer shared-memory window, kQWin instructions per bulk
+    // copy; a multi-step launch reads it once per step.  Window fetches, instruction slots and
+    // completion records are indexed by running counts over all steps.
+    int qf = 0;                              // window fetches issued so far
     auto fetch_chunk = [&](int chunk) {
         const int n = min(kQWin, p.Q - chunk * kQWin);
-        uint64_t* bar = sh.qfull + (chunk & 1);
+        uint64_t* bar = sh.qfull + (qf & 1);
         mbar_arrive_expect_tx(bar, uint32_t(n * kWords * 4));
-        bulk_g2s(sh.qwin + (chunk & 1) * kQWin * kWords, q + size_t(chunk) * kQWin * kWords, uint32_t(n * kWords * 4),
+        bulk_g2s(sh.qwin + (qf & 1) * kQWin * kWords, q + size_t(chunk) * kQWin * kWords, uint32_t(n * kWords * 4),
                  bar, pol);
+        ++qf;
     };
-    fetch_chunk(0);
-    if (n_chunks > 1) fetch_chunk(1);
-    int chunks_issued = n_chunks > 1 ? 2 : 1;
-    int chunks_waited = 0;
+    uint32_t gi = 0;                         // instructions published so far
     uint32_t page_seq = 0;                   // pages issued so far
     uint32_t cur_slot = 0, cur_phase = 0;    // ring slot and phase parity of the next page
-    for (int pc = 0; pc < p.Q; ++pc) {
-        const int slot = pc % kSlots;
-        const int chunk = pc / kQWin;
-        if (pc % kQWin == 0) {
-            if (!wait_bar(p, sh, sh.qfull + (chunk & 1), (chunk >> 1) & 1, ROLE_LOADER, pc)) break;
-            chunks_waited = chunk + 1;
-        }
-        if (pc >= kSlots && !wait_bar(p, sh, sh.ins_empty + slot, ((pc / kSlots) - 1) & 1, ROLE_LOADER, pc)) break;
-        SlotInfo& si = sh.slots[slot];
-        const int4* src = reinterpret_cast<const int4*>(sh.qwin + ((chunk & 1) * kQWin + pc % kQWin) * kWords);
-#pragma unroll
-        for (int i = 0; i < kWords / 4; ++i) reinterpret_cast<int4*>(si.w)[i] = src[i];
-        if (pc % kQWin == kQWin - 1 && chunks_issued < n_chunks) {
-            fence_proxy_async_smem();   // generic reads of this buffer before the async refill
-            fetch_chunk(chunks_issued++);
-        }
-        Stream st;
-        const int e = stream_of(p, si.w, st);
-        if (e != MK_OK) {
-            raise_error(p, sh, e, ROLE_LOADER, pc, -1, uint32_t(si.w[W_OP]), 0);
-            break;
-        }
-        si.first_page = int32_t(page_seq);
-        si.n_pages = st.pages;
-        si.kv_off = st.kv_off;
-        si.first_slot = int32_t(cur_slot);
-        si.first_phase = int32_t(cur_phase);
-        if (is_matvec(si.w[W_OP])) {   // shape of the op (bind-time table) and of this tile
-            si.rows = int32_t(st.rows);
-            si.inter = st.inter;
-            si.mv = p.mv[si.w[W_OP]];
-        }
-        {   // completion words for the publisher, which may lag up to kDone instructions behind
-            const uint64_t t0 = globaltimer();
-            bool stalled = false;
-            while (pc - *reinterpret_cast<volatile int*>(sh.published) >= kDone) {
-                __nanosleep(200);
-                if (*reinterpret_cast<volatile int*>(sh.abort)) { stalled = true; break; }
-                if (globaltimer() - t0 > budget(p, ROLE_LOADER)) {
-                    raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_LOADER, pc, -1, 0, 0);
-                    stalled = true;
-                    break;
-                }
+    bool stop = false;
+    int bar_seen = 0;                        // the last step whose boundary this thread has acquired
+    for (int s = 0; s < p.n_steps && !stop; ++s) {
+        const int f0 = qf;                   // fetch index of this step's chunk 0
+        if (s > 0) fence_proxy_async_smem();   // the previous step's generic reads of both buffers
+        fetch_chunk(0);
+        if (n_chunks > 1) fetch_chunk(1);
+        int chunks_issued = n_chunks > 1 ? 2 : 1;
+        int chunks_waited = 0;
+        for (int pc = 0; pc < p.Q; ++pc) {
+            const uint32_t g = gi++;
+            const int slot = int(g % kSlots);
+            const int chunk = pc / kQWin;
+            const int fi = f0 + chunk;       // this chunk's fetch: buffer fi & 1, phase (fi >> 1) & 1
+            if (pc % kQWin == 0) {
+                if (!wait_bar(p, sh, sh.qfull + (fi & 1), (fi >> 1) & 1, ROLE_LOADER, pc)) { stop = true; break; }
+                chunks_waited = chunk + 1;
             }
-            if (stalled) break;
-            int* pi = sh.pubinfo + (pc % kDone) * 8;
-            pi[0] = si.w[W_OP];
-            pi[1] = si.w[W_NPUB];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pi[2 + i] = si.w[W_PUB + i];
-            pi[6] = si.w[W_COND];   // 1: completions only if the consumer marks the tile as the group's last
-            pi[7] = 0;              // set by the consumer: this tile completed its group
-        }
-        stamp(p, pc, 0);
-        mbar_arrive(sh.ins_full + slot);   // release: the slot's words are visible to the consumers
-        if (si.w[W_OP] == OP_END) break;
-        bool stop = false;
-        // a matvec stream is warmed into L2 kL2Ahead pages ahead of the copies into the ring: the
-        // ring's own depth then only has to cover the L2 -> shared memory hop
-        if (st.rows)
-            for (int pg = 0; pg < min(st.pages, kL2Ahead); ++pg) {
-                uint32_t bytes;
-                const uint8_t* src = mv_page(st, uint32_t(pg), bytes);
-                prefetch_l2(src, bytes);
-            }
-        for (int pg = 0; pg < st.pages; ++pg) {
-            const uint32_t ps = cur_slot;
-            if (st.rows && pg + kL2Ahead < st.pages) {
-                uint32_t bytes;
-                const uint8_t* src = mv_page(st, uint32_t(pg + kL2Ahead), bytes);
-                prefetch_l2(src, bytes);
-            }
-            if (page_seq >= NP && !wait_bar(p, sh, sh.empty + ps, cur_phase ^ 1u, ROLE_LOADER, pc)) {
+            if (g >= uint32_t(kSlots) && !wait_bar(p, sh, sh.ins_empty + slot, ((g / kSlots) - 1) & 1, ROLE_LOADER, pc)) {
                 stop = true;
                 break;
             }
-            uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
-            if (st.rows) {   // matvec: a group of whole rows (gate/up: gate rows on even pages, up rows on odd)
-                uint32_t bytes;
-                const uint8_t* src = mv_page(st, uint32_t(pg), bytes);
-                mbar_arrive_expect_tx(sh.full + ps, bytes);
-                bulk_g2s(dst, src, bytes, sh.full + ps, pol);
-            } else {
-                const uint32_t lo = uint32_t(pg) * PB;
-                const uint32_t hi = min(lo + PB, st.total);
-                mbar_arrive_expect_tx(sh.full + ps, hi - lo);
+            SlotInfo& si = sh.slots[slot];
+            const int4* src = reinterpret_cast<const int4*>(sh.qwin + ((fi & 1) * kQWin + pc % kQWin) * kWords);
 #pragma unroll
-                for (int s = 0; s < 2; ++s) {   // (static indexes: the stream stays in registers)
-                    if (s >= st.nseg) break;
-                    const uint32_t a = max(lo, st.seg[s].off);
-                    const uint32_t z = min(hi, st.seg[s].off + st.seg[s].bytes);
-                    if (a < z) bulk_g2s(dst + (a - lo), st.seg[s].src + (a - st.seg[s].off), z - a, sh.full + ps, pol);
-                }
+            for (int i = 0; i < kWords / 4; ++i) reinterpret_cast<int4*>(si.w)[i] = src[i];
+            if (pc % kQWin == kQWin - 1 && chunks_issued < n_chunks) {
+                fence_proxy_async_smem();   // generic reads of this buffer before the async refill
+                fetch_chunk(chunks_issued++);
             }
-            ++page_seq;
-            if (++cur_slot == NP) { cur_slot = 0; cur_phase ^= 1u; }
+            Stream st;
+            const int e = stream_of(p, si.w, st, s);
+            if (e != MK_OK) {
+                raise_error(p, sh, e, ROLE_LOADER, pc, -1, uint32_t(si.w[W_OP]), 0);
+                stop = true;
+                break;
+            }
+            if (s > bar_seen && st.pages > 0 && !st.rows) {   // KV rows: after the step boundary
+                if (!loader_boundary(p, sh, s, pc)) { stop = true; break; }
+                bar_seen = s;
+            }
+            si.first_page = int32_t(page_seq);
+            si.n_pages = st.pages;
+            si.kv_off = st.kv_off;
+            si.first_slot = int32_t(cur_slot);
+            si.first_phase = int32_t(cur_phase);
+            if (is_matvec(si.w[W_OP])) {   // shape of the op (bind-time table) and of this tile
+                si.rows = int32_t(st.rows);
+                si.inter = st.inter;
+                si.mv = p.mv[si.w[W_OP]];
+            }
+            {   // completion words for the publisher, which may lag up to kDone instructions behind
+                const uint64_t t0 = globaltimer();
+                while (int(g) - *reinterpret_cast<volatile int*>(sh.published) >= kDone) {
+                    __nanosleep(200);
+                    if (*reinterpret_cast<volatile int*>(sh.abort) || *reinterpret_cast<volatile int*>(sh.stop)) {
+                        stop = true;
+                        break;
+                    }
+                    if (globaltimer() - t0 > budget(p, ROLE_LOADER)) {
+                        raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_LOADER, pc, -1, 0, 0);
+                        stop = true;
+                        break;
+                    }
+                }
+                if (stop) break;
+                int* pi = sh.pubinfo + (g % kDone) * 8;
+                pi[0] = si.w[W_OP];
+                pi[1] = si.w[W_NPUB];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pi[2 + i] = si.w[W_PUB + i];
+                pi[6] = si.w[W_COND];   // 1: completions only if the consumer marks the tile as the group's last
+                pi[7] = 0;              // set by the consumer: this tile completed its group
+            }
+            stamp(p, pc, 0);
+            mbar_arrive(sh.ins_full + slot);   // release: the slot's words are visible to the consumers
+            if (si.w[W_OP] == OP_END) break;
+            // a matvec stream is warmed into L2 kL2Ahead pages ahead of the copies into the ring: the
+            // ring's own depth then only has to cover the L2 -> shared memory hop
+            if (st.rows)
+                for (int pg = 0; pg < min(st.pages, kL2Ahead); ++pg) {
+                    uint32_t bytes;
+                    const uint8_t* psrc = mv_page(st, uint32_t(pg), bytes);
+                    prefetch_l2(psrc, bytes);
+                }
+            for (int pg = 0; pg < st.pages; ++pg) {
+                const uint32_t ps = cur_slot;
+                if (st.rows && pg + kL2Ahead < st.pages) {
+                    uint32_t bytes;
+                    const uint8_t* psrc = mv_page(st, uint32_t(pg + kL2Ahead), bytes);
+                    prefetch_l2(psrc, bytes);
+                }
+                if (page_seq >= NP && !wait_bar(p, sh, sh.empty + ps, cur_phase ^ 1u, ROLE_LOADER, pc)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
+                if (st.rows) {   // matvec: a group of whole rows (gate/up: gate rows on even pages, up rows on odd)
+                    uint32_t bytes;
+                    const uint8_t* psrc = mv_page(st, uint32_t(pg), bytes);
+                    mbar_arrive_expect_tx(sh.full + ps, bytes);
+                    bulk_g2s(dst, psrc, bytes, sh.full + ps, pol);
+                } else {
+                    const uint32_t lo = uint32_t(pg) * PB;
+                    const uint32_t hi = min(lo + PB, st.total);
+                    mbar_arrive_expect_tx(sh.full + ps, hi - lo);
+#pragma unroll
+                    for (int sg = 0; sg < 2; ++sg) {   // (static indexes: the stream stays in registers)
+                        if (sg >= st.nseg) break;
+                        const uint32_t a = max(lo, st.seg[sg].off);
+                        const uint32_t z = min(hi, st.seg[sg].off + st.seg[sg].bytes);
+                        if (a < z) bulk_g2s(dst + (a - lo), st.seg[sg].src + (a - st.seg[sg].off), z - a, sh.full + ps, pol);
+                    }
+                }
+                ++page_seq;
+                if (++cur_slot == NP) { cur_slot = 0; cur_phase ^= 1u; }
+            }
+            if (stop) break;
+            stamp(p, pc, 1);
+            *reinterpret_cast<volatile unsigned long long*>(sh.issued) += st.total;
         }
-        if (stop) break;
-        stamp(p, pc, 1);
-        *reinterpret_cast<volatile unsigned long long*>(sh.issued) += st.total;
+        // this step's window copies still in flight (prefetched past END, or abandoned): the next
+        // step (or the exit) reuses the buffers
+        for (int cch = chunks_waited; cch < chunks_issued; ++cch) {
+            const int fi = f0 + cch;
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(sh.qfull + (fi & 1), (fi >> 1) & 1))
+                if (globaltimer() - t0 > 1000000000ull) break;   // copies always land; 1 s cap
+        }
     }
-    // queue-window copies still in flight (prefetched past END, or abandoned on abort)
-    for (int c = chunks_waited; c < chunks_issued; ++c) {
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(sh.qfull + (c & 1), (c >> 1) & 1))
-            if (globaltimer() - t0 > 1000000000ull) break;   // copies always land; 1 s cap
-    }
-    if (*reinterpret_cast<volatile int*>(sh.abort)) {
-        // drain: wait for the last copy issued into every page so no bulk copy outlives the CTA
+    {   // drain: wait for the last copy issued into every page so no bulk copy outlives the CTA (after
+        // an abort, or a stop at a step boundary, the consumers may never take those pages; after a
+        // normal end these waits find completed phases)
         const uint32_t first = page_seq > NP ? page_seq - NP : 0;
         for (uint32_t k = first; k < page_seq; ++k) {
             const uint32_t ps = k % NP;
@@ -576,9 +646,10 @@ __device__ void publisher(const Params& p, const Shared& sh) {
     // taken into one batch: one release fence, then one add per distinct counter.  The publisher
     // owns its own completion ring (kDone deep), so a slow fence never holds up the loader.
     constexpr int kBatch = 32;
-    int pc = 0;
-    bool finished = false;
-    while (!finished) {
+    int pc = 0;     // instructions retired over all steps (the completion ring's index)
+    int qpc = 0;    // queue index of instruction pc within its step
+    int ends = 0;   // steps retired (an END closes a step)
+    while (ends < p.n_steps) {
         if (!wait_bar(p, sh, sh.done + (pc % kDone), (pc / kDone) & 1, ROLE_PUBLISHER, pc)) break;
         int n = 1;
         while (n < kBatch && sh.pubinfo[((pc + n - 1) % kDone) * 8] != OP_END &&
@@ -589,7 +660,7 @@ __device__ void publisher(const Params& p, const Shared& sh) {
         bool release = p.sync_counters != 0, any = false;
         for (int i = 0; i < n; ++i) {
             const int* pi = sh.pubinfo + ((pc + i) % kDone) * 8;
-            if (pi[0] == OP_END) { finished = true; n = i + 1; break; }
+            if (pi[0] == OP_END) { n = i + 1; break; }
             release |= (p.release_ops >> pi[0]) & 1;   // its output is read after an acquire, untagged
             any |= pi[1] > 0 && !(pi[6] && !pi[7]);
         }
@@ -616,8 +687,18 @@ __device__ void publisher(const Params& p, const Shared& sh) {
         }
         if (run_c >= 0) red_add_relaxed_gpu(p.counters + run_c, run_d);
         if (p.trace)
-            for (int i = 0; i < n; ++i) stamp(p, pc + i, 4);
+            for (int i = 0; i < n; ++i) stamp(p, qpc + i, 4);
+        const bool end = sh.pubinfo[((pc + n - 1) % kDone) * 8] == OP_END;
+        if (end) {
+            // the step is retired in this CTA: every consumer warp arrived on the END record after its
+            // last tile.  A next step in this launch reads what they wrote once the step word shows
+            // every CTA, so this CTA's writes are released first (cumulative over the CTA's warps)
+            if (ends + 1 < p.n_steps) fence_release_gpu();
+            red_add_relaxed_gpu(p.step_bar, 1u);
+        }
         pc += n;
+        qpc = end ? 0 : qpc + n;
+        ends += end ? 1 : 0;
         *reinterpret_cast<volatile int*>(sh.published) = pc;
     }
 }
@@ -637,6 +718,10 @@ struct Cw {
     int warp, lane;
     uint32_t cb_phase;   // consumer-barrier uses so far
     uint32_t xphase;     // input loads so far
+    // the step this warp is in: a launch runs p.n_steps steps, step s at epoch p.epoch + s (tag
+    // one more) with every position advanced by s
+    int32_t step;
+    uint32_t epoch, tag;
 };
 
 __device__ __forceinline__ const uint8_t* ring_ptr(const Shared& sh, const Params& p, uint32_t first_slot, uint32_t off) {
@@ -684,14 +769,7 @@ struct Spin {
     bool started = false;
     uint32_t rounds = 0;
 };
-// Another CTA's error reaches this CTA through the global error word; reading it costs a memory
-// round trip, so a poll reads it only every kErrCheckRounds rounds (its own CTA's abort flag, in
-// shared memory, every round).
-constexpr uint32_t kErrCheckRounds = 64;
-__device__ __forceinline__ bool other_cta_failed(const Params& p, uint32_t& rounds) {
-    return (++rounds % kErrCheckRounds) == 0 && ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(p.err)) != 0;
-}
-__device__ bool spin_more(const Params& p, const Shared& sh, int lane, Spin& sp, int pc) {
+__device__ bool spin_more(const Params& p, const Shared& sh, int lane, Spin& sp, int pc, uint32_t tag) {
     int stop = 0;
     if (lane == 0) {
         if (*reinterpret_cast<volatile int*>(sh.abort) || other_cta_failed(p, sp.rounds)) {
@@ -703,7 +781,7 @@ __device__ bool spin_more(const Params& p, const Shared& sh, int lane, Spin& sp,
                 sp.t0 = now;
                 sp.started = true;
             } else if (now - sp.t0 > p.timeout_ns) {
-                raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, 0, p.tag);
+                raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, 0, tag);
                 stop = 1;
             }
             if (!stop) __nanosleep(kPollBackoffNs);   // spaces a warp's polling rounds out in L2
@@ -711,7 +789,7 @@ __device__ bool spin_more(const Params& p, const Shared& sh, int lane, Spin& sp,
     }
     return __shfl_sync(0xFFFFFFFFu, stop, 0) == 0;
 }
-__device__ __forceinline__ bool spin_more(const Cw& c, Spin& sp, int pc) { return spin_more(c.p, c.sh, c.lane, sp, pc); }
+__device__ __forceinline__ bool spin_more(const Cw& c, Spin& sp, int pc) { return spin_more(c.p, c.sh, c.lane, sp, pc, c.tag); }
 // warp-wide: lanes with `valid` read the tagged words a0 and a1 until both carry this step's tag
 __device__ bool wpoll2(const Cw& c, bool valid, const uint64_t* a0, const uint64_t* a1, float& v0, float& v1, int pc) {
     Spin sp;
@@ -721,7 +799,7 @@ __device__ bool wpoll2(const Cw& c, bool valid, const uint64_t* a0, const uint64
             const uint64_t w0 = ld_tag(a0), w1 = ld_tag(a1);
             v0 = tag_val(w0);
             v1 = tag_val(w1);
-            ok = tag_of(w0) == c.p.tag && tag_of(w1) == c.p.tag;
+            ok = tag_of(w0) == c.tag && tag_of(w1) == c.tag;
         }
         if (__all_sync(0xFFFFFFFFu, ok)) return true;
         if (!spin_more(c, sp, pc)) return false;
@@ -729,20 +807,20 @@ __device__ bool wpoll2(const Cw& c, bool valid, const uint64_t* a0, const uint64
 }
 // one thread: one tagged element (a thread of a divergent branch).  On abort or timeout the CTA's
 // abort flag is set and the value read last is returned; the caller's next wait then gives up.
-__device__ float poll1(const Params& p, const Shared& sh, const uint64_t* a, int pc) {
+__device__ float poll1(const Params& p, const Shared& sh, const uint64_t* a, int pc, uint32_t tag) {
     uint64_t w = ld_tag(a);
-    if (tag_of(w) == p.tag) return tag_val(w);
+    if (tag_of(w) == tag) return tag_val(w);
     const uint64_t t0 = globaltimer();
     uint32_t rounds = 0;
     while (true) {
         w = ld_tag(a);
-        if (tag_of(w) == p.tag) break;
+        if (tag_of(w) == tag) break;
         if (*reinterpret_cast<volatile int*>(sh.abort) || other_cta_failed(p, rounds)) {
             *reinterpret_cast<volatile int*>(sh.abort) = 1;
             break;
         }
         if (globaltimer() - t0 > p.timeout_ns) {
-            raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, tag_of(w), p.tag);
+            raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, tag_of(w), tag);
             break;
         }
     }
@@ -792,12 +870,15 @@ __device__ __forceinline__ bool load4x(const XSrc& x, int e0, float* v, uint32_t
     return true;
 }
 
-// the step's input token of sequence b: from the host, or in a chained multi-step call the
-// previous step's greedy token in device memory -- clamped to the vocabulary, since a step that
-// failed may have left no token (its recorded error is what the host then reports)
-__device__ __forceinline__ int step_token(const Params& p, int b) {
-    if (!p.tok_dev) return p.tok[b];
-    return min(max(__ldcg(p.tok_dev + b), 0), p.V - 1);
+// the step's input token of sequence b: the first step's from the host (or, in a chained call,
+// from the previous launch's greedy tokens in device memory); a later step of a multi-step launch
+// takes the previous step's greedy token.  Device tokens are clamped to the vocabulary, since a
+// step that failed may have left none (its recorded error is what the host then reports).
+__device__ __forceinline__ int step_token(const Cw& c, int b) {
+    const Params& p = c.p;
+    const int32_t* src = c.step > 0 ? p.next_dev + size_t(c.step - 1) * p.B : p.tok_dev;
+    if (!src) return p.tok[b];
+    return min(max(__ldcg(src + b), 0), p.V - 1);
 }
 
 // where an epilogue's residual comes from: epoch-tagged words, or the bf16 embedding row (layer 0)
@@ -849,7 +930,7 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
 #pragma unroll
                 for (int q = 0; q < kXChunks; ++q) {
                     const int ch = base + q * kConsumerThreads + tid;
-                    if (ch < m.chunks) ok &= load8x(src, ch * 8, v[q], p.tag);
+                    if (ch < m.chunks) ok &= load8x(src, ch * 8, v[q], c.tag);
                 }
                 if (__all_sync(0xFFFFFFFFu, ok)) break;
                 if (!spin_more(c, sp, pc)) return false;
@@ -876,7 +957,7 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
             for (int i = 0; i < CPL; ++i) {
                 const int ch = c.lane + 32 * i;
                 if (ch < nch) {
-                    ok &= load8x(src, (cg0 + ch) * 8, &xr[8 * i], p.tag);
+                    ok &= load8x(src, (cg0 + ch) * 8, &xr[8 * i], c.tag);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
@@ -886,7 +967,7 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
             if (!spin_more(c, sp, pc)) return false;
         }
     }
-    if (rmine) res[tid] = rs.b ? rb : (tag_of(rw) == p.tag ? tag_val(rw) : poll1(p, c.sh, rs.t + tid, pc));
+    if (rmine) res[tid] = rs.b ? rb : (tag_of(rw) == c.tag ? tag_val(rw) : poll1(p, c.sh, rs.t + tid, pc, c.tag));
     __syncwarp();
     if (c.lane == 0) mbar_arrive(c.sh.xfull);
     if (!wait_bar(p, c.sh, c.sh.xfull, c.xphase & 1u, ROLE_CONSUMER, pc)) return false;
@@ -935,18 +1016,18 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
     const size_t lb = size_t(l) * p.B + b;
     const int row = si.w[W_A0] + ru;
     switch (op) {
-        case OP_QKV: st_tag(p.qkv + lb * p.nqkv + row, s0, p.tag); break;
+        case OP_QKV: st_tag(p.qkv + lb * p.nqkv + row, s0, c.tag); break;
         case OP_OPROJ: {
             const float r = ru < kResBuf ? res[ru]
-                          : (l == 0) ? bf16f(p.embed[size_t(step_token(p, b)) * p.H + row])
-                                     : poll1(p, c.sh, p.x_out + (lb - p.B) * p.H + row, pc);
-            st_tag(p.x_attn + lb * p.H + row, r + s0, p.tag);
+                          : (l == 0) ? bf16f(p.embed[size_t(step_token(c, b)) * p.H + row])
+                                     : poll1(p, c.sh, p.x_out + (lb - p.B) * p.H + row, pc, c.tag);
+            st_tag(p.x_attn + lb * p.H + row, r + s0, c.tag);
             break;
         }
-        case OP_UPGATE: st_htag(p.h + lb * p.F + row, __fdividef(s0, 1.0f + __expf(-s0)) * s1, htag(p.tag)); break;
+        case OP_UPGATE: st_htag(p.h + lb * p.F + row, __fdividef(s0, 1.0f + __expf(-s0)) * s1, htag(c.tag)); break;
         case OP_DOWN: {
-            const float r = ru < kResBuf ? res[ru] : poll1(p, c.sh, p.x_attn + lb * p.H + row, pc);
-            st_tag(p.x_out + lb * p.H + row, r + s0, p.tag);
+            const float r = ru < kResBuf ? res[ru] : poll1(p, c.sh, p.x_attn + lb * p.H + row, pc, c.tag);
+            st_tag(p.x_out + lb * p.H + row, r + s0, c.tag);
             break;
         }
         default:   // LM head: the logit, then this lane's running (max, lowest index)
@@ -1058,12 +1139,12 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
         switch (op) {
             case OP_QKV:
                 gain = c.sh.layers[l].attn_norm;
-                if (l == 0) src.b = p.embed + size_t(step_token(p, b)) * p.H;
+                if (l == 0) src.b = p.embed + size_t(step_token(c, b)) * p.H;
                 else src.t = p.x_out + (lb - p.B) * p.H;
                 break;
             case OP_OPROJ:
                 src.t = p.o + lb * p.qd;
-                if (l == 0) rs.b = p.embed + size_t(step_token(p, b)) * p.H + a0;
+                if (l == 0) rs.b = p.embed + size_t(step_token(c, b)) * p.H + a0;
                 else rs.t = p.x_out + (lb - p.B) * p.H + a0;
                 nres = min(R, kResBuf);
                 break;
@@ -1233,7 +1314,7 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
                 float2& run = c.sh.lmbest[c.warp * kMaxBatch + b];
                 if (bv > run.x || (bv == run.x && bi < __float_as_int(run.y))) run = make_float2(bv, __int_as_float(bi));
                 p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * kNumConsumerWarps + c.warp] =
-                    make_int4(__float_as_int(run.x), __float_as_int(run.y), int(p.epoch), 0);
+                    make_int4(__float_as_int(run.x), __float_as_int(run.y), int(c.epoch), 0);
             }
         }
         // batch > 1: the page slots' partials and counters serve the next sequence
@@ -1289,7 +1370,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     const int l = si.w[W_LAYER], b = si.w[W_B], g = si.w[W_A0], ch = si.w[W_A1], C = si.w[W_A2];
     const int d = p.d, half = d / 2, hpg = p.hpg;
     const int tid = c.warp * 32 + c.lane;
-    const int n_old = attn_old_rows(p, b, ch, C);
+    const int n_old = attn_old_rows(p, b, ch, C, c.step);
     const size_t lb = size_t(l) * p.B + b;
     const uint64_t* qkv = p.qkv + lb * p.nqkv;
     // [hpg][C] scores in the shared-x buffer: no warp reads a matvec input while the tile runs
@@ -1299,7 +1380,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     float* sc = c.sh.xbuf;
     float* cf = c.sh.ascr;
     if (n_old >= 0) {
-        const int pos = p.pos[b];
+        const int pos = p.pos[b] + c.step;
         const bool has_new = pos < ch * C + C;
         const int n = n_old + (has_new ? 1 : 0);
         const float2* rp = p.rope + size_t(pos) * half;
@@ -1411,13 +1492,13 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     if (tid == 0) {
         const uint32_t nch = uint32_t(si.w[W_ARRIVE_N]);
         const uint32_t old = atom_add_acq_rel_gpu(p.counters + si.w[W_ARRIVE], 1u);
-        const bool last = old - p.epoch * nch == nch - 1u;
+        const bool last = old - c.epoch * nch == nch - 1u;
         reinterpret_cast<volatile int*>(c.sh.red)[40] = last ? 1 : 0;
         if (last) c.sh.pubinfo[(pc % kDone) * 8 + 7] = 1;   // fire this tile's completion
     }
     if (!cbar(c, pc)) return false;
     if (!reinterpret_cast<volatile int*>(c.sh.red)[40]) return true;
-    const int nact = min(p.n_chunk, p.pos[b] / C + 1);
+    const int nact = min(p.n_chunk, (p.pos[b] + c.step) / C + 1);
     const float* pbase = p.part + (lb * p.nkv + g) * size_t(p.n_chunk) * hpg * (d + 2);
     // the group's active partials are one contiguous block; when it fits the shared input buffer
     // (free during attention: the tile began with every warp past its previous input) it is staged
@@ -1460,7 +1541,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) a4[r] = fmaf(f[k + r], ph[(k + r) * cs], a4[r]);
         for (; k < nact; ++k) a4[k & 3] = fmaf(f[k], ph[k * cs], a4[k & 3]);
-        st_tag(out + idx, ((a4[0] + a4[1]) + (a4[2] + a4[3])) / c.sh.cml[h], p.tag);
+        st_tag(out + idx, ((a4[0] + a4[1]) + (a4[2] + a4[3])) / c.sh.cml[h], c.tag);
     }
     // staged: no warp may refill the shared-x buffer (next instruction) while others still read it
     if (pb != pbase && !cbar(c, pc)) return false;
@@ -1478,7 +1559,7 @@ __device__ bool argmax_tile(Cw& c, const SlotInfo& si, int pc) {
     int bi = 0x7FFFFFFF;
     for (int i = tid; i < n; i += kConsumerThreads) {
         const int4 v = __ldcg(parts + i);
-        if (uint32_t(v.z) != p.epoch) continue;   // written in an earlier step: this warp had no LM rows
+        if (uint32_t(v.z) != c.epoch) continue;   // written in an earlier step: this warp had no LM rows
         const float val = __int_as_float(v.x);
         if (val > bv || (val == bv && v.y < bi)) { bv = val; bi = v.y; }
     }
@@ -1498,7 +1579,15 @@ __device__ bool argmax_tile(Cw& c, const SlotInfo& si, int pc) {
             if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
         }
         p.tokens_out[b] = bi;
-        if (p.next_dev) p.next_dev[b] = bi;
+        if (p.next_dev) p.next_dev[size_t(c.step) * p.B + b] = bi;
+        if (b == 0 && p.ctl) {
+            // a multi-step launch: the host's stop request, read once here, decides for every CTA
+            // whether a next step runs (each reads this step's word at the next step boundary; the
+            // words alternate, so a CTA slow to read it never sees the following step's decision);
+            // the steps done so far go back to the host
+            p.err[8 + (c.step & 1)] = ld_sys(p.ctl);
+            st_sys(p.ctl + 1, c.step + 1);
+        }
     }
     return true;
 }
@@ -1511,14 +1600,15 @@ struct CounterCache {
     int32_t id, need;
 };
 
-__device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* w, int pc, CounterCache& cc) {
+__device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* w, int pc, CounterCache& cc,
+                              uint32_t epoch) {
     const int nw = w[W_NWAIT];
     bool polled = false;
     for (int i = 0; i < nw; ++i) {
         const int cid = w[W_WAIT + 2 * i], need = w[W_WAIT + 2 * i + 1];
         if (cc.id == cid && cc.need == need) continue;
         polled = true;
-        const uint32_t target = p.epoch * __ldg(p.totals + cid) + uint32_t(need);
+        const uint32_t target = epoch * __ldg(p.totals + cid) + uint32_t(need);
         uint32_t v = ld_relaxed_gpu(p.counters + cid);
         if (int32_t(v - target) < 0) {
             const uint64_t t0 = globaltimer();
@@ -1543,49 +1633,96 @@ __device__ bool wait_counters(const Params& p, const Shared& sh, const int32_t* 
     return true;
 }
 
+// The boundary into step c.step (> 0) of a multi-step launch: every CTA has retired the previous
+// step (each added 1 to the step word after a release fence), so its greedy tokens -- this step's
+// inputs -- and everything else it wrote are visible after the acquire.  The previous step's stop
+// word, written by its first argmax, decides for every CTA alike.  False: stop, or the CTA aborts.
+__device__ bool step_boundary(Cw& c, int pc) {
+    const Params& p = c.p;
+    int ok = 1;
+    if (c.lane == 0) {
+        const uint32_t target = c.epoch * gridDim.x;
+        const uint64_t t0 = globaltimer();
+        uint32_t rounds = 0;
+        while (int32_t(ld_relaxed_gpu(p.step_bar) - target) < 0) {
+            if (*reinterpret_cast<volatile int*>(c.sh.abort) || other_cta_failed(p, rounds)) {
+                *reinterpret_cast<volatile int*>(c.sh.abort) = 1;
+                ok = 0;
+                break;
+            }
+            if (globaltimer() - t0 > p.timeout_ns) {
+                raise_error(p, c.sh, MK_ERR_TIMEOUT, ROLE_COUNTER, pc, -1, ld_relaxed_gpu(p.step_bar), target);
+                ok = 0;
+                break;
+            }
+        }
+        if (ok) {
+            fence_acquire_gpu();
+            if (*reinterpret_cast<volatile const int32_t*>(p.err + 8 + ((c.step - 1) & 1)) != 0) {
+                *reinterpret_cast<volatile int*>(c.sh.stop) = 1;
+                ok = 0;
+            } else {
+                // this warp's LM-head running bests start over
+                for (int b = 0; b < p.B; ++b)
+                    c.sh.lmbest[c.warp * kMaxBatch + b] = make_float2(-INFINITY, __int_as_float(0x7FFFFFFF));
+            }
+        }
+    }
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
 template <int CPL>
 __device__ void consumer_warp(const Params& p, const Shared& sh) {
-    Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u};
-    CounterCache cc{-1, -1};
-    for (int pc = 0;; ++pc) {
-        const int slot = pc % kSlots;
-        if (!wait_bar(p, sh, sh.ins_full + slot, (pc / kSlots) & 1, ROLE_CONSUMER, pc)) break;
-        const SlotInfo& si = sh.slots[slot];
-        const int op = si.w[W_OP];
-        if (op != OP_END) {
-            // the RMSNorm gain of a new input depends on no counter: start fetching it into L1
-            // before waiting, so the normalisation after the wait does not pay a second round trip
-            const uint16_t* gain = op == OP_QKV ? sh.layers[si.w[W_LAYER]].attn_norm
-                                 : op == OP_UPGATE ? sh.layers[si.w[W_LAYER]].mlp_norm
-                                 : op == OP_LMHEAD ? p.final_norm : nullptr;
-            if (gain && c.lane * 64 < p.H * 2)
-                for (int off = c.lane * 64; off < p.H * 2; off += 32 * 64)
-                    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(gain) + off));
-            // counters (with acquire semantics) in the counters mode and for the consumers that read
-            // their inputs without tags (the argmax over the LM-head partials, the MLP down
-            // projection's SwiGLU input, matvecs whose rows are cut into segments); every other
-            // consumer polls the tagged words it reads until they carry this step's tag, with no
-            // counter in between: a counter poll before the data read would add a round trip
-            int ok = 1;
-            if (c.lane == 0 && (p.sync_counters || ((p.acquire_ops >> op) & 1)))
-                ok = wait_counters(p, sh, si.w, pc, cc);
-            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-            if (threadIdx.x == 0) stamp(p, pc, 2);
-            bool good;
-            switch (op) {
-                case OP_ATTN: good = attn_tile(c, si, pc); break;
-                case OP_ARGMAX: good = argmax_tile(c, si, pc); break;
-                default: good = matvec_tile<CPL>(c, si, pc); break;
+    Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u, 0, p.epoch, p.tag};
+    // slots and completion records are indexed by g, the instructions taken over all steps
+    uint32_t g = 0;
+    for (int s = 0; s < p.n_steps; ++s) {
+        c.step = s;
+        c.epoch = p.epoch + uint32_t(s);
+        c.tag = c.epoch + 1u;
+        if (s > 0 && !step_boundary(c, int(g))) return;
+        CounterCache cc{-1, -1};
+        for (;; ++g) {
+            const int slot = int(g % kSlots);
+            const int pc = int(g);
+            if (!wait_bar(p, sh, sh.ins_full + slot, (g / kSlots) & 1, ROLE_CONSUMER, pc)) return;
+            const SlotInfo& si = sh.slots[slot];
+            const int op = si.w[W_OP];
+            if (op != OP_END) {
+                // the RMSNorm gain of a new input depends on no counter: start fetching it into L1
+                // before waiting, so the normalisation after the wait does not pay a second round trip
+                const uint16_t* gain = op == OP_QKV ? sh.layers[si.w[W_LAYER]].attn_norm
+                                     : op == OP_UPGATE ? sh.layers[si.w[W_LAYER]].mlp_norm
+                                     : op == OP_LMHEAD ? p.final_norm : nullptr;
+                if (gain && c.lane * 64 < p.H * 2)
+                    for (int off = c.lane * 64; off < p.H * 2; off += 32 * 64)
+                        asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(gain) + off));
+                // counters (with acquire semantics) in the counters mode and for the consumers that read
+                // their inputs without tags (the argmax over the LM-head partials, the MLP down
+                // projection's SwiGLU input, matvecs whose rows are cut into segments); every other
+                // consumer polls the tagged words it reads until they carry this step's tag, with no
+                // counter in between: a counter poll before the data read would add a round trip
+                int ok = 1;
+                if (c.lane == 0 && (p.sync_counters || ((p.acquire_ops >> op) & 1)))
+                    ok = wait_counters(p, sh, si.w, pc, cc, c.epoch);
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return;
+                if (threadIdx.x == 0) stamp(p, pc, 2);
+                bool good;
+                switch (op) {
+                    case OP_ATTN: good = attn_tile(c, si, pc); break;
+                    case OP_ARGMAX: good = argmax_tile(c, si, pc); break;
+                    default: good = matvec_tile<CPL>(c, si, pc); break;
+                }
+                if (!good) return;
+                if (threadIdx.x == 0) stamp(p, pc, 3);
             }
-            if (!good) break;
-            if (threadIdx.x == 0) stamp(p, pc, 3);
+            __syncwarp();
+            if (c.lane == 0) {
+                mbar_arrive(sh.ins_empty + slot);
+                mbar_arrive(sh.done + (g % kDone));
+            }
+            if (op == OP_END) { ++g; break; }
         }
-        __syncwarp();
-        if (c.lane == 0) {
-            mbar_arrive(sh.ins_empty + slot);
-            mbar_arrive(sh.done + (pc % kDone));
-        }
-        if (op == OP_END) break;
     }
 }
 
@@ -1610,6 +1747,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
         mbar_init(sh.xfull, kNumConsumerWarps);
         mbar_init(sh.xfree, kNumConsumerWarps);
         *sh.abort = 0;
+        *sh.stop = 0;
         *sh.issued = 0ull;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }

@@ -75,3 +75,8 @@ def test_step_calls_reject_null_and_bad_arguments_without_a_device():
     assert lib.mk_decode_steps(None, t, p, 2, dummy, dummy, out) == mk.MK_ERR_ARG      # no context
     assert lib.mk_launch_step(None, t, p, dummy, None) == mk.MK_ERR_ARG
     assert lib.mk_decode_step(None, t, p, dummy, out) == mk.MK_ERR_ARG
+    n = ctypes.c_int32(0)
+    assert lib.mk_decode_persistent_start(None, t, p, 4, dummy, dummy) == mk.MK_ERR_ARG   # no context
+    assert lib.mk_decode_persistent_stop(None) == mk.MK_ERR_ARG
+    assert lib.mk_decode_persistent_progress(None, ctypes.byref(n)) == mk.MK_ERR_ARG
+    assert lib.mk_decode_persistent_wait(None, ctypes.byref(n), out) == mk.MK_ERR_ARG
