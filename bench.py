@@ -255,6 +255,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--attn-chunk", type=int, default=0,
+                    help="KV positions per split-K attention tile (0: the scheduler's rule)")
     ap.add_argument("--sync", default="tags", choices=["tags", "counters"],
                     help="how consumers learn their inputs are ready (mk_set_sync)")
     args = ap.parse_args()
@@ -283,7 +285,8 @@ def main():
     kv = prefilled_kv(cfg, wl.kv_len, seed=0, device="cuda")
     S = mk.device_sm_count()
     stream = torch.cuda.Stream()
-    dec = mk.Decoder(mk.Schedule(cfg, S), w, kv, stream=stream)
+    sched = mk.Schedule(cfg, S, attn_chunk=args.attn_chunk)
+    dec = mk.Decoder(sched, w, kv, stream=stream)
     dec.set_sync(args.sync)
     span = cfg.max_seq - max(wl.kv_len)
     toks = token_ids(cfg, (W + K) * cfg.batch, seed=1, tag="bench")
@@ -372,7 +375,7 @@ def main():
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "batch": cfg.batch, "kv_len": wl.kv_len[0] if cfg.batch == 1 else wl.kv_len,
                    "weights": "bf16", "kv": "bf16", "sm_count": S, "parallelism": "replicas" if world > 1 else "single",
-                   "sync": args.sync,
+                   "sync": args.sync, "attn_chunk": sched.attn_chunk,
                    "l2": "inputs larger than L2 (2.47 GB of weights streamed per step)",
                    "step_us_mean": mean_us, "step_us_median": med, "step_us_p10": p10, "step_us_p90": p90},
         "e2e": {"value": e2e_us, "unit": "us/token", "h2d_bytes_per_step": 8 * cfg.batch,

@@ -104,9 +104,10 @@ mk_status mk_build_schedule(const mk_model_cfg* cfg, int32_t sm_count, const mk_
  *   [6] number of waits (<= 4)   [7..14] (counter, need) pairs
  *   [15] number of completions (<= 2)   [16..19] (counter, delta) pairs
  *   [20] pages of the largest stream the tile may need   [21] tile id   [22] wave
- *   [23] 1 = conditional completions: the tile adds 1 to arrival counter [24] itself and its
- *        completions fire only if it is the last of [25] arrivals (ATTN: the group's combine)
- *   [26..31] 0 (the bound device copy carries the tile's resolved stream addresses here)
+ *   [23] 1 = conditional completions (ATTN): only the tile whose chunk holds the step's
+ *        position fires them; it combines the group's chunk partials, waiting inside its wave
+ *        for the lower chunks (each queue runs its tiles of a wave in tile-id order)
+ *   [24..31] 0 (the bound device copy carries the tile's resolved stream addresses in [26..31])
  * A wait is satisfied when counter - (epoch * total[counter] + need) >= 0 (mod 2^32).  END is
  * all zeros and pads every queue. */
 mk_status mk_schedule_queues(const mk_schedule* s, const int32_t** queues, int32_t* sm_count,

@@ -14,10 +14,11 @@ Tiles (per layer l, in this order; ids are assigned in enumeration order):
           touches one or two KV groups' q, k or v ranges and completes each group it touches.
           RMSNorm of the layer input is its prologue.
   ATTN    (b, g, c): sequence b, KV group g, KV positions [c*C, (c+1)*C) -- split-K decode
-          attention; c runs over ceil(max_seq / C) chunks (chunks past pos do no work).  Every
-          chunk tile adds 1 to the group's arrival counter itself; the tile that completes the
-          group (the last arriver) also does the fixed-order log-sum-exp combine of the group's
-          chunk partials and alone carries the tile's completion (a conditional completion).
+          attention; c runs over ceil(max_seq / C) chunks (chunks past pos do no work).  The
+          tile whose chunk holds the step's position (known at run time only) also does the
+          fixed-order log-sum-exp combine of the group's chunk partials, reading the lower
+          chunks' partials as they land, and alone carries the tile's completion (a conditional
+          completion).
   OPROJ   rows of Wo, residual add.
   UPGATE  row pairs [r, r+R_up) of gate and of up, SiLU(gate)*up epilogue.
   DOWN    rows of Wdown, residual add.
@@ -35,7 +36,9 @@ the SMs holding fewer than ceil(n / S) of the n tiles of its pool in this wave; 
 cost carries across waves.  cost = streamed bytes + TILE_OVERHEAD.
 With a non-zero shuffle seed the wave's tiles are instead put in a splitmix64 Fisher-Yates
 order (pools still kept apart) -- the "shuffled assignment" used to test determinism.
-Queue of an SM: its tiles in assignment order, padded with END (all-zero words).
+Queue of an SM: its tiles wave by wave, in tile-id order within a wave (so the combining
+attention tile, which waits inside its wave on lower chunks of its group, only ever waits on tiles
+every queue runs before it), padded with END (all-zero words).
 """
 from __future__ import annotations
 
@@ -106,11 +109,10 @@ class Counters:
     def __init__(self, cfg):
         L, nkv, B = cfg.n_layers, cfg.n_kv_heads, cfg.batch
         self.L, self.nkv, self.B = L, nkv, B
-        self.base2 = L * nkv * (1 + B)
+        self.base2 = L * nkv
         self.n = self.base2 + 4 * L + 2
 
     def qkv(self, l, g): return l * self.nkv + g
-    def attn(self, l, b, g): return self.L * self.nkv + (l * self.B + b) * self.nkv + g
     def comb(self, l): return self.base2 + l
     def o(self, l): return self.base2 + self.L + l
     def up(self, l): return self.base2 + 2 * self.L + l
@@ -132,8 +134,7 @@ class Tile:
     pubs: List[Tuple[int, int]]
     stream_bytes: int
     tid: int = -1
-    arrive: int = -1     # ATTN: arrival counter the tile increments itself; pubs then belong
-    arrive_n: int = 0    # to the last of arrive_n arrivals only
+    cond: bool = False   # ATTN: pubs only from the tile that combines its group
 
     @property
     def memory(self) -> bool:
@@ -206,8 +207,7 @@ def enumerate_tiles(cfg, o: SchedOpts, S: int) -> Tuple[List[Tile], Counters, Di
                 for c in range(nchunk):
                     tiles.append(Tile(ATTN, l, b, g, c, C, 5 * l + 1,
                                       [(cnt.qkv(l, g), qkv_tiles_of_group[g])],
-                                      [(cnt.comb(l), 1)], 2 * C * d * 2,
-                                      arrive=cnt.attn(l, b, g), arrive_n=nchunk))
+                                      [(cnt.comb(l), 1)], 2 * C * d * 2, cond=True))
         for t in range(n_o):
             r0 = t * R["o"]
             n = min(R["o"], H - r0)
@@ -278,8 +278,8 @@ def encode(t: Tile, n_pages: int) -> List[int]:
     w[20] = n_pages
     w[21] = t.tid
     w[22] = t.wave
-    if t.arrive >= 0:   # completions only from the last of arrive_n arrivals on counter `arrive`
-        w[23], w[24], w[25] = 1, t.arrive, t.arrive_n
+    if t.cond:   # completions only from the tile that combines its group
+        w[23] = 1
     return w
 
 
@@ -304,6 +304,7 @@ def build_schedule(cfg, S: int, opts: Optional[SchedOpts] = None):
             pools = [sorted(mem, key=lambda t: (-t.cost, t.tid)), sorted(cmp_, key=lambda t: (-t.cost, t.tid))]
         else:
             pools = [_shuffle(mem, rng), _shuffle(cmp_, rng)]
+        start = [len(q) for q in per_sm]
         for pool in pools:
             cap = ceil_div(len(pool), S)
             in_wave = np.zeros(S, dtype=np.int64)
@@ -313,6 +314,8 @@ def build_schedule(cfg, S: int, opts: Optional[SchedOpts] = None):
                 per_sm[s].append(t)
                 acc[s] += t.cost
                 in_wave[s] += 1
+        for s in range(S):   # a queue runs its tiles of a wave in id order
+            per_sm[s][start[s]:] = sorted(per_sm[s][start[s]:], key=lambda t: t.tid)
     Q = 1 + max(len(q) for q in per_sm)
     queues = np.zeros((S, Q, WORDS), dtype=np.int32)
     for s in range(S):
@@ -320,14 +323,10 @@ def build_schedule(cfg, S: int, opts: Optional[SchedOpts] = None):
             queues[s, i] = encode(t, tile_pages(t, cfg, o))
     totals = np.zeros(cnt.n, dtype=np.uint64)
     for t in tiles:
-        if t.arrive >= 0:
-            totals[t.arrive] += 1                 # each tile arrives once
-            if t.a1 == t.arrive_n - 1:            # the group's completion counts once
-                for c, dl in t.pubs:
-                    totals[c] += dl
-        else:
-            for c, dl in t.pubs:
-                totals[c] += dl
+        if t.cond and t.a1 != 0:   # a group's completion counts once
+            continue
+        for c, dl in t.pubs:
+            totals[c] += dl
     info = dict(rows=R, n_tiles=len(tiles), counters=cnt, tiles=tiles,
                 n_chunks=ceil_div(cfg.max_seq, attn_chunk(cfg, o, S)))
     return queues, totals.astype(np.uint32), info
@@ -342,8 +341,7 @@ def _decode(w) -> Tile:
     pubs = [(int(w[16 + 2 * i]), int(w[17 + 2 * i])) for i in range(int(w[15]))]
     t = Tile(int(w[0]), int(w[1]), int(w[2]), int(w[3]), int(w[4]), int(w[5]), int(w[22]),
              waits, pubs, 0, int(w[21]))
-    if w[23] == 1:
-        t.arrive, t.arrive_n = int(w[24]), int(w[25])
+    t.cond = int(w[23]) == 1
     return t
 
 
@@ -357,7 +355,11 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
     * waits point only at counters produced in strictly lower waves, and each SM's queue is in
       non-decreasing wave order (the forward-progress rule: a waiter never holds an SM that a
       producer it waits on still needs);
-    * (DAG + per-SM program order) is acyclic -- implied by the two previous points;
+    * within a wave each SM's tiles are in increasing tile-id order, and the attention chunk
+      tiles of a group carry conditional completions (exactly one completion per group is
+      counted): the combining chunk tile's wait inside its wave is on lower chunks of its group,
+      i.e. on lower ids, which no queue runs after a higher id of that wave;
+    * (DAG + per-SM program order) is acyclic -- implied by the points above;
     * capacity: at most 4 waits and 2 completions per instruction; at batch > 1 no instruction
       needs more pages than the ring holds.
     """
@@ -370,11 +372,10 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
     seen: Dict[int, Tuple[int, int]] = {}
     pub_sum = np.zeros(cnt.n, dtype=np.int64)
     producer_wave: Dict[int, int] = {}
-    arrivals: Dict[int, int] = {}
-    cond_pubs: Dict[int, Tuple[int, list, int]] = {}
     for s in range(S):
         ended = False
         last_wave = -1
+        last_tid = -1
         for i in range(Q):
             w = queues[s, i]
             if w[0] == END:
@@ -393,14 +394,17 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
             seen[t.tid] = (s, i)
             if t.wave < last_wave:
                 errs.append(f"sm {s} slot {i}: wave {t.wave} after wave {last_wave}")
-            last_wave = t.wave
+            elif t.wave == last_wave and t.tid < last_tid:
+                errs.append(f"sm {s} slot {i}: tile {t.tid} after tile {last_tid} of the same wave")
+            last_wave, last_tid = t.wave, t.tid
             if len(t.waits) > MAX_WAIT or len(t.pubs) > MAX_PUB:
                 errs.append(f"tile {t.tid}: too many waits/completions")
-            produced = list(t.pubs)
-            if t.arrive >= 0:
-                arrivals[t.arrive] = arrivals.get(t.arrive, 0) + 1
-                produced = [(t.arrive, 1)]
-                cond_pubs.setdefault(t.arrive, (t.arrive_n, list(t.pubs), t.wave))
+            if t.cond != (t.op == ATTN):
+                errs.append(f"tile {t.tid}: conditional completions on a {OPNAMES[t.op]} tile"
+                            if t.cond else f"tile {t.tid}: attention tile without conditional completions")
+            # conditional completions: one per group, counted at its chunk 0 (which tile fires it
+            # is decided at run time)
+            produced = [] if (t.cond and t.a1 != 0) else list(t.pubs)
             for c, dl in produced:
                 pub_sum[c] += dl
                 pw = producer_wave.setdefault(c, t.wave)
@@ -418,14 +422,6 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
             errs.append(f"sm {s}: queue not END-terminated")
     if len(seen) != len(ref_tiles):
         errs.append(f"{len(seen)} tiles scheduled, model has {len(ref_tiles)}")
-    for a, (n_arr, pubs, wave) in cond_pubs.items():   # each completed group publishes once
-        if arrivals.get(a, 0) != n_arr:
-            errs.append(f"arrival counter {a}: {arrivals.get(a, 0)} tiles arrive, {n_arr} expected")
-        for c, dl in pubs:
-            pub_sum[c] += dl
-            pw = producer_wave.setdefault(c, wave)
-            if pw != wave:
-                errs.append(f"counter {c} produced in waves {pw} and {wave}")
     if not np.array_equal(pub_sum.astype(np.uint32), np.asarray(totals, dtype=np.uint32)):
         errs.append("per-step counter totals differ from the sum of published deltas")
     for s in range(S):
@@ -469,9 +465,8 @@ def _reads_writes(t: Tile, cfg):
 
         for r in range(t.a0, t.a0 + t.a1):   # rows counted per KV group (a tile may touch two)
             W.append((("qkv", l, group(r)), 1))
-    elif op == ATTN:
+    elif op == ATTN:   # (its partial and the combine's output: in the simulator, by position)
         R.append((("qkv", l, t.a0), (hpg + 2) * d))
-        W.append((("part", l, t.b, t.a0), 1))
     elif op == OPROJ:
         R.append((("o", l), cfg.batch * nkv))
         if l > 0:
@@ -494,12 +489,18 @@ def _reads_writes(t: Tile, cfg):
 
 
 def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, seed: int = 0,
-             track_data: bool = True) -> List[str]:
+             track_data: bool = True, pos: Optional[List[int]] = None) -> List[str]:
     """Runs the S queues on the host under a random interleaving, for n_epochs consecutive steps
     with epoch-offset counter targets (target = epoch * total + need, compared modulo 2^32).
-    Reports a deadlock (no SM can progress before all reach END) and any read of a buffer whose
-    writer has not yet run in the current step."""
+    Sequence b decodes position pos[b] (default max_seq - 1: every attention chunk active): the
+    chunk tiles past it do nothing, the others write their partial, and the tile of the chunk
+    holding it waits (inside its wave) until the lower chunks of its group have written theirs,
+    then writes the group's attention output and fires the completion.  Reports a deadlock (no
+    SM can progress before all reach END) and any read of a buffer whose writer has not yet run
+    in the current step."""
     S, Q, _ = queues.shape
+    if pos is None:
+        pos = [cfg.max_seq - 1] * cfg.batch
     rng = random.Random(seed)
     counters = np.zeros(len(totals), dtype=np.int64)
     errs: List[str] = []
@@ -520,6 +521,10 @@ def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, see
                     continue  # reached END
                 ok = all(((int(counters[c]) - (epoch * int(totals[c]) + need)) % U32) < (U32 >> 1)
                          for c, need in t.waits)
+                c_pos = pos[t.b] // t.a2 if t.op == ATTN else -1   # the chunk holding pos
+                part_key = ("part", t.layer, t.b, t.a0)
+                if ok and t.op == ATTN and t.a1 == c_pos:   # the combine reads chunks 0 .. c_pos - 1
+                    ok = written.get(part_key, 0) >= c_pos
                 if ok:
                     if track_data:
                         if t.tid not in rw_cache:
@@ -533,16 +538,13 @@ def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, see
                         for key, n in wr:
                             written[key] = written.get(key, 0) + n
                     pubs = t.pubs
-                    if t.arrive >= 0:
-                        counters[t.arrive] += 1
-                        last = ((int(counters[t.arrive]) - epoch * t.arrive_n) % U32) == t.arrive_n
-                        pubs = t.pubs if last else []
-                        if last and track_data:   # the last arriver combines the group's partials
-                            key = ("part", t.layer, t.b, t.a0)
-                            if written.get(key, 0) < t.arrive_n:
-                                errs.append(f"epoch {epoch}: combine of {key} before all chunks")
-                                return errs
+                    if t.op == ATTN:
+                        if t.a1 <= c_pos:
+                            written[part_key] = written.get(part_key, 0) + 1
+                        if t.a1 == c_pos:
                             written[("o", t.layer)] = written.get(("o", t.layer), 0) + 1
+                        else:
+                            pubs = []
                     for c, dl in pubs:
                         counters[c] += dl
                     pc[s] += 1

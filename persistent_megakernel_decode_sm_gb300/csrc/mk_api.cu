@@ -152,7 +152,7 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, std::
                 break;
             case OP_ATTN:
                 if (unsigned(a0) >= unsigned(nkv) || unsigned(a1) >= unsigned(g.n_chunk) || a2 != g.attn_chunk ||
-                    x[W_COND] != 1 || unsigned(x[W_ARRIVE]) >= unsigned(g.n_counters) || x[W_ARRIVE_N] != g.n_chunk)
+                    x[W_COND] != 1)
                     return bad("attention fields");
                 break;
             case OP_ARGMAX:
@@ -257,7 +257,8 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     asf = (asf + 3) & ~3;
     const int qrf = (hpg * d + 3) & ~3;
     int n_pages = 0;
-    while (int64_t(n_pages + 1) * g.page_bytes + smem_misc_bytes(n_pages + 1, asf, qrf, xbuf, comb_stride) <= optin)
+    while (n_pages < kMaxRingPages &&
+           int64_t(n_pages + 1) * g.page_bytes + smem_misc_bytes(n_pages + 1, asf, qrf, xbuf, comb_stride) <= optin)
         ++n_pages;
     if (n_pages < 1) return fail(MK_ERR_CAPACITY, "no room for a page ring");
     const int misc = smem_misc_bytes(n_pages, asf, qrf, xbuf, comb_stride);
@@ -354,7 +355,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     p.x_attn = reinterpret_cast<uint64_t*>(sb + sl.x_attn);
     p.x_out = reinterpret_cast<uint64_t*>(sb + sl.x_out);
     p.qkv = reinterpret_cast<uint64_t*>(sb + sl.qkv);
-    p.part = reinterpret_cast<float*>(sb + sl.part);
+    p.part = reinterpret_cast<uint64_t*>(sb + sl.part);
     p.o = reinterpret_cast<uint64_t*>(sb + sl.o);
     p.h = reinterpret_cast<uint32_t*>(sb + sl.h);
     p.lm_part = reinterpret_cast<int4*>(sb + sl.lm_part);

@@ -21,7 +21,7 @@ enum Op : int32_t { OP_END = 0, OP_QKV = 1, OP_ATTN = 2, OP_COMB = 3, OP_OPROJ =
 enum Word : int {
     W_OP = 0, W_LAYER = 1, W_B = 2, W_A0 = 3, W_A1 = 4, W_A2 = 5, W_NWAIT = 6, W_WAIT = 7,
     W_NPUB = 15, W_PUB = 16, W_NPAGES = 20, W_TILE = 21, W_WAVE = 22,
-    W_COND = 23, W_ARRIVE = 24, W_ARRIVE_N = 25,  // completions only from the last of N arrivals
+    W_COND = 23,   // 1: completions only from the tile that combines its group (ATTN: the chunk holding pos)
     W_SRC0 = 26, W_SRC1 = 28, W_BYTES0 = 30, W_BYTES1 = 31   // device copy: resolved weight stream (matvec)
 };
 constexpr int kWords = 32;
@@ -49,8 +49,9 @@ constexpr int kMaxCpl = 8;           // 16-byte chunks a lane holds of its row s
 constexpr int kMaxSeg = 8;           // row segments of a matvec (a power of two dividing the warp count)
 constexpr int kDirectMinK = 4097;    // rows this long take their input per warp, not through the shared buffer
 constexpr int kXChunks = 2;          // 8-element input chunks a consumer thread polls per round
+constexpr int kCombWords = 12;       // partial words a consumer thread polls per round of the attention combine
 constexpr int kResBuf = 64;          // residual words of a tile's rows staged in shared memory (per buffer)
-constexpr int kL2Ahead = 8;          // pages of a matvec stream warmed into L2 ahead of the ring copies
+constexpr int kMaxRingPages = 64;    // cap on the page ring's length (the shared memory sets the rest)
 constexpr int kMinXBuf = 3072;       // floats of the shared input buffer at least (attention scores, combine)
 constexpr int kAttnChunkTiles = 152; // default attention chunk: grown while a layer has more chunks
 
@@ -69,9 +70,8 @@ struct Geometry {
 struct CounterMap {
     int32_t L, nkv, B, base2;
     explicit CounterMap(const mk_model_cfg& c)
-        : L(c.n_layers), nkv(c.n_kv_heads), B(c.batch), base2(c.n_layers * c.n_kv_heads * (1 + c.batch)) {}
+        : L(c.n_layers), nkv(c.n_kv_heads), B(c.batch), base2(c.n_layers * c.n_kv_heads) {}
     int32_t qkv(int l, int g) const { return l * nkv + g; }
-    int32_t attn(int l, int b, int g) const { return L * nkv + (l * B + b) * nkv + g; }
     int32_t comb(int l) const { return base2 + l; }
     int32_t o(int l) const { return base2 + L + l; }
     int32_t up(int l) const { return base2 + 2 * L + l; }
@@ -104,7 +104,7 @@ inline ScratchLayout scratch_layout(const mk_model_cfg& c, const Geometry& g, in
     s.x_attn = take(L * B * H * 8);                   // tagged
     s.x_out = take(L * B * H * 8);                    // tagged
     s.qkv = take(L * B * (qd + 2 * kvd) * 8);         // tagged
-    s.part = take(L * B * size_t(c.n_kv_heads) * g.n_chunk * hpg * (d + 2) * 4);   // fp32 chunk partials
+    s.part = take(L * B * size_t(c.n_kv_heads) * g.n_chunk * hpg * (d + 2) * 8);   // tagged chunk partials
     s.o = take(L * B * qd * 8);                       // tagged
     s.h = take(L * B * size_t(c.ffn) * 4);            // fp32 with a 3-bit tag
     s.lm_part = take(B * size_t(S) * kNumConsumerWarps * 16);   // per (sequence, CTA, warp): max, index, epoch
@@ -184,7 +184,7 @@ struct Params {
     uint64_t* x_attn;   // tagged [L][B][H]: residual stream after attention
     uint64_t* x_out;    // tagged [L][B][H]: residual stream after the MLP
     uint64_t* qkv;      // tagged [L][B][nqkv]
-    float* part;        // [L][B][nkv][n_chunk][hpg][d + 2] attention chunk partials
+    uint64_t* part;     // [L][B][nkv][n_chunk][hpg][d + 2] attention chunk partials (tagged)
     uint64_t* o;        // tagged [L][B][qd]: attention output
     uint32_t* h;        // [L][B][F]: SwiGLU output, fp32 with a 3-bit step tag in the low mantissa bits
     int4* lm_part;      // [B][S][kNumConsumerWarps]: (max bits, index, epoch, 0)
@@ -252,8 +252,8 @@ MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qr
     m.pubinfo = take(4u * kDone * 8u, 16);            // completion words of in-flight instructions
     m.red = take(4u * 64u, 16);                     // argmax scratch [0..31]; abort flag [32], published count [33],
                                                     // stream bytes the loader has issued [34..35] (u64),
-                                                    // last-arrival flag [40], per-warp sums of
-                                                    // squares of the shared input [48..63]
+                                                    // stop flag [41],
+                                                    // per-warp sums of squares of the shared input [48..63]
     m.lmbest = take(8u * kNumConsumerWarps * kMaxBatch, 8);   // LM-head running (max, index) per warp / sequence
     m.qrot = take(4u * uint32_t(qrot_floats), 16);
     m.ascr = take(4u * uint32_t(attn_scratch_floats), 16);

@@ -89,10 +89,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
-// warms L2 with `bytes` (a multiple of 16) from global memory; no shared memory, no completion
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -573,21 +569,8 @@ __device__ void loader(const Params& p, const Shared& sh) {
             stamp(p, pc, 0);
             mbar_arrive(sh.ins_full + slot);   // release: the slot's words are visible to the consumers
             if (si.w[W_OP] == OP_END) break;
-            // a matvec stream is warmed into L2 kL2Ahead pages ahead of the copies into the ring: the
-            // ring's own depth then only has to cover the L2 -> shared memory hop
-            if (st.rows)
-                for (int pg = 0; pg < min(st.pages, kL2Ahead); ++pg) {
-                    uint32_t bytes;
-                    const uint8_t* psrc = mv_page(st, uint32_t(pg), bytes);
-                    prefetch_l2(psrc, bytes);
-                }
             for (int pg = 0; pg < st.pages; ++pg) {
                 const uint32_t ps = cur_slot;
-                if (st.rows && pg + kL2Ahead < st.pages) {
-                    uint32_t bytes;
-                    const uint8_t* psrc = mv_page(st, uint32_t(pg + kL2Ahead), bytes);
-                    prefetch_l2(psrc, bytes);
-                }
                 if (page_seq >= NP && !wait_bar(p, sh, sh.empty + ps, cur_phase ^ 1u, ROLE_LOADER, pc)) {
                     stop = true;
                     break;
@@ -918,6 +901,18 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
         if (rs.b) rb = bf16f(rs.b[tid]);
         else rw = ld_tag(rs.t + tid);
     }
+    // the RMSNorm gain of this warp's segment depends on nothing: it is loaded into registers
+    // before the poll, so its round trip overlaps the wait for the input (at 8 chunks per lane
+    // the registers are not there: the gain is loaded after the poll)
+    constexpr bool kGainEarly = CPL == 4;
+    uint4 gw[CPL];
+    if (kGainEarly && gain && !m.direct) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            const int ch = c.lane + 32 * i;
+            gw[i] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(gain + (cg0 + ch) * 8)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
     Spin sp;
     if (!m.direct) {
         // every chunk of this thread is loaded before any tag is checked: one round trip for a row
@@ -989,11 +984,11 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
                 const float4 b = *reinterpret_cast<const float4*>(c.sh.xbuf + cg * 8 + 4);
                 x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
                 if (gain) {
-                    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(gain + cg * 8));
-                    x[0] = (x[0] * scale) * bf_lo(gw.x); x[1] = (x[1] * scale) * bf_hi(gw.x);
-                    x[2] = (x[2] * scale) * bf_lo(gw.y); x[3] = (x[3] * scale) * bf_hi(gw.y);
-                    x[4] = (x[4] * scale) * bf_lo(gw.z); x[5] = (x[5] * scale) * bf_hi(gw.z);
-                    x[6] = (x[6] * scale) * bf_lo(gw.w); x[7] = (x[7] * scale) * bf_hi(gw.w);
+                    if (!kGainEarly) gw[i] = __ldg(reinterpret_cast<const uint4*>(gain + cg * 8));
+                    x[0] = (x[0] * scale) * bf_lo(gw[i].x); x[1] = (x[1] * scale) * bf_hi(gw[i].x);
+                    x[2] = (x[2] * scale) * bf_lo(gw[i].y); x[3] = (x[3] * scale) * bf_hi(gw[i].y);
+                    x[4] = (x[4] * scale) * bf_lo(gw[i].z); x[5] = (x[5] * scale) * bf_hi(gw[i].z);
+                    x[6] = (x[6] * scale) * bf_lo(gw[i].w); x[7] = (x[7] * scale) * bf_hi(gw[i].w);
                 }
             } else {
 #pragma unroll
@@ -1375,10 +1370,8 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
     const uint64_t* qkv = p.qkv + lb * p.nqkv;
     // [hpg][C] scores in the shared-x buffer: no warp reads a matvec input while the tile runs
     // (every warp passed its previous instruction at the first barrier, and the next
-    // instruction's input is written only after the arrival barrier below); [hpg][n_chunk]
-    // combine factors in the attention scratch
+    // instruction's input is written only after the barrier that ends the chunk's work below)
     float* sc = c.sh.xbuf;
-    float* cf = c.sh.ascr;
     if (n_old >= 0) {
         const int pos = p.pos[b] + c.step;
         const bool has_new = pos < ch * C + C;
@@ -1429,7 +1422,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         }
         if (!wait_pages(c, si, pc)) return false;
         if (!cbar(c, pc)) return false;
-        const uint32_t first_slot = uint32_t(si.first_slot);
+            const uint32_t first_slot = uint32_t(si.first_slot);
         const uint32_t rowb = uint32_t(d) * 2u;
         const uint32_t voff = uint32_t(n_old) * rowb;
         const uint32_t kbytes = voff;
@@ -1461,7 +1454,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         }
         if (!cbar(c, pc)) return false;
         // 4. o[h][e] = sum_t w_t v_t[e]
-        float* dst = p.part + ((lb * p.nkv + g) * p.n_chunk + ch) * size_t(hpg) * (d + 2);
+        uint64_t* dst = p.part + ((lb * p.nkv + g) * p.n_chunk + ch) * size_t(hpg) * (d + 2);
         for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
             const int h = idx / d, e = idx % d;
             const float* wts = sc + h * C;
@@ -1480,71 +1473,82 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
             }
             float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
             if (has_new) acc = fmaf(wts[n_old], bf16f(c.sh.vnew[e]), acc);
-            float* dh = dst + size_t(h) * (d + 2);
-            dh[e] = acc;
-            if (e == 0) { dh[d] = c.sh.ml[2 * h]; dh[d + 1] = c.sh.ml[2 * h + 1]; }
+            uint64_t* dh = dst + size_t(h) * (d + 2);
+            st_tag(dh + e, acc, c.tag);
+            if (e == 0) {
+                st_tag(dh + d, c.sh.ml[2 * h], c.tag);
+                st_tag(dh + d + 1, c.sh.ml[2 * h + 1], c.tag);
+            }
         }
         release_pages(c, si);
     }
-    // 5. arrive on the group; the last arrival combines M = max_c m_c, f_c = exp(m_c - M),
-    //    L = sum_c f_c l_c, o = sum_c f_c o_c / L over the active chunks, in chunk order
-    if (!cbar(c, pc)) return false;   // every thread's partial is written (CTA scope) before the release
-    if (tid == 0) {
-        const uint32_t nch = uint32_t(si.w[W_ARRIVE_N]);
-        const uint32_t old = atom_add_acq_rel_gpu(p.counters + si.w[W_ARRIVE], 1u);
-        const bool last = old - c.epoch * nch == nch - 1u;
-        reinterpret_cast<volatile int*>(c.sh.red)[40] = last ? 1 : 0;
-        if (last) c.sh.pubinfo[(pc % kDone) * 8 + 7] = 1;   // fire this tile's completion
-    }
+    // 5. the tile of the chunk that holds pos combines the group's active partials in chunk order:
+    //    M = max_c m_c, f_c = exp(m_c - M), L = sum_c f_c l_c, o = sum_c f_c o_c / L.  The
+    //    partials are tagged, so the combining tile polls them straight from the other tiles'
+    //    writes (no arrival counter, no second round trip); the barrier first also frees the
+    //    scores buffer and the new k/v for what follows.
     if (!cbar(c, pc)) return false;
-    if (!reinterpret_cast<volatile int*>(c.sh.red)[40]) return true;
     const int nact = min(p.n_chunk, (p.pos[b] + c.step) / C + 1);
-    const float* pbase = p.part + (lb * p.nkv + g) * size_t(p.n_chunk) * hpg * (d + 2);
-    // the group's active partials are one contiguous block; when it fits the shared input buffer
-    // (free during attention: the tile began with every warp past its previous input) it is staged
-    // there in one round trip, and the combine below reads shared memory
-    const int blk = nact * hpg * (d + 2);
-    const float* pb = pbase;
-    if (blk <= p.xbuf_floats) {
-        float* stage = c.sh.xbuf;
-        for (int i = tid; i < blk; i += kConsumerThreads) stage[i] = __ldcg(pbase + i);
-        if (!cbar(c, pc)) return false;
-        pb = stage;
-    }
-    if (c.warp < hpg) {
-        const int h = c.warp;
-        float M = -INFINITY;
-#pragma unroll 1
-        for (int k = c.lane; k < nact; k += 32) M = fmaxf(M, pb[(size_t(k) * hpg + h) * (d + 2) + d]);
-        M = warp_max(M);
-        float Ls = 0.f;
-#pragma unroll 1
-        for (int k = c.lane; k < nact; k += 32) {
-            const float* ph = pb + (size_t(k) * hpg + h) * (d + 2);
-            const float f = expf(ph[d] - M);
-            cf[h * p.n_chunk + k] = f;
-            Ls = fmaf(f, ph[d + 1], Ls);
-        }
-        Ls = warp_sum(Ls);
-        if (c.lane == 0) c.sh.cml[h] = Ls;
-    }
-    if (!cbar(c, pc)) return false;
-    uint64_t* out = p.o + lb * p.qd + size_t(g) * hpg * d;
-    for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
-        const int h = idx / d, e = idx % d;
-        const float* f = cf + h * p.n_chunk;
-        const float* ph = pb + size_t(h) * (d + 2) + e;
-        const size_t cs = size_t(hpg) * (d + 2);   // stride of one chunk's partials
-        float a4[4] = {0.f, 0.f, 0.f, 0.f};
-        int k = 0;
-        for (; k + 4 <= nact; k += 4)
+    if (ch != nact - 1) return true;
+    if (tid == 0) c.sh.pubinfo[(pc % kDone) * 8 + 7] = 1;   // this tile alone fires the completion
+    const int per = hpg * (d + 2);   // words of one chunk's partial
+    const uint64_t* pbase = p.part + (lb * p.nkv + g) * size_t(p.n_chunk) * per;
+    // chunks staged at a time in the shared-x buffer (free: every warp is past its last input);
+    // with more active chunks the combine runs over groups of them, rescaling the running sums by
+    // exp(M_old - M_new) (0 before the first group)
+    const int kg = (kCombWords * kConsumerThreads) / per;
+    float* stage = c.sh.xbuf;
+    constexpr int kOut = kMaxHpg * kMaxHeadDim / kConsumerThreads;   // outputs per thread at most
+    float Mr[kOut], Lr[kOut], Ar[kOut];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) a4[r] = fmaf(f[k + r], ph[(k + r) * cs], a4[r]);
-        for (; k < nact; ++k) a4[k & 3] = fmaf(f[k], ph[k * cs], a4[k & 3]);
-        st_tag(out + idx, ((a4[0] + a4[1]) + (a4[2] + a4[3])) / c.sh.cml[h], c.tag);
+    for (int j = 0; j < kOut; ++j) { Mr[j] = -INFINITY; Lr[j] = 0.f; Ar[j] = 0.f; }
+    for (int k0 = 0; k0 < nact; k0 += kg) {
+        const int items = min(kg, nact - k0) * per;
+        const uint64_t* src = pbase + size_t(k0) * per;
+        Spin sp;
+        while (true) {   // every word of this thread loaded before any tag is checked
+            bool ok = true;
+#pragma unroll
+            for (int j = 0; j < kCombWords; ++j) {
+                const int i = tid + j * kConsumerThreads;
+                if (i < items) {
+                    const uint64_t w = ld_tag(src + i);
+                    stage[i] = tag_val(w);   // (rewritten by the next round if a tag was stale)
+                    ok &= tag_of(w) == c.tag;
+                }
+            }
+            if (__all_sync(0xFFFFFFFFu, ok)) break;
+            if (!spin_more(c, sp, pc)) return false;
+        }
+        if (!cbar(c, pc)) return false;
+            const int kn = items / per;
+#pragma unroll
+        for (int j = 0; j < kOut; ++j) {
+            const int idx = tid + j * kConsumerThreads;
+            if (idx >= hpg * d) break;
+            const int h = idx / d, e = idx % d;
+            const float* ph = stage + h * (d + 2);
+            float M = Mr[j];
+            for (int k = 0; k < kn; ++k) M = fmaxf(M, ph[k * per + d]);
+            const float r = expf(Mr[j] - M);
+            float Ls = Lr[j] * r, A = Ar[j] * r;
+            for (int k = 0; k < kn; ++k) {
+                const float f = expf(ph[k * per + d] - M);
+                Ls = fmaf(f, ph[k * per + d + 1], Ls);
+                A = fmaf(f, ph[k * per + e], A);
+            }
+            Mr[j] = M;
+            Lr[j] = Ls;
+            Ar[j] = A;
+        }
+        if (!cbar(c, pc)) return false;   // the stage is refilled next (next group, next input)
     }
-    // staged: no warp may refill the shared-x buffer (next instruction) while others still read it
-    if (pb != pbase && !cbar(c, pc)) return false;
+    uint64_t* out = p.o + lb * p.qd + size_t(g) * hpg * d;
+#pragma unroll
+    for (int j = 0; j < kOut; ++j) {
+        const int idx = tid + j * kConsumerThreads;
+        if (idx < hpg * d) st_tag(out + idx, Ar[j] / Lr[j], c.tag);
+    }
     return true;
 }
 
@@ -1689,19 +1693,10 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
             const SlotInfo& si = sh.slots[slot];
             const int op = si.w[W_OP];
             if (op != OP_END) {
-                // the RMSNorm gain of a new input depends on no counter: start fetching it into L1
-                // before waiting, so the normalisation after the wait does not pay a second round trip
-                const uint16_t* gain = op == OP_QKV ? sh.layers[si.w[W_LAYER]].attn_norm
-                                     : op == OP_UPGATE ? sh.layers[si.w[W_LAYER]].mlp_norm
-                                     : op == OP_LMHEAD ? p.final_norm : nullptr;
-                if (gain && c.lane * 64 < p.H * 2)
-                    for (int off = c.lane * 64; off < p.H * 2; off += 32 * 64)
-                        asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(gain) + off));
-                // counters (with acquire semantics) in the counters mode and for the consumers that read
-                // their inputs without tags (the argmax over the LM-head partials, the MLP down
-                // projection's SwiGLU input, matvecs whose rows are cut into segments); every other
-                // consumer polls the tagged words it reads until they carry this step's tag, with no
-                // counter in between: a counter poll before the data read would add a round trip
+                // counters (with acquire semantics) in the counters mode and for the one consumer
+                // that reads its inputs without tags (the argmax over the LM-head partials); every
+                // other consumer polls the tagged words it reads until they carry this step's tag,
+                // with no counter in between: a counter poll before the data read would add a round trip
                 int ok = 1;
                 if (c.lane == 0 && (p.sync_counters || ((p.acquire_ops >> op) & 1)))
                     ok = wait_counters(p, sh, si.w, pc, cc, c.epoch);

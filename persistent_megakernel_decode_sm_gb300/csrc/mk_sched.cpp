@@ -8,14 +8,16 @@
 // kernel (the page's object table gives the queue only as an int32 tensor of shape [S, Q, 32]).
 // The page fixes none of the concrete rules; this file states them:
 //  * tiles per layer: QKV row tiles (<= head_dim rows: a tile touches one or two KV groups and
-//    completes each), attention chunks (sequence, group, chunk of attn_chunk positions),
-//    combine per (sequence, group), O row tiles, gate/up row-pair tiles, down row tiles; then
+//    completes each), attention chunks (sequence, group, chunk of attn_chunk positions), O row
+//    tiles, gate/up row-pair tiles, down row tiles; then
 //    LM-head row tiles and one argmax per sequence;
 //  * DAG: a consumer waits on one counter per producer set -- QKV(l) on down(l-1), attention
 //    chunks of group g on the QKV tiles of group g, O on the combined attention of every group,
 //    up/gate on O, down on up/gate, LM head on the last layer's down, argmax on the LM head.
-//    The combine of a group's chunk partials is done by the chunk tile that arrives last on the
-//    group's arrival counter, which alone carries the completion O waits on;
+//    The combine of a group's chunk partials is done by the chunk tile that holds the step's
+//    position (known only at run time), which alone carries the completion O waits on; it reads
+//    the other chunks' tagged partials as they land (a wait inside the wave, on tiles of lower
+//    id, which every queue runs first);
 //  * waves = longest-path level (5 per layer, then LM head, then argmax); the waits of a tile
 //    point only at lower waves (forward-progress contract);
 //  * pools: memory = tiles that stream weights or KV, compute = argmax; within a wave memory
@@ -26,7 +28,8 @@
 //    Fisher-Yates order when shuffle_seed != 0 -- each to the queue with the smallest
 //    accumulated cost (ties to the lowest SM) among the queues holding fewer than ceil(n / S)
 //    of the wave's n tiles of that pool, the accumulated cost carried across waves;
-//    cost = streamed bytes + a fixed per-tile overhead.
+//    cost = streamed bytes + a fixed per-tile overhead.  Each queue then runs its tiles of a wave
+//    in id order (so a wait inside a wave is always on tiles that every queue runs earlier).
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
@@ -61,7 +64,7 @@ struct Tile {
     int32_t pub[kMaxPub][2];
     int64_t stream_bytes;
     int32_t id;
-    int32_t arrive, arrive_n;   // ATTN: arrival counter and arrivals per group (-1: none)
+    bool cond;   // ATTN: completions only from the tile that combines its group
     bool memory() const { return op != OP_ARGMAX; }
     int64_t cost() const { return stream_bytes + kTileOverhead; }
 };
@@ -184,7 +187,7 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
 
     // ---- tiles in enumeration order (ids) ------------------------------------------------
     std::vector<Tile> tiles;
-    tiles.reserve(size_t(L) * (g.n_qkv + B * nkv * (g.n_chunk + 1) + g.n_o + g.n_up + g.n_dn) + g.n_lm + B);
+    tiles.reserve(size_t(L) * (g.n_qkv + B * nkv * g.n_chunk + g.n_o + g.n_up + g.n_dn) + g.n_lm + B);
     auto add = [&](int32_t op, int32_t layer, int32_t b, int32_t a0, int32_t a1, int32_t a2, int32_t wave,
                    std::initializer_list<std::pair<int32_t, int32_t>> waits,
                    std::pair<int32_t, int32_t> pub, int64_t bytes) {
@@ -193,8 +196,7 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         for (auto& w : waits) { t.wait[t.nwait][0] = w.first; t.wait[t.nwait][1] = w.second; ++t.nwait; }
         t.pub[0][0] = pub.first; t.pub[0][1] = pub.second; t.npub = 1;
         t.stream_bytes = bytes;
-        t.arrive = -1;
-        t.arrive_n = 0;
+        t.cond = false;
         t.id = int32_t(tiles.size());
         tiles.push_back(t);
     };
@@ -233,8 +235,7 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
                 for (int32_t ch = 0; ch < g.n_chunk; ++ch) {
                     add(OP_ATTN, l, b, gr, ch, g.attn_chunk, 5 * l + 1, {{cm.qkv(l, gr), qkv_tiles_of_group[gr]}},
                         {cm.comb(l), 1}, int64_t(2) * g.attn_chunk * d * 2);
-                    tiles.back().arrive = cm.attn(l, b, gr);
-                    tiles.back().arrive_n = g.n_chunk;
+                    tiles.back().cond = true;
                 }
         for (int32_t t = 0; t < g.n_o; ++t) {
             int32_t r0 = t * g.r_o, n = std::min(g.r_o, H - r0);
@@ -285,6 +286,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         };
         order(mem);
         order(cmp);
+        std::vector<size_t> start(S);
+        for (int32_t s = 0; s < S; ++s) start[s] = per_sm[s].size();
         for (auto* v : {&mem, &cmp}) {
             const int32_t cap = cdiv(int64_t(v->size()), S);
             std::fill(in_wave.begin(), in_wave.end(), 0);
@@ -297,6 +300,7 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
                 ++in_wave[best];
             }
         }
+        for (int32_t s = 0; s < S; ++s) std::sort(per_sm[s].begin() + ptrdiff_t(start[s]), per_sm[s].end());
         i = j;
     }
 
@@ -333,14 +337,11 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
             w[W_NPAGES] = int32_t(pages);
             w[W_TILE] = t.id;
             w[W_WAVE] = t.wave;
-            if (t.arrive >= 0) { w[W_COND] = 1; w[W_ARRIVE] = t.arrive; w[W_ARRIVE_N] = t.arrive_n; }
+            if (t.cond) w[W_COND] = 1;
             sch->max_pages = std::max(sch->max_pages, int32_t(pages));
         }
     for (const Tile& t : tiles) {
-        if (t.arrive >= 0) {
-            sch->totals[t.arrive] += 1u;                      // every chunk tile arrives once
-            if (t.a1 != t.arrive_n - 1) continue;             // the group's completion counts once
-        }
+        if (t.cond && t.a1 != 0) continue;   // one completion per group (from its combining tile)
         for (int q = 0; q < t.npub; ++q) sch->totals[t.pub[q][0]] += uint32_t(t.pub[q][1]);
     }
 

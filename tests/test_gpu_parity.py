@@ -84,13 +84,15 @@ def _llama1b_outputs(name, s_count, seed, steps):
     return out
 
 
-@pytest.mark.parametrize("S_div,shuffle", [(2, 0), (0, 0), (1, 7)])
-def test_llama1b_bit_identical_across_sm_counts(S_div, shuffle):
+@pytest.mark.parametrize("S_spec,shuffle", [("half", 0), ("37", 0), ("full", 7), ("8", 11)])
+def test_llama1b_bit_identical_across_sm_counts(S_spec, shuffle):
     # the full-size paths: two segments per row (the segment sums meet in shared memory), the
     # MLP down projection's eight-segment rows polled per warp, ten-chunk attention groups combined
-    # in chunk order -- identical logits and caches whatever the SM count and placement
+    # in chunk order -- identical logits and caches whatever the SM count and placement (at 8
+    # queues, shuffled, every queue holds about ten attention chunk tiles of a layer, and the
+    # combining tile waits inside the wave for chunks that other queues run)
     full = mk.device_sm_count()
-    S = 37 if S_div == 0 else full // S_div
+    S = {"half": full // 2, "37": 37, "full": full, "8": 8}[S_spec]
     ref = _llama1b_outputs("llama1b_ctx512", full, 0, 2)
     got = _llama1b_outputs("llama1b_ctx512", S, shuffle, 2)
     for a, b in zip(got, ref):

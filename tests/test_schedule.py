@@ -130,8 +130,8 @@ def test_counter_totals_match_waits():
     q, t, info = sr.build_schedule(cfg, 152)
     cnt = info["counters"]
     L, B, nkv = cfg.n_layers, cfg.batch, cfg.n_kv_heads
-    assert t[cnt.comb(3)] == B * nkv
-    assert t[cnt.attn(2, 0, 1)] == info["n_chunks"]
+    assert t[cnt.comb(3)] == B * nkv   # one completion per (sequence, KV group)
+    assert len(t) == L * nkv + 4 * L + 2
     assert t[cnt.lm()] == -(-cfg.vocab // info["rows"]["lm"])
     assert t[cnt.final()] == B
 
@@ -161,3 +161,40 @@ def test_random_small_configs_bit_exact_valid_and_deadlock_free():
         assert sr.simulate(q, t, cfg, n_epochs=1, seed=checked) == [], cfg
         checked += 1
     assert checked >= 40
+
+
+def test_queues_run_each_wave_in_tile_id_order_also_when_shuffled():
+    cfg = get_workload("llama1b_ctx512").cfg
+    for seed in (0, 7):
+        q, t, _ = sr.build_schedule(cfg, 5, sr.SchedOpts(shuffle_seed=seed))
+        for s in range(q.shape[0]):
+            live = [w for w in q[s] if w[0] != sr.END]
+            keys = [(int(w[22]), int(w[21])) for w in live]
+            assert keys == sorted(keys)
+
+
+@pytest.mark.parametrize("pos", [0, 63, 64, 300, 639])
+def test_combining_tile_waits_inside_its_wave_without_deadlock(pos):
+    """Five queues hold many attention chunk tiles each; the tile of the chunk holding pos waits
+    for the lower chunks of its group inside the wave -- at every position and under shuffled
+    placement the simulator completes two steps."""
+    cfg = get_workload("llama1b_ctx512").cfg
+    for seed in (0, 3):
+        q, t, _ = sr.build_schedule(cfg, 5, sr.SchedOpts(shuffle_seed=seed))
+        assert sr.simulate(q, t, cfg, n_epochs=2, seed=seed, pos=[pos]) == []
+
+
+def test_combining_tile_ahead_of_a_lower_chunk_deadlocks_and_is_rejected():
+    """Planted: on one queue a group's chunk-9 tile moved ahead of its chunk-3 tile (same wave).
+    The validator flags the order and the simulator, decoding position 639 (chunk 9 combines),
+    reports the deadlock."""
+    cfg = get_workload("llama1b_ctx512").cfg
+    q, t, _ = sr.build_schedule(cfg, 1)
+    live = [i for i in range(q.shape[1]) if q[0, i, 0] == sr.ATTN and q[0, i, 1] == 0 and q[0, i, 3] == 0]
+    i3 = next(i for i in live if q[0, i, 4] == 3)
+    i9 = next(i for i in live if q[0, i, 4] == 9)
+    bad = q.copy()
+    bad[0, [i3, i9]] = bad[0, [i9, i3]]
+    assert any("same wave" in e for e in sr.validate(bad, t, cfg))
+    assert any("deadlock" in e for e in sr.simulate(bad, t, cfg, n_epochs=1, pos=[639]))
+    assert sr.simulate(q, t, cfg, n_epochs=1, pos=[639]) == []
