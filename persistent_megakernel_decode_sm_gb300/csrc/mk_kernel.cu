@@ -1422,7 +1422,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         }
         if (!wait_pages(c, si, pc)) return false;
         if (!cbar(c, pc)) return false;
-            const uint32_t first_slot = uint32_t(si.first_slot);
+        const uint32_t first_slot = uint32_t(si.first_slot);
         const uint32_t rowb = uint32_t(d) * 2u;
         const uint32_t voff = uint32_t(n_old) * rowb;
         const uint32_t kbytes = voff;
@@ -1521,7 +1521,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
             if (!spin_more(c, sp, pc)) return false;
         }
         if (!cbar(c, pc)) return false;
-            const int kn = items / per;
+        const int kn = items / per;
 #pragma unroll
         for (int j = 0; j < kOut; ++j) {
             const int idx = tid + j * kConsumerThreads;

@@ -97,8 +97,9 @@ mk_status check_cfg(const mk_model_cfg& c) {
     if (c.n_q_heads % c.n_kv_heads) return fail(MK_ERR_ARG, "n_q_heads %% n_kv_heads != 0");
     if (c.n_q_heads / c.n_kv_heads > kMaxHpg)
         return fail(MK_ERR_ARG, "more than %d query heads per KV head", kMaxHpg);
-    if (c.head_dim % 16 || c.head_dim > kMaxHeadDim)
-        return fail(MK_ERR_ARG, "head_dim must be a multiple of 16 and <= %d", kMaxHeadDim);
+    // (the attention reduces a K row over head_dim / 8 lanes with butterfly shuffles: a power of two)
+    if ((c.head_dim != 32 && c.head_dim != 64 && c.head_dim != 128) || c.head_dim > kMaxHeadDim)
+        return fail(MK_ERR_ARG, "head_dim must be 32, 64 or 128");
     const int64_t qd = int64_t(c.n_q_heads) * c.head_dim;
     if (c.hidden % 8 || c.ffn % 8 || qd % 8 || c.hidden > kMaxK || c.ffn > kMaxK || qd > kMaxK)
         return fail(MK_ERR_ARG, "hidden, ffn and n_q_heads*head_dim must be multiples of 8 and <= %d",
