@@ -3,7 +3,8 @@
 Three translation units compiled in parallel and linked into one shared library:
   csrc/mk_sched.cpp  host scheduler
   csrc/mk_api.cu     binding, launch and status (host)
-  csrc/mk_kernel.cu  the persistent megakernel and the RoPE table kernel (device)
+  csrc/mk_kernel.cu  the persistent megakernel (batch-1 instances) and the RoPE table kernel (device)
+  csrc/mk_kernel_batch.cu  the batch > 1 instance of the same kernel source (tensor-core matvec tiles)
 """
 from __future__ import annotations
 
@@ -19,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libmk.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["mk_sched.cpp", "mk_api.cu", "mk_kernel.cu"]
+SOURCES = ["mk_sched.cpp", "mk_api.cu", "mk_kernel.cu", "mk_kernel_batch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

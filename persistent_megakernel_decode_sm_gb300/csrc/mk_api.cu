@@ -26,6 +26,9 @@ namespace mk {
 const void* megakernel_fn(int cpl);
 cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st);
 }  // namespace mk
+namespace mk_bat {
+const void* megakernel_fn_batched();   // (mk_kernel_batch.cu: the same kernel source, batch > 1)
+}
 
 using namespace mk;
 
@@ -234,7 +237,14 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     if (s->S > sms) return fail(MK_ERR_RESOURCES, "schedule has %d queues but the device has %d SMs", s->S, sms);
     // shared input buffer: the hidden size (the normed inputs) and at least kMinXBuf floats (the
     // attention's scores and combine); matvec inputs longer than it are polled per warp
-    const int xbuf = std::max(kMinXBuf, H);
+    int xbuf = std::max(kMinXBuf, H);
+    if (c.batch > 1) {   // every sequence's staged inputs for one range of positions, then the partials
+        if (H > kMmvRange)
+            return fail(MK_ERR_ARG, "batch > 1 needs hidden <= %d (the RMSNorm inputs are staged in one range)", kMmvRange);
+        const int kmx = std::max(H, std::max(qd, c.ffn));
+        const uint32_t stage = uint32_t(c.batch) * mmv_row_stride(std::min(kmx, kMmvRange));
+        xbuf = std::max(xbuf, int((stage + kMmvPartBytes) / 4u));
+    }
     if (hpg * g.attn_chunk > xbuf)
         return fail(MK_ERR_ARG, "attn_chunk %d: the scores of %d heads do not fit %d floats", g.attn_chunk, hpg, xbuf);
     // matvec shapes: whole rows per page, segments per row (a property of the row length only)
@@ -252,7 +262,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
             return fail(MK_ERR_ARG, "matvec row length %d cannot be cut into %d segments", K, kMaxSeg);
         comb_stride = std::max(comb_stride, mv[op].rpp * mv[op].G);   // (row, segment) units of a page
     }
-    const void* fn = megakernel_fn(cpl);
+    const void* fn = c.batch > 1 ? mk_bat::megakernel_fn_batched() : megakernel_fn(cpl);
     int asf = hpg * g.n_chunk;
     asf = (asf + 3) & ~3;
     const int qrf = (hpg * d + 3) & ~3;

@@ -265,6 +265,17 @@ MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qr
     return m;
 }
 
+// Batch > 1 matvec inputs staged in shared memory, one range of at most kMmvRange positions at a
+// time: per sequence a row of mmv_row_stride(range) bytes holding a 32-bit word per position
+// (fp32 as polled, then a bf16 (hi, lo) pair), rounded to 128 bytes plus 64 (consecutive
+// sequences' rows then start 64 bytes apart in the banks); after the rows, the partial sums of two
+// 16-row blocks from the 8 consumer warps.  A thread polls at most kMmvItems 8-element chunks of
+// a range per round.
+constexpr int kMmvRange = 2048;
+constexpr int kMmvItems = 8;
+MK_HD inline uint32_t mmv_row_stride(int K) { return ((uint32_t((K + 31) / 32) * 128u + 127u) & ~127u) + 64u; }
+constexpr uint32_t kMmvPartBytes = 2u * kNumConsumerWarps * 16u * 8u * 4u;
+
 inline int smem_misc_bytes(int n_pages, int attn_scratch_floats, int qrot_floats, int xbuf_floats, int comb_stride) {
     return int(misc_layout(n_pages, attn_scratch_floats, qrot_floats, xbuf_floats, comb_stride).total);
 }

@@ -1004,6 +1004,7 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
 
 // Output of one matvec row (tile row ru, run by one lane).  The LM head keeps this lane's running
 // (max, lowest index) in bv / bi.
+template <bool RES = true>   // RES: residuals of rows below kResBuf are in res (batch 1)
 __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int pc, int b, int ru, float s0,
                                             float s1, const float* res, float& bv, int& bi) {
     const Params& p = c.p;
@@ -1013,7 +1014,7 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
     switch (op) {
         case OP_QKV: st_tag(p.qkv + lb * p.nqkv + row, s0, c.tag); break;
         case OP_OPROJ: {
-            const float r = ru < kResBuf ? res[ru]
+            const float r = (RES && ru < kResBuf) ? res[ru]
                           : (l == 0) ? bf16f(p.embed[size_t(step_token(c, b)) * p.H + row])
                                      : poll1(p, c.sh, p.x_out + (lb - p.B) * p.H + row, pc, c.tag);
             st_tag(p.x_attn + lb * p.H + row, r + s0, c.tag);
@@ -1021,7 +1022,7 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
         }
         case OP_UPGATE: st_htag(p.h + lb * p.F + row, __fdividef(s0, 1.0f + __expf(-s0)) * s1, htag(c.tag)); break;
         case OP_DOWN: {
-            const float r = ru < kResBuf ? res[ru] : poll1(p, c.sh, p.x_attn + lb * p.H + row, pc, c.tag);
+            const float r = (RES && ru < kResBuf) ? res[ru] : poll1(p, c.sh, p.x_attn + lb * p.H + row, pc, c.tag);
             st_tag(p.x_out + lb * p.H + row, r + s0, c.tag);
             break;
         }
@@ -1094,6 +1095,263 @@ __device__ bool finish_group(const Cw& c, const SlotInfo& si, int pc, int b, con
     group_epilogue(c, si, pc, b, gr, res, bv, bi);
     __syncwarp();
     if (c.lane == 0) *cnt = 0;   // (seen by the slot's next use of this phase through the ring's mbarriers)
+    return true;
+}
+
+// ------------------------------------------------------------------- batch > 1 matvec ------
+// A batch > 1 matvec tile is one contraction of the tile's rows with the batch's input vectors on
+// the tensor cores: mma.sync m16n8k16, bf16 operands, fp32 accumulation, the sequences as the
+// 8 columns.  Each input element is split as hi = bf16(x), lo = bf16(x - hi); the weights are
+// bf16 already, so W x = W hi + W lo keeps the input to about 16 mantissa bits.  The row length
+// is taken in ranges of up to kMmvRange positions: the inputs of every sequence for one range are
+// staged in shared memory once per tile (fp32 as polled, then turned in place into (hi, lo) word
+// pairs, normalised for the RMSNorm operators), and the products of the range are added into
+// accumulators that persist over the ranges.  The tile's pages hold whole rows and stay leased
+// for the tile.  An MMA takes 16 rows -- row r of the first page of a pair of pages and row r of
+// the second (for gate/up: the gate row and the up row) -- over 16 positions; one 16-byte load per
+// row and lane covers two MMAs, the same positions for every row and for the inputs.  Warp w takes
+// the 32-position steps w, w + 8, ... of each range; the 8 warps' sums meet in shared memory and
+// are added in warp order.
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float e0, float e1) {   // e0 in the low half
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(e1), "f"(e0));
+    return d;
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// where sequence b's input of a matvec operator comes from (and its RMSNorm gain)
+__device__ __forceinline__ XSrc mmv_src(const Cw& c, int op, int l, int b, const uint16_t*& gain) {
+    const Params& p = c.p;
+    XSrc src{nullptr, nullptr, nullptr};
+    const size_t lb = size_t(l) * p.B + b;
+    gain = nullptr;
+    switch (op) {
+        case OP_QKV:
+            gain = c.sh.layers[l].attn_norm;
+            if (l == 0) src.b = p.embed + size_t(step_token(c, b)) * p.H;
+            else src.t = p.x_out + (lb - p.B) * p.H;
+            break;
+        case OP_OPROJ: src.t = p.o + lb * p.qd; break;
+        case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; src.t = p.x_attn + lb * p.H; break;
+        case OP_DOWN: src.h = p.h + lb * p.F; break;
+        default: gain = p.final_norm; src.t = p.x_out + (size_t(p.L - 1) * p.B + b) * p.H; break;
+    }
+    return src;
+}
+
+// The 32-position steps of one row block pair (two 16-row blocks, 4 accumulator chains) over the
+// staged range: positions [k0, k0 + kr) of the rows, [0, kr) of the staged inputs.
+struct MmvBlk {
+    uint32_t a0, a1;   // shared addresses of this lane's rows (g, g + 8) at position 0
+    bool v0, v1;
+};
+__device__ __forceinline__ void mmv_steps(const Cw& c, const MmvBlk (&bk)[2], int nb, uint32_t xrow, int k0, int kr,
+                                          float (&acc)[2][2][4]) {
+    const int t4 = c.lane & 3;
+    const int npr = (kr + 31) / 32;
+    for (int pr = c.warp; pr < npr; pr += kNumConsumerWarps) {
+        const int kl = pr * 32 + 8 * t4;   // position within the range
+        const bool kv = kl < kr;           // (only a range's last 32-step can be short: zeros past it;
+                                           // every lane still takes part in the MMAs)
+        const uint32_t ka = uint32_t(k0 + kl) * 2u;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 x0 = kv ? lds128(xrow + uint32_t(kl) * 4u) : z, x1 = kv ? lds128(xrow + uint32_t(kl) * 4u + 16u) : z;
+        // staged words: hi in the low half, lo in the high half
+        const uint32_t h0 = __byte_perm(x0.x, x0.y, 0x5410), h1 = __byte_perm(x0.z, x0.w, 0x5410);
+        const uint32_t h2 = __byte_perm(x1.x, x1.y, 0x5410), h3 = __byte_perm(x1.z, x1.w, 0x5410);
+        const uint32_t l0 = __byte_perm(x0.x, x0.y, 0x7632), l1 = __byte_perm(x0.z, x0.w, 0x7632);
+        const uint32_t l2 = __byte_perm(x1.x, x1.y, 0x7632), l3 = __byte_perm(x1.z, x1.w, 0x7632);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            if (q >= nb) break;
+            const uint4 A0 = (kv && bk[q].v0) ? lds128(bk[q].a0 + ka) : z;
+            const uint4 A1 = (kv && bk[q].v1) ? lds128(bk[q].a1 + ka) : z;
+            mma16816(acc[q][0], A0.x, A1.x, A0.y, A1.y, h0, h1);
+            mma16816(acc[q][1], A0.x, A1.x, A0.y, A1.y, l0, l1);
+            mma16816(acc[q][0], A0.z, A1.z, A0.w, A1.w, h2, h3);
+            mma16816(acc[q][1], A0.z, A1.z, A0.w, A1.w, l2, l3);
+        }
+    }
+}
+
+__device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
+    const Params& p = c.p;
+    const MvShape& m = si.mv;
+    const int op = si.w[W_OP], l = si.w[W_LAYER];
+    const bool pair = si.inter != 0;
+    const int K = m.K, R = si.rows, rpp = m.rpp, B = p.B;
+    const int tid = c.warp * 32 + c.lane, g = c.lane >> 2, t4 = c.lane & 3;
+    const int KR = min(K, kMmvRange), RS = int(mmv_row_stride(KR));
+    uint8_t* stage = reinterpret_cast<uint8_t*>(c.sh.xbuf);
+    float* part = reinterpret_cast<float*>(stage + uint32_t(p.xbuf_floats) * 4u - kMmvPartBytes);
+    const uint32_t stage_s = smem_u32(stage), ring_base = smem_u32(c.sh.ring);
+    const int npg = si.n_pages, nsb = (rpp + 7) / 8, nblk = ((npg + 1) / 2) * nsb;
+    const int gs = min(g, B - 1);   // (columns past the batch read a valid row; unused)
+    const uint16_t* gain;
+    mmv_src(c, op, l, 0, gain);
+    const bool multi = K > KR;      // accumulators persist over the ranges (then at most 2 blocks)
+    float bv = -INFINITY;           // LM head: this lane's running (max, lowest index) for sequence lane % 8
+    int bi = 0x7FFFFFFF;
+    float acc[2][2][4];
+    if (multi && nblk > 2) {   // (a tile of more than 4 pages with rows longer than a range: not scheduled)
+        raise_error(p, c.sh, MK_ERR_CAPACITY, ROLE_CONSUMER, pc, -1, uint32_t(nblk), 2u);
+        return false;
+    }
+    if (!wait_pages(c, si, pc)) return false;   // (the inputs are polled after: their producers run
+                                                // while the pages land)
+    for (int k0 = 0; k0 < K; k0 += KR) {
+        const int kr = min(KR, K - k0), csr = kr / 8, items = B * csr;
+        // 1. the range's inputs, every element polled until it carries this step's tag and stored
+        //    into the stage as fp32 (rewritten on every round); items (sequence i / csr, chunk
+        //    i % csr), i = tid, tid + 256, ...
+        {
+            Spin spn;
+            while (true) {
+                bool ok = true;
+#pragma unroll
+                for (int j = 0; j < kMmvItems; ++j) {
+                    const int i = tid + j * kConsumerThreads;
+                    if (i >= items) break;
+                    const int s = i / csr, ci = i % csr;
+                    const uint16_t* gn;
+                    const XSrc src = mmv_src(c, op, l, s, gn);
+                    float v[8];
+                    ok &= load8x(src, k0 + ci * 8, v, c.tag);
+                    float4* dst = reinterpret_cast<float4*>(stage + s * RS + ci * 32);
+                    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+                    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+                }
+                if (__all_sync(0xFFFFFFFFu, ok)) break;
+                if (!spin_more(c, spn, pc)) return false;
+            }
+        }
+        if (gain) {   // RMSNorm (one range: the row length is at most kMmvRange): 1 / rms per sequence
+            for (int i = tid; i < items; i += kConsumerThreads) {
+                const float4* src4 = reinterpret_cast<const float4*>(stage + (i / csr) * RS + (i % csr) * 32);
+                const float4 u = src4[0], w = src4[1];
+                part[i] = ((u.x * u.x + u.y * u.y) + (u.z * u.z + u.w * u.w)) + ((w.x * w.x + w.y * w.y) + (w.z * w.z + w.w * w.w));
+            }
+            if (!cbar(c, pc)) return false;
+            if (c.warp < B) {   // warp s: sequence s's chunk sums, lane-strided, then a butterfly
+                float q = 0.f;
+                for (int ci = c.lane; ci < csr; ci += 32) q += part[c.warp * csr + ci];
+                q = warp_sum(q);
+                if (c.lane == 0) c.sh.red[48 + c.warp] = rsqrtf(q / float(K) + p.rms_eps);
+            }
+        }
+        if (!cbar(c, pc)) return false;
+        // 2. in place, each thread its own items: x (* 1 / rms * gain) -> (hi, lo) word pairs
+        for (int i = tid; i < items; i += kConsumerThreads) {
+            const int s = i / csr, ci = i % csr;
+            uint4* w4 = reinterpret_cast<uint4*>(stage + s * RS + ci * 32);
+            const uint4 u = w4[0], w = w4[1];
+            float x[8] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w),
+                          __uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w)};
+            if (gain) {
+                const float scale = c.sh.red[48 + s];
+                const uint4 gw = __ldg(reinterpret_cast<const uint4*>(gain + k0 + ci * 8));
+                x[0] = (x[0] * scale) * bf_lo(gw.x); x[1] = (x[1] * scale) * bf_hi(gw.x);
+                x[2] = (x[2] * scale) * bf_lo(gw.y); x[3] = (x[3] * scale) * bf_hi(gw.y);
+                x[4] = (x[4] * scale) * bf_lo(gw.z); x[5] = (x[5] * scale) * bf_hi(gw.z);
+                x[6] = (x[6] * scale) * bf_lo(gw.w); x[7] = (x[7] * scale) * bf_hi(gw.w);
+            }
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t hb = bf16x2_rn(x[e], 0.f) & 0xFFFFu;
+                const float lo = x[e] - __uint_as_float(hb << 16);
+                o[e] = hb | (bf16x2_rn(lo, 0.f) << 16);
+            }
+            w4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            w4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        if (!cbar(c, pc)) return false;   // staged words visible; the partial area and the scales are free again
+        // 3. the contraction of the range, two row blocks at a time
+        const uint32_t xrow = stage_s + uint32_t(gs * RS);
+        for (int blk0 = 0; blk0 < nblk; blk0 += 2) {
+            const int nb = min(2, nblk - blk0);
+            MmvBlk bk[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int blk = blk0 + q;
+                const int pj = blk / nsb, r = 8 * (blk % nsb) + g;
+                const int p0 = 2 * pj, p1 = p0 + 1;
+                const int row0 = pair ? pj * rpp + r : p0 * rpp + r;
+                const int row1 = pair ? row0 : p1 * rpp + r;
+                uint32_t s0 = uint32_t(si.first_slot) + uint32_t(p0), s1 = s0 + 1u;
+                if (s0 >= uint32_t(p.n_pages)) s0 -= uint32_t(p.n_pages);
+                if (s1 >= uint32_t(p.n_pages)) s1 -= uint32_t(p.n_pages);
+                bk[q].v0 = q < nb && r < rpp && row0 < R;
+                bk[q].v1 = q < nb && r < rpp && p1 < npg && row1 < R;
+                bk[q].a0 = ring_base + (s0 << p.page_shift) + uint32_t(r) * m.rowbytes;
+                bk[q].a1 = ring_base + (s1 << p.page_shift) + uint32_t(r) * m.rowbytes;
+            }
+            if (!multi || k0 == 0)
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[q][h][e] = 0.f;
+            mmv_steps(c, bk, nb, xrow, k0, kr, acc);
+            if (multi && k0 + KR < K) continue;   // the next range adds to the same accumulators (<= 2 blocks)
+            if (blk0 + 2 >= nblk) release_pages(c, si);   // this warp's last page read
+            // D (row g, column 2 t4 + {0, 1}) and (row g + 8, ...): hi and lo chains added
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float* pw = part + (q * kNumConsumerWarps + c.warp) * 128;
+                pw[g * 8 + 2 * t4] = acc[q][0][0] + acc[q][1][0];
+                pw[g * 8 + 2 * t4 + 1] = acc[q][0][1] + acc[q][1][1];
+                pw[(g + 8) * 8 + 2 * t4] = acc[q][0][2] + acc[q][1][2];
+                pw[(g + 8) * 8 + 2 * t4 + 1] = acc[q][0][3] + acc[q][1][3];
+            }
+            if (!cbar(c, pc)) return false;
+            {   // outputs of the two blocks: thread (block q, MMA row rr, column = sequence col)
+                const int q = tid >> 7, rr = (tid >> 3) & 15, col = tid & 7;
+                const int blk = blk0 + q;
+                if (q < nb && col < B && (!pair || rr < 8)) {
+                    const int pj = blk / nsb, r = 8 * (blk % nsb) + (rr & 7);
+                    const int pg = 2 * pj + (rr >> 3);
+                    const int row = pair ? pj * rpp + r : pg * rpp + r;
+                    if (r < rpp && pg < npg && row < R) {
+                        float s0 = 0.f, s1 = 0.f;
+                        for (int w = 0; w < kNumConsumerWarps; ++w) {
+                            s0 += part[(q * kNumConsumerWarps + w) * 128 + rr * 8 + col];
+                            if (pair) s1 += part[(q * kNumConsumerWarps + w) * 128 + (rr + 8) * 8 + col];
+                        }
+                        mv_epilogue<false>(c, si, pc, col, row, s0, s1, nullptr, bv, bi);
+                    }
+                }
+            }
+            if (!cbar(c, pc)) return false;   // the partial area is reused
+        }
+        if (k0 + KR < K && !cbar(c, pc)) return false;   // (the next range restages the inputs)
+    }
+    if (op == OP_LMHEAD) {   // per sequence: this warp's running best (lanes col, col + 8, col + 16, col + 24)
+#pragma unroll
+        for (int o = 8; o <= 16; o <<= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (c.lane < B) {
+            const int b = c.lane;
+            float2& run = c.sh.lmbest[c.warp * kMaxBatch + b];
+            if (bv > run.x || (bv == run.x && bi < __float_as_int(run.y))) run = make_float2(bv, __int_as_float(bi));
+            p.lm_part[(size_t(b) * gridDim.x + blockIdx.x) * kNumConsumerWarps + c.warp] =
+                make_int4(__float_as_int(run.x), __float_as_int(run.y), int(c.epoch), 0);
+        }
+    }
     return true;
 }
 
@@ -1675,7 +1933,10 @@ __device__ bool step_boundary(Cw& c, int pc) {
     return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
-template <int CPL>
+// CPL: 16-byte chunks a lane holds of its row segment (batch 1); BAT: the batch > 1 kernel, whose
+// matvec tiles run on the tensor cores (its own instance: no register allocation is shared with
+// the batch-1 matvec path)
+template <int CPL, bool BAT>
 __device__ void consumer_warp(const Params& p, const Shared& sh) {
     Cw c{p, sh, int(threadIdx.x) >> 5, int(threadIdx.x) & 31, 0u, 0u, 0, p.epoch, p.tag};
     // slots and completion records are indexed by g, the instructions taken over all steps
@@ -1706,7 +1967,10 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
                 switch (op) {
                     case OP_ATTN: good = attn_tile(c, si, pc); break;
                     case OP_ARGMAX: good = argmax_tile(c, si, pc); break;
-                    default: good = matvec_tile<CPL>(c, si, pc); break;
+                    default:
+                        if constexpr (BAT) good = mmv_tile(c, si, pc);
+                        else good = matvec_tile<CPL>(c, si, pc);
+                        break;
                 }
                 if (!good) return;
                 if (threadIdx.x == 0) stamp(p, pc, 3);
@@ -1721,7 +1985,7 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
     }
 }
 
-template <int CPL>
+template <int CPL, bool BAT>
 __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Shared sh = carve(smem, p);
@@ -1753,12 +2017,17 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const Params p) {
     if (threadIdx.x == 0) stamp(p, 0, 5);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < kNumConsumerWarps) consumer_warp<CPL>(p, sh);
+    if (warp < kNumConsumerWarps) consumer_warp<CPL, BAT>(p, sh);
     else if (warp == kLoaderWarp) { if (lane == 0) loader(p, sh); }
     else if (lane == 0) publisher(p, sh);
     cta_sync_divergent();
 }
 
+#ifdef MK_BATCHED_TU
+// This translation unit holds the batch > 1 kernel alone (the same device code compiled apart, so
+// the batch-1 kernels keep their own inlining and register allocation).
+const void* megakernel_fn_batched() { return reinterpret_cast<const void*>(&megakernel<4, true>); }
+#else
 // RoPE table: rope[p][i] = (cos, sin)(p * theta^(-2i/d)), angles in double
 __global__ void rope_table_kernel(float2* out, int max_seq, int d, double theta) {
     const int half = d / 2;
@@ -1770,9 +2039,10 @@ __global__ void rope_table_kernel(float2* out, int max_seq, int d, double theta)
     }
 }
 
-// CPL: 16-byte chunks a lane holds of its row segment (4 or 8)
+// the batch-1 kernel instance for a binding, by CPL (4 or 8)
 const void* megakernel_fn(int cpl) {
-    return cpl == 4 ? reinterpret_cast<const void*>(&megakernel<4>) : reinterpret_cast<const void*>(&megakernel<kMaxCpl>);
+    return cpl == 4 ? reinterpret_cast<const void*>(&megakernel<4, false>)
+                    : reinterpret_cast<const void*>(&megakernel<kMaxCpl, false>);
 }
 
 cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cudaStream_t st) {
@@ -1781,5 +2051,6 @@ cudaError_t launch_rope_table(float2* out, int max_seq, int d, double theta, cud
     rope_table_kernel<<<blocks, 256, 0, st>>>(out, max_seq, d, theta);
     return cudaGetLastError();
 }
+#endif
 
 }  // namespace mk
