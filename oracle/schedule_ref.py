@@ -28,8 +28,9 @@ Waves: the DAG's longest-path level; per layer QKV=5l, ATTN=5l+1, OPROJ=5l+2, UP
 DOWN=5l+4; LMHEAD=5L, ARGMAX=5L+1.
 Pools: memory pool = tiles that stream weights or KV (QKV, ATTN, OPROJ, UPGATE, DOWN,
 LMHEAD); compute pool = ARGMAX.  Within a wave memory tiles are placed before compute tiles.
-Rows per tile: at batch 1 (tile_bytes 0) about one tile per operator per SM -- such a tile
-streams through the page ring page by page; otherwise tiles of about tile_bytes.
+Rows per tile: (tile_bytes 0) about one tile per operator per SM -- such a tile streams through
+the page ring page by page; at batch > 1 the down projection, when its rows are longer than
+MMV_RANGE, holds its pages in tiles of about 131072 bytes; otherwise tiles of about tile_bytes.
 Assignment, wave by wave: memory tiles sorted by (cost desc, tile id asc), then compute tiles
 likewise; each tile goes to the SM with the smallest accumulated cost (ties: lowest SM id) among
 the SMs holding fewer than ceil(n / S) of the n tiles of its pool in this wave; the accumulated
@@ -64,7 +65,7 @@ M64 = (1 << 64) - 1
 @dataclass
 class SchedOpts:
     page_bytes: int = 32768
-    tile_bytes: int = 0     # 0: per-SM tiles at batch 1, 131072-byte tiles at batch > 1
+    tile_bytes: int = 0     # 0: per-SM tiles (batch > 1: 131072-byte down tiles when F > MMV_RANGE)
     attn_chunk: int = 0     # 0: 64 positions, doubled up to 256 while B * n_kv * chunks > 152
     shuffle_seed: int = 0
     rows_qkv: int = 0   # 0: derived from tile_bytes
@@ -74,18 +75,23 @@ class SchedOpts:
     rows_lm: int = 0
 
 
+MMV_RANGE = 2048   # batch > 1: longest row whose tile streams (longer rows: the tile holds its pages)
+
+
 def tile_rows(cfg, o: SchedOpts, S: int) -> Dict[str, int]:
-    """Rows (pairs for gate/up) per matvec tile.  Batch 1 with tile_bytes 0: about one tile per
-    operator per SM (QKV tiles at most head_dim rows, so a tile touches one or two KV groups).
-    Otherwise tiles of about tile_bytes (default 131072).  Explicit rows_* override either."""
+    """Rows (pairs for gate/up) per matvec tile.  tile_bytes 0: about one tile per operator per SM
+    (QKV tiles at most head_dim rows, so a tile touches one or two KV groups); at batch > 1 the
+    down projection, when its rows are longer than MMV_RANGE, takes tiles of about 131072 bytes
+    (at most 8 rows).  Otherwise tiles of about tile_bytes.  Explicit rows_* override either."""
     H, F, V, d = cfg.hidden, cfg.ffn, cfg.vocab, cfg.head_dim
     qd = cfg.n_q_heads * cfg.head_dim
     nqkv = qd + 2 * cfg.n_kv_heads * d
-    if cfg.batch == 1 and o.tile_bytes == 0:
+    if o.tile_bytes == 0:
+        down = max(1, min(8, 131072 // (2 * F))) if (cfg.batch > 1 and F > MMV_RANGE) else ceil_div(H, S)
         R = dict(qkv=min(d, ceil_div(nqkv, S)), o=ceil_div(H, S), up=ceil_div(F, S),
-                 down=ceil_div(H, S), lm=ceil_div(V, S))
+                 down=down, lm=ceil_div(V, S))
     else:
-        tb = o.tile_bytes or 131072
+        tb = o.tile_bytes
 
         def fit(limit, nbytes_per_row):
             return max(1, min(limit, tb // nbytes_per_row))

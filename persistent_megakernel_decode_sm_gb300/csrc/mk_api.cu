@@ -272,12 +272,13 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
         ++n_pages;
     if (n_pages < 1) return fail(MK_ERR_CAPACITY, "no room for a page ring");
     const int misc = smem_misc_bytes(n_pages, asf, qrf, xbuf, comb_stride);
-    // capacity: at batch > 1 a tile's pages are held until it is done, so the ring must hold the
-    // largest tile; at batch 1 a matvec tile streams through the ring one group of two pages at a
-    // time, and an attention tile holds its K and V rows
-    int need_pages = 2;
-    if (c.batch > 1) need_pages = std::max(need_pages, s->max_pages);
-    else need_pages = std::max<int>(need_pages, int((2ll * g.attn_chunk * d * 2 + g.page_bytes - 1) / g.page_bytes));
+    // capacity: a matvec tile streams through the ring one group of two pages at a time, except at
+    // batch > 1 a tile whose rows are longer than kMmvRange (held until it is done); an attention
+    // tile holds its K and V rows
+    int need_pages = std::max<int>(2, int((2ll * g.attn_chunk * d * 2 + g.page_bytes - 1) / g.page_bytes));
+    if (c.batch > 1 && c.ffn > kMmvRange)
+        for (size_t i = 0; i < s->queues.size(); i += kWords)
+            if (s->queues[i + W_OP] == OP_DOWN) need_pages = std::max(need_pages, int(s->queues[i + W_NPAGES]));
     if (n_pages < need_pages)
         return fail(MK_ERR_CAPACITY, "page ring of %d pages cannot hold the %d pages a step needs", n_pages, need_pages);
     const int smem = n_pages * g.page_bytes + misc;

@@ -401,7 +401,10 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos
         st.rpp = uint32_t(p.mv[op].rpp);
         if (b0 == 0 || st.rpp == 0 || b0 != st.rows * st.rowbytes || b1 != (st.inter ? b0 : 0u)) return MK_ERR_BOUNDS;
         st.pages = int((st.rows + st.rpp - 1u) / st.rpp) * (st.inter ? 2 : 1);
-        if (st.pages > w[W_NPAGES] || (p.B > 1 && st.pages > p.n_pages)) return MK_ERR_CAPACITY;
+        // (at batch > 1 a tile whose rows are longer than kMmvRange holds all its pages: it must fit
+        // the ring; every other matvec tile streams through it)
+        if (st.pages > w[W_NPAGES] || (p.B > 1 && p.mv[op].K > kMmvRange && st.pages > p.n_pages))
+            return MK_ERR_CAPACITY;
         return MK_OK;
     } else if (op == OP_ATTN) {
         const int l = w[W_LAYER], b = w[W_B], g = w[W_A0], c = w[W_A1], C = w[W_A2];
@@ -422,9 +425,8 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos
         return MK_ERR_OPCODE;
     }
     st.pages = int((st.total + uint32_t(p.page_bytes) - 1u) >> p.page_shift);
-    // a tile whose consumers hold all its pages at once (attention; every tile at batch > 1) must
-    // fit the ring; batch-1 matvec tiles stream through it
-    if (st.pages > w[W_NPAGES] || ((op == OP_ATTN || p.B > 1) && st.pages > p.n_pages)) return MK_ERR_CAPACITY;
+    // an attention tile's consumers hold all its pages at once: it must fit the ring
+    if (st.pages > w[W_NPAGES] || (op == OP_ATTN && st.pages > p.n_pages)) return MK_ERR_CAPACITY;
     return MK_OK;
 }
 
@@ -1146,14 +1148,14 @@ __device__ __forceinline__ XSrc mmv_src(const Cw& c, int op, int l, int b, const
     return src;
 }
 
-// The 32-position steps of one row block pair (two 16-row blocks, 4 accumulator chains) over the
-// staged range: positions [k0, k0 + kr) of the rows, [0, kr) of the staged inputs.
+// The 32-position steps of one 16-row block over the staged range: positions [k0, k0 + kr) of
+// the rows, [0, kr) of the staged inputs; the hi and lo products in two accumulator chains.
 struct MmvBlk {
     uint32_t a0, a1;   // shared addresses of this lane's rows (g, g + 8) at position 0
     bool v0, v1;
 };
-__device__ __forceinline__ void mmv_steps(const Cw& c, const MmvBlk (&bk)[2], int nb, uint32_t xrow, int k0, int kr,
-                                          float (&acc)[2][2][4]) {
+__device__ __forceinline__ void mmv_steps(const Cw& c, const MmvBlk& bk, uint32_t xrow, int k0, int kr,
+                                          float (&acc)[2][4]) {
     const int t4 = c.lane & 3;
     const int npr = (kr + 31) / 32;
     for (int pr = c.warp; pr < npr; pr += kNumConsumerWarps) {
@@ -1163,22 +1165,20 @@ __device__ __forceinline__ void mmv_steps(const Cw& c, const MmvBlk (&bk)[2], in
         const uint32_t ka = uint32_t(k0 + kl) * 2u;
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
         const uint4 x0 = kv ? lds128(xrow + uint32_t(kl) * 4u) : z, x1 = kv ? lds128(xrow + uint32_t(kl) * 4u + 16u) : z;
+        const uint4 A0 = (kv && bk.v0) ? lds128(bk.a0 + ka) : z;
+        const uint4 A1 = (kv && bk.v1) ? lds128(bk.a1 + ka) : z;
         // staged words: hi in the low half, lo in the high half
-        const uint32_t h0 = __byte_perm(x0.x, x0.y, 0x5410), h1 = __byte_perm(x0.z, x0.w, 0x5410);
-        const uint32_t h2 = __byte_perm(x1.x, x1.y, 0x5410), h3 = __byte_perm(x1.z, x1.w, 0x5410);
-        const uint32_t l0 = __byte_perm(x0.x, x0.y, 0x7632), l1 = __byte_perm(x0.z, x0.w, 0x7632);
-        const uint32_t l2 = __byte_perm(x1.x, x1.y, 0x7632), l3 = __byte_perm(x1.z, x1.w, 0x7632);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            if (q >= nb) break;
-            const uint4 A0 = (kv && bk[q].v0) ? lds128(bk[q].a0 + ka) : z;
-            const uint4 A1 = (kv && bk[q].v1) ? lds128(bk[q].a1 + ka) : z;
-            mma16816(acc[q][0], A0.x, A1.x, A0.y, A1.y, h0, h1);
-            mma16816(acc[q][1], A0.x, A1.x, A0.y, A1.y, l0, l1);
-            mma16816(acc[q][0], A0.z, A1.z, A0.w, A1.w, h2, h3);
-            mma16816(acc[q][1], A0.z, A1.z, A0.w, A1.w, l2, l3);
-        }
+        mma16816(acc[0], A0.x, A1.x, A0.y, A1.y, __byte_perm(x0.x, x0.y, 0x5410), __byte_perm(x0.z, x0.w, 0x5410));
+        mma16816(acc[1], A0.x, A1.x, A0.y, A1.y, __byte_perm(x0.x, x0.y, 0x7632), __byte_perm(x0.z, x0.w, 0x7632));
+        mma16816(acc[0], A0.z, A1.z, A0.w, A1.w, __byte_perm(x1.x, x1.y, 0x5410), __byte_perm(x1.z, x1.w, 0x5410));
+        mma16816(acc[1], A0.z, A1.z, A0.w, A1.w, __byte_perm(x1.x, x1.y, 0x7632), __byte_perm(x1.z, x1.w, 0x7632));
     }
+}
+// the slot and phase of page pg of a tile
+__device__ __forceinline__ void tile_page(const Params& p, const SlotInfo& si, int pg, uint32_t& slot, uint32_t& ph) {
+    const uint32_t idx = uint32_t(si.first_slot) + uint32_t(pg);
+    slot = idx % uint32_t(p.n_pages);
+    ph = uint32_t(si.first_phase) ^ ((idx / uint32_t(p.n_pages)) & 1u);
 }
 
 __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
@@ -1204,8 +1204,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
         raise_error(p, c.sh, MK_ERR_CAPACITY, ROLE_CONSUMER, pc, -1, uint32_t(nblk), 2u);
         return false;
     }
-    if (!wait_pages(c, si, pc)) return false;   // (the inputs are polled after: their producers run
-                                                // while the pages land)
+    if (multi && !wait_pages(c, si, pc)) return false;   // (held tiles: the inputs are polled after)
     for (int k0 = 0; k0 < K; k0 += KR) {
         const int kr = min(KR, K - k0), csr = kr / 8, items = B * csr;
         // 1. the range's inputs, every element polled until it carries this step's tag and stored
@@ -1285,9 +1284,9 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                 const int p0 = 2 * pj, p1 = p0 + 1;
                 const int row0 = pair ? pj * rpp + r : p0 * rpp + r;
                 const int row1 = pair ? row0 : p1 * rpp + r;
-                uint32_t s0 = uint32_t(si.first_slot) + uint32_t(p0), s1 = s0 + 1u;
-                if (s0 >= uint32_t(p.n_pages)) s0 -= uint32_t(p.n_pages);
-                if (s1 >= uint32_t(p.n_pages)) s1 -= uint32_t(p.n_pages);
+                uint32_t s0, s1, ph_unused;   // ring slots of the pair (a streamed tile wraps the ring many times)
+                tile_page(p, si, p0, s0, ph_unused);
+                tile_page(p, si, p1, s1, ph_unused);
                 bk[q].v0 = q < nb && r < rpp && row0 < R;
                 bk[q].v1 = q < nb && r < rpp && p1 < npg && row1 < R;
                 bk[q].a0 = ring_base + (s0 << p.page_shift) + uint32_t(r) * m.rowbytes;
@@ -1300,9 +1299,35 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc[q][h][e] = 0.f;
-            mmv_steps(c, bk, nb, xrow, k0, kr, acc);
-            if (multi && k0 + KR < K) continue;   // the next range adds to the same accumulators (<= 2 blocks)
-            if (blk0 + 2 >= nblk) release_pages(c, si);   // this warp's last page read
+            if (multi) {   // the tile holds its pages: the next range adds to the same accumulators
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    if (q < nb) mmv_steps(c, bk[q], xrow, k0, kr, acc[q]);
+                if (k0 + KR < K) continue;
+                if (blk0 + 2 >= nblk) release_pages(c, si);   // this warp's last page read
+            } else {   // streaming: a pair of pages is waited for at its first block, given back after its last
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    if (q >= nb) break;
+                    const int blk = blk0 + q, pj = blk / nsb;
+                    if (blk % nsb == 0)
+                        for (int pg = 2 * pj; pg < min(2 * pj + 2, npg); ++pg) {
+                            uint32_t slot, ph;
+                            tile_page(p, si, pg, slot, ph);
+                            if (!wait_bar(p, c.sh, c.sh.full + slot, ph, ROLE_CONSUMER, pc)) return false;
+                        }
+                    mmv_steps(c, bk[q], xrow, k0, kr, acc[q]);
+                    if (blk % nsb == nsb - 1 || blk == nblk - 1) {
+                        __syncwarp();
+                        if (c.lane == 0)
+                            for (int pg = 2 * pj; pg < min(2 * pj + 2, npg); ++pg) {
+                                uint32_t slot, ph;
+                                tile_page(p, si, pg, slot, ph);
+                                mbar_arrive(c.sh.empty + slot);
+                            }
+                    }
+                }
+            }
             // D (row g, column 2 t4 + {0, 1}) and (row g + 8, ...): hi and lo chains added
 #pragma unroll
             for (int q = 0; q < 2; ++q) {

@@ -22,8 +22,9 @@
 //    point only at lower waves (forward-progress contract);
 //  * pools: memory = tiles that stream weights or KV, compute = argmax; within a wave memory
 //    tiles are placed first;
-//  * rows per tile: at batch 1 about one tile per operator per SM (streamed through the page
-//    ring page by page, whole rows per page), otherwise about tile_bytes per tile;
+//  * rows per tile: about one tile per operator per SM (streamed through the page ring page by
+//    page, whole rows per page) -- at batch > 1 the down projection's tiles hold their pages and
+//    take about 131072 bytes when its rows are longer than kMmvRange -- or about tile_bytes;
 //  * placement: within a wave, tiles in (cost desc, id asc) order -- or a seeded splitmix64
 //    Fisher-Yates order when shuffle_seed != 0 -- each to the queue with the smallest
 //    accumulated cost (ties to the lowest SM) among the queues holding fewer than ceil(n / S)
@@ -148,16 +149,18 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     const int32_t nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim, hpg = nq / nkv;
     const int32_t qd = nq * d, kvd = nkv * d, nqkv = qd + 2 * kvd;
 
-    // rows per tile.  Batch 1 (tile_bytes 0): about one tile per operator per SM -- a tile streams
-    // through the page ring page by page, so it need not fit the ring, and the per-tile costs
-    // (dispatch, input vector, first touch of its pages, completion) are paid once per operator
-    // and SM.  QKV tiles keep <= head_dim rows (a tile then touches at most two KV groups).
-    // Batch > 1 or an explicit tile_bytes: tiles of about tile_bytes, which must fit the ring.
-    if (B == 1 && g.tile_bytes == 0) {
+    // rows per tile.  tile_bytes 0: about one tile per operator per SM -- a tile streams through
+    // the page ring page by page, so it need not fit the ring, and the per-tile costs (dispatch,
+    // input vector, first touch of its pages, completion) are paid once per operator and SM.  QKV
+    // tiles keep <= head_dim rows (a tile then touches at most two KV groups).  At batch > 1 an
+    // operator whose rows are longer than kMmvRange (the MLP down projection) holds its pages for
+    // the tile, which then takes about 131072 bytes so that it fits the ring.  An explicit
+    // tile_bytes: tiles of about tile_bytes.
+    if (g.tile_bytes == 0) {
         g.r_qkv = std::min(d, cdiv(nqkv, S));
         g.r_o = cdiv(H, S);
         g.r_up = cdiv(F, S);
-        g.r_dn = cdiv(H, S);
+        g.r_dn = (B > 1 && F > kMmvRange) ? fit(8, 131072, 2ll * F) : cdiv(H, S);
         g.r_lm = cdiv(V, S);
     } else {
         const int64_t tb = g.tile_bytes ? g.tile_bytes : 131072;
