@@ -285,10 +285,13 @@ def main():
     kv = prefilled_kv(cfg, wl.kv_len, seed=0, device="cuda")
     S = mk.device_sm_count()
     stream = torch.cuda.Stream()
-    sched = mk.Schedule(cfg, S, attn_chunk=args.attn_chunk)
+    # a batch of uneven lengths is planned for the positions this run reaches: attention chunks
+    # past each sequence's window get no tile (variable-length re-planning)
+    span = cfg.max_seq - max(wl.kv_len)
+    windows = [min(cfg.max_seq, l + min(W + K, span) + 1) for l in wl.kv_len] if cfg.batch > 1 else None
+    sched = mk.Schedule(cfg, S, attn_chunk=args.attn_chunk, kv_limit=windows)
     dec = mk.Decoder(sched, w, kv, stream=stream)
     dec.set_sync(args.sync)
-    span = cfg.max_seq - max(wl.kv_len)
     toks = token_ids(cfg, (W + K) * cfg.batch, seed=1, tag="bench")
 
     def args_for(i):
@@ -375,7 +378,7 @@ def main():
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "batch": cfg.batch, "kv_len": wl.kv_len[0] if cfg.batch == 1 else wl.kv_len,
                    "weights": "bf16", "kv": "bf16", "sm_count": S, "parallelism": "replicas" if world > 1 else "single",
-                   "sync": args.sync, "attn_chunk": sched.attn_chunk,
+                   "sync": args.sync, "attn_chunk": sched.attn_chunk, "kv_windows": windows,
                    "l2": "inputs larger than L2 (2.47 GB of weights streamed per step)",
                    "step_us_mean": mean_us, "step_us_median": med, "step_us_p10": p10, "step_us_p90": p90},
         "e2e": {"value": e2e_us, "unit": "us/token", "h2d_bytes_per_step": 8 * cfg.batch,

@@ -56,21 +56,28 @@ typedef struct {
 } mk_model_cfg;
 
 /* Schedule knobs; pass NULL to mk_build_schedule for the defaults (each 0 field = default).
- * At batch 1 with tile_bytes 0 every matvec operator is cut into about sm_count tiles (QKV tiles
- * at most head_dim rows), each streamed through the page ring step by step; otherwise tiles hold
- * about tile_bytes and must fit the ring.  A row's arithmetic never depends on the tiling. */
+ * With tile_bytes 0 every matvec operator is cut into about sm_count tiles (QKV tiles at most
+ * head_dim rows), each streamed through the page ring step by step -- except at batch > 1 the
+ * MLP down projection when ffn > 2048, whose tiles of about 131072 bytes hold their pages;
+ * otherwise tiles hold about tile_bytes.  A row's arithmetic never depends on the tiling.
+ * kv_limit is the variable-length re-planning of the page's boundaries paragraph ("Inference
+ * MegaKernel", section "Hand-written whole-model MegaKernel": dynamic batches and variable-length
+ * requests change the static queue): attention chunks past a sequence's window get no tile, so a
+ * batch of uneven lengths is placed by the work it has; mk_rebind_schedule moves a binding to a
+ * schedule with new windows. */
 typedef struct {
     int32_t page_bytes;  /* shared-memory page size (a power of two); default 32768             */
-    int32_t tile_bytes;  /* 0: per-SM tiles at batch 1, 131072 at batch > 1; else the target
-                            weight bytes per matvec tile (capped at 8 rows for QKV, O and down,
-                            16 gate/up pairs, 32 LM-head rows)                                   */
+    int32_t tile_bytes;  /* 0: per-SM tiles (see above); else the target weight bytes per matvec
+                            tile (capped at 8 rows for QKV, O and down, 16 gate/up pairs, 32
+                            LM-head rows)                                                        */
     int32_t attn_chunk;  /* KV positions per split-K attention tile; 0: 64, doubled (up to 256)
                             while batch * n_kv_heads * ceil(max_seq / chunk) > 152 (a property
-                            of the configuration, not of sm_count);
-                            n_q_heads / n_kv_heads * attn_chunk <= 2048 (checked at bind)        */
+                            of the configuration, not of sm_count)                               */
     int32_t rows_qkv, rows_o, pairs_up, rows_down, rows_lm; /* explicit rows (pairs) per tile,
                             overriding the above; rows_qkv <= head_dim                           */
     uint64_t shuffle_seed; /* 0: cost-ordered placement; otherwise a seeded shuffled placement  */
+    int32_t kv_limit[8];   /* per sequence: positions the schedule serves, [0, kv_limit) (0 or
+                            max_seq: all); a step at pos >= kv_limit[b] is rejected (MK_ERR_ARG) */
 } mk_sched_opts;
 
 typedef struct mk_schedule mk_schedule; /* opaque, library-owned host object */
@@ -207,6 +214,15 @@ mk_status mk_bind(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, ui
  * attention chunk, a table that cannot cover max_seq, or strides that do not cover the pool. */
 mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, const mk_kv* kv, const mk_kv_pages* pages,
                         uint32_t* counters, void* scratch, void* stream, mk_ctx** out);
+
+/* Moves a binding to another schedule of the same model configuration, SM count, page size,
+ * attention chunk and tile rows -- in practice one built with other kv_limit windows (the
+ * re-planning for a changing batch of variable-length requests; see mk_sched_opts).  The new
+ * queues are resolved against the bound weights and uploaded; counters, epoch, KV cache and
+ * scratch carry over, so decoding continues where it was.  Waits for the bound stream first.
+ * Errors: MK_ERR_ARG (null argument, an incompatible schedule, a persistent launch in flight),
+ * MK_ERR_POISONED, MK_ERR_CUDA. */
+mk_status mk_rebind_schedule(mk_ctx* c, const mk_schedule* s);
 
 /* Time budget, in nanoseconds, of a single device wait: counter spins and tagged-data polls get
  * ns, waits of the consumer warps on one another 2 ns, the loader's and publisher's waits (which

@@ -14,7 +14,8 @@ Tiles (per layer l, in this order; ids are assigned in enumeration order):
           touches one or two KV groups' q, k or v ranges and completes each group it touches.
           RMSNorm of the layer input is its prologue.
   ATTN    (b, g, c): sequence b, KV group g, KV positions [c*C, (c+1)*C) -- split-K decode
-          attention; c runs over ceil(max_seq / C) chunks (chunks past pos do no work).  The
+          attention; c runs over the chunks of the sequence's window [0, kv_limit[b]) (default
+          max_seq; chunks past pos do no work).  The
           tile whose chunk holds the step's position (known at run time only) also does the
           fixed-order log-sum-exp combine of the group's chunk partials, reading the lower
           chunks' partials as they land, and alone carries the tile's completion (a conditional
@@ -73,6 +74,13 @@ class SchedOpts:
     pairs_up: int = 0
     rows_down: int = 0
     rows_lm: int = 0
+    kv_limit: Tuple[int, ...] = (0,) * 8   # per sequence: positions served, [0, kv_limit) (0: max_seq)
+
+
+def kv_window(cfg, o: SchedOpts, b: int) -> int:
+    """Positions [0, window) of sequence b the schedule serves (variable-length re-planning)."""
+    lim = o.kv_limit[b] if b < len(o.kv_limit) else 0
+    return lim if lim else cfg.max_seq
 
 
 MMV_RANGE = 2048   # batch > 1: longest row whose tile streams (longer rows: the tile holds its pages)
@@ -211,6 +219,8 @@ def enumerate_tiles(cfg, o: SchedOpts, S: int) -> Tuple[List[Tile], Counters, Di
         for b in range(B):
             for g in range(nkv):
                 for c in range(nchunk):
+                    if c * C >= kv_window(cfg, o, b):   # chunks past the sequence's window: no tile
+                        break
                     tiles.append(Tile(ATTN, l, b, g, c, C, 5 * l + 1,
                                       [(cnt.qkv(l, g), qkv_tiles_of_group[g])],
                                       [(cnt.comb(l), 1)], 2 * C * d * 2, cond=True))
@@ -498,15 +508,17 @@ def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, see
              track_data: bool = True, pos: Optional[List[int]] = None) -> List[str]:
     """Runs the S queues on the host under a random interleaving, for n_epochs consecutive steps
     with epoch-offset counter targets (target = epoch * total + need, compared modulo 2^32).
-    Sequence b decodes position pos[b] (default max_seq - 1: every attention chunk active): the
+    Sequence b decodes position pos[b] (default: the last position its scheduled chunks cover): the
     chunk tiles past it do nothing, the others write their partial, and the tile of the chunk
     holding it waits (inside its wave) until the lower chunks of its group have written theirs,
     then writes the group's attention output and fires the completion.  Reports a deadlock (no
     SM can progress before all reach END) and any read of a buffer whose writer has not yet run
     in the current step."""
     S, Q, _ = queues.shape
-    if pos is None:
-        pos = [cfg.max_seq - 1] * cfg.batch
+    decoded0 = [_decode(queues[s, i]) for s in range(S) for i in range(Q) if queues[s, i, 0] != END]
+    if pos is None:   # the last position each sequence's scheduled chunks cover
+        pos = [min(cfg.max_seq - 1, max([(t.a1 + 1) * t.a2 - 1 for t in decoded0 if t.op == ATTN and t.b == b],
+                                        default=cfg.max_seq - 1)) for b in range(cfg.batch)]
     rng = random.Random(seed)
     counters = np.zeros(len(totals), dtype=np.int64)
     errs: List[str] = []

@@ -37,7 +37,7 @@ EXPORTS = ["mk_build_schedule", "mk_schedule_queues", "mk_schedule_counters", "m
            "mk_launch_step", "mk_ctx_status", "mk_device_sm_count", "mk_last_error", "mk_unbind", "mk_set_trace",
            "mk_decode_step_static", "mk_set_sync", "mk_decode_steps", "mk_bind_paged", "mk_schedule_attn_chunk",
            "mk_decode_persistent_start", "mk_decode_persistent_stop", "mk_decode_persistent_progress",
-           "mk_decode_persistent_wait"]
+           "mk_decode_persistent_wait", "mk_rebind_schedule"]
 
 
 class MkError(RuntimeError):
@@ -55,7 +55,7 @@ class mk_model_cfg(ctypes.Structure):
 class mk_sched_opts(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("page_bytes", "tile_bytes", "attn_chunk", "rows_qkv", "rows_o",
                                               "pairs_up", "rows_down", "rows_lm")] + \
-               [("shuffle_seed", ctypes.c_uint64)]
+               [("shuffle_seed", ctypes.c_uint64), ("kv_limit", ctypes.c_int32 * 8)]
 
 
 _P = ctypes.c_void_p
@@ -113,6 +113,8 @@ lib.mk_decode_persistent_progress.restype = ctypes.c_int
 lib.mk_decode_persistent_progress.argtypes = [_P, _I32P]
 lib.mk_decode_persistent_wait.restype = ctypes.c_int
 lib.mk_decode_persistent_wait.argtypes = [_P, _I32P, _I32P]
+lib.mk_rebind_schedule.restype = ctypes.c_int
+lib.mk_rebind_schedule.argtypes = [_P, _P]
 lib.mk_ctx_status.restype = ctypes.c_int
 lib.mk_ctx_status.argtypes = [_P, _I32P]
 lib.mk_device_sm_count.restype = ctypes.c_int
@@ -151,11 +153,12 @@ class Schedule:
 
     def __init__(self, cfg, sm_count: int, page_bytes: int = 0, tile_bytes: int = 0, attn_chunk: int = 0,
                  rows_qkv: int = 0, rows_o: int = 0, pairs_up: int = 0, rows_down: int = 0, rows_lm: int = 0,
-                 shuffle_seed: int = 0):
+                 shuffle_seed: int = 0, kv_limit: Optional[Sequence[int]] = None):
         self.cfg = cfg
         self._c = make_cfg(cfg)
+        lim = list(kv_limit or []) + [0] * (8 - len(kv_limit or []))
         o = mk_sched_opts(page_bytes, tile_bytes, attn_chunk, rows_qkv, rows_o, pairs_up, rows_down, rows_lm,
-                          shuffle_seed)
+                          shuffle_seed, (ctypes.c_int32 * 8)(*lim))
         h = _P()
         _check(lib.mk_build_schedule(ctypes.byref(self._c), int(sm_count), ctypes.byref(o), ctypes.byref(h)))
         self.handle = h
@@ -295,6 +298,12 @@ class Decoder:
         out = (ctypes.c_int32 * (max(n_steps, 1) * B))()
         _check(lib.mk_decode_steps(self.handle, t, p, int(n_steps), _ptr(lg), _ptr(tokens_dev), out))
         return [list(out[i * B:(i + 1) * B]) for i in range(n_steps)]
+
+    def rebind(self, sched: "Schedule"):
+        """mk_rebind_schedule: continue on another schedule of the same model and SM count (new KV
+        windows: the variable-length re-planning).  The schedule object must outlive its use."""
+        _check(lib.mk_rebind_schedule(self.handle, sched.handle))
+        self.sched = sched
 
     def persistent_start(self, tokens: Sequence[int], pos: Sequence[int], n_steps: int, logits=None,
                          tokens_dev=None):

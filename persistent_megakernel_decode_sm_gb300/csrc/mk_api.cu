@@ -57,6 +57,14 @@ struct mk_ctx {
     int32_t run_steps;
     const int32_t* run_tokens;
     mk_model_cfg cfg;
+    // what a schedule switch (mk_rebind_schedule) needs: the bound weights (pointer tables copied),
+    // the geometry and counter totals of the bound schedule, its KV windows per sequence
+    mk_weights w;
+    std::vector<const void*> wtab;   // the per-layer pointer tables behind w
+    Geometry geo;
+    int32_t S;
+    std::vector<uint32_t> totals;
+    size_t queue_words;               // capacity of d_queues in words
 };
 
 static mk_status cuda_fail(cudaError_t e, const char* what) {
@@ -288,14 +296,29 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     if (per_sm < 1) return fail(MK_ERR_RESOURCES, "the kernel cannot be resident (%d B shared memory)", smem);
 
     // ---- context ----
-    mk_ctx* x = new mk_ctx();
-    std::memset(x, 0, sizeof(*x));
+    mk_ctx* x = new mk_ctx();   // (value-initialised: every scalar field zero)
     x->cfg = c;
     x->fn = fn;
     x->grid = s->S;
     x->smem = smem;
     x->stream = static_cast<cudaStream_t>(stream);
     x->device = dev;
+    x->geo = g;
+    x->S = s->S;
+    x->totals = s->totals;
+    x->queue_words = s->queues.size();
+    {   // the weights' pointer tables, for resolving another schedule's queues later
+        x->wtab.reserve(size_t(6) * L);
+        const void* const* tabs[6] = {w->attn_norm, w->wqkv, w->wo, w->mlp_norm, w->wgate_up, w->wdown};
+        for (auto* t : tabs) x->wtab.insert(x->wtab.end(), t, t + L);
+        x->w = *w;
+        x->w.attn_norm = &x->wtab[0];
+        x->w.wqkv = &x->wtab[size_t(L)];
+        x->w.wo = &x->wtab[size_t(2) * L];
+        x->w.mlp_norm = &x->wtab[size_t(3) * L];
+        x->w.wgate_up = &x->wtab[size_t(4) * L];
+        x->w.wdown = &x->wtab[size_t(5) * L];
+    }
     auto bail = [&](mk_status st) { free_ctx(x); return st; };
     cudaError_t e;
     const size_t qbytes = s->queues.size() * sizeof(int32_t);
@@ -402,6 +425,36 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     return MK_OK;
 }
 
+extern "C" mk_status mk_rebind_schedule(mk_ctx* c, const mk_schedule* s) {
+    if (!c || !s) return fail(MK_ERR_ARG, "null argument");
+    if (c->run_active) return fail(MK_ERR_ARG, "a persistent launch is in flight (mk_decode_persistent_wait first)");
+    if (c->poisoned) return fail(MK_ERR_POISONED, "context poisoned by an earlier device error");
+    // the same model, SM count and shapes: only the tiles' placement and the KV windows may differ
+    const Geometry& a = c->geo;
+    const Geometry& b = s->geo;
+    if (std::memcmp(&s->cfg, &c->cfg, sizeof(mk_model_cfg)) != 0 || s->S != c->S || b.page_bytes != a.page_bytes ||
+        b.attn_chunk != a.attn_chunk || b.n_chunk != a.n_chunk || b.r_qkv != a.r_qkv || b.r_o != a.r_o ||
+        b.r_up != a.r_up || b.r_dn != a.r_dn || b.r_lm != a.r_lm || b.n_counters != a.n_counters ||
+        s->totals != c->totals)
+        return fail(MK_ERR_ARG, "the schedule differs from the bound one in more than placement and KV windows");
+    std::vector<int32_t> dq;
+    const mk_status rs = resolve_queues(s, &c->w, dq);
+    if (rs != MK_OK) return rs;
+    CK(cudaStreamSynchronize(c->stream));   // no launch reads the queues any more
+    if (dq.size() > c->queue_words) {
+        int32_t* nq = nullptr;
+        CK(cudaMalloc(&nq, dq.size() * sizeof(int32_t)));
+        cudaFree(c->d_queues);
+        c->d_queues = nq;
+        c->queue_words = dq.size();
+    }
+    CK(cudaMemcpy(c->d_queues, dq.data(), dq.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+    c->base.queues = c->d_queues;
+    c->base.Q = s->Q;
+    c->geo = b;
+    return MK_OK;
+}
+
 extern "C" mk_status mk_set_timeout(mk_ctx* c, uint64_t ns) {
     if (!c || ns == 0) return fail(MK_ERR_ARG, "bad argument");
     c->base.timeout_ns = ns;
@@ -479,6 +532,9 @@ static mk_status check_step_args(mk_ctx* c, const int32_t* tokens, const int32_t
         if (pos[b] < 0 || int64_t(pos[b]) + n_steps > c->cfg.max_seq)
             return fail(MK_ERR_ARG, "positions %d..%d outside the KV capacity [0, %d)", pos[b], pos[b] + n_steps - 1,
                         c->cfg.max_seq);
+        if (int64_t(pos[b]) + n_steps > c->geo.kv_limit[b])
+            return fail(MK_ERR_ARG, "sequence %d: positions up to %d outside the schedule's window [0, %d) (re-plan: "
+                        "mk_rebind_schedule)", b, pos[b] + n_steps - 1, c->geo.kv_limit[b]);
     }
     return MK_OK;
 }
@@ -691,6 +747,9 @@ extern "C" mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, con
         if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab) return fail(MK_ERR_ARG, "token %d out of range", tokens[b]);
         if (pos[b] < 0 || pos[b] >= c->cfg.max_seq)
             return fail(MK_ERR_ARG, "pos %d outside the KV capacity [0, %d)", pos[b], c->cfg.max_seq);
+        if (pos[b] >= c->geo.kv_limit[b])
+            return fail(MK_ERR_ARG, "sequence %d: pos %d outside the schedule's window [0, %d)", b, pos[b],
+                        c->geo.kv_limit[b]);
         p.tok[b] = tokens[b];
         p.pos[b] = pos[b];
     }

@@ -64,6 +64,7 @@ struct Geometry {
     int32_t n_chunk;                          // attention chunks per (sequence, group)
     int32_t n_counters;
     uint64_t shuffle_seed;
+    int32_t kv_limit[kMaxBatch];              // per sequence: positions [0, kv_limit) served
 };
 
 // counter ids

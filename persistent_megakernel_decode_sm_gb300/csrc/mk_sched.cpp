@@ -8,7 +8,8 @@
 // kernel (the page's object table gives the queue only as an int32 tensor of shape [S, Q, 32]).
 // The page fixes none of the concrete rules; this file states them:
 //  * tiles per layer: QKV row tiles (<= head_dim rows: a tile touches one or two KV groups and
-//    completes each), attention chunks (sequence, group, chunk of attn_chunk positions), O row
+//    completes each), attention chunks (sequence, group, chunk of attn_chunk positions; only the
+//    chunks inside the sequence's kv_limit window), O row
 //    tiles, gate/up row-pair tiles, down row tiles; then
 //    LM-head row tiles and one argmax per sequence;
 //  * DAG: a consumer waits on one counter per producer set -- QKV(l) on down(l-1), attention
@@ -140,6 +141,10 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
             g.attn_chunk *= 2;
     }
     g.shuffle_seed = o.shuffle_seed;
+    for (int b = 0; b < kMaxBatch; ++b) {
+        if (o.kv_limit[b] < 0 || o.kv_limit[b] > c.max_seq) return fail(MK_ERR_ARG, "kv_limit[%d] out of [0, max_seq]", b);
+        g.kv_limit[b] = o.kv_limit[b] ? o.kv_limit[b] : c.max_seq;
+    }
     if (g.page_bytes < 1024 || g.page_bytes % 128 || g.page_bytes > (1 << 20))
         return fail(MK_ERR_ARG, "page_bytes must be a multiple of 128 in [1024, 1 MiB]");
     if (g.tile_bytes != 0 && g.tile_bytes < 16) return fail(MK_ERR_ARG, "tile_bytes too small");
@@ -236,7 +241,7 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         }
         for (int32_t b = 0; b < B; ++b)
             for (int32_t gr = 0; gr < nkv; ++gr)
-                for (int32_t ch = 0; ch < g.n_chunk; ++ch) {
+                for (int32_t ch = 0; ch < g.n_chunk && int64_t(ch) * g.attn_chunk < g.kv_limit[b]; ++ch) {
                     add(OP_ATTN, l, b, gr, ch, g.attn_chunk, 5 * l + 1, {{cm.qkv(l, gr), qkv_tiles_of_group[gr]}},
                         {cm.comb(l), 1}, int64_t(2) * g.attn_chunk * d * 2);
                     tiles.back().cond = true;

@@ -45,7 +45,8 @@ def test_cpp_shuffled_placement_bit_exact(seed):
     assert np.array_equal(s.queues(), q) and np.array_equal(s.totals(), t)
 
 
-@pytest.mark.parametrize("kw", [dict(page_bytes=16384, tile_bytes=32768, attn_chunk=32),
+@pytest.mark.parametrize("kw", [dict(kv_limit=[100, 300, 1, 233]), dict(kv_limit=[65, 0, 7], shuffle_seed=5),
+                                dict(page_bytes=16384, tile_bytes=32768, attn_chunk=32),
                                 dict(rows_qkv=4, rows_o=3, pairs_up=5, rows_down=7, rows_lm=9),
                                 dict(attn_chunk=100)])
 def test_cpp_knobs_bit_exact(kw):
@@ -198,3 +199,33 @@ def test_combining_tile_ahead_of_a_lower_chunk_deadlocks_and_is_rejected():
     assert any("same wave" in e for e in sr.validate(bad, t, cfg))
     assert any("deadlock" in e for e in sr.simulate(bad, t, cfg, n_epochs=1, pos=[639]))
     assert sr.simulate(q, t, cfg, n_epochs=1, pos=[639]) == []
+
+
+@pytest.mark.parametrize("seed", [0, 9])
+def test_kv_windows_drop_the_chunks_past_each_sequence(seed):
+    """Variable-length re-planning: a batch-8 schedule with per-sequence windows keeps exactly the
+    attention chunks inside each window (C++ bit-exact with the restatement), stays valid, and the
+    host simulator completes steps at the windows' last positions and at smaller ones."""
+    cfg = get_workload("llama1b_batch8").cfg
+    lens = get_workload("llama1b_batch8").kv_len
+    lim = [n + 4 for n in lens]
+    o = sr.SchedOpts(kv_limit=tuple(lim), shuffle_seed=seed)
+    q, t, info = sr.build_schedule(cfg, 37, o)
+    s = mk.Schedule(cfg, 37, kv_limit=lim, shuffle_seed=seed)
+    assert np.array_equal(s.queues(), q) and np.array_equal(s.totals(), t)
+    assert sr.validate(q, t, cfg, o) == []
+    C = s.attn_chunk
+    for b in range(cfg.batch):
+        chunks = sorted({int(w[4]) for w in q.reshape(-1, q.shape[-1]) if w[0] == sr.ATTN and w[2] == b and w[1] == 0 and w[3] == 0})
+        assert chunks == list(range(-(-lim[b] // C)))
+    assert sr.simulate(q, t, cfg, n_epochs=2, seed=seed) == []
+    assert sr.simulate(q, t, cfg, n_epochs=1, seed=seed, pos=[n // 2 for n in lens]) == []
+    full, _, _ = sr.build_schedule(cfg, 37, sr.SchedOpts(shuffle_seed=seed))
+    assert (q[..., 0] == sr.ATTN).sum() < (full[..., 0] == sr.ATTN).sum()
+
+
+def test_kv_limit_out_of_range_is_rejected():
+    cfg = get_workload("tiny").cfg
+    with pytest.raises(mk.MkError) as e:
+        mk.Schedule(cfg, 4, kv_limit=[cfg.max_seq + 1])
+    assert e.value.status == mk.MK_ERR_ARG
