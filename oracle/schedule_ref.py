@@ -30,8 +30,9 @@ DOWN=5l+4; LMHEAD=5L, ARGMAX=5L+1.
 Pools: memory pool = tiles that stream weights or KV (QKV, ATTN, OPROJ, UPGATE, DOWN,
 LMHEAD); compute pool = ARGMAX.  Within a wave memory tiles are placed before compute tiles.
 Rows per tile: (tile_bytes 0) about one tile per operator per SM -- such a tile streams through
-the page ring page by page; at batch > 1 the down projection, when its rows are longer than
-MMV_RANGE, holds its pages in tiles of about 131072 bytes; otherwise tiles of about tile_bytes.
+the page ring page by page; at batch > 1 rows longer than MMV_RANGE stream in slices of MMV_RANGE
+positions (pages: every row group of a slice, slice by slice), at most 64 rows per tile;
+otherwise tiles of about tile_bytes.
 Assignment, wave by wave: memory tiles sorted by (cost desc, tile id asc), then compute tiles
 likewise; each tile goes to the SM with the smallest accumulated cost (ties: lowest SM id) among
 the SMs holding fewer than ceil(n / S) of the n tiles of its pool in this wave; the accumulated
@@ -66,7 +67,7 @@ M64 = (1 << 64) - 1
 @dataclass
 class SchedOpts:
     page_bytes: int = 32768
-    tile_bytes: int = 0     # 0: per-SM tiles (batch > 1: 131072-byte down tiles when F > MMV_RANGE)
+    tile_bytes: int = 0     # 0: per-SM tiles (batch > 1: at most 64 down rows when F > MMV_RANGE)
     attn_chunk: int = 0     # 0: 64 positions, doubled up to 256 while B * n_kv * chunks > 152
     shuffle_seed: int = 0
     rows_qkv: int = 0   # 0: derived from tile_bytes
@@ -83,20 +84,21 @@ def kv_window(cfg, o: SchedOpts, b: int) -> int:
     return lim if lim else cfg.max_seq
 
 
-MMV_RANGE = 2048   # batch > 1: longest row whose tile streams (longer rows: the tile holds its pages)
+MMV_RANGE = 2048   # batch > 1: positions staged at a time; longer rows stream in slices of MMV_RANGE
 
 
 def tile_rows(cfg, o: SchedOpts, S: int) -> Dict[str, int]:
     """Rows (pairs for gate/up) per matvec tile.  tile_bytes 0: about one tile per operator per SM
     (QKV tiles at most head_dim rows, so a tile touches one or two KV groups); at batch > 1 the
-    down projection, when its rows are longer than MMV_RANGE, takes tiles of about 131072 bytes
-    (at most 8 rows).  Otherwise tiles of about tile_bytes.  Explicit rows_* override either."""
+    down (and output) projection, when its rows are longer than MMV_RANGE (streamed in row
+    slices), takes at most 64 rows.  Otherwise tiles of about tile_bytes.  Explicit rows_* override either."""
     H, F, V, d = cfg.hidden, cfg.ffn, cfg.vocab, cfg.head_dim
     qd = cfg.n_q_heads * cfg.head_dim
     nqkv = qd + 2 * cfg.n_kv_heads * d
     if o.tile_bytes == 0:
-        down = max(1, min(8, 131072 // (2 * F))) if (cfg.batch > 1 and F > MMV_RANGE) else ceil_div(H, S)
-        R = dict(qkv=min(d, ceil_div(nqkv, S)), o=ceil_div(H, S), up=ceil_div(F, S),
+        down = min(64, ceil_div(H, S)) if (cfg.batch > 1 and F > MMV_RANGE) else ceil_div(H, S)
+        o_rows = min(64, ceil_div(H, S)) if (cfg.batch > 1 and qd > MMV_RANGE) else ceil_div(H, S)
+        R = dict(qkv=min(d, ceil_div(nqkv, S)), o=o_rows, up=ceil_div(F, S),
                  down=down, lm=ceil_div(V, S))
     else:
         tb = o.tile_bytes
@@ -277,6 +279,9 @@ def tile_pages(t: Tile, cfg, o: SchedOpts) -> int:
     row groups in alternate pages); an attention tile streams its bytes contiguously."""
     if t.op in (QKV, OPROJ, UPGATE, DOWN, LMHEAD):
         K = cfg.q_dim if t.op == OPROJ else (cfg.ffn if t.op == DOWN else cfg.hidden)
+        if cfg.batch > 1 and K > MMV_RANGE:   # row slices of MMV_RANGE positions, slice-major
+            rps = o.page_bytes // (2 * MMV_RANGE)
+            return ceil_div(K, MMV_RANGE) * ceil_div(t.a1, rps)
         rpp = o.page_bytes // (2 * K)
         return ceil_div(t.a1, rpp) * (2 if t.op == UPGATE else 1)
     return ceil_div(t.stream_bytes, o.page_bytes)

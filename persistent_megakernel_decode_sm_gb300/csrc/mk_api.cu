@@ -102,7 +102,8 @@ extern "C" mk_status mk_device_sm_count(int32_t* out) {
 // device then trusts those fields) and writes the resolved weight stream of each matvec tile into
 // words 26..31 (source addresses and byte counts), so the loader on the device does no decoding.
 // Unknown opcodes are copied as they are: the device rejects them (MK_ERR_OPCODE).
-static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, std::vector<int32_t>& dq) {
+static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, const MvShape* mv, const int32_t* kslice,
+                                std::vector<int32_t>& dq) {
     const mk_model_cfg& c = s->cfg;
     const Geometry& g = s->geo;
     const int L = c.n_layers, H = c.hidden, F = c.ffn, V = c.vocab, B = c.batch, nkv = c.n_kv_heads;
@@ -171,11 +172,10 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, std::
                 break;
             default: break;
         }
-        if (src0) {   // whole rows per page; gate/up: gate and up row groups in alternate pages
-            const int64_t K = op == OP_OPROJ ? qd : (op == OP_DOWN ? F : H);
-            const int64_t rpp = g.page_bytes / (2 * K);
-            if (rpp < 1) return bad("a page holds no row");
-            const int64_t pages = ((a1 + rpp - 1) / rpp) * (op == OP_UPGATE ? 2 : 1);
+        if (src0) {   // whole rows (or row slices) per page; gate/up: gate and up row groups alternate
+            if (mv[op].rpp < 1) return bad("a page holds no row");
+            if (kslice[op] && (a1 + mv[op].rpp - 1) / mv[op].rpp > 8) return bad("sliced tile rows");   // (<= 4 row blocks)
+            const int64_t pages = mv_tile_pages(mv[op], kslice[op], a1, op == OP_UPGATE);
             if (pages != x[W_NPAGES] || b0 + b1 > (int64_t(1) << 31) - 1) return bad("page count");
             put64(x + W_SRC0, src0);
             put64(x + W_SRC1, src1);
@@ -260,15 +260,21 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     const int kmax = std::max(H, std::max(qd, c.ffn));
     const int cpl = (kmax / 8 + kMaxSeg - 1) / kMaxSeg <= 128 ? 4 : kMaxCpl;
     MvShape mv[OP_COUNT] = {};
+    int32_t kslice[OP_COUNT] = {};
     int comb_stride = 1;
     for (int op : {int(OP_QKV), int(OP_OPROJ), int(OP_UPGATE), int(OP_DOWN), int(OP_LMHEAD)}) {
         const int K = op == OP_OPROJ ? qd : (op == OP_DOWN ? c.ffn : H);
         mv[op] = mv_shape(K, cpl, g.page_bytes, xbuf);
-        if (mv[op].rpp < 1)
-            return fail(MK_ERR_CAPACITY, "a %d-byte page holds no %d-element row", g.page_bytes, K);
         if (mv[op].segch > 32 * cpl)
             return fail(MK_ERR_ARG, "matvec row length %d cannot be cut into %d segments", K, kMaxSeg);
-        comb_stride = std::max(comb_stride, mv[op].rpp * mv[op].G);   // (row, segment) units of a page
+        if (c.batch == 1)
+            comb_stride = std::max(comb_stride, mv[op].rpp * mv[op].G);   // (row, segment) units of a page
+        else if (K > kMmvRange) {   // pages of row slices (the tensor-core tiles stage a range at a time)
+            kslice[op] = kMmvRange;
+            mv[op].rpp = g.page_bytes / (2 * kMmvRange);
+        }
+        if (mv[op].rpp < 1)
+            return fail(MK_ERR_CAPACITY, "a %d-byte page holds no %d-element row", g.page_bytes, K);
     }
     const void* fn = c.batch > 1 ? mk_bat::megakernel_fn_batched() : megakernel_fn(cpl);
     int asf = hpg * g.n_chunk;
@@ -280,13 +286,9 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
         ++n_pages;
     if (n_pages < 1) return fail(MK_ERR_CAPACITY, "no room for a page ring");
     const int misc = smem_misc_bytes(n_pages, asf, qrf, xbuf, comb_stride);
-    // capacity: a matvec tile streams through the ring one group of two pages at a time, except at
-    // batch > 1 a tile whose rows are longer than kMmvRange (held until it is done); an attention
-    // tile holds its K and V rows
-    int need_pages = std::max<int>(2, int((2ll * g.attn_chunk * d * 2 + g.page_bytes - 1) / g.page_bytes));
-    if (c.batch > 1 && c.ffn > kMmvRange)
-        for (size_t i = 0; i < s->queues.size(); i += kWords)
-            if (s->queues[i + W_OP] == OP_DOWN) need_pages = std::max(need_pages, int(s->queues[i + W_NPAGES]));
+    // capacity: a matvec tile streams through the ring one group of two pages at a time; an
+    // attention tile holds its K and V rows
+    const int need_pages = std::max<int>(2, int((2ll * g.attn_chunk * d * 2 + g.page_bytes - 1) / g.page_bytes));
     if (n_pages < need_pages)
         return fail(MK_ERR_CAPACITY, "page ring of %d pages cannot hold the %d pages a step needs", n_pages, need_pages);
     const int smem = n_pages * g.page_bytes + misc;
@@ -343,7 +345,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
                  static_cast<const uint16_t*>(w->wgate_up[l]), static_cast<const uint16_t*>(w->wdown[l])};
     std::vector<int32_t> dq;
     {
-        const mk_status rs = resolve_queues(s, w, dq);
+        const mk_status rs = resolve_queues(s, w, mv, kslice, dq);
         if (rs != MK_OK) return bail(rs);
     }
     if ((e = cudaMemcpy(x->d_queues, dq.data(), qbytes, cudaMemcpyHostToDevice)) != cudaSuccess ||
@@ -354,7 +356,10 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     const ScratchLayout sl = scratch_layout(c, g, s->S);
     uint8_t* sb = static_cast<uint8_t*>(scratch);
     Params& p = x->base;
-    for (int op = 0; op < OP_COUNT; ++op) p.mv[op] = mv[op];
+    for (int op = 0; op < OP_COUNT; ++op) {
+        p.mv[op] = mv[op];
+        p.kslice[op] = kslice[op];
+    }
     p.L = L; p.H = H; p.nq = c.n_q_heads; p.nkv = c.n_kv_heads; p.d = d; p.F = c.ffn; p.V = c.vocab;
     p.B = c.batch; p.max_seq = c.max_seq; p.hpg = hpg; p.qd = qd; p.kvd = c.n_kv_heads * d;
     p.nqkv = qd + 2 * p.kvd;
@@ -438,7 +443,7 @@ extern "C" mk_status mk_rebind_schedule(mk_ctx* c, const mk_schedule* s) {
         s->totals != c->totals)
         return fail(MK_ERR_ARG, "the schedule differs from the bound one in more than placement and KV windows");
     std::vector<int32_t> dq;
-    const mk_status rs = resolve_queues(s, &c->w, dq);
+    const mk_status rs = resolve_queues(s, &c->w, c->base.mv, c->base.kslice, dq);
     if (rs != MK_OK) return rs;
     CK(cudaStreamSynchronize(c->stream));   // no launch reads the queues any more
     if (dq.size() > c->queue_words) {

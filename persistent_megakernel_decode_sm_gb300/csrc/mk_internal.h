@@ -53,6 +53,7 @@ constexpr int kCombWords = 12;       // partial words a consumer thread polls pe
 constexpr int kResBuf = 64;          // residual words of a tile's rows staged in shared memory (per buffer)
 constexpr int kMaxRingPages = 64;    // cap on the page ring's length (the shared memory sets the rest)
 constexpr int kMinXBuf = 3072;       // floats of the shared input buffer at least (attention scores, combine)
+constexpr int kMmvRange = 2048;      // batch > 1: positions of a row staged at a time (longer rows are sliced)
 constexpr int kAttnChunkTiles = 152; // default attention chunk: grown while a layer has more chunks
 
 
@@ -137,7 +138,7 @@ struct MvShape {
     int32_t G, logG;         // segments per row, log2
     int32_t segch;           // chunks per segment
     uint32_t rowbytes;       // 2 K
-    int32_t rpp;             // whole rows per page
+    int32_t rpp;             // rows per page (whole rows, or row slices)
     int32_t direct;          // 1: each warp polls its own input segment (no shared input buffer)
 };
 
@@ -153,6 +154,14 @@ MK_HD inline MvShape mv_shape(int K, int cpl, int page_bytes, int xbuf_floats) {
     m.rpp = page_bytes / int(m.rowbytes);
     m.direct = K > xbuf_floats ? 1 : 0;
     return m;
+}
+
+// pages of a matvec tile of `rows` rows (pairs for gate/up): whole rows per page (gate and up row
+// groups in alternate pages), or for sliced rows (kslice > 0): every row group of every slice,
+// slice-major
+MK_HD inline int64_t mv_tile_pages(const MvShape& m, int kslice, int64_t rows, bool pair) {
+    if (kslice) return ((m.K + kslice - 1) / kslice) * ((rows + m.rpp - 1) / m.rpp);
+    return ((rows + m.rpp - 1) / m.rpp) * (pair ? 2 : 1);
 }
 
 // ---- kernel parameters (passed by value) ----------------------------------------------------
@@ -212,6 +221,8 @@ struct Params {
     int32_t qrot_floats;
     int32_t xbuf_floats;     // shared input buffer (floats)
     int32_t comb_stride;     // (row, segment) units of a page, at most: partial words per page slot
+    int32_t kslice[OP_COUNT];  // by opcode: 0, pages hold whole rows; else (batch > 1, K > kMmvRange)
+                               // pages hold mv.rpp rows' slices of kslice positions, 2 kslice bytes apart
 };
 
 // one instruction slot: words + where its stream sits + the matvec shape.  16-byte aligned and
@@ -272,7 +283,6 @@ MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qr
 // sequences' rows then start 64 bytes apart in the banks); after the rows, the partial sums of two
 // 16-row blocks from the 8 consumer warps.  A thread polls at most kMmvItems 8-element chunks of
 // a range per round.
-constexpr int kMmvRange = 2048;
 constexpr int kMmvItems = 8;
 MK_HD inline uint32_t mmv_row_stride(int K) { return ((uint32_t((K + 31) / 32) * 128u + 127u) & ~127u) + 64u; }
 constexpr uint32_t kMmvPartBytes = 2u * kNumConsumerWarps * 16u * 8u * 4u;

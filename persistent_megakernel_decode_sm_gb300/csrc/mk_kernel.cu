@@ -28,6 +28,11 @@
 #include "mk_internal.h"
 
 namespace mk {
+#ifdef MK_BATCHED_TU
+constexpr bool kBatchedKernel = true;    // this unit holds the batch > 1 kernel
+#else
+constexpr bool kBatchedKernel = false;
+#endif
 
 enum Role : int { ROLE_LOADER = 1, ROLE_CONSUMER = 2, ROLE_PUBLISHER = 3, ROLE_COUNTER = 4, ROLE_DATA = 5 };
 
@@ -347,6 +352,7 @@ struct Stream {
     int pages;
     int inter;                       // gate/up tile: page 2j = gate rows [j rpp, (j+1) rpp), 2j+1 = up rows
     uint32_t rows, rowbytes, rpp;    // matvec: whole rows per page (0 rows: a plain byte stream)
+    uint32_t kslice, ngroups, K;     // matvec with row slices: positions per slice, row groups per slice
 };
 
 __device__ __forceinline__ int attn_old_rows(const Params& p, int b, int c, int chunk, int dpos) {
@@ -388,6 +394,7 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos
     st.kv_off = 0;
     st.inter = 0;
     st.rows = st.rowbytes = st.rpp = 0;
+    st.kslice = st.ngroups = st.K = 0;
     const int op = w[W_OP];
     if (is_matvec(op)) {   // whole rows per page; gate/up: gate and up row groups in alternate pages
         const uint32_t b0 = uint32_t(w[W_BYTES0]), b1 = uint32_t(w[W_BYTES1]);
@@ -400,11 +407,15 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos
         st.rowbytes = p.mv[op].rowbytes;
         st.rpp = uint32_t(p.mv[op].rpp);
         if (b0 == 0 || st.rpp == 0 || b0 != st.rows * st.rowbytes || b1 != (st.inter ? b0 : 0u)) return MK_ERR_BOUNDS;
-        st.pages = int((st.rows + st.rpp - 1u) / st.rpp) * (st.inter ? 2 : 1);
-        // (at batch > 1 a tile whose rows are longer than kMmvRange holds all its pages: it must fit
-        // the ring; every other matvec tile streams through it)
-        if (st.pages > w[W_NPAGES] || (p.B > 1 && p.mv[op].K > kMmvRange && st.pages > p.n_pages))
-            return MK_ERR_CAPACITY;
+        if (kBatchedKernel) {   // (row slices exist at batch > 1 only)
+            st.kslice = uint32_t(p.kslice[op]);
+            st.K = uint32_t(p.mv[op].K);
+            st.ngroups = (st.rows + st.rpp - 1u) / st.rpp;
+            st.pages = int(mv_tile_pages(p.mv[op], p.kslice[op], st.rows, st.inter));
+        } else {
+            st.pages = int((st.rows + st.rpp - 1u) / st.rpp) * (st.inter ? 2 : 1);
+        }
+        if (st.pages > w[W_NPAGES]) return MK_ERR_CAPACITY;   // (matvec tiles stream through the ring)
         return MK_OK;
     } else if (op == OP_ATTN) {
         const int l = w[W_LAYER], b = w[W_B], g = w[W_A0], c = w[W_A1], C = w[W_A2];
@@ -578,7 +589,14 @@ __device__ void loader(const Params& p, const Shared& sh) {
                     break;
                 }
                 uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
-                if (st.rows) {   // matvec: a group of whole rows (gate/up: gate rows on even pages, up rows on odd)
+                if (kBatchedKernel && st.rows && st.kslice) {   // matvec, row slices: slice pg / ngroups, group pg % ngroups
+                    const uint32_t sl = uint32_t(pg) / st.ngroups, r0 = (uint32_t(pg) % st.ngroups) * st.rpp;
+                    const uint32_t nr = min(st.rpp, st.rows - r0), k0 = sl * st.kslice, kn = min(st.kslice, st.K - k0);
+                    mbar_arrive_expect_tx(sh.full + ps, nr * kn * 2u);
+                    for (uint32_t r = 0; r < nr; ++r)   // one copy per row: rows 2 kslice bytes apart in the page
+                        bulk_g2s(dst + r * st.kslice * 2u, st.seg[0].src + size_t(r0 + r) * st.rowbytes + size_t(k0) * 2u,
+                                 kn * 2u, sh.full + ps, pol);
+                } else if (st.rows) {   // matvec: a group of whole rows (gate/up: gate rows on even pages, up rows on odd)
                     uint32_t bytes;
                     const uint8_t* psrc = mv_page(st, uint32_t(pg), bytes);
                     mbar_arrive_expect_tx(sh.full + ps, bytes);
@@ -1188,23 +1206,94 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
     const bool pair = si.inter != 0;
     const int K = m.K, R = si.rows, rpp = m.rpp, B = p.B;
     const int tid = c.warp * 32 + c.lane, g = c.lane >> 2, t4 = c.lane & 3;
-    const int KR = min(K, kMmvRange), RS = int(mmv_row_stride(KR));
+    // sliced rows (longer than kMmvRange): pages hold rpp rows' slices, slice-major; the sums of
+    // every row block of the tile persist over the slices (at most 4 blocks: 64 rows, scheduled so)
+    const int ksl = p.kslice[op];
+    const bool sliced = ksl != 0;
+    const int KR = sliced ? ksl : K, RS = int(mmv_row_stride(KR));
     uint8_t* stage = reinterpret_cast<uint8_t*>(c.sh.xbuf);
     float* part = reinterpret_cast<float*>(stage + uint32_t(p.xbuf_floats) * 4u - kMmvPartBytes);
     const uint32_t stage_s = smem_u32(stage), ring_base = smem_u32(c.sh.ring);
-    const int npg = si.n_pages, nsb = (rpp + 7) / 8, nblk = ((npg + 1) / 2) * nsb;
+    const int npg = si.n_pages;
+    const int ngrp = sliced ? (R + rpp - 1) / rpp : npg;   // row groups (pages of one slice) / pages
+    const int nsb = (rpp + 7) / 8;
+    const int nblk = ((ngrp + 1) / 2) * nsb;
+    const uint32_t pstride = sliced ? uint32_t(ksl) * 2u : m.rowbytes;   // bytes between a page's rows
     const int gs = min(g, B - 1);   // (columns past the batch read a valid row; unused)
     const uint16_t* gain;
     mmv_src(c, op, l, 0, gain);
-    const bool multi = K > KR;      // accumulators persist over the ranges (then at most 2 blocks)
-    float bv = -INFINITY;           // LM head: this lane's running (max, lowest index) for sequence lane % 8
+    float bv = -INFINITY;   // LM head: this lane's running (max, lowest index) for sequence lane % 8
     int bi = 0x7FFFFFFF;
-    float acc[2][2][4];
-    if (multi && nblk > 2) {   // (a tile of more than 4 pages with rows longer than a range: not scheduled)
-        raise_error(p, c.sh, MK_ERR_CAPACITY, ROLE_CONSUMER, pc, -1, uint32_t(nblk), 2u);
+    if (sliced && nblk > 4) {   // (not scheduled: the sliced operators' tiles take at most 64 rows)
+        raise_error(p, c.sh, MK_ERR_CAPACITY, ROLE_CONSUMER, pc, -1, uint32_t(nblk), 4u);
         return false;
     }
-    if (multi && !wait_pages(c, si, pc)) return false;   // (held tiles: the inputs are polled after)
+    float acc[4][2][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[q][h][e] = 0.f;
+    // block blk: rows g of page (group) 2 pj and g of 2 pj + 1 (pj = blk / nsb, row 8 (blk % nsb) + g)
+    auto block = [&](int blk, int slice, MmvBlk& bk) {
+        const int pj = blk / nsb, r = 8 * (blk % nsb) + g;
+        const int p0 = 2 * pj, p1 = p0 + 1;
+        const int row0 = pair ? pj * rpp + r : p0 * rpp + r;
+        const int row1 = pair ? row0 : p1 * rpp + r;
+        uint32_t s0, s1, phu;   // ring slots of the pair (a streamed tile wraps the ring many times)
+        tile_page(p, si, slice * ngrp + p0, s0, phu);
+        tile_page(p, si, slice * ngrp + p1, s1, phu);
+        bk.v0 = r < rpp && row0 < R;
+        bk.v1 = r < rpp && p1 < ngrp && row1 < R;
+        bk.a0 = ring_base + (s0 << p.page_shift) + uint32_t(r) * pstride;
+        bk.a1 = ring_base + (s1 << p.page_shift) + uint32_t(r) * pstride;
+    };
+    auto pair_pages = [&](int slice, int pj, bool release) -> bool {
+        for (int pg = 2 * pj; pg < min(2 * pj + 2, ngrp); ++pg) {
+            uint32_t slot, ph;
+            tile_page(p, si, slice * ngrp + pg, slot, ph);
+            if (!release) {
+                if (!wait_bar(p, c.sh, c.sh.full + slot, ph, ROLE_CONSUMER, pc)) return false;
+            } else if (c.lane == 0) {
+                mbar_arrive(c.sh.empty + slot);
+            }
+        }
+        return true;
+    };
+    // the outputs of blocks blk0 and blk0 + 1 from their sums: the 8 warps' partials meet in shared
+    // memory and are added in warp order
+    auto outputs = [&](int blk0, float (&a0)[2][4], float (&a1)[2][4]) -> bool {
+        const int nb = min(2, nblk - blk0);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float (&a)[2][4] = q == 0 ? a0 : a1;
+            float* pw = part + (q * kNumConsumerWarps + c.warp) * 128;
+            pw[g * 8 + 2 * t4] = a[0][0] + a[1][0];
+            pw[g * 8 + 2 * t4 + 1] = a[0][1] + a[1][1];
+            pw[(g + 8) * 8 + 2 * t4] = a[0][2] + a[1][2];
+            pw[(g + 8) * 8 + 2 * t4 + 1] = a[0][3] + a[1][3];
+        }
+        if (!cbar(c, pc)) return false;
+        {   // thread (block q, MMA row rr, column = sequence col)
+            const int q = tid >> 7, rr = (tid >> 3) & 15, col = tid & 7;
+            const int blk = blk0 + q;
+            if (q < nb && col < B && (!pair || rr < 8)) {
+                const int pj = blk / nsb, r = 8 * (blk % nsb) + (rr & 7);
+                const int pg = 2 * pj + (rr >> 3);
+                const int row = pair ? pj * rpp + r : pg * rpp + r;
+                if (r < rpp && pg < ngrp && row < R) {
+                    float s0 = 0.f, s1 = 0.f;
+                    for (int w = 0; w < kNumConsumerWarps; ++w) {
+                        s0 += part[(q * kNumConsumerWarps + w) * 128 + rr * 8 + col];
+                        if (pair) s1 += part[(q * kNumConsumerWarps + w) * 128 + (rr + 8) * 8 + col];
+                    }
+                    mv_epilogue<false>(c, si, pc, col, row, s0, s1, nullptr, bv, bi);
+                }
+            }
+        }
+        return cbar(c, pc);   // the partial area is reused
+    };
     for (int k0 = 0; k0 < K; k0 += KR) {
         const int kr = min(KR, K - k0), csr = kr / 8, items = B * csr;
         // 1. the range's inputs, every element polled until it carries this step's tag and stored
@@ -1244,8 +1333,8 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                 q = warp_sum(q);
                 if (c.lane == 0) c.sh.red[48 + c.warp] = rsqrtf(q / float(K) + p.rms_eps);
             }
+            if (!cbar(c, pc)) return false;
         }
-        if (!cbar(c, pc)) return false;
         // 2. in place, each thread its own items: x (* 1 / rms * gain) -> (hi, lo) word pairs
         for (int i = tid; i < items; i += kConsumerThreads) {
             const int s = i / csr, ci = i % csr;
@@ -1272,92 +1361,50 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
             w4[1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
         if (!cbar(c, pc)) return false;   // staged words visible; the partial area and the scales are free again
-        // 3. the contraction of the range, two row blocks at a time
+        // 3. the contraction of the range
         const uint32_t xrow = stage_s + uint32_t(gs * RS);
-        for (int blk0 = 0; blk0 < nblk; blk0 += 2) {
-            const int nb = min(2, nblk - blk0);
-            MmvBlk bk[2];
+        if (sliced) {   // every block of this slice into its persistent sums; a pair of pages per block
+            const int sl = k0 / KR;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int blk = blk0 + q;
-                const int pj = blk / nsb, r = 8 * (blk % nsb) + g;
-                const int p0 = 2 * pj, p1 = p0 + 1;
-                const int row0 = pair ? pj * rpp + r : p0 * rpp + r;
-                const int row1 = pair ? row0 : p1 * rpp + r;
-                uint32_t s0, s1, ph_unused;   // ring slots of the pair (a streamed tile wraps the ring many times)
-                tile_page(p, si, p0, s0, ph_unused);
-                tile_page(p, si, p1, s1, ph_unused);
-                bk[q].v0 = q < nb && r < rpp && row0 < R;
-                bk[q].v1 = q < nb && r < rpp && p1 < npg && row1 < R;
-                bk[q].a0 = ring_base + (s0 << p.page_shift) + uint32_t(r) * m.rowbytes;
-                bk[q].a1 = ring_base + (s1 << p.page_shift) + uint32_t(r) * m.rowbytes;
+            for (int q = 0; q < 4; ++q) {
+                if (q >= nblk) break;
+                if (!pair_pages(sl, q, false)) return false;
+                MmvBlk bk;
+                block(q, sl, bk);
+                mmv_steps(c, bk, xrow, 0, kr, acc[q]);   // (the slice starts at position 0 of its page)
+                __syncwarp();
+                pair_pages(sl, q, true);
             }
-            if (!multi || k0 == 0)
+            if (k0 + KR < K) {
+                if (!cbar(c, pc)) return false;   // the next slice restages the inputs
+                continue;
+            }
+            for (int blk0 = 0; blk0 < nblk; blk0 += 2)
+                if (!(blk0 == 0 ? outputs(0, acc[0], acc[1]) : outputs(2, acc[2], acc[3]))) return false;
+        } else {   // two row blocks at a time; a pair of pages is waited for at its first block and
+                   // given back after its last
+            for (int blk0 = 0; blk0 < nblk; blk0 += 2) {
+                const int nb = min(2, nblk - blk0);
 #pragma unroll
-                for (int q = 0; q < 2; ++q)
+                for (int q = 0; q < 2; ++q) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc[q][h][e] = 0.f;
-            if (multi) {   // the tile holds its pages: the next range adds to the same accumulators
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    if (q < nb) mmv_steps(c, bk[q], xrow, k0, kr, acc[q]);
-                if (k0 + KR < K) continue;
-                if (blk0 + 2 >= nblk) release_pages(c, si);   // this warp's last page read
-            } else {   // streaming: a pair of pages is waited for at its first block, given back after its last
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    if (q >= nb) break;
+                    if (q >= nb) continue;
                     const int blk = blk0 + q, pj = blk / nsb;
-                    if (blk % nsb == 0)
-                        for (int pg = 2 * pj; pg < min(2 * pj + 2, npg); ++pg) {
-                            uint32_t slot, ph;
-                            tile_page(p, si, pg, slot, ph);
-                            if (!wait_bar(p, c.sh, c.sh.full + slot, ph, ROLE_CONSUMER, pc)) return false;
-                        }
-                    mmv_steps(c, bk[q], xrow, k0, kr, acc[q]);
+                    if (blk % nsb == 0 && !pair_pages(0, pj, false)) return false;
+                    MmvBlk bk;
+                    block(blk, 0, bk);
+                    mmv_steps(c, bk, xrow, k0, kr, acc[q]);
                     if (blk % nsb == nsb - 1 || blk == nblk - 1) {
                         __syncwarp();
-                        if (c.lane == 0)
-                            for (int pg = 2 * pj; pg < min(2 * pj + 2, npg); ++pg) {
-                                uint32_t slot, ph;
-                                tile_page(p, si, pg, slot, ph);
-                                mbar_arrive(c.sh.empty + slot);
-                            }
+                        pair_pages(0, pj, true);
                     }
                 }
+                if (!outputs(blk0, acc[0], acc[1])) return false;
             }
-            // D (row g, column 2 t4 + {0, 1}) and (row g + 8, ...): hi and lo chains added
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float* pw = part + (q * kNumConsumerWarps + c.warp) * 128;
-                pw[g * 8 + 2 * t4] = acc[q][0][0] + acc[q][1][0];
-                pw[g * 8 + 2 * t4 + 1] = acc[q][0][1] + acc[q][1][1];
-                pw[(g + 8) * 8 + 2 * t4] = acc[q][0][2] + acc[q][1][2];
-                pw[(g + 8) * 8 + 2 * t4 + 1] = acc[q][0][3] + acc[q][1][3];
-            }
-            if (!cbar(c, pc)) return false;
-            {   // outputs of the two blocks: thread (block q, MMA row rr, column = sequence col)
-                const int q = tid >> 7, rr = (tid >> 3) & 15, col = tid & 7;
-                const int blk = blk0 + q;
-                if (q < nb && col < B && (!pair || rr < 8)) {
-                    const int pj = blk / nsb, r = 8 * (blk % nsb) + (rr & 7);
-                    const int pg = 2 * pj + (rr >> 3);
-                    const int row = pair ? pj * rpp + r : pg * rpp + r;
-                    if (r < rpp && pg < npg && row < R) {
-                        float s0 = 0.f, s1 = 0.f;
-                        for (int w = 0; w < kNumConsumerWarps; ++w) {
-                            s0 += part[(q * kNumConsumerWarps + w) * 128 + rr * 8 + col];
-                            if (pair) s1 += part[(q * kNumConsumerWarps + w) * 128 + (rr + 8) * 8 + col];
-                        }
-                        mv_epilogue<false>(c, si, pc, col, row, s0, s1, nullptr, bv, bi);
-                    }
-                }
-            }
-            if (!cbar(c, pc)) return false;   // the partial area is reused
         }
-        if (k0 + KR < K && !cbar(c, pc)) return false;   // (the next range restages the inputs)
     }
     if (op == OP_LMHEAD) {   // per sequence: this warp's running best (lanes col, col + 8, col + 16, col + 24)
 #pragma unroll
@@ -1603,6 +1650,55 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     return true;
 }
 
+#ifdef MK_BATCHED_TU
+// (the batch > 1 kernel: the rotated q read once into registers -- in the batch-1 kernel those
+// registers would reshape the matvec path's allocation)
+// Scores of one attention chunk for heads h0 .. h0 + HPG - 1: sc[h][t] = (q_h . k_t) * scale for
+// t < n (row n_old is the new key), d/8 consecutive lanes sharing a position.  The HPG heads are
+// unrolled at compile time (the caller takes four at a time); heads past hpg are computed on a
+// clamped head and not stored.
+template <int HPG>
+__device__ __forceinline__ void attn_scores_q(const Cw& c, int tid, int n, int n_old, int h0, int hpg, int C,
+                                            const uint8_t* kbase, bool k1p, uint32_t first_slot, float* sc) {
+    const Params& p = c.p;
+    const int d = p.d, cpr = d / 8;
+    const uint32_t rowb = uint32_t(d) * 2u;
+    // a thread always takes the same 8-element chunk j of its rows (the thread count is a multiple
+    // of d / 8): the rotated q of that chunk is read once, into registers
+    const int j = tid % cpr;
+    float q[HPG][8];
+#pragma unroll
+    for (int h = 0; h < HPG; ++h) {
+        const float4 qa = *reinterpret_cast<const float4*>(c.sh.qrot + min(h0 + h, hpg - 1) * d + j * 8);
+        const float4 qb = *reinterpret_cast<const float4*>(c.sh.qrot + min(h0 + h, hpg - 1) * d + j * 8 + 4);
+        q[h][0] = qa.x; q[h][1] = qa.y; q[h][2] = qa.z; q[h][3] = qa.w;
+        q[h][4] = qb.x; q[h][5] = qb.y; q[h][6] = qb.z; q[h][7] = qb.w;
+    }
+    for (int base = 0; base < n * cpr; base += kConsumerThreads) {
+        const int idx = base + tid;
+        const bool valid = idx < n * cpr;
+        const int t = idx / cpr;
+        float part[HPG];
+        if (valid) {
+            const uint32_t off = uint32_t(t) * rowb + uint32_t(j) * 16u;
+            const uint4 kv = (t < n_old) ? *reinterpret_cast<const uint4*>(k1p ? kbase + off : ring_ptr(c.sh, p, first_slot, off))
+                                         : *reinterpret_cast<const uint4*>(c.sh.knew + j * 8);
+#pragma unroll
+            for (int h = 0; h < HPG; ++h) part[h] = dot8(kv, q[h], 0.f);
+        } else {
+#pragma unroll
+            for (int h = 0; h < HPG; ++h) part[h] = 0.f;
+        }
+        for (int o = 1; o < cpr; o <<= 1)
+#pragma unroll
+            for (int h = 0; h < HPG; ++h) part[h] += __shfl_xor_sync(0xFFFFFFFFu, part[h], o);
+        if (valid && j == 0)
+#pragma unroll
+            for (int h = 0; h < HPG; ++h)
+                if (h0 + h < hpg) sc[(h0 + h) * C + t] = part[h] * p.attn_scale;
+    }
+}
+#endif
 // Scores of one attention chunk: sc[h][t] = (q_h . k_t) * scale for t < n (row n_old is the new
 // key), d/8 consecutive lanes sharing a position.  HPG heads are unrolled at compile time; a head
 // count other than 4 runs the kMaxHpg variant with heads past hpg computed on a clamped head and
@@ -1715,8 +1811,13 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         const uint8_t* kbase = ring_ptr(c.sh, p, first_slot, 0u);
         const uint8_t* vbase = ring_ptr(c.sh, p, first_slot, voff);
         // 2. scores s[h][t] = (q_h . k_t) * scale; d/8 consecutive lanes share a position
+#ifdef MK_BATCHED_TU
+        for (int h0 = 0; h0 < hpg; h0 += 4)   // four heads at a time
+            attn_scores_q<4>(c, tid, n, n_old, h0, hpg, C, kbase, k1p, first_slot, sc);
+#else
         if (hpg == 4) attn_scores<4>(c, tid, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
         else attn_scores<kMaxHpg>(c, tid, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
+#endif
         if (!cbar(c, pc)) return false;
         // 3. softmax pieces per head (warp h): m, w_t = exp(s_t - m), l = sum w_t
         if (c.warp < hpg) {
@@ -1746,6 +1847,14 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
             if (v1p) {
                 const uint16_t* vcol = reinterpret_cast<const uint16_t*>(vbase) + e;
                 int t = 0;
+                if (kBatchedKernel && (C & 3) == 0)   // four weights per shared-memory read (16-byte aligned rows)
+                    for (; t + 4 <= n_old; t += 4) {
+                        const float4 w4 = *reinterpret_cast<const float4*>(wts + t);
+                        a4[0] = fmaf(w4.x, bf16f(vcol[t * d]), a4[0]);
+                        a4[1] = fmaf(w4.y, bf16f(vcol[(t + 1) * d]), a4[1]);
+                        a4[2] = fmaf(w4.z, bf16f(vcol[(t + 2) * d]), a4[2]);
+                        a4[3] = fmaf(w4.w, bf16f(vcol[(t + 3) * d]), a4[3]);
+                    }
                 for (; t + 4 <= n_old; t += 4)
 #pragma unroll
                     for (int r = 0; r < 4; ++r) a4[r] = fmaf(wts[t + r], bf16f(vcol[(t + r) * d]), a4[r]);

@@ -24,8 +24,8 @@
 //  * pools: memory = tiles that stream weights or KV, compute = argmax; within a wave memory
 //    tiles are placed first;
 //  * rows per tile: about one tile per operator per SM (streamed through the page ring page by
-//    page, whole rows per page) -- at batch > 1 the down projection's tiles hold their pages and
-//    take about 131072 bytes when its rows are longer than kMmvRange -- or about tile_bytes;
+//    page, whole rows per page; at batch > 1 rows longer than kMmvRange in slices of kMmvRange
+//    positions, at most 64 rows per tile), or about tile_bytes;
 //  * placement: within a wave, tiles in (cost desc, id asc) order -- or a seeded splitmix64
 //    Fisher-Yates order when shuffle_seed != 0 -- each to the queue with the smallest
 //    accumulated cost (ties to the lowest SM) among the queues holding fewer than ceil(n / S)
@@ -158,14 +158,14 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     // the page ring page by page, so it need not fit the ring, and the per-tile costs (dispatch,
     // input vector, first touch of its pages, completion) are paid once per operator and SM.  QKV
     // tiles keep <= head_dim rows (a tile then touches at most two KV groups).  At batch > 1 an
-    // operator whose rows are longer than kMmvRange (the MLP down projection) holds its pages for
-    // the tile, which then takes about 131072 bytes so that it fits the ring.  An explicit
-    // tile_bytes: tiles of about tile_bytes.
+    // operator whose rows are longer than kMmvRange (the MLP down projection) streams pages of row
+    // slices, slice-major, and its tiles take at most 64 rows.  An explicit tile_bytes: tiles of
+    // about tile_bytes.
     if (g.tile_bytes == 0) {
         g.r_qkv = std::min(d, cdiv(nqkv, S));
-        g.r_o = cdiv(H, S);
+        g.r_o = (B > 1 && qd > kMmvRange) ? std::min(64, cdiv(H, S)) : cdiv(H, S);   // (sliced: <= 4 row blocks)
         g.r_up = cdiv(F, S);
-        g.r_dn = (B > 1 && F > kMmvRange) ? fit(8, 131072, 2ll * F) : cdiv(H, S);
+        g.r_dn = (B > 1 && F > kMmvRange) ? std::min(64, cdiv(H, S)) : cdiv(H, S);
         g.r_lm = cdiv(V, S);
     } else {
         const int64_t tb = g.tile_bytes ? g.tile_bytes : 131072;
@@ -182,6 +182,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     if (o.rows_down) g.r_dn = o.rows_down;
     if (o.rows_lm) g.r_lm = o.rows_lm;
     if (g.r_qkv < 1 || g.r_qkv > d) return fail(MK_ERR_ARG, "rows_qkv must be in [1, head_dim]");
+    if (B > 1 && ((qd > kMmvRange && g.r_o > 64) || (F > kMmvRange && g.r_dn > 64)))
+        return fail(MK_ERR_ARG, "at batch > 1 a tile of rows longer than %d takes at most 64 rows", kMmvRange);
     if (g.r_o < 1 || g.r_up < 1 || g.r_lm < 1 || g.r_dn < 1) return fail(MK_ERR_ARG, "rows per tile must be >= 1");
     if (g.page_bytes < 2 * std::max(H, std::max(qd, F)))   // matvec tiles stream whole rows per page
         return fail(MK_ERR_ARG, "page_bytes %d holds no matvec row (%d bytes)", g.page_bytes, 2 * std::max(H, std::max(qd, F)));
@@ -339,8 +341,13 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
             int64_t pages = (t.stream_bytes + g.page_bytes - 1) / g.page_bytes;
             if (t.op == OP_QKV || t.op == OP_OPROJ || t.op == OP_UPGATE || t.op == OP_DOWN || t.op == OP_LMHEAD) {
                 const int64_t K = t.op == OP_OPROJ ? qd : (t.op == OP_DOWN ? F : H);
-                const int64_t rpp = g.page_bytes / (2 * K);
-                pages = ((t.a1 + rpp - 1) / rpp) * (t.op == OP_UPGATE ? 2 : 1);
+                if (B > 1 && K > kMmvRange) {   // row slices of kMmvRange positions, slice-major
+                    const int64_t rps = g.page_bytes / (2 * kMmvRange);
+                    pages = ((K + kMmvRange - 1) / kMmvRange) * ((t.a1 + rps - 1) / rps);
+                } else {
+                    const int64_t rpp = g.page_bytes / (2 * K);
+                    pages = ((t.a1 + rpp - 1) / rpp) * (t.op == OP_UPGATE ? 2 : 1);
+                }
             }
             if (pages > (1 << 20)) { delete sch; return fail(MK_ERR_CAPACITY, "tile too large"); }
             w[W_NPAGES] = int32_t(pages);
