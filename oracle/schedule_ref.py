@@ -34,9 +34,10 @@ the page ring page by page; at batch > 1 rows longer than MMV_RANGE stream in sl
 positions (pages: every row group of a slice, slice by slice), at most 64 rows per tile;
 otherwise tiles of about tile_bytes.
 Assignment, wave by wave: memory tiles sorted by (cost desc, tile id asc), then compute tiles
-likewise; each tile goes to the SM with the smallest accumulated cost (ties: lowest SM id) among
-the SMs holding fewer than ceil(n / S) of the n tiles of its pool in this wave; the accumulated
-cost carries across waves.  cost = streamed bytes + TILE_OVERHEAD.
+likewise; the k-th tile of that order (from 0) goes to the SM with the smallest accumulated cost
+(ties: lowest SM id) among the SMs holding at most k // S of the pool's tiles in this wave -- the
+placement runs in rounds of S tiles, one per SM -- and the accumulated cost carries across waves.
+cost = streamed bytes + TILE_OVERHEAD.
 With a non-zero shuffle seed the wave's tiles are instead put in a splitmix64 Fisher-Yates
 order (pools still kept apart) -- the "shuffled assignment" used to test determinism.
 Queue of an SM: its tiles wave by wave, in tile-id order within a wave (so the combining
@@ -315,7 +316,7 @@ def build_schedule(cfg, S: int, opts: Optional[SchedOpts] = None):
         by_wave.setdefault(t.wave, []).append(t)
     rng = SplitMix64(o.shuffle_seed) if o.shuffle_seed else None
     # each tile, in order, to the SM with the smallest accumulated cost (ties: lowest SM) among
-    # those holding fewer than ceil(n / S) of the wave's tiles of its pool
+    # those holding at most k // S of the wave's tiles of its pool (rounds of S tiles, one per SM)
     acc = np.zeros(S, dtype=np.int64)
     per_sm: List[List[Tile]] = [[] for _ in range(S)]
     for wv in sorted(by_wave):
@@ -327,10 +328,10 @@ def build_schedule(cfg, S: int, opts: Optional[SchedOpts] = None):
             pools = [_shuffle(mem, rng), _shuffle(cmp_, rng)]
         start = [len(q) for q in per_sm]
         for pool in pools:
-            cap = ceil_div(len(pool), S)
             in_wave = np.zeros(S, dtype=np.int64)
             big = np.iinfo(np.int64).max
-            for t in pool:
+            for k, t in enumerate(pool):
+                cap = k // S + 1   # round k // S: every SM takes a tile of it before any takes another
                 s = int(np.argmin(np.where(in_wave < cap, acc, big)))   # first minimum: lowest SM
                 per_sm[s].append(t)
                 acc[s] += t.cost

@@ -252,6 +252,9 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
         const int kmx = std::max(H, std::max(qd, c.ffn));
         const uint32_t stage = uint32_t(c.batch) * mmv_row_stride(std::min(kmx, kMmvRange));
         xbuf = std::max(xbuf, int((stage + kMmvPartBytes) / 4u));
+        // attention: scores [hpg][C], weights [C][hp], one partial output per consumer warp [8][hp][d]
+        const int hp = hpg <= 4 ? 4 : kMaxHpg;
+        xbuf = std::max(xbuf, ((hpg * g.attn_chunk + 3) & ~3) + g.attn_chunk * hp + kNumConsumerWarps * hp * d);
     }
     if (hpg * g.attn_chunk > xbuf)
         return fail(MK_ERR_ARG, "attn_chunk %d: the scores of %d heads do not fit %d floats", g.attn_chunk, hpg, xbuf);

@@ -1651,52 +1651,121 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
 }
 
 #ifdef MK_BATCHED_TU
-// (the batch > 1 kernel: the rotated q read once into registers -- in the batch-1 kernel those
-// registers would reshape the matvec path's allocation)
-// Scores of one attention chunk for heads h0 .. h0 + HPG - 1: sc[h][t] = (q_h . k_t) * scale for
-// t < n (row n_old is the new key), d/8 consecutive lanes sharing a position.  The HPG heads are
-// unrolled at compile time (the caller takes four at a time); heads past hpg are computed on a
-// clamped head and not stored.
-template <int HPG>
-__device__ __forceinline__ void attn_scores_q(const Cw& c, int tid, int n, int n_old, int h0, int hpg, int C,
-                                            const uint8_t* kbase, bool k1p, uint32_t first_slot, float* sc) {
+// (the batch > 1 kernel only: in the batch-1 kernel these registers would reshape the matvec
+// path's allocation)
+// bf16x2 of (a, b) (a in the low half), or of their rounding remainders
+__device__ __forceinline__ uint32_t bf_part2(float a, float b, bool lo) {
+    const uint32_t h = bf16x2_rn(a, b);
+    return lo ? bf16x2_rn(a - bf_lo(h), b - bf_hi(h)) : h;
+}
+// Scores of one attention chunk on the tensor cores: sc[h][t] = (q_h . k_t) * scale for t < n
+// (row n_old is the new key).  An MMA (m16n8k16) takes 16 positions (rows) over 16 elements of
+// head_dim against 8 columns: the bf16 high parts of four heads' rotated q, then their remainders,
+// so the two column halves add up to the fp32 q.  A lane's 16-byte load of a K row covers two MMAs:
+// within each 32 elements, lane quad t4 takes elements 8 t4 .. 8 t4 + 7 (the same order for the q
+// columns -- the contraction does not depend on it).  Warp w takes the 16-row blocks w, w + 8, ...
+template <int NP>   // head_dim / 32
+__device__ __forceinline__ void attn_scores_mma(const Cw& c, int n, int n_old, int hpg, int C, const uint8_t* kbase,
+                                                bool k1p, uint32_t first_slot, float* sc) {
     const Params& p = c.p;
-    const int d = p.d, cpr = d / 8;
-    const uint32_t rowb = uint32_t(d) * 2u;
-    // a thread always takes the same 8-element chunk j of its rows (the thread count is a multiple
-    // of d / 8): the rotated q of that chunk is read once, into registers
-    const int j = tid % cpr;
-    float q[HPG][8];
+    constexpr int d = NP * 32;
+    constexpr uint32_t rowb = uint32_t(d) * 2u;
+    const int g = c.lane >> 2, t4 = c.lane & 3;
+    const int nmt = (n + 15) >> 4;
+    const uint8_t* knew = reinterpret_cast<const uint8_t*>(c.sh.knew);
+    for (int h0 = 0; h0 < hpg; h0 += 4) {
+        uint32_t bq[NP][4];   // column g: head h0 + g % 4, high part (g < 4) or remainder
+        {
+            const float* qh = c.sh.qrot + min(h0 + (g & 3), hpg - 1) * d + 8 * t4;
+            const bool lo = g >= 4;
 #pragma unroll
-    for (int h = 0; h < HPG; ++h) {
-        const float4 qa = *reinterpret_cast<const float4*>(c.sh.qrot + min(h0 + h, hpg - 1) * d + j * 8);
-        const float4 qb = *reinterpret_cast<const float4*>(c.sh.qrot + min(h0 + h, hpg - 1) * d + j * 8 + 4);
-        q[h][0] = qa.x; q[h][1] = qa.y; q[h][2] = qa.z; q[h][3] = qa.w;
-        q[h][4] = qb.x; q[h][5] = qb.y; q[h][6] = qb.z; q[h][7] = qb.w;
-    }
-    for (int base = 0; base < n * cpr; base += kConsumerThreads) {
-        const int idx = base + tid;
-        const bool valid = idx < n * cpr;
-        const int t = idx / cpr;
-        float part[HPG];
-        if (valid) {
-            const uint32_t off = uint32_t(t) * rowb + uint32_t(j) * 16u;
-            const uint4 kv = (t < n_old) ? *reinterpret_cast<const uint4*>(k1p ? kbase + off : ring_ptr(c.sh, p, first_slot, off))
-                                         : *reinterpret_cast<const uint4*>(c.sh.knew + j * 8);
-#pragma unroll
-            for (int h = 0; h < HPG; ++h) part[h] = dot8(kv, q[h], 0.f);
-        } else {
-#pragma unroll
-            for (int h = 0; h < HPG; ++h) part[h] = 0.f;
+            for (int pp = 0; pp < NP; ++pp) {
+                const float4 qa = *reinterpret_cast<const float4*>(qh + 32 * pp);
+                const float4 qb = *reinterpret_cast<const float4*>(qh + 32 * pp + 4);
+                bq[pp][0] = bf_part2(qa.x, qa.y, lo);
+                bq[pp][1] = bf_part2(qa.z, qa.w, lo);
+                bq[pp][2] = bf_part2(qb.x, qb.y, lo);
+                bq[pp][3] = bf_part2(qb.z, qb.w, lo);
+            }
         }
-        for (int o = 1; o < cpr; o <<= 1)
+        for (int mt = c.warp; mt < nmt; mt += kNumConsumerWarps) {
+            const int r0 = mt * 16 + g, r1 = r0 + 8;
+            auto row = [&](int r) -> const uint8_t* {   // (rows past n read the new key; not stored)
+                if (r < n_old) return k1p ? kbase + uint32_t(r) * rowb : ring_ptr(c.sh, p, first_slot, uint32_t(r) * rowb);
+                return knew;
+            };
+            const uint8_t* a0p = row(r0) + 16 * t4;
+            const uint8_t* a1p = row(r1) + 16 * t4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int h = 0; h < HPG; ++h) part[h] += __shfl_xor_sync(0xFFFFFFFFu, part[h], o);
-        if (valid && j == 0)
+            for (int pp = 0; pp < NP; ++pp) {
+                const uint4 A0 = *reinterpret_cast<const uint4*>(a0p + 64 * pp);
+                const uint4 A1 = *reinterpret_cast<const uint4*>(a1p + 64 * pp);
+                mma16816(acc, A0.x, A1.x, A0.y, A1.y, bq[pp][0], bq[pp][1]);
+                mma16816(acc, A0.z, A1.z, A0.w, A1.w, bq[pp][2], bq[pp][3]);
+            }
+            // D (row, column 2 t4 + {0, 1}): quads t4 and t4 ^ 2 hold the two parts of the same heads
 #pragma unroll
-            for (int h = 0; h < HPG; ++h)
-                if (h0 + h < hpg) sc[(h0 + h) * C + t] = part[h] * p.attn_scale;
+            for (int e = 0; e < 4; ++e) acc[e] += __shfl_xor_sync(0xFFFFFFFFu, acc[e], 2);
+            if (t4 < 2) {
+                const int h = h0 + 2 * t4;
+                if (r0 < n) {
+                    if (h < hpg) sc[h * C + r0] = acc[0] * p.attn_scale;
+                    if (h + 1 < hpg) sc[(h + 1) * C + r0] = acc[1] * p.attn_scale;
+                }
+                if (r1 < n) {
+                    if (h < hpg) sc[h * C + r1] = acc[2] * p.attn_scale;
+                    if (h + 1 < hpg) sc[(h + 1) * C + r1] = acc[3] * p.attn_scale;
+                }
+            }
+        }
     }
+}
+// o partial of one consumer warp: sum over its positions t = warp, warp + 8, ... < n of
+// w[t][h] v_t[e] (row n_old is the new value), lane the EPL elements EPL lane .. EPL lane + EPL - 1
+// of every head; written to pw[warp][h][e].  One V row is one contiguous read of the warp.
+template <int EPL, int HP>   // head_dim / 32; heads padded to HP
+__device__ __forceinline__ void attn_pv_warp(const Cw& c, int n, int n_old, int hpg, const uint8_t* vbase, bool v1p,
+                                             uint32_t first_slot, uint32_t voff, const float* wT, float* pw) {
+    const Params& p = c.p;
+    constexpr int d = EPL * 32;
+    constexpr uint32_t rowb = uint32_t(d) * 2u;
+    float acc[HP][EPL];
+#pragma unroll
+    for (int h = 0; h < HP; ++h)
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) acc[h][i] = 0.f;
+    const uint8_t* vnew = reinterpret_cast<const uint8_t*>(c.sh.vnew);
+#pragma unroll 4
+    for (int t = c.warp; t < n; t += kNumConsumerWarps) {
+        const uint8_t* vr = t < n_old ? (v1p ? vbase + uint32_t(t) * rowb : ring_ptr(c.sh, p, first_slot, voff + uint32_t(t) * rowb))
+                                      : vnew;
+        float v[EPL];
+        if constexpr (EPL == 1) {
+            v[0] = bf16f(*reinterpret_cast<const uint16_t*>(vr + c.lane * 2));
+        } else if constexpr (EPL == 2) {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(vr + c.lane * 4);
+            v[0] = bf_lo(u); v[1] = bf_hi(u);
+        } else {
+            const uint2 u = *reinterpret_cast<const uint2*>(vr + c.lane * 8);
+            v[0] = bf_lo(u.x); v[1] = bf_hi(u.x); v[2] = bf_lo(u.y); v[3] = bf_hi(u.y);
+        }
+        float w[HP];
+#pragma unroll
+        for (int h4 = 0; h4 < HP; h4 += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(wT + t * HP + h4);
+            w[h4] = w4.x; w[h4 + 1] = w4.y; w[h4 + 2] = w4.z; w[h4 + 3] = w4.w;
+        }
+#pragma unroll
+        for (int h = 0; h < HP; ++h)
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) acc[h][i] = fmaf(w[h], v[i], acc[h][i]);
+    }
+#pragma unroll
+    for (int h = 0; h < HP; ++h)
+        if (h < hpg)
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) pw[(c.warp * HP + h) * d + c.lane * EPL + i] = acc[h][i];
 }
 #endif
 // Scores of one attention chunk: sc[h][t] = (q_h . k_t) * scale for t < n (row n_old is the new
@@ -1810,14 +1879,62 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         const bool v1p = n_old == 0 || (voff >> p.page_shift) == ((voff + kbytes - 1u) >> p.page_shift);
         const uint8_t* kbase = ring_ptr(c.sh, p, first_slot, 0u);
         const uint8_t* vbase = ring_ptr(c.sh, p, first_slot, voff);
-        // 2. scores s[h][t] = (q_h . k_t) * scale; d/8 consecutive lanes share a position
 #ifdef MK_BATCHED_TU
-        for (int h0 = 0; h0 < hpg; h0 += 4)   // four heads at a time
-            attn_scores_q<4>(c, tid, n, n_old, h0, hpg, C, kbase, k1p, first_slot, sc);
+        // 2. scores on the tensor cores; 3. softmax pieces per head (warp h), the weights stored
+        //    [t][head]; 4. each warp's o partial over its positions, then the 8 partials added in
+        //    warp order
+        const int hp = hpg <= 4 ? 4 : kMaxHpg;
+        float* wT = sc + ((hpg * C + 3) & ~3);       // [C][hp] (16-byte aligned rows)
+        float* pw = wT + C * hp;                     // [8][hp][d]
+        if (d == 64) attn_scores_mma<2>(c, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
+        else if (d == 128) attn_scores_mma<4>(c, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
+        else attn_scores_mma<1>(c, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
+        if (!cbar(c, pc)) return false;
+        if (c.warp < hpg) {
+            const int h = c.warp;
+            float m = -INFINITY;
+#pragma unroll 1
+            for (int t = c.lane; t < n; t += 32) m = fmaxf(m, sc[h * C + t]);
+            m = warp_max(m);
+            float s = 0.f;
+#pragma unroll 1
+            for (int t = c.lane; t < n; t += 32) {
+                const float e = expf(sc[h * C + t] - m);
+                wT[t * hp + h] = e;
+                s += e;
+            }
+            s = warp_sum(s);
+            if (c.lane == 0) { c.sh.ml[2 * h] = m; c.sh.ml[2 * h + 1] = s; }
+        }
+        if (!cbar(c, pc)) return false;
+        if (hp == 4) {
+            if (d == 64) attn_pv_warp<2, 4>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
+            else if (d == 128) attn_pv_warp<4, 4>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
+            else attn_pv_warp<1, 4>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
+        } else {
+            if (d == 64) attn_pv_warp<2, kMaxHpg>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
+            else if (d == 128) attn_pv_warp<4, kMaxHpg>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
+            else attn_pv_warp<1, kMaxHpg>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
+        }
+        release_pages(c, si);
+        if (!cbar(c, pc)) return false;
+        uint64_t* dst = p.part + ((lb * p.nkv + g) * p.n_chunk + ch) * size_t(hpg) * (d + 2);
+        for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
+            const int h = idx / d, e = idx % d;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kNumConsumerWarps; ++w) acc += pw[(w * hp + h) * d + e];
+            uint64_t* dh = dst + size_t(h) * (d + 2);
+            st_tag(dh + e, acc, c.tag);
+            if (e == 0) {
+                st_tag(dh + d, c.sh.ml[2 * h], c.tag);
+                st_tag(dh + d + 1, c.sh.ml[2 * h + 1], c.tag);
+            }
+        }
 #else
+        // 2. scores s[h][t] = (q_h . k_t) * scale; d/8 consecutive lanes share a position
         if (hpg == 4) attn_scores<4>(c, tid, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
         else attn_scores<kMaxHpg>(c, tid, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
-#endif
         if (!cbar(c, pc)) return false;
         // 3. softmax pieces per head (warp h): m, w_t = exp(s_t - m), l = sum w_t
         if (c.warp < hpg) {
@@ -1847,14 +1964,6 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
             if (v1p) {
                 const uint16_t* vcol = reinterpret_cast<const uint16_t*>(vbase) + e;
                 int t = 0;
-                if (kBatchedKernel && (C & 3) == 0)   // four weights per shared-memory read (16-byte aligned rows)
-                    for (; t + 4 <= n_old; t += 4) {
-                        const float4 w4 = *reinterpret_cast<const float4*>(wts + t);
-                        a4[0] = fmaf(w4.x, bf16f(vcol[t * d]), a4[0]);
-                        a4[1] = fmaf(w4.y, bf16f(vcol[(t + 1) * d]), a4[1]);
-                        a4[2] = fmaf(w4.z, bf16f(vcol[(t + 2) * d]), a4[2]);
-                        a4[3] = fmaf(w4.w, bf16f(vcol[(t + 3) * d]), a4[3]);
-                    }
                 for (; t + 4 <= n_old; t += 4)
 #pragma unroll
                     for (int r = 0; r < 4; ++r) a4[r] = fmaf(wts[t + r], bf16f(vcol[(t + r) * d]), a4[r]);
@@ -1873,6 +1982,7 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
             }
         }
         release_pages(c, si);
+#endif
     }
     // 5. the tile of the chunk that holds pos combines the group's active partials in chunk order:
     //    M = max_c m_c, f_c = exp(m_c - M), L = sum_c f_c l_c, o = sum_c f_c o_c / L.  The

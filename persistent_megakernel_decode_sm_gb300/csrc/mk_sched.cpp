@@ -28,8 +28,9 @@
 //    positions, at most 64 rows per tile), or about tile_bytes;
 //  * placement: within a wave, tiles in (cost desc, id asc) order -- or a seeded splitmix64
 //    Fisher-Yates order when shuffle_seed != 0 -- each to the queue with the smallest
-//    accumulated cost (ties to the lowest SM) among the queues holding fewer than ceil(n / S)
-//    of the wave's n tiles of that pool, the accumulated cost carried across waves;
+//    accumulated cost (ties to the lowest SM) among the queues holding at most k / S of the
+//    wave's tiles of that pool for the k-th tile (rounds of S tiles, one per SM), the
+//    accumulated cost carried across waves;
 //    cost = streamed bytes + a fixed per-tile overhead.  Each queue then runs its tiles of a wave
 //    in id order (so a wait inside a wave is always on tiles that every queue runs earlier).
 #include <algorithm>
@@ -270,8 +271,9 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
 
     // ---- placement ------------------------------------------------------------------------
     // each tile, in order, to the SM with the smallest accumulated cost (ties: lowest SM) among
-    // those holding fewer than ceil(n / S) of the wave's tiles of this pool (a wave is spread over
-    // the SMs before any SM takes a second tile of it)
+    // those holding at most k / S of the wave's tiles of this pool for the k-th tile: rounds of S
+    // tiles, one per SM, so tiles of neighbouring ids run at about the same time (an attention
+    // group's combining tile then waits on chunks of its own round or an earlier one)
     std::vector<int64_t> acc(S, 0);
     std::vector<int32_t> in_wave(S, 0);
     std::vector<std::vector<int32_t>> per_sm(S);
@@ -300,9 +302,10 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         std::vector<size_t> start(S);
         for (int32_t s = 0; s < S; ++s) start[s] = per_sm[s].size();
         for (auto* v : {&mem, &cmp}) {
-            const int32_t cap = cdiv(int64_t(v->size()), S);
             std::fill(in_wave.begin(), in_wave.end(), 0);
-            for (int32_t id : *v) {
+            for (size_t k = 0; k < v->size(); ++k) {
+                const int32_t id = (*v)[k];
+                const int32_t cap = int32_t(k / size_t(S)) + 1;   // round k / S: one tile per SM
                 int32_t best = -1;
                 for (int32_t s = 0; s < S; ++s)
                     if (in_wave[s] < cap && (best < 0 || acc[s] < acc[best])) best = s;
