@@ -103,17 +103,19 @@ mk_status mk_build_schedule(const mk_model_cfg* cfg, int32_t sm_count, const mk_
  * whole-model MegaKernel") lists the instruction queue as an int32 tensor of shape [S, Q, 32]
  * held in HBM for the life of the kernel; the word layout is this library's (the page gives none).
  * Errors: MK_ERR_ARG on a null argument.  Word layout of one instruction:
- *   [0] opcode (0 END, 1 QKV, 2 ATTN, 4 OPROJ, 5 UPGATE, 6 DOWN, 7 LMHEAD, 8 ARGMAX; 3 is
- *       reserved and rejected)
- *   [1] layer (n_layers for LMHEAD / ARGMAX)   [2] sequence b (attention, argmax)
+ *   [0] opcode (0 END, 1 QKV, 2 ATTN, 3 COMB, 4 OPROJ, 5 UPGATE, 6 DOWN, 7 LMHEAD, 8 ARGMAX;
+ *       COMB, the combine of one (sequence, KV group)'s chunk partials, exists at batch > 1 only)
+ *   [1] layer (n_layers for LMHEAD / ARGMAX)   [2] sequence b (attention, combine, argmax)
  *   [3] a0: first row | KV group             [4] a1: rows (pairs for UPGATE) | chunk | #LM tiles
- *   [5] a2: chunk length (ATTN) | LM tile index (LMHEAD)
+ *   [5] a2: chunk length (ATTN, COMB) | LM tile index (LMHEAD)
  *   [6] number of waits (<= 4)   [7..14] (counter, need) pairs
  *   [15] number of completions (<= 2)   [16..19] (counter, delta) pairs
  *   [20] pages of the largest stream the tile may need   [21] tile id   [22] wave
- *   [23] 1 = conditional completions (ATTN): only the tile whose chunk holds the step's
- *        position fires them; it combines the group's chunk partials, waiting inside its wave
- *        for the lower chunks (each queue runs its tiles of a wave in tile-id order)
+ *   [23] 1 = conditional completions (ATTN at batch 1): only the tile whose chunk holds the
+ *        step's position fires them; it combines the group's chunk partials, waiting inside its
+ *        wave for the lower chunks (each queue runs its tiles of a wave in tile-id order).  At
+ *        batch > 1 it is 0: the chunk tiles complete nothing and the group's COMB tile, of a
+ *        higher id in the same wave, waits for their partials, combines them and completes
  *   [24..31] 0 (the bound device copy carries the tile's resolved stream addresses in [26..31])
  * A wait is satisfied when counter - (epoch * total[counter] + need) >= 0 (mod 2^32).  END is
  * all zeros and pads every queue. */

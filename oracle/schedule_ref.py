@@ -15,11 +15,13 @@ Tiles (per layer l, in this order; ids are assigned in enumeration order):
           RMSNorm of the layer input is its prologue.
   ATTN    (b, g, c): sequence b, KV group g, KV positions [c*C, (c+1)*C) -- split-K decode
           attention; c runs over the chunks of the sequence's window [0, kv_limit[b]) (default
-          max_seq; chunks past pos do no work).  The
-          tile whose chunk holds the step's position (known at run time only) also does the
-          fixed-order log-sum-exp combine of the group's chunk partials, reading the lower
-          chunks' partials as they land, and alone carries the tile's completion (a conditional
-          completion).
+          max_seq; chunks past pos do no work).  At batch 1 the tile whose chunk holds the
+          step's position (known at run time only) also does the fixed-order log-sum-exp combine
+          of the group's chunk partials, reading the lower chunks' partials as they land, and
+          alone carries the tile's completion (a conditional completion); at batch > 1 the
+          chunk tiles complete nothing and
+  COMB    (b, g) (batch > 1 only, after every ATTN tile of the layer, in the same wave) does
+          that combine for the group and carries its completion.
   OPROJ   rows of Wo, residual add.
   UPGATE  row pairs [r, r+R_up) of gate and of up, SiLU(gate)*up epilogue.
   DOWN    rows of Wdown, residual add.
@@ -28,7 +30,8 @@ ARGMAX (b).
 Waves: the DAG's longest-path level; per layer QKV=5l, ATTN=5l+1, OPROJ=5l+2, UPGATE=5l+3,
 DOWN=5l+4; LMHEAD=5L, ARGMAX=5L+1.
 Pools: memory pool = tiles that stream weights or KV (QKV, ATTN, OPROJ, UPGATE, DOWN,
-LMHEAD); compute pool = ARGMAX.  Within a wave memory tiles are placed before compute tiles.
+LMHEAD); compute pool = COMB and ARGMAX.  Within a wave memory tiles are placed before compute
+tiles.
 Rows per tile: (tile_bytes 0) about one tile per operator per SM -- such a tile streams through
 the page ring page by page; at batch > 1 rows longer than MMV_RANGE stream in slices of MMV_RANGE
 positions (pages: every row group of a slice, slice by slice), at most 64 rows per tile;
@@ -224,9 +227,17 @@ def enumerate_tiles(cfg, o: SchedOpts, S: int) -> Tuple[List[Tile], Counters, Di
                 for c in range(nchunk):
                     if c * C >= kv_window(cfg, o, b):   # chunks past the sequence's window: no tile
                         break
-                    tiles.append(Tile(ATTN, l, b, g, c, C, 5 * l + 1,
-                                      [(cnt.qkv(l, g), qkv_tiles_of_group[g])],
-                                      [(cnt.comb(l), 1)], 2 * C * d * 2, cond=True))
+                    if B == 1:   # the chunk holding pos combines and completes
+                        tiles.append(Tile(ATTN, l, b, g, c, C, 5 * l + 1,
+                                          [(cnt.qkv(l, g), qkv_tiles_of_group[g])],
+                                          [(cnt.comb(l), 1)], 2 * C * d * 2, cond=True))
+                    else:        # combined by the group's COMB tile
+                        tiles.append(Tile(ATTN, l, b, g, c, C, 5 * l + 1,
+                                          [(cnt.qkv(l, g), qkv_tiles_of_group[g])], [], 2 * C * d * 2))
+        if B > 1:
+            for b in range(B):
+                for g in range(nkv):
+                    tiles.append(Tile(COMB, l, b, g, 0, C, 5 * l + 1, [], [(cnt.comb(l), 1)], 0))
         for t in range(n_o):
             r0 = t * R["o"]
             n = min(R["o"], H - r0)
@@ -377,13 +388,14 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
     * waits point only at counters produced in strictly lower waves, and each SM's queue is in
       non-decreasing wave order (the forward-progress rule: a waiter never holds an SM that a
       producer it waits on still needs);
-    * within a wave each SM's tiles are in increasing tile-id order, and the attention chunk
-      tiles of a group carry conditional completions (exactly one completion per group is
-      counted): the combining chunk tile's wait inside its wave is on lower chunks of its group,
-      i.e. on lower ids, which no queue runs after a higher id of that wave;
+    * within a wave each SM's tiles are in increasing tile-id order, and at batch 1 the
+      attention chunk tiles of a group carry conditional completions (exactly one completion per
+      group is counted): the combining chunk tile's wait inside its wave is on lower chunks of
+      its group, i.e. on lower ids, which no queue runs after a higher id of that wave (at
+      batch > 1 the COMB tile of the group waits likewise on the chunk tiles, all of lower id);
     * (DAG + per-SM program order) is acyclic -- implied by the points above;
-    * capacity: at most 4 waits and 2 completions per instruction; at batch > 1 no instruction
-      needs more pages than the ring holds.
+    * capacity: at most 4 waits and 2 completions per instruction; no attention tile needs more
+      pages than the ring holds.
     """
     o = opts or SchedOpts()
     errs: List[str] = []
@@ -421,9 +433,9 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
             last_wave, last_tid = t.wave, t.tid
             if len(t.waits) > MAX_WAIT or len(t.pubs) > MAX_PUB:
                 errs.append(f"tile {t.tid}: too many waits/completions")
-            if t.cond != (t.op == ATTN):
+            if t.cond != (t.op == ATTN and cfg.batch == 1):
                 errs.append(f"tile {t.tid}: conditional completions on a {OPNAMES[t.op]} tile"
-                            if t.cond else f"tile {t.tid}: attention tile without conditional completions")
+                            if t.cond else f"tile {t.tid}: batch-1 attention tile without conditional completions")
             # conditional completions: one per group, counted at its chunk 0 (which tile fires it
             # is decided at run time)
             produced = [] if (t.cond and t.a1 != 0) else list(t.pubs)
@@ -432,9 +444,9 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
                 pw = producer_wave.setdefault(c, t.wave)
                 if pw != t.wave:
                     errs.append(f"counter {c} produced in waves {pw} and {t.wave}")
-            # batch > 1 consumers hold a tile's pages until the tile is done: it must fit the ring
-            # (at batch 1 a tile streams through the ring page by page)
-            if page_bytes_capacity is not None and cfg.batch > 1 and w[20] * o.page_bytes > page_bytes_capacity:
+            # an attention tile holds its pages until it is done: it must fit the ring (a matvec
+            # tile streams through the ring page by page)
+            if page_bytes_capacity is not None and t.op == ATTN and w[20] * o.page_bytes > page_bytes_capacity:
                 errs.append(f"tile {t.tid}: needs {w[20]} pages, ring too small")
             ref = ref_tiles[t.tid] if 0 <= t.tid < len(ref_tiles) else None
             if ref is None or (ref.op, ref.layer, ref.b, ref.a0, ref.a1, ref.a2) != \
@@ -517,7 +529,8 @@ def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, see
     Sequence b decodes position pos[b] (default: the last position its scheduled chunks cover): the
     chunk tiles past it do nothing, the others write their partial, and the tile of the chunk
     holding it waits (inside its wave) until the lower chunks of its group have written theirs,
-    then writes the group's attention output and fires the completion.  Reports a deadlock (no
+    then writes the group's attention output and fires the completion (at batch > 1 the group's
+    COMB tile waits for every active chunk's partial and does that).  Reports a deadlock (no
     SM can progress before all reach END) and any read of a buffer whose writer has not yet run
     in the current step."""
     S, Q, _ = queues.shape
@@ -545,10 +558,11 @@ def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, see
                     continue  # reached END
                 ok = all(((int(counters[c]) - (epoch * int(totals[c]) + need)) % U32) < (U32 >> 1)
                          for c, need in t.waits)
-                c_pos = pos[t.b] // t.a2 if t.op == ATTN else -1   # the chunk holding pos
+                c_pos = pos[t.b] // t.a2 if t.op in (ATTN, COMB) else -1   # the chunk holding pos
                 part_key = ("part", t.layer, t.b, t.a0)
-                if ok and t.op == ATTN and t.a1 == c_pos:   # the combine reads chunks 0 .. c_pos - 1
-                    ok = written.get(part_key, 0) >= c_pos
+                combines = (t.op == ATTN and t.cond and t.a1 == c_pos) or t.op == COMB
+                if ok and combines:   # the combine reads chunks 0 .. c_pos - 1 (COMB: 0 .. c_pos)
+                    ok = written.get(part_key, 0) >= (c_pos if t.op == ATTN else c_pos + 1)
                 if ok:
                     if track_data:
                         if t.tid not in rw_cache:
@@ -565,10 +579,12 @@ def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, see
                     if t.op == ATTN:
                         if t.a1 <= c_pos:
                             written[part_key] = written.get(part_key, 0) + 1
-                        if t.a1 == c_pos:
+                        if combines:
                             written[("o", t.layer)] = written.get(("o", t.layer), 0) + 1
-                        else:
+                        elif t.cond:
                             pubs = []
+                    elif t.op == COMB:
+                        written[("o", t.layer)] = written.get(("o", t.layer), 0) + 1
                     for c, dl in pubs:
                         counters[c] += dl
                     pc[s] += 1

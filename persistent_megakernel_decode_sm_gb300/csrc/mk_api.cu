@@ -117,7 +117,7 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, const
     for (size_t i = 0; i < dq.size(); i += kWords) {
         int32_t* x = &dq[i];
         const int op = x[W_OP];
-        if (op == OP_END || op < 0 || op >= OP_COUNT || op == OP_COMB) continue;
+        if (op == OP_END || op < 0 || op >= OP_COUNT) continue;
         const int l = x[W_LAYER], b = x[W_B], a0 = x[W_A0], a1 = x[W_A1], a2 = x[W_A2];
         const long slot = long(i / kWords);
         auto bad = [&](const char* what) {
@@ -162,10 +162,15 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, const
                 src0 = static_cast<const uint8_t*>(w->lm_head) + int64_t(a0) * H * 2;
                 b0 = int64_t(a1) * H * 2;
                 break;
-            case OP_ATTN:
+            case OP_ATTN:   // (batch 1: the chunk holding pos combines; batch > 1: COMB tiles do)
                 if (unsigned(a0) >= unsigned(nkv) || unsigned(a1) >= unsigned(g.n_chunk) || a2 != g.attn_chunk ||
-                    x[W_COND] != 1)
+                    x[W_COND] != (B == 1 ? 1 : 0))
                     return bad("attention fields");
+                break;
+            case OP_COMB:
+                if (B == 1 || unsigned(a0) >= unsigned(nkv) || a1 != 0 || a2 != g.attn_chunk || x[W_COND] != 0 ||
+                    x[W_NPAGES] != 0)
+                    return bad("combine fields");
                 break;
             case OP_ARGMAX:
                 if (a1 != g.n_lm) return bad("argmax fields");

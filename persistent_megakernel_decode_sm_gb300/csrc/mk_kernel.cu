@@ -432,7 +432,7 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos
             st.nseg = 2;
             st.total = 2 * nb;
         }
-    } else if (op != OP_ARGMAX && op != OP_END) {
+    } else if (op != OP_ARGMAX && op != OP_END && !(kBatchedKernel && op == OP_COMB)) {
         return MK_ERR_OPCODE;
     }
     st.pages = int((st.total + uint32_t(p.page_bytes) - 1u) >> p.page_shift);
@@ -1803,6 +1803,75 @@ __device__ __forceinline__ void attn_scores(const Cw& c, int tid, int n, int n_o
     }
 }
 
+// Combine of one (sequence, KV group)'s chunk partials (chunks 0 .. nact - 1) in chunk order:
+// M = max_c m_c, f_c = exp(m_c - M), L = sum_c f_c l_c, o = sum_c f_c o_c / L.  The partials are
+// tagged, so the combining tile polls them straight from the chunk tiles' writes (no arrival
+// counter, no second round trip).  lb = layer * B + sequence.
+__device__ __forceinline__ bool attn_combine(Cw& c, int pc, size_t lb, int g, int nact) {
+    const Params& p = c.p;
+    const int d = p.d, hpg = p.hpg;
+    const int tid = c.warp * 32 + c.lane;
+    const int per = hpg * (d + 2);   // words of one chunk's partial
+    const uint64_t* pbase = p.part + (lb * p.nkv + g) * size_t(p.n_chunk) * per;
+    // chunks staged at a time in the shared-x buffer (free: every warp is past its last input);
+    // with more active chunks the combine runs over groups of them, rescaling the running sums by
+    // exp(M_old - M_new) (0 before the first group)
+    const int kg = (kCombWords * kConsumerThreads) / per;
+    float* stage = c.sh.xbuf;
+    constexpr int kOut = kMaxHpg * kMaxHeadDim / kConsumerThreads;   // outputs per thread at most
+    float Mr[kOut], Lr[kOut], Ar[kOut];
+#pragma unroll
+    for (int j = 0; j < kOut; ++j) { Mr[j] = -INFINITY; Lr[j] = 0.f; Ar[j] = 0.f; }
+    for (int k0 = 0; k0 < nact; k0 += kg) {
+        const int items = min(kg, nact - k0) * per;
+        const uint64_t* src = pbase + size_t(k0) * per;
+        Spin sp;
+        while (true) {   // every word of this thread loaded before any tag is checked
+            bool ok = true;
+#pragma unroll
+            for (int j = 0; j < kCombWords; ++j) {
+                const int i = tid + j * kConsumerThreads;
+                if (i < items) {
+                    const uint64_t w = ld_tag(src + i);
+                    stage[i] = tag_val(w);   // (rewritten by the next round if a tag was stale)
+                    ok &= tag_of(w) == c.tag;
+                }
+            }
+            if (__all_sync(0xFFFFFFFFu, ok)) break;
+            if (!spin_more(c, sp, pc)) return false;
+        }
+        if (!cbar(c, pc)) return false;
+        const int kn = items / per;
+#pragma unroll
+        for (int j = 0; j < kOut; ++j) {
+            const int idx = tid + j * kConsumerThreads;
+            if (idx >= hpg * d) break;
+            const int h = idx / d, e = idx % d;
+            const float* ph = stage + h * (d + 2);
+            float M = Mr[j];
+            for (int k = 0; k < kn; ++k) M = fmaxf(M, ph[k * per + d]);
+            const float r = expf(Mr[j] - M);
+            float Ls = Lr[j] * r, A = Ar[j] * r;
+            for (int k = 0; k < kn; ++k) {
+                const float f = expf(ph[k * per + d] - M);
+                Ls = fmaf(f, ph[k * per + d + 1], Ls);
+                A = fmaf(f, ph[k * per + e], A);
+            }
+            Mr[j] = M;
+            Lr[j] = Ls;
+            Ar[j] = A;
+        }
+        if (!cbar(c, pc)) return false;   // the stage is refilled next (next group, next input)
+    }
+    uint64_t* out = p.o + lb * p.qd + size_t(g) * hpg * d;
+#pragma unroll
+    for (int j = 0; j < kOut; ++j) {
+        const int idx = tid + j * kConsumerThreads;
+        if (idx < hpg * d) st_tag(out + idx, Ar[j] / Lr[j], c.tag);
+    }
+    return true;
+}
+
 // Split-K decode attention over one chunk of KV positions for one (sequence, KV group); the
 // chunk that holds pos also applies RoPE to the new k, rounds k and v to bf16 and appends them
 // to the cache.  Writes the chunk partial (o[d] unnormalised, m, l) for each query head, then
@@ -1984,74 +2053,25 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         release_pages(c, si);
 #endif
     }
-    // 5. the tile of the chunk that holds pos combines the group's active partials in chunk order:
-    //    M = max_c m_c, f_c = exp(m_c - M), L = sum_c f_c l_c, o = sum_c f_c o_c / L.  The
-    //    partials are tagged, so the combining tile polls them straight from the other tiles'
-    //    writes (no arrival counter, no second round trip); the barrier first also frees the
-    //    scores buffer and the new k/v for what follows.
+    // 5. the tile of the chunk that holds pos combines the group's partials (at batch > 1 the
+    //    group's COMB tile does); the barrier first also frees the scores buffer and the new k/v
+    //    for what follows.
     if (!cbar(c, pc)) return false;
+    if (kBatchedKernel && si.w[W_COND] == 0) return true;
     const int nact = min(p.n_chunk, (p.pos[b] + c.step) / C + 1);
     if (ch != nact - 1) return true;
     if (tid == 0) c.sh.pubinfo[(pc % kDone) * 8 + 7] = 1;   // this tile alone fires the completion
-    const int per = hpg * (d + 2);   // words of one chunk's partial
-    const uint64_t* pbase = p.part + (lb * p.nkv + g) * size_t(p.n_chunk) * per;
-    // chunks staged at a time in the shared-x buffer (free: every warp is past its last input);
-    // with more active chunks the combine runs over groups of them, rescaling the running sums by
-    // exp(M_old - M_new) (0 before the first group)
-    const int kg = (kCombWords * kConsumerThreads) / per;
-    float* stage = c.sh.xbuf;
-    constexpr int kOut = kMaxHpg * kMaxHeadDim / kConsumerThreads;   // outputs per thread at most
-    float Mr[kOut], Lr[kOut], Ar[kOut];
-#pragma unroll
-    for (int j = 0; j < kOut; ++j) { Mr[j] = -INFINITY; Lr[j] = 0.f; Ar[j] = 0.f; }
-    for (int k0 = 0; k0 < nact; k0 += kg) {
-        const int items = min(kg, nact - k0) * per;
-        const uint64_t* src = pbase + size_t(k0) * per;
-        Spin sp;
-        while (true) {   // every word of this thread loaded before any tag is checked
-            bool ok = true;
-#pragma unroll
-            for (int j = 0; j < kCombWords; ++j) {
-                const int i = tid + j * kConsumerThreads;
-                if (i < items) {
-                    const uint64_t w = ld_tag(src + i);
-                    stage[i] = tag_val(w);   // (rewritten by the next round if a tag was stale)
-                    ok &= tag_of(w) == c.tag;
-                }
-            }
-            if (__all_sync(0xFFFFFFFFu, ok)) break;
-            if (!spin_more(c, sp, pc)) return false;
-        }
-        if (!cbar(c, pc)) return false;
-        const int kn = items / per;
-#pragma unroll
-        for (int j = 0; j < kOut; ++j) {
-            const int idx = tid + j * kConsumerThreads;
-            if (idx >= hpg * d) break;
-            const int h = idx / d, e = idx % d;
-            const float* ph = stage + h * (d + 2);
-            float M = Mr[j];
-            for (int k = 0; k < kn; ++k) M = fmaxf(M, ph[k * per + d]);
-            const float r = expf(Mr[j] - M);
-            float Ls = Lr[j] * r, A = Ar[j] * r;
-            for (int k = 0; k < kn; ++k) {
-                const float f = expf(ph[k * per + d] - M);
-                Ls = fmaf(f, ph[k * per + d + 1], Ls);
-                A = fmaf(f, ph[k * per + e], A);
-            }
-            Mr[j] = M;
-            Lr[j] = Ls;
-            Ar[j] = A;
-        }
-        if (!cbar(c, pc)) return false;   // the stage is refilled next (next group, next input)
-    }
-    uint64_t* out = p.o + lb * p.qd + size_t(g) * hpg * d;
-#pragma unroll
-    for (int j = 0; j < kOut; ++j) {
-        const int idx = tid + j * kConsumerThreads;
-        if (idx < hpg * d) st_tag(out + idx, Ar[j] / Lr[j], c.tag);
-    }
-    return true;
+    return attn_combine(c, pc, lb, g, nact);
+}
+
+// Combine tile (batch > 1) of (sequence, KV group): combines the chunk partials of the group's
+// active chunks once they land.  The barrier first: the previous instruction's warps may still
+// read the shared-x buffer the combine stages into.
+__device__ bool comb_tile(Cw& c, const SlotInfo& si, int pc) {
+    const int l = si.w[W_LAYER], b = si.w[W_B], g = si.w[W_A0], C = si.w[W_A2];
+    const int nact = min(c.p.n_chunk, (c.p.pos[b] + c.step) / C + 1);
+    if (!cbar(c, pc)) return false;
+    return attn_combine(c, pc, size_t(l) * c.p.B + b, g, nact);
 }
 
 // Greedy token: argmax over the LM-head tile partials (largest value, lowest index on ties).
@@ -2212,7 +2232,7 @@ __device__ void consumer_warp(const Params& p, const Shared& sh) {
                     case OP_ATTN: good = attn_tile(c, si, pc); break;
                     case OP_ARGMAX: good = argmax_tile(c, si, pc); break;
                     default:
-                        if constexpr (BAT) good = mmv_tile(c, si, pc);
+                        if constexpr (BAT) good = op == OP_COMB ? comb_tile(c, si, pc) : mmv_tile(c, si, pc);
                         else good = matvec_tile<CPL>(c, si, pc);
                         break;
                 }

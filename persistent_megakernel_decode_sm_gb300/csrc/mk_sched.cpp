@@ -9,20 +9,23 @@
 // The page fixes none of the concrete rules; this file states them:
 //  * tiles per layer: QKV row tiles (<= head_dim rows: a tile touches one or two KV groups and
 //    completes each), attention chunks (sequence, group, chunk of attn_chunk positions; only the
-//    chunks inside the sequence's kv_limit window), O row
-//    tiles, gate/up row-pair tiles, down row tiles; then
+//    chunks inside the sequence's kv_limit window; at batch > 1 then one combine tile per
+//    (sequence, group)), O row tiles, gate/up row-pair tiles, down row tiles; then
 //    LM-head row tiles and one argmax per sequence;
 //  * DAG: a consumer waits on one counter per producer set -- QKV(l) on down(l-1), attention
 //    chunks of group g on the QKV tiles of group g, O on the combined attention of every group,
 //    up/gate on O, down on up/gate, LM head on the last layer's down, argmax on the LM head.
-//    The combine of a group's chunk partials is done by the chunk tile that holds the step's
-//    position (known only at run time), which alone carries the completion O waits on; it reads
-//    the other chunks' tagged partials as they land (a wait inside the wave, on tiles of lower
-//    id, which every queue runs first);
+//    At batch 1 the combine of a group's chunk partials is done by the chunk tile that holds the
+//    step's position (known only at run time), which alone carries the completion O waits on; it
+//    reads the other chunks' tagged partials as they land (a wait inside the wave, on tiles of
+//    lower id, which every queue runs first).  At batch > 1 a COMB tile per (sequence, group),
+//    enumerated after every chunk tile of the layer, does it and carries the completion, and the
+//    chunk tiles complete nothing -- a chunk tile then never holds its SM for a combine while
+//    chunks of later rounds queue behind it;
 //  * waves = longest-path level (5 per layer, then LM head, then argmax); the waits of a tile
 //    point only at lower waves (forward-progress contract);
-//  * pools: memory = tiles that stream weights or KV, compute = argmax; within a wave memory
-//    tiles are placed first;
+//  * pools: memory = tiles that stream weights or KV, compute = argmax and combine; within a
+//    wave memory tiles are placed first;
 //  * rows per tile: about one tile per operator per SM (streamed through the page ring page by
 //    page, whole rows per page; at batch > 1 rows longer than kMmvRange in slices of kMmvRange
 //    positions, at most 64 rows per tile), or about tile_bytes;
@@ -68,7 +71,7 @@ struct Tile {
     int64_t stream_bytes;
     int32_t id;
     bool cond;   // ATTN: completions only from the tile that combines its group
-    bool memory() const { return op != OP_ARGMAX; }
+    bool memory() const { return op != OP_ARGMAX && op != OP_COMB; }
     int64_t cost() const { return stream_bytes + kTileOverhead; }
 };
 
@@ -247,8 +250,13 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
                 for (int32_t ch = 0; ch < g.n_chunk && int64_t(ch) * g.attn_chunk < g.kv_limit[b]; ++ch) {
                     add(OP_ATTN, l, b, gr, ch, g.attn_chunk, 5 * l + 1, {{cm.qkv(l, gr), qkv_tiles_of_group[gr]}},
                         {cm.comb(l), 1}, int64_t(2) * g.attn_chunk * d * 2);
-                    tiles.back().cond = true;
+                    if (B == 1) tiles.back().cond = true;   // the chunk holding pos combines and completes
+                    else tiles.back().npub = 0;               // combined by the group's COMB tile
                 }
+        if (B > 1)   // one combine tile per (sequence, KV group), after every chunk tile of the layer
+            for (int32_t b = 0; b < B; ++b)
+                for (int32_t gr = 0; gr < nkv; ++gr)
+                    add(OP_COMB, l, b, gr, 0, g.attn_chunk, 5 * l + 1, {}, {cm.comb(l), 1}, 0);
         for (int32_t t = 0; t < g.n_o; ++t) {
             int32_t r0 = t * g.r_o, n = std::min(g.r_o, H - r0);
             add(OP_OPROJ, l, 0, r0, n, 0, 5 * l + 2, {{cm.comb(l), B * nkv}}, {cm.o(l), 1}, int64_t(n) * qd * 2);
