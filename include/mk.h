@@ -66,7 +66,8 @@ typedef struct {
  * batch of uneven lengths is placed by the work it has; mk_rebind_schedule moves a binding to a
  * schedule with new windows. */
 typedef struct {
-    int32_t page_bytes;  /* shared-memory page size (a power of two); default 32768             */
+    int32_t page_bytes;  /* shared-memory page size (a power of two); default 32768, at batch > 1
+                            65536 (a page is then a 16-row block over page_bytes / 32 positions) */
     int32_t tile_bytes;  /* 0: per-SM tiles (see above); else the target weight bytes per matvec
                             tile (capped at 8 rows for QKV, O and down, 16 gate/up pairs, 32
                             LM-head rows)                                                        */

@@ -33,9 +33,9 @@ Pools: memory pool = tiles that stream weights or KV (QKV, ATTN, OPROJ, UPGATE, 
 LMHEAD); compute pool = COMB and ARGMAX.  Within a wave memory tiles are placed before compute
 tiles.
 Rows per tile: (tile_bytes 0) about one tile per operator per SM -- such a tile streams through
-the page ring page by page; at batch > 1 rows longer than MMV_RANGE stream in slices of MMV_RANGE
-positions (pages: every row group of a slice, slice by slice), at most 64 rows per tile;
-otherwise tiles of about tile_bytes.
+the page ring page by page (at batch > 1 a page is a 16-row block over page_bytes / 32
+positions); at batch > 1 a tile of rows longer than MMV_RANGE (its sums held over several
+staging ranges) takes at most 64 rows; otherwise tiles of about tile_bytes.
 Assignment, wave by wave: memory tiles sorted by (cost desc, tile id asc), then compute tiles
 likewise; the k-th tile of that order (from 0) goes to the SM with the smallest accumulated cost
 (ties: lowest SM id) among the SMs holding at most k // S of the pool's tiles in this wave -- the
@@ -70,7 +70,7 @@ M64 = (1 << 64) - 1
 
 @dataclass
 class SchedOpts:
-    page_bytes: int = 32768
+    page_bytes: int = 0     # 0: 32768 at batch 1, 65536 at batch > 1 (a 16-row block over 2048 positions)
     tile_bytes: int = 0     # 0: per-SM tiles (batch > 1: at most 64 down rows when F > MMV_RANGE)
     attn_chunk: int = 0     # 0: 64 positions, doubled up to 256 while B * n_kv * chunks > 152
     shuffle_seed: int = 0
@@ -88,14 +88,14 @@ def kv_window(cfg, o: SchedOpts, b: int) -> int:
     return lim if lim else cfg.max_seq
 
 
-MMV_RANGE = 2048   # batch > 1: positions staged at a time; longer rows stream in slices of MMV_RANGE
+MMV_RANGE = 2048   # batch > 1: positions of the inputs staged at a time (longer rows: several ranges)
 
 
 def tile_rows(cfg, o: SchedOpts, S: int) -> Dict[str, int]:
     """Rows (pairs for gate/up) per matvec tile.  tile_bytes 0: about one tile per operator per SM
     (QKV tiles at most head_dim rows, so a tile touches one or two KV groups); at batch > 1 the
-    down (and output) projection, when its rows are longer than MMV_RANGE (streamed in row
-    slices), takes at most 64 rows.  Otherwise tiles of about tile_bytes.  Explicit rows_* override either."""
+    down (and output) projection, when its rows are longer than MMV_RANGE (its sums held over
+    several staging ranges), takes at most 64 rows.  Otherwise tiles of about tile_bytes.  Explicit rows_* override either."""
     H, F, V, d = cfg.hidden, cfg.ffn, cfg.vocab, cfg.head_dim
     qd = cfg.n_q_heads * cfg.head_dim
     nqkv = qd + 2 * cfg.n_kv_heads * d
@@ -286,17 +286,23 @@ def _shuffle(xs: List[Tile], rng: SplitMix64) -> List[Tile]:
     return xs
 
 
+def page_bytes_of(cfg, o: SchedOpts) -> int:
+    return o.page_bytes or (65536 if cfg.batch > 1 else 32768)
+
+
 def tile_pages(t: Tile, cfg, o: SchedOpts) -> int:
-    """Pages of a tile's stream: a matvec tile streams whole rows per page (gate/up: gate and up
-    row groups in alternate pages); an attention tile streams its bytes contiguously."""
+    """Pages of a tile's stream: at batch 1 a matvec tile streams whole rows per page (gate/up:
+    gate and up row groups in alternate pages), at batch > 1 one 16-row block (gate/up: 8 gate
+    rows and the 8 up rows of the same pairs) over page_bytes / 32 positions per page; an
+    attention tile streams its bytes contiguously."""
     if t.op in (QKV, OPROJ, UPGATE, DOWN, LMHEAD):
         K = cfg.q_dim if t.op == OPROJ else (cfg.ffn if t.op == DOWN else cfg.hidden)
-        if cfg.batch > 1 and K > MMV_RANGE:   # row slices of MMV_RANGE positions, slice-major
-            rps = o.page_bytes // (2 * MMV_RANGE)
-            return ceil_div(K, MMV_RANGE) * ceil_div(t.a1, rps)
-        rpp = o.page_bytes // (2 * K)
+        if cfg.batch > 1:   # 16-row blocks (gate/up: 8 pairs) over page_bytes / 32 positions
+            kp = page_bytes_of(cfg, o) // 32
+            return ceil_div(t.a1, 8 if t.op == UPGATE else 16) * ceil_div(K, kp)
+        rpp = page_bytes_of(cfg, o) // (2 * K)
         return ceil_div(t.a1, rpp) * (2 if t.op == UPGATE else 1)
-    return ceil_div(t.stream_bytes, o.page_bytes)
+    return ceil_div(t.stream_bytes, page_bytes_of(cfg, o))
 
 
 def encode(t: Tile, n_pages: int) -> List[int]:
@@ -446,7 +452,7 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
                     errs.append(f"counter {c} produced in waves {pw} and {t.wave}")
             # an attention tile holds its pages until it is done: it must fit the ring (a matvec
             # tile streams through the ring page by page)
-            if page_bytes_capacity is not None and t.op == ATTN and w[20] * o.page_bytes > page_bytes_capacity:
+            if page_bytes_capacity is not None and t.op == ATTN and w[20] * page_bytes_of(cfg, o) > page_bytes_capacity:
                 errs.append(f"tile {t.tid}: needs {w[20]} pages, ring too small")
             ref = ref_tiles[t.tid] if 0 <= t.tid < len(ref_tiles) else None
             if ref is None or (ref.op, ref.layer, ref.b, ref.a0, ref.a1, ref.a2) != \

@@ -8,6 +8,7 @@
 //   resources -- one CTA with the kernel's registers and shared memory is resident on each of
 //                the S SMs (the launch is cooperative, so an oversubscribed grid fails instead of
 //                deadlocking: the forward-progress contract).
+#include <cuda.h>   // tensor-map types (the encoder itself is fetched through the runtime)
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -48,6 +49,7 @@ struct mk_ctx {
     // the epoch (the 3-bit SwiGLU tag repeats every 7 steps), so it is cleared before its next use
     bool bound_stale;
     const int32_t* last_err;   // error word of the last launched step (bound or static scratch)
+    uint8_t* d_tmaps;          // batch > 1: the weights' TMA tensor maps
     uint32_t* d_step_bar;      // grid-wide step word: each CTA adds 1 per step it retires
     volatile int32_t* h_ctl;   // mapped pinned words: [0] stop request (host), [1] steps done (device)
     int32_t* d_ctl;            // their device address
@@ -70,6 +72,29 @@ struct mk_ctx {
 static mk_status cuda_fail(cudaError_t e, const char* what) {
     return fail(MK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+// batch > 1: TMA tensor maps over the matvec weights.  A [R][K] bf16 matrix is described as the
+// 3-d tensor [R][K / g0][g0] (mmv_g0) with a box of (g0, kp / g0, rows): one box is one page of
+// the ring, a block of rows over kp positions, rows 2 kp bytes apart; rows past R read as zeros
+static_assert(sizeof(CUtensorMap) == 128, "tensor maps are indexed in 128-byte records");
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static mk_status weight_map(EncodeTiledFn enc, CUtensorMap* out, const void* base, int64_t R, int64_t K, int kp,
+                            int rows) {
+    const int g0 = mmv_g0(int(K), kp);
+    if (reinterpret_cast<uintptr_t>(base) % 16 || K % 8)
+        return fail(MK_ERR_ARG, "batch > 1 needs 16-byte aligned weight matrices with rows of a multiple of 8");
+    const cuuint64_t dim[3] = {cuuint64_t(g0), cuuint64_t(K / g0), cuuint64_t(R)};
+    const cuuint64_t stride[2] = {cuuint64_t(g0) * 2u, cuuint64_t(K) * 2u};
+    const cuuint32_t box[3] = {cuuint32_t(g0), cuuint32_t(kp / g0), cuuint32_t(rows)};
+    const cuuint32_t es[3] = {1u, 1u, 1u};
+    const CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3u, const_cast<void*>(base), dim, stride, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled: error %d", int(r));
+    return MK_OK;
+}
 #define CK(call)                                    \
     do {                                            \
         cudaError_t e_ = (call);                    \
@@ -85,6 +110,7 @@ static void free_ctx(mk_ctx* c) {
     if (c->d_layers) cudaFree(c->d_layers);
     if (c->h_result) cudaFreeHost(c->h_result);
     if (c->d_step_bar) cudaFree(c->d_step_bar);
+    if (c->d_tmaps) cudaFree(c->d_tmaps);
     if (c->h_ctl) cudaFreeHost(const_cast<int32_t*>(c->h_ctl));
     delete c;
 }
@@ -102,7 +128,7 @@ extern "C" mk_status mk_device_sm_count(int32_t* out) {
 // device then trusts those fields) and writes the resolved weight stream of each matvec tile into
 // words 26..31 (source addresses and byte counts), so the loader on the device does no decoding.
 // Unknown opcodes are copied as they are: the device rejects them (MK_ERR_OPCODE).
-static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, const MvShape* mv, const int32_t* kslice,
+static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, const MvShape* mv, int kp,
                                 std::vector<int32_t>& dq) {
     const mk_model_cfg& c = s->cfg;
     const Geometry& g = s->geo;
@@ -179,8 +205,8 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, const
         }
         if (src0) {   // whole rows (or row slices) per page; gate/up: gate and up row groups alternate
             if (mv[op].rpp < 1) return bad("a page holds no row");
-            if (kslice[op] && (a1 + mv[op].rpp - 1) / mv[op].rpp > 8) return bad("sliced tile rows");   // (<= 4 row blocks)
-            const int64_t pages = mv_tile_pages(mv[op], kslice[op], a1, op == OP_UPGATE);
+            if (kp && mv[op].K > kMmvRange && a1 > 64) return bad("rows of a tile over several ranges");   // (<= 4 blocks)
+            const int64_t pages = mv_tile_pages(mv[op], kp, a1, op == OP_UPGATE);
             if (pages != x[W_NPAGES] || b0 + b1 > (int64_t(1) << 31) - 1) return bad("page count");
             put64(x + W_SRC0, src0);
             put64(x + W_SRC1, src1);
@@ -257,9 +283,10 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
         const int kmx = std::max(H, std::max(qd, c.ffn));
         const uint32_t stage = uint32_t(c.batch) * mmv_row_stride(std::min(kmx, kMmvRange));
         xbuf = std::max(xbuf, int((stage + kMmvPartBytes) / 4u));
-        // attention: scores [hpg][C], weights [C][hp], one partial output per consumer warp [8][hp][d]
+        // attention: scores [hpg][C], weights [C][hp], per consumer warp an output partial [hp][d]
+        // and its (m, l) per head
         const int hp = hpg <= 4 ? 4 : kMaxHpg;
-        xbuf = std::max(xbuf, ((hpg * g.attn_chunk + 3) & ~3) + g.attn_chunk * hp + kNumConsumerWarps * hp * d);
+        xbuf = std::max(xbuf, ((hpg * g.attn_chunk + 3) & ~3) + g.attn_chunk * hp + kNumConsumerWarps * hp * (d + 2));
     }
     if (hpg * g.attn_chunk > xbuf)
         return fail(MK_ERR_ARG, "attn_chunk %d: the scores of %d heads do not fit %d floats", g.attn_chunk, hpg, xbuf);
@@ -268,7 +295,10 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     const int kmax = std::max(H, std::max(qd, c.ffn));
     const int cpl = (kmax / 8 + kMaxSeg - 1) / kMaxSeg <= 128 ? 4 : kMaxCpl;
     MvShape mv[OP_COUNT] = {};
-    int32_t kslice[OP_COUNT] = {};
+    // batch > 1: a page holds a 16-row block over kp positions (kp divides kMmvRange, MMA steps of 32)
+    const int kp = c.batch > 1 ? g.page_bytes / 32 : 0;
+    if (c.batch > 1 && (kp < 32 || kp > kMmvRange))
+        return fail(MK_ERR_ARG, "batch > 1 needs page_bytes in [1024, %d]", 32 * kMmvRange);
     int comb_stride = 1;
     for (int op : {int(OP_QKV), int(OP_OPROJ), int(OP_UPGATE), int(OP_DOWN), int(OP_LMHEAD)}) {
         const int K = op == OP_OPROJ ? qd : (op == OP_DOWN ? c.ffn : H);
@@ -277,10 +307,8 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
             return fail(MK_ERR_ARG, "matvec row length %d cannot be cut into %d segments", K, kMaxSeg);
         if (c.batch == 1)
             comb_stride = std::max(comb_stride, mv[op].rpp * mv[op].G);   // (row, segment) units of a page
-        else if (K > kMmvRange) {   // pages of row slices (the tensor-core tiles stage a range at a time)
-            kslice[op] = kMmvRange;
-            mv[op].rpp = g.page_bytes / (2 * kMmvRange);
-        }
+        else
+            mv[op].rpp = 16;   // (a block of rows over kp positions)
         if (mv[op].rpp < 1)
             return fail(MK_ERR_CAPACITY, "a %d-byte page holds no %d-element row", g.page_bytes, K);
     }
@@ -346,6 +374,30 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
         if ((e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&x->d_ctl), ctl, 0)) != cudaSuccess)
             return bail(cuda_fail(e, "cudaHostGetDevicePointer(control words)"));
     }
+    if (c.batch > 1) {   // tensor maps over every matvec weight matrix
+        cudaDriverEntryPointQueryResult q{};
+        void* fnp = nullptr;
+        if ((e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fnp, 12000, cudaEnableDefault, &q)) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess || !fnp)
+            return bail(fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available"));
+        const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(fnp);
+        std::vector<CUtensorMap> maps(size_t(4) * L + 1);
+        for (int l = 0; l < L; ++l) {
+            mk_status st = weight_map(enc, &maps[4 * l + 0], w->wqkv[l], qd + 2 * c.n_kv_heads * d, H, kp, 16);
+            if (st == MK_OK) st = weight_map(enc, &maps[4 * l + 1], w->wo[l], H, qd, kp, 16);
+            if (st == MK_OK) st = weight_map(enc, &maps[4 * l + 2], w->wgate_up[l], 2 * int64_t(c.ffn), H, kp, 8);
+            if (st == MK_OK) st = weight_map(enc, &maps[4 * l + 3], w->wdown[l], H, c.ffn, kp, 16);
+            if (st != MK_OK) return bail(st);
+        }
+        {
+            const mk_status st = weight_map(enc, &maps[4 * L], w->lm_head, c.vocab, H, kp, 16);
+            if (st != MK_OK) return bail(st);
+        }
+        const size_t mb = maps.size() * sizeof(CUtensorMap);
+        if ((e = cudaMalloc(&x->d_tmaps, mb)) != cudaSuccess) return bail(cuda_fail(e, "cudaMalloc(tensor maps)"));
+        if ((e = cudaMemcpy(x->d_tmaps, maps.data(), mb, cudaMemcpyHostToDevice)) != cudaSuccess)
+            return bail(cuda_fail(e, "cudaMemcpy(tensor maps)"));
+    }
     std::vector<LayerPtrs> lp(L);
     for (int l = 0; l < L; ++l)
         lp[l] = {static_cast<const uint16_t*>(w->attn_norm[l]), static_cast<const uint16_t*>(w->wqkv[l]),
@@ -353,7 +405,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
                  static_cast<const uint16_t*>(w->wgate_up[l]), static_cast<const uint16_t*>(w->wdown[l])};
     std::vector<int32_t> dq;
     {
-        const mk_status rs = resolve_queues(s, w, mv, kslice, dq);
+        const mk_status rs = resolve_queues(s, w, mv, kp, dq);
         if (rs != MK_OK) return bail(rs);
     }
     if ((e = cudaMemcpy(x->d_queues, dq.data(), qbytes, cudaMemcpyHostToDevice)) != cudaSuccess ||
@@ -364,10 +416,9 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     const ScratchLayout sl = scratch_layout(c, g, s->S);
     uint8_t* sb = static_cast<uint8_t*>(scratch);
     Params& p = x->base;
-    for (int op = 0; op < OP_COUNT; ++op) {
-        p.mv[op] = mv[op];
-        p.kslice[op] = kslice[op];
-    }
+    for (int op = 0; op < OP_COUNT; ++op) p.mv[op] = mv[op];
+    p.mmv_kp = kp;
+    p.tmaps = x->d_tmaps;
     p.L = L; p.H = H; p.nq = c.n_q_heads; p.nkv = c.n_kv_heads; p.d = d; p.F = c.ffn; p.V = c.vocab;
     p.B = c.batch; p.max_seq = c.max_seq; p.hpg = hpg; p.qd = qd; p.kvd = c.n_kv_heads * d;
     p.nqkv = qd + 2 * p.kvd;
@@ -451,7 +502,7 @@ extern "C" mk_status mk_rebind_schedule(mk_ctx* c, const mk_schedule* s) {
         s->totals != c->totals)
         return fail(MK_ERR_ARG, "the schedule differs from the bound one in more than placement and KV windows");
     std::vector<int32_t> dq;
-    const mk_status rs = resolve_queues(s, &c->w, c->base.mv, c->base.kslice, dq);
+    const mk_status rs = resolve_queues(s, &c->w, c->base.mv, c->base.mmv_kp, dq);
     if (rs != MK_OK) return rs;
     CK(cudaStreamSynchronize(c->stream));   // no launch reads the queues any more
     if (dq.size() > c->queue_words) {

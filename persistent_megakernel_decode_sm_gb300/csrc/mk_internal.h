@@ -53,7 +53,7 @@ constexpr int kCombWords = 12;       // partial words a consumer thread polls pe
 constexpr int kResBuf = 64;          // residual words of a tile's rows staged in shared memory (per buffer)
 constexpr int kMaxRingPages = 64;    // cap on the page ring's length (the shared memory sets the rest)
 constexpr int kMinXBuf = 3072;       // floats of the shared input buffer at least (attention scores, combine)
-constexpr int kMmvRange = 2048;      // batch > 1: positions of a row staged at a time (longer rows are sliced)
+constexpr int kMmvRange = 2048;      // batch > 1: positions of a row staged at a time (longer rows: ranges)
 constexpr int kAttnChunkTiles = 152; // default attention chunk: grown while a layer has more chunks
 
 
@@ -156,11 +156,12 @@ MK_HD inline MvShape mv_shape(int K, int cpl, int page_bytes, int xbuf_floats) {
     return m;
 }
 
-// pages of a matvec tile of `rows` rows (pairs for gate/up): whole rows per page (gate and up row
-// groups in alternate pages), or for sliced rows (kslice > 0): every row group of every slice,
-// slice-major
-MK_HD inline int64_t mv_tile_pages(const MvShape& m, int kslice, int64_t rows, bool pair) {
-    if (kslice) return ((m.K + kslice - 1) / kslice) * ((rows + m.rpp - 1) / m.rpp);
+// pages of a matvec tile of `rows` rows (pairs for gate/up).  Batch 1 (kp 0): whole rows per page,
+// gate and up row groups in alternate pages.  Batch > 1: a page holds one 16-row block (gate/up:
+// 8 gate rows, then the 8 up rows of the same pairs) over kp positions; every block of every
+// slice, in the order (staging range, block, slice)
+MK_HD inline int64_t mv_tile_pages(const MvShape& m, int kp, int64_t rows, bool pair) {
+    if (kp) return ((rows + (pair ? 7 : 15)) / (pair ? 8 : 16)) * ((m.K + kp - 1) / kp);
     return ((rows + m.rpp - 1) / m.rpp) * (pair ? 2 : 1);
 }
 
@@ -221,9 +222,22 @@ struct Params {
     int32_t qrot_floats;
     int32_t xbuf_floats;     // shared input buffer (floats)
     int32_t comb_stride;     // (row, segment) units of a page, at most: partial words per page slot
-    int32_t kslice[OP_COUNT];  // by opcode: 0, pages hold whole rows; else (batch > 1, K > kMmvRange)
-                               // pages hold mv.rpp rows' slices of kslice positions, 2 kslice bytes apart
+    int32_t mmv_kp;          // batch > 1: positions of a row in a page (page_bytes / 32: a page holds a
+                             // 16-row block, rows 2 mmv_kp bytes apart); 0 at batch 1 (whole rows)
+    const uint8_t* tmaps;    // batch > 1: TMA tensor maps (128 bytes each) over the matvec weights:
+                             // [4 l + {QKV, O, gate/up, down}], then the LM head at [4 L]
 };
+
+// batch > 1: a [R][K] weight matrix is viewed as [R][K / g0][g0] elements, so that one tensor box
+// of (g0, kp / g0, rows) is a block of rows over kp positions (every box edge at most 256)
+MK_HD inline int mmv_g0(int K, int kp) {
+    int g0 = 8;
+    while (g0 < 256 && K % (2 * g0) == 0 && kp % (2 * g0) == 0) g0 *= 2;
+    return g0;
+}
+MK_HD inline int tmap_index(int op, int layer) {   // the tensor map of a matvec operator
+    return op == OP_LMHEAD ? 4 * layer : 4 * layer + (op == OP_QKV ? 0 : op == OP_OPROJ ? 1 : op == OP_UPGATE ? 2 : 3);
+}
 
 // one instruction slot: words + where its stream sits + the matvec shape.  16-byte aligned and
 // sized: the loader fills the words of each slot of the array with 16-byte stores

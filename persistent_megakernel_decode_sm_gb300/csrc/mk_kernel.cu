@@ -94,6 +94,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
+// one box of a 3-d TMA tensor map (coordinates innermost first) into shared memory
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int c0, int c1, int c2, uint64_t* bar,
+                                            uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -352,7 +361,9 @@ struct Stream {
     int pages;
     int inter;                       // gate/up tile: page 2j = gate rows [j rpp, (j+1) rpp), 2j+1 = up rows
     uint32_t rows, rowbytes, rpp;    // matvec: whole rows per page (0 rows: a plain byte stream)
-    uint32_t kslice, ngroups, K;     // matvec with row slices: positions per slice, row groups per slice
+    uint32_t K, nblk;                // batch > 1: row length, 16-row blocks (gate/up: 8 pairs),
+    uint32_t row0, g0, up;           // first row, innermost box edge, row offset of the up rows
+    const uint8_t* tmap;             // and the weights' tensor map
 };
 
 __device__ __forceinline__ int attn_old_rows(const Params& p, int b, int c, int chunk, int dpos) {
@@ -394,7 +405,8 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos
     st.kv_off = 0;
     st.inter = 0;
     st.rows = st.rowbytes = st.rpp = 0;
-    st.kslice = st.ngroups = st.K = 0;
+    st.K = st.nblk = st.row0 = st.g0 = st.up = 0;
+    st.tmap = nullptr;
     const int op = w[W_OP];
     if (is_matvec(op)) {   // whole rows per page; gate/up: gate and up row groups in alternate pages
         const uint32_t b0 = uint32_t(w[W_BYTES0]), b1 = uint32_t(w[W_BYTES1]);
@@ -407,11 +419,14 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos
         st.rowbytes = p.mv[op].rowbytes;
         st.rpp = uint32_t(p.mv[op].rpp);
         if (b0 == 0 || st.rpp == 0 || b0 != st.rows * st.rowbytes || b1 != (st.inter ? b0 : 0u)) return MK_ERR_BOUNDS;
-        if (kBatchedKernel) {   // (row slices exist at batch > 1 only)
-            st.kslice = uint32_t(p.kslice[op]);
+        if (kBatchedKernel) {   // 16-row blocks over mmv_kp positions per page, through the tensor map
             st.K = uint32_t(p.mv[op].K);
-            st.ngroups = (st.rows + st.rpp - 1u) / st.rpp;
-            st.pages = int(mv_tile_pages(p.mv[op], p.kslice[op], st.rows, st.inter));
+            st.nblk = (st.rows + (st.inter ? 7u : 15u)) / (st.inter ? 8u : 16u);
+            st.pages = int(mv_tile_pages(p.mv[op], p.mmv_kp, st.rows, st.inter));
+            st.row0 = uint32_t(w[W_A0]);
+            st.g0 = uint32_t(mmv_g0(int(st.K), p.mmv_kp));
+            st.up = uint32_t(p.F);
+            st.tmap = p.tmaps + size_t(tmap_index(op, w[W_LAYER])) * 128u;
         } else {
             st.pages = int((st.rows + st.rpp - 1u) / st.rpp) * (st.inter ? 2 : 1);
         }
@@ -589,13 +604,21 @@ __device__ void loader(const Params& p, const Shared& sh) {
                     break;
                 }
                 uint8_t* dst = sh.ring + (size_t(ps) << p.page_shift);
-                if (kBatchedKernel && st.rows && st.kslice) {   // matvec, row slices: slice pg / ngroups, group pg % ngroups
-                    const uint32_t sl = uint32_t(pg) / st.ngroups, r0 = (uint32_t(pg) % st.ngroups) * st.rpp;
-                    const uint32_t nr = min(st.rpp, st.rows - r0), k0 = sl * st.kslice, kn = min(st.kslice, st.K - k0);
-                    mbar_arrive_expect_tx(sh.full + ps, nr * kn * 2u);
-                    for (uint32_t r = 0; r < nr; ++r)   // one copy per row: rows 2 kslice bytes apart in the page
-                        bulk_g2s(dst + r * st.kslice * 2u, st.seg[0].src + size_t(r0 + r) * st.rowbytes + size_t(k0) * 2u,
-                                 kn * 2u, sh.full + ps, pol);
+                if (kBatchedKernel && st.rows) {
+                    // batch > 1: block q of rows (gate/up: 8 gate rows, then the same pairs' up rows)
+                    // over the kp positions of slice sl; pages in the order (range, block, slice)
+                    const uint32_t kp = uint32_t(p.mmv_kp), nsr = uint32_t(kMmvRange) / kp;
+                    const uint32_t nsl = (st.K + kp - 1u) / kp, per_r = st.nblk * nsr;
+                    const uint32_t r = uint32_t(pg) / per_r, rem = uint32_t(pg) % per_r;
+                    const uint32_t nsl_r = min(nsr, nsl - r * nsr);
+                    const uint32_t q = rem / nsl_r, sl = r * nsr + rem % nsl_r;
+                    // one tensor box per page (gate/up: the 8 gate rows, then the same pairs' up
+                    // rows); a box counts its full size, positions past K and rows past the matrix
+                    // read as zeros
+                    const int c1 = int((sl * kp) / st.g0), row = int(st.row0 + q * (st.inter ? 8u : 16u));
+                    mbar_arrive_expect_tx(sh.full + ps, uint32_t(p.page_bytes));
+                    tma_load_3d(dst, st.tmap, 0, c1, row, sh.full + ps, pol);
+                    if (st.inter) tma_load_3d(dst + 8u * kp * 2u, st.tmap, 0, c1, row + int(st.up), sh.full + ps, pol);
                 } else if (st.rows) {   // matvec: a group of whole rows (gate/up: gate rows on even pages, up rows on odd)
                     uint32_t bytes;
                     const uint8_t* psrc = mv_page(st, uint32_t(pg), bytes);
@@ -1204,27 +1227,26 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
     const MvShape& m = si.mv;
     const int op = si.w[W_OP], l = si.w[W_LAYER];
     const bool pair = si.inter != 0;
-    const int K = m.K, R = si.rows, rpp = m.rpp, B = p.B;
+    const int K = m.K, R = si.rows, B = p.B, kp = p.mmv_kp;
     const int tid = c.warp * 32 + c.lane, g = c.lane >> 2, t4 = c.lane & 3;
-    // sliced rows (longer than kMmvRange): pages hold rpp rows' slices, slice-major; the sums of
-    // every row block of the tile persist over the slices (at most 4 blocks: 64 rows, scheduled so)
-    const int ksl = p.kslice[op];
-    const bool sliced = ksl != 0;
-    const int KR = sliced ? ksl : K, RS = int(mmv_row_stride(KR));
+    // a page is one 16-row block (gate/up: 8 pairs, gate rows then up rows) over kp positions, the
+    // pages in the order (staging range, block, slice).  Rows longer than a staging range keep the
+    // sums of every block of the tile over the ranges (at most 4 blocks: 64 rows, scheduled so)
+    const int KR = min(K, kMmvRange), RS = int(mmv_row_stride(KR));
+    const bool multi = K > KR;
     uint8_t* stage = reinterpret_cast<uint8_t*>(c.sh.xbuf);
     float* part = reinterpret_cast<float*>(stage + uint32_t(p.xbuf_floats) * 4u - kMmvPartBytes);
     const uint32_t stage_s = smem_u32(stage), ring_base = smem_u32(c.sh.ring);
-    const int npg = si.n_pages;
-    const int ngrp = sliced ? (R + rpp - 1) / rpp : npg;   // row groups (pages of one slice) / pages
-    const int nsb = (rpp + 7) / 8;
-    const int nblk = ((ngrp + 1) / 2) * nsb;
-    const uint32_t pstride = sliced ? uint32_t(ksl) * 2u : m.rowbytes;   // bytes between a page's rows
+    const int rb = pair ? 8 : 16;   // tile rows (pairs) of a block
+    const int nblk = (R + rb - 1) / rb;
+    const int nsl = (K + kp - 1) / kp;
+    const uint32_t pstride = uint32_t(kp) * 2u;   // bytes between a page's rows
     const int gs = min(g, B - 1);   // (columns past the batch read a valid row; unused)
     const uint16_t* gain;
     mmv_src(c, op, l, 0, gain);
     float bv = -INFINITY;   // LM head: this lane's running (max, lowest index) for sequence lane % 8
     int bi = 0x7FFFFFFF;
-    if (sliced && nblk > 4) {   // (not scheduled: the sliced operators' tiles take at most 64 rows)
+    if (multi && nblk > 4) {   // (not scheduled: such tiles take at most 64 rows)
         raise_error(p, c.sh, MK_ERR_CAPACITY, ROLE_CONSUMER, pc, -1, uint32_t(nblk), 4u);
         return false;
     }
@@ -1235,29 +1257,24 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
         for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[q][h][e] = 0.f;
-    // block blk: rows g of page (group) 2 pj and g of 2 pj + 1 (pj = blk / nsb, row 8 (blk % nsb) + g)
-    auto block = [&](int blk, int slice, MmvBlk& bk) {
-        const int pj = blk / nsb, r = 8 * (blk % nsb) + g;
-        const int p0 = 2 * pj, p1 = p0 + 1;
-        const int row0 = pair ? pj * rpp + r : p0 * rpp + r;
-        const int row1 = pair ? row0 : p1 * rpp + r;
-        uint32_t s0, s1, phu;   // ring slots of the pair (a streamed tile wraps the ring many times)
-        tile_page(p, si, slice * ngrp + p0, s0, phu);
-        tile_page(p, si, slice * ngrp + p1, s1, phu);
-        bk.v0 = r < rpp && row0 < R;
-        bk.v1 = r < rpp && p1 < ngrp && row1 < R;
-        bk.a0 = ring_base + (s0 << p.page_shift) + uint32_t(r) * pstride;
-        bk.a1 = ring_base + (s1 << p.page_shift) + uint32_t(r) * pstride;
-    };
-    auto pair_pages = [&](int slice, int pj, bool release) -> bool {
-        for (int pg = 2 * pj; pg < min(2 * pj + 2, ngrp); ++pg) {
+    int pg = 0;   // the tile's next page
+    // block q over the slices [s0, s1) of the staged range (positions from k0): MMA rows g and
+    // g + 8 are page rows g and g + 8; each page is waited for, used and given back in turn
+    auto block = [&](int q, int s0, int s1, int k0, uint32_t xrow, float (&a)[2][4]) -> bool {
+        const bool v0 = pair ? q * 8 + g < R : q * 16 + g < R;
+        const bool v1 = pair ? v0 : q * 16 + g + 8 < R;
+        for (int sl = s0; sl < s1; ++sl, ++pg) {
             uint32_t slot, ph;
-            tile_page(p, si, slice * ngrp + pg, slot, ph);
-            if (!release) {
-                if (!wait_bar(p, c.sh, c.sh.full + slot, ph, ROLE_CONSUMER, pc)) return false;
-            } else if (c.lane == 0) {
-                mbar_arrive(c.sh.empty + slot);
-            }
+            tile_page(p, si, pg, slot, ph);
+            if (!wait_bar(p, c.sh, c.sh.full + slot, ph, ROLE_CONSUMER, pc)) return false;
+            MmvBlk bk;
+            bk.v0 = v0;
+            bk.v1 = v1;
+            bk.a0 = ring_base + (slot << p.page_shift) + uint32_t(g) * pstride;
+            bk.a1 = bk.a0 + 8u * pstride;
+            mmv_steps(c, bk, xrow + uint32_t(sl * kp - k0) * 4u, 0, min(kp, K - sl * kp), a);
+            __syncwarp();
+            if (c.lane == 0) mbar_arrive(c.sh.empty + slot);
         }
         return true;
     };
@@ -1279,10 +1296,8 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
             const int q = tid >> 7, rr = (tid >> 3) & 15, col = tid & 7;
             const int blk = blk0 + q;
             if (q < nb && col < B && (!pair || rr < 8)) {
-                const int pj = blk / nsb, r = 8 * (blk % nsb) + (rr & 7);
-                const int pg = 2 * pj + (rr >> 3);
-                const int row = pair ? pj * rpp + r : pg * rpp + r;
-                if (r < rpp && pg < ngrp && row < R) {
+                const int row = blk * rb + rr;   // (gate/up: pair rr, its up row at MMA row rr + 8)
+                if (row < R) {
                     float s0 = 0.f, s1 = 0.f;
                     for (int w = 0; w < kNumConsumerWarps; ++w) {
                         s0 += part[(q * kNumConsumerWarps + w) * 128 + rr * 8 + col];
@@ -1335,8 +1350,19 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
             }
             if (!cbar(c, pc)) return false;
         }
-        // 2. in place, each thread its own items: x (* 1 / rms * gain) -> (hi, lo) word pairs
-        for (int i = tid; i < items; i += kConsumerThreads) {
+        // 2. in place, each thread its own items: x (* 1 / rms * gain) -> (hi, lo) word pairs; the
+        //    gain chunks of all the thread's items are loaded first (one round trip)
+        uint4 gws[kMmvItems];
+#pragma unroll
+        for (int j = 0; j < kMmvItems; ++j) {
+            const int i = tid + j * kConsumerThreads;
+            gws[j] = (gain && i < items) ? __ldg(reinterpret_cast<const uint4*>(gain + k0 + (i % csr) * 8))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kMmvItems; ++j) {
+            const int i = tid + j * kConsumerThreads;
+            if (i >= items) break;
             const int s = i / csr, ci = i % csr;
             uint4* w4 = reinterpret_cast<uint4*>(stage + s * RS + ci * 32);
             const uint4 u = w4[0], w = w4[1];
@@ -1344,7 +1370,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                           __uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w)};
             if (gain) {
                 const float scale = c.sh.red[48 + s];
-                const uint4 gw = __ldg(reinterpret_cast<const uint4*>(gain + k0 + ci * 8));
+                const uint4 gw = gws[j];
                 x[0] = (x[0] * scale) * bf_lo(gw.x); x[1] = (x[1] * scale) * bf_hi(gw.x);
                 x[2] = (x[2] * scale) * bf_lo(gw.y); x[3] = (x[3] * scale) * bf_hi(gw.y);
                 x[4] = (x[4] * scale) * bf_lo(gw.z); x[5] = (x[5] * scale) * bf_hi(gw.z);
@@ -1363,45 +1389,29 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
         if (!cbar(c, pc)) return false;   // staged words visible; the partial area and the scales are free again
         // 3. the contraction of the range
         const uint32_t xrow = stage_s + uint32_t(gs * RS);
-        if (sliced) {   // every block of this slice into its persistent sums; a pair of pages per block
-            const int sl = k0 / KR;
+        const int s0 = k0 / kp, s1 = min(nsl, s0 + KR / kp);   // the range's slices
+        if (multi) {   // every block into its sums over the ranges
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (q >= nblk) break;
-                if (!pair_pages(sl, q, false)) return false;
-                MmvBlk bk;
-                block(q, sl, bk);
-                mmv_steps(c, bk, xrow, 0, kr, acc[q]);   // (the slice starts at position 0 of its page)
-                __syncwarp();
-                pair_pages(sl, q, true);
+                if (!block(q, s0, s1, k0, xrow, acc[q])) return false;
             }
             if (k0 + KR < K) {
-                if (!cbar(c, pc)) return false;   // the next slice restages the inputs
+                if (!cbar(c, pc)) return false;   // the next range restages the inputs
                 continue;
             }
-            for (int blk0 = 0; blk0 < nblk; blk0 += 2)
-                if (!(blk0 == 0 ? outputs(0, acc[0], acc[1]) : outputs(2, acc[2], acc[3]))) return false;
-        } else {   // two row blocks at a time; a pair of pages is waited for at its first block and
-                   // given back after its last
+            if (!outputs(0, acc[0], acc[1])) return false;
+            if (nblk > 2 && !outputs(2, acc[2], acc[3])) return false;
+        } else {   // two blocks at a time
             for (int blk0 = 0; blk0 < nblk; blk0 += 2) {
-                const int nb = min(2, nblk - blk0);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int q = 0; q < 2; ++q)
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc[q][h][e] = 0.f;
-                    if (q >= nb) continue;
-                    const int blk = blk0 + q, pj = blk / nsb;
-                    if (blk % nsb == 0 && !pair_pages(0, pj, false)) return false;
-                    MmvBlk bk;
-                    block(blk, 0, bk);
-                    mmv_steps(c, bk, xrow, k0, kr, acc[q]);
-                    if (blk % nsb == nsb - 1 || blk == nblk - 1) {
-                        __syncwarp();
-                        pair_pages(0, pj, true);
-                    }
-                }
+                if (!block(blk0, s0, s1, k0, xrow, acc[0])) return false;
+                if (blk0 + 1 < nblk && !block(blk0 + 1, s0, s1, k0, xrow, acc[1])) return false;
                 if (!outputs(blk0, acc[0], acc[1])) return false;
             }
         }
@@ -1721,51 +1731,93 @@ __device__ __forceinline__ void attn_scores_mma(const Cw& c, int n, int n_old, i
         }
     }
 }
-// o partial of one consumer warp: sum over its positions t = warp, warp + 8, ... < n of
-// w[t][h] v_t[e] (row n_old is the new value), lane the EPL elements EPL lane .. EPL lane + EPL - 1
-// of every head; written to pw[warp][h][e].  One V row is one contiguous read of the warp.
+// Softmax pieces and o partial of one consumer warp over its own positions -- the 16-row blocks
+// mt = warp, warp + 8, ... whose scores it computed: m_w[h] = max_t s[h][t], w[t][h] =
+// exp(s[h][t] - m_w[h]), l_w[h] = sum_t w[t][h], o_w[h][e] = sum_t w[t][h] v_t[e] (row n_old is the
+// new value); lane the EPL elements EPL lane .. EPL lane + EPL - 1 of every head.  Written to
+// pw[warp][h][e] and mlw[warp][h] = (m_w, l_w); nothing is shared with the other warps until then.
 template <int EPL, int HP>   // head_dim / 32; heads padded to HP
-__device__ __forceinline__ void attn_pv_warp(const Cw& c, int n, int n_old, int hpg, const uint8_t* vbase, bool v1p,
-                                             uint32_t first_slot, uint32_t voff, const float* wT, float* pw) {
+__device__ __forceinline__ void attn_softmax_pv_warp(const Cw& c, int n, int n_old, int hpg, int C, const float* sc,
+                                                     const uint8_t* vbase, bool v1p, uint32_t first_slot, uint32_t voff,
+                                                     float* wT, float* pw, float* mlw) {
     const Params& p = c.p;
     constexpr int d = EPL * 32;
     constexpr uint32_t rowb = uint32_t(d) * 2u;
+    const int nmt = (n + 15) >> 4;
+    const int nw = nmt > c.warp ? ((nmt - 1 - c.warp) / kNumConsumerWarps + 1) * 16 : 0;   // this warp's slots
+    auto pos = [&](int j) { return (c.warp + (j >> 4) * kNumConsumerWarps) * 16 + (j & 15); };
+    __syncwarp();   // this warp's scores
+    float mh[HP], lh[HP];
+#pragma unroll
+    for (int h = 0; h < HP; ++h) { mh[h] = -INFINITY; lh[h] = 0.f; }
+    for (int j = c.lane; j < nw; j += 32) {
+        const int t = pos(j);
+        if (t < n)
+#pragma unroll
+            for (int h = 0; h < HP; ++h)
+                if (h < hpg) mh[h] = fmaxf(mh[h], sc[h * C + t]);
+    }
+#pragma unroll
+    for (int h = 0; h < HP; ++h) mh[h] = warp_max(mh[h]);
+    for (int j = c.lane; j < nw; j += 32) {
+        const int t = pos(j);
+        if (t < n) {
+            float e[HP];
+#pragma unroll
+            for (int h = 0; h < HP; ++h) {
+                e[h] = h < hpg ? expf(sc[h * C + t] - mh[h]) : 0.f;
+                lh[h] += e[h];
+            }
+#pragma unroll
+            for (int h4 = 0; h4 < HP; h4 += 4)
+                *reinterpret_cast<float4*>(wT + t * HP + h4) = make_float4(e[h4], e[h4 + 1], e[h4 + 2], e[h4 + 3]);
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < HP; ++h) lh[h] = warp_sum(lh[h]);
+    __syncwarp();   // the weights
     float acc[HP][EPL];
 #pragma unroll
     for (int h = 0; h < HP; ++h)
 #pragma unroll
         for (int i = 0; i < EPL; ++i) acc[h][i] = 0.f;
     const uint8_t* vnew = reinterpret_cast<const uint8_t*>(c.sh.vnew);
+    for (int mt = c.warp; mt < nmt; mt += kNumConsumerWarps) {
 #pragma unroll 4
-    for (int t = c.warp; t < n; t += kNumConsumerWarps) {
-        const uint8_t* vr = t < n_old ? (v1p ? vbase + uint32_t(t) * rowb : ring_ptr(c.sh, p, first_slot, voff + uint32_t(t) * rowb))
-                                      : vnew;
-        float v[EPL];
-        if constexpr (EPL == 1) {
-            v[0] = bf16f(*reinterpret_cast<const uint16_t*>(vr + c.lane * 2));
-        } else if constexpr (EPL == 2) {
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(vr + c.lane * 4);
-            v[0] = bf_lo(u); v[1] = bf_hi(u);
-        } else {
-            const uint2 u = *reinterpret_cast<const uint2*>(vr + c.lane * 8);
-            v[0] = bf_lo(u.x); v[1] = bf_hi(u.x); v[2] = bf_lo(u.y); v[3] = bf_hi(u.y);
+        for (int r = 0; r < 16; ++r) {
+            const int t = mt * 16 + r;
+            if (t >= n) break;
+            const uint8_t* vr = t < n_old ? (v1p ? vbase + uint32_t(t) * rowb : ring_ptr(c.sh, p, first_slot, voff + uint32_t(t) * rowb))
+                                          : vnew;
+            float v[EPL];
+            if constexpr (EPL == 1) {
+                v[0] = bf16f(*reinterpret_cast<const uint16_t*>(vr + c.lane * 2));
+            } else if constexpr (EPL == 2) {
+                const uint32_t u = *reinterpret_cast<const uint32_t*>(vr + c.lane * 4);
+                v[0] = bf_lo(u); v[1] = bf_hi(u);
+            } else {
+                const uint2 u = *reinterpret_cast<const uint2*>(vr + c.lane * 8);
+                v[0] = bf_lo(u.x); v[1] = bf_hi(u.x); v[2] = bf_lo(u.y); v[3] = bf_hi(u.y);
+            }
+            float w[HP];
+#pragma unroll
+            for (int h4 = 0; h4 < HP; h4 += 4) {
+                const float4 w4 = *reinterpret_cast<const float4*>(wT + t * HP + h4);
+                w[h4] = w4.x; w[h4 + 1] = w4.y; w[h4 + 2] = w4.z; w[h4 + 3] = w4.w;
+            }
+#pragma unroll
+            for (int h = 0; h < HP; ++h)
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) acc[h][i] = fmaf(w[h], v[i], acc[h][i]);
         }
-        float w[HP];
-#pragma unroll
-        for (int h4 = 0; h4 < HP; h4 += 4) {
-            const float4 w4 = *reinterpret_cast<const float4*>(wT + t * HP + h4);
-            w[h4] = w4.x; w[h4 + 1] = w4.y; w[h4 + 2] = w4.z; w[h4 + 3] = w4.w;
-        }
-#pragma unroll
-        for (int h = 0; h < HP; ++h)
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) acc[h][i] = fmaf(w[h], v[i], acc[h][i]);
     }
 #pragma unroll
     for (int h = 0; h < HP; ++h)
-        if (h < hpg)
+        if (h < hpg) {
 #pragma unroll
             for (int i = 0; i < EPL; ++i) pw[(c.warp * HP + h) * d + c.lane * EPL + i] = acc[h][i];
+            if (c.lane == 0) { mlw[(c.warp * HP + h) * 2] = mh[h]; mlw[(c.warp * HP + h) * 2 + 1] = lh[h]; }
+        }
 }
 #endif
 // Scores of one attention chunk: sc[h][t] = (q_h . k_t) * scale for t < n (row n_old is the new
@@ -1949,55 +2001,44 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         const uint8_t* kbase = ring_ptr(c.sh, p, first_slot, 0u);
         const uint8_t* vbase = ring_ptr(c.sh, p, first_slot, voff);
 #ifdef MK_BATCHED_TU
-        // 2. scores on the tensor cores; 3. softmax pieces per head (warp h), the weights stored
-        //    [t][head]; 4. each warp's o partial over its positions, then the 8 partials added in
-        //    warp order
+        // 2. scores on the tensor cores; 3. each warp's softmax pieces and o partial over its own
+        //    positions; 4. the 8 warps' partials merged in warp order (rescaled to the largest m)
         const int hp = hpg <= 4 ? 4 : kMaxHpg;
         float* wT = sc + ((hpg * C + 3) & ~3);       // [C][hp] (16-byte aligned rows)
         float* pw = wT + C * hp;                     // [8][hp][d]
+        float* mlw = pw + kNumConsumerWarps * hp * d;   // [8][hp][2]
         if (d == 64) attn_scores_mma<2>(c, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
         else if (d == 128) attn_scores_mma<4>(c, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
         else attn_scores_mma<1>(c, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
-        if (!cbar(c, pc)) return false;
-        if (c.warp < hpg) {
-            const int h = c.warp;
-            float m = -INFINITY;
-#pragma unroll 1
-            for (int t = c.lane; t < n; t += 32) m = fmaxf(m, sc[h * C + t]);
-            m = warp_max(m);
-            float s = 0.f;
-#pragma unroll 1
-            for (int t = c.lane; t < n; t += 32) {
-                const float e = expf(sc[h * C + t] - m);
-                wT[t * hp + h] = e;
-                s += e;
-            }
-            s = warp_sum(s);
-            if (c.lane == 0) { c.sh.ml[2 * h] = m; c.sh.ml[2 * h + 1] = s; }
-        }
-        if (!cbar(c, pc)) return false;
         if (hp == 4) {
-            if (d == 64) attn_pv_warp<2, 4>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
-            else if (d == 128) attn_pv_warp<4, 4>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
-            else attn_pv_warp<1, 4>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
+            if (d == 64) attn_softmax_pv_warp<2, 4>(c, n, n_old, hpg, C, sc, vbase, v1p, first_slot, voff, wT, pw, mlw);
+            else if (d == 128) attn_softmax_pv_warp<4, 4>(c, n, n_old, hpg, C, sc, vbase, v1p, first_slot, voff, wT, pw, mlw);
+            else attn_softmax_pv_warp<1, 4>(c, n, n_old, hpg, C, sc, vbase, v1p, first_slot, voff, wT, pw, mlw);
         } else {
-            if (d == 64) attn_pv_warp<2, kMaxHpg>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
-            else if (d == 128) attn_pv_warp<4, kMaxHpg>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
-            else attn_pv_warp<1, kMaxHpg>(c, n, n_old, hpg, vbase, v1p, first_slot, voff, wT, pw);
+            if (d == 64) attn_softmax_pv_warp<2, kMaxHpg>(c, n, n_old, hpg, C, sc, vbase, v1p, first_slot, voff, wT, pw, mlw);
+            else if (d == 128) attn_softmax_pv_warp<4, kMaxHpg>(c, n, n_old, hpg, C, sc, vbase, v1p, first_slot, voff, wT, pw, mlw);
+            else attn_softmax_pv_warp<1, kMaxHpg>(c, n, n_old, hpg, C, sc, vbase, v1p, first_slot, voff, wT, pw, mlw);
         }
         release_pages(c, si);
         if (!cbar(c, pc)) return false;
         uint64_t* dst = p.part + ((lb * p.nkv + g) * p.n_chunk + ch) * size_t(hpg) * (d + 2);
         for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
             const int h = idx / d, e = idx % d;
-            float acc = 0.f;
+            float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kNumConsumerWarps; ++w) acc += pw[(w * hp + h) * d + e];
+            for (int w = 0; w < kNumConsumerWarps; ++w) M = fmaxf(M, mlw[(w * hp + h) * 2]);
+            float acc = 0.f, L = 0.f;
+#pragma unroll
+            for (int w = 0; w < kNumConsumerWarps; ++w) {   // (a warp without positions: m = -inf, f = 0)
+                const float f = expf(mlw[(w * hp + h) * 2] - M);
+                acc = fmaf(f, pw[(w * hp + h) * d + e], acc);
+                L = fmaf(f, mlw[(w * hp + h) * 2 + 1], L);
+            }
             uint64_t* dh = dst + size_t(h) * (d + 2);
             st_tag(dh + e, acc, c.tag);
             if (e == 0) {
-                st_tag(dh + d, c.sh.ml[2 * h], c.tag);
-                st_tag(dh + d + 1, c.sh.ml[2 * h + 1], c.tag);
+                st_tag(dh + d, M, c.tag);
+                st_tag(dh + d + 1, L, c.tag);
             }
         }
 #else

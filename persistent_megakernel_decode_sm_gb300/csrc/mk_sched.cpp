@@ -27,8 +27,9 @@
 //  * pools: memory = tiles that stream weights or KV, compute = argmax and combine; within a
 //    wave memory tiles are placed first;
 //  * rows per tile: about one tile per operator per SM (streamed through the page ring page by
-//    page, whole rows per page; at batch > 1 rows longer than kMmvRange in slices of kMmvRange
-//    positions, at most 64 rows per tile), or about tile_bytes;
+//    page: at batch 1 whole rows per page, at batch > 1 a 16-row block over page_bytes / 32
+//    positions per page, at most 64 rows per tile for rows longer than kMmvRange), or about
+//    tile_bytes;
 //  * placement: within a wave, tiles in (cost desc, id asc) order -- or a seeded splitmix64
 //    Fisher-Yates order when shuffle_seed != 0 -- each to the queue with the smallest
 //    accumulated cost (ties to the lowest SM) among the queues holding at most k / S of the
@@ -131,7 +132,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     mk_sched_opts o{};
     if (opts) o = *opts;
     Geometry g{};
-    g.page_bytes = o.page_bytes ? o.page_bytes : 32768;
+    // default page: 32768 at batch 1; at batch > 1 one 16-row block over kMmvRange positions
+    g.page_bytes = o.page_bytes ? o.page_bytes : (c.batch > 1 ? 32 * kMmvRange : 32768);
     g.tile_bytes = o.tile_bytes;   // 0: matvec tiles sized per SM (batch 1) / 131072 bytes (batch > 1)
     // attention chunk: 64 positions, doubled (up to 256) while the chunks of all sequences and KV
     // heads would outnumber the 152 SMs of a GB300 (long contexts, batches): fewer, larger split-K
@@ -162,9 +164,9 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     // the page ring page by page, so it need not fit the ring, and the per-tile costs (dispatch,
     // input vector, first touch of its pages, completion) are paid once per operator and SM.  QKV
     // tiles keep <= head_dim rows (a tile then touches at most two KV groups).  At batch > 1 an
-    // operator whose rows are longer than kMmvRange (the MLP down projection) streams pages of row
-    // slices, slice-major, and its tiles take at most 64 rows.  An explicit tile_bytes: tiles of
-    // about tile_bytes.
+    // operator whose rows are longer than kMmvRange (the MLP down projection) keeps the sums of
+    // all its rows over several staging ranges, so its tiles take at most 64 rows.  An explicit
+    // tile_bytes: tiles of about tile_bytes.
     if (g.tile_bytes == 0) {
         g.r_qkv = std::min(d, cdiv(nqkv, S));
         g.r_o = (B > 1 && qd > kMmvRange) ? std::min(64, cdiv(H, S)) : cdiv(H, S);   // (sliced: <= 4 row blocks)
@@ -189,8 +191,10 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     if (B > 1 && ((qd > kMmvRange && g.r_o > 64) || (F > kMmvRange && g.r_dn > 64)))
         return fail(MK_ERR_ARG, "at batch > 1 a tile of rows longer than %d takes at most 64 rows", kMmvRange);
     if (g.r_o < 1 || g.r_up < 1 || g.r_lm < 1 || g.r_dn < 1) return fail(MK_ERR_ARG, "rows per tile must be >= 1");
-    if (g.page_bytes < 2 * std::max(H, std::max(qd, F)))   // matvec tiles stream whole rows per page
+    if (B == 1 && g.page_bytes < 2 * std::max(H, std::max(qd, F)))   // batch 1: whole rows per page
         return fail(MK_ERR_ARG, "page_bytes %d holds no matvec row (%d bytes)", g.page_bytes, 2 * std::max(H, std::max(qd, F)));
+    if (B > 1 && g.page_bytes > 32 * kMmvRange)   // batch > 1: a 16-row block of at most kMmvRange positions
+        return fail(MK_ERR_ARG, "at batch > 1 page_bytes is at most %d", 32 * kMmvRange);
     g.n_qkv = cdiv(nqkv, g.r_qkv);
     g.n_o = cdiv(H, g.r_o);
     g.n_up = cdiv(F, g.r_up);
@@ -352,9 +356,9 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
             int64_t pages = (t.stream_bytes + g.page_bytes - 1) / g.page_bytes;
             if (t.op == OP_QKV || t.op == OP_OPROJ || t.op == OP_UPGATE || t.op == OP_DOWN || t.op == OP_LMHEAD) {
                 const int64_t K = t.op == OP_OPROJ ? qd : (t.op == OP_DOWN ? F : H);
-                if (B > 1 && K > kMmvRange) {   // row slices of kMmvRange positions, slice-major
-                    const int64_t rps = g.page_bytes / (2 * kMmvRange);
-                    pages = ((K + kMmvRange - 1) / kMmvRange) * ((t.a1 + rps - 1) / rps);
+                if (B > 1) {   // 16-row blocks (gate/up: 8 pairs) over page_bytes / 32 positions
+                    const int64_t kp = g.page_bytes / 32, rb = t.op == OP_UPGATE ? 8 : 16;
+                    pages = ((t.a1 + rb - 1) / rb) * ((K + kp - 1) / kp);
                 } else {
                     const int64_t rpp = g.page_bytes / (2 * K);
                     pages = ((t.a1 + rpp - 1) / rpp) * (t.op == OP_UPGATE ? 2 : 1);

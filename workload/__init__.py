@@ -22,6 +22,10 @@ this library is tested on:
 * ``llama8b_ctx2048`` Llama-3.1-8B shape (32 layers, hidden 4096, head_dim 128,
                     FFN 14336, untied LM head); KV prefilled to 2048; 64 steps.
 
+Two profiling cases (not benchmark lines) keep the 1B layer shapes with 2 layers
+and vocab 32000: ``llama1b_reduced`` (batch 1, KV 512) and
+``llama1b_reduced_batch8`` (the batch-8 KV lengths).
+
 Value recipe: every matrix ~ N(0, 0.02) rounded to bf16 (round to nearest
 even); every RMSNorm gain = 1.0; prefilled K/V ~ N(0, 1) rounded to bf16 and
 taken as already-rotated cache contents; token ids uniform in [0, vocab).
@@ -121,6 +125,15 @@ def get_workload(name: str) -> Workload:
                           rope_theta=500000.0)
         return Workload(name, cfg, prompt_len=0, kv_len=[512], decode_steps=128,
                         description="reduced Llama-3.2-1B shape for profiling: 2 layers, vocab 32000")
+    if name == "llama1b_reduced_batch8":
+        # profiling case (not a benchmark line): the batch-8 workload's shapes and KV lengths with 2
+        # layers and vocab 32000 (~520 MB of weights and KV cache on the device)
+        lens = _kv_lengths_batch8(0)
+        cfg = ModelConfig(n_layers=2, hidden=2048, n_q_heads=32, n_kv_heads=8, head_dim=64, ffn=8192,
+                          vocab=32000, tied_embeddings=True, batch=8, max_seq=4096 + 64, rms_eps=1e-5,
+                          rope_theta=500000.0)
+        return Workload(name, cfg, prompt_len=0, kv_len=lens, decode_steps=64,
+                        description="reduced batch-8 Llama-3.2-1B shape for profiling: 2 layers, vocab 32000")
     if name == "llama8b_ctx2048":
         cfg = ModelConfig(n_layers=32, hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
                           ffn=14336, vocab=128256, tied_embeddings=False, batch=1,
