@@ -379,7 +379,7 @@ def main():
         "config": {"workload": args.workload, "batch": cfg.batch, "kv_len": wl.kv_len[0] if cfg.batch == 1 else wl.kv_len,
                    "weights": "bf16", "kv": "bf16", "sm_count": S, "parallelism": "replicas" if world > 1 else "single",
                    "sync": args.sync, "attn_chunk": sched.attn_chunk, "kv_windows": windows,
-                   "l2": "inputs larger than L2 (2.47 GB of weights streamed per step)",
+                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of weights and KV streamed per step)",
                    "step_us_mean": mean_us, "step_us_median": med, "step_us_p10": p10, "step_us_p90": p90},
         "e2e": {"value": e2e_us, "unit": "us/token", "h2d_bytes_per_step": 8 * cfg.batch,
                 "d2h_bytes_per_step": 96},
