@@ -1312,8 +1312,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
     for (int k0 = 0; k0 < K; k0 += KR) {
         const int kr = min(KR, K - k0), csr = kr / 8, items = B * csr;
         // 1. the range's inputs, every element polled until it carries this step's tag and stored
-        //    into the stage as fp32 (rewritten on every round); items (sequence i / csr, chunk
-        //    i % csr), i = tid, tid + 256, ...
+        //    into the stage as fp32 (rewritten on every round)
         {
             Spin spn;
             while (true) {
@@ -1328,8 +1327,19 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                     float v[8];
                     ok &= load8x(src, k0 + ci * 8, v, c.tag);
                     float4* dst = reinterpret_cast<float4*>(stage + s * RS + ci * 32);
-                    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-                    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+                    if (gain) {
+                        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+                        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+                    } else {   // no norm: straight as the (high, remainder) words the contraction reads
+                        uint32_t o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const uint32_t hb = bf16x2_rn(v[e], 0.f) & 0xFFFFu;
+                            o[e] = hb | (bf16x2_rn(v[e] - __uint_as_float(hb << 16), 0.f) << 16);
+                        }
+                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
                 }
                 if (__all_sync(0xFFFFFFFFu, ok)) break;
                 if (!spin_more(c, spn, pc)) return false;
@@ -1350,41 +1360,43 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
             }
             if (!cbar(c, pc)) return false;
         }
-        // 2. in place, each thread its own items: x (* 1 / rms * gain) -> (hi, lo) word pairs; the
-        //    gain chunks of all the thread's items are loaded first (one round trip)
-        uint4 gws[kMmvItems];
+        // 2. with a norm, in place, each thread its own items: x * 1 / rms * gain -> (hi, lo) word
+        //    pairs; the gain chunks of all the thread's items are loaded first (one round trip)
+        if (gain) {
+            uint4 gws[kMmvItems];
 #pragma unroll
-        for (int j = 0; j < kMmvItems; ++j) {
-            const int i = tid + j * kConsumerThreads;
-            gws[j] = (gain && i < items) ? __ldg(reinterpret_cast<const uint4*>(gain + k0 + (i % csr) * 8))
-                                         : make_uint4(0u, 0u, 0u, 0u);
-        }
+            for (int j = 0; j < kMmvItems; ++j) {
+                const int i = tid + j * kConsumerThreads;
+                gws[j] = (gain && i < items) ? __ldg(reinterpret_cast<const uint4*>(gain + k0 + (i % csr) * 8))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-        for (int j = 0; j < kMmvItems; ++j) {
-            const int i = tid + j * kConsumerThreads;
-            if (i >= items) break;
-            const int s = i / csr, ci = i % csr;
-            uint4* w4 = reinterpret_cast<uint4*>(stage + s * RS + ci * 32);
-            const uint4 u = w4[0], w = w4[1];
-            float x[8] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w),
-                          __uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w)};
-            if (gain) {
+            for (int j = 0; j < kMmvItems; ++j) {
+                const int i = tid + j * kConsumerThreads;
+                if (i >= items) break;
+                const int s = i / csr, ci = i % csr;
+                uint4* w4 = reinterpret_cast<uint4*>(stage + s * RS + ci * 32);
+                const uint4 u = w4[0], w = w4[1];
+                float x[8] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w),
+                              __uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w)};
+                if (gain) {
                 const float scale = c.sh.red[48 + s];
                 const uint4 gw = gws[j];
                 x[0] = (x[0] * scale) * bf_lo(gw.x); x[1] = (x[1] * scale) * bf_hi(gw.x);
                 x[2] = (x[2] * scale) * bf_lo(gw.y); x[3] = (x[3] * scale) * bf_hi(gw.y);
                 x[4] = (x[4] * scale) * bf_lo(gw.z); x[5] = (x[5] * scale) * bf_hi(gw.z);
                 x[6] = (x[6] * scale) * bf_lo(gw.w); x[7] = (x[7] * scale) * bf_hi(gw.w);
-            }
-            uint32_t o[8];
+                }
+                uint32_t o[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t hb = bf16x2_rn(x[e], 0.f) & 0xFFFFu;
-                const float lo = x[e] - __uint_as_float(hb << 16);
-                o[e] = hb | (bf16x2_rn(lo, 0.f) << 16);
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t hb = bf16x2_rn(x[e], 0.f) & 0xFFFFu;
+                    const float lo = x[e] - __uint_as_float(hb << 16);
+                    o[e] = hb | (bf16x2_rn(lo, 0.f) << 16);
+                }
+                w4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                w4[1] = make_uint4(o[4], o[5], o[6], o[7]);
             }
-            w4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            w4[1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
         if (!cbar(c, pc)) return false;   // staged words visible; the partial area and the scales are free again
         // 3. the contraction of the range
@@ -1673,7 +1685,8 @@ __device__ __forceinline__ uint32_t bf_part2(float a, float b, bool lo) {
 // head_dim against 8 columns: the bf16 high parts of four heads' rotated q, then their remainders,
 // so the two column halves add up to the fp32 q.  A lane's 16-byte load of a K row covers two MMAs:
 // within each 32 elements, lane quad t4 takes elements 8 t4 .. 8 t4 + 7 (the same order for the q
-// columns -- the contraction does not depend on it).  Warp w takes the 16-row blocks w, w + 8, ...
+// columns -- the contraction does not depend on it).  Warp w takes the 16-row blocks w, w + 8, ...,
+// two of them a round (every load of both blocks issued before their MMAs).
 template <int NP>   // head_dim / 32
 __device__ __forceinline__ void attn_scores_mma(const Cw& c, int n, int n_old, int hpg, int C, const uint8_t* kbase,
                                                 bool k1p, uint32_t first_slot, float* sc) {
@@ -1698,34 +1711,54 @@ __device__ __forceinline__ void attn_scores_mma(const Cw& c, int n, int n_old, i
                 bq[pp][3] = bf_part2(qb.z, qb.w, lo);
             }
         }
-        for (int mt = c.warp; mt < nmt; mt += kNumConsumerWarps) {
-            const int r0 = mt * 16 + g, r1 = r0 + 8;
-            auto row = [&](int r) -> const uint8_t* {   // (rows past n read the new key; not stored)
-                if (r < n_old) return k1p ? kbase + uint32_t(r) * rowb : ring_ptr(c.sh, p, first_slot, uint32_t(r) * rowb);
-                return knew;
-            };
-            const uint8_t* a0p = row(r0) + 16 * t4;
-            const uint8_t* a1p = row(r1) + 16 * t4;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        auto row = [&](int r) -> const uint8_t* {   // (rows past n read the new key; not stored)
+            if (r < n_old) return k1p ? kbase + uint32_t(r) * rowb : ring_ptr(c.sh, p, first_slot, uint32_t(r) * rowb);
+            return knew;
+        };
+        // two 16-row blocks (mt, mt + 8) a round: every load of both first, then their MMAs
+        for (int mt = c.warp; mt < nmt; mt += 2 * kNumConsumerWarps) {
+            const bool two = mt + kNumConsumerWarps < nmt;
+            const int ra = mt * 16 + g, rb = ra + kNumConsumerWarps * 16;
+            const uint32_t p0 = smem_u32(row(ra)) + 16u * t4;   // (shared-window addresses: plain ld.shared)
+            const uint32_t p1 = smem_u32(row(ra + 8)) + 16u * t4;
+            const uint32_t p2 = smem_u32(row(two ? rb : ra)) + 16u * t4;
+            const uint32_t p3 = smem_u32(row(two ? rb + 8 : ra + 8)) + 16u * t4;
+            uint4 A[NP][4];
 #pragma unroll
             for (int pp = 0; pp < NP; ++pp) {
-                const uint4 A0 = *reinterpret_cast<const uint4*>(a0p + 64 * pp);
-                const uint4 A1 = *reinterpret_cast<const uint4*>(a1p + 64 * pp);
-                mma16816(acc, A0.x, A1.x, A0.y, A1.y, bq[pp][0], bq[pp][1]);
-                mma16816(acc, A0.z, A1.z, A0.w, A1.w, bq[pp][2], bq[pp][3]);
+                A[pp][0] = lds128(p0 + 64u * pp);
+                A[pp][1] = lds128(p1 + 64u * pp);
+                A[pp][2] = lds128(p2 + 64u * pp);
+                A[pp][3] = lds128(p3 + 64u * pp);
             }
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int pp = 0; pp < NP; ++pp)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint4 X = A[pp][2 * q], Y = A[pp][2 * q + 1];
+                    mma16816(acc[q], X.x, Y.x, X.y, Y.y, bq[pp][0], bq[pp][1]);
+                    mma16816(acc[q], X.z, Y.z, X.w, Y.w, bq[pp][2], bq[pp][3]);
+                }
             // D (row, column 2 t4 + {0, 1}): quads t4 and t4 ^ 2 hold the two parts of the same heads
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] += __shfl_xor_sync(0xFFFFFFFFu, acc[e], 2);
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[q][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[q][e], 2);
             if (t4 < 2) {
                 const int h = h0 + 2 * t4;
-                if (r0 < n) {
-                    if (h < hpg) sc[h * C + r0] = acc[0] * p.attn_scale;
-                    if (h + 1 < hpg) sc[(h + 1) * C + r0] = acc[1] * p.attn_scale;
-                }
-                if (r1 < n) {
-                    if (h < hpg) sc[h * C + r1] = acc[2] * p.attn_scale;
-                    if (h + 1 < hpg) sc[(h + 1) * C + r1] = acc[3] * p.attn_scale;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    if (q == 1 && !two) break;
+                    const int r0 = q == 0 ? ra : rb, r1 = r0 + 8;
+                    if (r0 < n) {
+                        if (h < hpg) sc[h * C + r0] = acc[q][0] * p.attn_scale;
+                        if (h + 1 < hpg) sc[(h + 1) * C + r0] = acc[q][1] * p.attn_scale;
+                    }
+                    if (r1 < n) {
+                        if (h < hpg) sc[h * C + r1] = acc[q][2] * p.attn_scale;
+                        if (h + 1 < hpg) sc[(h + 1) * C + r1] = acc[q][3] * p.attn_scale;
+                    }
                 }
             }
         }
@@ -1783,8 +1816,39 @@ __device__ __forceinline__ void attn_softmax_pv_warp(const Cw& c, int n, int n_o
         for (int i = 0; i < EPL; ++i) acc[h][i] = 0.f;
     const uint8_t* vnew = reinterpret_cast<const uint8_t*>(c.sh.vnew);
     for (int mt = c.warp; mt < nmt; mt += kNumConsumerWarps) {
-#pragma unroll 4
-        for (int r = 0; r < 16; ++r) {
+        if (v1p && mt * 16 + 16 <= n_old) {   // a block of cached rows: eight rows' loads, then their products
+#pragma unroll
+            for (int r8 = 0; r8 < 16; r8 += 8) {
+                const int t0 = mt * 16 + r8;
+                float v[8][EPL], w[8][HP];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const uint8_t* vr = vbase + uint32_t(t0 + r) * rowb;
+                    if constexpr (EPL == 1) {
+                        v[r][0] = bf16f(*reinterpret_cast<const uint16_t*>(vr + c.lane * 2));
+                    } else if constexpr (EPL == 2) {
+                        const uint32_t u = *reinterpret_cast<const uint32_t*>(vr + c.lane * 4);
+                        v[r][0] = bf_lo(u); v[r][1] = bf_hi(u);
+                    } else {
+                        const uint2 u = *reinterpret_cast<const uint2*>(vr + c.lane * 8);
+                        v[r][0] = bf_lo(u.x); v[r][1] = bf_hi(u.x); v[r][2] = bf_lo(u.y); v[r][3] = bf_hi(u.y);
+                    }
+#pragma unroll
+                    for (int h4 = 0; h4 < HP; h4 += 4) {
+                        const float4 w4 = *reinterpret_cast<const float4*>(wT + (t0 + r) * HP + h4);
+                        w[r][h4] = w4.x; w[r][h4 + 1] = w4.y; w[r][h4 + 2] = w4.z; w[r][h4 + 3] = w4.w;
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+#pragma unroll
+                    for (int h = 0; h < HP; ++h)
+#pragma unroll
+                        for (int i = 0; i < EPL; ++i) acc[h][i] = fmaf(w[r][h], v[r][i], acc[h][i]);
+            }
+            continue;
+        }
+        for (int r = 0; r < 16; ++r) {   // (the block with the new row, or a ragged one)
             const int t = mt * 16 + r;
             if (t >= n) break;
             const uint8_t* vr = t < n_old ? (v1p ? vbase + uint32_t(t) * rowb : ring_ptr(c.sh, p, first_slot, voff + uint32_t(t) * rowb))
