@@ -1309,10 +1309,14 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
         }
         return cbar(c, pc);   // the partial area is reused
     };
-    for (int k0 = 0; k0 < K; k0 += KR) {
+    const int nrg = (K + KR - 1) / KR;
+    for (int rr = 0; rr < nrg; ++rr) {
+        const int k0 = rr * KR;
         const int kr = min(KR, K - k0), csr = kr / 8, items = B * csr;
         // 1. the range's inputs, every element polled until it carries this step's tag and stored
-        //    into the stage as fp32 (rewritten on every round)
+        //    into the stage as fp32 (rewritten on every round), with a norm also each item's sum of
+        //    squares.  (Every SM reads the inputs in the same order: spreading the SMs over
+        //    different parts of the inputs at a time was measured slower.)
         {
             Spin spn;
             while (true) {
@@ -1330,6 +1334,8 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                     if (gain) {
                         dst[0] = make_float4(v[0], v[1], v[2], v[3]);
                         dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+                        part[i] = ((v[0] * v[0] + v[1] * v[1]) + (v[2] * v[2] + v[3] * v[3])) +
+                                  ((v[4] * v[4] + v[5] * v[5]) + (v[6] * v[6] + v[7] * v[7]));
                     } else {   // no norm: straight as the (high, remainder) words the contraction reads
                         uint32_t o[8];
 #pragma unroll
@@ -1346,12 +1352,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
             }
         }
         if (gain) {   // RMSNorm (one range: the row length is at most kMmvRange): 1 / rms per sequence
-            for (int i = tid; i < items; i += kConsumerThreads) {
-                const float4* src4 = reinterpret_cast<const float4*>(stage + (i / csr) * RS + (i % csr) * 32);
-                const float4 u = src4[0], w = src4[1];
-                part[i] = ((u.x * u.x + u.y * u.y) + (u.z * u.z + u.w * u.w)) + ((w.x * w.x + w.y * w.y) + (w.z * w.z + w.w * w.w));
-            }
-            if (!cbar(c, pc)) return false;
+            if (!cbar(c, pc)) return false;   // every item's sum of squares
             if (c.warp < B) {   // warp s: sequence s's chunk sums, lane-strided, then a butterfly
                 float q = 0.f;
                 for (int ci = c.lane; ci < csr; ci += 32) q += part[c.warp * csr + ci];
@@ -1408,7 +1409,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                 if (q >= nblk) break;
                 if (!block(q, s0, s1, k0, xrow, acc[q])) return false;
             }
-            if (k0 + KR < K) {
+            if (rr + 1 < nrg) {
                 if (!cbar(c, pc)) return false;   // the next range restages the inputs
                 continue;
             }
