@@ -283,7 +283,8 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
         const int kmx = std::max(H, std::max(qd, c.ffn));
         const uint32_t stage = uint32_t(c.batch) * mmv_row_stride(std::min(kmx, kMmvRange));
         xbuf = std::max(xbuf, int((stage + kMmvPartBytes) / 4u));
-        // attention: scores [hpg][C], weights [C][hp], per consumer warp an output partial [hp][d]
+    }
+    {   // attention: scores [hpg][C], weights [C][hp], per consumer warp an output partial [hp][d]
         // and its (m, l) per head
         const int hp = hpg <= 4 ? 4 : kMaxHpg;
         xbuf = std::max(xbuf, ((hpg * g.attn_chunk + 3) & ~3) + g.attn_chunk * hp + kNumConsumerWarps * hp * (d + 2));

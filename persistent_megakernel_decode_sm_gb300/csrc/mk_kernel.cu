@@ -1673,9 +1673,6 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     return true;
 }
 
-#ifdef MK_BATCHED_TU
-// (the batch > 1 kernel only: in the batch-1 kernel these registers would reshape the matvec
-// path's allocation)
 // bf16x2 of (a, b) (a in the low half), or of their rounding remainders
 __device__ __forceinline__ uint32_t bf_part2(float a, float b, bool lo) {
     const uint32_t h = bf16x2_rn(a, b);
@@ -1884,42 +1881,6 @@ __device__ __forceinline__ void attn_softmax_pv_warp(const Cw& c, int n, int n_o
             if (c.lane == 0) { mlw[(c.warp * HP + h) * 2] = mh[h]; mlw[(c.warp * HP + h) * 2 + 1] = lh[h]; }
         }
 }
-#endif
-// Scores of one attention chunk: sc[h][t] = (q_h . k_t) * scale for t < n (row n_old is the new
-// key), d/8 consecutive lanes sharing a position.  HPG heads are unrolled at compile time; a head
-// count other than 4 runs the kMaxHpg variant with heads past hpg computed on a clamped head and
-// not stored.
-template <int HPG>
-__device__ __forceinline__ void attn_scores(const Cw& c, int tid, int n, int n_old, int hpg, int C, const uint8_t* kbase,
-                                            bool k1p, uint32_t first_slot, float* sc) {
-    const Params& p = c.p;
-    const int d = p.d, cpr = d / 8;
-    const uint32_t rowb = uint32_t(d) * 2u;
-    for (int base = 0; base < n * cpr; base += kConsumerThreads) {
-        const int idx = base + tid;
-        const bool valid = idx < n * cpr;
-        const int t = idx / cpr, j = idx - t * cpr;
-        float part[HPG];
-        if (valid) {
-            const uint32_t off = uint32_t(t) * rowb + uint32_t(j) * 16u;
-            const uint4 kv = (t < n_old) ? *reinterpret_cast<const uint4*>(k1p ? kbase + off : ring_ptr(c.sh, p, first_slot, off))
-                                         : *reinterpret_cast<const uint4*>(c.sh.knew + j * 8);
-#pragma unroll
-            for (int h = 0; h < HPG; ++h) part[h] = dot8(kv, c.sh.qrot + min(h, hpg - 1) * d + j * 8, 0.f);
-        } else {
-#pragma unroll
-            for (int h = 0; h < HPG; ++h) part[h] = 0.f;
-        }
-        for (int o = 1; o < cpr; o <<= 1)
-#pragma unroll
-            for (int h = 0; h < HPG; ++h) part[h] += __shfl_xor_sync(0xFFFFFFFFu, part[h], o);
-        if (valid && j == 0)
-#pragma unroll
-            for (int h = 0; h < HPG; ++h)
-                if (h < hpg) sc[h * C + t] = part[h] * p.attn_scale;
-    }
-}
-
 // Combine of one (sequence, KV group)'s chunk partials (chunks 0 .. nact - 1) in chunk order:
 // M = max_c m_c, f_c = exp(m_c - M), L = sum_c f_c l_c, o = sum_c f_c o_c / L.  The partials are
 // tagged, so the combining tile polls them straight from the chunk tiles' writes (no arrival
@@ -2065,7 +2026,6 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
         const bool v1p = n_old == 0 || (voff >> p.page_shift) == ((voff + kbytes - 1u) >> p.page_shift);
         const uint8_t* kbase = ring_ptr(c.sh, p, first_slot, 0u);
         const uint8_t* vbase = ring_ptr(c.sh, p, first_slot, voff);
-#ifdef MK_BATCHED_TU
         // 2. scores on the tensor cores; 3. each warp's softmax pieces and o partial over its own
         //    positions; 4. the 8 warps' partials merged in warp order (rescaled to the largest m)
         const int hp = hpg <= 4 ? 4 : kMaxHpg;
@@ -2106,58 +2066,6 @@ __device__ bool attn_tile(Cw& c, const SlotInfo& si, int pc) {
                 st_tag(dh + d + 1, L, c.tag);
             }
         }
-#else
-        // 2. scores s[h][t] = (q_h . k_t) * scale; d/8 consecutive lanes share a position
-        if (hpg == 4) attn_scores<4>(c, tid, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
-        else attn_scores<kMaxHpg>(c, tid, n, n_old, hpg, C, kbase, k1p, first_slot, sc);
-        if (!cbar(c, pc)) return false;
-        // 3. softmax pieces per head (warp h): m, w_t = exp(s_t - m), l = sum w_t
-        if (c.warp < hpg) {
-            const int h = c.warp;
-            float m = -INFINITY;
-#pragma unroll 1
-            for (int t = c.lane; t < n; t += 32) m = fmaxf(m, sc[h * C + t]);
-            m = warp_max(m);
-            float s = 0.f;
-#pragma unroll 1
-            for (int t = c.lane; t < n; t += 32) {
-                const float e = expf(sc[h * C + t] - m);
-                sc[h * C + t] = e;
-                s += e;
-            }
-            s = warp_sum(s);
-            if (c.lane == 0) { c.sh.ml[2 * h] = m; c.sh.ml[2 * h + 1] = s; }
-        }
-        if (!cbar(c, pc)) return false;
-        // 4. o[h][e] = sum_t w_t v_t[e]
-        uint64_t* dst = p.part + ((lb * p.nkv + g) * p.n_chunk + ch) * size_t(hpg) * (d + 2);
-        for (int idx = tid; idx < hpg * d; idx += kConsumerThreads) {
-            const int h = idx / d, e = idx % d;
-            const float* wts = sc + h * C;
-            // four interleaved partial sums (positions t mod 4), added pairwise at the end
-            float a4[4] = {0.f, 0.f, 0.f, 0.f};
-            if (v1p) {
-                const uint16_t* vcol = reinterpret_cast<const uint16_t*>(vbase) + e;
-                int t = 0;
-                for (; t + 4 <= n_old; t += 4)
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) a4[r] = fmaf(wts[t + r], bf16f(vcol[(t + r) * d]), a4[r]);
-                for (; t < n_old; ++t) a4[t & 3] = fmaf(wts[t], bf16f(vcol[t * d]), a4[t & 3]);
-            } else {
-                for (int t = 0; t < n_old; ++t)
-                    a4[t & 3] = fmaf(wts[t], bf16f(*reinterpret_cast<const uint16_t*>(ring_ptr(c.sh, p, first_slot, voff + uint32_t(t) * rowb + uint32_t(e) * 2u))), a4[t & 3]);
-            }
-            float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
-            if (has_new) acc = fmaf(wts[n_old], bf16f(c.sh.vnew[e]), acc);
-            uint64_t* dh = dst + size_t(h) * (d + 2);
-            st_tag(dh + e, acc, c.tag);
-            if (e == 0) {
-                st_tag(dh + d, c.sh.ml[2 * h], c.tag);
-                st_tag(dh + d + 1, c.sh.ml[2 * h + 1], c.tag);
-            }
-        }
-        release_pages(c, si);
-#endif
     }
     // 5. the tile of the chunk that holds pos combines the group's partials (at batch > 1 the
     //    group's COMB tile does); the barrier first also frees the scores buffer and the new k/v

@@ -25,9 +25,9 @@ def test_cpp_schedule_bit_exact_vs_restatement(name, S):
 
 
 def test_default_attention_chunk_depends_on_the_configuration_only():
-    """64 positions, doubled up to 256 while a layer has more than 152 chunks -- whatever the SM
+    """128 positions, doubled up to 256 while a layer has more than 152 chunks -- whatever the SM
     count, so outputs stay bit-identical across SM counts."""
-    expect = {"tiny": 64, "llama1b_ctx512": 64, "llama1b_reduced": 64, "llama8b_ctx2048": 128,
+    expect = {"tiny": 128, "llama1b_ctx512": 128, "llama1b_reduced": 128, "llama8b_ctx2048": 128,
               "llama1b_ctx8192": 256, "llama1b_batch8": 256}
     for name, C in expect.items():
         cfg = get_workload(name).cfg
@@ -116,7 +116,8 @@ def test_validator_and_simulator_catch_planted_errors():
         for i in range(q.shape[1]):
             if q[s, i, 0] == sr.UPGATE:
                 bad[s, i, 6] = 0
-    assert any("before" in e for e in sr.simulate(bad, t, cfg, n_epochs=1, seed=1))
+    # (some random interleaving runs an up/gate tile before its O rows are written)
+    assert any(any("before" in e for e in sr.simulate(bad, t, cfg, n_epochs=1, seed=sd)) for sd in range(16))
     # per-SM wave order broken
     S_, Q_ = q.shape[0], q.shape[1]
     s = max(range(S_), key=lambda k: int((q[k, :, 0] != 0).sum()))
@@ -190,13 +191,14 @@ def test_combining_tile_ahead_of_a_lower_chunk_deadlocks_and_is_rejected():
     The validator flags the order and the simulator, decoding position 639 (chunk 9 combines),
     reports the deadlock."""
     cfg = get_workload("llama1b_ctx512").cfg
-    q, t, _ = sr.build_schedule(cfg, 1)
+    o = sr.SchedOpts(attn_chunk=64)   # ten chunks of 64 positions per group
+    q, t, _ = sr.build_schedule(cfg, 1, o)
     live = [i for i in range(q.shape[1]) if q[0, i, 0] == sr.ATTN and q[0, i, 1] == 0 and q[0, i, 3] == 0]
     i3 = next(i for i in live if q[0, i, 4] == 3)
     i9 = next(i for i in live if q[0, i, 4] == 9)
     bad = q.copy()
     bad[0, [i3, i9]] = bad[0, [i9, i3]]
-    assert any("same wave" in e for e in sr.validate(bad, t, cfg))
+    assert any("same wave" in e for e in sr.validate(bad, t, cfg, o))
     assert any("deadlock" in e for e in sr.simulate(bad, t, cfg, n_epochs=1, pos=[639]))
     assert sr.simulate(q, t, cfg, n_epochs=1, pos=[639]) == []
 
