@@ -1402,7 +1402,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
         if (!cbar(c, pc)) return false;   // staged words visible; the partial area and the scales are free again
         // 3. the contraction of the range
         const uint32_t xrow = stage_s + uint32_t(gs * RS);
-        const int s0 = k0 / kp, s1 = min(nsl, s0 + KR / kp);   // the range's slices
+        const int s0 = k0 / kp, s1 = min(nsl, s0 + (KR + kp - 1) / kp);   // the range's slices (rows shorter than a page: one)
         if (multi) {   // every block into its sums over the ranges
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
