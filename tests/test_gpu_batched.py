@@ -1,4 +1,5 @@
-"""The batch > 1 kernel on small shapes chosen to reach its edge cases, against the oracle.
+"""The batch > 1 kernel (and the attention body both kernels share) on small shapes chosen to
+reach their edge cases, against the oracle.
 
 Each case runs teacher-forced steps through the C ABI and compares logits and tokens with the
 oracle (tolerances of test_gpu_parity), then checks that a schedule for another SM count gives
@@ -7,7 +8,7 @@ bit-identical outputs.  The shapes cover:
 - a page of 512 positions, so the last slice of a row is partly past the matrix (zero fill);
 - rows longer than one 2048-position staging range with a short last range (2560);
 - two query heads per KV group (padded head columns), and eight (the wide head path) at
-  head_dim 32;
+  head_dim 32; head_dim 128;
 - 3 and 5 sequences (MMA columns past the batch), with uneven KV lengths over several chunks.
 """
 import pytest
@@ -27,6 +28,10 @@ CASES = {
     "b3_ffn688_p16k": (dict(batch=3, max_seq=300), [5, 200, 64], dict(page_bytes=16384)),
     "b5_ffn2560": (dict(batch=5, ffn=2560, max_seq=200), [40, 1, 129, 77, 150], {}),
     "b2_hpg8_d32": (dict(batch=2, n_q_heads=16, n_kv_heads=2, head_dim=32, max_seq=260), [100, 240], {}),
+    "b2_d128": (dict(batch=2, n_q_heads=4, n_kv_heads=2, head_dim=128, max_seq=300), [129, 3], {}),
+    # the same attention body in the batch-1 kernel
+    "b1_hpg8_d32": (dict(batch=1, n_q_heads=16, n_kv_heads=2, head_dim=32, max_seq=300), [257], {}),
+    "b1_d128": (dict(batch=1, n_q_heads=4, n_kv_heads=2, head_dim=128, max_seq=300), [200], {}),
 }
 
 
