@@ -71,7 +71,7 @@ typedef struct {
     int32_t tile_bytes;  /* 0: per-SM tiles (see above); else the target weight bytes per matvec
                             tile (capped at 8 rows for QKV, O and down, 16 gate/up pairs, 32
                             LM-head rows)                                                        */
-    int32_t attn_chunk;  /* KV positions per split-K attention tile; 0: 128, doubled (up to 256)
+    int32_t attn_chunk;  /* KV positions per split-K attention tile; 0: 128, doubled (up to 512)
                             while batch * n_kv_heads * ceil(max_seq / chunk) > 152 (a property
                             of the configuration, not of sm_count)                               */
     int32_t rows_qkv, rows_o, pairs_up, rows_down, rows_lm; /* explicit rows (pairs) per tile,

@@ -72,7 +72,7 @@ M64 = (1 << 64) - 1
 class SchedOpts:
     page_bytes: int = 0     # 0: 32768 at batch 1, 65536 at batch > 1 (a 16-row block over 2048 positions)
     tile_bytes: int = 0     # 0: per-SM tiles (batch > 1: at most 64 down rows when F > MMV_RANGE)
-    attn_chunk: int = 0     # 0: 128 positions, doubled up to 256 while B * n_kv * chunks > 152
+    attn_chunk: int = 0     # 0: 128 positions, doubled up to 512 while B * n_kv * chunks > 152
     shuffle_seed: int = 0
     rows_qkv: int = 0   # 0: derived from tile_bytes
     rows_o: int = 0
@@ -169,13 +169,13 @@ ATTN_CHUNK_TILES = 152   # the default chunk grows while a layer has more chunks
 
 
 def attn_chunk(cfg, o: SchedOpts, S: int) -> int:
-    """KV positions per split-K attention tile: the option, else 128 doubled (at most to 256) as
+    """KV positions per split-K attention tile: the option, else 128 doubled (at most to 512) as
     long as the chunks of all sequences and KV heads outnumber ATTN_CHUNK_TILES -- a property of
     the configuration, independent of the queue count S."""
     if o.attn_chunk:
         return o.attn_chunk
     C = 128
-    while C < 256 and cfg.batch * cfg.n_kv_heads * ceil_div(cfg.max_seq, C) > ATTN_CHUNK_TILES:
+    while C < 512 and cfg.batch * cfg.n_kv_heads * ceil_div(cfg.max_seq, C) > ATTN_CHUNK_TILES:
         C *= 2
     return C
 

@@ -135,14 +135,14 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     // default page: 32768 at batch 1; at batch > 1 one 16-row block over kMmvRange positions
     g.page_bytes = o.page_bytes ? o.page_bytes : (c.batch > 1 ? 32 * kMmvRange : 32768);
     g.tile_bytes = o.tile_bytes;   // 0: matvec tiles sized per SM (batch 1) / 131072 bytes (batch > 1)
-    // attention chunk: 128 positions, doubled (up to 256) while the chunks of all sequences and KV
+    // attention chunk: 128 positions, doubled (up to 512) while the chunks of all sequences and KV
     // heads would outnumber the 152 SMs of a GB300 (long contexts, batches): fewer, larger split-K
     // tiles.  A property of the model configuration alone, like every tile shape: the results do
     // not depend on the SM count the schedule is built for.
     g.attn_chunk = o.attn_chunk;
     if (g.attn_chunk == 0) {
         g.attn_chunk = 128;
-        while (g.attn_chunk < 256 &&
+        while (g.attn_chunk < 512 &&
                int64_t(c.batch) * c.n_kv_heads * cdiv(c.max_seq, g.attn_chunk) > kAttnChunkTiles)
             g.attn_chunk *= 2;
     }

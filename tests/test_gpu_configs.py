@@ -1,5 +1,5 @@
 """GPU parity of the megakernel against the CPU oracle on the larger configurations, through the
-C ABI (libmk.so): a long context (33 attention chunks of 256 positions per group, combined over
+C ABI (libmk.so): a long context (17 attention chunks of 512 positions per group, combined over
 partials in L2), batch 8 with uneven KV lengths (tiles held whole in the page ring, one input
 vector per sequence), and the 8B shape (8 chunks per lane, untied LM head).
 
@@ -38,7 +38,7 @@ def test_llama1b_long_context_parity():
 
 
 def test_llama1b_long_context_bit_identical_across_sm_counts():
-    # 33 attention chunks of 256 positions per group, combined in chunk order
+    # 17 attention chunks of 512 positions per group, combined in chunk order
     outs = []
     for S in (mk.device_sm_count(), 76):
         s = make_setup("llama1b_ctx8192")
