@@ -853,6 +853,26 @@ __device__ float poll1(const Params& p, const Shared& sh, const uint64_t* a, int
     return tag_val(w);
 }
 
+// the same for a 3-bit-tagged 32-bit word (batch > 1 activations)
+__device__ float poll1h(const Params& p, const Shared& sh, const uint32_t* a, int pc, uint32_t tag) {
+    const uint32_t ht = htag(tag);
+    const uint64_t t0 = globaltimer();
+    uint32_t rounds = 0, w;
+    while (true) {
+        asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(w) : "l"(a));
+        if (((w ^ ht) & 7u) == 0) break;
+        if (*reinterpret_cast<volatile int*>(sh.abort) || other_cta_failed(p, rounds)) {
+            *reinterpret_cast<volatile int*>(sh.abort) = 1;
+            break;
+        }
+        if (globaltimer() - t0 > p.timeout_ns) {
+            raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, w & 7u, ht);
+            break;
+        }
+    }
+    return __uint_as_float(w & ~7u);
+}
+
 __device__ __forceinline__ void load8_bf16(const uint16_t* src, float* v) {
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
     v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
@@ -1057,6 +1077,13 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
     switch (op) {
         case OP_QKV: st_tag(p.qkv + lb * p.nqkv + row, s0, c.tag); break;
         case OP_OPROJ: {
+            if constexpr (kBatchedKernel) {   // (batch > 1: 3-bit-tagged 32-bit residual words)
+                const float r = l == 0 ? bf16f(p.embed[size_t(step_token(c, b)) * p.H + row])
+                                       : poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_out) + (lb - p.B) * p.H + row,
+                                                pc, c.tag);
+                st_htag(reinterpret_cast<uint32_t*>(p.x_attn) + lb * p.H + row, r + s0, htag(c.tag));
+                break;
+            }
             const float r = (RES && ru < kResBuf) ? res[ru]
                           : (l == 0) ? bf16f(p.embed[size_t(step_token(c, b)) * p.H + row])
                                      : poll1(p, c.sh, p.x_out + (lb - p.B) * p.H + row, pc, c.tag);
@@ -1065,6 +1092,11 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
         }
         case OP_UPGATE: st_htag(p.h + lb * p.F + row, __fdividef(s0, 1.0f + __expf(-s0)) * s1, htag(c.tag)); break;
         case OP_DOWN: {
+            if constexpr (kBatchedKernel) {
+                const float r = poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_attn) + lb * p.H + row, pc, c.tag);
+                st_htag(reinterpret_cast<uint32_t*>(p.x_out) + lb * p.H + row, r + s0, htag(c.tag));
+                break;
+            }
             const float r = (RES && ru < kResBuf) ? res[ru] : poll1(p, c.sh, p.x_attn + lb * p.H + row, pc, c.tag);
             st_tag(p.x_out + lb * p.H + row, r + s0, c.tag);
             break;
@@ -1175,16 +1207,19 @@ __device__ __forceinline__ XSrc mmv_src(const Cw& c, int op, int l, int b, const
     XSrc src{nullptr, nullptr, nullptr};
     const size_t lb = size_t(l) * p.B + b;
     gain = nullptr;
+    // (the batch > 1 kernel keeps the residual streams and the attention output as 3-bit-tagged
+    // 32-bit words, like the SwiGLU output: half the bytes every SM polls)
+    const uint32_t* xo = reinterpret_cast<const uint32_t*>(p.x_out);
     switch (op) {
         case OP_QKV:
             gain = c.sh.layers[l].attn_norm;
             if (l == 0) src.b = p.embed + size_t(step_token(c, b)) * p.H;
-            else src.t = p.x_out + (lb - p.B) * p.H;
+            else src.h = xo + (lb - p.B) * p.H;
             break;
-        case OP_OPROJ: src.t = p.o + lb * p.qd; break;
-        case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; src.t = p.x_attn + lb * p.H; break;
+        case OP_OPROJ: src.h = reinterpret_cast<const uint32_t*>(p.o) + lb * p.qd; break;
+        case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; src.h = reinterpret_cast<const uint32_t*>(p.x_attn) + lb * p.H; break;
         case OP_DOWN: src.h = p.h + lb * p.F; break;
-        default: gain = p.final_norm; src.t = p.x_out + (size_t(p.L - 1) * p.B + b) * p.H; break;
+        default: gain = p.final_norm; src.h = xo + (size_t(p.L - 1) * p.B + b) * p.H; break;
     }
     return src;
 }
@@ -1351,6 +1386,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                 if (!spin_more(c, spn, pc)) return false;
             }
         }
+        if (rr == 0 && c.warp == 0 && c.lane == 0) stamp(p, pc, 6);   // (trace: this warp's inputs polled)
         if (gain) {   // RMSNorm (one range: the row length is at most kMmvRange): 1 / rms per sequence
             if (!cbar(c, pc)) return false;   // every item's sum of squares
             if (c.warp < B) {   // warp s: sequence s's chunk sums, lane-strided, then a butterfly
@@ -1945,7 +1981,11 @@ __device__ __forceinline__ bool attn_combine(Cw& c, int pc, size_t lb, int g, in
 #pragma unroll
     for (int j = 0; j < kOut; ++j) {
         const int idx = tid + j * kConsumerThreads;
-        if (idx < hpg * d) st_tag(out + idx, Ar[j] / Lr[j], c.tag);
+        if (idx >= hpg * d) continue;
+        if constexpr (kBatchedKernel)
+            st_htag(reinterpret_cast<uint32_t*>(p.o) + lb * p.qd + size_t(g) * hpg * d + idx, Ar[j] / Lr[j], htag(c.tag));
+        else
+            st_tag(out + idx, Ar[j] / Lr[j], c.tag);
     }
     return true;
 }
