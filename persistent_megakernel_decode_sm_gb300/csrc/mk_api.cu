@@ -314,15 +314,13 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
             return fail(MK_ERR_CAPACITY, "a %d-byte page holds no %d-element row", g.page_bytes, K);
     }
     const void* fn = c.batch > 1 ? mk_bat::megakernel_fn_batched() : megakernel_fn(cpl);
-    int asf = hpg * g.n_chunk;
-    asf = (asf + 3) & ~3;
     const int qrf = (hpg * d + 3) & ~3;
     int n_pages = 0;
     while (n_pages < kMaxRingPages &&
-           int64_t(n_pages + 1) * g.page_bytes + smem_misc_bytes(n_pages + 1, asf, qrf, xbuf, comb_stride) <= optin)
+           int64_t(n_pages + 1) * g.page_bytes + smem_misc_bytes(n_pages + 1, qrf, xbuf, comb_stride) <= optin)
         ++n_pages;
     if (n_pages < 1) return fail(MK_ERR_CAPACITY, "no room for a page ring");
-    const int misc = smem_misc_bytes(n_pages, asf, qrf, xbuf, comb_stride);
+    const int misc = smem_misc_bytes(n_pages, qrf, xbuf, comb_stride);
     // capacity: a matvec tile streams through the ring one group of two pages at a time; an
     // attention tile holds its K and V rows
     const int need_pages = std::max<int>(2, int((2ll * g.attn_chunk * d * 2 + g.page_bytes - 1) / g.page_bytes));
@@ -469,7 +467,6 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     p.ctl = nullptr;
     x->last_err = p.err;
     p.smem_misc_off = n_pages * g.page_bytes;
-    p.attn_scratch_floats = asf;
     p.qrot_floats = qrf;
     p.xbuf_floats = xbuf;
     p.comb_stride = comb_stride;

@@ -218,7 +218,6 @@ struct Params {
     uint64_t* trace;         // optional [S][Q][8] globaltimer stamps (null: off)
     // shared-memory carve-up
     int32_t smem_misc_off;   // byte offset of the non-ring area
-    int32_t attn_scratch_floats;
     int32_t qrot_floats;
     int32_t xbuf_floats;     // shared input buffer (floats)
     int32_t comb_stride;     // (row, segment) units of a page, at most: partial words per page slot
@@ -256,11 +255,10 @@ static_assert(sizeof(SlotInfo) % 16 == 0 && offsetof(SlotInfo, w) == 0, "slot wo
 
 // byte offsets of the non-ring shared memory (after the page ring); shared by host and device
 struct MiscLayout {
-    uint32_t slots, qwin, layers, bars, comb, combcnt, pubinfo, red, lmbest, qrot, ascr, ml, kv, res, xbuf, total;
+    uint32_t slots, qwin, layers, bars, comb, combcnt, pubinfo, red, lmbest, qrot, kv, res, xbuf, total;
 };
 
-MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qrot_floats, int xbuf_floats,
-                                    int comb_stride) {
+MK_HD inline MiscLayout misc_layout(int n_pages, int qrot_floats, int xbuf_floats, int comb_stride) {
     MiscLayout m{};
     uint32_t o = 0;
     auto take = [&o](uint32_t bytes, uint32_t align) {
@@ -282,8 +280,6 @@ MK_HD inline MiscLayout misc_layout(int n_pages, int attn_scratch_floats, int qr
                                                     // per-warp sums of squares of the shared input [48..63]
     m.lmbest = take(8u * kNumConsumerWarps * kMaxBatch, 8);   // LM-head running (max, index) per warp / sequence
     m.qrot = take(4u * uint32_t(qrot_floats), 16);
-    m.ascr = take(4u * uint32_t(attn_scratch_floats), 16);
-    m.ml = take(4u * 4u * kMaxHpg, 16);             // (m, l) per head, combine L per head
     m.kv = take(2u * 2u * kMaxHeadDim, 16);         // new k, v (bf16)
     m.res = take(4u * 2u * kResBuf, 16);            // residual words of the tile's rows, two buffers
     m.xbuf = take(4u * uint32_t(xbuf_floats), 16);  // shared matvec input (raw), one per CTA
@@ -301,8 +297,8 @@ constexpr int kMmvItems = 8;
 MK_HD inline uint32_t mmv_row_stride(int K) { return ((uint32_t((K + 31) / 32) * 128u + 127u) & ~127u) + 64u; }
 constexpr uint32_t kMmvPartBytes = 2u * kNumConsumerWarps * 16u * 8u * 4u;
 
-inline int smem_misc_bytes(int n_pages, int attn_scratch_floats, int qrot_floats, int xbuf_floats, int comb_stride) {
-    return int(misc_layout(n_pages, attn_scratch_floats, qrot_floats, xbuf_floats, comb_stride).total);
+inline int smem_misc_bytes(int n_pages, int qrot_floats, int xbuf_floats, int comb_stride) {
+    return int(misc_layout(n_pages, qrot_floats, xbuf_floats, comb_stride).total);
 }
 
 // records a message for mk_last_error() and returns st

@@ -262,15 +262,12 @@ struct Shared {
     int* published;    // [1] instructions the publisher has retired
     unsigned long long* issued;   // [1] stream bytes the loader has staged into pages
     float* qrot;       // [8][128]
-    float* ascr;       // [attn_scratch_floats]
-    float* ml;         // [8][2]
-    float* cml;        // [8]
     uint16_t* knew;    // [128]
     uint16_t* vnew;    // [128]
 };
 
 __device__ __forceinline__ Shared carve(uint8_t* base, const Params& p) {
-    const MiscLayout m = misc_layout(p.n_pages, p.attn_scratch_floats, p.qrot_floats, p.xbuf_floats, p.comb_stride);
+    const MiscLayout m = misc_layout(p.n_pages, p.qrot_floats, p.xbuf_floats, p.comb_stride);
     uint8_t* b = base + p.smem_misc_off;
     Shared s;
     s.ring = base;
@@ -298,9 +295,6 @@ __device__ __forceinline__ Shared carve(uint8_t* base, const Params& p) {
     s.published = reinterpret_cast<int*>(b + m.red) + 33;
     s.issued = reinterpret_cast<unsigned long long*>(reinterpret_cast<int*>(b + m.red) + 34);
     s.qrot = reinterpret_cast<float*>(b + m.qrot);
-    s.ascr = reinterpret_cast<float*>(b + m.ascr);
-    s.ml = reinterpret_cast<float*>(b + m.ml);
-    s.cml = s.ml + 2 * kMaxHpg;
     s.knew = reinterpret_cast<uint16_t*>(b + m.kv);
     s.vnew = s.knew + kMaxHeadDim;
     return s;
