@@ -57,9 +57,10 @@ typedef struct {
 
 /* Schedule knobs; pass NULL to mk_build_schedule for the defaults (each 0 field = default).
  * With tile_bytes 0 every matvec operator is cut into about sm_count tiles (QKV tiles at most
- * head_dim rows), each streamed through the page ring step by step -- except at batch > 1 the
- * MLP down projection when ffn > 2048, whose tiles of about 131072 bytes hold their pages;
- * otherwise tiles hold about tile_bytes.  A row's arithmetic never depends on the tiling.
+ * head_dim rows), each streamed through the page ring page by page (at batch > 1 a tile whose rows
+ * are longer than 2048 takes at most 64 rows: its sums stay in registers over the staging
+ * ranges); otherwise tiles hold about tile_bytes.  A row's arithmetic never depends on the
+ * tiling.
  * kv_limit is the variable-length re-planning of the page's boundaries paragraph ("Inference
  * MegaKernel", section "Hand-written whole-model MegaKernel": dynamic batches and variable-length
  * requests change the static queue): attention chunks past a sequence's window get no tile, so a

@@ -134,7 +134,7 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     Geometry g{};
     // default page: 32768 at batch 1; at batch > 1 one 16-row block over kMmvRange positions
     g.page_bytes = o.page_bytes ? o.page_bytes : (c.batch > 1 ? 32 * kMmvRange : 32768);
-    g.tile_bytes = o.tile_bytes;   // 0: matvec tiles sized per SM (batch 1) / 131072 bytes (batch > 1)
+    g.tile_bytes = o.tile_bytes;   // 0: matvec tiles sized per SM (see the rows per tile below)
     // attention chunk: 128 positions, doubled (up to 512) while the chunks of all sequences and KV
     // heads would outnumber the 152 SMs of a GB300 (long contexts, batches): fewer, larger split-K
     // tiles.  A property of the model configuration alone, like every tile shape: the results do

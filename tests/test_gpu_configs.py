@@ -1,7 +1,8 @@
 """GPU parity of the megakernel against the CPU oracle on the larger configurations, through the
 C ABI (libmk.so): a long context (17 attention chunks of 512 positions per group, combined over
-partials in L2), batch 8 with uneven KV lengths (tiles held whole in the page ring, one input
-vector per sequence), and the 8B shape (8 chunks per lane, untied LM head).
+partials in L2), batch 8 with uneven KV lengths (the tensor-core kernel: 16-row TMA pages, every
+sequence's inputs staged once per range, COMB tiles), and the 8B shape (8 chunks per lane, untied
+LM head).
 
 Tolerances as in test_gpu_parity: logits within max |error| <= 1e-2 * max |oracle logit| per
 sequence, the greedy token equal wherever the oracle's top-2 margin exceeds 0.05, appended K/V
