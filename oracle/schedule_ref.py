@@ -93,7 +93,8 @@ MMV_RANGE = 2048   # batch > 1: positions of the inputs staged at a time (longer
 
 def tile_rows(cfg, o: SchedOpts, S: int) -> Dict[str, int]:
     """Rows (pairs for gate/up) per matvec tile.  tile_bytes 0: about one tile per operator per SM
-    (QKV tiles at most head_dim rows, so a tile touches one or two KV groups); at batch > 1 the
+    (QKV tiles at most head_dim rows, so a tile touches one or two KV groups; at batch > 1 whole
+    16-row MMA blocks of them); at batch > 1 the
     down (and output) projection, when its rows are longer than MMV_RANGE (its sums held over
     several staging ranges), takes at most 64 rows.  Otherwise tiles of about tile_bytes.  Explicit rows_* override either."""
     H, F, V, d = cfg.hidden, cfg.ffn, cfg.vocab, cfg.head_dim
@@ -102,7 +103,10 @@ def tile_rows(cfg, o: SchedOpts, S: int) -> Dict[str, int]:
     if o.tile_bytes == 0:
         down = min(64, ceil_div(H, S)) if (cfg.batch > 1 and F > MMV_RANGE) else ceil_div(H, S)
         o_rows = min(64, ceil_div(H, S)) if (cfg.batch > 1 and qd > MMV_RANGE) else ceil_div(H, S)
-        R = dict(qkv=min(d, ceil_div(nqkv, S)), o=o_rows, up=ceil_div(F, S),
+        qkv = min(d, ceil_div(nqkv, S))
+        if cfg.batch > 1:   # whole 16-row MMA blocks
+            qkv = min(d, ceil_div(qkv, 16) * 16)
+        R = dict(qkv=qkv, o=o_rows, up=ceil_div(F, S),
                  down=down, lm=ceil_div(V, S))
     else:
         tb = o.tile_bytes

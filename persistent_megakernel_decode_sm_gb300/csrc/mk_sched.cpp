@@ -163,12 +163,14 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     // rows per tile.  tile_bytes 0: about one tile per operator per SM -- a tile streams through
     // the page ring page by page, so it need not fit the ring, and the per-tile costs (dispatch,
     // input vector, first touch of its pages, completion) are paid once per operator and SM.  QKV
-    // tiles keep <= head_dim rows (a tile then touches at most two KV groups).  At batch > 1 an
+    // tiles keep <= head_dim rows (a tile then touches at most two KV groups; at batch > 1 they
+    // take whole 16-row MMA blocks: 21 rows would waste 11 of a second block).  At batch > 1 an
     // operator whose rows are longer than kMmvRange (the MLP down projection) keeps the sums of
     // all its rows over several staging ranges, so its tiles take at most 64 rows.  An explicit
     // tile_bytes: tiles of about tile_bytes.
     if (g.tile_bytes == 0) {
         g.r_qkv = std::min(d, cdiv(nqkv, S));
+        if (B > 1) g.r_qkv = std::min(d, (g.r_qkv + 15) / 16 * 16);   // (whole 16-row MMA blocks)
         g.r_o = (B > 1 && qd > kMmvRange) ? std::min(64, cdiv(H, S)) : cdiv(H, S);   // (sliced: <= 4 row blocks)
         g.r_up = cdiv(F, S);
         g.r_dn = (B > 1 && F > kMmvRange) ? std::min(64, cdiv(H, S)) : cdiv(H, S);
