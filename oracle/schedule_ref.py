@@ -92,22 +92,36 @@ MMV_RANGE = 2048   # batch > 1: positions of the inputs staged at a time (longer
 
 
 def tile_rows(cfg, o: SchedOpts, S: int) -> Dict[str, int]:
-    """Rows (pairs for gate/up) per matvec tile.  tile_bytes 0: about one tile per operator per SM
-    (QKV tiles at most head_dim rows, so a tile touches one or two KV groups; at batch > 1 whole
-    16-row MMA blocks of them); at batch > 1 the
-    down (and output) projection, when its rows are longer than MMV_RANGE (its sums held over
-    several staging ranges), takes at most 64 rows.  Otherwise tiles of about tile_bytes.  Explicit rows_* override either."""
+    """Rows (pairs for gate/up) per matvec tile.  tile_bytes 0: about one tile per operator per SM,
+    at batch 1 rounded up to whole consumer groups (two pages of whole rows -- for gate/up a gate
+    page and its up page -- at most 16 rows or 8 pairs), at batch > 1 only the QKV rows, to a
+    16-row MMA block; QKV tiles at most head_dim rows, so a tile touches one or two KV groups; at batch > 1 the down
+    (and output) projection, when its rows are longer than MMV_RANGE (its sums held over several
+    staging ranges), takes at most 64 rows.  Otherwise tiles of about tile_bytes.  Explicit rows_*
+    override either."""
     H, F, V, d = cfg.hidden, cfg.ffn, cfg.vocab, cfg.head_dim
     qd = cfg.n_q_heads * cfg.head_dim
     nqkv = qd + 2 * cfg.n_kv_heads * d
     if o.tile_bytes == 0:
-        down = min(64, ceil_div(H, S)) if (cfg.batch > 1 and F > MMV_RANGE) else ceil_div(H, S)
-        o_rows = min(64, ceil_div(H, S)) if (cfg.batch > 1 and qd > MMV_RANGE) else ceil_div(H, S)
-        qkv = min(d, ceil_div(nqkv, S))
-        if cfg.batch > 1:   # whole 16-row MMA blocks
-            qkv = min(d, ceil_div(qkv, 16) * 16)
-        R = dict(qkv=qkv, o=o_rows, up=ceil_div(F, S),
-                 down=down, lm=ceil_div(V, S))
+        pb = page_bytes_of(cfg, o)
+
+        def grp(K, pair):   # rows (pairs) a tile is rounded up to
+            if cfg.batch > 1:
+                return 1
+            rpp = max(1, pb // (2 * K))
+            return min(rpp, 8) if pair else min(2 * rpp, 16)
+
+        def up_to(r, m):
+            return ceil_div(r, m) * m
+
+        o_rows = up_to(ceil_div(H, S), grp(qd, False))
+        if cfg.batch > 1 and qd > MMV_RANGE:
+            o_rows = min(64, o_rows)
+        down = up_to(ceil_div(H, S), grp(F, False))
+        if cfg.batch > 1 and F > MMV_RANGE:
+            down = min(64, down)
+        R = dict(qkv=min(d, up_to(ceil_div(nqkv, S), 16 if cfg.batch > 1 else grp(H, False))), o=o_rows,
+                 up=up_to(ceil_div(F, S), grp(H, True)), down=down, lm=up_to(ceil_div(V, S), grp(H, False)))
     else:
         tb = o.tile_bytes
 

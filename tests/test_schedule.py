@@ -88,7 +88,7 @@ def test_batch1_wave_spread_one_matvec_tile_per_sm():
         waves = [int(w[22]) for w in q[s] if w[0] != sr.END]
         assert len(waves) == len(set(waves)), f"sm {s} holds two tiles of one wave"
     n_up = sum(1 for s in range(S) for w in q[s] if w[0] == sr.UPGATE and w[1] == 0)
-    assert n_up == S
+    assert n_up == -(-cfg.ffn // 56) <= S   # 54 pairs per SM, rounded up to whole groups of 8
 
 
 def _mutate(q, fn):
