@@ -42,6 +42,13 @@ def test_build_schedule_rejects_bad_arguments():
         mk.Schedule(small_config(hidden=1024), 4, page_bytes=1024)   # holds no gate/up row
     with pytest.raises(mk.MkError):
         mk.Schedule(small_config(), 4, page_bytes=1000)
+    # batch > 1: a page is a 16-row block over page_bytes / 32 <= 2048 positions, and a tile of
+    # rows longer than 2048 keeps at most 64 rows of sums
+    with pytest.raises(mk.MkError):
+        mk.Schedule(small_config(batch=2), 4, page_bytes=131072)
+    with pytest.raises(mk.MkError):
+        mk.Schedule(small_config(batch=2, ffn=4096), 4, rows_down=65)
+    assert mk.Schedule(small_config(batch=2, ffn=4096), 4, rows_down=64).attn_chunk > 0
 
 
 def test_patch_and_scratch_size():
