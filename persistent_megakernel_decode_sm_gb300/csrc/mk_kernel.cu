@@ -1071,10 +1071,11 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
     switch (op) {
         case OP_QKV: st_tag(p.qkv + lb * p.nqkv + row, s0, c.tag); break;
         case OP_OPROJ: {
-            if constexpr (kBatchedKernel) {   // (batch > 1: 3-bit-tagged 32-bit residual words)
+            if constexpr (kBatchedKernel) {   // (batch > 1: 3-bit-tagged 32-bit residual words; res: read ahead)
                 const float r = l == 0 ? bf16f(p.embed[size_t(step_token(c, b)) * p.H + row])
-                                       : poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_out) + (lb - p.B) * p.H + row,
-                                                pc, c.tag);
+                              : res   ? *res
+                                      : poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_out) + (lb - p.B) * p.H + row,
+                                               pc, c.tag);
                 st_htag(reinterpret_cast<uint32_t*>(p.x_attn) + lb * p.H + row, r + s0, htag(c.tag));
                 break;
             }
@@ -1087,7 +1088,7 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
         case OP_UPGATE: st_htag(p.h + lb * p.F + row, __fdividef(s0, 1.0f + __expf(-s0)) * s1, htag(c.tag)); break;
         case OP_DOWN: {
             if constexpr (kBatchedKernel) {
-                const float r = poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_attn) + lb * p.H + row, pc, c.tag);
+                const float r = res ? *res : poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_attn) + lb * p.H + row, pc, c.tag);
                 st_htag(reinterpret_cast<uint32_t*>(p.x_out) + lb * p.H + row, r + s0, htag(c.tag));
                 break;
             }
@@ -1287,6 +1288,23 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[q][h][e] = 0.f;
     int pg = 0;   // the tile's next page
+    // the residual of this thread's output in the first round of outputs, read ahead of the input
+    // poll (produced an operator or more earlier: almost always ready), so the two round trips
+    // overlap; a stale tag leaves it to the epilogue's poll
+    float rres = 0.f;
+    bool rok = false;
+    {
+        const int oq = tid >> 7, orr = (tid >> 3) & 15, ocol = tid & 7, orow = oq * rb + orr;
+        if ((op == OP_DOWN || (op == OP_OPROJ && l > 0)) && !pair && oq < nblk && ocol < B && orow < R) {
+            const size_t lb = size_t(l) * B + ocol;
+            const uint32_t* a = op == OP_DOWN ? reinterpret_cast<const uint32_t*>(p.x_attn) + lb * p.H + si.w[W_A0] + orow
+                                              : reinterpret_cast<const uint32_t*>(p.x_out) + (lb - B) * p.H + si.w[W_A0] + orow;
+            uint32_t w;
+            asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(w) : "l"(a));
+            rok = ((w ^ htag(c.tag)) & 7u) == 0;
+            rres = __uint_as_float(w & ~7u);
+        }
+    }
     // block q over the slices [s0, s1) of the staged range (positions from k0): MMA rows g and
     // g + 8 are page rows g and g + 8; each page is waited for, used and given back in turn
     auto block = [&](int q, int s0, int s1, int k0, uint32_t xrow, float (&a)[2][4]) -> bool {
@@ -1332,7 +1350,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                         s0 += part[(q * kNumConsumerWarps + w) * 128 + rr * 8 + col];
                         if (pair) s1 += part[(q * kNumConsumerWarps + w) * 128 + (rr + 8) * 8 + col];
                     }
-                    mv_epilogue<false>(c, si, pc, col, row, s0, s1, nullptr, bv, bi);
+                    mv_epilogue<false>(c, si, pc, col, row, s0, s1, (blk0 == 0 && rok) ? &rres : nullptr, bv, bi);
                 }
             }
         }
