@@ -1288,6 +1288,10 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[q][h][e] = 0.f;
     int pg = 0;   // the tile's next page
+    // rows of 8 x 256 positions (one range): a thread's items all take gain chunk tid, read ahead
+    // of the input poll so that its round trip overlaps the poll
+    const bool gpre = gain && K == 8 * kConsumerThreads;
+    const uint4 gw_pre = gpre ? __ldg(reinterpret_cast<const uint4*>(gain + tid * 8)) : make_uint4(0u, 0u, 0u, 0u);
     // the residual of this thread's output in the first round of outputs, read ahead of the input
     // poll (produced an operator or more earlier: almost always ready), so the two round trips
     // overlap; a stale tag leaves it to the epilogue's poll
@@ -1416,8 +1420,8 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
 #pragma unroll
             for (int j = 0; j < kMmvItems; ++j) {
                 const int i = tid + j * kConsumerThreads;
-                gws[j] = (gain && i < items) ? __ldg(reinterpret_cast<const uint4*>(gain + k0 + (i % csr) * 8))
-                                   : make_uint4(0u, 0u, 0u, 0u);
+                gws[j] = (!gpre && i < items) ? __ldg(reinterpret_cast<const uint4*>(gain + k0 + (i % csr) * 8))
+                                              : gw_pre;
             }
 #pragma unroll
             for (int j = 0; j < kMmvItems; ++j) {
