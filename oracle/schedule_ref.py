@@ -245,13 +245,14 @@ def enumerate_tiles(cfg, o: SchedOpts, S: int) -> Tuple[List[Tile], Counters, Di
                 for c in range(nchunk):
                     if c * C >= kv_window(cfg, o, b):   # chunks past the sequence's window: no tile
                         break
+                    rows = min(C, kv_window(cfg, o, b) - c * C)   # the chunk's K/V rows in the window
                     if B == 1:   # the chunk holding pos combines and completes
                         tiles.append(Tile(ATTN, l, b, g, c, C, 5 * l + 1,
                                           [(cnt.qkv(l, g), qkv_tiles_of_group[g])],
-                                          [(cnt.comb(l), 1)], 2 * C * d * 2, cond=True))
+                                          [(cnt.comb(l), 1)], 2 * rows * d * 2, cond=True))
                     else:        # combined by the group's COMB tile
                         tiles.append(Tile(ATTN, l, b, g, c, C, 5 * l + 1,
-                                          [(cnt.qkv(l, g), qkv_tiles_of_group[g])], [], 2 * C * d * 2))
+                                          [(cnt.qkv(l, g), qkv_tiles_of_group[g])], [], 2 * rows * d * 2))
         if B > 1:
             for b in range(B):
                 for g in range(nkv):

@@ -263,8 +263,11 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         for (int32_t b = 0; b < B; ++b)
             for (int32_t gr = 0; gr < nkv; ++gr)
                 for (int32_t ch = 0; ch < g.n_chunk && int64_t(ch) * g.attn_chunk < g.kv_limit[b]; ++ch) {
+                    // (its stream: the chunk's K and V rows inside the window -- the last chunk of a
+                    // window is partly filled, so it costs less and is placed last in its wave)
+                    const int64_t rows = std::min<int64_t>(g.attn_chunk, int64_t(g.kv_limit[b]) - int64_t(ch) * g.attn_chunk);
                     add(OP_ATTN, l, b, gr, ch, g.attn_chunk, 5 * l + 1, {{cm.qkv(l, gr), qkv_tiles_of_group[gr]}},
-                        {cm.comb(l), 1}, int64_t(2) * g.attn_chunk * d * 2);
+                        {cm.comb(l), 1}, int64_t(2) * rows * d * 2);
                     if (B == 1) tiles.back().cond = true;   // the chunk holding pos combines and completes
                     else tiles.back().npub = 0;               // combined by the group's COMB tile
                 }
