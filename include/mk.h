@@ -68,7 +68,8 @@ typedef struct {
  * schedule with new windows. */
 typedef struct {
     int32_t page_bytes;  /* shared-memory page size (a power of two); default 32768, at batch > 1
-                            65536 (a page is then a 16-row block over page_bytes / 32 positions) */
+                            65536 (a page is then a 16-row block over page_bytes / 32 positions,
+                            which must divide the 2048-position staging range: MK_ERR_ARG) */
     int32_t tile_bytes;  /* 0: per-SM tiles (see above); else the target weight bytes per matvec
                             tile (capped at 8 rows for QKV, O and down, 16 gate/up pairs, 32
                             LM-head rows)                                                        */
@@ -91,8 +92,9 @@ typedef struct mk_ctx mk_ctx;           /* opaque, library-owned bound context *
  * Tiles: per layer QKV rows (RMSNorm prologue), split-K attention chunks (RoPE + KV append in
  * the chunk that holds pos; the chunk that completes its KV group also does the group's
  * log-sum-exp combine), O rows (+ residual), gate/up row pairs (SiLU(gate)*up), down rows
- * (+ residual); then LM-head rows (final RMSNorm prologue, running max/argmax) and one argmax
- * per sequence.
+ * (+ residual; at batch > 1 with ffn > 2048 one tile per (2048-position staging range, row
+ * block), the last range's tile adding the others' partial sums); then LM-head rows (final
+ * RMSNorm prologue, running max/argmax) and one argmax per sequence.
  * sm_count: number of queues (= CTAs launched), 1 <= sm_count <= 4096.
  * opts: NULL for defaults.  On success *out receives a new schedule (free with
  * mk_schedule_free).  Errors: MK_ERR_ARG (bad cfg/opts), MK_ERR_CAPACITY (a tile needs more
@@ -109,7 +111,11 @@ mk_status mk_build_schedule(const mk_model_cfg* cfg, int32_t sm_count, const mk_
  *       COMB, the combine of one (sequence, KV group)'s chunk partials, exists at batch > 1 only)
  *   [1] layer (n_layers for LMHEAD / ARGMAX)   [2] sequence b (attention, combine, argmax)
  *   [3] a0: first row | KV group             [4] a1: rows (pairs for UPGATE) | chunk | #LM tiles
- *   [5] a2: chunk length (ATTN, COMB) | LM tile index (LMHEAD)
+ *   [5] a2: chunk length (ATTN, COMB) | LM tile index (LMHEAD) | staging range (DOWN at batch
+ *       > 1 with ffn > 2048: the tile covers positions [2048 a2, 2048 (a2 + 1)) of its rows; a
+ *       tile of a lower range completes nothing and stores its partial sums, the tile of the
+ *       last range, of a higher id in the same wave, waits for them, adds them in range order,
+ *       writes the rows and completes)
  *   [6] number of waits (<= 4)   [7..14] (counter, need) pairs
  *   [15] number of completions (<= 2)   [16..19] (counter, delta) pairs
  *   [20] pages of the largest stream the tile may need   [21] tile id   [22] wave

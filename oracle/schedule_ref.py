@@ -24,7 +24,11 @@ Tiles (per layer l, in this order; ids are assigned in enumeration order):
           that combine for the group and carries its completion.
   OPROJ   rows of Wo, residual add.
   UPGATE  row pairs [r, r+R_up) of gate and of up, SiLU(gate)*up epilogue.
-  DOWN    rows of Wdown, residual add.
+  DOWN    rows of Wdown, residual add.  At batch > 1 with rows longer than MMV_RANGE: one tile
+          per (staging range a2, row block), all tiles of range 0 first, then range 1, ...; a
+          tile of a lower range stores its partial sums, the tile of the last range (so of
+          higher id than every partial it needs) adds them in range order, writes the rows and
+          alone carries the completion.
 then LMHEAD (rows of the LM head, final RMSNorm prologue, per-tile max/argmax partial) and
 ARGMAX (b).
 Waves: the DAG's longest-path level; per layer QKV=5l, ATTN=5l+1, OPROJ=5l+2, UPGATE=5l+3,
@@ -34,7 +38,9 @@ LMHEAD); compute pool = COMB and ARGMAX.  Within a wave memory tiles are placed 
 tiles.
 Rows per tile: (tile_bytes 0) about one tile per operator per SM -- such a tile streams through
 the page ring page by page (at batch > 1 a page is a 16-row block over page_bytes / 32
-positions); at batch > 1 a tile of rows longer than MMV_RANGE (its sums held over several
+positions); at batch > 1 the down projection of rows longer than MMV_RANGE takes about
+H * ranges / S rows per tile (whole 16-row blocks, at most 64); any other tile of rows longer
+than MMV_RANGE (its sums held over several
 staging ranges) takes at most 64 rows; otherwise tiles of about tile_bytes.
 Assignment, wave by wave: memory tiles sorted by (cost desc, tile id asc), then compute tiles
 likewise; the k-th tile of that order (from 0) goes to the SM with the smallest accumulated cost
@@ -117,9 +123,8 @@ def tile_rows(cfg, o: SchedOpts, S: int) -> Dict[str, int]:
         o_rows = up_to(ceil_div(H, S), grp(qd, False))
         if cfg.batch > 1 and qd > MMV_RANGE:
             o_rows = min(64, o_rows)
-        down = up_to(ceil_div(H, S), grp(F, False))
-        if cfg.batch > 1 and F > MMV_RANGE:
-            down = min(64, down)
+        nrg = down_ranges(cfg)
+        down = min(64, up_to(ceil_div(H * nrg, S), 16)) if nrg > 1 else up_to(ceil_div(H, S), grp(F, False))
         R = dict(qkv=min(d, up_to(ceil_div(nqkv, S), 16 if cfg.batch > 1 else grp(H, False))), o=o_rows,
                  up=up_to(ceil_div(F, S), grp(H, True)), down=down, lm=up_to(ceil_div(V, S), grp(H, False)))
     else:
@@ -267,11 +272,14 @@ def enumerate_tiles(cfg, o: SchedOpts, S: int) -> Tuple[List[Tile], Counters, Di
             n = min(R["up"], F - r0)
             tiles.append(Tile(UPGATE, l, 0, r0, n, 0, 5 * l + 3, [(cnt.o(l), n_o)],
                               [(cnt.up(l), 1)], 2 * n * H * 2))
-        for t in range(n_dn):
-            r0 = t * R["down"]
-            n = min(R["down"], H - r0)
-            tiles.append(Tile(DOWN, l, 0, r0, n, 0, 5 * l + 4, [(cnt.up(l), n_up)],
-                              [(cnt.down(l), 1)], n * F * 2))
+        nrg = down_ranges(cfg)
+        for r in range(nrg):
+            kr = min(MMV_RANGE, F - r * MMV_RANGE) if nrg > 1 else F
+            for t in range(n_dn):
+                r0 = t * R["down"]
+                n = min(R["down"], H - r0)
+                tiles.append(Tile(DOWN, l, 0, r0, n, r, 5 * l + 4, [(cnt.up(l), n_up)],
+                                  [(cnt.down(l), 1)] if r == nrg - 1 else [], n * kr * 2))
     for t in range(n_lm):
         r0 = t * R["lm"]
         n = min(R["lm"], V - r0)
@@ -305,6 +313,12 @@ def _shuffle(xs: List[Tile], rng: SplitMix64) -> List[Tile]:
     return xs
 
 
+def down_ranges(cfg) -> int:
+    """Staging ranges of the down projection's rows when it runs one tile per (range, row block):
+    at batch > 1 with rows longer than MMV_RANGE; else 1."""
+    return ceil_div(cfg.ffn, MMV_RANGE) if cfg.batch > 1 and cfg.ffn > MMV_RANGE else 1
+
+
 def page_bytes_of(cfg, o: SchedOpts) -> int:
     return o.page_bytes or (65536 if cfg.batch > 1 else 32768)
 
@@ -318,6 +332,8 @@ def tile_pages(t: Tile, cfg, o: SchedOpts) -> int:
         K = cfg.q_dim if t.op == OPROJ else (cfg.ffn if t.op == DOWN else cfg.hidden)
         if cfg.batch > 1:   # 16-row blocks (gate/up: 8 pairs) over page_bytes / 32 positions
             kp = page_bytes_of(cfg, o) // 32
+            if t.op == DOWN and down_ranges(cfg) > 1:   # one staging range of the rows
+                K = min(MMV_RANGE, K - t.a2 * MMV_RANGE)
             return ceil_div(t.a1, 8 if t.op == UPGATE else 16) * ceil_div(K, kp)
         rpp = page_bytes_of(cfg, o) // (2 * K)
         return ceil_div(t.a1, rpp) * (2 if t.op == UPGATE else 1)
@@ -417,7 +433,8 @@ def validate(queues: np.ndarray, totals: np.ndarray, cfg, opts: Optional[SchedOp
       attention chunk tiles of a group carry conditional completions (exactly one completion per
       group is counted): the combining chunk tile's wait inside its wave is on lower chunks of
       its group, i.e. on lower ids, which no queue runs after a higher id of that wave (at
-      batch > 1 the COMB tile of the group waits likewise on the chunk tiles, all of lower id);
+      batch > 1 the COMB tile of the group waits likewise on the chunk tiles, all of lower id, and
+      a down tile of the last staging range on the same rows' tiles of the other ranges);
     * (DAG + per-SM program order) is acyclic -- implied by the points above;
     * capacity: at most 4 waits and 2 completions per instruction; no attention tile needs more
       pages than the ring holds.
@@ -536,8 +553,12 @@ def _reads_writes(t: Tile, cfg):
         W.append((("h", l), t.a1))
     elif op == DOWN:
         R.append((("h", l), F))
-        R.append((("x_attn", l), H))
-        W.append((("x_out", l), t.a1))
+        nrg = down_ranges(cfg)
+        if t.a2 + 1 < nrg:   # a partial of range a2 (the last range's tile reads it: in the simulator)
+            W.append((("dpart", l, t.a0), 1))
+        else:
+            R.append((("x_attn", l), H))
+            W.append((("x_out", l), t.a1))
     elif op == LMHEAD:
         R.append((("x_out", L - 1), H))
         W.append((("lmpart",), 1))
@@ -555,7 +576,8 @@ def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, see
     chunk tiles past it do nothing, the others write their partial, and the tile of the chunk
     holding it waits (inside its wave) until the lower chunks of its group have written theirs,
     then writes the group's attention output and fires the completion (at batch > 1 the group's
-    COMB tile waits for every active chunk's partial and does that).  Reports a deadlock (no
+    COMB tile waits for every active chunk's partial and does that; a batch > 1 down tile of the
+    last staging range waits likewise for the partials of its rows' other ranges).  Reports a deadlock (no
     SM can progress before all reach END) and any read of a buffer whose writer has not yet run
     in the current step."""
     S, Q, _ = queues.shape
@@ -588,6 +610,9 @@ def simulate(queues: np.ndarray, totals: np.ndarray, cfg, n_epochs: int = 2, see
                 combines = (t.op == ATTN and t.cond and t.a1 == c_pos) or t.op == COMB
                 if ok and combines:   # the combine reads chunks 0 .. c_pos - 1 (COMB: 0 .. c_pos)
                     ok = written.get(part_key, 0) >= (c_pos if t.op == ATTN else c_pos + 1)
+                nrg = down_ranges(cfg) if t.op == DOWN else 1
+                if ok and nrg > 1 and t.a2 == nrg - 1:   # the last range's tile reads the other partials
+                    ok = written.get(("dpart", t.layer, t.a0), 0) >= nrg - 1
                 if ok:
                     if track_data:
                         if t.tid not in rw_cache:

@@ -178,8 +178,8 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, const
                 src1 = static_cast<const uint8_t*>(w->wgate_up[l]) + int64_t(F + a0) * H * 2;
                 b0 = b1 = int64_t(a1) * H * 2;
                 break;
-            case OP_DOWN:
-                if (!rows(H, H)) return bad("rows");
+            case OP_DOWN:   // (batch > 1, rows longer than kMmvRange: a2 = the tile's staging range)
+                if (!rows(H, H) || unsigned(a2) >= unsigned(mmv_down_ranges(B, F))) return bad("rows");
                 src0 = static_cast<const uint8_t*>(w->wdown[l]) + int64_t(a0) * F * 2;
                 b0 = int64_t(a1) * F * 2;
                 break;
@@ -206,7 +206,8 @@ static mk_status resolve_queues(const mk_schedule* s, const mk_weights* w, const
         if (src0) {   // whole rows (or row slices) per page; gate/up: gate and up row groups alternate
             if (mv[op].rpp < 1) return bad("a page holds no row");
             if (kp && mv[op].K > kMmvRange && a1 > 64) return bad("rows of a tile over several ranges");   // (<= 4 blocks)
-            const int64_t pages = mv_tile_pages(mv[op], kp, a1, op == OP_UPGATE);
+            const int64_t pages = (op == OP_DOWN && mmv_down_ranges(B, F) > 1)
+                                      ? mmv_range_pages(F, kp, a1, a2) : mv_tile_pages(mv[op], kp, a1, op == OP_UPGATE);
             if (pages != x[W_NPAGES] || b0 + b1 > (int64_t(1) << 31) - 1) return bad("page count");
             put64(x + W_SRC0, src0);
             put64(x + W_SRC1, src1);
@@ -455,6 +456,7 @@ extern "C" mk_status mk_bind_paged(const mk_schedule* s, const mk_weights* w, co
     p.part = reinterpret_cast<uint64_t*>(sb + sl.part);
     p.o = reinterpret_cast<uint64_t*>(sb + sl.o);
     p.h = reinterpret_cast<uint32_t*>(sb + sl.h);
+    p.dpart = reinterpret_cast<uint32_t*>(sb + sl.dpart);
     p.lm_part = reinterpret_cast<int4*>(sb + sl.lm_part);
     p.rope = reinterpret_cast<const float2*>(sb + sl.rope);
     // The one reader without tags: the argmax over the LM-head partials, after an acquiring wait
@@ -827,6 +829,7 @@ extern "C" mk_status mk_decode_step_static(mk_ctx* c, const int32_t* tokens, con
     p.part = move(p.part);
     p.o = move(p.o);
     p.h = move(p.h);
+    p.dpart = move(p.dpart);
     p.lm_part = move(p.lm_part);
     p.rope = move(const_cast<float2*>(p.rope));
     // the array keeps the previous call's contents: reset what must start fresh (error word and

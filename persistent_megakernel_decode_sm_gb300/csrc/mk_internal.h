@@ -54,6 +54,9 @@ constexpr int kResBuf = 64;          // residual words of a tile's rows staged i
 constexpr int kMaxRingPages = 64;    // cap on the page ring's length (the shared memory sets the rest)
 constexpr int kMinXBuf = 3072;       // floats of the shared input buffer at least (attention scores, combine)
 constexpr int kMmvRange = 2048;      // batch > 1: positions of a row staged at a time (longer rows: ranges)
+// batch > 1: staging ranges of the MLP down projection's rows when it is cut into one tile per
+// (range, row block) -- rows longer than kMmvRange -- else 1 (whole-row tiles)
+MK_HD inline int mmv_down_ranges(int B, int F) { return B > 1 && F > kMmvRange ? (F + kMmvRange - 1) / kMmvRange : 1; }
 constexpr int kAttnChunkTiles = 152; // default attention chunk: grown while a layer has more chunks
 
 
@@ -89,7 +92,7 @@ struct CounterMap {
 // half, written and read as single 64-bit accesses.  A reader that sees this step's tag has the
 // value of this step -- the element needs no separate flag, fence or counter to be consumed.
 struct ScratchLayout {
-    size_t err, tokens, x_attn, x_out, qkv, part, o, h, lm_part, rope, total;
+    size_t err, tokens, x_attn, x_out, qkv, part, o, h, dpart, lm_part, rope, total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -109,6 +112,7 @@ inline ScratchLayout scratch_layout(const mk_model_cfg& c, const Geometry& g, in
     s.part = take(L * B * size_t(c.n_kv_heads) * g.n_chunk * hpg * (d + 2) * 8);   // tagged chunk partials
     s.o = take(L * B * qd * 8);                       // tagged
     s.h = take(L * B * size_t(c.ffn) * 4);            // fp32 with a 3-bit tag
+    s.dpart = take(L * size_t(mmv_down_ranges(c.batch, c.ffn) - 1) * B * H * 4);   // down partial sums, 3-bit tag
     s.lm_part = take(B * size_t(S) * kNumConsumerWarps * 16);   // per (sequence, CTA, warp): max, index, epoch
     s.rope = take(size_t(c.max_seq) * (d / 2) * 8);
     s.total = off;
@@ -164,6 +168,11 @@ MK_HD inline int64_t mv_tile_pages(const MvShape& m, int kp, int64_t rows, bool 
     if (kp) return ((rows + (pair ? 7 : 15)) / (pair ? 8 : 16)) * ((m.K + kp - 1) / kp);
     return ((rows + m.rpp - 1) / m.rpp) * (pair ? 2 : 1);
 }
+// batch > 1: pages of a tile over staging range r of rows of length K (16-row blocks)
+MK_HD inline int64_t mmv_range_pages(int K, int kp, int64_t rows, int r) {
+    const int64_t kr = K - int64_t(r) * kMmvRange < kMmvRange ? K - int64_t(r) * kMmvRange : kMmvRange;
+    return ((rows + 15) / 16) * ((kr + kp - 1) / kp);
+}
 
 // ---- kernel parameters (passed by value) ----------------------------------------------------
 struct Params {
@@ -198,6 +207,7 @@ struct Params {
     uint64_t* part;     // [L][B][nkv][n_chunk][hpg][d + 2] attention chunk partials (tagged)
     uint64_t* o;        // tagged [L][B][qd]: attention output
     uint32_t* h;        // [L][B][F]: SwiGLU output, fp32 with a 3-bit step tag in the low mantissa bits
+    uint32_t* dpart;    // batch > 1: [L][ranges - 1][B][H] partial sums of the down projection's range tiles (3-bit tag)
     int4* lm_part;      // [B][S][kNumConsumerWarps]: (max bits, index, epoch, 0)
     const float2* rope; // [max_seq][d/2] (cos, sin)
     // step
@@ -289,12 +299,14 @@ MK_HD inline MiscLayout misc_layout(int n_pages, int qrot_floats, int xbuf_float
 
 // Batch > 1 matvec inputs staged in shared memory, one range of at most kMmvRange positions at a
 // time: per sequence a row of mmv_row_stride(range) bytes holding a 32-bit word per position
-// (fp32 as polled, then a bf16 (hi, lo) pair), rounded to 128 bytes plus 64 (consecutive
-// sequences' rows then start 64 bytes apart in the banks); after the rows, the partial sums of two
+// (fp32 as polled, then a bf16 (hi, lo) pair), rounded to 128 bytes plus 16: the eight lanes of
+// a quarter warp read 16 bytes each at (sequence g in {2j, 2j + 1}, 32 t4 bytes into a 128-byte
+// step), distinct bank quads only when consecutive rows start 16 bytes apart in the banks
+// (measured at batch 8 against 64 bytes apart, a two-way conflict: 1645 -> 1621 us a step); after the rows, the partial sums of two
 // 16-row blocks from the 8 consumer warps.  A thread polls at most kMmvItems 8-element chunks of
 // a range per round.
 constexpr int kMmvItems = 8;
-MK_HD inline uint32_t mmv_row_stride(int K) { return ((uint32_t((K + 31) / 32) * 128u + 127u) & ~127u) + 64u; }
+MK_HD inline uint32_t mmv_row_stride(int K) { return ((uint32_t((K + 31) / 32) * 128u + 127u) & ~127u) + 16u; }
 constexpr uint32_t kMmvPartBytes = 2u * kNumConsumerWarps * 16u * 8u * 4u;
 
 inline int smem_misc_bytes(int n_pages, int qrot_floats, int xbuf_floats, int comb_stride) {

@@ -357,6 +357,7 @@ struct Stream {
     uint32_t rows, rowbytes, rpp;    // matvec: whole rows per page (0 rows: a plain byte stream)
     uint32_t K, nblk;                // batch > 1: row length, 16-row blocks (gate/up: 8 pairs),
     uint32_t row0, g0, up;           // first row, innermost box edge, row offset of the up rows
+    uint32_t r0;                     // the first staging range (a down tile of one range: its range)
     const uint8_t* tmap;             // and the weights' tensor map
 };
 
@@ -399,7 +400,7 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos
     st.kv_off = 0;
     st.inter = 0;
     st.rows = st.rowbytes = st.rpp = 0;
-    st.K = st.nblk = st.row0 = st.g0 = st.up = 0;
+    st.K = st.nblk = st.row0 = st.g0 = st.up = st.r0 = 0;
     st.tmap = nullptr;
     const int op = w[W_OP];
     if (is_matvec(op)) {   // whole rows per page; gate/up: gate and up row groups in alternate pages
@@ -417,6 +418,11 @@ __device__ int stream_of(const Params& p, const int32_t* w, Stream& st, int dpos
             st.K = uint32_t(p.mv[op].K);
             st.nblk = (st.rows + (st.inter ? 7u : 15u)) / (st.inter ? 8u : 16u);
             st.pages = int(mv_tile_pages(p.mv[op], p.mmv_kp, st.rows, st.inter));
+            if (op == OP_DOWN && mmv_down_ranges(p.B, p.F) > 1) {   // one staging range of the rows
+                st.r0 = uint32_t(w[W_A2]);
+                if (st.r0 >= uint32_t(mmv_down_ranges(p.B, p.F))) return MK_ERR_BOUNDS;
+                st.pages = int(mmv_range_pages(int(st.K), p.mmv_kp, st.rows, int(st.r0)));
+            }
             st.row0 = uint32_t(w[W_A0]);
             st.g0 = uint32_t(mmv_g0(int(st.K), p.mmv_kp));
             st.up = uint32_t(p.F);
@@ -603,7 +609,7 @@ __device__ void loader(const Params& p, const Shared& sh) {
                     // over the kp positions of slice sl; pages in the order (range, block, slice)
                     const uint32_t kp = uint32_t(p.mmv_kp), nsr = uint32_t(kMmvRange) / kp;
                     const uint32_t nsl = (st.K + kp - 1u) / kp, per_r = st.nblk * nsr;
-                    const uint32_t r = uint32_t(pg) / per_r, rem = uint32_t(pg) % per_r;
+                    const uint32_t r = st.r0 + uint32_t(pg) / per_r, rem = uint32_t(pg) % per_r;
                     const uint32_t nsl_r = min(nsr, nsl - r * nsr);
                     const uint32_t q = rem / nsl_r, sl = r * nsr + rem % nsl_r;
                     // one tensor box per page (gate/up: the 8 gate rows, then the same pairs' up
@@ -1252,6 +1258,36 @@ __device__ __forceinline__ void tile_page(const Params& p, const SlotInfo& si, i
     ph = uint32_t(si.first_phase) ^ ((idx / uint32_t(p.n_pages)) & 1u);
 }
 
+// A down-projection tile of one staging range (batch > 1, rows longer than kMmvRange): the tile
+// of a lower range r stores its sum s of row `row` for sequence b as a 3-bit-tagged partial
+// ([L][ranges - 1][B][H]) and returns s; the tile of the last range reads the other ranges'
+// partials as they land (the loads of up to four issued before any tag is checked), adds them in
+// range order and its own sum last, and returns the row's sum.
+__device__ float down_partials(const Cw& c, int pc, int l, int b, int row, int r, int nrg, float s) {
+    const Params& p = c.p;
+    const size_t rstride = size_t(p.B) * p.H;
+    uint32_t* base = p.dpart + size_t(l) * (nrg - 1) * rstride + size_t(b) * p.H + row;
+    const uint32_t ht = htag(c.tag);
+    if (r + 1 < nrg) {
+        st_htag(base + r * rstride, s, ht);
+        return s;
+    }
+    float t = 0.f;
+    for (int r0 = 0; r0 < nrg - 1; r0 += 4) {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (r0 + i < nrg - 1)
+                asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(w[i]) : "l"(base + (r0 + i) * rstride));
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (r0 + i < nrg - 1)
+                t += ((w[i] ^ ht) & 7u) == 0 ? __uint_as_float(w[i] & ~7u)
+                                             : poll1h(p, c.sh, base + (r0 + i) * rstride, pc, c.tag);
+    }
+    return t + s;
+}
+
 __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
     const Params& p = c.p;
     const MvShape& m = si.mv;
@@ -1264,6 +1300,12 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
     // sums of every block of the tile over the ranges (at most 4 blocks: 64 rows, scheduled so)
     const int KR = min(K, kMmvRange), RS = int(mmv_row_stride(KR));
     const bool multi = K > KR;
+    // the down projection of such rows runs one staging range per tile (range a2); the tile of the
+    // last range adds the other ranges' partial sums and alone writes the rows
+    const int nrg = (K + KR - 1) / KR;
+    const bool dsplit = op == OP_DOWN && mmv_down_ranges(B, p.F) > 1;
+    const int rr0 = dsplit ? si.w[W_A2] : 0, rr1 = dsplit ? rr0 + 1 : nrg;
+    const bool dred = rr1 == nrg;   // this tile writes the rows
     uint8_t* stage = reinterpret_cast<uint8_t*>(c.sh.xbuf);
     float* part = reinterpret_cast<float*>(stage + uint32_t(p.xbuf_floats) * 4u - kMmvPartBytes);
     const uint32_t stage_s = smem_u32(stage), ring_base = smem_u32(c.sh.ring);
@@ -1299,7 +1341,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
     bool rok = false;
     {
         const int oq = tid >> 7, orr = (tid >> 3) & 15, ocol = tid & 7, orow = oq * rb + orr;
-        if ((op == OP_DOWN || (op == OP_OPROJ && l > 0)) && !pair && oq < nblk && ocol < B && orow < R) {
+        if (((op == OP_DOWN && dred) || (op == OP_OPROJ && l > 0)) && !pair && oq < nblk && ocol < B && orow < R) {
             const size_t lb = size_t(l) * B + ocol;
             const uint32_t* a = op == OP_DOWN ? reinterpret_cast<const uint32_t*>(p.x_attn) + lb * p.H + si.w[W_A0] + orow
                                               : reinterpret_cast<const uint32_t*>(p.x_out) + (lb - B) * p.H + si.w[W_A0] + orow;
@@ -1354,14 +1396,14 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                         s0 += part[(q * kNumConsumerWarps + w) * 128 + rr * 8 + col];
                         if (pair) s1 += part[(q * kNumConsumerWarps + w) * 128 + (rr + 8) * 8 + col];
                     }
-                    mv_epilogue<false>(c, si, pc, col, row, s0, s1, (blk0 == 0 && rok) ? &rres : nullptr, bv, bi);
+                    if (dsplit) s0 = down_partials(c, pc, l, col, si.w[W_A0] + row, rr0, nrg, s0);
+                    if (dred) mv_epilogue<false>(c, si, pc, col, row, s0, s1, (blk0 == 0 && rok) ? &rres : nullptr, bv, bi);
                 }
             }
         }
         return cbar(c, pc);   // the partial area is reused
     };
-    const int nrg = (K + KR - 1) / KR;
-    for (int rr = 0; rr < nrg; ++rr) {
+    for (int rr = rr0; rr < rr1; ++rr) {
         const int k0 = rr * KR;
         const int kr = min(KR, K - k0), csr = kr / 8, items = B * csr;
         // 1. the range's inputs, every element polled until it carries this step's tag and stored
@@ -1402,7 +1444,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                 if (!spin_more(c, spn, pc)) return false;
             }
         }
-        if (rr == 0 && c.warp == 0 && c.lane == 0) stamp(p, pc, 6);   // (trace: this warp's inputs polled)
+        if (rr == rr0 && c.warp == 0 && c.lane == 0) stamp(p, pc, 6);   // (trace: this warp's inputs polled)
         if (gain) {   // RMSNorm (one range: the row length is at most kMmvRange): 1 / rms per sequence
             if (!cbar(c, pc)) return false;   // every item's sum of squares
             if (c.warp < B) {   // warp s: sequence s's chunk sums, lane-strided, then a butterfly
@@ -1461,7 +1503,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                 if (q >= nblk) break;
                 if (!block(q, s0, s1, k0, xrow, acc[q])) return false;
             }
-            if (rr + 1 < nrg) {
+            if (rr + 1 < rr1) {
                 if (!cbar(c, pc)) return false;   // the next range restages the inputs
                 continue;
             }

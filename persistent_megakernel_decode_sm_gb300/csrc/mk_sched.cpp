@@ -15,6 +15,10 @@
 //  * DAG: a consumer waits on one counter per producer set -- QKV(l) on down(l-1), attention
 //    chunks of group g on the QKV tiles of group g, O on the combined attention of every group,
 //    up/gate on O, down on up/gate, LM head on the last layer's down, argmax on the LM head.
+//    At batch > 1 a down projection with rows longer than kMmvRange has a tile per (staging
+//    range, row block); the tile of the last range (enumerated after every other range's tiles)
+//    reads their tagged partial sums as they land, adds them in range order, writes the rows and
+//    alone carries the completion.
 //    At batch 1 the combine of a group's chunk partials is done by the chunk tile that holds the
 //    step's position (known only at run time), which alone carries the completion O waits on; it
 //    reads the other chunks' tagged partials as they land (a wait inside the wave, on tiles of
@@ -167,9 +171,13 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     // a gate page and its up page), at most 16 rows (8 pairs), so no tile ends in a partly filled
     // group (measured: 1B step 722 -> 709 us); at batch > 1 only the QKV rows are rounded up, to
     // a 16-row MMA block (measured: the others' rounding cost 10 us at batch 8).  QKV tiles keep
-    // <= head_dim rows (a tile then touches at most two KV groups).  At batch > 1 an operator whose rows are longer than kMmvRange (the MLP down
-    // projection) keeps the sums of all its rows over several staging ranges, so its tiles take
-    // at most 64 rows.  An explicit tile_bytes: tiles of about tile_bytes.
+    // <= head_dim rows (a tile then touches at most two KV groups).  At batch > 1 the MLP down
+    // projection, when its rows are longer than kMmvRange, is cut into one tile per (staging
+    // range, row block): each tile polls its inputs once instead of once per range (measured:
+    // every poll of a 64 KB input range is a loaded-memory round trip of about 4 us), the tile of
+    // the last range adds the partial sums of the others; any other operator with such rows keeps
+    // the sums of all its rows over the ranges, so its tiles take at most 64 rows.  An explicit
+    // tile_bytes: tiles of about tile_bytes.
     if (g.tile_bytes == 0) {
         auto grp = [&](int64_t K, bool pair) -> int32_t {   // rows (pairs) a tile is rounded up to
             if (B > 1) return 1;
@@ -181,8 +189,10 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
         g.r_o = up_to(cdiv(H, S), grp(qd, false));
         if (B > 1 && qd > kMmvRange) g.r_o = std::min(64, g.r_o);   // (sums over ranges: <= 4 row blocks)
         g.r_up = up_to(cdiv(F, S), grp(H, true));
-        g.r_dn = up_to(cdiv(H, S), grp(F, false));
-        if (B > 1 && F > kMmvRange) g.r_dn = std::min(64, g.r_dn);
+        // (batch > 1, rows longer than kMmvRange: one tile per staging range of a row block, so
+        // about one tile per SM takes H * ranges / S rows, in whole 16-row blocks, at most 64)
+        const int32_t nrg_dn = mmv_down_ranges(B, F);
+        g.r_dn = nrg_dn > 1 ? std::min(64, up_to(cdiv(H * nrg_dn, S), 16)) : up_to(cdiv(H, S), grp(F, false));
         g.r_lm = up_to(cdiv(V, S), grp(H, false));
     } else {
         const int64_t tb = g.tile_bytes ? g.tile_bytes : 131072;
@@ -204,8 +214,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
     if (g.r_o < 1 || g.r_up < 1 || g.r_lm < 1 || g.r_dn < 1) return fail(MK_ERR_ARG, "rows per tile must be >= 1");
     if (B == 1 && g.page_bytes < 2 * std::max(H, std::max(qd, F)))   // batch 1: whole rows per page
         return fail(MK_ERR_ARG, "page_bytes %d holds no matvec row (%d bytes)", g.page_bytes, 2 * std::max(H, std::max(qd, F)));
-    if (B > 1 && g.page_bytes > 32 * kMmvRange)   // batch > 1: a 16-row block of at most kMmvRange positions
-        return fail(MK_ERR_ARG, "at batch > 1 page_bytes is at most %d", 32 * kMmvRange);
+    if (B > 1 && (g.page_bytes > 32 * kMmvRange || kMmvRange % (g.page_bytes / 32)))   // a 16-row block over
+        return fail(MK_ERR_ARG, "at batch > 1 page_bytes / 32 must divide %d", kMmvRange);   // a part of a range
     g.n_qkv = cdiv(nqkv, g.r_qkv);
     g.n_o = cdiv(H, g.r_o);
     g.n_up = cdiv(F, g.r_up);
@@ -217,7 +227,8 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
 
     // ---- tiles in enumeration order (ids) ------------------------------------------------
     std::vector<Tile> tiles;
-    tiles.reserve(size_t(L) * (g.n_qkv + B * nkv * g.n_chunk + g.n_o + g.n_up + g.n_dn) + g.n_lm + B);
+    tiles.reserve(size_t(L) * (g.n_qkv + B * nkv * (g.n_chunk + 1) + g.n_o + g.n_up + g.n_dn * mmv_down_ranges(B, F)) +
+                  g.n_lm + B);
     auto add = [&](int32_t op, int32_t layer, int32_t b, int32_t a0, int32_t a1, int32_t a2, int32_t wave,
                    std::initializer_list<std::pair<int32_t, int32_t>> waits,
                    std::pair<int32_t, int32_t> pub, int64_t bytes) {
@@ -283,10 +294,17 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
             int32_t r0 = t * g.r_up, n = std::min(g.r_up, F - r0);
             add(OP_UPGATE, l, 0, r0, n, 0, 5 * l + 3, {{cm.o(l), g.n_o}}, {cm.up(l), 1}, int64_t(2) * n * H * 2);
         }
-        for (int32_t t = 0; t < g.n_dn; ++t) {
-            int32_t r0 = t * g.r_dn, n = std::min(g.r_dn, H - r0);
-            add(OP_DOWN, l, 0, r0, n, 0, 5 * l + 4, {{cm.up(l), g.n_up}}, {cm.down(l), 1}, int64_t(n) * F * 2);
-        }
+        // at batch > 1 with rows longer than kMmvRange: a tile per (staging range a2, row block),
+        // the ranges in order; the tile of the last range (highest ids) adds the others' partial
+        // sums and alone completes the rows
+        const int32_t nrg_dn = mmv_down_ranges(B, F);
+        for (int32_t r = 0; r < nrg_dn; ++r)
+            for (int32_t t = 0; t < g.n_dn; ++t) {
+                int32_t r0 = t * g.r_dn, n = std::min(g.r_dn, H - r0);
+                const int64_t kr = nrg_dn > 1 ? std::min<int64_t>(kMmvRange, F - int64_t(r) * kMmvRange) : F;
+                add(OP_DOWN, l, 0, r0, n, r, 5 * l + 4, {{cm.up(l), g.n_up}}, {cm.down(l), 1}, int64_t(n) * kr * 2);
+                if (r + 1 < nrg_dn) tiles.back().npub = 0;
+            }
     }
     for (int32_t t = 0; t < g.n_lm; ++t) {
         int32_t r0 = t * g.r_lm, n = std::min(g.r_lm, V - r0);
@@ -372,7 +390,9 @@ extern "C" mk_status mk_build_schedule(const mk_model_cfg* cfgp, int32_t S, cons
                 const int64_t K = t.op == OP_OPROJ ? qd : (t.op == OP_DOWN ? F : H);
                 if (B > 1) {   // 16-row blocks (gate/up: 8 pairs) over page_bytes / 32 positions
                     const int64_t kp = g.page_bytes / 32, rb = t.op == OP_UPGATE ? 8 : 16;
-                    pages = ((t.a1 + rb - 1) / rb) * ((K + kp - 1) / kp);
+                    const int64_t Kt = (t.op == OP_DOWN && mmv_down_ranges(B, F) > 1)
+                                           ? std::min<int64_t>(kMmvRange, K - int64_t(t.a2) * kMmvRange) : K;
+                    pages = ((t.a1 + rb - 1) / rb) * ((Kt + kp - 1) / kp);
                 } else {
                     const int64_t rpp = g.page_bytes / (2 * K);
                     pages = ((t.a1 + rpp - 1) / rpp) * (t.op == OP_UPGATE ? 2 : 1);

@@ -71,11 +71,13 @@ def test_schedule_tiles_cover_every_row_once(name, S):
     tiles, cnt, R = sr.enumerate_tiles(cfg, sr.SchedOpts(), S)
     for op, total in ((sr.QKV, cfg.qkv_rows), (sr.OPROJ, cfg.hidden), (sr.UPGATE, cfg.ffn),
                       (sr.DOWN, cfg.hidden), (sr.LMHEAD, cfg.vocab)):
+        # (batch > 1 down projection of rows longer than a staging range: once per range)
+        nrg = sr.down_ranges(cfg) if op == sr.DOWN else 1
         for l in (range(cfg.n_layers) if op != sr.LMHEAD else [cfg.n_layers]):
-            rows = np.zeros(total, int)
+            rows = np.zeros((nrg, total), int)
             for t in tiles:
                 if t.op == op and t.layer == l:
-                    rows[t.a0:t.a0 + t.a1] += 1
+                    rows[t.a2 if op == sr.DOWN else 0, t.a0:t.a0 + t.a1] += 1
             assert np.all(rows == 1)
 
 
@@ -125,6 +127,16 @@ def test_validator_and_simulator_catch_planted_errors():
     bad = q.copy()
     bad[s, [0, n - 1]] = bad[s, [n - 1, 0]]
     assert sr.validate(bad, t, cfg)
+    # batch > 1, down rows over two staging ranges: a range-0 tile relabelled as range 1 leaves
+    # the last range's tile of those rows waiting for a partial nobody writes
+    cfg = small_config(batch=2, ffn=4096, max_seq=64)
+    q, t, _ = sr.build_schedule(cfg, 5)
+    assert sr.down_ranges(cfg) == 2 and sr.simulate(q, t, cfg, n_epochs=1) == []
+    at = next((s, i) for s in range(q.shape[0]) for i in range(q.shape[1]) if q[s, i, 0] == sr.DOWN and q[s, i, 5] == 0)
+    bad = q.copy()
+    bad[at][5] = 1
+    assert sr.validate(bad, t, cfg)
+    assert any("deadlock" in e for e in sr.simulate(bad, t, cfg, n_epochs=1))
 
 
 def test_counter_totals_match_waits():
@@ -149,7 +161,8 @@ def test_random_small_configs_bit_exact_valid_and_deadlock_free():
         d = int(rng.choice([64, 128]))
         cfg = small_config(n_layers=int(rng.integers(1, 4)), hidden=int(rng.choice([128, 256, 512])),
                            n_q_heads=nkv * hpg, n_kv_heads=nkv, head_dim=d,
-                           ffn=8 * int(rng.integers(16, 120)), vocab=8 * int(rng.integers(64, 600)),
+                           ffn=8 * int(rng.integers(16, 120) if rng.random() < 0.7 else rng.integers(257, 800)),
+                           vocab=8 * int(rng.integers(64, 600)),
                            batch=int(rng.choice([1, 1, 2, 3])), max_seq=int(rng.integers(8, 400)))
         S = int(rng.choice([1, 3, 7, 16, 37]))
         try:
