@@ -1396,6 +1396,11 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                         s0 += part[(q * kNumConsumerWarps + w) * 128 + rr * 8 + col];
                         if (pair) s1 += part[(q * kNumConsumerWarps + w) * 128 + (rr + 8) * 8 + col];
                     }
+                    if (gain) {   // RMSNorm: the sequence's 1 / rms
+                        const float sc = c.sh.red[48 + col];
+                        s0 *= sc;
+                        s1 *= sc;
+                    }
                     if (dsplit) s0 = down_partials(c, pc, l, col, si.w[W_A0] + row, rr0, nrg, s0);
                     if (dred) mv_epilogue<false>(c, si, pc, col, row, s0, s1, (blk0 == 0 && rok) ? &rres : nullptr, bv, bi);
                 }
@@ -1407,9 +1412,12 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
         const int k0 = rr * KR;
         const int kr = min(KR, K - k0), csr = kr / 8, items = B * csr;
         // 1. the range's inputs, every element polled until it carries this step's tag and stored
-        //    into the stage as fp32 (rewritten on every round), with a norm also each item's sum of
-        //    squares.  (Every SM reads the inputs in the same order: spreading the SMs over
-        //    different parts of the inputs at a time was measured slower.)
+        //    into the stage (rewritten on every round) as the (high, remainder) words the
+        //    contraction reads; with a norm they hold x * gain, each item's sum of squares of x is
+        //    kept, and the sequence's 1 / rms scales the row sums in the outputs (a pass rescaling
+        //    the staged inputs cost about 2 us a tile).  (Every SM reads the inputs in the same
+        //    order: spreading the SMs over different parts of the inputs at a time was measured
+        //    slower.)
         {
             Spin spn;
             while (true) {
@@ -1423,74 +1431,40 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                     const XSrc src = mmv_src(c, op, l, s, gn);
                     float v[8];
                     ok &= load8x(src, k0 + ci * 8, v, c.tag);
-                    float4* dst = reinterpret_cast<float4*>(stage + s * RS + ci * 32);
+                    float y[8];
                     if (gain) {
-                        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-                        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+                        const uint4 gw = gpre ? gw_pre : __ldg(reinterpret_cast<const uint4*>(gain + k0 + ci * 8));
+                        y[0] = v[0] * bf_lo(gw.x); y[1] = v[1] * bf_hi(gw.x); y[2] = v[2] * bf_lo(gw.y); y[3] = v[3] * bf_hi(gw.y);
+                        y[4] = v[4] * bf_lo(gw.z); y[5] = v[5] * bf_hi(gw.z); y[6] = v[6] * bf_lo(gw.w); y[7] = v[7] * bf_hi(gw.w);
                         part[i] = ((v[0] * v[0] + v[1] * v[1]) + (v[2] * v[2] + v[3] * v[3])) +
                                   ((v[4] * v[4] + v[5] * v[5]) + (v[6] * v[6] + v[7] * v[7]));
-                    } else {   // no norm: straight as the (high, remainder) words the contraction reads
-                        uint32_t o[8];
+                    } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const uint32_t hb = bf16x2_rn(v[e], 0.f) & 0xFFFFu;
-                            o[e] = hb | (bf16x2_rn(v[e] - __uint_as_float(hb << 16), 0.f) << 16);
-                        }
-                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                        for (int e = 0; e < 8; ++e) y[e] = v[e];
                     }
+                    uint32_t o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t hb = bf16x2_rn(y[e], 0.f) & 0xFFFFu;
+                        o[e] = hb | (bf16x2_rn(y[e] - __uint_as_float(hb << 16), 0.f) << 16);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(stage + s * RS + ci * 32);
+                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
                 }
                 if (__all_sync(0xFFFFFFFFu, ok)) break;
                 if (!spin_more(c, spn, pc)) return false;
             }
         }
         if (rr == rr0 && c.warp == 0 && c.lane == 0) stamp(p, pc, 6);   // (trace: this warp's inputs polled)
-        if (gain) {   // RMSNorm (one range: the row length is at most kMmvRange): 1 / rms per sequence
-            if (!cbar(c, pc)) return false;   // every item's sum of squares
+        if (gain) {   // RMSNorm (one range: the row length is at most kMmvRange): 1 / rms per sequence,
+                      // read by the outputs after their barrier
+            if (!cbar(c, pc)) return false;   // every item's sum of squares (and staged words)
             if (c.warp < B) {   // warp s: sequence s's chunk sums, lane-strided, then a butterfly
                 float q = 0.f;
                 for (int ci = c.lane; ci < csr; ci += 32) q += part[c.warp * csr + ci];
                 q = warp_sum(q);
                 if (c.lane == 0) c.sh.red[48 + c.warp] = rsqrtf(q / float(K) + p.rms_eps);
-            }
-            if (!cbar(c, pc)) return false;
-        }
-        // 2. with a norm, in place, each thread its own items: x * 1 / rms * gain -> (hi, lo) word
-        //    pairs; the gain chunks of all the thread's items are loaded first (one round trip)
-        if (gain) {
-            uint4 gws[kMmvItems];
-#pragma unroll
-            for (int j = 0; j < kMmvItems; ++j) {
-                const int i = tid + j * kConsumerThreads;
-                gws[j] = (!gpre && i < items) ? __ldg(reinterpret_cast<const uint4*>(gain + k0 + (i % csr) * 8))
-                                              : gw_pre;
-            }
-#pragma unroll
-            for (int j = 0; j < kMmvItems; ++j) {
-                const int i = tid + j * kConsumerThreads;
-                if (i >= items) break;
-                const int s = i / csr, ci = i % csr;
-                uint4* w4 = reinterpret_cast<uint4*>(stage + s * RS + ci * 32);
-                const uint4 u = w4[0], w = w4[1];
-                float x[8] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w),
-                              __uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w)};
-                if (gain) {
-                const float scale = c.sh.red[48 + s];
-                const uint4 gw = gws[j];
-                x[0] = (x[0] * scale) * bf_lo(gw.x); x[1] = (x[1] * scale) * bf_hi(gw.x);
-                x[2] = (x[2] * scale) * bf_lo(gw.y); x[3] = (x[3] * scale) * bf_hi(gw.y);
-                x[4] = (x[4] * scale) * bf_lo(gw.z); x[5] = (x[5] * scale) * bf_hi(gw.z);
-                x[6] = (x[6] * scale) * bf_lo(gw.w); x[7] = (x[7] * scale) * bf_hi(gw.w);
-                }
-                uint32_t o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t hb = bf16x2_rn(x[e], 0.f) & 0xFFFFu;
-                    const float lo = x[e] - __uint_as_float(hb << 16);
-                    o[e] = hb | (bf16x2_rn(lo, 0.f) << 16);
-                }
-                w4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                w4[1] = make_uint4(o[4], o[5], o[6], o[7]);
             }
         }
         if (!cbar(c, pc)) return false;   // staged words visible; the partial area and the scales are free again
