@@ -243,12 +243,11 @@ mk_status mk_set_timeout(mk_ctx* c, uint64_t ns);
 
 /* How a consumer learns that the inputs of its instruction are ready.
  *  MK_SYNC_TAGS (default): the activation vectors one operator hands to the next (q/k/v,
- *    attention output, both residual streams) are epoch-tagged -- every element is
- *    one 64-bit word holding the fp32 value and the step's tag -- and a consumer polls the
- *    elements it reads until each carries this step's tag.  The SwiGLU output (and, at batch
- *    > 1, the residual streams and the attention output too: every SM reads them whole) is
- *    32-bit fp32 words whose three low mantissa bits hold a 3-bit step tag, polled the same
- *    way.  One read
+ *    attention output, both residual streams, SwiGLU output) are tagged and a consumer polls
+ *    the elements it reads until each carries this step's tag: q/k/v (and the attention chunk
+ *    partials) as 64-bit words holding the fp32 value and the step's tag; the SwiGLU output,
+ *    the residual streams and the attention output (every SM reads them whole) as 32-bit fp32
+ *    words whose three low mantissa bits hold a 3-bit step tag.  One read
  *    both proves readiness and fetches the data, so a dependency costs one memory round trip
  *    instead of the publisher's release fence, the counter add, the consumer's counter poll and
  *    then the data read.  Such a consumer reads no counter at all.  Counters are still

@@ -133,7 +133,8 @@ __device__ __forceinline__ uint64_t globaltimer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// epoch-tagged activation words: fp32 bits low, tag high, one single-copy-atomic 64-bit access
+// epoch-tagged activation words (q/k/v, attention chunk partials): fp32 bits low, tag high, one
+// single-copy-atomic 64-bit access
 __device__ __forceinline__ void st_tag(uint64_t* a, float v, uint32_t tag) {
     const uint64_t w = (uint64_t(tag) << 32) | uint64_t(__float_as_uint(v));
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(w) : "memory");
@@ -166,7 +167,9 @@ __device__ __forceinline__ bool ld8_tagged(const uint64_t* a, float* v, uint32_t
 }
 
 // The SwiGLU output is read by the down projection a whole 2048-element segment per warp, where
-// 64-bit words would not fit the registers next to x: its elements are 32-bit words, fp32 with
+// 64-bit words would not fit the registers next to x, and the residual streams and the attention
+// output are read whole by every SM, where half the bytes shorten every poll (measured: batch-8
+// step 1807 -> 1726 us, batch-1 708 -> 691 us): their elements are 32-bit words, fp32 with
 // the three low mantissa bits replaced by a 3-bit step tag, (epoch mod 7) + 1 -- never 0 (the
 // cleared scratch) and never the previous step's.  The stored value is the fp32 result with those
 // bits cleared (a relative change below 2^-20).
@@ -929,7 +932,7 @@ __device__ __forceinline__ int step_token(const Cw& c, int b) {
 
 // where an epilogue's residual comes from: epoch-tagged words, or the bf16 embedding row (layer 0)
 struct RSrc {
-    const uint64_t* t;
+    const uint32_t* t;   // 3-bit-tagged fp32 words
     const uint16_t* b;
 };
 
@@ -958,11 +961,11 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
     // the residual word of tile row tid: its load is issued before the input poll, so the two round
     // trips overlap (the residual was produced an operator earlier: it is almost always ready)
     const bool rmine = tid < nres;
-    uint64_t rw = 0;
+    uint32_t rw = 0;
     float rb = 0.f;
     if (rmine) {
         if (rs.b) rb = bf16f(rs.b[tid]);
-        else rw = ld_tag(rs.t + tid);
+        else asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(rw) : "l"(rs.t + tid));
     }
     // the RMSNorm gain of this warp's segment depends on nothing: it is loaded into registers
     // before the poll, so its round trip overlaps the wait for the input (at 8 chunks per lane
@@ -1025,7 +1028,9 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
             if (!spin_more(c, sp, pc)) return false;
         }
     }
-    if (rmine) res[tid] = rs.b ? rb : (tag_of(rw) == c.tag ? tag_val(rw) : poll1(p, c.sh, rs.t + tid, pc, c.tag));
+    if (rmine)
+        res[tid] = rs.b ? rb
+                        : (((rw ^ htag(c.tag)) & 7u) == 0 ? __uint_as_float(rw & ~7u) : poll1h(p, c.sh, rs.t + tid, pc, c.tag));
     __syncwarp();
     if (c.lane == 0) mbar_arrive(c.sh.xfull);
     if (!wait_bar(p, c.sh, c.sh.xfull, c.xphase & 1u, ROLE_CONSUMER, pc)) return false;
@@ -1076,30 +1081,22 @@ __device__ __forceinline__ void mv_epilogue(const Cw& c, const SlotInfo& si, int
     const int row = si.w[W_A0] + ru;
     switch (op) {
         case OP_QKV: st_tag(p.qkv + lb * p.nqkv + row, s0, c.tag); break;
-        case OP_OPROJ: {
-            if constexpr (kBatchedKernel) {   // (batch > 1: 3-bit-tagged 32-bit residual words; res: read ahead)
-                const float r = l == 0 ? bf16f(p.embed[size_t(step_token(c, b)) * p.H + row])
-                              : res   ? *res
-                                      : poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_out) + (lb - p.B) * p.H + row,
-                                               pc, c.tag);
-                st_htag(reinterpret_cast<uint32_t*>(p.x_attn) + lb * p.H + row, r + s0, htag(c.tag));
-                break;
-            }
+        case OP_OPROJ: {   // (3-bit-tagged 32-bit residual words; res: the tile's residual buffer, or
+                           // at batch > 1 the one word read ahead)
             const float r = (RES && ru < kResBuf) ? res[ru]
-                          : (l == 0) ? bf16f(p.embed[size_t(step_token(c, b)) * p.H + row])
-                                     : poll1(p, c.sh, p.x_out + (lb - p.B) * p.H + row, pc, c.tag);
-            st_tag(p.x_attn + lb * p.H + row, r + s0, c.tag);
+                          : l == 0            ? bf16f(p.embed[size_t(step_token(c, b)) * p.H + row])
+                          : (!RES && res)     ? *res
+                                              : poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_out) + (lb - p.B) * p.H + row,
+                                                       pc, c.tag);
+            st_htag(reinterpret_cast<uint32_t*>(p.x_attn) + lb * p.H + row, r + s0, htag(c.tag));
             break;
         }
         case OP_UPGATE: st_htag(p.h + lb * p.F + row, __fdividef(s0, 1.0f + __expf(-s0)) * s1, htag(c.tag)); break;
         case OP_DOWN: {
-            if constexpr (kBatchedKernel) {
-                const float r = res ? *res : poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_attn) + lb * p.H + row, pc, c.tag);
-                st_htag(reinterpret_cast<uint32_t*>(p.x_out) + lb * p.H + row, r + s0, htag(c.tag));
-                break;
-            }
-            const float r = (RES && ru < kResBuf) ? res[ru] : poll1(p, c.sh, p.x_attn + lb * p.H + row, pc, c.tag);
-            st_tag(p.x_out + lb * p.H + row, r + s0, c.tag);
+            const float r = (RES && ru < kResBuf) ? res[ru]
+                          : (!RES && res)     ? *res
+                                              : poll1h(p, c.sh, reinterpret_cast<const uint32_t*>(p.x_attn) + lb * p.H + row, pc, c.tag);
+            st_htag(reinterpret_cast<uint32_t*>(p.x_out) + lb * p.H + row, r + s0, htag(c.tag));
             break;
         }
         default:   // LM head: the logit, then this lane's running (max, lowest index)
@@ -1208,8 +1205,8 @@ __device__ __forceinline__ XSrc mmv_src(const Cw& c, int op, int l, int b, const
     XSrc src{nullptr, nullptr, nullptr};
     const size_t lb = size_t(l) * p.B + b;
     gain = nullptr;
-    // (the batch > 1 kernel keeps the residual streams and the attention output as 3-bit-tagged
-    // 32-bit words, like the SwiGLU output: half the bytes every SM polls)
+    // (the residual streams and the attention output are 3-bit-tagged 32-bit words, like the
+    // SwiGLU output: half the bytes every SM polls)
     const uint32_t* xo = reinterpret_cast<const uint32_t*>(p.x_out);
     switch (op) {
         case OP_QKV:
@@ -1549,6 +1546,9 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
     // this lane's partial word within a unit: lane 0 the first sum (word 0), lane 16 the second
     // (gate/up: word 1 of the same unit; otherwise word 0 of the second page's unit)
     const int pword = (pair && c.lane == 16) ? 1 : 0;
+    // (the residual streams and the attention output: 3-bit-tagged 32-bit words)
+    const uint32_t* xo = reinterpret_cast<const uint32_t*>(p.x_out);
+    const uint32_t* xa = reinterpret_cast<const uint32_t*>(p.x_attn);
     for (int b = 0; b < p.B; ++b) {
         XSrc src{nullptr, nullptr, nullptr};
         RSrc rs{nullptr, nullptr};
@@ -1559,21 +1559,21 @@ __device__ bool matvec_tile(Cw& c, const SlotInfo& si, int pc) {
             case OP_QKV:
                 gain = c.sh.layers[l].attn_norm;
                 if (l == 0) src.b = p.embed + size_t(step_token(c, b)) * p.H;
-                else src.t = p.x_out + (lb - p.B) * p.H;
+                else src.h = xo + (lb - p.B) * p.H;
                 break;
             case OP_OPROJ:
-                src.t = p.o + lb * p.qd;
+                src.h = reinterpret_cast<const uint32_t*>(p.o) + lb * p.qd;
                 if (l == 0) rs.b = p.embed + size_t(step_token(c, b)) * p.H + a0;
-                else rs.t = p.x_out + (lb - p.B) * p.H + a0;
+                else rs.t = xo + (lb - p.B) * p.H + a0;
                 nres = min(R, kResBuf);
                 break;
-            case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; src.t = p.x_attn + lb * p.H; break;
+            case OP_UPGATE: gain = c.sh.layers[l].mlp_norm; src.h = xa + lb * p.H; break;
             case OP_DOWN:
                 src.h = p.h + lb * p.F;
-                rs.t = p.x_attn + lb * p.H + a0;
+                rs.t = xa + lb * p.H + a0;
                 nres = min(R, kResBuf);
                 break;
-            default: gain = p.final_norm; src.t = p.x_out + (size_t(p.L - 1) * p.B + b) * p.H; break;
+            default: gain = p.final_norm; src.h = xo + (size_t(p.L - 1) * p.B + b) * p.H; break;
         }
         float* res;
         if (!load_input<CPL>(c, si, src, gain, rs, nres, xr, res, pc)) return false;
@@ -2012,15 +2012,12 @@ __device__ __forceinline__ bool attn_combine(Cw& c, int pc, size_t lb, int g, in
         }
         if (!cbar(c, pc)) return false;   // the stage is refilled next (next group, next input)
     }
-    uint64_t* out = p.o + lb * p.qd + size_t(g) * hpg * d;
+    uint32_t* out = reinterpret_cast<uint32_t*>(p.o) + lb * p.qd + size_t(g) * hpg * d;   // 3-bit-tagged words
 #pragma unroll
     for (int j = 0; j < kOut; ++j) {
         const int idx = tid + j * kConsumerThreads;
         if (idx >= hpg * d) continue;
-        if constexpr (kBatchedKernel)
-            st_htag(reinterpret_cast<uint32_t*>(p.o) + lb * p.qd + size_t(g) * hpg * d + idx, Ar[j] / Lr[j], htag(c.tag));
-        else
-            st_tag(out + idx, Ar[j] / Lr[j], c.tag);
+        st_htag(out + idx, Ar[j] / Lr[j], htag(c.tag));
     }
     return true;
 }
