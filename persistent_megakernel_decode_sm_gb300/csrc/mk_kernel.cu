@@ -986,12 +986,17 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
         float ss = 0.f;
         for (int base = 0; base < m.chunks; base += kXChunks * kConsumerThreads) {   // warp-uniform
             float v[kXChunks][8];
+            uint32_t good = 0;   // chunks already read with this step's tag: not read again
             while (true) {
                 bool ok = true;
 #pragma unroll
                 for (int q = 0; q < kXChunks; ++q) {
                     const int ch = base + q * kConsumerThreads + tid;
-                    if (ch < m.chunks) ok &= load8x(src, ch * 8, v[q], c.tag);
+                    if (ch < m.chunks && !((good >> q) & 1u)) {
+                        const bool gq = load8x(src, ch * 8, v[q], c.tag);
+                        good |= uint32_t(gq) << q;
+                        ok &= gq;
+                    }
                 }
                 if (__all_sync(0xFFFFFFFFu, ok)) break;
                 if (!spin_more(c, sp, pc)) return false;
@@ -1012,13 +1017,18 @@ __device__ bool load_input(Cw& c, const SlotInfo& si, const XSrc& src, const uin
             if (c.lane == 0) c.sh.red[48 + c.warp] = ss;
         }
     } else {
+        uint32_t good = 0;   // chunks already read with this step's tag: not read again
         while (true) {
             bool ok = true;
 #pragma unroll
             for (int i = 0; i < CPL; ++i) {
                 const int ch = c.lane + 32 * i;
                 if (ch < nch) {
-                    ok &= load8x(src, (cg0 + ch) * 8, &xr[8 * i], c.tag);
+                    if (!((good >> i) & 1u)) {
+                        const bool gi = load8x(src, (cg0 + ch) * 8, &xr[8 * i], c.tag);
+                        good |= uint32_t(gi) << i;
+                        ok &= gi;
+                    }
                 } else {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) xr[8 * i + e] = 0.f;
@@ -1417,6 +1427,7 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
         //    slower.)
         {
             Spin spn;
+            uint32_t good = 0;   // items already read with this step's tag: not read again
             while (true) {
                 bool ok = true;
                 // (two items per unrolled step: the kernel carries every operator body and its
@@ -1426,11 +1437,14 @@ __device__ bool mmv_tile(Cw& c, const SlotInfo& si, int pc) {
                 for (int j = 0; j < kMmvItems; ++j) {
                     const int i = tid + j * kConsumerThreads;
                     if (i >= items) break;
+                    if ((good >> j) & 1u) continue;
                     const int s = i / csr, ci = i % csr;
                     const uint16_t* gn;
                     const XSrc src = mmv_src(c, op, l, s, gn);
                     float v[8];
-                    ok &= load8x(src, k0 + ci * 8, v, c.tag);
+                    const bool gj = load8x(src, k0 + ci * 8, v, c.tag);
+                    good |= uint32_t(gj) << j;
+                    ok &= gj;
                     float y[8];
                     if (gain) {
                         const uint4 gw = gpre ? gw_pre : __ldg(reinterpret_cast<const uint4*>(gain + k0 + ci * 8));
