@@ -813,7 +813,7 @@ __device__ bool spin_more(const Params& p, const Shared& sh, int lane, Spin& sp,
                 raise_error(p, sh, MK_ERR_TIMEOUT, ROLE_DATA, pc, -1, 0, tag);
                 stop = 1;
             }
-            if (!stop) __nanosleep(kPollBackoffNs);   // spaces a warp's polling rounds out in L2
+            if (!stop) __nanosleep(kPollBackoffNs);   // (yields the issue slot between polling rounds)
         }
     }
     return __shfl_sync(0xFFFFFFFFu, stop, 0) == 0;
